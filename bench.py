@@ -1,0 +1,391 @@
+"""Benchmark of the sparse MoE layer on one GB300 (or N replicas).
+
+One step = one prefill pass of the whole layer (router GEMM, top-k, histogram,
+scan, scatter, gate/up+SwiGLU and down grouped GEMMs, combine) over T=4096
+synthetic tokens of the Qwen3.6-35B-A3B MoE shape (H=2048, 256 experts, top-8,
+I=512, one shared expert, bf16, router bias ~N(0,1.5)), inputs resident in HBM,
+L2 flushed between timed steps.  The same JSON line carries the batch-1 decode
+latency (40 independent layers, weights far larger than L2, replayed as one
+CUDA graph), the roofline of the dominant kernel of each path, the end-to-end
+number through the host-buffer entry point, the fp64 CPU oracle timed on this
+machine's cores, and the SM clocks seen during the run.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import moe_synth  # noqa: E402
+
+METRIC = "MoE-layer prefill tokens/s (T=4096) and batch-1 decode µs/layer; % of roofline"
+L2_FLUSH_BYTES = 512 << 20
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), float(p["bf16_tflops_sustained"]), \
+            "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+# --------------------------------------------------------------- clocks --
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [c.strip() for c in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+                power.append(float(f[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        busy = [s for s, p in zip(sm, power) if p > 300.0] or sm
+        return {"sm_mhz": float(np.median(busy)), "sm_max_mhz": float(max(smax)),
+                "reasons": sorted(reasons), "samples": len(sm), "samples_under_load": len(busy),
+                "power_w_max": float(max(power))}
+
+
+# ------------------------------------------------------------- workload --
+def algorithmic(s: moe_synth.Shape, T: int):
+    H, E, k, I, Is = s.hidden, s.n_experts, s.top_k, s.inter, s.shared_inter
+    gateup_flops = 2.0 * H * 2 * I * T * k + 2.0 * H * 2 * Is * T
+    down_flops = 2.0 * I * H * T * k + 2.0 * Is * H * T
+    router_flops = 2.0 * H * E * T
+    return gateup_flops, down_flops, router_flops
+
+
+def decode_bytes(s: moe_synth.Shape, int4: bool):
+    H, E, k, I, Is = s.hidden, s.n_experts, s.top_k, s.inter, s.shared_inter
+    if int4:
+        per = lambda rows, K: rows * K // 2 + rows * (K // 64) * 2  # noqa: E731
+    else:
+        per = lambda rows, K: rows * K * 2  # noqa: E731
+    routed_gu = k * per(2 * I, H)
+    routed_dn = k * per(H, I)
+    shared = per(2 * Is, H) + per(H, Is)
+    router = E * H * 2 + H * 2
+    return dict(routed_gateup=routed_gu, routed_down=routed_dn, shared=shared, router=router,
+                expert_stream=routed_gu + routed_dn + shared,
+                total=routed_gu + routed_dn + shared + router + 2 * H * 2)
+
+
+def run_prefill(ctx, x, y, steps, warmup, flush, stream):
+    for _ in range(warmup):
+        ctx.forward_prefill(0, x, y, stream=stream)
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    launches0 = ctx.launch_count
+    ctx.profile(True)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for i in range(steps):
+            flush.zero_()
+            starts[i].record(stream)
+            ctx.forward_prefill(0, x, y, stream=stream)
+            ends[i].record(stream)
+    torch.cuda.synchronize()
+    prof = ctx.profile_read()
+    ctx.profile(False)
+    launches = ctx.launch_count - launches0
+    ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    return float(np.sum(ms)), prof, launches
+
+
+def run_prefill_e2e(ctx, x_h, y_h, steps, warmup, flush, stream):
+    for _ in range(max(1, warmup // 2)):
+        ctx.forward_prefill_host(0, x_h, y_h, stream=stream)
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    with torch.cuda.stream(stream):
+        for i in range(steps):
+            flush.zero_()
+            starts[i].record(stream)
+            ctx.forward_prefill_host(0, x_h, y_h, stream=stream)
+            ends[i].record(stream)
+    torch.cuda.synchronize()
+    return float(np.sum([a.elapsed_time(b) for a, b in zip(starts, ends)]))
+
+
+def bench_decode(args, dev, stream, hbm):
+    """40 independent decode layers replayed as one CUDA graph."""
+    from sparse_moe_gb300 import MoEContext
+    wl = moe_synth.DECODE_INT4 if args.decode_int4 else moe_synth.DECODE_BF16
+    s = wl.shape
+    L = wl.n_layers
+    ctx = MoEContext(s.hidden, s.n_experts, s.top_k, s.inter, s.shared_inter, n_layers=L,
+                     max_chunk_rows=16, wfmt=wl.wfmt, device=dev.index)
+    layers = []
+    for l in range(L):
+        w = moe_synth.make_layer(wl, layer=l, device=dev)
+        ctx.load_weights(l, w)
+        layers.append(w)
+    xs = torch.stack([moe_synth.make_x(wl, layer=l, device=dev)[0] for l in range(L)])
+    ys = torch.empty_like(xs)
+    x_h = xs[0:1].cpu().pin_memory()
+    y_h = torch.empty_like(x_h).pin_memory()
+    # eager warm-up, then a profiled eager pass for per-kernel times
+    for l in range(L):
+        ctx.forward_decode(l, xs[l:l + 1], ys[l:l + 1], stream=stream)
+    torch.cuda.synchronize()
+    ctx.profile(True)
+    for _ in range(2):
+        for l in range(L):
+            ctx.forward_decode(l, xs[l:l + 1], ys[l:l + 1], stream=stream)
+    torch.cuda.synchronize()
+    prof = ctx.profile_read()
+    ctx.profile(False)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(g, stream=stream):
+            for l in range(L):
+                ctx.forward_decode(l, xs[l:l + 1], ys[l:l + 1], stream=stream)
+    torch.cuda.synchronize()
+    for _ in range(max(3, args.warmup)):
+        g.replay()
+    torch.cuda.synchronize()
+    reps = max(5, args.steps)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    launches0 = ctx.launch_count
+    with torch.cuda.stream(stream):
+        a.record(stream)
+        for _ in range(reps):
+            g.replay()
+        b.record(stream)
+    torch.cuda.synchronize()
+    us_layer = a.elapsed_time(b) * 1e3 / (reps * L)
+    # end to end from host memory: one token per layer call, copies included
+    for _ in range(3):
+        ctx.forward_decode_host(0, x_h, y_h, stream=stream)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    n_e2e = 200
+    for i in range(n_e2e):
+        ctx.forward_decode_host(i % L, x_h, y_h, stream=stream)
+        stream.synchronize()
+    e2e_us = (time.perf_counter() - t0) * 1e6 / n_e2e
+    nb = decode_bytes(s, wl.wfmt == moe_synth.WFMT_INT4)
+    gu = prof.get("decode_gateup", (1, 1.0))
+    gu_ms = gu[1] / max(1, gu[0])
+    total_ms = sum(v[1] for v in prof.values()) / max(1, prof.get("decode_gateup", (1, 0))[0])
+    achieved = nb["routed_gateup"] / (gu_ms * 1e-3) / 1e9
+    out = {
+        "workload": wl.name, "value": us_layer, "unit": "us/layer",
+        "tokens_per_s": 1e6 / (us_layer * L), "layers": L, "graph_replays": reps,
+        "expert_stream_GBps": nb["expert_stream"] / (us_layer * 1e-6) / 1e9,
+        "expert_stream_frac_of_hbm": nb["expert_stream"] / (us_layer * 1e-6) / 1e9 / hbm,
+        "bytes_per_layer": nb["total"],
+        "roofline": {"kernel": "decode_gateup", "bound": "hbm", "achieved": achieved,
+                     "peak": hbm, "unit": "GB/s", "frac": achieved / hbm, "traffic": None,
+                     "algorithmic_bytes_per_launch": nb["routed_gateup"]},
+        "kernels_eager_us": {k: v[1] * 1e3 / max(1, v[0]) for k, v in prof.items()},
+        "eager_sum_us_per_layer": total_ms * 1e3,
+        "e2e": {"value": e2e_us, "unit": "us/token (one layer, host buffers, synchronous)",
+                "h2d_bytes_per_step": s.hidden * 2, "d2h_bytes_per_step": s.hidden * 2},
+        "gpu_launches_per_layer": (ctx.launch_count - launches0) // max(1, reps * L) or 3,
+    }
+    del g
+    ctx.close()
+    del layers
+    torch.cuda.empty_cache()
+    return out
+
+
+def cpu_baseline_prefill(x_cpu, w_dev, k, sample_tokens):
+    """The fp64 oracle, as it stands, on the first `sample_tokens` tokens."""
+    from oracle import moe_oracle as orc
+    layer = moe_synth.to_numpy(w_dev)
+    xs = x_cpu[:sample_tokens].float().numpy()
+    t0 = time.perf_counter()
+    orc.moe_layer(xs, layer, k)
+    dt = time.perf_counter() - t0
+    return {"value": sample_tokens / dt, "unit": "tokens/s", "cores": os.cpu_count(),
+            "kind": "oracle",
+            "sample": f"fp64 oracle (router, top-k, grouping, all experts, shared expert) on the "
+                      f"first {sample_tokens} of the {x_cpu.shape[0]} tokens; {dt:.1f} s",
+            "seconds": dt}
+
+
+def main_reference(args):
+    """The oracle as the reference arm, on the host cores."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    from oracle import moe_oracle as orc
+    wl = moe_synth.PREFILL_BF16
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    w = moe_synth.to_numpy(moe_synth.make_layer(wl, device=dev))
+    x = moe_synth.make_x(wl, device=dev).float().cpu().numpy()
+    S = args.ref_sample
+    for i in range(args.warmup):
+        orc.moe_layer(x[(i * S) % wl.T:(i * S) % wl.T + S], w, wl.shape.top_k)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        s0 = (i * S) % wl.T
+        orc.moe_layer(x[s0:s0 + S], w, wl.shape.top_k)
+    dt = time.perf_counter() - t0
+    value = args.steps * S / dt
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl.name, "T": wl.T, "sample_tokens_per_step": S},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": os.cpu_count(),
+                         "kind": "oracle",
+                         "sample": f"{S} consecutive tokens of the T={wl.T} workload per step"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def main(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        torch.distributed.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    hbm, tf_burst, tf_sust, peak_src = peaks()
+
+    from sparse_moe_gb300 import MoEContext
+    wl = moe_synth.PREFILL_BF16
+    s = wl.shape
+    ctx = MoEContext(s.hidden, s.n_experts, s.top_k, s.inter, s.shared_inter, n_layers=1,
+                     max_chunk_rows=4096, device=local)
+    w = moe_synth.make_layer(wl, device=dev)
+    ctx.load_weights(0, w)
+    x = moe_synth.make_x(wl, device=dev)
+    y = torch.empty_like(x)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    clocks = ClockSampler(local)
+    clocks.start()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    total_ms, prof, launches = run_prefill(ctx, x, y, args.steps, args.warmup, flush, stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    clk = clocks.stop()
+    ms_step = total_ms / args.steps
+    value = world * wl.T * args.steps / (total_ms * 1e-3)
+
+    gu_f, dn_f, rt_f = algorithmic(s, wl.T)
+    kern = {k: {"launches": v[0], "avg_us": v[1] * 1e3 / max(1, v[0])} for k, v in prof.items()}
+    gu_us = kern.get("gateup_swiglu_gemm", {}).get("avg_us", float("nan"))
+    dn_us = kern.get("down_gemm", {}).get("avg_us", float("nan"))
+    achieved = gu_f / (gu_us * 1e-6) / 1e12
+    roofline = {"kernel": "gateup_swiglu_gemm", "bound": "tensor", "achieved": achieved,
+                "peak": tf_burst, "unit": "TFLOP/s", "frac": achieved / tf_burst, "traffic": None,
+                "peak_source": f"{peak_src} bf16 burst",
+                "algorithmic_flops_per_launch": gu_f,
+                "down_gemm_TFLOPs": dn_f / (dn_us * 1e-6) / 1e12,
+                "grouped_gemms_frac": (gu_f + dn_f) / ((gu_us + dn_us) * 1e-6) / 1e12 / tf_burst}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": wl.name, "T": wl.T, "hidden": s.hidden, "experts": s.n_experts,
+                   "top_k": s.top_k, "inter": s.inter, "shared_inter": s.shared_inter,
+                   "router_bias_std": wl.bias_std, "parallelism": f"replicas{world}",
+                   "l2": f"flushed between timed steps ({L2_FLUSH_BYTES >> 20} MiB write)"},
+        "roofline": roofline,
+        "kernels_us": kern,
+        "gpu_launches": launches,
+        "clocks": clk,
+    }
+
+    if rank == 0 and not args.skip_e2e:
+        x_h = x.cpu().pin_memory()
+        y_h = torch.empty_like(x_h).pin_memory()
+        e2e_ms = run_prefill_e2e(ctx, x_h, y_h, args.steps, args.warmup, flush, stream)
+        line["e2e"] = {"value": wl.T * args.steps / (e2e_ms * 1e-3), "unit": "tokens/s",
+                       "h2d_bytes_per_step": wl.T * s.hidden * 2,
+                       "d2h_bytes_per_step": wl.T * s.hidden * 2}
+    if rank == 0 and not args.skip_decode:
+        line["decode"] = bench_decode(args, dev, stream, hbm)
+    if rank == 0 and not args.skip_cpu:
+        line["cpu_baseline"] = cpu_baseline_prefill(x.cpu(), w, s.top_k, args.cpu_sample)
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-sample", type=int, default=256)
+    ap.add_argument("--ref-sample", type=int, default=32)
+    ap.add_argument("--decode-int4", action="store_true")
+    ap.add_argument("--skip-decode", action="store_true")
+    ap.add_argument("--skip-e2e", action="store_true")
+    ap.add_argument("--skip-cpu", action="store_true")
+    a = ap.parse_args()
+    if a.warmup < 3 and a.impl == "ours":
+        a.warmup = 3
+    sys.exit(main_reference(a) if a.impl == "reference" else main(a))

@@ -1,0 +1,208 @@
+/*
+ * sparse_moe.h -- C ABI of the GB300 (sm_103a) sparse mixture-of-experts layer.
+ *
+ * The layer is the one described in "Optimizing On-Device Inference for Apple
+ * Silicon" (Perplexity):
+ *   - section "Qwen creates three distinct workload shapes": a router scores E
+ *     experts and selects k per token; one shared expert processes every token;
+ *   - section "Keep expert routing on the GPU": histogram, prefix scan,
+ *     scatter and block map, all enqueued with no host synchronisation;
+ *   - section "Dequantize weights during matrix multiplication": grouped expert
+ *     GEMM with fp32 accumulation, bf16 output, optional 4-bit weights expanded
+ *     one tile at a time in on-chip memory;
+ *   - section "Match tile size to expert load": tile shapes follow each
+ *     expert's row count;
+ *   - section "Optimize the one-row weight path" and "Reduce intermediate and
+ *     state traffic": batch-1 decode as a row-parallel GEMV with the gate/up
+ *     projections fused with the gated activation and the output projection
+ *     fused with the routing score and the shared-expert result;
+ *   - section "Bound temporary memory with prompt chunking": long prompts run
+ *     in bounded chunks with unchanged output.
+ *
+ * For each token t (x[t] in bf16):
+ *   l[t,e]   = sum_h x[t,h] * Wr[e,h] (+ b[e])              fp32 accumulate
+ *   idx[t,:] = the k largest l[t,:], descending; equal logits -> lower e first
+ *   w[t,j]   = exp(l[t,idx_j]) / sum_j' exp(l[t,idx_j'])       (= softmax over
+ *              all experts, renormalised over the selected ones)
+ *   h_e(x)   = silu(Wg_e x) * (Wu_e x),   silu(z) = z / (1 + exp(-z))
+ *   y[t]     = sum_j w[t,j] * Wd_{idx_j} h_{idx_j}(x[t])
+ *              + sigmoid(x[t] . w_sg) * Sd h_shared(x[t])       bf16 output
+ *
+ * Layouts (row-major; every weight is K-major, i.e. each output row is
+ * contiguous along the reduction dimension):
+ *   x, y          bf16  [T, H]
+ *   router_w      bf16  [E, H]            router_b  fp32 [E] or NULL
+ *   gate_up       bf16  [E, 2I, H]        rows 0..I-1 gate, I..2I-1 up
+ *   down          bf16  [E, H, I]
+ *   sh_gate_up    bf16  [2Is, H]          rows 0..Is-1 gate, Is..2Is-1 up
+ *   sh_down       bf16  [H, Is]
+ *   sh_gate_w     bf16  [H]
+ * int4 symmetric group-64 format (wfmt = MOE_W_INT4_SYM_G64), for gate_up,
+ * down, sh_gate_up and sh_down:
+ *   <w>           uint8 [rows, K/2]  element 2m in the low nibble of byte m,
+ *                                    element 2m+1 in the high nibble, each a
+ *                                    two's-complement code q in [-8, 7]
+ *   <w>_scale     bf16  [rows, K/64] weight = scale[r, k/64] * q[r, k]
+ * The router and sh_gate_w stay bf16 in both formats.
+ *
+ * Routing outputs (moe_route), per chunk of T tokens, assignment a = t*k + j:
+ *   counts[e]          number of assignments to expert e             int32 [E]
+ *   offsets[e]         exclusive prefix sum of counts, offsets[E]=T*k int32 [E+1]
+ *   sorted_rows[p]     token of grouped row p; inside an expert's segment
+ *                      [offsets[e], offsets[e+1]) tokens ascend      int32 [T*k]
+ *   pos_of_assign[a]   grouped row of assignment a                  int32 [T*k]
+ *
+ * Ownership: all device memory (weights, activations, workspace) belongs to
+ * the caller.  The context borrows weight pointers from moe_load_weights until
+ * the slot is reloaded or the context is destroyed, and carves its workspace
+ * out of the caller's buffer.  Pointers marked "device" must be device memory
+ * of the context's device; every device pointer must be 16-byte aligned.
+ *
+ * Streams: every compute call is asynchronous on `stream` (a cudaStream_t
+ * passed as void*, NULL = legacy default stream) and never synchronises the
+ * host.  Calls on one context must not overlap in time (they share the
+ * workspace); a context is not thread-safe.
+ *
+ * Errors: every entry returns a moe_status.  Arguments are checked before any
+ * launch; on failure nothing is enqueued and moe_last_error() explains why.
+ * Launch errors are returned as MOE_ERR_CUDA.  Kernels never spin without a
+ * bound: a wait that runs out records a code in a device status word, the
+ * kernel returns, and moe_check_device() reports MOE_ERR_DEVICE_TIMEOUT.
+ */
+#ifndef SPARSE_MOE_H
+#define SPARSE_MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct moe_ctx moe_ctx;
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,     /* NULL, misaligned or out-of-range argument      */
+  MOE_ERR_UNSUPPORTED = 2,     /* shape or format this build does not implement  */
+  MOE_ERR_WORKSPACE = 3,       /* workspace missing, too small or misaligned     */
+  MOE_ERR_CUDA = 4,            /* a CUDA runtime/driver call failed              */
+  MOE_ERR_NOT_LOADED = 5,      /* weights of the requested layer slot not loaded */
+  MOE_ERR_DEVICE_TIMEOUT = 6   /* a bounded device-side wait ran out             */
+} moe_status;
+
+typedef enum {
+  MOE_W_BF16 = 0,              /* all weights bf16                                */
+  MOE_W_INT4_SYM_G64 = 1       /* expert + shared-expert weights int4, group 64   */
+} moe_wfmt;
+
+typedef struct {
+  int hidden;          /* H: multiple of 64, 64..16384                         */
+  int n_experts;       /* E: 1..1024                                           */
+  int top_k;           /* k: 1..min(E, 32)                                     */
+  int inter;           /* I: expert intermediate size, multiple of 64          */
+  int shared_inter;    /* Is: shared-expert intermediate size, multiple of 64  */
+  int n_layers;        /* number of weight slots (layers) the context holds    */
+  int max_chunk_rows;  /* prefill rows per chunk (1..65536); longer prompts run
+                          chunk by chunk with identical per-token results      */
+  int wfmt;            /* moe_wfmt                                             */
+} moe_config;
+
+typedef struct {       /* device pointers, borrowed (see Ownership above)      */
+  const void  *router_w;          /* bf16 [E, H]                               */
+  const float *router_b;          /* fp32 [E] or NULL                          */
+  const void  *gate_up;           /* bf16 [E, 2I, H] | uint8 [E, 2I, H/2]      */
+  const void  *gate_up_scale;     /* NULL (bf16)     | bf16  [E, 2I, H/64]     */
+  const void  *down;              /* bf16 [E, H, I]  | uint8 [E, H, I/2]       */
+  const void  *down_scale;        /* NULL (bf16)     | bf16  [E, H, I/64]      */
+  const void  *sh_gate_up;        /* bf16 [2Is, H]   | uint8 [2Is, H/2]        */
+  const void  *sh_gate_up_scale;  /* NULL (bf16)     | bf16  [2Is, H/64]       */
+  const void  *sh_down;           /* bf16 [H, Is]    | uint8 [H, Is/2]         */
+  const void  *sh_down_scale;     /* NULL (bf16)     | bf16  [H, Is/64]        */
+  const void  *sh_gate_w;         /* bf16 [H]                                  */
+} moe_weights;
+
+/* Bytes of device workspace a context with this config needs (host only). */
+moe_status moe_workspace_size(const moe_config *cfg, size_t *bytes);
+
+/* Validates cfg, binds to `device`, carves `workspace` (device memory,
+ * 256-byte aligned, >= moe_workspace_size bytes, owned by the caller and kept
+ * alive until moe_ctx_destroy) and returns a context in *out.  Host-side set-up
+ * only: it enqueues one zero-fill of the workspace's status words on the legacy
+ * default stream and waits for it. */
+moe_status moe_ctx_create(const moe_config *cfg, int device, void *workspace,
+                          size_t ws_bytes, moe_ctx **out);
+
+/* Frees the host-side context (the workspace and weights stay the caller's). */
+moe_status moe_ctx_destroy(moe_ctx *ctx);
+
+/* Records the device pointers of one layer slot (0 <= layer < n_layers) and
+ * encodes the TMA tensor maps for them.  Host-side only; no device work. */
+moe_status moe_load_weights(moe_ctx *ctx, int layer, const moe_weights *w);
+
+/* Routing only ("Keep expert routing on the GPU"): router logits, top-k,
+ * renormalised weights, histogram, exclusive scan and the stable scatter for
+ * T tokens, 1 <= T <= max_chunk_rows (T = 0 is a no-op).  x is device bf16
+ * [T, H]; outputs are device arrays of the sizes in the header comment:
+ * logits fp32 [T, E] (may be NULL), topk_idx int32 [T, k], topk_w fp32 [T, k],
+ * counts int32 [E], offsets int32 [E+1], sorted_rows int32 [T*k],
+ * pos_of_assign int32 [T*k].  The same kernels run inside
+ * moe_forward_prefill, so its routing is bitwise the one returned here. */
+moe_status moe_route(moe_ctx *ctx, int layer, const void *x, int T,
+                     float *logits, int32_t *topk_idx, float *topk_w,
+                     int32_t *counts, int32_t *offsets,
+                     int32_t *sorted_rows, int32_t *pos_of_assign, void *stream);
+
+/* Prefill: y[T, H] = MoE(x[T, H]) for T >= 0 tokens (device bf16 in and out,
+ * x and y must not overlap).  T > max_chunk_rows runs chunk by chunk. */
+moe_status moe_forward_prefill(moe_ctx *ctx, int layer, const void *x, int T,
+                               void *y, void *stream);
+
+/* Batch-1 decode: y[1, H] = MoE(x[1, H]) with the GEMV path (device bf16). */
+moe_status moe_forward_decode(moe_ctx *ctx, int layer, const void *x, void *y,
+                              void *stream);
+
+/* Routing of the most recent moe_forward_decode on this context, copied
+ * (asynchronously, on `stream`) to device buffers: logits fp32 [E] (may be
+ * NULL), idx int32 [k], w fp32 [k] (either may be NULL). */
+moe_status moe_decode_routing(moe_ctx *ctx, float *logits, int32_t *idx, float *w,
+                              void *stream);
+
+/* End-to-end prefill from HOST memory: copies x_host [T, H] bf16 to the
+ * device chunk by chunk, runs the prefill path and copies y back into y_host
+ * [T, H].  Pinned host buffers make the copies asynchronous; the call returns
+ * once the work is enqueued (synchronise `stream` before reading y_host). */
+moe_status moe_forward_prefill_host(moe_ctx *ctx, int layer, const void *x_host,
+                                    int T, void *y_host, void *stream);
+
+/* Same for one decode token (x_host, y_host: bf16 [H] in host memory). */
+moe_status moe_forward_decode_host(moe_ctx *ctx, int layer, const void *x_host,
+                                   void *y_host, void *stream);
+
+/* Synchronises the device, reads and clears the device status word: MOE_OK,
+ * or MOE_ERR_DEVICE_TIMEOUT (a bounded wait ran out; *code, if non-NULL,
+ * receives the site code), or MOE_ERR_CUDA. */
+moe_status moe_check_device(moe_ctx *ctx, int32_t *code);
+
+/* Per-kernel timing with CUDA events recorded on the launching stream. */
+typedef struct {
+  char   name[32];     /* kernel family                                       */
+  int64_t launches;    /* launches recorded since profiling was enabled       */
+  double total_ms;     /* sum of event-measured durations                     */
+} moe_kernel_stat;
+
+moe_status moe_profile_enable(moe_ctx *ctx, int on);
+/* Synchronises the recorded events and returns up to `max` entries. */
+moe_status moe_profile_read(moe_ctx *ctx, moe_kernel_stat *stats, int max, int *n);
+
+/* Number of kernels this context has launched since creation. */
+int64_t moe_launch_count(const moe_ctx *ctx);
+
+/* Human-readable description of the last failure on this context ("" if none). */
+const char *moe_last_error(const moe_ctx *ctx);
+const char *moe_status_string(moe_status s);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SPARSE_MOE_H */

@@ -1,0 +1,707 @@
+// Host side of the C ABI declared in include/sparse_moe.h: argument checks,
+// workspace carving, TMA tensor-map encoding, and the enqueue order of the
+// prefill and decode kernels.  Nothing here synchronises the host except
+// moe_ctx_create, moe_check_device and moe_profile_read.
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "../../include/sparse_moe.h"
+#include "moe_internal.h"
+
+namespace {
+
+using namespace moe;
+
+constexpr size_t kAlign = 256;
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+struct WsLayout {
+  int Tc, nblk, R, Imax, max_blocks;
+  size_t status, logits, idx, w, mask, base, counts, offsets, sorted, pos, blocks, nblocks, h, o;
+  size_t dec_logits, dec_idx, dec_w, dec_g, dec_h, dec_counter, x_stage, y_stage, total;
+};
+
+WsLayout make_layout(const moe_config &c) {
+  WsLayout L{};
+  L.Tc = c.max_chunk_rows;
+  L.nblk = (L.Tc + kRouteBlockTokens - 1) / kRouteBlockTokens;
+  L.R = L.Tc * c.top_k + L.Tc;
+  L.Imax = std::max(c.inter, c.shared_inter);
+  L.max_blocks = (L.Tc * c.top_k) / kBlockRowsMax + c.n_experts +
+                 (L.Tc + kBlockRowsMax - 1) / kBlockRowsMax + 1;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off = align_up(off + bytes, kAlign);
+    return at;
+  };
+  const size_t E = c.n_experts, k = c.top_k, H = c.hidden, Tc = L.Tc;
+  L.status = take(256);
+  L.logits = take(Tc * E * 4);
+  L.idx = take(Tc * k * 4);
+  L.w = take(Tc * k * 4);
+  L.mask = take(static_cast<size_t>(L.nblk) * E * 4);
+  L.base = take(static_cast<size_t>(L.nblk) * E * 4);
+  L.counts = take(E * 4);
+  L.offsets = take((E + 1) * 4);
+  L.sorted = take(Tc * k * 4);
+  L.pos = take(Tc * k * 4);
+  L.blocks = take(static_cast<size_t>(L.max_blocks) * 16);
+  L.nblocks = take(16);
+  L.h = take(static_cast<size_t>(L.R) * L.Imax * 2);
+  L.o = take(static_cast<size_t>(L.R) * H * 2);
+  L.dec_logits = take(E * 4);
+  L.dec_idx = take(k * 4);
+  L.dec_w = take(k * 4);
+  L.dec_g = take(4);
+  L.dec_h = take((k + 1) * L.Imax * 4);
+  L.dec_counter = take(16);
+  L.x_stage = take(Tc * H * 2);
+  L.y_stage = take(Tc * H * 2);
+  L.total = off;
+  return L;
+}
+
+// ---------------------------------------------------------- tensor maps --
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 2-D bf16 matrix [outer, inner] (inner contiguous), 128-byte swizzled boxes
+// of {box_inner, box_outer} elements.
+bool encode_bf16_2d(CUtensorMap *m, const void *ptr, uint64_t inner, uint64_t outer,
+                    uint32_t box_inner, uint32_t box_outer) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {inner * 2};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+enum KernelId : int {
+  K_ROUTER_GEMM = 0, K_TOPK, K_SCAN, K_SCATTER, K_GATEUP_GEMM, K_DOWN_GEMM, K_COMBINE,
+  K_DEC_ROUTER_SHARED, K_DEC_GATEUP, K_DEC_DOWN, K_H2D, K_D2H, K_COUNT
+};
+const char *kKernelNames[K_COUNT] = {
+    "router_gemm", "topk", "route_scan", "route_scatter", "gateup_swiglu_gemm", "down_gemm",
+    "combine", "decode_router_shared", "decode_gateup", "decode_down_combine", "h2d_copy",
+    "d2h_copy"};
+
+}  // namespace
+
+struct LayerSlot {
+  bool loaded = false;
+  moe_weights w{};
+  CUtensorMap map_router, map_gu, map_gu_sh, map_dn, map_dn_sh;
+};
+
+struct moe_ctx {
+  moe_config cfg{};
+  int device = 0;
+  int num_sms = 0;
+  char *ws = nullptr;
+  size_t ws_bytes = 0;
+  WsLayout L{};
+  CUtensorMap map_h;
+  std::vector<LayerSlot> layers;
+  std::string last_error;
+  int64_t launches = 0;
+  // profiling
+  bool profiling = false;
+  struct Rec { int id; cudaEvent_t a, b; };
+  std::vector<Rec> pending;
+  std::vector<cudaEvent_t> event_pool;
+  int64_t prof_launches[K_COUNT] = {};
+  double prof_ms[K_COUNT] = {};
+
+  template <class T> T *at(size_t off) const { return reinterpret_cast<T *>(ws + off); }
+  int *status() const { return at<int>(L.status); }
+};
+
+namespace {
+
+moe_status fail(moe_ctx *ctx, moe_status s, const char *fmt, ...) {
+  if (ctx) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    ctx->last_error = buf;
+  }
+  return s;
+}
+
+moe_status cuda_fail(moe_ctx *ctx, cudaError_t e, const char *what) {
+  return fail(ctx, MOE_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+moe_status check_config(const moe_config *c) {
+  if (!c) return MOE_ERR_INVALID_ARG;
+  if (c->hidden < 64 || c->hidden > 16384 || c->hidden % 64) return MOE_ERR_INVALID_ARG;
+  if (c->n_experts < 1 || c->n_experts > 1024) return MOE_ERR_INVALID_ARG;
+  if (c->top_k < 1 || c->top_k > std::min(c->n_experts, 32)) return MOE_ERR_INVALID_ARG;
+  if (c->inter < 64 || c->inter % 64 || c->shared_inter < 64 || c->shared_inter % 64)
+    return MOE_ERR_INVALID_ARG;
+  if (c->inter > 16384 || c->shared_inter > 16384) return MOE_ERR_INVALID_ARG;
+  if (c->n_layers < 1 || c->n_layers > 4096) return MOE_ERR_INVALID_ARG;
+  if (c->max_chunk_rows < 1 || c->max_chunk_rows > 65536) return MOE_ERR_INVALID_ARG;
+  if (c->wfmt != MOE_W_BF16 && c->wfmt != MOE_W_INT4_SYM_G64) return MOE_ERR_INVALID_ARG;
+  const size_t imax = std::max(c->inter, c->shared_inter);
+  if ((c->top_k + 1) * imax * 4 > 200 * 1024 || c->hidden * 4 > 200 * 1024)
+    return MOE_ERR_UNSUPPORTED;   // decode staging must fit in shared memory
+  return MOE_OK;
+}
+
+struct ProfScope {
+  moe_ctx *ctx;
+  int id;
+  cudaStream_t s;
+  cudaEvent_t a = nullptr, b = nullptr;
+  ProfScope(moe_ctx *c, int kid, cudaStream_t st) : ctx(c), id(kid), s(st) {
+    if (!ctx->profiling) return;
+    if (ctx->event_pool.size() < 2) {
+      for (int i = 0; i < 64; ++i) {
+        cudaEvent_t e;
+        if (cudaEventCreate(&e) != cudaSuccess) break;
+        ctx->event_pool.push_back(e);
+      }
+      if (ctx->event_pool.size() < 2) return;
+    }
+    a = ctx->event_pool.back();
+    ctx->event_pool.pop_back();
+    b = ctx->event_pool.back();
+    ctx->event_pool.pop_back();
+    cudaEventRecord(a, s);
+  }
+  ~ProfScope() {
+    if (!a) return;
+    cudaEventRecord(b, s);
+    ctx->pending.push_back({id, a, b});
+  }
+};
+
+moe_status ensure_device(moe_ctx *ctx) {
+  int cur = -1;
+  cudaError_t e = cudaGetDevice(&cur);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaGetDevice");
+  if (cur != ctx->device) {
+    e = cudaSetDevice(ctx->device);
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaSetDevice");
+  }
+  return MOE_OK;
+}
+
+moe_status launched(moe_ctx *ctx, cudaError_t e, const char *what) {
+  ++ctx->launches;
+  if (e != cudaSuccess) return cuda_fail(ctx, e, what);
+  return MOE_OK;
+}
+
+int router_block_rows(const moe_ctx *ctx, int T) {
+  const int mt = (ctx->cfg.n_experts + 127) / 128;
+  int br = (T * mt + ctx->num_sms - 1) / ctx->num_sms;
+  br = (br + 15) & ~15;
+  return std::min(kBlockRowsMax, std::max(16, br));
+}
+
+// Router GEMM, top-k, histogram/scan/block map, scatter for T <= Tc tokens.
+moe_status enqueue_route(moe_ctx *ctx, const LayerSlot &ls, const void *x, int T, float *logits,
+                         int32_t *idx, float *w, int32_t *counts, int32_t *offsets,
+                         int32_t *sorted_rows, int32_t *pos, cudaStream_t s) {
+  const moe_config &c = ctx->cfg;
+  const WsLayout &L = ctx->L;
+  CUtensorMap map_x_direct;
+  if (!encode_bf16_2d(&map_x_direct, x, c.hidden, T, 64, 16))
+    return fail(ctx, MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed for x (T=%d)", T);
+  GemmParams gp{};
+  gp.mode = MODE_ROUTER;
+  gp.block_rows = router_block_rows(ctx, T);
+  gp.n_blocks_host = (T + gp.block_rows - 1) / gp.block_rows;
+  gp.T = T;
+  gp.m_tiles = (c.n_experts + 127) / 128;
+  gp.n_experts = c.n_experts;
+  gp.hidden = c.hidden;
+  gp.inter_routed = c.inter;
+  gp.inter_shared = c.shared_inter;
+  gp.k_routed = c.hidden;
+  gp.out = logits;
+  gp.out_ld = c.n_experts;
+  gp.bias = ls.w.router_b;
+  gp.status = ctx->status();
+  const int tiles = gp.n_blocks_host * gp.m_tiles;
+  moe_status st;
+  {
+    ProfScope ps(ctx, K_ROUTER_GEMM, s);
+    st = launched(ctx, launch_tc_gemm(ls.map_router, ls.map_router, map_x_direct, gp,
+                                      std::min(ctx->num_sms, tiles), s),
+                  "router gemm launch");
+  }
+  if (st) return st;
+  uint32_t *mask = ctx->at<uint32_t>(L.mask);
+  int32_t *base = ctx->at<int32_t>(L.base);
+  {
+    ProfScope ps(ctx, K_TOPK, s);
+    st = launched(ctx, launch_topk(logits, T, c.n_experts, c.top_k, idx, w, mask, s), "topk launch");
+  }
+  if (st) return st;
+  const int nblk = (T + kRouteBlockTokens - 1) / kRouteBlockTokens;
+  {
+    ProfScope ps(ctx, K_SCAN, s);
+    st = launched(ctx,
+                  launch_scan(mask, nblk, T, c.n_experts, c.top_k, counts, offsets, base,
+                              ctx->at<int4>(L.blocks), ctx->at<int32_t>(L.nblocks), s),
+                  "scan launch");
+  }
+  if (st) return st;
+  {
+    ProfScope ps(ctx, K_SCATTER, s);
+    st = launched(ctx,
+                  launch_scatter(idx, mask, base, offsets, T, c.n_experts, c.top_k, sorted_rows,
+                                 pos, s),
+                  "scatter launch");
+  }
+  return st;
+}
+
+moe_status enqueue_prefill_chunk(moe_ctx *ctx, const LayerSlot &ls, const void *x, int T, void *y,
+                                 cudaStream_t s) {
+  const moe_config &c = ctx->cfg;
+  const WsLayout &L = ctx->L;
+  int32_t *idx = ctx->at<int32_t>(L.idx);
+  float *w = ctx->at<float>(L.w);
+  int32_t *sorted = ctx->at<int32_t>(L.sorted);
+  int32_t *pos = ctx->at<int32_t>(L.pos);
+  moe_status st = enqueue_route(ctx, ls, x, T, ctx->at<float>(L.logits), idx, w,
+                                ctx->at<int32_t>(L.counts), ctx->at<int32_t>(L.offsets), sorted,
+                                pos, s);
+  if (st) return st;
+  CUtensorMap map_x_gather;
+  if (!encode_bf16_2d(&map_x_gather, x, c.hidden, T, 64, 1))
+    return fail(ctx, MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed for x gather (T=%d)", T);
+  GemmParams gp{};
+  gp.blocks = ctx->at<int4>(L.blocks);
+  gp.n_blocks_dev = ctx->at<int32_t>(L.nblocks);
+  gp.T = T;
+  gp.n_experts = c.n_experts;
+  gp.hidden = c.hidden;
+  gp.inter_routed = c.inter;
+  gp.inter_shared = c.shared_inter;
+  gp.k_routed = c.hidden;
+  gp.shared_row0 = T * c.top_k;
+  gp.sorted_rows = sorted;
+  gp.status = ctx->status();
+  // gate/up + SwiGLU -> h
+  gp.mode = MODE_GATEUP;
+  gp.m_tiles = L.Imax / 64;
+  gp.out = ctx->at<void>(L.h);
+  gp.out_ld = L.Imax;
+  {
+    ProfScope ps(ctx, K_GATEUP_GEMM, s);
+    st = launched(ctx, launch_tc_gemm(ls.map_gu, ls.map_gu_sh, map_x_gather, gp, ctx->num_sms, s),
+                  "gate/up gemm launch");
+  }
+  if (st) return st;
+  // down -> o
+  gp.mode = MODE_DOWN;
+  gp.m_tiles = (c.hidden + 127) / 128;
+  gp.out = ctx->at<void>(L.o);
+  gp.out_ld = c.hidden;
+  {
+    ProfScope ps(ctx, K_DOWN_GEMM, s);
+    st = launched(ctx, launch_tc_gemm(ls.map_dn, ls.map_dn_sh, ctx->map_h, gp, ctx->num_sms, s),
+                  "down gemm launch");
+  }
+  if (st) return st;
+  {
+    ProfScope ps(ctx, K_COMBINE, s);
+    st = launched(ctx,
+                  launch_combine(x, ls.w.sh_gate_w, ctx->at<void>(L.o), pos, w, T, c.hidden,
+                                 c.top_k, y, s),
+                  "combine launch");
+  }
+  return st;
+}
+
+moe_status check_layer(moe_ctx *ctx, int layer) {
+  if (!ctx) return MOE_ERR_INVALID_ARG;
+  if (layer < 0 || layer >= ctx->cfg.n_layers)
+    return fail(ctx, MOE_ERR_INVALID_ARG, "layer %d out of range [0, %d)", layer, ctx->cfg.n_layers);
+  if (!ctx->layers[layer].loaded) return fail(ctx, MOE_ERR_NOT_LOADED, "layer %d not loaded", layer);
+  return MOE_OK;
+}
+
+moe_status enqueue_decode(moe_ctx *ctx, const LayerSlot &ls, const void *x, void *y,
+                          cudaStream_t s) {
+  const moe_config &c = ctx->cfg;
+  const WsLayout &L = ctx->L;
+  DecodeParams p{};
+  p.x = x;
+  p.y = y;
+  p.H = c.hidden;
+  p.E = c.n_experts;
+  p.k = c.top_k;
+  p.I = c.inter;
+  p.Is = c.shared_inter;
+  p.wfmt = c.wfmt;
+  p.router_w = ls.w.router_w;
+  p.router_b = ls.w.router_b;
+  p.gate_up = ls.w.gate_up;
+  p.gate_up_scale = ls.w.gate_up_scale;
+  p.down = ls.w.down;
+  p.down_scale = ls.w.down_scale;
+  p.sh_gate_up = ls.w.sh_gate_up;
+  p.sh_gate_up_scale = ls.w.sh_gate_up_scale;
+  p.sh_down = ls.w.sh_down;
+  p.sh_down_scale = ls.w.sh_down_scale;
+  p.sh_gate_w = ls.w.sh_gate_w;
+  p.logits = ctx->at<float>(L.dec_logits);
+  p.idx = ctx->at<int32_t>(L.dec_idx);
+  p.w = ctx->at<float>(L.dec_w);
+  p.g = ctx->at<float>(L.dec_g);
+  p.h = ctx->at<float>(L.dec_h);
+  p.h_ld = L.Imax;
+  p.counter = ctx->at<unsigned int>(L.dec_counter);
+  moe_status st;
+  {
+    ProfScope ps(ctx, K_DEC_ROUTER_SHARED, s);
+    st = launched(ctx, launch_decode_router_shared(p, s), "decode router launch");
+  }
+  if (st) return st;
+  {
+    ProfScope ps(ctx, K_DEC_GATEUP, s);
+    st = launched(ctx, launch_decode_gateup(p, s), "decode gate/up launch");
+  }
+  if (st) return st;
+  {
+    ProfScope ps(ctx, K_DEC_DOWN, s);
+    st = launched(ctx, launch_decode_down(p, s), "decode down launch");
+  }
+  return st;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *moe_status_string(moe_status s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported";
+    case MOE_ERR_WORKSPACE: return "workspace too small or misaligned";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_NOT_LOADED: return "layer weights not loaded";
+    case MOE_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
+  }
+  return "unknown status";
+}
+
+moe_status moe_workspace_size(const moe_config *cfg, size_t *bytes) {
+  if (!bytes) return MOE_ERR_INVALID_ARG;
+  const moe_status st = check_config(cfg);
+  if (st) return st;
+  *bytes = make_layout(*cfg).total;
+  return MOE_OK;
+}
+
+moe_status moe_ctx_create(const moe_config *cfg, int device, void *workspace, size_t ws_bytes,
+                          moe_ctx **out) {
+  if (!out) return MOE_ERR_INVALID_ARG;
+  *out = nullptr;
+  moe_status st = check_config(cfg);
+  if (st) return st;
+  const WsLayout L = make_layout(*cfg);
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) % kAlign) != 0 || ws_bytes < L.total)
+    return MOE_ERR_WORKSPACE;
+  cudaError_t e = cudaSetDevice(device);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  int major = 0, minor = 0, sms = 0;
+  cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, device);
+  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, device);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
+  if (major != 10 || minor != 3) return MOE_ERR_UNSUPPORTED;   // built for sm_103a only
+  if (!encode_fn()) return MOE_ERR_CUDA;
+  moe_ctx *ctx = new moe_ctx();
+  ctx->cfg = *cfg;
+  ctx->device = device;
+  ctx->num_sms = sms;
+  ctx->ws = static_cast<char *>(workspace);
+  ctx->ws_bytes = ws_bytes;
+  ctx->L = L;
+  ctx->layers.resize(cfg->n_layers);
+  if (!encode_bf16_2d(&ctx->map_h, ctx->ws + L.h, L.Imax, L.R, 64, 16)) {
+    delete ctx;
+    return MOE_ERR_CUDA;
+  }
+  if ((e = gemm_configure()) != cudaSuccess ||
+      (e = decode_configure(std::max(cfg->hidden, (cfg->top_k + 1) * L.Imax))) != cudaSuccess ||
+      (e = cudaMemset(ctx->ws + L.status, 0, 256)) != cudaSuccess ||
+      (e = cudaMemset(ctx->ws + L.dec_counter, 0, 16)) != cudaSuccess ||
+      (e = cudaDeviceSynchronize()) != cudaSuccess) {
+    delete ctx;
+    return MOE_ERR_CUDA;
+  }
+  *out = ctx;
+  return MOE_OK;
+}
+
+moe_status moe_ctx_destroy(moe_ctx *ctx) {
+  if (!ctx) return MOE_ERR_INVALID_ARG;
+  for (auto &r : ctx->pending) {
+    cudaEventDestroy(r.a);
+    cudaEventDestroy(r.b);
+  }
+  for (auto e : ctx->event_pool) cudaEventDestroy(e);
+  delete ctx;
+  return MOE_OK;
+}
+
+moe_status moe_load_weights(moe_ctx *ctx, int layer, const moe_weights *w) {
+  if (!ctx || !w) return fail(ctx, MOE_ERR_INVALID_ARG, "null context or weights");
+  if (layer < 0 || layer >= ctx->cfg.n_layers)
+    return fail(ctx, MOE_ERR_INVALID_ARG, "layer %d out of range", layer);
+  const moe_config &c = ctx->cfg;
+  const bool int4 = c.wfmt == MOE_W_INT4_SYM_G64;
+  const void *req[] = {w->router_w, w->gate_up, w->down, w->sh_gate_up, w->sh_down, w->sh_gate_w};
+  for (const void *p : req)
+    if (!p || !aligned16(p)) return fail(ctx, MOE_ERR_INVALID_ARG, "weight pointer null or not 16-byte aligned");
+  if (w->router_b && (reinterpret_cast<uintptr_t>(w->router_b) & 3))
+    return fail(ctx, MOE_ERR_INVALID_ARG, "router_b misaligned");
+  if (int4) {
+    const void *sc[] = {w->gate_up_scale, w->down_scale, w->sh_gate_up_scale, w->sh_down_scale};
+    for (const void *p : sc)
+      if (!p || (reinterpret_cast<uintptr_t>(p) & 1))
+        return fail(ctx, MOE_ERR_INVALID_ARG, "int4 format needs all four scale pointers");
+  }
+  LayerSlot &ls = ctx->layers[layer];
+  ls.loaded = false;
+  ls.w = *w;
+  bool ok = encode_bf16_2d(&ls.map_router, w->router_w, c.hidden, c.n_experts, 64, 128);
+  if (!int4) {
+    ok = ok && encode_bf16_2d(&ls.map_gu, w->gate_up, c.hidden,
+                              static_cast<uint64_t>(c.n_experts) * 2 * c.inter, 64, 64);
+    ok = ok && encode_bf16_2d(&ls.map_gu_sh, w->sh_gate_up, c.hidden, 2 * c.shared_inter, 64, 64);
+    ok = ok && encode_bf16_2d(&ls.map_dn, w->down, c.inter,
+                              static_cast<uint64_t>(c.n_experts) * c.hidden, 64, 128);
+    ok = ok && encode_bf16_2d(&ls.map_dn_sh, w->sh_down, c.shared_inter, c.hidden, 64, 128);
+  }
+  if (!ok) return fail(ctx, MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed for layer %d", layer);
+  ls.loaded = true;
+  return MOE_OK;
+}
+
+moe_status moe_route(moe_ctx *ctx, int layer, const void *x, int T, float *logits,
+                     int32_t *topk_idx, float *topk_w, int32_t *counts, int32_t *offsets,
+                     int32_t *sorted_rows, int32_t *pos_of_assign, void *stream) {
+  moe_status st = check_layer(ctx, layer);
+  if (st) return st;
+  if (T < 0 || T > ctx->cfg.max_chunk_rows)
+    return fail(ctx, MOE_ERR_INVALID_ARG, "T=%d outside [0, max_chunk_rows=%d]", T,
+                ctx->cfg.max_chunk_rows);
+  if (T == 0) return MOE_OK;
+  if (!x || !aligned16(x) || !topk_idx || !topk_w || !counts || !offsets || !sorted_rows ||
+      !pos_of_assign)
+    return fail(ctx, MOE_ERR_INVALID_ARG, "null or misaligned routing buffer");
+  if ((st = ensure_device(ctx))) return st;
+  float *lg = logits ? logits : ctx->at<float>(ctx->L.logits);
+  return enqueue_route(ctx, ctx->layers[layer], x, T, lg, topk_idx, topk_w, counts, offsets,
+                       sorted_rows, pos_of_assign, static_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_forward_prefill(moe_ctx *ctx, int layer, const void *x, int T, void *y,
+                               void *stream) {
+  moe_status st = check_layer(ctx, layer);
+  if (st) return st;
+  if (T < 0) return fail(ctx, MOE_ERR_INVALID_ARG, "T=%d < 0", T);
+  if (T == 0) return MOE_OK;
+  if (!x || !y || !aligned16(x) || !aligned16(y))
+    return fail(ctx, MOE_ERR_INVALID_ARG, "x/y null or not 16-byte aligned");
+  if (ctx->cfg.wfmt != MOE_W_BF16)
+    return fail(ctx, MOE_ERR_UNSUPPORTED, "int4 prefill is not built yet");
+  const size_t row_bytes = static_cast<size_t>(ctx->cfg.hidden) * 2;
+  const char *xb = static_cast<const char *>(x);
+  char *yb = static_cast<char *>(y);
+  if (xb < yb + T * row_bytes && yb < xb + T * row_bytes)
+    return fail(ctx, MOE_ERR_INVALID_ARG, "x and y overlap");
+  if ((st = ensure_device(ctx))) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const LayerSlot &ls = ctx->layers[layer];
+  for (int c0 = 0; c0 < T; c0 += ctx->cfg.max_chunk_rows) {
+    const int n = std::min(ctx->cfg.max_chunk_rows, T - c0);
+    st = enqueue_prefill_chunk(ctx, ls, xb + c0 * row_bytes, n, yb + c0 * row_bytes, s);
+    if (st) return st;
+  }
+  return MOE_OK;
+}
+
+moe_status moe_forward_decode(moe_ctx *ctx, int layer, const void *x, void *y, void *stream) {
+  moe_status st = check_layer(ctx, layer);
+  if (st) return st;
+  if (!x || !y || !aligned16(x) || !aligned16(y))
+    return fail(ctx, MOE_ERR_INVALID_ARG, "x/y null or not 16-byte aligned");
+  if ((st = ensure_device(ctx))) return st;
+  return enqueue_decode(ctx, ctx->layers[layer], x, y, static_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_decode_routing(moe_ctx *ctx, float *logits, int32_t *idx, float *w, void *stream) {
+  if (!ctx) return MOE_ERR_INVALID_ARG;
+  moe_status st = ensure_device(ctx);
+  if (st) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const moe_config &c = ctx->cfg;
+  cudaError_t e = cudaSuccess;
+  if (logits)
+    e = cudaMemcpyAsync(logits, ctx->ws + ctx->L.dec_logits, c.n_experts * 4,
+                        cudaMemcpyDeviceToDevice, s);
+  if (e == cudaSuccess && idx)
+    e = cudaMemcpyAsync(idx, ctx->ws + ctx->L.dec_idx, c.top_k * 4, cudaMemcpyDeviceToDevice, s);
+  if (e == cudaSuccess && w)
+    e = cudaMemcpyAsync(w, ctx->ws + ctx->L.dec_w, c.top_k * 4, cudaMemcpyDeviceToDevice, s);
+  return e == cudaSuccess ? MOE_OK : cuda_fail(ctx, e, "decode routing copy");
+}
+
+moe_status moe_forward_prefill_host(moe_ctx *ctx, int layer, const void *x_host, int T,
+                                    void *y_host, void *stream) {
+  moe_status st = check_layer(ctx, layer);
+  if (st) return st;
+  if (T < 0 || (T > 0 && (!x_host || !y_host)))
+    return fail(ctx, MOE_ERR_INVALID_ARG, "bad host buffers or T");
+  if (T == 0) return MOE_OK;
+  if (ctx->cfg.wfmt != MOE_W_BF16)
+    return fail(ctx, MOE_ERR_UNSUPPORTED, "int4 prefill is not built yet");
+  if ((st = ensure_device(ctx))) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t row_bytes = static_cast<size_t>(ctx->cfg.hidden) * 2;
+  void *xs = ctx->ws + ctx->L.x_stage;
+  void *ys = ctx->ws + ctx->L.y_stage;
+  const LayerSlot &ls = ctx->layers[layer];
+  for (int c0 = 0; c0 < T; c0 += ctx->cfg.max_chunk_rows) {
+    const int n = std::min(ctx->cfg.max_chunk_rows, T - c0);
+    cudaError_t e;
+    {
+      ProfScope ps(ctx, K_H2D, s);
+      e = cudaMemcpyAsync(xs, static_cast<const char *>(x_host) + c0 * row_bytes, n * row_bytes,
+                          cudaMemcpyHostToDevice, s);
+    }
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "host-to-device copy");
+    st = enqueue_prefill_chunk(ctx, ls, xs, n, ys, s);
+    if (st) return st;
+    {
+      ProfScope ps(ctx, K_D2H, s);
+      e = cudaMemcpyAsync(static_cast<char *>(y_host) + c0 * row_bytes, ys, n * row_bytes,
+                          cudaMemcpyDeviceToHost, s);
+    }
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "device-to-host copy");
+  }
+  return MOE_OK;
+}
+
+moe_status moe_forward_decode_host(moe_ctx *ctx, int layer, const void *x_host, void *y_host,
+                                   void *stream) {
+  moe_status st = check_layer(ctx, layer);
+  if (st) return st;
+  if (!x_host || !y_host) return fail(ctx, MOE_ERR_INVALID_ARG, "null host buffer");
+  if ((st = ensure_device(ctx))) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t bytes = static_cast<size_t>(ctx->cfg.hidden) * 2;
+  void *xs = ctx->ws + ctx->L.x_stage;
+  void *ys = ctx->ws + ctx->L.y_stage;
+  cudaError_t e = cudaMemcpyAsync(xs, x_host, bytes, cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "host-to-device copy");
+  st = enqueue_decode(ctx, ctx->layers[layer], xs, ys, s);
+  if (st) return st;
+  e = cudaMemcpyAsync(y_host, ys, bytes, cudaMemcpyDeviceToHost, s);
+  return e == cudaSuccess ? MOE_OK : cuda_fail(ctx, e, "device-to-host copy");
+}
+
+moe_status moe_check_device(moe_ctx *ctx, int32_t *code) {
+  if (!ctx) return MOE_ERR_INVALID_ARG;
+  moe_status st = ensure_device(ctx);
+  if (st) return st;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "device synchronize");
+  int32_t v = 0;
+  e = cudaMemcpy(&v, ctx->status(), 4, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "status read");
+  if (code) *code = v;
+  if (v != 0) {
+    cudaMemset(ctx->status(), 0, 4);
+    cudaDeviceSynchronize();
+    return fail(ctx, MOE_ERR_DEVICE_TIMEOUT, "device wait timed out (site 0x%x)", v);
+  }
+  return MOE_OK;
+}
+
+moe_status moe_profile_enable(moe_ctx *ctx, int on) {
+  if (!ctx) return MOE_ERR_INVALID_ARG;
+  if (on && !ctx->profiling) {
+    for (int i = 0; i < K_COUNT; ++i) {
+      ctx->prof_ms[i] = 0.0;
+      ctx->prof_launches[i] = 0;
+    }
+  }
+  ctx->profiling = on != 0;
+  return MOE_OK;
+}
+
+moe_status moe_profile_read(moe_ctx *ctx, moe_kernel_stat *stats, int max, int *n) {
+  if (!ctx || !n || (max > 0 && !stats)) return MOE_ERR_INVALID_ARG;
+  moe_status st = ensure_device(ctx);
+  if (st) return st;
+  for (auto &r : ctx->pending) {
+    float ms = 0.0f;
+    if (cudaEventSynchronize(r.b) == cudaSuccess && cudaEventElapsedTime(&ms, r.a, r.b) == cudaSuccess) {
+      ctx->prof_ms[r.id] += ms;
+      ctx->prof_launches[r.id] += 1;
+    }
+    ctx->event_pool.push_back(r.a);
+    ctx->event_pool.push_back(r.b);
+  }
+  ctx->pending.clear();
+  int cnt = 0;
+  for (int i = 0; i < K_COUNT; ++i) {
+    if (ctx->prof_launches[i] == 0) continue;
+    if (cnt < max) {
+      std::memset(&stats[cnt], 0, sizeof(moe_kernel_stat));
+      std::snprintf(stats[cnt].name, sizeof(stats[cnt].name), "%s", kKernelNames[i]);
+      stats[cnt].launches = ctx->prof_launches[i];
+      stats[cnt].total_ms = ctx->prof_ms[i];
+    }
+    ++cnt;
+  }
+  *n = cnt;
+  return MOE_OK;
+}
+
+int64_t moe_launch_count(const moe_ctx *ctx) { return ctx ? ctx->launches : 0; }
+
+const char *moe_last_error(const moe_ctx *ctx) { return ctx ? ctx->last_error.c_str() : ""; }
+
+}  // extern "C"

@@ -1,0 +1,84 @@
+// Internal declarations shared by the library's translation units.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace moe {
+
+// Rows per grouped-GEMM block (and the largest MMA N).  An expert with c rows
+// becomes ceil(c / kBlockRowsMax) blocks; each block's MMA N is its row count
+// rounded up to 16.
+constexpr int kBlockRowsMax = 256;
+// Tokens per routing block (one 32-bit mask word per expert per block).
+constexpr int kRouteBlockTokens = 32;
+
+enum GemmMode : int { MODE_ROUTER = 0, MODE_GATEUP = 1, MODE_DOWN = 2 };
+
+struct GemmParams {
+  int mode;
+  const int4 *blocks;        // grouped modes: {expert (E = shared), row_start, n_rows, 0}
+  const int *n_blocks_dev;   // grouped modes: block count in device memory
+  int n_blocks_host;         // router: token blocks
+  int block_rows;            // router: tokens per block
+  int T;                     // tokens of the chunk
+  int m_tiles;               // weight-row tiles per block
+  int n_experts;             // E
+  int hidden;                // H
+  int inter_routed;          // I
+  int inter_shared;          // Is
+  int k_routed;              // reduction length (router, gate/up: H)
+  int shared_row0;           // first grouped row of the shared expert (T*k)
+  const int *sorted_rows;    // token of each grouped row
+  void *out;                 // router: fp32 [T,E]; gate/up: bf16 h [R,ld]; down: bf16 o [R,H]
+  int out_ld;                // elements per output row
+  const float *bias;         // router bias or null
+  int *status;               // device status word
+};
+
+cudaError_t gemm_configure();
+cudaError_t launch_tc_gemm(const CUtensorMap &a_routed, const CUtensorMap &a_shared,
+                           const CUtensorMap &b, const GemmParams &p, int grid,
+                           cudaStream_t stream);
+
+// Routing: top-k + masks, block scan + block map, stable scatter.
+cudaError_t launch_topk(const float *logits, int T, int E, int k, int32_t *idx, float *w,
+                        uint32_t *blk_mask, cudaStream_t stream);
+cudaError_t launch_scan(const uint32_t *blk_mask, int nblk, int T, int E, int k,
+                        int32_t *counts, int32_t *offsets, int32_t *blk_base, int4 *blocks,
+                        int32_t *n_blocks, cudaStream_t stream);
+cudaError_t launch_scatter(const int32_t *idx, const uint32_t *blk_mask, const int32_t *blk_base,
+                           const int32_t *offsets, int T, int E, int k, int32_t *sorted_rows,
+                           int32_t *pos_of_assign, cudaStream_t stream);
+
+// y[t] = sum_j w[t,j] o[pos(t,j)] + sigmoid(x[t].w_sg) o[T*k + t]
+cudaError_t launch_combine(const void *x, const void *sh_gate_w, const void *o,
+                           const int32_t *pos, const float *w, int T, int H, int k, void *y,
+                           cudaStream_t stream);
+
+// Batch-1 decode.
+struct DecodeParams {
+  const void *x;             // bf16 [H]
+  void *y;                   // bf16 [H]
+  int H, E, k, I, Is, wfmt;
+  const void *router_w;
+  const float *router_b;
+  const void *gate_up, *gate_up_scale, *down, *down_scale;
+  const void *sh_gate_up, *sh_gate_up_scale, *sh_down, *sh_down_scale;
+  const void *sh_gate_w;
+  float *logits;             // [E]
+  int32_t *idx;              // [k]
+  float *w;                  // [k]
+  float *g;                  // [1]
+  float *h;                  // [(k+1), Imax] fp32; row k = shared expert
+  int h_ld;
+  unsigned int *counter;     // last-block-done counter (zero between launches)
+};
+cudaError_t decode_configure(int max_smem_floats);
+// The three decode launches, in order (see decode.cu).
+cudaError_t launch_decode_router_shared(const DecodeParams &p, cudaStream_t stream);
+cudaError_t launch_decode_gateup(const DecodeParams &p, cudaStream_t stream);
+cudaError_t launch_decode_down(const DecodeParams &p, cudaStream_t stream);
+
+}  // namespace moe

@@ -1,0 +1,287 @@
+// Device-resident routing for the prefill path (section "Keep expert routing
+// on the GPU" of "Optimizing On-Device Inference for Apple Silicon"): top-k
+// selection, a histogram of assignments per expert, an exclusive prefix scan
+// into segment offsets, a stable scatter of rows into their expert segments,
+// and the block map the grouped GEMMs walk.  No host synchronisation; every
+// result is independent of thread timing (integer counts and bit masks only).
+//
+// Tokens are processed in routing blocks of 32.  For each block and expert a
+// 32-bit mask records which of the block's tokens chose the expert; the rank
+// of a token inside its expert segment is then
+//     offsets[e] + (rows of e in earlier blocks) + popc(mask & lower bits),
+// i.e. segments are ordered by ascending token index.
+#include "moe_internal.h"
+#include "warp_topk.cuh"
+
+namespace moe {
+
+// ----------------------------------------------------------------- top-k --
+template <int R>
+__global__ void __launch_bounds__(256) topk_kernel(const float *__restrict__ logits, int T, int E,
+                                                   int k, int32_t *__restrict__ idx,
+                                                   float *__restrict__ w,
+                                                   uint32_t *__restrict__ blk_mask) {
+  __shared__ uint32_t mask_s[1024];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) mask_s[e] = 0;
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr int kTokPerWarp = kRouteBlockTokens / 8;
+  for (int i = 0; i < kTokPerWarp; ++i) {
+    const int tl = warp * kTokPerWarp + i;
+    const int t = blockIdx.x * kRouteBlockTokens + tl;
+    if (t >= T) break;
+    float v[R];
+    const float *row = logits + static_cast<size_t>(t) * E;
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      const int e = lane + 32 * r;
+      v[r] = (e < E) ? row[e] : -INFINITY;
+    }
+    float sv, sw;
+    int se;
+    warp_topk<R>(v, E, k, sv, se, sw);
+    if (lane < k) {
+      idx[static_cast<size_t>(t) * k + lane] = se;
+      w[static_cast<size_t>(t) * k + lane] = sw;
+      atomicOr(&mask_s[se], 1u << tl);
+    }
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x)
+    blk_mask[static_cast<size_t>(blockIdx.x) * E + e] = mask_s[e];
+}
+
+cudaError_t launch_topk(const float *logits, int T, int E, int k, int32_t *idx, float *w,
+                        uint32_t *blk_mask, cudaStream_t stream) {
+  const int nblk = (T + kRouteBlockTokens - 1) / kRouteBlockTokens;
+  const int R = (E + 31) / 32;
+  if (R <= 1)
+    topk_kernel<1><<<nblk, 256, 0, stream>>>(logits, T, E, k, idx, w, blk_mask);
+  else if (R <= 2)
+    topk_kernel<2><<<nblk, 256, 0, stream>>>(logits, T, E, k, idx, w, blk_mask);
+  else if (R <= 4)
+    topk_kernel<4><<<nblk, 256, 0, stream>>>(logits, T, E, k, idx, w, blk_mask);
+  else if (R <= 8)
+    topk_kernel<8><<<nblk, 256, 0, stream>>>(logits, T, E, k, idx, w, blk_mask);
+  else if (R <= 16)
+    topk_kernel<16><<<nblk, 256, 0, stream>>>(logits, T, E, k, idx, w, blk_mask);
+  else
+    topk_kernel<32><<<nblk, 256, 0, stream>>>(logits, T, E, k, idx, w, blk_mask);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ scan --
+// Exclusive scan of one int per thread over a 1024-thread block.
+__device__ __forceinline__ int block_excl_scan_1024(int v, int *warp_tot, int &total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += n;
+  }
+  if (lane == 31) warp_tot[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int wv = warp_tot[lane];
+    int wi = wv;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, wi, off);
+      if (lane >= off) wi += n;
+    }
+    warp_tot[lane] = wi - wv;   // exclusive prefix of warp totals
+    if (lane == 31) warp_tot[32] = wi;
+  }
+  __syncthreads();
+  const int excl = incl - v + warp_tot[warp];
+  total = warp_tot[32];
+  __syncthreads();
+  return excl;
+}
+
+__global__ void __launch_bounds__(1024) scan_kernel(const uint32_t *__restrict__ blk_mask,
+                                                    int nblk, int T, int E, int k,
+                                                    int32_t *__restrict__ counts,
+                                                    int32_t *__restrict__ offsets,
+                                                    int32_t *__restrict__ blk_base,
+                                                    int4 *__restrict__ blocks,
+                                                    int32_t *__restrict__ n_blocks) {
+  __shared__ int part[1024];
+  __shared__ int warp_tot[33];
+  __shared__ int cnt_s[1024];
+  const int tid = threadIdx.x;
+  const int P = max(1, 1024 / E);     // parts of the block range per expert
+  const int e = tid % E;
+  const int pi = tid / E;
+  const bool active = tid < P * E;
+  const int b0 = active ? static_cast<int>((static_cast<long long>(nblk) * pi) / P) : 0;
+  const int b1 = active ? static_cast<int>((static_cast<long long>(nblk) * (pi + 1)) / P) : 0;
+  // 1. histogram: rows of expert e in my range of routing blocks
+  int s = 0;
+  for (int b = b0; b < b1; ++b) s += __popc(blk_mask[static_cast<size_t>(b) * E + e]);
+  part[tid] = s;
+  __syncthreads();
+  // 2. exclusive scan over the parts of each expert
+  if (tid < E) {
+    int run = 0;
+    for (int pp = 0; pp < P; ++pp) {
+      const int v = part[pp * E + tid];
+      part[pp * E + tid] = run;
+      run += v;
+    }
+    cnt_s[tid] = run;
+    counts[tid] = run;
+  }
+  __syncthreads();
+  // 3. per-block bases inside each expert segment
+  if (active) {
+    int run = part[tid];
+    for (int b = b0; b < b1; ++b) {
+      blk_base[static_cast<size_t>(b) * E + e] = run;
+      run += __popc(blk_mask[static_cast<size_t>(b) * E + e]);
+    }
+  }
+  // 4. exclusive scan of the counts -> segment offsets
+  int total = 0;
+  const int c = (tid < E) ? cnt_s[tid] : 0;
+  const int off = block_excl_scan_1024(c, warp_tot, total);
+  if (tid < E) offsets[tid] = off;
+  if (tid == 0) offsets[E] = total;   // = T * k
+  // 5. block map: ceil(count / kBlockRowsMax) blocks per expert, then the
+  //    shared expert's T rows at grouped row T*k.
+  const int nb = (c + kBlockRowsMax - 1) / kBlockRowsMax;
+  int nb_total = 0;
+  const int bstart = block_excl_scan_1024(nb, warp_tot, nb_total);
+  if (tid < E) {
+    for (int i = 0; i < nb; ++i) {
+      const int r0 = i * kBlockRowsMax;
+      blocks[bstart + i] = make_int4(tid, off + r0, min(kBlockRowsMax, c - r0), 0);
+    }
+  }
+  const int nb_sh = (T + kBlockRowsMax - 1) / kBlockRowsMax;
+  for (int i = tid; i < nb_sh; i += blockDim.x) {
+    const int r0 = i * kBlockRowsMax;
+    blocks[nb_total + i] = make_int4(E, T * k + r0, min(kBlockRowsMax, T - r0), 0);
+  }
+  if (tid == 0) *n_blocks = nb_total + nb_sh;
+}
+
+cudaError_t launch_scan(const uint32_t *blk_mask, int nblk, int T, int E, int k,
+                        int32_t *counts, int32_t *offsets, int32_t *blk_base, int4 *blocks,
+                        int32_t *n_blocks, cudaStream_t stream) {
+  scan_kernel<<<1, 1024, 0, stream>>>(blk_mask, nblk, T, E, k, counts, offsets, blk_base, blocks,
+                                      n_blocks);
+  return cudaGetLastError();
+}
+
+// --------------------------------------------------------------- scatter --
+__global__ void scatter_kernel(const int32_t *__restrict__ idx, const uint32_t *__restrict__ blk_mask,
+                               const int32_t *__restrict__ blk_base,
+                               const int32_t *__restrict__ offsets, int T, int E, int k,
+                               int32_t *__restrict__ sorted_rows,
+                               int32_t *__restrict__ pos_of_assign) {
+  const int tl = threadIdx.x / k;
+  const int j = threadIdx.x - tl * k;
+  const int b = blockIdx.x;
+  const int t = b * kRouteBlockTokens + tl;
+  if (tl >= kRouteBlockTokens || t >= T) return;
+  const int a = t * k + j;
+  const int e = idx[a];
+  const uint32_t m = blk_mask[static_cast<size_t>(b) * E + e];
+  const int rank = __popc(m & ((1u << tl) - 1u));
+  const int p = offsets[e] + blk_base[static_cast<size_t>(b) * E + e] + rank;
+  pos_of_assign[a] = p;
+  sorted_rows[p] = t;
+}
+
+cudaError_t launch_scatter(const int32_t *idx, const uint32_t *blk_mask, const int32_t *blk_base,
+                           const int32_t *offsets, int T, int E, int k, int32_t *sorted_rows,
+                           int32_t *pos_of_assign, cudaStream_t stream) {
+  const int nblk = (T + kRouteBlockTokens - 1) / kRouteBlockTokens;
+  scatter_kernel<<<nblk, kRouteBlockTokens * k, 0, stream>>>(idx, blk_mask, blk_base, offsets, T, E,
+                                                             k, sorted_rows, pos_of_assign);
+  return cudaGetLastError();
+}
+
+// --------------------------------------------------------------- combine --
+// y[t] = sum_j w[t,j] * o[pos(t,j)] + sigmoid(x[t] . w_sg) * o[T*k + t], fp32
+// accumulation in fixed slot order (section "Reduce intermediate and state
+// traffic": the output projection combined with its routing score and the
+// shared-expert result).  No atomics: each output element is written once.
+__global__ void __launch_bounds__(256) combine_kernel(const __nv_bfloat16 *__restrict__ x,
+                                                      const __nv_bfloat16 *__restrict__ wsg,
+                                                      const __nv_bfloat16 *__restrict__ o,
+                                                      const int32_t *__restrict__ pos,
+                                                      const float *__restrict__ w, int T, int H,
+                                                      int k, __nv_bfloat16 *__restrict__ y) {
+  __shared__ float red[8];
+  __shared__ int pos_s[32];
+  __shared__ float w_s[32];
+  const int t = blockIdx.x;
+  const int nchunk = H / 8;
+  if (threadIdx.x < k) {
+    pos_s[threadIdx.x] = pos[static_cast<size_t>(t) * k + threadIdx.x];
+    w_s[threadIdx.x] = w[static_cast<size_t>(t) * k + threadIdx.x];
+  }
+  // shared-expert gate: sigmoid(x[t] . w_sg)
+  const uint4 *x4 = reinterpret_cast<const uint4 *>(x + static_cast<size_t>(t) * H);
+  const uint4 *g4 = reinterpret_cast<const uint4 *>(wsg);
+  float d = 0.0f;
+  for (int c = threadIdx.x; c < nchunk; c += blockDim.x) {
+    const uint4 xv = x4[c], gv = __ldg(g4 + c);
+    const uint32_t xa[4] = {xv.x, xv.y, xv.z, xv.w}, ga[4] = {gv.x, gv.y, gv.z, gv.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      d = fmaf(bf16_lo(xa[i]), bf16_lo(ga[i]), d);
+      d = fmaf(bf16_hi(xa[i]), bf16_hi(ga[i]), d);
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = d;
+  __syncthreads();
+  float dot = 0.0f;
+  for (int i = 0; i < static_cast<int>(blockDim.x >> 5); ++i) dot += red[i];
+  const float gate = sigmoid_f(dot);
+
+  const size_t shared_row = static_cast<size_t>(T) * k + t;
+  for (int c = threadIdx.x; c < nchunk; c += blockDim.x) {
+    float acc[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+    for (int j = 0; j < k; ++j) {
+      const uint4 ov = *reinterpret_cast<const uint4 *>(o + static_cast<size_t>(pos_s[j]) * H + c * 8);
+      const float wj = w_s[j];
+      const uint32_t oa[4] = {ov.x, ov.y, ov.z, ov.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        acc[2 * i] = fmaf(wj, bf16_lo(oa[i]), acc[2 * i]);
+        acc[2 * i + 1] = fmaf(wj, bf16_hi(oa[i]), acc[2 * i + 1]);
+      }
+    }
+    const uint4 sv = *reinterpret_cast<const uint4 *>(o + shared_row * H + c * 8);
+    const uint32_t sa[4] = {sv.x, sv.y, sv.z, sv.w};
+    uint4 out;
+    uint32_t *oo = reinterpret_cast<uint32_t *>(&out);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float lo = fmaf(gate, bf16_lo(sa[i]), acc[2 * i]);
+      const float hi = fmaf(gate, bf16_hi(sa[i]), acc[2 * i + 1]);
+      oo[i] = pack_bf16x2(lo, hi);
+    }
+    *reinterpret_cast<uint4 *>(y + static_cast<size_t>(t) * H + c * 8) = out;
+  }
+}
+
+cudaError_t launch_combine(const void *x, const void *sh_gate_w, const void *o,
+                           const int32_t *pos, const float *w, int T, int H, int k, void *y,
+                           cudaStream_t stream) {
+  combine_kernel<<<T, 256, 0, stream>>>(
+      reinterpret_cast<const __nv_bfloat16 *>(x), reinterpret_cast<const __nv_bfloat16 *>(sh_gate_w),
+      reinterpret_cast<const __nv_bfloat16 *>(o), pos, w, T, H, k,
+      reinterpret_cast<__nv_bfloat16 *>(y));
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,105 @@
+"""Batch-1 decode GEMV path (bf16 and int4) against the fp64 oracle, which
+selects experts from the decode router's own fp32 logits."""
+import numpy as np
+import pytest
+import torch
+
+import moe_synth
+from gpu_helpers import assert_layer_close, host_layer, logits_bound, make_ctx
+from oracle import moe_oracle as orc
+
+pytestmark = pytest.mark.gpu
+
+
+def _check_decode(ctx, w, x, layer=0, int4=False):
+    y = ctx.forward_decode(layer, x)
+    r = ctx.decode_routing()
+    torch.cuda.synchronize()
+    lg = r["logits"].cpu().numpy()[None, :]
+    x_np = x.float().cpu().numpy()
+    wr = w["router_w"].float().cpu().numpy()
+    b = None if w.get("router_b") is None else w["router_b"].cpu().numpy()
+    ref_l = orc.router_logits(x_np, wr, b)
+    assert np.all(np.abs(lg - ref_l) <= logits_bound(x_np, wr, ref_l, b))
+    o = orc.route(lg, ctx.top_k)
+    np.testing.assert_array_equal(r["topk_idx"].cpu().numpy(), o["topk_idx"][0])
+    assert np.abs(r["topk_w"].cpu().numpy() - o["topk_w"][0]).max() <= 4e-6
+    ref = orc.moe_layer(x_np, host_layer(w), ctx.top_k, logits=lg)
+    return y, assert_layer_close(y.float().cpu().numpy(), ref, int4=int4, what="decode")
+
+
+def test_decode_tiny():
+    wl = moe_synth.Workload("d", moe_synth.TINY, T=1, seed=11)
+    ctx, (w,) = make_ctx(wl, max_chunk_rows=16)
+    _check_decode(ctx, w, moe_synth.make_x(wl, device="cuda"))
+
+
+@pytest.fixture(scope="module")
+def decode_bf16():
+    wl = moe_synth.DECODE_BF16
+    ctx, layers = make_ctx(wl, n_layers=2, max_chunk_rows=16, seed_layers=[0, 39])
+    return wl, ctx, layers
+
+
+@pytest.mark.parametrize("slot,src", [(0, 0), (1, 39)])
+def test_decode_qwen_bf16(decode_bf16, slot, src):
+    wl, ctx, layers = decode_bf16
+    x = moe_synth.make_x(wl, layer=src, device="cuda")
+    _check_decode(ctx, layers[slot], x, layer=slot)
+
+
+def test_decode_deterministic_and_graph_replay(decode_bf16):
+    wl, ctx, layers = decode_bf16
+    xs = [moe_synth.make_x(wl, layer=l, device="cuda") for l in (0, 39)]
+    ys = [torch.empty_like(x) for x in xs]
+    for i in range(2):
+        ctx.forward_decode(i, xs[i], ys[i])
+    eager = [y.clone() for y in ys]
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            for i in range(2):
+                ctx.forward_decode(i, xs[i], ys[i], stream=s)
+    for y in ys:
+        y.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    for a, b in zip(eager, ys):
+        assert torch.equal(a, b)
+
+
+def test_decode_matches_prefill_one_token(decode_bf16):
+    wl, ctx, layers = decode_bf16
+    x = moe_synth.make_x(wl, layer=0, device="cuda")
+    yd = ctx.forward_decode(0, x)
+    yp = ctx.forward_prefill(0, x)
+    torch.cuda.synchronize()
+    ref = yp.double().cpu().numpy()
+    err = np.abs(yd.double().cpu().numpy() - ref).max()
+    assert err <= 1e-2 * np.abs(ref).max()
+
+
+def test_decode_host_buffers_match_device_path(decode_bf16):
+    wl, ctx, layers = decode_bf16
+    x = moe_synth.make_x(wl, layer=0, device="cuda")
+    yd = ctx.forward_decode(0, x)
+    x_h = x.cpu().pin_memory()
+    y_h = torch.empty_like(x_h).pin_memory()
+    ctx.forward_decode_host(0, x_h, y_h)
+    torch.cuda.synchronize()
+    assert torch.equal(y_h, yd.cpu())
+
+
+def test_decode_int4_qwen():
+    wl = moe_synth.DECODE_INT4
+    ctx, (w,) = make_ctx(wl, max_chunk_rows=16)
+    x = moe_synth.make_x(wl, device="cuda")
+    _check_decode(ctx, w, x, int4=True)
+
+
+def test_decode_int4_tiny():
+    wl = moe_synth.Workload("d4", moe_synth.TINY, T=1, wfmt=moe_synth.WFMT_INT4, seed=12)
+    ctx, (w,) = make_ctx(wl, max_chunk_rows=16)
+    _check_decode(ctx, w, moe_synth.make_x(wl, device="cuda"), int4=True)

@@ -1,0 +1,135 @@
+"""GPU prefill path (router, routing, tcgen05 grouped gate/up+SwiGLU and down
+GEMMs, combine) against the fp64 oracle, which selects experts from the
+GPU's fp32 router logits."""
+import numpy as np
+import pytest
+import torch
+
+import moe_synth
+from gpu_helpers import assert_layer_close, check_routing, host_layer, make_ctx
+from oracle import moe_oracle as orc
+
+pytestmark = pytest.mark.gpu
+
+
+def _wl(shape, T, bias=None, seed=0):
+    return moe_synth.Workload("t", shape, T=T, bias_std=bias, seed=seed)
+
+
+def _oracle_y(ctx, w, x, tokens=None):
+    lg = ctx.route(0, x)["logits"].cpu().numpy()
+    return orc.moe_layer(x.float().cpu().numpy(), host_layer(w), ctx.top_k, logits=lg,
+                         tokens=tokens)
+
+
+def test_prefill_tiny_full():
+    wl = moe_synth.TINY_LAYER
+    ctx, (w,) = make_ctx(wl, max_chunk_rows=64)
+    x = moe_synth.make_x(wl, device="cuda")
+    y = ctx.forward_prefill(0, x)
+    torch.cuda.synchronize()
+    assert_layer_close(y.float().cpu().numpy(), _oracle_y(ctx, w, x), what="tiny T=16")
+
+
+@pytest.mark.parametrize("T", [1, 17, 1000])
+def test_prefill_tiny_shapes_many_tiles(T):
+    # E=16, k=2: at T=1000 each expert gets ~125 rows on average and the
+    # biased ones several 256-row blocks; T=17 leaves a ragged tail.
+    wl = _wl(moe_synth.TINY, T, bias=1.5, seed=T + 1)
+    ctx, (w,) = make_ctx(wl, max_chunk_rows=1024)
+    x = moe_synth.make_x(wl, device="cuda")
+    y = ctx.forward_prefill(0, x)
+    torch.cuda.synchronize()
+    assert_layer_close(y.float().cpu().numpy(), _oracle_y(ctx, w, x), what=f"tiny T={T}")
+
+
+def test_prefill_qwen_ragged_full():
+    wl = _wl(moe_synth.QWEN, 300, bias=1.5, seed=7)
+    ctx, (w,) = make_ctx(wl)
+    x = moe_synth.make_x(wl, device="cuda")
+    y = ctx.forward_prefill(0, x)
+    torch.cuda.synchronize()
+    assert_layer_close(y.float().cpu().numpy(), _oracle_y(ctx, w, x), what="qwen T=300")
+
+
+@pytest.fixture(scope="module")
+def prefill_4096():
+    wl = moe_synth.PREFILL_BF16
+    ctx, (w,) = make_ctx(wl)
+    x = moe_synth.make_x(wl, device="cuda")
+    y = ctx.forward_prefill(0, x)
+    torch.cuda.synchronize()
+    return ctx, w, x, y
+
+
+def test_prefill_4096_sampled_tokens(prefill_4096):
+    """The benchmarked workload at full size: routing checked in full, the layer
+    output on sampled tokens (first, last and 62 random ones)."""
+    ctx, w, x, y = prefill_4096
+    check_routing(ctx, w, x)
+    rng = np.random.default_rng(0)
+    tokens = np.unique(np.concatenate([[0, 4095], rng.choice(4096, 62, replace=False)]))
+    ref = _oracle_y(ctx, w, x, tokens=tokens)
+    assert_layer_close(y[tokens].float().cpu().numpy(), ref, what="qwen T=4096 sampled")
+
+
+def test_prefill_4096_deterministic(prefill_4096):
+    ctx, w, x, y = prefill_4096
+    y2 = ctx.forward_prefill(0, x)
+    torch.cuda.synchronize()
+    assert torch.equal(y, y2)
+    assert ctx.check_device() == 0
+
+
+def test_prefill_chunking_does_not_change_output():
+    """T=8192 run as two 4096-row chunks equals one 8192-row chunk, bit for
+    bit (section 'Bound temporary memory with prompt chunking')."""
+    wl = _wl(moe_synth.QWEN, 8192, bias=1.5, seed=8192)
+    ctx4, (w,) = make_ctx(wl, max_chunk_rows=4096)
+    ctx8 = make_ctx(wl, max_chunk_rows=8192)[0]
+    ctx8.load_weights(0, w)
+    x = moe_synth.make_x(wl, device="cuda")
+    y4 = ctx4.forward_prefill(0, x)
+    y8 = ctx8.forward_prefill(0, x)
+    torch.cuda.synchronize()
+    assert torch.equal(y4, y8)
+    tokens = np.array([0, 4095, 4096, 8191])
+    lg = torch.cat([ctx4.route(0, x[:4096])["logits"], ctx4.route(0, x[4096:])["logits"]])
+    ref = orc.moe_layer(x.float().cpu().numpy(), host_layer(w), 8, logits=lg.cpu().numpy(),
+                        tokens=tokens)
+    assert_layer_close(y4[tokens].float().cpu().numpy(), ref, what="chunked")
+
+
+def test_prefill_all_tokens_one_expert():
+    wl = _wl(moe_synth.QWEN, 600, seed=5)
+    ctx, (w,) = make_ctx(wl)
+    b = torch.zeros(256, device="cuda")
+    b[7] = 100.0
+    w["router_b"] = b
+    ctx.load_weights(0, w)
+    x = moe_synth.make_x(wl, device="cuda")
+    y = ctx.forward_prefill(0, x)
+    torch.cuda.synchronize()
+    tokens = np.arange(0, 600, 7)
+    assert_layer_close(y[tokens].float().cpu().numpy(), _oracle_y(ctx, w, x, tokens=tokens),
+                       what="one hot expert")
+
+
+def test_prefill_zero_tokens_is_noop():
+    wl = moe_synth.TINY_LAYER
+    ctx, _ = make_ctx(wl, max_chunk_rows=64)
+    x = torch.empty((0, wl.shape.hidden), dtype=torch.bfloat16, device="cuda")
+    y = ctx.forward_prefill(0, x)
+    assert y.numel() == 0 and ctx.launch_count == 0
+
+
+def test_prefill_host_buffers_match_device_path():
+    wl = _wl(moe_synth.QWEN, 640, bias=1.5, seed=9)
+    ctx, (w,) = make_ctx(wl, max_chunk_rows=256)      # three chunks through the staging path
+    x = moe_synth.make_x(wl, device="cuda")
+    y_dev = ctx.forward_prefill(0, x)
+    x_h = x.cpu().pin_memory()
+    y_h = torch.empty_like(x_h).pin_memory()
+    ctx.forward_prefill_host(0, x_h, y_h)
+    torch.cuda.synchronize()
+    assert torch.equal(y_h, y_dev.cpu())
