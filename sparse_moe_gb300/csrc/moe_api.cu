@@ -88,14 +88,14 @@ EncodeTiledFn encode_fn() {
 }
 
 // 2-D bf16 matrix [outer, inner] (inner contiguous), 128-byte swizzled boxes
-// of {box_inner, box_outer} elements.
-bool encode_bf16_2d(CUtensorMap *m, const void *ptr, uint64_t inner, uint64_t outer,
-                    uint32_t box_inner, uint32_t box_outer) {
+// of {64, box_rows} elements: the K-major weight tiles of the grouped GEMMs.
+bool encode_weight_map(CUtensorMap *m, const void *ptr, uint64_t inner, uint64_t outer,
+                       uint32_t box_rows) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   const cuuint64_t dims[2] = {inner, outer};
   const cuuint64_t strides[1] = {inner * 2};
-  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t box[2] = {64, box_rows};
   const cuuint32_t es[2] = {1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -118,6 +118,7 @@ const char *kKernelNames[K_COUNT] = {
 struct LayerSlot {
   bool loaded = false;
   moe_weights w{};
+  // TMA descriptors of the weight (A) operands, encoded at load time
   CUtensorMap map_router, map_gu, map_gu_sh, map_dn, map_dn_sh;
 };
 
@@ -128,7 +129,6 @@ struct moe_ctx {
   char *ws = nullptr;
   size_t ws_bytes = 0;
   WsLayout L{};
-  CUtensorMap map_h;
   std::vector<LayerSlot> layers;
   std::string last_error;
   int64_t launches = 0;
@@ -174,6 +174,13 @@ moe_status check_config(const moe_config *c) {
   if (c->max_chunk_rows < 1 || c->max_chunk_rows > 65536) return MOE_ERR_INVALID_ARG;
   if (c->wfmt != MOE_W_BF16 && c->wfmt != MOE_W_INT4_SYM_G64) return MOE_ERR_INVALID_ARG;
   const size_t imax = std::max(c->inter, c->shared_inter);
+  // the GEMM producers address operand rows with 32-bit element offsets
+  const size_t lim = size_t(1) << 31;
+  const size_t R = static_cast<size_t>(c->max_chunk_rows) * (c->top_k + 1);
+  if (static_cast<size_t>(c->n_experts) * 2 * c->inter * c->hidden >= lim ||
+      static_cast<size_t>(c->n_experts) * c->hidden * c->inter >= lim ||
+      R * imax >= lim || static_cast<size_t>(c->max_chunk_rows) * c->hidden >= lim)
+    return MOE_ERR_UNSUPPORTED;
   if ((c->top_k + 1) * imax * 4 > 200 * 1024 || c->hidden * 4 > 200 * 1024)
     return MOE_ERR_UNSUPPORTED;   // decode staging must fit in shared memory
   return MOE_OK;
@@ -237,11 +244,12 @@ moe_status enqueue_route(moe_ctx *ctx, const LayerSlot &ls, const void *x, int T
                          int32_t *sorted_rows, int32_t *pos, cudaStream_t s) {
   const moe_config &c = ctx->cfg;
   const WsLayout &L = ctx->L;
-  CUtensorMap map_x_direct;
-  if (!encode_bf16_2d(&map_x_direct, x, c.hidden, T, 64, 16))
-    return fail(ctx, MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed for x (T=%d)", T);
   GemmParams gp{};
   gp.mode = MODE_ROUTER;
+  gp.a_routed = gp.a_shared = ls.w.router_w;
+  gp.lda_routed = gp.lda_shared = c.hidden;
+  gp.b = x;
+  gp.ldb = c.hidden;
   gp.block_rows = router_block_rows(ctx, T);
   gp.n_blocks_host = (T + gp.block_rows - 1) / gp.block_rows;
   gp.T = T;
@@ -259,7 +267,7 @@ moe_status enqueue_route(moe_ctx *ctx, const LayerSlot &ls, const void *x, int T
   moe_status st;
   {
     ProfScope ps(ctx, K_ROUTER_GEMM, s);
-    st = launched(ctx, launch_tc_gemm(ls.map_router, ls.map_router, map_x_direct, gp,
+    st = launched(ctx, launch_tc_gemm(ls.map_router, ls.map_router, gp, CONV_NONE,
                                       std::min(ctx->num_sms, tiles), s),
                   "router gemm launch");
   }
@@ -302,9 +310,6 @@ moe_status enqueue_prefill_chunk(moe_ctx *ctx, const LayerSlot &ls, const void *
                                 ctx->at<int32_t>(L.counts), ctx->at<int32_t>(L.offsets), sorted,
                                 pos, s);
   if (st) return st;
-  CUtensorMap map_x_gather;
-  if (!encode_bf16_2d(&map_x_gather, x, c.hidden, T, 64, 1))
-    return fail(ctx, MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed for x gather (T=%d)", T);
   GemmParams gp{};
   gp.blocks = ctx->at<int4>(L.blocks);
   gp.n_blocks_dev = ctx->at<int32_t>(L.nblocks);
@@ -319,23 +324,35 @@ moe_status enqueue_prefill_chunk(moe_ctx *ctx, const LayerSlot &ls, const void *
   gp.status = ctx->status();
   // gate/up + SwiGLU -> h
   gp.mode = MODE_GATEUP;
+  gp.a_routed = ls.w.gate_up;
+  gp.a_shared = ls.w.sh_gate_up;
+  gp.lda_routed = gp.lda_shared = c.hidden;
+  gp.b = x;
+  gp.ldb = c.hidden;
   gp.m_tiles = L.Imax / 64;
   gp.out = ctx->at<void>(L.h);
   gp.out_ld = L.Imax;
   {
     ProfScope ps(ctx, K_GATEUP_GEMM, s);
-    st = launched(ctx, launch_tc_gemm(ls.map_gu, ls.map_gu_sh, map_x_gather, gp, ctx->num_sms, s),
+    st = launched(ctx, launch_tc_gemm(ls.map_gu, ls.map_gu_sh, gp, CONV_NONE, ctx->num_sms, s),
                   "gate/up gemm launch");
   }
   if (st) return st;
   // down -> o
   gp.mode = MODE_DOWN;
+  gp.a_routed = ls.w.down;
+  gp.a_shared = ls.w.sh_down;
+  gp.lda_routed = c.inter;
+  gp.lda_shared = c.shared_inter;
+  gp.b = ctx->at<void>(L.h);
+  gp.ldb = L.Imax;
   gp.m_tiles = (c.hidden + 127) / 128;
   gp.out = ctx->at<void>(L.o);
   gp.out_ld = c.hidden;
   {
     ProfScope ps(ctx, K_DOWN_GEMM, s);
-    st = launched(ctx, launch_tc_gemm(ls.map_dn, ls.map_dn_sh, ctx->map_h, gp, ctx->num_sms, s),
+    st = launched(ctx,
+                  launch_tc_gemm(ls.map_dn, ls.map_dn_sh, gp, CONV_BF16_TO_F16, ctx->num_sms, s),
                   "down gemm launch");
   }
   if (st) return st;
@@ -456,10 +473,6 @@ moe_status moe_ctx_create(const moe_config *cfg, int device, void *workspace, si
   ctx->ws_bytes = ws_bytes;
   ctx->L = L;
   ctx->layers.resize(cfg->n_layers);
-  if (!encode_bf16_2d(&ctx->map_h, ctx->ws + L.h, L.Imax, L.R, 64, 16)) {
-    delete ctx;
-    return MOE_ERR_CUDA;
-  }
   if ((e = gemm_configure()) != cudaSuccess ||
       (e = decode_configure(std::max(cfg->hidden, (cfg->top_k + 1) * L.Imax))) != cudaSuccess ||
       (e = cudaMemset(ctx->ws + L.status, 0, 256)) != cudaSuccess ||
@@ -503,14 +516,14 @@ moe_status moe_load_weights(moe_ctx *ctx, int layer, const moe_weights *w) {
   LayerSlot &ls = ctx->layers[layer];
   ls.loaded = false;
   ls.w = *w;
-  bool ok = encode_bf16_2d(&ls.map_router, w->router_w, c.hidden, c.n_experts, 64, 128);
+  bool ok = encode_weight_map(&ls.map_router, w->router_w, c.hidden, c.n_experts, 128);
   if (!int4) {
-    ok = ok && encode_bf16_2d(&ls.map_gu, w->gate_up, c.hidden,
-                              static_cast<uint64_t>(c.n_experts) * 2 * c.inter, 64, 64);
-    ok = ok && encode_bf16_2d(&ls.map_gu_sh, w->sh_gate_up, c.hidden, 2 * c.shared_inter, 64, 64);
-    ok = ok && encode_bf16_2d(&ls.map_dn, w->down, c.inter,
-                              static_cast<uint64_t>(c.n_experts) * c.hidden, 64, 128);
-    ok = ok && encode_bf16_2d(&ls.map_dn_sh, w->sh_down, c.shared_inter, c.hidden, 64, 128);
+    ok = ok && encode_weight_map(&ls.map_gu, w->gate_up, c.hidden,
+                                 static_cast<uint64_t>(c.n_experts) * 2 * c.inter, 64);
+    ok = ok && encode_weight_map(&ls.map_gu_sh, w->sh_gate_up, c.hidden, 2 * c.shared_inter, 64);
+    ok = ok && encode_weight_map(&ls.map_dn, w->down, c.inter,
+                                 static_cast<uint64_t>(c.n_experts) * c.hidden, 128);
+    ok = ok && encode_weight_map(&ls.map_dn_sh, w->sh_down, c.shared_inter, c.hidden, 128);
   }
   if (!ok) return fail(ctx, MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed for layer %d", layer);
   ls.loaded = true;

@@ -5,6 +5,7 @@
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 namespace moe {
@@ -17,17 +18,16 @@ enum : int {
   DEV_TIMEOUT_MMA = 0x102,
   DEV_TIMEOUT_EPILOGUE = 0x103,
   DEV_TIMEOUT_DRAIN = 0x104,
+  DEV_TIMEOUT_CONVERTER = 0x105,
 };
 
-// A wait that has not completed within this many nanoseconds gives up.  Every
-// correct wait in these kernels completes in microseconds.
-constexpr unsigned long long kWaitLimitNs = 1000ull * 1000ull * 1000ull;  // 1 s
+// A wait that has not completed within this many SM clock cycles gives up
+// (about 1 s at the 2.07 GHz maximum clock, longer at lower clocks).  Every
+// correct wait in these kernels completes in microseconds.  The SM-local cycle
+// counter is used because reading it costs a few cycles.
+constexpr long long kWaitLimitCycles = 2000000000ll;
 
-__device__ __forceinline__ unsigned long long globaltimer_ns() {
-  unsigned long long t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
+__device__ __forceinline__ long long cycles_now() { return clock64(); }
 
 // ------------------------------------------------------------------ bf16 --
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
@@ -36,6 +36,10 @@ __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t *>(&p);
+}
+
+__device__ __forceinline__ float2 half2_to_float2(uint32_t v) {
+  return __half22float2(*reinterpret_cast<const __half2 *>(&v));
 }
 
 __device__ __forceinline__ float silu_f(float z) { return z / (1.0f + __expf(-z)); }
@@ -76,18 +80,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Waits for the phase of parity `parity` to complete.  Gives up (returns
-// false) when `abort_flag` is raised by another role or when kWaitLimitNs
-// elapses; in the latter case it raises the flag and records `code` in the
+// false) when `abort_flag` is raised by another role or when kWaitLimitCycles
+// cycles elapse; in the latter case it raises the flag and records `code` in the
 // device status word.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
                                                   volatile int *abort_flag, int *status,
                                                   int code) {
   if (mbar_try_wait(bar, parity)) return true;
-  const unsigned long long t0 = globaltimer_ns();
+  const long long t0 = cycles_now();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+    if (cycles_now() - t0 > kWaitLimitCycles) {
       *abort_flag = 1;
       atomicExch(status, code);
       return false;
@@ -114,6 +118,12 @@ __device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap *map
       " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar)
       : "memory");
+}
+
+// Fire-and-forget prefetch of `bytes` (multiple of 16, 16-byte aligned) into
+// L2 through the bulk-copy unit; nothing waits for it.
+__device__ __forceinline__ void prefetch_l2_bulk(const void *src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
@@ -197,6 +207,13 @@ __device__ __forceinline__ uint32_t idesc_bf16_f32(uint32_t M, uint32_t N) {
          | (1u << 7)          // A format: bf16
          | (1u << 10)         // B format: bf16
          | ((N >> 3) << 17)   // N / 8
+         | ((M >> 4) << 24);  // M / 16
+}
+
+// Instruction descriptor, kind::f16: fp16 A and B (both K-major), fp32 D.
+__device__ __forceinline__ uint32_t idesc_f16_f32(uint32_t M, uint32_t N) {
+  return (1u << 4)            // D format: f32
+         | ((N >> 3) << 17)   // N / 8   (A, B format 0 = f16)
          | ((M >> 4) << 24);  // M / 16
 }
 

@@ -15,9 +15,17 @@ constexpr int kBlockRowsMax = 256;
 constexpr int kRouteBlockTokens = 32;
 
 enum GemmMode : int { MODE_ROUTER = 0, MODE_GATEUP = 1, MODE_DOWN = 2 };
+// In-shared-memory conversion of the weight (A) tile before the MMA.
+enum GemmConv : int { CONV_NONE = 0, CONV_BF16_TO_F16 = 1 };
 
 struct GemmParams {
   int mode;
+  const void *a_routed;      // weights (A, K-major bf16): router / gate_up / down
+  const void *a_shared;      // shared-expert weights for the same role (or = a_routed)
+  int lda_routed;            // elements per A row
+  int lda_shared;
+  const void *b;             // B rows (K-major): x (router, gate/up) or h (down)
+  int ldb;                   // elements per B row
   const int4 *blocks;        // grouped modes: {expert (E = shared), row_start, n_rows, 0}
   const int *n_blocks_dev;   // grouped modes: block count in device memory
   int n_blocks_host;         // router: token blocks
@@ -31,7 +39,7 @@ struct GemmParams {
   int k_routed;              // reduction length (router, gate/up: H)
   int shared_row0;           // first grouped row of the shared expert (T*k)
   const int *sorted_rows;    // token of each grouped row
-  void *out;                 // router: fp32 [T,E]; gate/up: bf16 h [R,ld]; down: bf16 o [R,H]
+  void *out;                 // router: fp32 [T,E]; gate/up: fp16 h [R,ld]; down: fp16 o [R,H]
   int out_ld;                // elements per output row
   const float *bias;         // router bias or null
   int *status;               // device status word
@@ -39,8 +47,7 @@ struct GemmParams {
 
 cudaError_t gemm_configure();
 cudaError_t launch_tc_gemm(const CUtensorMap &a_routed, const CUtensorMap &a_shared,
-                           const CUtensorMap &b, const GemmParams &p, int grid,
-                           cudaStream_t stream);
+                           const GemmParams &p, int conv, int grid, cudaStream_t stream);
 
 // Routing: top-k + masks, block scan + block map, stable scatter.
 cudaError_t launch_topk(const float *logits, int T, int E, int k, int32_t *idx, float *w,

@@ -206,12 +206,12 @@ cudaError_t launch_scatter(const int32_t *idx, const uint32_t *blk_mask, const i
 
 // --------------------------------------------------------------- combine --
 // y[t] = sum_j w[t,j] * o[pos(t,j)] + sigmoid(x[t] . w_sg) * o[T*k + t], fp32
-// accumulation in fixed slot order (section "Reduce intermediate and state
+// accumulation in fixed slot order (o holds the per-expert outputs in fp16) (section "Reduce intermediate and state
 // traffic": the output projection combined with its routing score and the
 // shared-expert result).  No atomics: each output element is written once.
 __global__ void __launch_bounds__(256) combine_kernel(const __nv_bfloat16 *__restrict__ x,
                                                       const __nv_bfloat16 *__restrict__ wsg,
-                                                      const __nv_bfloat16 *__restrict__ o,
+                                                      const __half *__restrict__ o,
                                                       const int32_t *__restrict__ pos,
                                                       const float *__restrict__ w, int T, int H,
                                                       int k, __nv_bfloat16 *__restrict__ y) {
@@ -256,8 +256,9 @@ __global__ void __launch_bounds__(256) combine_kernel(const __nv_bfloat16 *__res
       const uint32_t oa[4] = {ov.x, ov.y, ov.z, ov.w};
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        acc[2 * i] = fmaf(wj, bf16_lo(oa[i]), acc[2 * i]);
-        acc[2 * i + 1] = fmaf(wj, bf16_hi(oa[i]), acc[2 * i + 1]);
+        const float2 f = half2_to_float2(oa[i]);
+        acc[2 * i] = fmaf(wj, f.x, acc[2 * i]);
+        acc[2 * i + 1] = fmaf(wj, f.y, acc[2 * i + 1]);
       }
     }
     const uint4 sv = *reinterpret_cast<const uint4 *>(o + shared_row * H + c * 8);
@@ -266,8 +267,9 @@ __global__ void __launch_bounds__(256) combine_kernel(const __nv_bfloat16 *__res
     uint32_t *oo = reinterpret_cast<uint32_t *>(&out);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const float lo = fmaf(gate, bf16_lo(sa[i]), acc[2 * i]);
-      const float hi = fmaf(gate, bf16_hi(sa[i]), acc[2 * i + 1]);
+      const float2 f = half2_to_float2(sa[i]);
+      const float lo = fmaf(gate, f.x, acc[2 * i]);
+      const float hi = fmaf(gate, f.y, acc[2 * i + 1]);
       oo[i] = pack_bf16x2(lo, hi);
     }
     *reinterpret_cast<uint4 *>(y + static_cast<size_t>(t) * H + c * 8) = out;
@@ -279,7 +281,7 @@ cudaError_t launch_combine(const void *x, const void *sh_gate_w, const void *o,
                            cudaStream_t stream) {
   combine_kernel<<<T, 256, 0, stream>>>(
       reinterpret_cast<const __nv_bfloat16 *>(x), reinterpret_cast<const __nv_bfloat16 *>(sh_gate_w),
-      reinterpret_cast<const __nv_bfloat16 *>(o), pos, w, T, H, k,
+      reinterpret_cast<const __half *>(o), pos, w, T, H, k,
       reinterpret_cast<__nv_bfloat16 *>(y));
   return cudaGetLastError();
 }
