@@ -126,6 +126,7 @@ struct moe_ctx {
   moe_config cfg{};
   int device = 0;
   int num_sms = 0;
+  int gemm_grid = 0;   // CTAs of the persistent grouped-GEMM grid (whole pairs)
   char *ws = nullptr;
   size_t ws_bytes = 0;
   WsLayout L{};
@@ -231,11 +232,13 @@ moe_status launched(moe_ctx *ctx, cudaError_t e, const char *what) {
   return MOE_OK;
 }
 
+// Token rows per router tile: enough tiles for every CTA pair, at least 32.
 int router_block_rows(const moe_ctx *ctx, int T) {
-  const int mt = (ctx->cfg.n_experts + 127) / 128;
-  int br = (T * mt + ctx->num_sms - 1) / ctx->num_sms;
-  br = (br + 15) & ~15;
-  return std::min(kBlockRowsMax, std::max(16, br));
+  const int mt = (ctx->cfg.n_experts + gemm_pair_rows() - 1) / gemm_pair_rows();
+  const int pairs = std::max(1, ctx->num_sms / 2);
+  int br = (T * mt + pairs - 1) / pairs;
+  br = (br + 31) & ~31;
+  return std::min(kBlockRowsMax, std::max(32, br));
 }
 
 // Router GEMM, top-k, histogram/scan/block map, scatter for T <= Tc tokens.
@@ -253,7 +256,7 @@ moe_status enqueue_route(moe_ctx *ctx, const LayerSlot &ls, const void *x, int T
   gp.block_rows = router_block_rows(ctx, T);
   gp.n_blocks_host = (T + gp.block_rows - 1) / gp.block_rows;
   gp.T = T;
-  gp.m_tiles = (c.n_experts + 127) / 128;
+  gp.m_tiles = (c.n_experts + gemm_pair_rows() - 1) / gemm_pair_rows();
   gp.n_experts = c.n_experts;
   gp.hidden = c.hidden;
   gp.inter_routed = c.inter;
@@ -268,7 +271,7 @@ moe_status enqueue_route(moe_ctx *ctx, const LayerSlot &ls, const void *x, int T
   {
     ProfScope ps(ctx, K_ROUTER_GEMM, s);
     st = launched(ctx, launch_tc_gemm(ls.map_router, ls.map_router, gp, CONV_NONE,
-                                      std::min(ctx->num_sms, tiles), s),
+                                      std::min(ctx->gemm_grid, 2 * tiles), s),
                   "router gemm launch");
   }
   if (st) return st;
@@ -324,17 +327,17 @@ moe_status enqueue_prefill_chunk(moe_ctx *ctx, const LayerSlot &ls, const void *
   gp.status = ctx->status();
   // gate/up + SwiGLU -> h
   gp.mode = MODE_GATEUP;
+  gp.m_tiles = (L.Imax + gemm_pair_rows() / 2 - 1) / (gemm_pair_rows() / 2);   // 128 SwiGLU outputs per pair
   gp.a_routed = ls.w.gate_up;
   gp.a_shared = ls.w.sh_gate_up;
   gp.lda_routed = gp.lda_shared = c.hidden;
   gp.b = x;
   gp.ldb = c.hidden;
-  gp.m_tiles = L.Imax / 64;
   gp.out = ctx->at<void>(L.h);
   gp.out_ld = L.Imax;
   {
     ProfScope ps(ctx, K_GATEUP_GEMM, s);
-    st = launched(ctx, launch_tc_gemm(ls.map_gu, ls.map_gu_sh, gp, CONV_NONE, ctx->num_sms, s),
+    st = launched(ctx, launch_tc_gemm(ls.map_gu, ls.map_gu_sh, gp, CONV_NONE, ctx->gemm_grid, s),
                   "gate/up gemm launch");
   }
   if (st) return st;
@@ -346,13 +349,13 @@ moe_status enqueue_prefill_chunk(moe_ctx *ctx, const LayerSlot &ls, const void *
   gp.lda_shared = c.shared_inter;
   gp.b = ctx->at<void>(L.h);
   gp.ldb = L.Imax;
-  gp.m_tiles = (c.hidden + 127) / 128;
+  gp.m_tiles = (c.hidden + gemm_pair_rows() - 1) / gemm_pair_rows();
   gp.out = ctx->at<void>(L.o);
   gp.out_ld = c.hidden;
   {
     ProfScope ps(ctx, K_DOWN_GEMM, s);
     st = launched(ctx,
-                  launch_tc_gemm(ls.map_dn, ls.map_dn_sh, gp, CONV_BF16_TO_F16, ctx->num_sms, s),
+                  launch_tc_gemm(ls.map_dn, ls.map_dn_sh, gp, CONV_BF16_TO_F16, ctx->gemm_grid, s),
                   "down gemm launch");
   }
   if (st) return st;
@@ -473,7 +476,12 @@ moe_status moe_ctx_create(const moe_config *cfg, int device, void *workspace, si
   ctx->ws_bytes = ws_bytes;
   ctx->L = L;
   ctx->layers.resize(cfg->n_layers);
-  if ((e = gemm_configure()) != cudaSuccess ||
+  if ((e = gemm_configure()) != cudaSuccess) {
+    delete ctx;
+    return MOE_ERR_CUDA;
+  }
+  ctx->gemm_grid = gemm_max_grid(sms);
+  if (
       (e = decode_configure(std::max(cfg->hidden, (cfg->top_k + 1) * L.Imax))) != cudaSuccess ||
       (e = cudaMemset(ctx->ws + L.status, 0, 256)) != cudaSuccess ||
       (e = cudaMemset(ctx->ws + L.dec_counter, 0, 16)) != cudaSuccess ||

@@ -46,6 +46,10 @@ struct GemmParams {
 };
 
 cudaError_t gemm_configure();
+// Weight rows one GEMM tile covers (a CTA pair, 128 rows per CTA).
+int gemm_pair_rows();
+// Largest persistent grid (CTAs, whole pairs) whose clusters are co-resident.
+int gemm_max_grid(int num_sms);
 cudaError_t launch_tc_gemm(const CUtensorMap &a_routed, const CUtensorMap &a_shared,
                            const GemmParams &p, int conv, int grid, cudaStream_t stream);
 

@@ -12,31 +12,41 @@
 // to each expert, fp32 accumulation, tile shape from the expert's row count.)
 //
 // Design (GB300-first, not the page's Metal design):
-//  * weights sit on the MMA M side (128 rows per tile) and the routed token
-//    rows on the N side (N = row count rounded up to 16, at most 256), so an
-//    expert with 5 rows runs a 128x16 MMA rather than padding to 128 rows;
-//  * the gate/up tile stacks 64 gate rows over the 64 matching up rows, so one
-//    MMA produces both halves of 64 SwiGLU outputs; the epilogue pairs them
-//    through a small shared-memory exchange;
+//  * a pair of CTAs on two SMs (a cluster of 2) runs one 256 x N tile with
+//    tcgen05.mma.cta_group::2: weights on the MMA M side (each CTA stages its
+//    own 128 rows) and the routed token rows on the N side (each CTA stages
+//    half of them), so every SM moves 32 KB per 64-deep k-step for 2 x 128 x
+//    N x 64 multiply-adds.  N is the block's row count rounded up to 32 (at
+//    most 256): an expert with 5 rows runs a 256x32 MMA, not a padded 256-row
+//    token tile;
+//  * the gate/up tile stacks, in each CTA, 64 gate rows over the 64 matching
+//    up rows, so one MMA produces both halves of 64 SwiGLU outputs per CTA;
+//    the epilogue pairs them through a small shared-memory exchange;
 //  * the weight tile (A) of each k-step is one or two TMA boxes (128-byte
 //    swizzle) prefetched into L2 a tile ahead; the token rows (B) are
 //    gathered by a group of warps per pipeline stage with 16-byte cp.async
 //    copies written straight into the same 128-byte-swizzled K-major layout,
 //    so no permuted copy of x is ever written.  (Measured on GB300: TMA
 //    gather4 moves 512 bytes per request and tops out near 7-18 bytes/clock
-//    per SM; the load/store path scales with the number of issuing warps.)
-//  * one persistent CTA per SM walks the device-built tile list; one thread
-//    of the MMA warp issues tcgen05.mma, four epilogue warps drain the
-//    double-buffered TMEM accumulator while the next tile computes, and
-//    transpose each 32x16 piece through shared memory so global stores are
-//    16-byte vectors;
+//    per SM; one warp of cp.async sustains about 7 bytes/clock; a single-SM
+//    128 x 256 tile would need 96 bytes/clock, the pair needs 64.)
+//  * the pair's CTAs walk the device-built tile list persistently; one thread
+//    of the leader issues the MMAs once both CTAs' stage is ready (a finisher
+//    warp per stage and CTA forwards readiness, the peer's with a
+//    cluster-scope release-arrive, so successive stages signal in parallel);
+//    four epilogue warps
+//    per CTA drain their half of the double-buffered TMEM accumulator while
+//    the next tile computes, and transpose each 32x16 piece through shared
+//    memory so global stores are 16-byte vectors;
 //  * the down projection runs with fp16 operands: the gate/up epilogue stores
-//    h in fp16 (11 significant bits instead of bf16's 8), and four converter
-//    warps turn each bf16 weight tile into fp16 in place in shared memory
+//    h in fp16 (11 significant bits instead of bf16's 8), and the stage
+//    finisher warps turn each bf16 weight tile into fp16 in place in shared memory
 //    before the MMA reads it (exact for |w| >= 2^-17; the swizzled layout is
 //    unchanged since both types are 2 bytes).  o is stored in fp16.
 #include "moe_common.cuh"
 #include "moe_internal.h"
+
+#include <algorithm>
 
 namespace moe {
 
@@ -54,41 +64,38 @@ __device__ unsigned long long g_moe_trace[3][1024][16];
 #define MOE_TADD(slot)
 #endif
 
-constexpr int BM = 128;                 // MMA M
+constexpr int BM = 128;                 // A rows per CTA (MMA M = 256 per pair)
+constexpr int PAIR_M = 2 * BM;
 constexpr int BK = 64;                  // K per pipeline stage (128-byte rows)
 constexpr int BN_MAX = kBlockRowsMax;   // max MMA N (tokens per tile)
-constexpr int STAGES = 4;
+constexpr int BN_HALF = BN_MAX / 2;     // token rows staged per CTA
+constexpr int STAGES = 6;
 constexpr int A_BYTES = BM * BK * 2;            // 16 KB
-constexpr int B_BYTES = BN_MAX * BK * 2;        // 32 KB
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // 48 KB
+constexpr int B_BYTES = BN_HALF * BK * 2;       // 16 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // 32 KB
 constexpr int ACC_COLS = 256;                   // one accumulator buffer
 constexpr int TMEM_COLS = 512;                  // two buffers
-// Warp roles.  The weight tile (A, contiguous rows) is loaded by TMA, issued
-// by one thread; the token rows (B, gathered) by 16-byte cp.async from a
-// group of warps per pipeline stage.  Measured on GB300: one warp sustains
-// only about 7 bytes/clock of cp.async traffic, TMA about 30 bytes/clock per
-// SM, and an M128 x N256 tile needs 32 (A) + 64 (B) bytes/clock.
-constexpr int B_WARPS_PER_STAGE = 4;
+// Warp roles (identical in both CTAs of a pair).
+constexpr int B_WARPS_PER_STAGE = 2;
 constexpr int TMA_WARP = 0;                                  // warp 0
-constexpr int B_WARP0 = 1;                                   // warps 1..16
+constexpr int B_WARP0 = 1;                                   // warps 1..12
 constexpr int B_WARPS = STAGES * B_WARPS_PER_STAGE;
-constexpr int MMA_WARP = B_WARP0 + B_WARPS;                  // warp 17
-constexpr int EPI_WARP0 = MMA_WARP + 1;                      // warps 18..21
-constexpr int CONV_WARP0 = EPI_WARP0 + 4;                    // warps 22..25 (converting modes)
-constexpr int BASE_THREADS = CONV_WARP0 * 32;
-constexpr int CONV_THREADS = 128;
+constexpr int MMA_WARP = B_WARP0 + B_WARPS;                  // warp 13
+constexpr int EPI_WARP0 = MMA_WARP + 1;                      // warps 14..17
+constexpr int FIN_WARP0 = EPI_WARP0 + 4;                     // warps 18..23: one per stage
+constexpr int NUM_THREADS = (FIN_WARP0 + STAGES) * 32;
 constexpr int XCH_FLOATS = 2 * 2 * 2 * 8 * 32;  // [buf][pair][dir][8 cols][32 lanes]
 constexpr int EPI_STAGE_BYTES = 4 * 16 * 64;    // per epilogue warp: 16 rows x 64 bytes
 // Per B producer warp: offsets of the token rows it copies (every
-// B_WARPS_PER_STAGE-th group of four rows of up to 256).
-constexpr int kRowTab = 4 * ((BN_MAX / 4 + B_WARPS_PER_STAGE - 1) / B_WARPS_PER_STAGE);
+// B_WARPS_PER_STAGE-th group of four rows of up to 128).
+constexpr int kRowTab = 4 * ((BN_HALF / 4 + B_WARPS_PER_STAGE - 1) / B_WARPS_PER_STAGE);
 
 struct SmemTail {
-  uint64_t full[STAGES];
-  uint64_t conv[STAGES];
-  uint64_t empty[STAGES];
-  uint64_t tmem_full[2];
-  uint64_t tmem_empty[2];
+  uint64_t full[STAGES];        // local: TMA (A) + this CTA's B warps
+  uint64_t ready[STAGES];       // leader: both CTAs' stage finishers
+  uint64_t empty[STAGES];       // local: arrives from the leader's commit
+  uint64_t tmem_full[2];        // local: arrives from the leader's commit
+  uint64_t tmem_empty[2];       // leader: 4 + 4 epilogue warps
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
@@ -105,11 +112,13 @@ struct Tile {
   int nk;
   int m;
   int shared;
-  int a_row, a_row2;   // first A row (a_row2: first up row for gate/up)
-  int a_valid_rows;    // A rows at or beyond this (tile-relative) read as zero
+  int a_row, a_row2;   // this CTA's first A row (a_row2: first up row for gate/up)
+  int a_valid_rows;    // this CTA's A rows at or beyond this index are not outputs
+  int out_base;        // first output row (gate/up: i, down: n, router: e) of this CTA
+  int out_limit;       // number of valid output rows of the operator (I/Is, H, E)
 };
 
-__device__ __forceinline__ Tile decode_tile(const GemmParams &p, int tile) {
+__device__ __forceinline__ Tile decode_tile(const GemmParams &p, int tile, int rank) {
   Tile t;
   const int b = tile / p.m_tiles;
   t.m = tile - b * p.m_tiles;
@@ -125,27 +134,31 @@ __device__ __forceinline__ Tile decode_tile(const GemmParams &p, int tile) {
     t.nrows = blk.z;
     t.shared = (e == p.n_experts);
   }
-  t.nmma = max(16, (t.nrows + 15) & ~15);
+  t.nmma = max(32, (t.nrows + 31) & ~31);
   t.valid = t.nrows > 0;
   if (p.mode == MODE_ROUTER) {
     t.nk = p.k_routed / BK;
-    t.a_row = t.m * BM;
+    t.out_base = t.m * PAIR_M + rank * BM;
+    t.out_limit = p.n_experts;
+    t.a_row = t.out_base;
     t.a_row2 = 0;
-    t.a_valid_rows = p.n_experts - t.m * BM;
   } else if (p.mode == MODE_GATEUP) {
     const int inter = t.shared ? p.inter_shared : p.inter_routed;
     t.nk = p.k_routed / BK;
-    t.valid = t.valid && (t.m * 64 < inter);
+    t.valid = t.valid && (t.m * 128 < inter);
+    t.out_base = t.m * 128 + rank * 64;     // 64 SwiGLU outputs per CTA
+    t.out_limit = inter;
     const int base = t.shared ? 0 : e * 2 * p.inter_routed;
-    t.a_row = base + t.m * 64;
-    t.a_row2 = base + inter + t.m * 64;
-    t.a_valid_rows = BM;
+    t.a_row = base + t.out_base;
+    t.a_row2 = base + inter + t.out_base;
   } else {  // MODE_DOWN
     t.nk = (t.shared ? p.inter_shared : p.inter_routed) / BK;
-    t.a_row = (t.shared ? 0 : e * p.hidden) + t.m * BM;
+    t.out_base = t.m * PAIR_M + rank * BM;
+    t.out_limit = p.hidden;
+    t.a_row = (t.shared ? 0 : e * p.hidden) + t.out_base;
     t.a_row2 = 0;
-    t.a_valid_rows = p.hidden - t.m * BM;
   }
+  t.a_valid_rows = t.out_limit - t.out_base;
   return t;
 }
 
@@ -173,11 +186,11 @@ __device__ __forceinline__ void cp_async_wait() {
 }
 
 // In-place bf16 -> fp16 conversion of one 128x64 A tile (1024 16-byte
-// chunks) by the 128 converter threads.
-__device__ __forceinline__ void convert_tile_bf16_to_f16(uint32_t tile_addr, int ctid) {
-#pragma unroll
-  for (int i = 0; i < (A_BYTES / 16) / CONV_THREADS; ++i) {
-    const uint32_t addr = tile_addr + (ctid + i * CONV_THREADS) * 16;
+// chunks) by one warp.
+__device__ __forceinline__ void convert_tile_bf16_to_f16(uint32_t tile_addr, int lane) {
+#pragma unroll 4
+  for (int i = 0; i < (A_BYTES / 16) / 32; ++i) {
+    const uint32_t addr = tile_addr + (lane + i * 32) * 16;
     uint32_t w0, w1, w2, w3;
     asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
                  : "=r"(w0), "=r"(w1), "=r"(w2), "=r"(w3)
@@ -209,9 +222,9 @@ __device__ __forceinline__ void warp_store_rows_f16(const uint8_t *stage, int ro
 }
 
 template <int CONV>
-__global__ void __launch_bounds__(BASE_THREADS + (CONV != CONV_NONE ? CONV_THREADS : 0), 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a_routed,
-                   const __grid_constant__ CUtensorMap map_a_shared, const GemmParams p) {
+                       const __grid_constant__ CUtensorMap map_a_shared, const GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
@@ -224,16 +237,18 @@ __global__ void __launch_bounds__(BASE_THREADS + (CONV != CONV_NONE ? CONV_THREA
   const int warp = threadIdx.x >> 5;
   const int lane = lane_id();
   const uint32_t smem_base = smem_u32(smem);
-
+  const int rank = static_cast<int>(cluster_ctarank());   // 0: leader, 1: peer
+  const int pair_id = blockIdx.x >> 1;
+  const int num_pairs = gridDim.x >> 1;
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(smem_u32(&tail->full[s]), 1 + B_WARPS_PER_STAGE);
-      mbar_init(smem_u32(&tail->conv[s]), CONV_THREADS / 32);
+      mbar_init(smem_u32(&tail->ready[s]), 2);
       mbar_init(smem_u32(&tail->empty[s]), 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(smem_u32(&tail->tmem_full[a]), 1);
-      mbar_init(smem_u32(&tail->tmem_empty[a]), 4);
+      mbar_init(smem_u32(&tail->tmem_empty[a]), 8);
     }
     mbar_init(smem_u32(&tail->drain), 1);
     tail->abort_flag = 0;
@@ -242,11 +257,12 @@ __global__ void __launch_bounds__(BASE_THREADS + (CONV != CONV_NONE ? CONV_THREA
     prefetch_tensormap(&map_a_shared);
   }
   if (warp == MMA_WARP) {
-    tmem_alloc(smem_u32(&tail->tmem_base), TMEM_COLS);
-    tmem_relinquish();
+    tmem_alloc_pair(smem_u32(&tail->tmem_base), TMEM_COLS);
+    tmem_relinquish_pair();
   }
   tc_fence_before();
   __syncthreads();
+  cluster_sync_all();   // both CTAs' barriers exist before any remote arrive
   tc_fence_after();
   const uint32_t tmem_base = tail->tmem_base;
   const int ntiles = num_tiles(p);
@@ -256,22 +272,25 @@ __global__ void __launch_bounds__(BASE_THREADS + (CONV != CONV_NONE ? CONV_THREA
 
   if (warp == TMA_WARP) {
     // ------------------------------------------------ weight tiles (TMA) --
-    // Lane 0 loads each k-step's 128 weight rows with TMA into the stage's A
-    // region (complete_tx on the stage's full barrier); all lanes prefetch the
-    // next tile's weight rows (all of K) into L2 first, since they stream from
-    // DRAM and one SM cannot keep enough requests in flight to cover its
-    // latency.
+    // Lane 0 loads each k-step's 128 weight rows of this CTA with TMA into
+    // the stage's A region (complete_tx on the local full barrier); all lanes
+    // prefetch the next tile's weight rows (all of K) into L2 first, since
+    // they stream from DRAM and one SM cannot keep enough requests in flight
+    // to cover its latency.
     const __nv_bfloat16 *a_routed = reinterpret_cast<const __nv_bfloat16 *>(p.a_routed);
     const __nv_bfloat16 *a_shared = reinterpret_cast<const __nv_bfloat16 *>(p.a_shared);
     auto prefetch_a = [&](int tile_id) {
       if (tile_id >= ntiles) return;
-      const Tile u = decode_tile(p, tile_id);
+      const Tile u = decode_tile(p, tile_id, rank);
       if (!u.valid) return;
       const __nv_bfloat16 *ab = u.shared ? a_shared : a_routed;
       const int ld = u.shared ? p.lda_shared : p.lda_routed;
       const uint32_t kbytes = static_cast<uint32_t>(u.nk * BK * 2);
-      for (int r = lane; r < BM && r < u.a_valid_rows; r += 32) {
-        const int row = (p.mode == MODE_GATEUP) ? ((r < 64) ? u.a_row + r : u.a_row2 + (r - 64))
+      const int half = (p.mode == MODE_GATEUP) ? 64 : BM;
+      for (int r = lane; r < BM; r += 32) {
+        const int rr = (r < half) ? r : r - half;
+        if (rr >= u.a_valid_rows) continue;
+        const int row = (p.mode == MODE_GATEUP) ? ((r < 64) ? u.a_row + rr : u.a_row2 + rr)
                                                 : u.a_row + r;
         prefetch_l2_bulk(ab + static_cast<size_t>(row) * ld, kbytes);
       }
@@ -282,10 +301,10 @@ __global__ void __launch_bounds__(BASE_THREADS + (CONV != CONV_NONE ? CONV_THREA
 #pragma unroll
     for (int s2 = 0; s2 < STAGES; ++s2) issued_parity[s2] = -1;
     int ok = 1;
-    if (blockIdx.x < ntiles) prefetch_a(blockIdx.x);
-    for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
-      const Tile t = decode_tile(p, tile);
-      prefetch_a(tile + gridDim.x);
+    if (pair_id < ntiles) prefetch_a(pair_id);
+    for (int tile = pair_id; tile < ntiles && ok; tile += num_pairs) {
+      const Tile t = decode_tile(p, tile, rank);
+      prefetch_a(tile + num_pairs);
       if (!t.valid) continue;
       if (lane == 0) {
         const CUtensorMap *amap = t.shared ? &map_a_shared : &map_a_routed;
@@ -329,10 +348,11 @@ __global__ void __launch_bounds__(BASE_THREADS + (CONV != CONV_NONE ? CONV_THREA
   } else if (warp >= B_WARP0 && warp < B_WARP0 + B_WARPS) {
     // ------------------------------------------------- token rows (cp.async) --
     // Warp group g owns pipeline stage g: for every k-step that lands in its
-    // stage it copies the B slice (nmma rows of 128 bytes), each warp of the
-    // group every B_WARPS_PER_STAGE-th group of four rows, waits for its own
-    // copies, fences them for the tensor core and arrives on the stage's full
-    // barrier.  Lane l copies 16-byte chunk l % 8 of rows 4 j + l / 8.
+    // stage it copies this CTA's half of the B slice (nmma / 2 rows of 128
+    // bytes), each warp of the group every B_WARPS_PER_STAGE-th group of four
+    // rows, waits for its own copies, fences them for the tensor core and
+    // arrives on the stage's full barrier.  Lane l copies 16-byte chunk l % 8
+    // of rows 4 j + l / 8.
     const int bw = warp - B_WARP0;
     const int g = bw / B_WARPS_PER_STAGE;
     const int gq = bw - g * B_WARPS_PER_STAGE;
@@ -346,28 +366,32 @@ __global__ void __launch_bounds__(BASE_THREADS + (CONV != CONV_NONE ? CONV_THREA
     const int btid = bw * 32 + lane;
     auto prefetch_b = [&](int tile_id) {
       if (tile_id >= ntiles) return;
-      const Tile u = decode_tile(p, tile_id);
+      const Tile u = decode_tile(p, tile_id, rank);
       if (!u.valid) return;
       const uint32_t kbytes = static_cast<uint32_t>(u.nk * BK * 2);
-      for (int rb = btid; rb < u.nrows; rb += B_WARPS * 32)
-        prefetch_l2_bulk(bsrc + static_cast<size_t>(b_row(p, u, rb)) * p.ldb, kbytes);
+      const int half = u.nmma / 2;
+      for (int rb = btid; rb < half; rb += B_WARPS * 32) {
+        const int r = rank * half + rb;
+        if (r < u.nrows) prefetch_l2_bulk(bsrc + static_cast<size_t>(b_row(p, u, r)) * p.ldb, kbytes);
+      }
     };
-    if (blockIdx.x < ntiles) prefetch_b(blockIdx.x);
+    if (pair_id < ntiles) prefetch_b(pair_id);
     int it = 0;   // k-step counter over all tiles of this CTA
     bool ok = true;
-    for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
-      const Tile t = decode_tile(p, tile);
-      prefetch_b(tile + gridDim.x);
+    for (int tile = pair_id; tile < ntiles && ok; tile += num_pairs) {
+      const Tile t = decode_tile(p, tile, rank);
+      prefetch_b(tile + num_pairs);
       if (!t.valid) continue;
       bool table_ready = false;
-      const int nquads = t.nmma / 4;
+      const int half = t.nmma / 2;
+      const int nquads = half / 4;
       for (int ks = 0; ks < t.nk; ++ks, ++it) {
         if ((it % STAGES) != g) continue;
         if (!table_ready) {
           __syncwarp();   // previous tile's table no longer read
           for (int e = lane; e < kRowTab; e += 32) {
             const int r = 4 * (gq + B_WARPS_PER_STAGE * (e >> 2)) + (e & 3);
-            rows_tab[e] = (r < t.nmma) ? b_row(p, t, r) * p.ldb : 0;
+            rows_tab[e] = (r < half) ? b_row(p, t, rank * half + r) * p.ldb : 0;
           }
           __syncwarp();
           table_ready = true;
@@ -414,106 +438,117 @@ __global__ void __launch_bounds__(BASE_THREADS + (CONV != CONV_NONE ? CONV_THREA
     }
     __syncwarp();
   } else if (warp == MMA_WARP) {
-    // --------------------------------------------------------- MMA issuer --
-    if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
-      int acc = 0;
-      uint32_t aphase = 0;
-      bool ok = true;
-      for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
-        const Tile t = decode_tile(p, tile);
-        if (!t.valid) continue;
-        {
-          MOE_T0();
-          const bool w_ok = mbar_wait_bounded(smem_u32(&tail->tmem_empty[acc]), aphase ^ 1,
-                                              abort_flag, p.status, DEV_TIMEOUT_MMA);
-          MOE_TADD(3);
-          if (!w_ok) {
-            ok = false;
-            break;
-          }
-        }
-        tc_fence_after();
-        const uint32_t d_tmem = tmem_base + acc * ACC_COLS;
-        const uint32_t idesc =
-            (CONV == CONV_BF16_TO_F16) ? idesc_f16_f32(BM, t.nmma) : idesc_bf16_f32(BM, t.nmma);
-        for (int ks = 0; ks < t.nk; ++ks) {
-          const uint32_t ready_bar =
-              (CONV != CONV_NONE) ? smem_u32(&tail->conv[stage]) : smem_u32(&tail->full[stage]);
-          MOE_T0();
-          const bool r_ok = mbar_wait_bounded(ready_bar, phase, abort_flag, p.status, DEV_TIMEOUT_MMA);
-          MOE_TADD(2);
-          if (!r_ok) {
-            ok = false;
-            break;
+    if (rank == 0) {
+      // ----------------------------------------------- MMA issuer (leader) --
+      if (lane == 0) {
+        int stage = 0;
+        uint32_t phase = 0;
+        int acc = 0;
+        uint32_t aphase = 0;
+        bool ok = true;
+        for (int tile = pair_id; tile < ntiles && ok; tile += num_pairs) {
+          const Tile t = decode_tile(p, tile, 0);
+          if (!t.valid) continue;
+          {
+            MOE_T0();
+            const bool w_ok = mbar_wait_bounded_cluster(smem_u32(&tail->tmem_empty[acc]), aphase ^ 1,
+                                                        abort_flag, p.status, DEV_TIMEOUT_MMA);
+            MOE_TADD(3);
+            if (!w_ok) {
+              ok = false;
+              break;
+            }
           }
           tc_fence_after();
+          const uint32_t d_tmem = tmem_base + acc * ACC_COLS;
+          const uint32_t idesc = (CONV == CONV_BF16_TO_F16) ? idesc_f16_f32(PAIR_M, t.nmma)
+                                                            : idesc_bf16_f32(PAIR_M, t.nmma);
+          for (int ks = 0; ks < t.nk; ++ks) {
+            MOE_T0();
+            const bool r_ok = mbar_wait_bounded_cluster(smem_u32(&tail->ready[stage]), phase,
+                                                        abort_flag, p.status, DEV_TIMEOUT_MMA);
+            MOE_TADD(2);
+            if (!r_ok) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
 #ifdef MOE_TRACE
-          const long long _ti = clock64();
+            const long long _ti = clock64();
 #endif
-          const uint32_t a_addr = smem_base + stage * STAGE_BYTES;
-          const uint64_t a_desc = smem_desc_sw128(a_addr);
-          const uint64_t b_desc = smem_desc_sw128(a_addr + A_BYTES);
+            const uint32_t a_addr = smem_base + stage * STAGE_BYTES;
+            const uint64_t a_desc = smem_desc_sw128(a_addr);
+            const uint64_t b_desc = smem_desc_sw128(a_addr + A_BYTES);
 #pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk)
-            tc_mma_bf16(d_tmem, a_desc + 2 * kk, b_desc + 2 * kk, idesc, (ks | kk) != 0);
-          tc_commit(smem_u32(&tail->empty[stage]));
+            for (int kk = 0; kk < BK / 16; ++kk)
+              tc_mma_pair(d_tmem, a_desc + 2 * kk, b_desc + 2 * kk, idesc, (ks | kk) != 0);
+            tc_commit_pair_mc(smem_u32(&tail->empty[stage]), 0x3);
 #ifdef MOE_TRACE
-          atomicAdd(&g_moe_trace[p.mode][blockIdx.x & 1023][1],
-                    static_cast<unsigned long long>(clock64() - _ti));
+            atomicAdd(&g_moe_trace[p.mode][blockIdx.x & 1023][1],
+                      static_cast<unsigned long long>(clock64() - _ti));
 #endif
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1;
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1;
+            }
+          }
+          if (!ok) break;
+          tc_commit_pair_mc(smem_u32(&tail->tmem_full[acc]), 0x3);
+          if (++acc == 2) {
+            acc = 0;
+            aphase ^= 1;
           }
         }
-        if (!ok) break;
-        tc_commit(smem_u32(&tail->tmem_full[acc]));
-        if (++acc == 2) {
-          acc = 0;
-          aphase ^= 1;
-        }
-      }
-      // All MMAs issued by this thread complete before TMEM is released.
-      tc_commit(smem_u32(&tail->drain));
-      const long long t0 = cycles_now();
-      while (!mbar_try_wait(smem_u32(&tail->drain), 0)) {
-        if (cycles_now() - t0 > kWaitLimitCycles) {
-          atomicExch(p.status, DEV_TIMEOUT_DRAIN);
-          break;
+        // All pair MMAs complete before TMEM is released or the peer exits.
+        tc_commit_pair_mc(smem_u32(&tail->drain), 0x1);
+        const long long t0 = cycles_now();
+        while (!mbar_try_wait(smem_u32(&tail->drain), 0)) {
+          if (cycles_now() - t0 > kWaitLimitCycles) {
+            atomicExch(p.status, DEV_TIMEOUT_DRAIN);
+            break;
+          }
         }
       }
     }
     __syncwarp();
-  } else if (warp >= CONV_WARP0) {
-    // ---------------------------------------------------------- converter --
-    if (CONV != CONV_NONE) {
-      const int ctid = threadIdx.x - CONV_WARP0 * 32;
-      int stage = 0;
-      uint32_t phase = 0;
-      bool ok = true;
-      for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
-        const Tile t = decode_tile(p, tile);
-        if (!t.valid) continue;
-        for (int ks = 0; ks < t.nk; ++ks) {
-          int got = 1;
-          if (lane == 0)
-            got = mbar_wait_bounded(smem_u32(&tail->full[stage]), phase, abort_flag, p.status,
-                                    DEV_TIMEOUT_CONVERTER);
-          got = __shfl_sync(0xffffffffu, got, 0);
-          if (!got) {
-            ok = false;
-            break;
-          }
-          convert_tile_bf16_to_f16(smem_base + stage * STAGE_BYTES, ctid);
+  } else if (warp >= FIN_WARP0) {
+    // --------------------------------------------------- stage finishers --
+    // Finisher warp f owns pipeline stage f: once this CTA's stage is full it
+    // (in the converting mode) turns the bf16 weight tile into fp16 in place,
+    // then tells the pair leader that this CTA's half of the stage is ready.
+    // One warp per stage keeps the cross-CTA signalling of successive stages
+    // overlapped.
+    const int f = warp - FIN_WARP0;
+    const uint32_t ready_bar = smem_u32(&tail->ready[f]);
+    const uint32_t ready_leader = mapa_shared(ready_bar, 0);
+    int it = 0;
+    bool ok = true;
+    for (int tile = pair_id; tile < ntiles && ok; tile += num_pairs) {
+      const Tile t = decode_tile(p, tile, rank);
+      if (!t.valid) continue;
+      for (int ks = 0; ks < t.nk; ++ks, ++it) {
+        if ((it % STAGES) != f) continue;
+        const uint32_t phase = static_cast<uint32_t>(it / STAGES) & 1u;
+        int got = 1;
+        if (lane == 0) {
+          MOE_T0();
+          got = mbar_wait_bounded(smem_u32(&tail->full[f]), phase, abort_flag, p.status,
+                                  DEV_TIMEOUT_CONVERTER);
+          MOE_TADD(14);
+        }
+        got = __shfl_sync(0xffffffffu, got, 0);
+        if (!got) {
+          ok = false;
+          break;
+        }
+        if (CONV == CONV_BF16_TO_F16) {
+          convert_tile_bf16_to_f16(smem_base + f * STAGE_BYTES, lane);
           fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(smem_u32(&tail->conv[stage]));
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1;
-          }
+        }
+        __syncwarp();
+        if (lane == 0) {
+          if (rank == 0) mbar_arrive(ready_bar);
+          else mbar_arrive_cluster(ready_leader);
         }
       }
     }
@@ -522,10 +557,11 @@ __global__ void __launch_bounds__(BASE_THREADS + (CONV != CONV_NONE ? CONV_THREA
     const int q = warp & 3;               // TMEM lane quarter this warp may access
     const int ew = warp - EPI_WARP0;      // 0..3
     uint8_t *my_stage = epi_stage + ew * (16 * 64);
+    const uint32_t tmem_empty0 = mapa_shared(smem_u32(&tail->tmem_empty[0]), 0);
     int acc = 0;
     uint32_t aphase = 0;
-    for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
-      const Tile t = decode_tile(p, tile);
+    for (int tile = pair_id; tile < ntiles; tile += num_pairs) {
+      const Tile t = decode_tile(p, tile, rank);
       if (!t.valid) continue;
       int got = 1;
       if (lane == 0) {
@@ -548,13 +584,15 @@ __global__ void __launch_bounds__(BASE_THREADS + (CONV != CONV_NONE ? CONV_THREA
 #endif
 
       if (p.mode == MODE_GATEUP) {
-        // Lanes 0..63 of the accumulator hold gate rows, 64..127 the matching
-        // up rows.  Warp quarter q<2 (gate) pairs with quarter q+2 (up); the
-        // gate warp finishes columns 0..7 of each 16-column chunk, the up warp
-        // columns 8..15.
+        // Lanes 0..63 of this CTA's accumulator hold gate rows, 64..127 the
+        // matching up rows.  Warp quarter q<2 (gate) pairs with quarter q+2
+        // (up); the gate warp finishes columns 0..7 of each 16-column chunk,
+        // the up warp columns 8..15.
         const bool is_gate = q < 2;
         const int pair = q & 1;
-        __half *hout = reinterpret_cast<__half *>(p.out) + t.m * 64 + pair * 32;
+        const int i0 = t.out_base + pair * 32;
+        const bool live = i0 < t.out_limit;        // whole 32-row group inside I
+        __half *hout = reinterpret_cast<__half *>(p.out) + i0;
         __half *sh = reinterpret_cast<__half *>(my_stage);
         int buf = 0;
         for (int c0 = 0; c0 < t.nmma; c0 += 16) {
@@ -575,13 +613,14 @@ __global__ void __launch_bounds__(BASE_THREADS + (CONV != CONV_NONE ? CONV_THREA
           }
           __syncwarp();
           const int col0 = c0 + (is_gate ? 0 : 8);
-          warp_store_rows_f16(my_stage, 8, t.nrows - col0,
-                              hout + static_cast<size_t>(t.row0 + col0) * p.out_ld, p.out_ld, lane);
+          if (live)
+            warp_store_rows_f16(my_stage, 8, t.nrows - col0,
+                                hout + static_cast<size_t>(t.row0 + col0) * p.out_ld, p.out_ld, lane);
           __syncwarp();
           buf ^= 1;
         }
       } else if (p.mode == MODE_DOWN) {
-        const int n0 = t.m * BM + q * 32;
+        const int n0 = t.out_base + q * 32;
         __half *oout = reinterpret_cast<__half *>(p.out) + n0;
         __half *sh = reinterpret_cast<__half *>(my_stage);
         const bool full_rows = n0 + 32 <= p.hidden;
@@ -605,7 +644,7 @@ __global__ void __launch_bounds__(BASE_THREADS + (CONV != CONV_NONE ? CONV_THREA
           }
         }
       } else {  // MODE_ROUTER: fp32 logits, 128 contiguous bytes per column
-        const int e = t.m * BM + q * 32 + lane;
+        const int e = t.out_base + q * 32 + lane;
         float *lout = reinterpret_cast<float *>(p.out);
         const float bias = (p.bias != nullptr && e < p.n_experts) ? __ldg(p.bias + e) : 0.0f;
         for (int c0 = 0; c0 < t.nmma; c0 += 16) {
@@ -628,7 +667,10 @@ __global__ void __launch_bounds__(BASE_THREADS + (CONV != CONV_NONE ? CONV_THREA
         atomicAdd(&g_moe_trace[p.mode][blockIdx.x & 1023][5],
                   static_cast<unsigned long long>(clock64() - _te));
 #endif
-      if (lane == 0) mbar_arrive(smem_u32(&tail->tmem_empty[acc]));
+      if (lane == 0) {
+        if (rank == 0) mbar_arrive(smem_u32(&tail->tmem_empty[acc]));
+        else mbar_arrive_cluster(tmem_empty0 + acc * 8);
+      }
       if (++acc == 2) {
         acc = 0;
         aphase ^= 1;
@@ -638,6 +680,7 @@ __global__ void __launch_bounds__(BASE_THREADS + (CONV != CONV_NONE ? CONV_THREA
 
   tc_fence_before();
   __syncthreads();
+  cluster_sync_all();   // the pair's MMAs and epilogues are done in both CTAs
   tc_fence_after();
 #ifdef MOE_TRACE
   if (threadIdx.x == 0) {
@@ -646,13 +689,9 @@ __global__ void __launch_bounds__(BASE_THREADS + (CONV != CONV_NONE ? CONV_THREA
     atomicAdd(&g_moe_trace[p.mode][blockIdx.x & 1023][7], 1ull);
   }
 #endif
-  if (warp == MMA_WARP) tmem_dealloc(tmem_base, TMEM_COLS);
+  if (warp == MMA_WARP) tmem_dealloc_pair(tmem_base, TMEM_COLS);
 }
 
-template <int CONV>
-static constexpr int gemm_threads() {
-  return BASE_THREADS + (CONV != CONV_NONE ? CONV_THREADS : 0);
-}
 
 cudaError_t gemm_configure() {
   cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<CONV_NONE>,
@@ -664,14 +703,40 @@ cudaError_t gemm_configure() {
                               static_cast<int>(kGemmSmemBytes));
 }
 
+int gemm_pair_rows() { return PAIR_M; }
+
+int gemm_max_grid(int num_sms) {
+  int grid = num_sms & ~1;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = kGemmSmemBytes;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int clusters = 0;
+  if (cudaOccupancyMaxActiveClusters(&clusters, tc_gemm_kernel<CONV_BF16_TO_F16>, &cfg) ==
+          cudaSuccess &&
+      clusters > 0)
+    grid = std::min(grid, 2 * clusters);
+  cudaGetLastError();
+  return grid > 2 ? grid : 2;
+}
+
 cudaError_t launch_tc_gemm(const CUtensorMap &a_routed, const CUtensorMap &a_shared,
                            const GemmParams &p, int conv, int grid, cudaStream_t stream) {
+  grid &= ~1;   // whole CTA pairs
+  if (grid < 2) grid = 2;
   if (conv == CONV_BF16_TO_F16)
     tc_gemm_kernel<CONV_BF16_TO_F16>
-        <<<grid, gemm_threads<CONV_BF16_TO_F16>(), kGemmSmemBytes, stream>>>(a_routed, a_shared, p);
+        <<<grid, NUM_THREADS, kGemmSmemBytes, stream>>>(a_routed, a_shared, p);
   else
     tc_gemm_kernel<CONV_NONE>
-        <<<grid, gemm_threads<CONV_NONE>(), kGemmSmemBytes, stream>>>(a_routed, a_shared, p);
+        <<<grid, NUM_THREADS, kGemmSmemBytes, stream>>>(a_routed, a_shared, p);
   return cudaGetLastError();
 }
 
