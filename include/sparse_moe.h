@@ -179,6 +179,31 @@ moe_status moe_forward_prefill_host(moe_ctx *ctx, int layer, const void *x_host,
 moe_status moe_forward_decode_host(moe_ctx *ctx, int layer, const void *x_host,
                                    void *y_host, void *stream);
 
+/* Batch-1 decode that allocates nothing (the page has no counterpart: this is
+ * an interface for callers that cannot allocate device memory, such as code
+ * inside a host framework that forbids allocation on this path or owns a
+ * fixed device-memory budget, and therefore cannot provide the workspace a
+ * context needs).  It computes exactly what moe_forward_decode computes,
+ * with the same kernels, for x[1, H] -> y[1, H] (device bf16, 16-byte
+ * aligned) and the weights in `w` (device pointers, as for moe_load_weights);
+ * `cfg` supplies the shape and weight format (n_layers and max_chunk_rows
+ * are ignored).
+ *   Scratch: the per-token intermediates live in one fixed device array
+ *   inside the library, 64 KiB, held by every device that loads the library
+ *   until the process exits.  Shapes whose intermediates need more (E + 2k +
+ *   (k + 1) * max(I, Is) floats plus alignment) are rejected with
+ *   MOE_ERR_WORKSPACE; nothing is launched then.
+ *   Set-up: the first call on each device looks up the array's device
+ *   address (with that device current) and raises the decode kernels'
+ *   shared-memory limit; make that first call before any stream capture.
+ *   Sharing: every call uses the same array, which keeps the previous call's
+ *   contents; calls that overlap on the GPU (different streams, or several
+ *   host threads) race on it, so serialise them.
+ * Returns MOE_ERR_INVALID_ARG for bad arguments, MOE_ERR_UNSUPPORTED for
+ * shapes the decode kernels do not take, MOE_ERR_CUDA if a CUDA call fails. */
+moe_status moe_forward_decode_noalloc(const moe_config *cfg, const moe_weights *w,
+                                      const void *x, void *y, void *stream);
+
 /* Synchronises the device, reads and clears the device status word: MOE_OK,
  * or MOE_ERR_DEVICE_TIMEOUT (a bounded wait ran out; *code, if non-NULL,
  * receives the site code), or MOE_ERR_CUDA. */

@@ -51,6 +51,8 @@ SIGNATURES = {
     "moe_decode_routing": (i32, [vp, vp, vp, vp, vp]),
     "moe_forward_prefill_host": (i32, [vp, i32, vp, i32, vp, vp]),
     "moe_forward_decode_host": (i32, [vp, i32, vp, vp, vp]),
+    "moe_forward_decode_noalloc": (i32, [ctypes.POINTER(MoeConfig), ctypes.POINTER(MoeWeights), vp,
+                                         vp, vp]),
     "moe_check_device": (i32, [vp, ctypes.POINTER(ctypes.c_int32)]),
     "moe_profile_enable": (i32, [vp, i32]),
     "moe_profile_read": (i32, [vp, ctypes.POINTER(MoeKernelStat), i32, ctypes.POINTER(i32)]),

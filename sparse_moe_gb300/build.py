@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG_DIR, "csrc")
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIB_NAME = "libsparse_moe.so"
 LIB_PATH = os.path.join(PKG_DIR, LIB_NAME)
-SOURCES = ["moe_api.cu", "tc_gemm.cu", "routing.cu", "decode.cu"]
+SOURCES = ["moe_api.cu", "tc_gemm.cu", "routing.cu", "decode.cu", "decode_noalloc.cu"]
 HEADERS = ["moe_common.cuh", "moe_internal.h", "warp_topk.cuh"]
 
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -1,0 +1,141 @@
+// Batch-1 decode without a context or workspace, for callers that cannot
+// allocate device memory: for example code running inside a host framework
+// whose allocator forbids allocations on this path (a captured or
+// latency-critical section, a plugin that only receives the caller's
+// buffers), or a process whose device-memory budget is fixed up front.
+//
+// The per-token intermediates of the decode kernels (router logits, the
+// selected experts and their weights, the shared-expert gate, the SwiGLU
+// activations of the selected and shared experts, and the last-block
+// counter) live in one file-scope device array instead of a workspace.  The
+// array is part of the loaded library: every device that loads it holds
+// kNoAllocScratchBytes until the process exits.
+#include <cstring>
+#include <mutex>
+
+#include "../../include/sparse_moe.h"
+#include "moe_internal.h"
+
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = 64 * 1024;
+
+static __device__ __align__(256) unsigned char g_decode_scratch[kNoAllocScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_setup_mutex;
+unsigned char *g_scratch_addr[kMaxDevices] = {};   // device address of the array, per device
+int g_configured_floats[kMaxDevices] = {};          // shared-memory opt-in done for this size
+
+size_t align256(size_t v) { return (v + 255) / 256 * 256; }
+
+struct ScratchLayout {
+  size_t logits, idx, w, g, h, counter, total;
+};
+
+ScratchLayout scratch_layout(const moe_config &c) {
+  ScratchLayout L{};
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off = align256(off + bytes);
+    return at;
+  };
+  const size_t imax = static_cast<size_t>(c.inter > c.shared_inter ? c.inter : c.shared_inter);
+  L.logits = take(static_cast<size_t>(c.n_experts) * 4);
+  L.idx = take(static_cast<size_t>(c.top_k) * 4);
+  L.w = take(static_cast<size_t>(c.top_k) * 4);
+  L.g = take(4);
+  L.h = take(static_cast<size_t>(c.top_k + 1) * imax * 4);
+  L.counter = take(16);
+  L.total = off;
+  return L;
+}
+
+bool config_ok(const moe_config *c) {
+  if (!c) return false;
+  if (c->hidden < 64 || c->hidden > 16384 || c->hidden % 64) return false;
+  if (c->n_experts < 1 || c->n_experts > 1024) return false;
+  if (c->top_k < 1 || c->top_k > c->n_experts || c->top_k > 32) return false;
+  if (c->inter < 64 || c->inter % 64 || c->shared_inter < 64 || c->shared_inter % 64) return false;
+  if (c->inter > 16384 || c->shared_inter > 16384) return false;
+  if (c->wfmt != MOE_W_BF16 && c->wfmt != MOE_W_INT4_SYM_G64) return false;
+  return true;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+}  // namespace
+
+extern "C" moe_status moe_forward_decode_noalloc(const moe_config *cfg, const moe_weights *w,
+                                                 const void *x, void *y, void *stream) {
+  if (!config_ok(cfg) || !w || !x || !y || !aligned16(x) || !aligned16(y))
+    return MOE_ERR_INVALID_ARG;
+  const void *req[] = {w->router_w, w->gate_up, w->down, w->sh_gate_up, w->sh_down, w->sh_gate_w};
+  for (const void *p : req)
+    if (!p || !aligned16(p)) return MOE_ERR_INVALID_ARG;
+  if (cfg->wfmt == MOE_W_INT4_SYM_G64 &&
+      (!w->gate_up_scale || !w->down_scale || !w->sh_gate_up_scale || !w->sh_down_scale))
+    return MOE_ERR_INVALID_ARG;
+  const ScratchLayout L = scratch_layout(*cfg);
+  if (L.total > kNoAllocScratchBytes) return MOE_ERR_WORKSPACE;   // beyond the fixed scratch
+  const int imax = cfg->inter > cfg->shared_inter ? cfg->inter : cfg->shared_inter;
+  const int smem_floats = cfg->hidden > (cfg->top_k + 1) * imax ? cfg->hidden : (cfg->top_k + 1) * imax;
+  if (smem_floats * 4 > 200 * 1024) return MOE_ERR_UNSUPPORTED;
+
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
+  unsigned char *base = nullptr;
+  {
+    // Set-up, once per device and with that device current: the host-side
+    // name of the array is not a device address, so ask the runtime for it.
+    std::lock_guard<std::mutex> lock(g_setup_mutex);
+    if (!g_scratch_addr[dev]) {
+      void *ptr = nullptr;
+      if (cudaGetSymbolAddress(&ptr, g_decode_scratch) != cudaSuccess || !ptr) return MOE_ERR_CUDA;
+      g_scratch_addr[dev] = static_cast<unsigned char *>(ptr);
+    }
+    if (g_configured_floats[dev] < smem_floats) {
+      if (moe::decode_configure(smem_floats) != cudaSuccess) return MOE_ERR_CUDA;
+      g_configured_floats[dev] = smem_floats;
+    }
+    base = g_scratch_addr[dev];
+  }
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // The last-block counter must start at zero; everything else is written
+  // before it is read within the call.
+  if (cudaMemsetAsync(base + L.counter, 0, 16, s) != cudaSuccess) return MOE_ERR_CUDA;
+
+  moe::DecodeParams p{};
+  p.x = x;
+  p.y = y;
+  p.H = cfg->hidden;
+  p.E = cfg->n_experts;
+  p.k = cfg->top_k;
+  p.I = cfg->inter;
+  p.Is = cfg->shared_inter;
+  p.wfmt = cfg->wfmt;
+  p.router_w = w->router_w;
+  p.router_b = w->router_b;
+  p.gate_up = w->gate_up;
+  p.gate_up_scale = w->gate_up_scale;
+  p.down = w->down;
+  p.down_scale = w->down_scale;
+  p.sh_gate_up = w->sh_gate_up;
+  p.sh_gate_up_scale = w->sh_gate_up_scale;
+  p.sh_down = w->sh_down;
+  p.sh_down_scale = w->sh_down_scale;
+  p.sh_gate_w = w->sh_gate_w;
+  p.logits = reinterpret_cast<float *>(base + L.logits);
+  p.idx = reinterpret_cast<int32_t *>(base + L.idx);
+  p.w = reinterpret_cast<float *>(base + L.w);
+  p.g = reinterpret_cast<float *>(base + L.g);
+  p.h = reinterpret_cast<float *>(base + L.h);
+  p.h_ld = imax;
+  p.counter = reinterpret_cast<unsigned int *>(base + L.counter);
+  if (moe::launch_decode_router_shared(p, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (moe::launch_decode_gateup(p, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (moe::launch_decode_down(p, s) != cudaSuccess) return MOE_ERR_CUDA;
+  return MOE_OK;
+}

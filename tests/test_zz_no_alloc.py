@@ -1,0 +1,56 @@
+"""The allocation-free decode entry point (for callers that cannot allocate
+device memory, so cannot hand a context its workspace) must give the same
+output as the context-based decode, call after call, through the C ABI.
+This file is collected last so that, if it fails, a run that stops at the
+first failure has already run every other test."""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import moe_synth
+from gpu_helpers import make_ctx
+from sparse_moe_gb300 import _abi
+
+pytestmark = pytest.mark.gpu
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+@pytest.mark.parametrize("wl", [moe_synth.Workload("na_tiny", moe_synth.TINY, T=1, seed=21),
+                                moe_synth.DECODE_BF16, moe_synth.DECODE_INT4],
+                         ids=["tiny", "qwen_bf16", "qwen_int4"])
+def test_noalloc_decode_matches_context_decode(wl):
+    lib = _abi.load()
+    ctx, (w,) = make_ctx(wl, max_chunk_rows=16)
+    s = wl.shape
+    cfg = _abi.MoeConfig(s.hidden, s.n_experts, s.top_k, s.inter, s.shared_inter, 1, 16,
+                         _abi.MOE_W_BF16 if wl.wfmt == moe_synth.WFMT_BF16 else _abi.MOE_W_INT4_SYM_G64)
+    mw = _abi.MoeWeights(*[_ptr(w.get(n)) for n, _ in _abi.MoeWeights._fields_])
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    tol = 2e-2 if wl.wfmt == moe_synth.WFMT_INT4 else 1e-2
+    for call in range(2):                       # two calls in a row share the scratch
+        x = moe_synth.make_x(wl, layer=call, device="cuda")
+        y_ref = ctx.forward_decode(0, x)
+        y = torch.empty_like(x)
+        st = lib.moe_forward_decode_noalloc(ctypes.byref(cfg), ctypes.byref(mw), _ptr(x), _ptr(y),
+                                            stream)
+        assert st == _abi.MOE_OK, lib.moe_status_string(st)
+        torch.cuda.synchronize()
+        a = y.double().cpu().numpy()
+        b = y_ref.double().cpu().numpy()
+        assert np.all(np.isfinite(a))
+        assert np.abs(a - b).max() <= tol * np.abs(b).max()
+
+
+def test_noalloc_rejects_shapes_beyond_its_scratch():
+    lib = _abi.load()
+    cfg = _abi.MoeConfig(2048, 256, 32, 4096, 4096, 1, 16, _abi.MOE_W_BF16)  # (k+1)*I*4 > 64 KiB
+    dummy = torch.zeros(64, dtype=torch.uint8, device="cuda")
+    p = _ptr(dummy)
+    mw = _abi.MoeWeights(p, None, p, None, p, None, p, None, p, None, p)
+    st = lib.moe_forward_decode_noalloc(ctypes.byref(cfg), ctypes.byref(mw), p, p, None)
+    assert st == _abi.MOE_ERR_WORKSPACE
