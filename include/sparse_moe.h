@@ -184,17 +184,17 @@ moe_status moe_forward_decode_host(moe_ctx *ctx, int layer, const void *x_host,
  * inside a host framework that forbids allocation on this path or owns a
  * fixed device-memory budget, and therefore cannot provide the workspace a
  * context needs).  It computes exactly what moe_forward_decode computes,
- * with the same kernels, for x[1, H] -> y[1, H] (device bf16, 16-byte
+ * with the same kernel, for x[1, H] -> y[1, H] (device bf16, 16-byte
  * aligned) and the weights in `w` (device pointers, as for moe_load_weights);
  * `cfg` supplies the shape and weight format (n_layers and max_chunk_rows
  * are ignored).
  *   Scratch: the per-token intermediates live in one fixed device array
  *   inside the library, 64 KiB, held by every device that loads the library
  *   until the process exits.  Shapes whose intermediates need more (E + 2k +
- *   (k + 1) * max(I, Is) floats plus alignment) are rejected with
+ *   (2k + 1) * max(I, Is) floats plus alignment) are rejected with
  *   MOE_ERR_WORKSPACE; nothing is launched then.
  *   Set-up: the first call on each device looks up the array's device
- *   address (with that device current) and raises the decode kernels'
+ *   address (with that device current) and raises the decode kernel's
  *   shared-memory limit; make that first call before any stream capture.
  *   Sharing: every call uses the same array, which keeps the previous call's
  *   contents; calls that overlap on the GPU (different streams, or several

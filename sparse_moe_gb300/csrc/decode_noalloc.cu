@@ -4,10 +4,10 @@
 // latency-critical section, a plugin that only receives the caller's
 // buffers), or a process whose device-memory budget is fixed up front.
 //
-// The per-token intermediates of the decode kernels (router logits, the
-// selected experts and their weights, the shared-expert gate, the SwiGLU
-// activations of the selected and shared experts, and the last-block
-// counter) live in one file-scope device array instead of a workspace.  The
+// The per-token intermediates of the decode kernel (router logits, the
+// selected experts and their weights, the shared-expert gate, the experts'
+// gate/up dot products, the shared expert's activations, and the grid-barrier
+// words) live in one file-scope device array instead of a workspace.  The
 // array is part of the loaded library: every device that loads it holds
 // kNoAllocScratchBytes until the process exits.
 #include <cstring>
@@ -25,12 +25,13 @@ static __device__ __align__(256) unsigned char g_decode_scratch[kNoAllocScratchB
 constexpr int kMaxDevices = 64;
 std::mutex g_setup_mutex;
 unsigned char *g_scratch_addr[kMaxDevices] = {};   // device address of the array, per device
+int g_grid[kMaxDevices] = {};                       // cooperative decode grid, per device
 int g_configured_floats[kMaxDevices] = {};          // shared-memory opt-in done for this size
 
 size_t align256(size_t v) { return (v + 255) / 256 * 256; }
 
 struct ScratchLayout {
-  size_t logits, idx, w, g, h, counter, total;
+  size_t logits, idx, w, g, h, counter, status, total;
 };
 
 ScratchLayout scratch_layout(const moe_config &c) {
@@ -46,8 +47,9 @@ ScratchLayout scratch_layout(const moe_config &c) {
   L.idx = take(static_cast<size_t>(c.top_k) * 4);
   L.w = take(static_cast<size_t>(c.top_k) * 4);
   L.g = take(4);
-  L.h = take(static_cast<size_t>(c.top_k + 1) * imax * 4);
+  L.h = take(moe::decode_h_floats(c.top_k, static_cast<int>(imax)) * 4);
   L.counter = take(16);
+  L.status = take(16);
   L.total = off;
   return L;
 }
@@ -80,12 +82,13 @@ extern "C" moe_status moe_forward_decode_noalloc(const moe_config *cfg, const mo
   const ScratchLayout L = scratch_layout(*cfg);
   if (L.total > kNoAllocScratchBytes) return MOE_ERR_WORKSPACE;   // beyond the fixed scratch
   const int imax = cfg->inter > cfg->shared_inter ? cfg->inter : cfg->shared_inter;
-  const int smem_floats = cfg->hidden > (cfg->top_k + 1) * imax ? cfg->hidden : (cfg->top_k + 1) * imax;
+  const int smem_floats = (cfg->top_k + 1) * imax;
   if (smem_floats * 4 > 200 * 1024) return MOE_ERR_UNSUPPORTED;
 
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
   unsigned char *base = nullptr;
+  int grid = 0;
   {
     // Set-up, once per device and with that device current: the host-side
     // name of the array is not a device address, so ask the runtime for it.
@@ -95,15 +98,22 @@ extern "C" moe_status moe_forward_decode_noalloc(const moe_config *cfg, const mo
       if (cudaGetSymbolAddress(&ptr, g_decode_scratch) != cudaSuccess || !ptr) return MOE_ERR_CUDA;
       g_scratch_addr[dev] = static_cast<unsigned char *>(ptr);
     }
+    if (!g_grid[dev]) {
+      int sms = 0;
+      if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
+        return MOE_ERR_CUDA;
+      g_grid[dev] = moe::decode_layer_grid(sms);
+    }
     if (g_configured_floats[dev] < smem_floats) {
       if (moe::decode_configure(smem_floats) != cudaSuccess) return MOE_ERR_CUDA;
       g_configured_floats[dev] = smem_floats;
     }
     base = g_scratch_addr[dev];
+    grid = g_grid[dev];
   }
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // The last-block counter must start at zero; everything else is written
+  // The grid-barrier words must start at zero; everything else is written
   // before it is read within the call.
   if (cudaMemsetAsync(base + L.counter, 0, 16, s) != cudaSuccess) return MOE_ERR_CUDA;
 
@@ -134,8 +144,7 @@ extern "C" moe_status moe_forward_decode_noalloc(const moe_config *cfg, const mo
   p.h = reinterpret_cast<float *>(base + L.h);
   p.h_ld = imax;
   p.counter = reinterpret_cast<unsigned int *>(base + L.counter);
-  if (moe::launch_decode_router_shared(p, s) != cudaSuccess) return MOE_ERR_CUDA;
-  if (moe::launch_decode_gateup(p, s) != cudaSuccess) return MOE_ERR_CUDA;
-  if (moe::launch_decode_down(p, s) != cudaSuccess) return MOE_ERR_CUDA;
+  p.status = reinterpret_cast<int *>(base + L.status);
+  if (moe::launch_decode_layer(p, grid, s) != cudaSuccess) return MOE_ERR_CUDA;
   return MOE_OK;
 }

@@ -5,6 +5,7 @@
 #include <algorithm>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <string>
@@ -59,7 +60,7 @@ WsLayout make_layout(const moe_config &c) {
   L.dec_idx = take(k * 4);
   L.dec_w = take(k * 4);
   L.dec_g = take(4);
-  L.dec_h = take((k + 1) * L.Imax * 4);
+  L.dec_h = take(decode_h_floats(c.top_k, L.Imax) * 4);
   L.dec_counter = take(16);
   L.x_stage = take(Tc * H * 2);
   L.y_stage = take(Tc * H * 2);
@@ -106,12 +107,11 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 
 
 enum KernelId : int {
   K_ROUTER_GEMM = 0, K_TOPK, K_SCAN, K_SCATTER, K_GATEUP_GEMM, K_DOWN_GEMM, K_COMBINE,
-  K_DEC_ROUTER_SHARED, K_DEC_GATEUP, K_DEC_DOWN, K_H2D, K_D2H, K_COUNT
+  K_DEC_LAYER, K_H2D, K_D2H, K_COUNT
 };
 const char *kKernelNames[K_COUNT] = {
     "router_gemm", "topk", "route_scan", "route_scatter", "gateup_swiglu_gemm", "down_gemm",
-    "combine", "decode_router_shared", "decode_gateup", "decode_down_combine", "h2d_copy",
-    "d2h_copy"};
+    "combine", "decode_layer", "h2d_copy", "d2h_copy"};
 
 }  // namespace
 
@@ -127,6 +127,8 @@ struct moe_ctx {
   int device = 0;
   int num_sms = 0;
   int gemm_grid = 0;   // CTAs of the persistent grouped-GEMM grid (whole pairs)
+  int gemm_prefetch = 0;   // L2 prefetch of the next tile's operands (MOE_GEMM_PREFETCH=1)
+  int decode_grid = 0;     // CTAs of the cooperative decode launch
   char *ws = nullptr;
   size_t ws_bytes = 0;
   WsLayout L{};
@@ -266,6 +268,7 @@ moe_status enqueue_route(moe_ctx *ctx, const LayerSlot &ls, const void *x, int T
   gp.out_ld = c.n_experts;
   gp.bias = ls.w.router_b;
   gp.status = ctx->status();
+  gp.prefetch = ctx->gemm_prefetch;
   const int tiles = gp.n_blocks_host * gp.m_tiles;
   moe_status st;
   {
@@ -325,6 +328,7 @@ moe_status enqueue_prefill_chunk(moe_ctx *ctx, const LayerSlot &ls, const void *
   gp.shared_row0 = T * c.top_k;
   gp.sorted_rows = sorted;
   gp.status = ctx->status();
+  gp.prefetch = ctx->gemm_prefetch;
   // gate/up + SwiGLU -> h
   gp.mode = MODE_GATEUP;
   gp.m_tiles = (L.Imax + gemm_pair_rows() / 2 - 1) / (gemm_pair_rows() / 2);   // 128 SwiGLU outputs per pair
@@ -408,22 +412,9 @@ moe_status enqueue_decode(moe_ctx *ctx, const LayerSlot &ls, const void *x, void
   p.h = ctx->at<float>(L.dec_h);
   p.h_ld = L.Imax;
   p.counter = ctx->at<unsigned int>(L.dec_counter);
-  moe_status st;
-  {
-    ProfScope ps(ctx, K_DEC_ROUTER_SHARED, s);
-    st = launched(ctx, launch_decode_router_shared(p, s), "decode router launch");
-  }
-  if (st) return st;
-  {
-    ProfScope ps(ctx, K_DEC_GATEUP, s);
-    st = launched(ctx, launch_decode_gateup(p, s), "decode gate/up launch");
-  }
-  if (st) return st;
-  {
-    ProfScope ps(ctx, K_DEC_DOWN, s);
-    st = launched(ctx, launch_decode_down(p, s), "decode down launch");
-  }
-  return st;
+  p.status = ctx->status();
+  ProfScope ps(ctx, K_DEC_LAYER, s);
+  return launched(ctx, launch_decode_layer(p, ctx->decode_grid, s), "decode layer launch");
 }
 
 }  // namespace
@@ -481,8 +472,10 @@ moe_status moe_ctx_create(const moe_config *cfg, int device, void *workspace, si
     return MOE_ERR_CUDA;
   }
   ctx->gemm_grid = gemm_max_grid(sms);
+  ctx->decode_grid = decode_layer_grid(sms);
+  if (const char *env = std::getenv("MOE_GEMM_PREFETCH")) ctx->gemm_prefetch = std::atoi(env) != 0;
   if (
-      (e = decode_configure(std::max(cfg->hidden, (cfg->top_k + 1) * L.Imax))) != cudaSuccess ||
+      (e = decode_configure((cfg->top_k + 1) * L.Imax)) != cudaSuccess ||
       (e = cudaMemset(ctx->ws + L.status, 0, 256)) != cudaSuccess ||
       (e = cudaMemset(ctx->ws + L.dec_counter, 0, 16)) != cudaSuccess ||
       (e = cudaDeviceSynchronize()) != cudaSuccess) {
@@ -674,6 +667,7 @@ moe_status moe_check_device(moe_ctx *ctx, int32_t *code) {
   if (code) *code = v;
   if (v != 0) {
     cudaMemset(ctx->status(), 0, 4);
+    cudaMemset(ctx->ws + ctx->L.dec_counter, 0, 16);   // a timed-out grid barrier
     cudaDeviceSynchronize();
     return fail(ctx, MOE_ERR_DEVICE_TIMEOUT, "device wait timed out (site 0x%x)", v);
   }

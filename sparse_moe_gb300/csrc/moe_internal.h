@@ -43,6 +43,7 @@ struct GemmParams {
   int out_ld;                // elements per output row
   const float *bias;         // router bias or null
   int *status;               // device status word
+  int prefetch;              // 1: prefetch the next tile's operand rows into L2
 };
 
 cudaError_t gemm_configure();
@@ -82,14 +83,17 @@ struct DecodeParams {
   int32_t *idx;              // [k]
   float *w;                  // [k]
   float *g;                  // [1]
-  float *h;                  // [(k+1), Imax] fp32; row k = shared expert
-  int h_ld;
-  unsigned int *counter;     // last-block-done counter (zero between launches)
+  float *h;                  // [2k * h_ld + h_ld] fp32: gate/up dots [k][2I], shared h [Is]
+  int h_ld;                  // max(I, Is)
+  unsigned int *counter;     // grid barrier: count, generation (zero-initialised once)
+  int *status;               // device status word
 };
+// Floats of the h region a decode needs.
+inline size_t decode_h_floats(int k, int h_ld) { return (2 * static_cast<size_t>(k) + 1) * h_ld; }
 cudaError_t decode_configure(int max_smem_floats);
-// The three decode launches, in order (see decode.cu).
-cudaError_t launch_decode_router_shared(const DecodeParams &p, cudaStream_t stream);
-cudaError_t launch_decode_gateup(const DecodeParams &p, cudaStream_t stream);
-cudaError_t launch_decode_down(const DecodeParams &p, cudaStream_t stream);
+// Co-resident grid of the decode layer kernel.
+int decode_layer_grid(int num_sms);
+// One decode layer (see decode.cu): a cooperative launch of decode_layer_grid CTAs.
+cudaError_t launch_decode_layer(const DecodeParams &p, int grid, cudaStream_t stream);
 
 }  // namespace moe

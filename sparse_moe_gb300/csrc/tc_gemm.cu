@@ -280,7 +280,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     const __nv_bfloat16 *a_routed = reinterpret_cast<const __nv_bfloat16 *>(p.a_routed);
     const __nv_bfloat16 *a_shared = reinterpret_cast<const __nv_bfloat16 *>(p.a_shared);
     auto prefetch_a = [&](int tile_id) {
-      if (tile_id >= ntiles) return;
+      if (!p.prefetch || tile_id >= ntiles) return;
       const Tile u = decode_tile(p, tile_id, rank);
       if (!u.valid) return;
       const __nv_bfloat16 *ab = u.shared ? a_shared : a_routed;
@@ -365,7 +365,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     const uint32_t empty_bar = smem_u32(&tail->empty[g]);
     const int btid = bw * 32 + lane;
     auto prefetch_b = [&](int tile_id) {
-      if (tile_id >= ntiles) return;
+      if (!p.prefetch || tile_id >= ntiles) return;
       const Tile u = decode_tile(p, tile_id, rank);
       if (!u.valid) return;
       const uint32_t kbytes = static_cast<uint32_t>(u.nk * BK * 2);
