@@ -191,7 +191,7 @@ moe_status moe_forward_decode_host(moe_ctx *ctx, int layer, const void *x_host,
  *   Scratch: the per-token intermediates live in one fixed device array
  *   inside the library, 64 KiB, held by every device that loads the library
  *   until the process exits.  Shapes whose intermediates need more (E + 2k +
- *   (2k + 1) * max(I, Is) floats plus alignment) are rejected with
+ *   (k + 1) * max(I, Is) floats plus alignment) are rejected with
  *   MOE_ERR_WORKSPACE; nothing is launched then.
  *   Set-up: the first call on each device looks up the array's device
  *   address (with that device current) and raises the decode kernel's

@@ -1,41 +1,54 @@
 // Batch-1 decode path (sections "Optimize the one-row weight path" and
 // "Reduce intermediate and state traffic" of "Optimizing On-Device Inference
 // for Apple Silicon"): with one activation row there is no weight reuse, so
-// every kernel is a row-parallel GEMV on the vector ALUs that streams each
-// weight row once with coalesced 128-bit loads.  One persistent cooperative
-// launch per layer runs three phases separated by grid barriers:
+// the layer is a chain of row-parallel GEMVs on the vector ALUs that stream
+// every weight row once.  One persistent cooperative launch per layer runs it
+// as three phases separated by two grid barriers:
 //
-//   1. router logits (+bias), the shared-expert gate sigmoid(x . w_sg) and the
-//      shared expert's gate/up projections with SwiGLU (all only need x);
-//   2. top-k selection (redone by every CTA from the logits in L2), then the
+//   A. router logits (+bias), the shared-expert gate sigmoid(x . w_sg) and
+//      the shared expert's gate and up dot products (all need only x);
+//   B. top-k selection (redone by every warp from the logits in L2), then the
 //      k routed experts' gate and up dot products;
-//   3. the output projections of the k experts and of the shared expert,
-//      fused with SwiGLU, the routing weights and the shared gate:
-//      y[n] = sum_j w_j (Wd_j h_j)[n] + g (Sd h_s)[n], in fixed j order.
+//   C. y[n] = sum_j w_j (Wd_j h_j)[n] + g (Sd h_s)[n] in fixed j order, with
+//      h = silu(gate) * up formed from the phase-A/B dot products.
 //
-// Every warp issues all of its weight loads (and its slice of x, read
-// straight from global memory) before any arithmetic, so each SM keeps a
-// large number of 16-byte requests in flight; staying resident across the
-// phases removes per-launch ramp-up and tails, which dominate a layer that
-// moves 58 MB in a few microseconds.  int4 weights are read packed (32 codes per
-// 128-bit load) and expanded in registers; each 16-byte chunk lies inside one
-// 64-wide scale group.
+// Phase C's weights are known early: the shared expert's output rows at the
+// start, the routed experts' right after top-k.  Each CTA owns a contiguous
+// range of output rows n and bulk-copies (cp.async.bulk, completing on an
+// mbarrier) exactly those rows of the k + 1 output projections into its
+// shared memory while the gate/up rows stream through registers.  The HBM
+// traffic of phases B and C therefore overlaps, and after the last barrier
+// only the h exchange (through L2) and shared-memory arithmetic remain.
+//
+// Gate/up rows are read with 128-bit loads, every load of a segment issued
+// before any arithmetic.  int4 weights are read packed (32 codes per 128-bit
+// load) and expanded in registers; each 16-byte chunk lies inside one 64-wide
+// scale group.
+#include "moe_common.cuh"
 #include "moe_internal.h"
-#include "warp_topk.cuh"
 
 namespace moe {
 
 constexpr int kDecLayerThreads = 512;
+constexpr int kDecWarps = kDecLayerThreads / 32;
 
 // Optional phase timestamps (compiled only with -DMOE_TRACE): per CTA, clock64
 // at each phase boundary of the last decode launch, read back with
 // moe_debug_read_decode_trace().
 #ifdef MOE_TRACE
-__device__ long long g_dec_trace[1024][8];
+__device__ long long g_dec_trace[1024][16];
 #define DEC_MARK(i) \
   if (threadIdx.x == 0) g_dec_trace[blockIdx.x & 1023][i] = clock64()
+// same, read only after `dep` has been computed
+#define DEC_MARK_DEP(i, dep)                                                          \
+  if (threadIdx.x == 0) {                                                             \
+    long long t_;                                                                     \
+    asm volatile("mov.u64 %0, %%clock64;" : "=l"(t_) : "f"(static_cast<float>(dep))); \
+    g_dec_trace[blockIdx.x & 1023][i] = t_;                                           \
+  }
 #else
 #define DEC_MARK(i)
+#define DEC_MARK_DEP(i, dep)
 #endif
 
 __device__ __forceinline__ uint4 ld_stream(const void *p) {
@@ -46,11 +59,38 @@ __device__ __forceinline__ uint4 ld_stream(const void *p) {
   return v;
 }
 
-__device__ __forceinline__ void grid_dependency_wait() {
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+// `bytes` (a multiple of 16) from global `src` to this CTA's shared memory at
+// `dst` (both 16-byte aligned); completes on the mbarrier at `bar`.
+__device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void *src, uint32_t bytes,
+                                              uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
 }
-__device__ __forceinline__ void allow_dependents() {
+
+__device__ __forceinline__ void prefetch_l2_line(const void *p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+// Start of the 128-byte line holding p.
+__device__ __forceinline__ const char *line_of(const char *p) {
+  return reinterpret_cast<const char *>(reinterpret_cast<uintptr_t>(p) & ~uintptr_t(127));
+}
+
+// Programmatic dependent launch: let the next kernel in the stream be
+// scheduled (its CTAs start as SMs free up), and wait until the previous one
+// has completed with its memory visible.  Both are no-ops without the launch
+// attribute.
+__device__ __forceinline__ void pdl_trigger() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// This warp's L2 prefetch of `bytes` of one weight row.
+__device__ __forceinline__ void prefetch_row_l2(const void *row, size_t bytes) {
+  const char *b = static_cast<const char *>(row);
+  for (size_t off = (threadIdx.x & 31) * 128; off < bytes; off += 32 * 128) prefetch_l2_line(b + off);
 }
 
 __device__ __forceinline__ float warp_sum(float v) {
@@ -72,18 +112,16 @@ __device__ __forceinline__ float dot8_bf16_bf16(const uint4 wv, const uint4 xv) 
   return a;
 }
 
-// 8 bf16 weights . 8 fp32 activations
-__device__ __forceinline__ float dot8_bf16_f32(const uint4 wv, const float *xs) {
-  const float4 x0 = *reinterpret_cast<const float4 *>(xs);
-  const float4 x1 = *reinterpret_cast<const float4 *>(xs + 4);
-  float a = bf16_lo(wv.x) * x0.x;
-  a = fmaf(bf16_hi(wv.x), x0.y, a);
-  a = fmaf(bf16_lo(wv.y), x0.z, a);
-  a = fmaf(bf16_hi(wv.y), x0.w, a);
-  a = fmaf(bf16_lo(wv.z), x1.x, a);
-  a = fmaf(bf16_hi(wv.z), x1.y, a);
-  a = fmaf(bf16_lo(wv.w), x1.z, a);
-  a = fmaf(bf16_hi(wv.w), x1.w, a);
+// 8 bf16 weights . 8 fp32 activations held in registers
+__device__ __forceinline__ float dot8_bf16_f32(const uint4 wv, const float (&xs)[8]) {
+  float a = bf16_lo(wv.x) * xs[0];
+  a = fmaf(bf16_hi(wv.x), xs[1], a);
+  a = fmaf(bf16_lo(wv.y), xs[2], a);
+  a = fmaf(bf16_hi(wv.y), xs[3], a);
+  a = fmaf(bf16_lo(wv.z), xs[4], a);
+  a = fmaf(bf16_hi(wv.z), xs[5], a);
+  a = fmaf(bf16_lo(wv.w), xs[6], a);
+  a = fmaf(bf16_hi(wv.w), xs[7], a);
   return a;
 }
 
@@ -110,18 +148,14 @@ __device__ __forceinline__ float dot32_int4_bf16(const uint4 wv, const uint4 (&x
   return a;
 }
 
-// Same with 32 fp32 activations.
-__device__ __forceinline__ float dot32_int4_f32(const uint4 wv, const float *xs) {
+// Same with 32 fp32 activations held in registers.
+__device__ __forceinline__ float dot32_int4_f32(const uint4 wv, const float (&xs)[32]) {
   const uint32_t words[4] = {wv.x, wv.y, wv.z, wv.w};
   float a = 0.0f;
 #pragma unroll
-  for (int w = 0; w < 4; ++w) {
-    const float4 x0 = *reinterpret_cast<const float4 *>(xs + 8 * w);
-    const float4 x1 = *reinterpret_cast<const float4 *>(xs + 8 * w + 4);
-    const float xv[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+  for (int w = 0; w < 4; ++w)
 #pragma unroll
-    for (int n = 0; n < 8; ++n) a = fmaf(nib(words[w], n), xv[n], a);
-  }
+    for (int n = 0; n < 8; ++n) a = fmaf(nib(words[w], n), xs[8 * w + n], a);
   return a;
 }
 
@@ -131,6 +165,11 @@ __device__ __forceinline__ float dot32_int4_f32(const uint4 wv, const float *xs)
 template <int WF> struct Fmt;
 template <> struct Fmt<0> { static constexpr int EPC = 8, XPC = 1, U = 8; };
 template <> struct Fmt<1> { static constexpr int EPC = 32, XPC = 4, U = 2; };
+
+// Bytes of one weight row of K elements.
+template <int WF> __host__ __device__ __forceinline__ size_t row_bytes(int K) {
+  return WF == 0 ? static_cast<size_t>(K) * 2 : static_cast<size_t>(K) / 2;
+}
 
 // Dot products of NR weight rows of length K with the bf16 vector x (global
 // memory), by one warp.  All loads of a segment (weights first, then x) are
@@ -149,6 +188,7 @@ __device__ __forceinline__ void warp_dots_x(const void *const (&rows)[NR],
   for (int c0 = 0; c0 < nchunk; c0 += 32 * F::U) {
     uint4 wv[NR][F::U];
     uint4 xv[F::U][F::XPC];
+    float sv[NR][F::U];
 #pragma unroll
     for (int r = 0; r < NR; ++r)
 #pragma unroll
@@ -156,6 +196,7 @@ __device__ __forceinline__ void warp_dots_x(const void *const (&rows)[NR],
         const int c = c0 + lane + 32 * u;
         wv[r][u] = (c < nchunk) ? ld_stream(reinterpret_cast<const uint4 *>(rows[r]) + c)
                                 : make_uint4(0, 0, 0, 0);
+        if constexpr (WF == 1) sv[r][u] = (c < nchunk) ? __bfloat162float(__ldg(srows[r] + (c >> 1))) : 0.0f;
       }
 #pragma unroll
     for (int u = 0; u < F::U; ++u)
@@ -164,19 +205,14 @@ __device__ __forceinline__ void warp_dots_x(const void *const (&rows)[NR],
         const int c = c0 + lane + 32 * u;
         xv[u][q] = (c < nchunk) ? __ldg(xg + c * F::XPC + q) : make_uint4(0, 0, 0, 0);
       }
+    // chunks past the row end were loaded as zeros and add nothing: no
+    // branches, so the NR * U dot chains interleave
 #pragma unroll
     for (int r = 0; r < NR; ++r)
 #pragma unroll
       for (int u = 0; u < F::U; ++u) {
-        const int c = c0 + lane + 32 * u;
-        if (c < nchunk) {
-          if constexpr (WF == 0) {
-            acc[r] += dot8_bf16_bf16(wv[r][u], xv[u][0]);
-          } else {
-            const float s = __bfloat162float(srows[r][c >> 1]);
-            acc[r] = fmaf(s, dot32_int4_bf16(wv[r][u], xv[u]), acc[r]);
-          }
-        }
+        if constexpr (WF == 0) acc[r] += dot8_bf16_bf16(wv[r][u], xv[u][0]);
+        else acc[r] = fmaf(sv[r][u], dot32_int4_bf16(wv[r][u], xv[u]), acc[r]);
       }
   }
 #pragma unroll
@@ -186,88 +222,281 @@ __device__ __forceinline__ void warp_dots_x(const void *const (&rows)[NR],
 // Row r of a K-major matrix with K columns, bf16 or packed int4.
 template <int WF>
 __device__ __forceinline__ const void *row_ptr(const void *base, size_t r, int K) {
-  return (WF == 0) ? static_cast<const void *>(reinterpret_cast<const __nv_bfloat16 *>(base) + r * K)
-                   : static_cast<const void *>(reinterpret_cast<const uint8_t *>(base) + r * (K / 2));
+  return static_cast<const uint8_t *>(base) + r * row_bytes<WF>(K);
 }
 __device__ __forceinline__ const __nv_bfloat16 *scale_row(const void *base, size_t r, int K) {
   return base ? reinterpret_cast<const __nv_bfloat16 *>(base) + r * (K / 64) : nullptr;
 }
 
 // ------------------------------------------------------ grid barrier --
-__device__ __forceinline__ unsigned int ld_acquire_gpu(const unsigned int *p) {
-  unsigned int v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+// A 64-bit arrival counter that only grows: barrier b of a launch completes
+// when the counter reaches base + b * gridDim.x, where base is the counter's
+// value at launch (a multiple of gridDim.x: every completed launch adds
+// exactly two grid-widths).  A CTA reads base before its first arrival; no
+// barrier of this launch can complete before that arrival, so the value it
+// reads lies in [base, base + gridDim.x).
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long *p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
   return v;
 }
+__device__ __forceinline__ void red_release_add_u64(unsigned long long *p, unsigned long long v) {
+  asm volatile("red.release.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
 
-// Barrier across all CTAs of a cooperative launch (all co-resident).  The
-// counter resets itself; the generation word only grows.  A CTA that waits
-// longer than kWaitLimitCycles records DEV_TIMEOUT_GRID and carries on.
-__device__ __forceinline__ void grid_barrier(unsigned int *count, unsigned int *gen, int *status) {
+// Arrive and wait until `target` arrivals; the CTA's earlier writes are
+// released with the arrival.  A CTA that waits longer than kWaitLimitCycles
+// records DEV_TIMEOUT_GRID and carries on.
+__device__ __forceinline__ void grid_sync(unsigned long long *bar, unsigned long long target,
+                                          int *status) {
   __syncthreads();
   if (threadIdx.x == 0) {
-    const unsigned int g0 = ld_acquire_gpu(gen);   // read before arriving
-    __threadfence();
-    if (atomicAdd(count, 1u) == gridDim.x - 1) {
-      atomicExch(count, 0u);
-      __threadfence();
-      atomicAdd(gen, 1u);
-    } else {
+    red_release_add_u64(bar, 1ull);
+    if (ld_acquire_u64(bar) < target) {
       const long long t0 = clock64();
-      while (ld_acquire_gpu(gen) == g0) {
+      while (ld_acquire_u64(bar) < target) {
         if (clock64() - t0 > kWaitLimitCycles) {
           atomicExch(status, DEV_TIMEOUT_GRID);
           break;
         }
       }
     }
-    __threadfence();
   }
   __syncthreads();
 }
 
+// --------------------------------------------------------------- top-k --
+// Order-preserving 32-bit key of a logit (-0 folded into +0 so that equal
+// values compare equal, as floats do).
+__device__ __forceinline__ uint32_t logit_key(float v) {
+  const uint32_t u = __float_as_uint(v + 0.0f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key_logit(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+// Top-k of the E logits (lane l holds experts l + 32 r in v[r]) in the order
+// larger logit first, equal logits -> lower expert first; then the weights
+// softmax(selected logits), which equal the softmax over all E logits
+// renormalised over the selection ("Qwen creates three distinct workload
+// shapes").  Lane j < k receives selection j: expert sel_e and weight sel_w.
+// Each round takes the warp maximum of the lanes' best keys and the lowest
+// expert holding it with two redux.sync reductions; every lane computes the
+// same result.
+template <int R>
+__device__ __forceinline__ void warp_topk_redux(const float (&v)[R], int E, int k, int &sel_e,
+                                                float &sel_w) {
+  const int lane = threadIdx.x & 31;
+  uint32_t key[R];
+#pragma unroll
+  for (int r = 0; r < R; ++r) key[r] = (lane + 32 * r < E) ? logit_key(v[r]) : 0u;
+  uint32_t sel_key = 0;
+  sel_e = 0;
+  for (int j = 0; j < k; ++j) {
+    uint32_t bk = key[0];
+    int br = 0;
+#pragma unroll
+    for (int r = 1; r < R; ++r)
+      if (key[r] > bk) {
+        bk = key[r];
+        br = r;
+      }
+    const uint32_t m = __reduce_max_sync(0xffffffffu, bk);
+    if (j == 0) DEC_MARK_DEP(11, m);
+    const uint32_t e = __reduce_min_sync(0xffffffffu, bk == m ? static_cast<uint32_t>(lane + 32 * br)
+                                                              : 0xffffffffu);
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+      key[r] = (e == static_cast<uint32_t>(lane + 32 * r)) ? 0u : key[r];
+    if (lane == j) {
+      sel_key = m;
+      sel_e = static_cast<int>(e);
+    }
+  }
+  DEC_MARK_DEP(12, sel_key);
+  const float sv = key_logit(sel_key);
+  const float vmax = __shfl_sync(0xffffffffu, sv, 0);
+  const float ex = (lane < k) ? expf(sv - vmax) : 0.0f;
+  float sum = ex;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+  sel_w = ex / sum;
+}
+
 // ------------------------------------------------- one decode layer --
-// Persistent cooperative kernel, one CTA per SM, three phases:
-//   1. router logits, shared gate sigmoid(x . w_sg), shared-expert SwiGLU h;
-//   2. (every CTA) top-k of the logits, then the k routed experts' gate and
-//      up dot products gu[j][r] = W_{e_j}[r] . x, one weight row per warp
-//      item, two items in flight per warp;
-//   3. y[n] = sum_j w_j (Wd_j h_j)[n] + g (Sd h_s)[n], one warp per n, with
-//      h_j = silu(gu[j][:I]) * gu[j][I:] staged in shared memory.
-// Each warp issues its first phase-3 weight loads before the last grid
-// barrier, so they overlap the barrier and the staging of h.
-template <int WF, int R, int KMAX>
-__global__ void __launch_bounds__(kDecLayerThreads, 1) decode_layer_kernel(const DecodeParams p) {
+// Dynamic shared memory of one CTA, in this order:
+//   part  [(k+1) p3_rows] fp32   per-slot dot products of the CTA's output rows
+//   w3    the CTA's output-projection rows (p3_stage only): k slots of p3_rows
+//         rows of I for the routed experts, then one of p3_rows rows of Is
+struct DecSmem {
+  size_t w3, w3_sh, unstaged, staged;
+};
+template <int WF>
+__host__ __device__ __forceinline__ DecSmem dec_smem(int k, int I, int Is, int rows) {
+  DecSmem L{};
+  L.w3 = (static_cast<size_t>(k + 1) * rows * sizeof(float) + 127) / 128 * 128;
+  L.unstaged = L.w3;
+  L.w3_sh = L.w3 + static_cast<size_t>(k) * rows * row_bytes<WF>(I);
+  L.staged = L.w3_sh + static_cast<size_t>(rows) * row_bytes<WF>(Is);
+  return L;
+}
+
+// One phase-C task: part[j][t0 + r] = (output-projection row n0 + t0 + r of
+// slot j) . h_j for r < 8, slot j < k a routed expert and j = k the shared
+// one.  The rows come from shared memory (STAGED) or global memory; h_j comes
+// from global memory (L2).  Lane l takes 16-byte chunks l + 32 m and keeps
+// the matching h elements in registers across the eight rows.
+template <int WF, bool STAGED>
+__device__ __forceinline__ void slot_task(const DecodeParams &p, int j, int t0, int n0, int nrows,
+                                          int expert, float *part, const unsigned char *w3,
+                                          const unsigned char *w3_sh) {
   using F = Fmt<WF>;
-  extern __shared__ float hs[];   // (k+1) rows of h_ld floats
+  const int lane = threadIdx.x & 31;
+  const bool sh = (j == p.k);
+  const int K = sh ? p.Is : p.I;
+  const int nch = K / F::EPC, ng = K / 64;
+  const size_t rb = row_bytes<WF>(K);
+  const float *hj = p.h + static_cast<size_t>(j) * p.h_ld;
+  const size_t r0 = (sh ? 0 : static_cast<size_t>(expert) * p.H) + n0 + t0;   // global row
+  const unsigned char *wrow;   // row t0 of the group
+  if constexpr (STAGED)
+    wrow = sh ? w3_sh + static_cast<size_t>(t0) * rb
+              : w3 + (static_cast<size_t>(j) * p.p3_rows + t0) * rb;
+  else
+    wrow = static_cast<const unsigned char *>(sh ? p.sh_down : p.down) + r0 * rb;
+  const __nv_bfloat16 *srow =
+      WF == 1 ? static_cast<const __nv_bfloat16 *>(sh ? p.sh_down_scale : p.down_scale) + r0 * ng
+              : nullptr;
+  // bf16 rows: two chunks per lane per pass, so that both h loads (from L2)
+  // are in flight together
+  constexpr int CU = WF == 0 ? 2 : 1;
+  float acc[8];
+#pragma unroll
+  for (int r = 0; r < 8; ++r) acc[r] = 0.0f;
+  for (int c0 = lane; c0 < nch; c0 += 32 * CU) {
+    float hv[CU][F::EPC];
+#pragma unroll
+    for (int u = 0; u < CU; ++u) {
+      const int c = c0 + 32 * u;
+#pragma unroll
+      for (int e = 0; e < F::EPC; e += 4) {
+        const float4 h4 = c < nch ? __ldcg(reinterpret_cast<const float4 *>(hj + c * F::EPC + e))
+                                  : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        hv[u][e] = h4.x;
+        hv[u][e + 1] = h4.y;
+        hv[u][e + 2] = h4.z;
+        hv[u][e + 3] = h4.w;
+      }
+    }
+    // rows past the CTA's last repeat that row (their sums are dropped) and
+    // chunks past the row end hold zero h: no branches, so the chains of the
+    // eight rows interleave
+#pragma unroll
+    for (int u = 0; u < CU; ++u) {
+      const int c = min(c0 + 32 * u, nch - 1);
+#pragma unroll
+      for (int r = 0; r < 8; ++r) {
+        const int rr = min(r, nrows - 1 - t0);
+        const uint4 wv = reinterpret_cast<const uint4 *>(wrow + rr * rb)[c];
+        if constexpr (WF == 0) {
+          acc[r] += dot8_bf16_f32(wv, hv[u]);
+        } else {
+          const float sc = __bfloat162float(__ldg(srow + rr * ng + (c >> 1)));
+          acc[r] = fmaf(sc, dot32_int4_f32(wv, hv[u]), acc[r]);
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < 8; ++r) acc[r] = warp_sum(acc[r]);
+  if (lane == 0) {
+#pragma unroll
+    for (int r = 0; r < 8; ++r)
+      if (t0 + r < nrows) part[j * p.p3_rows + t0 + r] = acc[r];
+  }
+}
+
+template <int WF>
+__device__ __forceinline__ void run_slot_task(const DecodeParams &p, int j, int t0, int n0,
+                                              int nrows, int expert, float *part,
+                                              const unsigned char *w3,
+                                              const unsigned char *w3_sh) {
+  if (p.p3_stage) slot_task<WF, true>(p, j, t0, n0, nrows, expert, part, w3, w3_sh);
+  else slot_task<WF, false>(p, j, t0, n0, nrows, expert, part, w3, w3_sh);
+}
+
+// Persistent cooperative kernel, one CTA per SM (see the top of this file).
+template <int WF, int R>
+__global__ void __launch_bounds__(kDecLayerThreads, 1) decode_layer_kernel(const DecodeParams p) {
+  extern __shared__ __align__(128) unsigned char dsm[];
+  __shared__ __align__(8) uint64_t mbar[2];   // [0] shared expert rows, [1] routed rows
   __shared__ int idx_s[32];
-  __shared__ float w_s[33];
+  __shared__ float w_s[33];                   // routing weights, then the shared gate
+  const DecSmem S = dec_smem<WF>(p.k, p.I, p.Is, p.p3_rows);
+  float *part = reinterpret_cast<float *>(dsm);
+  unsigned char *w3 = dsm + S.w3;
+  unsigned char *w3_sh = dsm + S.w3_sh;
   const __nv_bfloat16 *x = reinterpret_cast<const __nv_bfloat16 *>(p.x);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nwarps = kDecLayerThreads / 32;
-  const int gw = blockIdx.x * nwarps + warp;
-  const int nw = gridDim.x * nwarps;
-  float *gu = p.h;                                            // [k][2 I]
-  float *h_sh = p.h + static_cast<size_t>(p.k) * 2 * p.h_ld;  // [Is]
-  unsigned int *bar_count = p.counter;
-  unsigned int *bar_gen = p.counter + 1;
+  const int G = gridDim.x;
+  // warps numbered across CTAs first, so that a partly filled phase spreads
+  // over every SM
+  const int gw = warp * G + blockIdx.x;
+  const int nw = G * kDecWarps;
+  float *hg = p.h;   // [k+1][h_ld]: h of the k experts, then of the shared expert
+  // this CTA's output rows
+  const int n0 = static_cast<int>((static_cast<long long>(blockIdx.x) * p.H) / G);
+  const int n1 = static_cast<int>((static_cast<long long>(blockIdx.x + 1) * p.H) / G);
+  const int nrows = n1 - n0;
+  const int ngroups = (nrows + 7) / 8;
+  const size_t rbI = row_bytes<WF>(p.I), rbS = row_bytes<WF>(p.Is);
+  const uint32_t mb_sh = smem_u32(&mbar[0]), mb_rt = smem_u32(&mbar[1]);
 
   DEC_MARK(0);
-  // ---- phase 1: router rows, shared gate, shared-expert row pairs
-  const int n1 = p.E + 1 + p.Is;
-  for (int it = gw; it < n1; it += nw) {
-    if (it < p.E) {
-      const void *rows[1] = {row_ptr<0>(p.router_w, it, p.H)};
+  unsigned long long base = 0;   // barrier counter at launch (used by thread 0)
+  if (threadIdx.x == 0) {
+    // With a programmatic launch this CTA can start while the previous
+    // layer's CTAs finish, but only after the one on this SM exited, i.e.
+    // after that layer's last barrier completed: the counter is final.
+    const unsigned long long v = ld_acquire_u64(p.bar);
+    base = v - v % static_cast<unsigned long long>(G);
+    if (p.p3_stage) {
+      mbar_init(mb_sh, 1);
+      mbar_init(mb_rt, 1);
+      fence_mbarrier_init();
+      // the shared expert's output rows n0..n1 are needed whatever the routing
+      const uint32_t bytes = static_cast<uint32_t>(nrows * rbS);
+      mbar_arrive_expect_tx(mb_sh, bytes);
+      if (bytes) bulk_copy_g2s(smem_u32(w3_sh), row_ptr<WF>(p.sh_down, n0, p.Is), bytes, mb_sh);
+    }
+  }
+
+  pdl_trigger();
+  // Everything above and the prefetch below read only weights; x, and every
+  // buffer this kernel writes, may still be in use by the previous layer.
+  const int nA = p.E + 1 + p.Is;
+  if (gw < nA) {
+    if (gw < p.E) prefetch_row_l2(row_ptr<0>(p.router_w, gw, p.H), row_bytes<0>(p.H));
+    else if (gw == p.E) prefetch_row_l2(p.sh_gate_w, row_bytes<0>(p.H));
+    else {
+      prefetch_row_l2(row_ptr<WF>(p.sh_gate_up, gw - p.E - 1, p.H), row_bytes<WF>(p.H));
+      prefetch_row_l2(row_ptr<WF>(p.sh_gate_up, p.Is + gw - p.E - 1, p.H), row_bytes<WF>(p.H));
+    }
+  }
+  pdl_wait();
+
+  // ---- phase A: router rows, the shared gate row, shared-expert row pairs
+  for (int it = gw; it < nA; it += nw) {
+    if (it <= p.E) {
+      const void *rows[1] = {it < p.E ? row_ptr<0>(p.router_w, it, p.H) : p.sh_gate_w};
       const __nv_bfloat16 *sr[1] = {nullptr};
       float d[1];
       warp_dots_x<0, 1>(rows, sr, p.H, x, d);
-      if (lane == 0) p.logits[it] = d[0] + (p.router_b ? p.router_b[it] : 0.0f);
-    } else if (it == p.E) {
-      const void *rows[1] = {p.sh_gate_w};
-      const __nv_bfloat16 *sr[1] = {nullptr};
-      float d[1];
-      warp_dots_x<0, 1>(rows, sr, p.H, x, d);
-      if (lane == 0) *p.g = sigmoid_f(d[0]);
+      if (lane == 0) {
+        if (it < p.E) p.logits[it] = d[0] + (p.router_b ? p.router_b[it] : 0.0f);
+        else *p.g = sigmoid_f(d[0]);
+      }
     } else {
       const int i = it - p.E - 1;
       const void *rows[2] = {row_ptr<WF>(p.sh_gate_up, i, p.H),
@@ -276,191 +505,181 @@ __global__ void __launch_bounds__(kDecLayerThreads, 1) decode_layer_kernel(const
                                     scale_row(p.sh_gate_up_scale, p.Is + i, p.H)};
       float d[2];
       warp_dots_x<WF, 2>(rows, sr, p.H, x, d);
-      if (lane == 0) h_sh[i] = silu_f(d[0]) * d[1];
+      if (lane == 0) hg[static_cast<size_t>(p.k) * p.h_ld + i] = silu_f(d[0]) * d[1];
     }
   }
   DEC_MARK(1);
-  grid_barrier(bar_count, bar_gen, p.status);
+  grid_sync(p.bar, base + G, p.status);
   DEC_MARK(2);
 
-  // ---- top-k in every CTA (logits are in L2)
+  // ---- top-k (one warp per CTA; the logits are in L2)
   if (warp == 0) {
     float v[R];
 #pragma unroll
     for (int r = 0; r < R; ++r) {
       const int e = lane + 32 * r;
-      v[r] = (e < p.E) ? __ldcg(p.logits + e) : -INFINITY;
+      v[r] = (e < p.E) ? __ldcg(p.logits + e) : 0.0f;
     }
-    float sv, sw;
-    int se;
-    warp_topk<R>(v, p.E, p.k, sv, se, sw);
+    const float g = __ldcg(p.g);
+    int sel_e;
+    float sel_w;
+    warp_topk_redux<R>(v, p.E, p.k, sel_e, sel_w);
+    sel_e = min(max(sel_e, 0), p.E - 1);
     if (lane < p.k) {
-      idx_s[lane] = min(max(se, 0), p.E - 1);
-      w_s[lane] = sw;
+      idx_s[lane] = sel_e;
+      w_s[lane] = sel_w;
       if (blockIdx.x == 0) {
-        p.idx[lane] = se;
-        p.w[lane] = sw;
+        p.idx[lane] = sel_e;
+        p.w[lane] = sel_w;
       }
     }
-    if (lane == 0) w_s[32] = __ldcg(p.g);
+    if (lane == 0) w_s[32] = g;
   }
   __syncthreads();
   DEC_MARK(3);
+  // The last warps have the fewest phase-B rows: they issue the copies.
+  if (warp == kDecWarps - 1 && p.p3_stage) {
+    // the k routed experts' output rows n0..n1, one bulk copy per expert
+    const uint32_t bytes = static_cast<uint32_t>(nrows * rbI);
+    if (lane == 0) {
+      mbar_arrive_expect_tx(mb_rt, bytes * p.k);
+      if (bytes)
+        for (int j = 0; j < p.k; ++j)
+          bulk_copy_g2s(smem_u32(w3 + static_cast<size_t>(j) * p.p3_rows * rbI),
+                        row_ptr<WF>(p.down, static_cast<size_t>(idx_s[j]) * p.H + n0, p.I), bytes,
+                        mb_rt);
+    }
+  }
+  if (WF == 1 && warp == kDecWarps - 2 && nrows > 0) {
+    // int4 group scales of those rows, into L2 for phase C
+    for (int j = 0; j <= p.k; ++j) {
+      const bool sh = (j == p.k);
+      const size_t r0 = sh ? 0 : static_cast<size_t>(idx_s[j]) * p.H;
+      const int K = sh ? p.Is : p.I;
+      const void *sb = sh ? p.sh_down_scale : p.down_scale;
+      const char *s0 = reinterpret_cast<const char *>(scale_row(sb, r0 + n0, K));
+      const char *s1 = reinterpret_cast<const char *>(scale_row(sb, r0 + n1, K));
+      for (const char *a = line_of(s0) + lane * 128; a < s1; a += 32 * 128) prefetch_l2_line(a);
+    }
+  }
+  DEC_MARK(4);
 
-  // ---- phase 2: routed gate/up rows, two per warp iteration
-  const int I2 = 2 * p.I;
-  const int n2 = p.k * I2;
-  for (int base = gw; base < n2; base += 2 * nw) {
-    const int r0 = base;
-    const int r1 = (base + nw < n2) ? base + nw : base;
-    const int j0 = r0 / I2, rr0 = r0 - j0 * I2;
-    const int j1 = r1 / I2, rr1 = r1 - j1 * I2;
-    const size_t w0 = static_cast<size_t>(idx_s[j0]) * I2 + rr0;
-    const size_t w1 = static_cast<size_t>(idx_s[j1]) * I2 + rr1;
-    const void *rows[2] = {row_ptr<WF>(p.gate_up, w0, p.H), row_ptr<WF>(p.gate_up, w1, p.H)};
-    const __nv_bfloat16 *sr[2] = {scale_row(p.gate_up_scale, w0, p.H),
-                                  scale_row(p.gate_up_scale, w1, p.H)};
+  // ---- phase B: routed gate/up row pairs -> h
+  const int nB = p.k * p.I;
+  for (int q = gw; q < nB; q += nw) {
+    const int j = q / p.I, i = q - j * p.I;
+    const size_t rg = static_cast<size_t>(idx_s[j]) * 2 * p.I + i;
+    const void *rows[2] = {row_ptr<WF>(p.gate_up, rg, p.H), row_ptr<WF>(p.gate_up, rg + p.I, p.H)};
+    const __nv_bfloat16 *sr[2] = {scale_row(p.gate_up_scale, rg, p.H),
+                                  scale_row(p.gate_up_scale, rg + p.I, p.H)};
     float d[2];
     warp_dots_x<WF, 2>(rows, sr, p.H, x, d);
-    if (lane == 0) {
-      gu[static_cast<size_t>(j0) * I2 + rr0] = d[0];
-      if (r1 != r0) gu[static_cast<size_t>(j1) * I2 + rr1] = d[1];
-    }
+    if (lane == 0) hg[static_cast<size_t>(j) * p.h_ld + i] = silu_f(d[0]) * d[1];
   }
-
-  // ---- phase 3 weight loads for this warp's first output, ahead of the barrier
-  const int n_first = gw;
-  uint4 wv[KMAX + 1][2];
-  const uint4 *rowp[KMAX + 1];
-  const __nv_bfloat16 *srow[KMAX + 1];
-  int nchunk[KMAX + 1];
-  auto load_rows = [&](int n) {
-#pragma unroll
-    for (int j = 0; j <= KMAX; ++j) {
-      wv[j][0] = wv[j][1] = make_uint4(0, 0, 0, 0);
-      rowp[j] = nullptr;
-      srow[j] = nullptr;
-      nchunk[j] = 0;
-      if (j > p.k) continue;
-      const bool shared = (j == p.k);
-      const int K = shared ? p.Is : p.I;
-      const size_t r = shared ? static_cast<size_t>(n) : static_cast<size_t>(idx_s[j]) * p.H + n;
-      nchunk[j] = K / F::EPC;
-      rowp[j] = reinterpret_cast<const uint4 *>(row_ptr<WF>(shared ? p.sh_down : p.down, r, K));
-      srow[j] = scale_row(shared ? p.sh_down_scale : p.down_scale, r, K);
-#pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const int c = lane + 32 * u;
-        if (c < nchunk[j]) wv[j][u] = ld_stream(rowp[j] + c);
-      }
+  // The shared expert's slot needs only h_s (complete since the first
+  // barrier): the last warps, which have the fewest phase-B rows, do it now.
+  for (int s = kDecWarps - 1 - warp; s < ngroups; s += kDecWarps) {
+    if (p.p3_stage) {
+      volatile int no_abort = 0;
+      mbar_wait_bounded(mb_sh, 0, &no_abort, p.status, DEV_TIMEOUT_STAGE);
     }
-  };
-  DEC_MARK(4);
-  if (n_first < p.H) load_rows(n_first);
-  grid_barrier(bar_count, bar_gen, p.status);
+    run_slot_task<WF>(p, p.k, 8 * s, n0, nrows, 0, part, w3, w3_sh);
+  }
   DEC_MARK(5);
-
-  // ---- stage h: routed SwiGLU from the gate/up dots, then the shared row
-  const int nh = p.k * p.I;
-  for (int e = threadIdx.x; e < nh; e += blockDim.x) {
-    const int j = e / p.I, i = e - j * p.I;
-    const float g = __ldcg(gu + static_cast<size_t>(j) * I2 + i);
-    const float u = __ldcg(gu + static_cast<size_t>(j) * I2 + p.I + i);
-    hs[static_cast<size_t>(j) * p.h_ld + i] = silu_f(g) * u;
-  }
-  for (int i = threadIdx.x; i < p.Is; i += blockDim.x)
-    hs[static_cast<size_t>(p.k) * p.h_ld + i] = __ldcg(h_sh + i);
-  __syncthreads();
+  grid_sync(p.bar, base + 2 * static_cast<unsigned long long>(G), p.status);
   DEC_MARK(6);
 
-  // ---- phase 3: outputs
-  for (int n = n_first; n < p.H; n += nw) {
-    if (n != n_first) load_rows(n);
-    float y = 0.0f;
-#pragma unroll
-    for (int j = 0; j <= KMAX; ++j) {
-      if (j > p.k) continue;
-      const float *hj = hs + static_cast<size_t>(j) * p.h_ld;
-      float d = 0.0f;
-#pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const int c = lane + 32 * u;
-        if (c < nchunk[j]) {
-          if constexpr (WF == 0) d += dot8_bf16_f32(wv[j][u], hj + c * 8);
-          else d = fmaf(__bfloat162float(srow[j][c >> 1]), dot32_int4_f32(wv[j][u], hj + c * 32), d);
-        }
-      }
-      // chunks beyond the first 64 per row (I > 512 for bf16, > 2048 for int4)
-      for (int c = lane + 64; c < nchunk[j]; c += 32) {
-        const uint4 wc = ld_stream(rowp[j] + c);
-        if constexpr (WF == 0) d += dot8_bf16_f32(wc, hj + c * 8);
-        else d = fmaf(__bfloat162float(srow[j][c >> 1]), dot32_int4_f32(wc, hj + c * 32), d);
-      }
-      d = warp_sum(d);
-      y = fmaf(j == p.k ? w_s[32] : w_s[j], d, y);
-    }
-    if (lane == 0) reinterpret_cast<__nv_bfloat16 *>(p.y)[n] = __float2bfloat16_rn(y);
+  // ---- phase C: the routed slots, one (slot j, group of 8 rows) per warp
+  if (p.p3_stage) {
+    // the staged rows must have landed before this thread reads them
+    volatile int no_abort = 0;
+    mbar_wait_bounded(mb_rt, 0, &no_abort, p.status, DEV_TIMEOUT_STAGE);
+  }
+  DEC_MARK(7);
+  for (int task = warp; task < p.k * ngroups; task += kDecWarps) {
+    const int j = task / ngroups, t0 = (task - j * ngroups) * 8;
+    run_slot_task<WF>(p, j, t0, n0, nrows, idx_s[j], part, w3, w3_sh);
   }
   __syncthreads();
-  DEC_MARK(7);
+  DEC_MARK(8);
+  // y[n] = sum_j w_j part[j] + g part[k], in that order
+  for (int t = threadIdx.x; t < nrows; t += kDecLayerThreads) {
+    float y = 0.0f;
+    for (int j0 = 0; j0 <= p.k; j0 += 8) {
+      // eight slots per pass, loads first; slots past k add 0 * (a valid part)
+      float pw[8], pv[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int j = min(j0 + u, p.k);
+        pv[u] = part[j * p.p3_rows + t];
+        pw[u] = j0 + u > p.k ? 0.0f : w_s[j == p.k ? 32 : j];
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) y = fmaf(pw[u], pv[u], y);
+    }
+    reinterpret_cast<__nv_bfloat16 *>(p.y)[n0 + t] = __float2bfloat16_rn(y);
+  }
+  DEC_MARK(9);
+  DEC_MARK(10);
+#ifdef MOE_TRACE
+  if (threadIdx.x == 0) g_dec_trace[blockIdx.x & 1023][15] = p.p3_stage + 10 * p.p3_rows;
+#endif
 }
 
-template <int WF, int R, int KMAX>
-static cudaError_t launch_layer(const DecodeParams &p, int grid, cudaStream_t stream) {
+template <int WF, int R>
+static cudaError_t launch_layer(DecodeParams p, int grid, int smem_limit, bool pdl,
+                                cudaStream_t stream) {
+  p.p3_rows = (p.H + grid - 1) / grid;
+  const DecSmem S = dec_smem<WF>(p.k, p.I, p.Is, p.p3_rows);
+  p.p3_stage = S.staged <= static_cast<size_t>(smem_limit) ? 1 : 0;
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeCooperative;
   attr[0].val.cooperative = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.gridDim = dim3(grid, 1, 1);
   cfg.blockDim = dim3(kDecLayerThreads, 1, 1);
-  cfg.dynamicSmemBytes = static_cast<size_t>(p.k + 1) * p.h_ld * sizeof(float);
+  cfg.dynamicSmemBytes = p.p3_stage ? S.staged : S.unstaged;
   cfg.stream = stream;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_layer_kernel<WF, R, KMAX>, p);
+  cfg.numAttrs = pdl ? 2 : 1;
+  return cudaLaunchKernelEx(&cfg, decode_layer_kernel<WF, R>, p);
 }
 
-template <int WF>
-static cudaError_t launch_layer_wf(const DecodeParams &p, int grid, cudaStream_t stream) {
-  if (p.E <= 256) {
-    if (p.k <= 2) return launch_layer<WF, 8, 2>(p, grid, stream);
-    if (p.k <= 8) return launch_layer<WF, 8, 8>(p, grid, stream);
-    return launch_layer<WF, 8, 32>(p, grid, stream);
-  }
-  if (p.k <= 8) return launch_layer<WF, 32, 8>(p, grid, stream);
-  return launch_layer<WF, 32, 32>(p, grid, stream);
+cudaError_t launch_decode_layer(const DecodeParams &p, int grid, int smem_limit, bool pdl,
+                                cudaStream_t stream) {
+  if (p.wfmt == 0)
+    return p.E <= 256 ? launch_layer<0, 8>(p, grid, smem_limit, pdl, stream)
+                      : launch_layer<0, 32>(p, grid, smem_limit, pdl, stream);
+  return p.E <= 256 ? launch_layer<1, 8>(p, grid, smem_limit, pdl, stream)
+                    : launch_layer<1, 32>(p, grid, smem_limit, pdl, stream);
 }
 
-cudaError_t launch_decode_layer(const DecodeParams &p, int grid, cudaStream_t stream) {
-  return p.wfmt == 0 ? launch_layer_wf<0>(p, grid, stream) : launch_layer_wf<1>(p, grid, stream);
-}
-
-template <int WF, int R, int KMAX>
-static cudaError_t configure_one(int bytes) {
-  return cudaFuncSetAttribute(decode_layer_kernel<WF, R, KMAX>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-}
-
-cudaError_t decode_configure(int max_smem_floats) {
-  // Allow more than 48 KB of dynamic shared memory for large (k+1)*Imax.
-  const int bytes = max_smem_floats * static_cast<int>(sizeof(float));
+cudaError_t decode_configure(int *smem_limit) {
+  // Opt every instantiation into the device's largest dynamic shared memory;
+  // each launch then asks for what its shape needs.
+  int dev = 0, optin = 0;
   cudaError_t e;
-  if ((e = configure_one<0, 8, 2>(bytes)) || (e = configure_one<0, 8, 8>(bytes)) ||
-      (e = configure_one<0, 8, 32>(bytes)) || (e = configure_one<0, 32, 8>(bytes)) ||
-      (e = configure_one<0, 32, 32>(bytes)) || (e = configure_one<1, 8, 2>(bytes)) ||
-      (e = configure_one<1, 8, 8>(bytes)) || (e = configure_one<1, 8, 32>(bytes)) ||
-      (e = configure_one<1, 32, 8>(bytes)) || (e = configure_one<1, 32, 32>(bytes)))
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) !=
+      cudaSuccess)
     return e;
+  const int bytes = optin - 1024;   // room for the kernel's static shared memory
+  if ((e = cudaFuncSetAttribute(decode_layer_kernel<0, 8>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) ||
+      (e = cudaFuncSetAttribute(decode_layer_kernel<0, 32>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) ||
+      (e = cudaFuncSetAttribute(decode_layer_kernel<1, 8>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) ||
+      (e = cudaFuncSetAttribute(decode_layer_kernel<1, 32>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)))
+    return e;
+  *smem_limit = bytes;
   return cudaSuccess;
 }
 
 int decode_layer_grid(int num_sms) {
-  int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_layer_kernel<0, 8, 8>,
-                                                    kDecLayerThreads, 20 * 1024) != cudaSuccess ||
-      per_sm < 1)
-    per_sm = 1;
-  cudaGetLastError();
   return num_sms;   // one CTA per SM: every CTA must be co-resident
 }
 

@@ -26,7 +26,7 @@ constexpr int kMaxDevices = 64;
 std::mutex g_setup_mutex;
 unsigned char *g_scratch_addr[kMaxDevices] = {};   // device address of the array, per device
 int g_grid[kMaxDevices] = {};                       // cooperative decode grid, per device
-int g_configured_floats[kMaxDevices] = {};          // shared-memory opt-in done for this size
+int g_smem_limit[kMaxDevices] = {};                 // decode kernel's shared-memory limit, per device
 
 size_t align256(size_t v) { return (v + 255) / 256 * 256; }
 
@@ -82,13 +82,12 @@ extern "C" moe_status moe_forward_decode_noalloc(const moe_config *cfg, const mo
   const ScratchLayout L = scratch_layout(*cfg);
   if (L.total > kNoAllocScratchBytes) return MOE_ERR_WORKSPACE;   // beyond the fixed scratch
   const int imax = cfg->inter > cfg->shared_inter ? cfg->inter : cfg->shared_inter;
-  const int smem_floats = (cfg->top_k + 1) * imax;
-  if (smem_floats * 4 > 200 * 1024) return MOE_ERR_UNSUPPORTED;
+  if ((cfg->top_k + 1) * imax * 4 > 200 * 1024) return MOE_ERR_UNSUPPORTED;
 
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
   unsigned char *base = nullptr;
-  int grid = 0;
+  int grid = 0, smem_limit = 0;
   {
     // Set-up, once per device and with that device current: the host-side
     // name of the array is not a device address, so ask the runtime for it.
@@ -104,17 +103,19 @@ extern "C" moe_status moe_forward_decode_noalloc(const moe_config *cfg, const mo
         return MOE_ERR_CUDA;
       g_grid[dev] = moe::decode_layer_grid(sms);
     }
-    if (g_configured_floats[dev] < smem_floats) {
-      if (moe::decode_configure(smem_floats) != cudaSuccess) return MOE_ERR_CUDA;
-      g_configured_floats[dev] = smem_floats;
+    if (!g_smem_limit[dev]) {
+      int limit = 0;
+      if (moe::decode_configure(&limit) != cudaSuccess) return MOE_ERR_CUDA;
+      g_smem_limit[dev] = limit;
     }
     base = g_scratch_addr[dev];
     grid = g_grid[dev];
+    smem_limit = g_smem_limit[dev];
   }
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // The grid-barrier words must start at zero; everything else is written
-  // before it is read within the call.
+  // The grid-barrier counter must start at a multiple of the grid (zero);
+  // everything else is written before it is read within the call.
   if (cudaMemsetAsync(base + L.counter, 0, 16, s) != cudaSuccess) return MOE_ERR_CUDA;
 
   moe::DecodeParams p{};
@@ -143,8 +144,8 @@ extern "C" moe_status moe_forward_decode_noalloc(const moe_config *cfg, const mo
   p.g = reinterpret_cast<float *>(base + L.g);
   p.h = reinterpret_cast<float *>(base + L.h);
   p.h_ld = imax;
-  p.counter = reinterpret_cast<unsigned int *>(base + L.counter);
+  p.bar = reinterpret_cast<unsigned long long *>(base + L.counter);
   p.status = reinterpret_cast<int *>(base + L.status);
-  if (moe::launch_decode_layer(p, grid, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (moe::launch_decode_layer(p, grid, smem_limit, true, s) != cudaSuccess) return MOE_ERR_CUDA;
   return MOE_OK;
 }

@@ -129,6 +129,8 @@ struct moe_ctx {
   int gemm_grid = 0;   // CTAs of the persistent grouped-GEMM grid (whole pairs)
   int gemm_prefetch = 0;   // L2 prefetch of the next tile's operands (MOE_GEMM_PREFETCH=1)
   int decode_grid = 0;     // CTAs of the cooperative decode launch
+  int decode_smem = 0;     // dynamic shared-memory limit of the decode kernel
+  bool decode_pdl = true;  // decode launches overlap the previous kernel's tail
   char *ws = nullptr;
   size_t ws_bytes = 0;
   WsLayout L{};
@@ -411,10 +413,11 @@ moe_status enqueue_decode(moe_ctx *ctx, const LayerSlot &ls, const void *x, void
   p.g = ctx->at<float>(L.dec_g);
   p.h = ctx->at<float>(L.dec_h);
   p.h_ld = L.Imax;
-  p.counter = ctx->at<unsigned int>(L.dec_counter);
+  p.bar = ctx->at<unsigned long long>(L.dec_counter);
   p.status = ctx->status();
   ProfScope ps(ctx, K_DEC_LAYER, s);
-  return launched(ctx, launch_decode_layer(p, ctx->decode_grid, s), "decode layer launch");
+  return launched(ctx, launch_decode_layer(p, ctx->decode_grid, ctx->decode_smem, ctx->decode_pdl, s),
+                  "decode layer launch");
 }
 
 }  // namespace
@@ -474,8 +477,9 @@ moe_status moe_ctx_create(const moe_config *cfg, int device, void *workspace, si
   ctx->gemm_grid = gemm_max_grid(sms);
   ctx->decode_grid = decode_layer_grid(sms);
   if (const char *env = std::getenv("MOE_GEMM_PREFETCH")) ctx->gemm_prefetch = std::atoi(env) != 0;
+  if (const char *env = std::getenv("MOE_DECODE_PDL")) ctx->decode_pdl = std::atoi(env) != 0;
   if (
-      (e = decode_configure((cfg->top_k + 1) * L.Imax)) != cudaSuccess ||
+      (e = decode_configure(&ctx->decode_smem)) != cudaSuccess ||
       (e = cudaMemset(ctx->ws + L.status, 0, 256)) != cudaSuccess ||
       (e = cudaMemset(ctx->ws + L.dec_counter, 0, 16)) != cudaSuccess ||
       (e = cudaDeviceSynchronize()) != cudaSuccess) {

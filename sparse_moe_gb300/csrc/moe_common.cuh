@@ -21,6 +21,7 @@ enum : int {
   DEV_TIMEOUT_CONVERTER = 0x105,
   DEV_TIMEOUT_RELAY = 0x106,
   DEV_TIMEOUT_GRID = 0x107,
+  DEV_TIMEOUT_STAGE = 0x108,
 };
 
 // A wait that has not completed within this many SM clock cycles gives up

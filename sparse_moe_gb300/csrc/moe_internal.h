@@ -83,17 +83,23 @@ struct DecodeParams {
   int32_t *idx;              // [k]
   float *w;                  // [k]
   float *g;                  // [1]
-  float *h;                  // [2k * h_ld + h_ld] fp32: gate/up dots [k][2I], shared h [Is]
+  float *h;                  // [(k+1) h_ld] fp32: h of the k experts, then of the shared expert
   int h_ld;                  // max(I, Is)
-  unsigned int *counter;     // grid barrier: count, generation (zero-initialised once)
+  unsigned long long *bar;   // grid-barrier arrival counter (16-byte slot, zeroed once)
   int *status;               // device status word
+  int p3_rows, p3_stage;     // set by launch_decode_layer
 };
 // Floats of the h region a decode needs.
-inline size_t decode_h_floats(int k, int h_ld) { return (2 * static_cast<size_t>(k) + 1) * h_ld; }
-cudaError_t decode_configure(int max_smem_floats);
+inline size_t decode_h_floats(int k, int h_ld) { return (static_cast<size_t>(k) + 1) * h_ld; }
+// Raises the decode kernel's dynamic shared-memory limit on the current
+// device to the device maximum and returns it in *smem_limit.
+cudaError_t decode_configure(int *smem_limit);
 // Co-resident grid of the decode layer kernel.
 int decode_layer_grid(int num_sms);
-// One decode layer (see decode.cu): a cooperative launch of decode_layer_grid CTAs.
-cudaError_t launch_decode_layer(const DecodeParams &p, int grid, cudaStream_t stream);
+// One decode layer (see decode.cu): a cooperative launch of decode_layer_grid
+// CTAs, with at most smem_limit bytes of dynamic shared memory; `pdl` lets it
+// start while the previous kernel in the stream finishes.
+cudaError_t launch_decode_layer(const DecodeParams &p, int grid, int smem_limit, bool pdl,
+                                cudaStream_t stream);
 
 }  // namespace moe
