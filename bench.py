@@ -162,7 +162,7 @@ def bench_decode(args, dev, stream, hbm):
     from sparse_moe_gb300 import MoEContext
     wl = moe_synth.DECODE_INT4 if args.decode_int4 else moe_synth.DECODE_BF16
     s = wl.shape
-    L = wl.n_layers
+    L = args.decode_layers or wl.n_layers
     ctx = MoEContext(s.hidden, s.n_experts, s.top_k, s.inter, s.shared_inter, n_layers=L,
                      max_chunk_rows=16, wfmt=wl.wfmt, device=dev.index)
     layers = []
@@ -300,6 +300,14 @@ def main(args):
     dev = torch.device("cuda", local)
     hbm, tf_burst, tf_sust, peak_src = peaks()
 
+    if args.skip_prefill:
+        # decode only (a diagnostic mode: e.g. a small decode case for a profiler)
+        out = bench_decode(args, dev, torch.cuda.Stream(device=dev), hbm)
+        if rank == 0:
+            print(json.dumps({"metric": METRIC, "value": out["value"], "unit": out["unit"],
+                              "n_gpus": world, "higher_is_better": False, "decode": out}))
+        return 0
+
     from sparse_moe_gb300 import MoEContext
     wl = moe_synth.PREFILL_BF16
     s = wl.shape
@@ -384,6 +392,10 @@ if __name__ == "__main__":
     ap.add_argument("--skip-decode", action="store_true")
     ap.add_argument("--skip-e2e", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
+    ap.add_argument("--skip-prefill", action="store_true",
+                    help="decode measurements only (diagnostic; not the benchmark line)")
+    ap.add_argument("--decode-layers", type=int, default=0,
+                    help="layers in the decode graph (default: the workload's 40)")
     a = ap.parse_args()
     if a.warmup < 3 and a.impl == "ours":
         a.warmup = 3

@@ -23,7 +23,8 @@
 //    up rows, so one MMA produces both halves of 64 SwiGLU outputs per CTA;
 //    the epilogue pairs them through a small shared-memory exchange;
 //  * the weight tile (A) of each k-step is one or two TMA boxes (128-byte
-//    swizzle) prefetched into L2 a tile ahead; the token rows (B) are
+//    swizzle; an L2 prefetch of the next tile's boxes exists but is off by
+//    default, as it measured slower); the token rows (B) are
 //    gathered by a group of warps per pipeline stage with 16-byte cp.async
 //    copies written straight into the same 128-byte-swizzled K-major layout,
 //    so no permuted copy of x is ever written.  (Measured on GB300: TMA
