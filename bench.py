@@ -157,10 +157,42 @@ def run_prefill_e2e(ctx, x_h, y_h, steps, warmup, flush, stream):
     return float(np.sum([a.elapsed_time(b) for a, b in zip(starts, ends)]))
 
 
-def bench_decode(args, dev, stream, hbm):
+def bench_prefill_int4(args, dev, stream, flush, tf_burst):
+    """The int4 (symmetric, group 64) prefill workload at T=4096: weights are
+    dequantised tile by tile inside the grouped GEMMs."""
+    from sparse_moe_gb300 import MoEContext
+    wl = moe_synth.PREFILL_INT4
+    s = wl.shape
+    ctx = MoEContext(s.hidden, s.n_experts, s.top_k, s.inter, s.shared_inter, n_layers=1,
+                     max_chunk_rows=4096, wfmt=wl.wfmt, device=dev.index)
+    w = moe_synth.make_layer(wl, device=dev)
+    ctx.load_weights(0, w)
+    x = moe_synth.make_x(wl, device=dev)
+    y = torch.empty_like(x)
+    steps = max(5, args.steps // 2)
+    total_ms, prof, launches = run_prefill(ctx, x, y, steps, args.warmup, flush, stream)
+    gu_f, dn_f, _ = algorithmic(s, wl.T)
+    kern = {k: {"launches": v[0], "avg_us": v[1] * 1e3 / max(1, v[0])} for k, v in prof.items()}
+    gu_us = kern.get("gateup_swiglu_gemm", {}).get("avg_us", float("nan"))
+    dn_us = kern.get("down_gemm", {}).get("avg_us", float("nan"))
+    out = {"workload": wl.name, "value": wl.T * steps / (total_ms * 1e-3), "unit": "tokens/s",
+           "ms_per_step": total_ms / steps, "steps": steps,
+           "gateup_TFLOPs": gu_f / (gu_us * 1e-6) / 1e12,
+           "gateup_frac_of_bf16_peak": gu_f / (gu_us * 1e-6) / 1e12 / tf_burst,
+           "down_TFLOPs": dn_f / (dn_us * 1e-6) / 1e12, "kernels_us": kern,
+           "gpu_launches": launches}
+    ctx.close()
+    del w
+    torch.cuda.empty_cache()
+    return out
+
+
+def bench_decode(args, dev, stream, hbm, int4=None):
     """40 independent decode layers replayed as one CUDA graph."""
     from sparse_moe_gb300 import MoEContext
-    wl = moe_synth.DECODE_INT4 if args.decode_int4 else moe_synth.DECODE_BF16
+    if int4 is None:
+        int4 = args.decode_int4
+    wl = moe_synth.DECODE_INT4 if int4 else moe_synth.DECODE_BF16
     s = wl.shape
     L = args.decode_layers or wl.n_layers
     ctx = MoEContext(s.hidden, s.n_experts, s.top_k, s.inter, s.shared_inter, n_layers=L,
@@ -370,6 +402,10 @@ def main(args):
                        "d2h_bytes_per_step": wl.T * s.hidden * 2}
     if rank == 0 and not args.skip_decode:
         line["decode"] = bench_decode(args, dev, stream, hbm)
+    if rank == 0 and not args.skip_int4:
+        line["prefill_int4"] = bench_prefill_int4(args, dev, stream, flush, tf_burst)
+        if not args.skip_decode and not args.decode_int4:
+            line["decode_int4"] = bench_decode(args, dev, stream, hbm, int4=True)
     if rank == 0 and not args.skip_cpu:
         line["cpu_baseline"] = cpu_baseline_prefill(x.cpu(), w, s.top_k, args.cpu_sample)
     if rank == 0:
@@ -392,6 +428,8 @@ if __name__ == "__main__":
     ap.add_argument("--skip-decode", action="store_true")
     ap.add_argument("--skip-e2e", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
+    ap.add_argument("--skip-int4", action="store_true",
+                    help="skip the int4 prefill and decode measurements")
     ap.add_argument("--skip-prefill", action="store_true",
                     help="decode measurements only (diagnostic; not the benchmark line)")
     ap.add_argument("--decode-layers", type=int, default=0,

@@ -154,7 +154,11 @@ moe_status moe_route(moe_ctx *ctx, int layer, const void *x, int T,
                      int32_t *sorted_rows, int32_t *pos_of_assign, void *stream);
 
 /* Prefill: y[T, H] = MoE(x[T, H]) for T >= 0 tokens (device bf16 in and out,
- * x and y must not overlap).  T > max_chunk_rows runs chunk by chunk. */
+ * x and y must not overlap).  T > max_chunk_rows runs chunk by chunk
+ * ("Bound temporary memory with prompt chunking").  With int4 weights the
+ * grouped GEMMs dequantise each weight tile in shared memory right before its
+ * MMA ("Dequantize weights during matrix multiplication"): no expanded copy
+ * of the weights is ever written. */
 moe_status moe_forward_prefill(moe_ctx *ctx, int layer, const void *x, int T,
                                void *y, void *stream);
 

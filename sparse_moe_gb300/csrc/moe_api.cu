@@ -103,6 +103,22 @@ bool encode_weight_map(CUtensorMap *m, const void *ptr, uint64_t inner, uint64_t
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2-D matrix of packed int4 codes [outer rows, inner bytes] (two codes per
+// byte along K), unswizzled boxes of {32 bytes (64 codes), box_rows}: the
+// int4 weight tiles, dequantised in shared memory by the GEMM.
+bool encode_code_map(CUtensorMap *m, const void *ptr, uint64_t inner_bytes, uint64_t outer,
+                     uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {inner_bytes, outer};
+  const cuuint64_t strides[1] = {inner_bytes};
+  const cuuint32_t box[2] = {32, box_rows};
+  const cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(ptr), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
 enum KernelId : int {
@@ -127,7 +143,7 @@ struct moe_ctx {
   int device = 0;
   int num_sms = 0;
   int gemm_grid = 0;   // CTAs of the persistent grouped-GEMM grid (whole pairs)
-  int gemm_prefetch = 0;   // L2 prefetch of the next tile's operands (MOE_GEMM_PREFETCH=1)
+  int gemm_prefetch = 0;   // GEMM L2 prefetch bits (MOE_GEMM_PREFETCH; see GemmParams)
   int decode_grid = 0;     // CTAs of the cooperative decode launch
   int decode_smem = 0;     // dynamic shared-memory limit of the decode kernel
   bool decode_pdl = true;  // decode launches overlap the previous kernel's tail
@@ -255,6 +271,7 @@ moe_status enqueue_route(moe_ctx *ctx, const LayerSlot &ls, const void *x, int T
   gp.mode = MODE_ROUTER;
   gp.a_routed = gp.a_shared = ls.w.router_w;
   gp.lda_routed = gp.lda_shared = c.hidden;
+  gp.a_rows_routed = gp.a_rows_shared = c.n_experts;
   gp.b = x;
   gp.ldb = c.hidden;
   gp.block_rows = router_block_rows(ctx, T);
@@ -331,19 +348,26 @@ moe_status enqueue_prefill_chunk(moe_ctx *ctx, const LayerSlot &ls, const void *
   gp.sorted_rows = sorted;
   gp.status = ctx->status();
   gp.prefetch = ctx->gemm_prefetch;
+  const bool int4 = c.wfmt == MOE_W_INT4_SYM_G64;
   // gate/up + SwiGLU -> h
   gp.mode = MODE_GATEUP;
   gp.m_tiles = (L.Imax + gemm_pair_rows() / 2 - 1) / (gemm_pair_rows() / 2);   // 128 SwiGLU outputs per pair
   gp.a_routed = ls.w.gate_up;
   gp.a_shared = ls.w.sh_gate_up;
   gp.lda_routed = gp.lda_shared = c.hidden;
+  gp.a_rows_routed = c.n_experts * 2 * c.inter;
+  gp.a_rows_shared = 2 * c.shared_inter;
   gp.b = x;
   gp.ldb = c.hidden;
   gp.out = ctx->at<void>(L.h);
   gp.out_ld = L.Imax;
+  gp.a_scale_routed = int4 ? ls.w.gate_up_scale : nullptr;
+  gp.a_scale_shared = int4 ? ls.w.sh_gate_up_scale : nullptr;
   {
     ProfScope ps(ctx, K_GATEUP_GEMM, s);
-    st = launched(ctx, launch_tc_gemm(ls.map_gu, ls.map_gu_sh, gp, CONV_NONE, ctx->gemm_grid, s),
+    st = launched(ctx,
+                  launch_tc_gemm(ls.map_gu, ls.map_gu_sh, gp, int4 ? CONV_INT4_TO_BF16 : CONV_NONE,
+                                 ctx->gemm_grid, s),
                   "gate/up gemm launch");
   }
   if (st) return st;
@@ -353,15 +377,20 @@ moe_status enqueue_prefill_chunk(moe_ctx *ctx, const LayerSlot &ls, const void *
   gp.a_shared = ls.w.sh_down;
   gp.lda_routed = c.inter;
   gp.lda_shared = c.shared_inter;
+  gp.a_rows_routed = c.n_experts * c.hidden;
+  gp.a_rows_shared = c.hidden;
   gp.b = ctx->at<void>(L.h);
   gp.ldb = L.Imax;
   gp.m_tiles = (c.hidden + gemm_pair_rows() - 1) / gemm_pair_rows();
   gp.out = ctx->at<void>(L.o);
   gp.out_ld = c.hidden;
+  gp.a_scale_routed = int4 ? ls.w.down_scale : nullptr;
+  gp.a_scale_shared = int4 ? ls.w.sh_down_scale : nullptr;
   {
     ProfScope ps(ctx, K_DOWN_GEMM, s);
     st = launched(ctx,
-                  launch_tc_gemm(ls.map_dn, ls.map_dn_sh, gp, CONV_BF16_TO_F16, ctx->gemm_grid, s),
+                  launch_tc_gemm(ls.map_dn, ls.map_dn_sh, gp,
+                                 int4 ? CONV_INT4_TO_F16 : CONV_BF16_TO_F16, ctx->gemm_grid, s),
                   "down gemm launch");
   }
   if (st) return st;
@@ -476,7 +505,7 @@ moe_status moe_ctx_create(const moe_config *cfg, int device, void *workspace, si
   }
   ctx->gemm_grid = gemm_max_grid(sms);
   ctx->decode_grid = decode_layer_grid(sms);
-  if (const char *env = std::getenv("MOE_GEMM_PREFETCH")) ctx->gemm_prefetch = std::atoi(env) != 0;
+  if (const char *env = std::getenv("MOE_GEMM_PREFETCH")) ctx->gemm_prefetch = std::atoi(env);
   if (const char *env = std::getenv("MOE_DECODE_PDL")) ctx->decode_pdl = std::atoi(env) != 0;
   if (
       (e = decode_configure(&ctx->decode_smem)) != cudaSuccess ||
@@ -529,6 +558,13 @@ moe_status moe_load_weights(moe_ctx *ctx, int layer, const moe_weights *w) {
     ok = ok && encode_weight_map(&ls.map_dn, w->down, c.inter,
                                  static_cast<uint64_t>(c.n_experts) * c.hidden, 128);
     ok = ok && encode_weight_map(&ls.map_dn_sh, w->sh_down, c.shared_inter, c.hidden, 128);
+  } else {
+    ok = ok && encode_code_map(&ls.map_gu, w->gate_up, c.hidden / 2,
+                               static_cast<uint64_t>(c.n_experts) * 2 * c.inter, 64);
+    ok = ok && encode_code_map(&ls.map_gu_sh, w->sh_gate_up, c.hidden / 2, 2 * c.shared_inter, 64);
+    ok = ok && encode_code_map(&ls.map_dn, w->down, c.inter / 2,
+                               static_cast<uint64_t>(c.n_experts) * c.hidden, 128);
+    ok = ok && encode_code_map(&ls.map_dn_sh, w->sh_down, c.shared_inter / 2, c.hidden, 128);
   }
   if (!ok) return fail(ctx, MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed for layer %d", layer);
   ls.loaded = true;
@@ -561,8 +597,6 @@ moe_status moe_forward_prefill(moe_ctx *ctx, int layer, const void *x, int T, vo
   if (T == 0) return MOE_OK;
   if (!x || !y || !aligned16(x) || !aligned16(y))
     return fail(ctx, MOE_ERR_INVALID_ARG, "x/y null or not 16-byte aligned");
-  if (ctx->cfg.wfmt != MOE_W_BF16)
-    return fail(ctx, MOE_ERR_UNSUPPORTED, "int4 prefill is not built yet");
   const size_t row_bytes = static_cast<size_t>(ctx->cfg.hidden) * 2;
   const char *xb = static_cast<const char *>(x);
   char *yb = static_cast<char *>(y);
@@ -612,8 +646,6 @@ moe_status moe_forward_prefill_host(moe_ctx *ctx, int layer, const void *x_host,
   if (T < 0 || (T > 0 && (!x_host || !y_host)))
     return fail(ctx, MOE_ERR_INVALID_ARG, "bad host buffers or T");
   if (T == 0) return MOE_OK;
-  if (ctx->cfg.wfmt != MOE_W_BF16)
-    return fail(ctx, MOE_ERR_UNSUPPORTED, "int4 prefill is not built yet");
   if ((st = ensure_device(ctx))) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const size_t row_bytes = static_cast<size_t>(ctx->cfg.hidden) * 2;

@@ -82,6 +82,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Same, but a thread whose phase is not complete may sleep (up to about
+// kSuspendHintNs) until it completes instead of returning at once, so that
+// waiting warps stop competing for issue slots with working ones.
+constexpr uint32_t kSuspendHintNs = 20000;
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(kSuspendHintNs)
+      : "memory");
+  return ok != 0;
+}
+
 // Waits for the phase of parity `parity` to complete.  Gives up (returns
 // false) when `abort_flag` is raised by another role or when kWaitLimitCycles
 // cycles elapse; in the latter case it raises the flag and records `code` in the
@@ -92,7 +107,7 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = cycles_now();
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_sleep(bar, parity)) return true;
     if (*abort_flag) return false;
     if (cycles_now() - t0 > kWaitLimitCycles) {
       *abort_flag = 1;
@@ -247,6 +262,16 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
       : "memory");
   return ok != 0;
 }
+__device__ __forceinline__ bool mbar_try_wait_cluster_sleep(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(kSuspendHintNs)
+      : "memory");
+  return ok != 0;
+}
 // Bounded wait with cluster-scope acquire (arrivals come from the peer CTA).
 __device__ __forceinline__ bool mbar_wait_bounded_cluster(uint32_t bar, uint32_t parity,
                                                           volatile int *abort_flag, int *status,
@@ -254,7 +279,7 @@ __device__ __forceinline__ bool mbar_wait_bounded_cluster(uint32_t bar, uint32_t
   if (mbar_try_wait_cluster(bar, parity)) return true;
   const long long t0 = cycles_now();
   while (true) {
-    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if (mbar_try_wait_cluster_sleep(bar, parity)) return true;
     if (*abort_flag) return false;
     if (cycles_now() - t0 > kWaitLimitCycles) {
       *abort_flag = 1;

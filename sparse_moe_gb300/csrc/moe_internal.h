@@ -15,8 +15,15 @@ constexpr int kBlockRowsMax = 256;
 constexpr int kRouteBlockTokens = 32;
 
 enum GemmMode : int { MODE_ROUTER = 0, MODE_GATEUP = 1, MODE_DOWN = 2 };
-// In-shared-memory conversion of the weight (A) tile before the MMA.
-enum GemmConv : int { CONV_NONE = 0, CONV_BF16_TO_F16 = 1 };
+// In-shared-memory conversion of the weight (A) tile before the MMA: none,
+// bf16 -> fp16 in place, or int4 codes (symmetric, one bf16 scale per 64
+// along K) -> bf16 / fp16.
+enum GemmConv : int {
+  CONV_NONE = 0,
+  CONV_BF16_TO_F16 = 1,
+  CONV_INT4_TO_BF16 = 2,
+  CONV_INT4_TO_F16 = 3
+};
 
 struct GemmParams {
   int mode;
@@ -24,6 +31,8 @@ struct GemmParams {
   const void *a_shared;      // shared-expert weights for the same role (or = a_routed)
   int lda_routed;            // elements per A row
   int lda_shared;
+  int a_rows_routed;         // rows of the A tensors (rows past them read as zeros)
+  int a_rows_shared;
   const void *b;             // B rows (K-major): x (router, gate/up) or h (down)
   int ldb;                   // elements per B row
   const int4 *blocks;        // grouped modes: {expert (E = shared), row_start, n_rows, 0}
@@ -43,7 +52,9 @@ struct GemmParams {
   int out_ld;                // elements per output row
   const float *bias;         // router bias or null
   int *status;               // device status word
-  int prefetch;              // 1: prefetch the next tile's operand rows into L2
+  int prefetch;              // bit 1: L2-prefetch the next tile's token rows
+  const void *a_scale_routed;   // int4 weights: bf16 scales [rows, K/64] (else null)
+  const void *a_scale_shared;
 };
 
 cudaError_t gemm_configure();

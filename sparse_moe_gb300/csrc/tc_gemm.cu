@@ -74,6 +74,10 @@ constexpr int STAGES = 6;
 constexpr int A_BYTES = BM * BK * 2;            // 16 KB
 constexpr int B_BYTES = BN_HALF * BK * 2;       // 16 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // 32 KB
+// int4 weights: the TMA puts a stage's packed codes (BM rows x BK/2 bytes) in
+// the last 4 KB of the A region, where the finisher dequantises them in place.
+constexpr int A_CODE_BYTES = BM * BK / 2;       // 4 KB
+constexpr int CODE_OFF = A_BYTES - A_CODE_BYTES;
 constexpr int ACC_COLS = 256;                   // one accumulator buffer
 constexpr int TMEM_COLS = 512;                  // two buffers
 // Warp roles (identical in both CTAs of a pair).
@@ -210,6 +214,86 @@ __device__ __forceinline__ void convert_tile_bf16_to_f16(uint32_t tile_addr, int
   }
 }
 
+// In-place dequantisation of one stage's A tile by one warp: row r's int4
+// codes (32 bytes = 64 K values, element 2m in the low nibble of byte m, two's
+// complement) at tile + CODE_OFF + 32 r become q * s_r in bf16 (or fp16) in
+// the 128-byte-swizzled K-major layout the MMA reads.  sreg[j] holds, in lane
+// l, the scale of row 32 j + l.  Lane l writes 16-byte chunk l % 8 (K values
+// 8 (l % 8) .. +7) of rows 32 j + 4 m + l / 8, m = 0..7, batch j = 0..3, and
+// reads batch j + 1's codes before writing batch j.  Batch j's outputs cover
+// bytes [4096 j, 4096 j + 4096) and codes start at CODE_OFF = 12288, so only
+// the last batch overwrites codes, all of which every lane has read by then
+// (the __syncwarp before it).
+//
+// Conversion, two values per 32-bit word: with u = q + 8 in [0, 15], the
+// 16-bit pattern M | u is the number M + u exactly (M = 1024.0 for fp16,
+// 128.0 for bf16, both with unit spacing there), so one packed subtract of
+// M + 8 gives q exactly and one packed multiply by the scale rounds q * s
+// once -- the same value as rounding the exact product (exact in fp16: q * s
+// has at most 11 significant bits).
+template <bool F16>
+__device__ __forceinline__ uint32_t dq_pair(uint32_t lo_nib, uint32_t hi_nib, int h,
+                                            uint32_t s2) {
+  // result byte 0 <- byte h of lo_nib, byte 2 <- byte h of hi_nib (selector
+  // nibbles 0 and 2; bytes 1 and 3 are masked off)
+  const uint32_t sel = static_cast<uint32_t>(h) | (static_cast<uint32_t>(h + 4) << 8);
+  const uint32_t b = __byte_perm(lo_nib, hi_nib, sel) & 0x00FF00FFu;
+  const uint32_t v = b | (F16 ? 0x64006400u : 0x43004300u);
+  uint32_t r;
+  if constexpr (F16) {
+    asm("{\n .reg .b32 t;\n sub.f16x2 t, %1, %2;\n mul.f16x2 %0, t, %3;\n}"
+        : "=r"(r)
+        : "r"(v), "r"(0x64086408u), "r"(s2));
+  } else {
+    asm("{\n .reg .b32 t;\n sub.rn.bf16x2 t, %1, %2;\n mul.rn.bf16x2 %0, t, %3;\n}"
+        : "=r"(r)
+        : "r"(v), "r"(0x43084308u), "r"(s2));
+  }
+  return r;
+}
+
+template <bool F16>
+__device__ __forceinline__ void dequant_tile_int4(uint32_t tile, const float (&sreg)[4], int lane) {
+  const int c = lane & 7, rs = lane >> 3;
+  const uint32_t code0 = tile + CODE_OFF + rs * 32 + c * 4;   // + 1024 j + 128 m
+  uint32_t cur[8], nxt[8];
+#pragma unroll
+  for (int m = 0; m < 8; ++m)
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(cur[m]) : "r"(code0 + 128 * m));
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    if (j < 3) {
+#pragma unroll
+      for (int m = 0; m < 8; ++m)
+        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(nxt[m]) : "r"(code0 + 1024 * (j + 1) + 128 * m));
+    } else {
+      __syncwarp();
+    }
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+      const int r = 32 * j + 4 * m + rs;
+      // the row's scale (held by lane 4 m + l / 8) as a packed pair
+      const float s = __shfl_sync(0xffffffffu, sreg[j], 4 * m + rs);
+      uint32_t s2;
+      if constexpr (F16) asm("cvt.rn.f16x2.f32 %0, %1, %1;" : "=r"(s2) : "f"(s));
+      else asm("cvt.rn.bf16x2.f32 %0, %1, %1;" : "=r"(s2) : "f"(s));
+      const uint32_t w = cur[m];
+      const uint32_t lo = (w & 0x0F0F0F0Fu) ^ 0x08080808u;          // elements 0, 2, 4, 6
+      const uint32_t hi = ((w >> 4) & 0x0F0F0F0Fu) ^ 0x08080808u;   // elements 1, 3, 5, 7
+      uint32_t o[4];
+#pragma unroll
+      for (int h = 0; h < 4; ++h) o[h] = dq_pair<F16>(lo, hi, h, s2);
+      asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(tile + r * 128 + ((c ^ (r & 7)) << 4)),
+                   "r"(o[0]), "r"(o[1]), "r"(o[2]), "r"(o[3])
+                   : "memory");
+    }
+    if (j < 3) {
+#pragma unroll
+      for (int m = 0; m < 8; ++m) cur[m] = nxt[m];
+    }
+  }
+}
+
 // One warp stores a [rows x 32] block of fp16 values (row-major, 64 bytes per
 // row, staged in shared memory at `stage`) to global memory with 16-byte
 // stores: lane l writes row (l / 4) + 8 * pass, columns 8 * (l % 4) .. +7.
@@ -274,38 +358,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
   if (warp == TMA_WARP) {
     // ------------------------------------------------ weight tiles (TMA) --
     // Lane 0 loads each k-step's 128 weight rows of this CTA with TMA into
-    // the stage's A region (complete_tx on the local full barrier); all lanes
-    // prefetch the next tile's weight rows (all of K) into L2 first, since
-    // they stream from DRAM and one SM cannot keep enough requests in flight
-    // to cover its latency.
-    const __nv_bfloat16 *a_routed = reinterpret_cast<const __nv_bfloat16 *>(p.a_routed);
-    const __nv_bfloat16 *a_shared = reinterpret_cast<const __nv_bfloat16 *>(p.a_shared);
-    auto prefetch_a = [&](int tile_id) {
-      if (!p.prefetch || tile_id >= ntiles) return;
-      const Tile u = decode_tile(p, tile_id, rank);
-      if (!u.valid) return;
-      const __nv_bfloat16 *ab = u.shared ? a_shared : a_routed;
-      const int ld = u.shared ? p.lda_shared : p.lda_routed;
-      const uint32_t kbytes = static_cast<uint32_t>(u.nk * BK * 2);
-      const int half = (p.mode == MODE_GATEUP) ? 64 : BM;
-      for (int r = lane; r < BM; r += 32) {
-        const int rr = (r < half) ? r : r - half;
-        if (rr >= u.a_valid_rows) continue;
-        const int row = (p.mode == MODE_GATEUP) ? ((r < 64) ? u.a_row + rr : u.a_row2 + rr)
-                                                : u.a_row + r;
-        prefetch_l2_bulk(ab + static_cast<size_t>(row) * ld, kbytes);
-      }
-    };
+    // the stage's A region (complete_tx on the local full barrier); int4
+    // codes land packed at CODE_OFF for the stage finisher to expand.
+    // (Measured on GB300 and not kept: prefetching the weight rows into L2
+    // ahead of the boxes, by TMA or by plain prefetches, and loading part or
+    // all of the weight tile with cp.async from the stage producers -- each
+    // was slower than plain TMA boxes.)
+    constexpr bool INT4 = (CONV == CONV_INT4_TO_BF16 || CONV == CONV_INT4_TO_F16);
+    constexpr int kx = INT4 ? BK / 2 : BK;   // box x extent per k-step (bytes / elements)
     int stage = 0;
     uint32_t phase = 0;
     int issued_parity[STAGES];
 #pragma unroll
     for (int s2 = 0; s2 < STAGES; ++s2) issued_parity[s2] = -1;
     int ok = 1;
-    if (pair_id < ntiles) prefetch_a(pair_id);
     for (int tile = pair_id; tile < ntiles && ok; tile += num_pairs) {
       const Tile t = decode_tile(p, tile, rank);
-      prefetch_a(tile + num_pairs);
       if (!t.valid) continue;
       if (lane == 0) {
         const CUtensorMap *amap = t.shared ? &map_a_shared : &map_a_routed;
@@ -319,12 +387,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
           MOE_TADD(0);
           const uint32_t full_bar = smem_u32(&tail->full[stage]);
           const uint32_t a_dst = smem_base + stage * STAGE_BYTES;
-          mbar_arrive_expect_tx(full_bar, A_BYTES);
-          if (p.mode == MODE_GATEUP) {
-            tma_load_2d(a_dst, amap, ks * BK, t.a_row, full_bar);
-            tma_load_2d(a_dst + A_BYTES / 2, amap, ks * BK, t.a_row2, full_bar);
+          if constexpr (INT4) {
+            mbar_arrive_expect_tx(full_bar, A_CODE_BYTES);
+            if (p.mode == MODE_GATEUP) {
+              tma_load_2d(a_dst + CODE_OFF, amap, ks * kx, t.a_row, full_bar);
+              tma_load_2d(a_dst + CODE_OFF + A_CODE_BYTES / 2, amap, ks * kx, t.a_row2, full_bar);
+            } else {
+              tma_load_2d(a_dst + CODE_OFF, amap, ks * kx, t.a_row, full_bar);
+            }
           } else {
-            tma_load_2d(a_dst, amap, ks * BK, t.a_row, full_bar);
+            mbar_arrive_expect_tx(full_bar, A_BYTES);
+            if (p.mode == MODE_GATEUP) {
+              tma_load_2d(a_dst, amap, ks * kx, t.a_row, full_bar);
+              tma_load_2d(a_dst + A_BYTES / 2, amap, ks * kx, t.a_row2, full_bar);
+            } else {
+              tma_load_2d(a_dst, amap, ks * kx, t.a_row, full_bar);
+            }
           }
           issued_parity[stage] = static_cast<int>(phase);
           if (++stage == STAGES) {
@@ -353,7 +431,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     // bytes), each warp of the group every B_WARPS_PER_STAGE-th group of four
     // rows, waits for its own copies, fences them for the tensor core and
     // arrives on the stage's full barrier.  Lane l copies 16-byte chunk l % 8
-    // of rows 4 j + l / 8.
+    // of rows 4 j + l / 8.  (Weight tiles stay on TMA: loading them with
+    // cp.async from these warps measured 1.6x slower.)
     const int bw = warp - B_WARP0;
     const int g = bw / B_WARPS_PER_STAGE;
     const int gq = bw - g * B_WARPS_PER_STAGE;
@@ -366,7 +445,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     const uint32_t empty_bar = smem_u32(&tail->empty[g]);
     const int btid = bw * 32 + lane;
     auto prefetch_b = [&](int tile_id) {
-      if (!p.prefetch || tile_id >= ntiles) return;
+      if (!(p.prefetch & 2) || tile_id >= ntiles) return;
       const Tile u = decode_tile(p, tile_id, rank);
       if (!u.valid) return;
       const uint32_t kbytes = static_cast<uint32_t>(u.nk * BK * 2);
@@ -462,8 +541,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
           }
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + acc * ACC_COLS;
-          const uint32_t idesc = (CONV == CONV_BF16_TO_F16) ? idesc_f16_f32(PAIR_M, t.nmma)
-                                                            : idesc_bf16_f32(PAIR_M, t.nmma);
+          const uint32_t idesc = (CONV == CONV_BF16_TO_F16 || CONV == CONV_INT4_TO_F16)
+                                     ? idesc_f16_f32(PAIR_M, t.nmma)
+                                     : idesc_bf16_f32(PAIR_M, t.nmma);
           for (int ks = 0; ks < t.nk; ++ks) {
             MOE_T0();
             const bool r_ok = mbar_wait_bounded_cluster(smem_u32(&tail->ready[stage]), phase,
@@ -519,6 +599,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     // then tells the pair leader that this CTA's half of the stage is ready.
     // One warp per stage keeps the cross-CTA signalling of successive stages
     // overlapped.
+    constexpr bool INT4 = (CONV == CONV_INT4_TO_BF16 || CONV == CONV_INT4_TO_F16);
     const int f = warp - FIN_WARP0;
     const uint32_t ready_bar = smem_u32(&tail->ready[f]);
     const uint32_t ready_leader = mapa_shared(ready_bar, 0);
@@ -527,9 +608,32 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     for (int tile = pair_id; tile < ntiles && ok; tile += num_pairs) {
       const Tile t = decode_tile(p, tile, rank);
       if (!t.valid) continue;
+      // int4: scale row of A row 32 j + lane (rows past the operator's end
+      // get scale 0)
+      const __nv_bfloat16 *sbase = static_cast<const __nv_bfloat16 *>(
+          t.shared ? p.a_scale_shared : p.a_scale_routed);
+      int srow[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int r = 32 * j + lane;
+        if (p.mode == MODE_GATEUP) {
+          const int rr = r & 63;
+          srow[j] = rr < t.a_valid_rows ? ((r < 64) ? t.a_row : t.a_row2) + rr : -1;
+        } else {
+          srow[j] = r < t.a_valid_rows ? t.a_row + r : -1;
+        }
+      }
       for (int ks = 0; ks < t.nk; ++ks, ++it) {
         if ((it % STAGES) != f) continue;
         const uint32_t phase = static_cast<uint32_t>(it / STAGES) & 1u;
+        float sreg[4];
+        if constexpr (INT4) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            sreg[j] = srow[j] >= 0
+                          ? __bfloat162float(__ldg(sbase + static_cast<size_t>(srow[j]) * t.nk + ks))
+                          : 0.0f;
+        }
         int got = 1;
         if (lane == 0) {
           MOE_T0();
@@ -542,9 +646,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
           ok = false;
           break;
         }
-        if (CONV == CONV_BF16_TO_F16) {
+        if constexpr (CONV == CONV_BF16_TO_F16) {
           convert_tile_bf16_to_f16(smem_base + f * STAGE_BYTES, lane);
           fence_proxy_async_smem();
+        } else if constexpr (INT4) {
+#ifdef MOE_TRACE
+          const long long _td = clock64();
+#endif
+          dequant_tile_int4<CONV == CONV_INT4_TO_F16>(smem_base + f * STAGE_BYTES, sreg, lane);
+          fence_proxy_async_smem();
+#ifdef MOE_TRACE
+          if (lane == 0)
+            atomicAdd(&g_moe_trace[p.mode][blockIdx.x & 1023][15],
+                      static_cast<unsigned long long>(clock64() - _td));
+#endif
         }
         __syncwarp();
         if (lane == 0) {
@@ -695,13 +810,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
 
 
 cudaError_t gemm_configure() {
-  cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<CONV_NONE>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(kGemmSmemBytes));
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(tc_gemm_kernel<CONV_BF16_TO_F16>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              static_cast<int>(kGemmSmemBytes));
+  const int bytes = static_cast<int>(kGemmSmemBytes);
+  cudaError_t e;
+  if ((e = cudaFuncSetAttribute(tc_gemm_kernel<CONV_NONE>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) ||
+      (e = cudaFuncSetAttribute(tc_gemm_kernel<CONV_BF16_TO_F16>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) ||
+      (e = cudaFuncSetAttribute(tc_gemm_kernel<CONV_INT4_TO_BF16>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) ||
+      (e = cudaFuncSetAttribute(tc_gemm_kernel<CONV_INT4_TO_F16>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)))
+    return e;
+  return cudaSuccess;
 }
 
 int gemm_pair_rows() { return PAIR_M; }
@@ -732,12 +852,23 @@ cudaError_t launch_tc_gemm(const CUtensorMap &a_routed, const CUtensorMap &a_sha
                            const GemmParams &p, int conv, int grid, cudaStream_t stream) {
   grid &= ~1;   // whole CTA pairs
   if (grid < 2) grid = 2;
-  if (conv == CONV_BF16_TO_F16)
-    tc_gemm_kernel<CONV_BF16_TO_F16>
-        <<<grid, NUM_THREADS, kGemmSmemBytes, stream>>>(a_routed, a_shared, p);
-  else
-    tc_gemm_kernel<CONV_NONE>
-        <<<grid, NUM_THREADS, kGemmSmemBytes, stream>>>(a_routed, a_shared, p);
+  switch (conv) {
+    case CONV_BF16_TO_F16:
+      tc_gemm_kernel<CONV_BF16_TO_F16>
+          <<<grid, NUM_THREADS, kGemmSmemBytes, stream>>>(a_routed, a_shared, p);
+      break;
+    case CONV_INT4_TO_BF16:
+      tc_gemm_kernel<CONV_INT4_TO_BF16>
+          <<<grid, NUM_THREADS, kGemmSmemBytes, stream>>>(a_routed, a_shared, p);
+      break;
+    case CONV_INT4_TO_F16:
+      tc_gemm_kernel<CONV_INT4_TO_F16>
+          <<<grid, NUM_THREADS, kGemmSmemBytes, stream>>>(a_routed, a_shared, p);
+      break;
+    default:
+      tc_gemm_kernel<CONV_NONE>
+          <<<grid, NUM_THREADS, kGemmSmemBytes, stream>>>(a_routed, a_shared, p);
+  }
   return cudaGetLastError();
 }
 

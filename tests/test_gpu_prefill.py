@@ -133,3 +133,50 @@ def test_prefill_host_buffers_match_device_path():
     ctx.forward_prefill_host(0, x_h, y_h)
     torch.cuda.synchronize()
     assert torch.equal(y_h, y_dev.cpu())
+
+
+# ---- int4 weights (symmetric, group 64): dequantised inside the GEMMs; the
+# oracle applies the same dequant definition in fp64.
+
+def _wl4(shape, T, bias=None, seed=0):
+    return moe_synth.Workload("t4", shape, T=T, bias_std=bias, seed=seed, wfmt=moe_synth.WFMT_INT4)
+
+
+@pytest.mark.parametrize("T", [1, 16, 1000])
+def test_prefill_int4_tiny(T):
+    wl = _wl4(moe_synth.TINY, T, bias=1.5 if T > 16 else None, seed=40 + T)
+    ctx, (w,) = make_ctx(wl, max_chunk_rows=1024)
+    x = moe_synth.make_x(wl, device="cuda")
+    y = ctx.forward_prefill(0, x)
+    torch.cuda.synchronize()
+    assert_layer_close(y.float().cpu().numpy(), _oracle_y(ctx, w, x), int4=True,
+                       what=f"tiny int4 T={T}")
+
+
+def test_prefill_int4_qwen_ragged_full():
+    wl = _wl4(moe_synth.QWEN, 300, bias=1.5, seed=9)
+    ctx, (w,) = make_ctx(wl)
+    x = moe_synth.make_x(wl, device="cuda")
+    y = ctx.forward_prefill(0, x)
+    torch.cuda.synchronize()
+    assert_layer_close(y.float().cpu().numpy(), _oracle_y(ctx, w, x), int4=True,
+                       what="qwen int4 T=300")
+
+
+def test_prefill_int4_4096_sampled_tokens():
+    """The int4 prefill workload at full size: routing in full, the layer on
+    sampled tokens."""
+    wl = moe_synth.PREFILL_INT4
+    ctx, (w,) = make_ctx(wl)
+    x = moe_synth.make_x(wl, device="cuda")
+    y = ctx.forward_prefill(0, x)
+    torch.cuda.synchronize()
+    check_routing(ctx, w, x)
+    rng = np.random.default_rng(1)
+    tokens = np.unique(np.concatenate([[0, 4095], rng.choice(4096, 30, replace=False)]))
+    ref = _oracle_y(ctx, w, x, tokens=tokens)
+    assert_layer_close(y[tokens].float().cpu().numpy(), ref, int4=True,
+                       what="qwen int4 T=4096 sampled")
+    y2 = ctx.forward_prefill(0, x)
+    torch.cuda.synchronize()
+    assert torch.equal(y, y2)
