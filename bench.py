@@ -45,6 +45,9 @@ def peaks():
 
 # --------------------------------------------------------------- clocks --
 class ClockSampler:
+    """nvidia-smi samples every 20 ms on a reader thread, each stamped with the
+    host time it arrived; `mark_start` / `mark_end` bracket the timed region
+    and `stop` keeps only the samples that fall inside it."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -52,28 +55,50 @@ class ClockSampler:
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
+        self.lines = []
+        self.t0 = self.t1 = None
 
     def start(self):
+        import threading
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "50"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
+            return
+
+        def reader():
+            for line in self.proc.stdout:
+                self.lines.append((time.perf_counter(), line))
+        threading.Thread(target=reader, daemon=True).start()
+        deadline = time.perf_counter() + 10.0
+        while not self.lines and time.perf_counter() < deadline:   # sampling has begun
+            time.sleep(0.01)
+
+    def mark_start(self):
+        self.t0 = time.perf_counter()
+
+    def mark_end(self):
+        self.t1 = time.perf_counter()
 
     def stop(self) -> dict:
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.05)
         self.proc.terminate()
         try:
-            out, _ = self.proc.communicate(timeout=5)
+            self.proc.wait(timeout=5)
         except Exception:
             self.proc.kill()
-            out, _ = self.proc.communicate()
+        t0 = self.t0 if self.t0 is not None else -1e30
+        t1 = self.t1 if self.t1 is not None else 1e30
         sm, smax, reasons, power = [], [], set(), []
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in out.strip().splitlines():
+        for ts, line in list(self.lines):
+            if not (t0 <= ts <= t1 + 0.02):
+                continue
             f = [c.strip() for c in line.split(",")]
             if len(f) < 9:
                 continue
@@ -87,11 +112,11 @@ class ClockSampler:
                 if v.lower() == "active":
                     reasons.add(n)
         if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
-        busy = [s for s, p in zip(sm, power) if p > 300.0] or sm
-        return {"sm_mhz": float(np.median(busy)), "sm_max_mhz": float(max(smax)),
-                "reasons": sorted(reasons), "samples": len(sm), "samples_under_load": len(busy),
-                "power_w_max": float(max(power))}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples in the timed region"],
+                    "samples": 0}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(smax)),
+                "reasons": sorted(reasons), "samples": len(sm), "power_w_max": float(max(power)),
+                "window_s": (t1 - t0) if self.t0 is not None and self.t1 is not None else None}
 
 
 # ------------------------------------------------------------- workload --
@@ -118,7 +143,7 @@ def decode_bytes(s: moe_synth.Shape, int4: bool):
                 total=routed_gu + routed_dn + shared + router + 2 * H * 2)
 
 
-def run_prefill(ctx, x, y, steps, warmup, flush, stream):
+def run_prefill(ctx, x, y, steps, warmup, flush, stream, clocks=None):
     for _ in range(warmup):
         ctx.forward_prefill(0, x, y, stream=stream)
     torch.cuda.synchronize()
@@ -127,6 +152,8 @@ def run_prefill(ctx, x, y, steps, warmup, flush, stream):
     launches0 = ctx.launch_count
     ctx.profile(True)
     torch.cuda.synchronize()
+    if clocks is not None:
+        clocks.mark_start()
     with torch.cuda.stream(stream):
         for i in range(steps):
             flush.zero_()
@@ -134,6 +161,8 @@ def run_prefill(ctx, x, y, steps, warmup, flush, stream):
             ctx.forward_prefill(0, x, y, stream=stream)
             ends[i].record(stream)
     torch.cuda.synchronize()
+    if clocks is not None:
+        clocks.mark_end()
     prof = ctx.profile_read()
     ctx.profile(False)
     launches = ctx.launch_count - launches0
@@ -318,18 +347,23 @@ def bench_decode(args, dev, stream, hbm, int4=None):
     return out
 
 
-def cpu_baseline_prefill(x_cpu, w_dev, k, sample_tokens):
-    """The fp64 oracle, as it stands, on the first `sample_tokens` tokens."""
+def cpu_baseline_prefill(x_cpu, w_dev, k, min_seconds=10.0, max_passes=32):
+    """The fp64 oracle, as it stands, over the whole prefill workload, repeated
+    until about `min_seconds` of CPU work have been timed."""
     from oracle import moe_oracle as orc
     layer = moe_synth.to_numpy(w_dev)
-    xs = x_cpu[:sample_tokens].float().numpy()
+    xs = x_cpu.float().numpy()
     t0 = time.perf_counter()
-    orc.moe_layer(xs, layer, k)
+    passes = 0
+    while passes < max_passes and (passes == 0 or time.perf_counter() - t0 < min_seconds):
+        orc.moe_layer(xs, layer, k)
+        passes += 1
     dt = time.perf_counter() - t0
-    return {"value": sample_tokens / dt, "unit": "tokens/s", "cores": os.cpu_count(),
-            "kind": "oracle",
-            "sample": f"fp64 oracle (router, top-k, grouping, all experts, shared expert) on the "
-                      f"first {sample_tokens} of the {x_cpu.shape[0]} tokens; {dt:.1f} s",
+    T = xs.shape[0]
+    return {"value": T * passes / dt, "unit": "tokens/s", "cores": os.cpu_count(),
+            "threads": torch.get_num_threads(), "kind": "oracle",
+            "sample": f"fp64 oracle (router, top-k, grouping, all experts, shared expert) over all "
+                      f"{T} tokens of the workload, {passes} pass(es), {dt:.1f} s",
             "seconds": dt}
 
 
@@ -344,6 +378,16 @@ def main_reference(args):
     w = moe_synth.to_numpy(moe_synth.make_layer(wl, device=dev))
     x = moe_synth.make_x(wl, device=dev).float().cpu().numpy()
     S = args.ref_sample
+    # keep the whole run within a few minutes: shrink the per-step sample if
+    # one step of S tokens would make K + W steps take longer than ~150 s
+    t0 = time.perf_counter()
+    orc.moe_layer(x[:S], w, wl.shape.top_k)
+    t_step = time.perf_counter() - t0
+    while S > 16 and t_step * (args.steps + args.warmup) > 150.0:
+        S //= 2
+        t0 = time.perf_counter()
+        orc.moe_layer(x[:S], w, wl.shape.top_k)
+        t_step = time.perf_counter() - t0
     for i in range(args.warmup):
         orc.moe_layer(x[(i * S) % wl.T:(i * S) % wl.T + S], w, wl.shape.top_k)
     t0 = time.perf_counter()
@@ -402,7 +446,8 @@ def main(args):
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    total_ms, prof, launches = run_prefill(ctx, x, y, args.steps, args.warmup, flush, stream)
+    total_ms, prof, launches = run_prefill(ctx, x, y, args.steps, args.warmup, flush, stream,
+                                           clocks)
     torch.cuda.synchronize()
     if world > 1:
         t = torch.tensor([total_ms], device=dev)
@@ -455,7 +500,7 @@ def main(args):
         if not args.skip_decode and not args.decode_int4:
             line["decode_int4"] = bench_decode(args, dev, stream, hbm, int4=True)
     if rank == 0 and not args.skip_cpu:
-        line["cpu_baseline"] = cpu_baseline_prefill(x.cpu(), w, s.top_k, args.cpu_sample)
+        line["cpu_baseline"] = cpu_baseline_prefill(x.cpu(), w, s.top_k)
     if rank == 0:
         print(json.dumps(line))
     if world > 1:
@@ -467,11 +512,11 @@ def main(args):
 if __name__ == "__main__":
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--cpu-sample", type=int, default=256)
-    ap.add_argument("--ref-sample", type=int, default=32)
+    ap.add_argument("--ref-sample", type=int, default=128,
+                    help="tokens per step of the reference arm (the oracle on the host cores)")
     ap.add_argument("--decode-int4", action="store_true")
     ap.add_argument("--skip-decode", action="store_true")
     ap.add_argument("--skip-e2e", action="store_true")

@@ -127,6 +127,18 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
       : "memory");
 }
 
+// Same, for a CTA pair: the box lands in this CTA's shared memory at dst and
+// its bytes complete on the mbarrier at `bar_cluster`, which may be the peer
+// CTA's (a shared::cluster address, e.g. from mapa).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap *map, int c0,
+                                                 int c1, uint32_t bar_cluster) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar_cluster)
+      : "memory");
+}
+
 // Four rows (r0..r3) of `map`, each one box wide starting at column c0, land
 // contiguously at dst.  The map's box is {cols, 1}.
 __device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap *map, int c0, int r0,

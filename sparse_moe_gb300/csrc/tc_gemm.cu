@@ -32,9 +32,13 @@
 //    per SM; one warp of cp.async sustains about 7 bytes/clock; a single-SM
 //    128 x 256 tile would need 96 bytes/clock, the pair needs 64.)
 //  * the pair's CTAs walk the device-built tile list persistently; one thread
-//    of the leader issues the MMAs once both CTAs' stage is ready (a finisher
-//    warp per stage and CTA forwards readiness, the peer's with a
-//    cluster-scope release-arrive, so successive stages signal in parallel);
+//    of the leader issues the MMAs once both CTAs' stage is ready.  Without a
+//    conversion (router, bf16 gate/up) both CTAs' TMA boxes complete on the
+//    leader's full barrier (cta_group::2 loads) and the peer's token-row
+//    warps arrive on it remotely, so readiness needs no relay; when the
+//    weight tile must be converted first (down, int4), a finisher warp per
+//    stage and CTA converts it and forwards readiness to the leader, the
+//    peer's with a cluster-scope release-arrive;
 //    four epilogue warps
 //    per CTA drain their half of the double-buffered TMEM accumulator while
 //    the next tile computes, and transpose each 32x16 piece through shared
@@ -327,7 +331,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
   const int num_pairs = gridDim.x >> 1;
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(smem_u32(&tail->full[s]), 1 + B_WARPS_PER_STAGE);
+      // unconverted modes: the leader's full barrier also counts the peer's
+      // producers (and both CTAs' TMA bytes); otherwise each CTA's own
+      mbar_init(smem_u32(&tail->full[s]),
+                CONV == CONV_NONE ? 1 + 2 * B_WARPS_PER_STAGE : 1 + B_WARPS_PER_STAGE);
       mbar_init(smem_u32(&tail->ready[s]), 2);
       mbar_init(smem_u32(&tail->empty[s]), 1);
     }
@@ -395,6 +402,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
             } else {
               tma_load_2d(a_dst + CODE_OFF, amap, ks * kx, t.a_row, full_bar);
             }
+          } else if constexpr (CONV == CONV_NONE) {
+            // Both CTAs' boxes complete on the leader's full barrier, which
+            // expects the pair's bytes: no relay from the peer is needed.
+            const uint32_t lead_full = mapa_shared(full_bar, 0);
+            if (rank == 0) mbar_arrive_expect_tx(full_bar, 2 * A_BYTES);
+            if (p.mode == MODE_GATEUP) {
+              tma_load_2d_pair(a_dst, amap, ks * kx, t.a_row, lead_full);
+              tma_load_2d_pair(a_dst + A_BYTES / 2, amap, ks * kx, t.a_row2, lead_full);
+            } else {
+              tma_load_2d_pair(a_dst, amap, ks * kx, t.a_row, lead_full);
+            }
           } else {
             mbar_arrive_expect_tx(full_bar, A_BYTES);
             if (p.mode == MODE_GATEUP) {
@@ -404,7 +422,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
               tma_load_2d(a_dst, amap, ks * kx, t.a_row, full_bar);
             }
           }
-          issued_parity[stage] = static_cast<int>(phase);
+          // (the peer's boxes in the unconverted modes complete on the
+          // leader's barrier: nothing local to wait for on abort)
+          if (!(CONV == CONV_NONE && rank == 1)) issued_parity[stage] = static_cast<int>(phase);
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1;
@@ -513,7 +533,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
 #endif
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(full_bar);
+        if (lane == 0) {
+          if (CONV == CONV_NONE && rank == 1) mbar_arrive_cluster(mapa_shared(full_bar, 0));
+          else mbar_arrive(full_bar);
+        }
       }
     }
     __syncwarp();
@@ -546,7 +569,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
                                      : idesc_bf16_f32(PAIR_M, t.nmma);
           for (int ks = 0; ks < t.nk; ++ks) {
             MOE_T0();
-            const bool r_ok = mbar_wait_bounded_cluster(smem_u32(&tail->ready[stage]), phase,
+            // unconverted modes: both CTAs' producers signal this CTA's full
+            // barrier directly; otherwise the stage finishers' ready barrier
+            const uint32_t stage_bar = CONV == CONV_NONE ? smem_u32(&tail->full[stage])
+                                                         : smem_u32(&tail->ready[stage]);
+            const bool r_ok = mbar_wait_bounded_cluster(stage_bar, phase,
                                                         abort_flag, p.status, DEV_TIMEOUT_MMA);
             MOE_TADD(2);
             if (!r_ok) {
@@ -601,11 +628,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     // overlapped.
     constexpr bool INT4 = (CONV == CONV_INT4_TO_BF16 || CONV == CONV_INT4_TO_F16);
     const int f = warp - FIN_WARP0;
+    // Unconverted modes need no finisher: the producers signal the leader.
+    const int ntiles_fin = CONV == CONV_NONE ? 0 : ntiles;
     const uint32_t ready_bar = smem_u32(&tail->ready[f]);
     const uint32_t ready_leader = mapa_shared(ready_bar, 0);
     int it = 0;
     bool ok = true;
-    for (int tile = pair_id; tile < ntiles && ok; tile += num_pairs) {
+    for (int tile = pair_id; tile < ntiles_fin && ok; tile += num_pairs) {
       const Tile t = decode_tile(p, tile, rank);
       if (!t.valid) continue;
       // int4: scale row of A row 32 j + lane (rows past the operator's end
