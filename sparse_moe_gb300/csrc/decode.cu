@@ -37,6 +37,14 @@ constexpr int kDecWarps = kDecLayerThreads / 32;
 // moe_debug_read_decode_trace().
 #ifdef MOE_TRACE
 __device__ long long g_dec_trace[1024][16];
+// global-timer stamps per launch (ring of 64 launches, by barrier epoch):
+// [start, after the programmatic-launch wait, end] per CTA
+__device__ unsigned long long g_dec_gt[64][160][3];
+__device__ __forceinline__ unsigned long long gtimer() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
 #define DEC_MARK(i) \
   if (threadIdx.x == 0) g_dec_trace[blockIdx.x & 1023][i] = clock64()
 // same, read only after `dep` has been computed
@@ -454,6 +462,9 @@ __global__ void __launch_bounds__(kDecLayerThreads, 1) decode_layer_kernel(const
   const uint32_t mb_sh = smem_u32(&mbar[0]), mb_rt = smem_u32(&mbar[1]);
 
   DEC_MARK(0);
+#ifdef MOE_TRACE
+  const unsigned long long gt_start = gtimer();
+#endif
   unsigned long long base = 0;   // barrier counter at launch (used by thread 0)
   if (threadIdx.x == 0) {
     // With a programmatic launch this CTA can start while the previous
@@ -485,6 +496,9 @@ __global__ void __launch_bounds__(kDecLayerThreads, 1) decode_layer_kernel(const
     }
   }
   pdl_wait();
+#ifdef MOE_TRACE
+  const unsigned long long gt_wait = gtimer();
+#endif
 
   // ---- phase A: router rows, the shared gate row, shared-expert row pairs
   for (int it = gw; it < nA; it += nw) {
@@ -622,6 +636,14 @@ __global__ void __launch_bounds__(kDecLayerThreads, 1) decode_layer_kernel(const
   DEC_MARK(9);
   DEC_MARK(10);
 #ifdef MOE_TRACE
+  if (threadIdx.x == 0 && blockIdx.x < 160) {
+    const int slot = static_cast<int>((base / (2ull * G)) % 64);
+    g_dec_gt[slot][blockIdx.x][0] = gt_start;
+    g_dec_gt[slot][blockIdx.x][1] = gt_wait;
+    g_dec_gt[slot][blockIdx.x][2] = gtimer();
+  }
+#endif
+#ifdef MOE_TRACE
   if (threadIdx.x == 0) g_dec_trace[blockIdx.x & 1023][15] = p.p3_stage + 10 * p.p3_rows;
 #endif
 }
@@ -686,6 +708,10 @@ int decode_layer_grid(int num_sms) {
 }  // namespace moe
 
 #ifdef MOE_TRACE
+extern "C" int moe_debug_read_decode_gt(void *dst, size_t bytes) {
+  size_t n = bytes < sizeof(moe::g_dec_gt) ? bytes : sizeof(moe::g_dec_gt);
+  return cudaMemcpyFromSymbol(dst, moe::g_dec_gt, n) == cudaSuccess ? 0 : 1;
+}
 extern "C" int moe_debug_read_decode_trace(void *dst, size_t bytes) {
   size_t n = bytes < sizeof(moe::g_dec_trace) ? bytes : sizeof(moe::g_dec_trace);
   return cudaMemcpyFromSymbol(dst, moe::g_dec_trace, n) == cudaSuccess ? 0 : 1;

@@ -99,9 +99,18 @@ constexpr int EPI_STAGE_BYTES = 4 * 16 * 64;    // per epilogue warp: 16 rows x 
 // B_WARPS_PER_STAGE-th group of four rows of up to 128).
 constexpr int kRowTab = 4 * ((BN_HALF / 4 + B_WARPS_PER_STAGE - 1) / B_WARPS_PER_STAGE);
 
+// Warps that convert one stage's weight tile: for bf16 -> fp16 the stage's
+// finisher and its two token-row producers (each a share of the chunks); for
+// int4 the finisher alone (splitting the in-place dequantisation measured
+// slower).
+constexpr int kConvTeam = 1 + B_WARPS_PER_STAGE;
+template <int CONV> __host__ __device__ constexpr int conv_team() {
+  return CONV == CONV_BF16_TO_F16 ? kConvTeam : 1;
+}
+
 struct SmemTail {
   uint64_t full[STAGES];        // local: TMA (A) + this CTA's B warps
-  uint64_t ready[STAGES];       // leader: both CTAs' stage finishers
+  uint64_t ready[STAGES];       // leader: both CTAs' conversion teams
   uint64_t empty[STAGES];       // local: arrives from the leader's commit
   uint64_t tmem_full[2];        // local: arrives from the leader's commit
   uint64_t tmem_empty[2];       // leader: 4 + 4 epilogue warps
@@ -194,41 +203,6 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-// In-place bf16 -> fp16 conversion of one 128x64 A tile (1024 16-byte
-// chunks) by one warp.
-__device__ __forceinline__ void convert_tile_bf16_to_f16(uint32_t tile_addr, int lane) {
-#pragma unroll 4
-  for (int i = 0; i < (A_BYTES / 16) / 32; ++i) {
-    const uint32_t addr = tile_addr + (lane + i * 32) * 16;
-    uint32_t w0, w1, w2, w3;
-    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(w0), "=r"(w1), "=r"(w2), "=r"(w3)
-                 : "r"(addr));
-    uint32_t o[4];
-    const uint32_t wi[4] = {w0, w1, w2, w3};
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const float lo = __uint_as_float(wi[j] << 16);
-      const float hi = __uint_as_float(wi[j] & 0xffff0000u);
-      asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(o[j]) : "f"(hi), "f"(lo));
-    }
-    asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(o[0]), "r"(o[1]),
-                 "r"(o[2]), "r"(o[3])
-                 : "memory");
-  }
-}
-
-// In-place dequantisation of one stage's A tile by one warp: row r's int4
-// codes (32 bytes = 64 K values, element 2m in the low nibble of byte m, two's
-// complement) at tile + CODE_OFF + 32 r become q * s_r in bf16 (or fp16) in
-// the 128-byte-swizzled K-major layout the MMA reads.  sreg[j] holds, in lane
-// l, the scale of row 32 j + l.  Lane l writes 16-byte chunk l % 8 (K values
-// 8 (l % 8) .. +7) of rows 32 j + 4 m + l / 8, m = 0..7, batch j = 0..3, and
-// reads batch j + 1's codes before writing batch j.  Batch j's outputs cover
-// bytes [4096 j, 4096 j + 4096) and codes start at CODE_OFF = 12288, so only
-// the last batch overwrites codes, all of which every lane has read by then
-// (the __syncwarp before it).
-//
 // Conversion, two values per 32-bit word: with u = q + 8 in [0, 15], the
 // 16-bit pattern M | u is the number M + u exactly (M = 1024.0 for fp16,
 // 128.0 for bf16, both with unit spacing there), so one packed subtract of
@@ -256,6 +230,17 @@ __device__ __forceinline__ uint32_t dq_pair(uint32_t lo_nib, uint32_t hi_nib, in
   return r;
 }
 
+// In-place dequantisation of one stage's A tile by one warp: row r's int4
+// codes (32 bytes = 64 K values, element 2m in the low nibble of byte m, two's
+// complement) at tile + CODE_OFF + 32 r become q * s_r in bf16 (or fp16) in
+// the 128-byte-swizzled K-major layout the MMA reads.  sreg[j] holds, in lane
+// l, the scale of row 32 j + l.  Lane l writes 16-byte chunk l % 8 (K values
+// 8 (l % 8) .. +7) of rows 32 j + 4 m + l / 8, m = 0..7, batch j = 0..3, and
+// reads batch j + 1's codes before writing batch j.  Batch j's outputs cover
+// bytes [4096 j, 4096 j + 4096) and codes start at CODE_OFF = 12288, so only
+// the last batch overwrites codes, all of which every lane has read by then
+// (the __syncwarp before it).
+//
 template <bool F16>
 __device__ __forceinline__ void dequant_tile_int4(uint32_t tile, const float (&sreg)[4], int lane) {
   const int c = lane & 7, rs = lane >> 3;
@@ -298,6 +283,88 @@ __device__ __forceinline__ void dequant_tile_int4(uint32_t tile, const float (&s
   }
 }
 
+// Warp q's share of the in-place bf16 -> fp16 conversion of one stage's A
+// tile (16-byte chunks q * 32 + lane, stepping kConvTeam * 32).
+__device__ __forceinline__ void convert_share_bf16_to_f16(uint32_t tile, int q, int lane) {
+  for (int i = q * 32 + lane; i < A_BYTES / 16; i += kConvTeam * 32) {
+    const uint32_t addr = tile + i * 16;
+    uint32_t w0, w1, w2, w3;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(w0), "=r"(w1), "=r"(w2), "=r"(w3)
+                 : "r"(addr));
+    uint32_t o[4];
+    const uint32_t wi[4] = {w0, w1, w2, w3};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float lo = __uint_as_float(wi[j] << 16);
+      const float hi = __uint_as_float(wi[j] & 0xffff0000u);
+      asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(o[j]) : "f"(hi), "f"(lo));
+    }
+    asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(o[0]), "r"(o[1]),
+                 "r"(o[2]), "r"(o[3])
+                 : "memory");
+  }
+}
+
+// Scale rows (int4) of A rows 32 j + lane of a tile; rows past the
+// operator's end get -1 (scale 0).
+__device__ __forceinline__ void tile_scale_rows(const GemmParams &p, const Tile &t, int lane,
+                                                int (&srow)[4]) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int r = 32 * j + lane;
+    if (p.mode == MODE_GATEUP) {
+      const int rr = r & 63;
+      srow[j] = rr < t.a_valid_rows ? ((r < 64) ? t.a_row : t.a_row2) + rr : -1;
+    } else {
+      srow[j] = r < t.a_valid_rows ? t.a_row + r : -1;
+    }
+  }
+}
+
+// int4: the scales of this k-step for A rows 32 j + lane (0 past the end).
+__device__ __forceinline__ void load_stage_scales(const GemmParams &p, const Tile &t, int ks,
+                                                  int lane, float (&sreg)[4]) {
+  int srow[4];
+  tile_scale_rows(p, t, lane, srow);
+  const __nv_bfloat16 *sbase =
+      static_cast<const __nv_bfloat16 *>(t.shared ? p.a_scale_shared : p.a_scale_routed);
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    sreg[j] = srow[j] >= 0 ? __bfloat162float(__ldg(sbase + static_cast<size_t>(srow[j]) * t.nk + ks))
+                           : 0.0f;
+}
+
+// Team warp q's part of a converting stage: a bounded wait for the stage to
+// be full, its share of the conversion (int4: with the scales in sreg, loaded
+// earlier by the caller), and its arrival on the pair leader's ready barrier.
+// Returns false on a timeout or abort.
+template <int CONV>
+__device__ __forceinline__ bool convert_stage(const GemmParams &p, const float (&sreg)[4], int stage,
+                                              uint32_t phase, int q, int rank, uint32_t smem_base,
+                                              SmemTail *tail, volatile int *abort_flag, int lane) {
+  constexpr bool INT4 = (CONV == CONV_INT4_TO_BF16 || CONV == CONV_INT4_TO_F16);
+  int got = 1;
+  if (lane == 0)
+    got = mbar_wait_bounded(smem_u32(&tail->full[stage]), phase, abort_flag, p.status,
+                            DEV_TIMEOUT_CONVERTER);
+  if (!__shfl_sync(0xffffffffu, got, 0)) return false;
+  const uint32_t tile = smem_base + stage * STAGE_BYTES;
+  if constexpr (CONV == CONV_BF16_TO_F16) {
+    convert_share_bf16_to_f16(tile, q, lane);
+  } else if constexpr (INT4) {
+    dequant_tile_int4<CONV == CONV_INT4_TO_F16>(tile, sreg, lane);
+  }
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    const uint32_t ready = smem_u32(&tail->ready[stage]);
+    if (rank == 0) mbar_arrive(ready);
+    else mbar_arrive_cluster(mapa_shared(ready, 0));
+  }
+  return true;
+}
+
 // One warp stores a [rows x 32] block of fp16 values (row-major, 64 bytes per
 // row, staged in shared memory at `stage`) to global memory with 16-byte
 // stores: lane l writes row (l / 4) + 8 * pass, columns 8 * (l % 4) .. +7.
@@ -335,7 +402,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       // producers (and both CTAs' TMA bytes); otherwise each CTA's own
       mbar_init(smem_u32(&tail->full[s]),
                 CONV == CONV_NONE ? 1 + 2 * B_WARPS_PER_STAGE : 1 + B_WARPS_PER_STAGE);
-      mbar_init(smem_u32(&tail->ready[s]), 2);
+      mbar_init(smem_u32(&tail->ready[s]), 2 * conv_team<CONV>());
       mbar_init(smem_u32(&tail->empty[s]), 1);
     }
     for (int a = 0; a < 2; ++a) {
@@ -537,6 +604,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
           if (CONV == CONV_NONE && rank == 1) mbar_arrive_cluster(mapa_shared(full_bar, 0));
           else mbar_arrive(full_bar);
         }
+        if constexpr (CONV == CONV_BF16_TO_F16) {
+          // this warp's share of the stage's conversion (team warps 1, 2)
+          const float sreg[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+          if (!convert_stage<CONV>(p, sreg, g, phase, 1 + gq, rank, smem_base, tail, abort_flag,
+                                   lane)) {
+            ok = false;
+            break;
+          }
+        }
       }
     }
     __syncwarp();
@@ -621,79 +697,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     __syncwarp();
   } else if (warp >= FIN_WARP0) {
     // --------------------------------------------------- stage finishers --
-    // Finisher warp f owns pipeline stage f: once this CTA's stage is full it
-    // (in the converting mode) turns the bf16 weight tile into fp16 in place,
-    // then tells the pair leader that this CTA's half of the stage is ready.
-    // One warp per stage keeps the cross-CTA signalling of successive stages
-    // overlapped.
-    constexpr bool INT4 = (CONV == CONV_INT4_TO_BF16 || CONV == CONV_INT4_TO_F16);
-    const int f = warp - FIN_WARP0;
+    // Finisher warp f owns pipeline stage f.  In the converting modes it is
+    // warp 0 of the stage's conversion team (with the stage's two token-row
+    // producers): once this CTA's stage is full it converts its share of the
+    // weight tile in place and arrives on the pair leader's ready barrier.
     // Unconverted modes need no finisher: the producers signal the leader.
+    const int f = warp - FIN_WARP0;
     const int ntiles_fin = CONV == CONV_NONE ? 0 : ntiles;
-    const uint32_t ready_bar = smem_u32(&tail->ready[f]);
-    const uint32_t ready_leader = mapa_shared(ready_bar, 0);
     int it = 0;
     bool ok = true;
     for (int tile = pair_id; tile < ntiles_fin && ok; tile += num_pairs) {
       const Tile t = decode_tile(p, tile, rank);
       if (!t.valid) continue;
-      // int4: scale row of A row 32 j + lane (rows past the operator's end
-      // get scale 0)
-      const __nv_bfloat16 *sbase = static_cast<const __nv_bfloat16 *>(
-          t.shared ? p.a_scale_shared : p.a_scale_routed);
-      int srow[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int r = 32 * j + lane;
-        if (p.mode == MODE_GATEUP) {
-          const int rr = r & 63;
-          srow[j] = rr < t.a_valid_rows ? ((r < 64) ? t.a_row : t.a_row2) + rr : -1;
-        } else {
-          srow[j] = r < t.a_valid_rows ? t.a_row + r : -1;
-        }
-      }
       for (int ks = 0; ks < t.nk; ++ks, ++it) {
         if ((it % STAGES) != f) continue;
         const uint32_t phase = static_cast<uint32_t>(it / STAGES) & 1u;
-        float sreg[4];
-        if constexpr (INT4) {
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-            sreg[j] = srow[j] >= 0
-                          ? __bfloat162float(__ldg(sbase + static_cast<size_t>(srow[j]) * t.nk + ks))
-                          : 0.0f;
-        }
-        int got = 1;
-        if (lane == 0) {
-          MOE_T0();
-          got = mbar_wait_bounded(smem_u32(&tail->full[f]), phase, abort_flag, p.status,
-                                  DEV_TIMEOUT_CONVERTER);
-          MOE_TADD(14);
-        }
-        got = __shfl_sync(0xffffffffu, got, 0);
-        if (!got) {
+        float sreg[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        if constexpr (CONV == CONV_INT4_TO_BF16 || CONV == CONV_INT4_TO_F16)
+          load_stage_scales(p, t, ks, lane, sreg);
+        if (!convert_stage<CONV>(p, sreg, f, phase, 0, rank, smem_base, tail, abort_flag, lane)) {
           ok = false;
           break;
-        }
-        if constexpr (CONV == CONV_BF16_TO_F16) {
-          convert_tile_bf16_to_f16(smem_base + f * STAGE_BYTES, lane);
-          fence_proxy_async_smem();
-        } else if constexpr (INT4) {
-#ifdef MOE_TRACE
-          const long long _td = clock64();
-#endif
-          dequant_tile_int4<CONV == CONV_INT4_TO_F16>(smem_base + f * STAGE_BYTES, sreg, lane);
-          fence_proxy_async_smem();
-#ifdef MOE_TRACE
-          if (lane == 0)
-            atomicAdd(&g_moe_trace[p.mode][blockIdx.x & 1023][15],
-                      static_cast<unsigned long long>(clock64() - _td));
-#endif
-        }
-        __syncwarp();
-        if (lane == 0) {
-          if (rank == 0) mbar_arrive(ready_bar);
-          else mbar_arrive_cluster(ready_leader);
         }
       }
     }
