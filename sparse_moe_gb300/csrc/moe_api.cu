@@ -23,7 +23,7 @@ size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 struct WsLayout {
   int Tc, nblk, R, Imax, max_blocks;
-  size_t status, logits, idx, w, mask, base, counts, offsets, sorted, pos, blocks, nblocks, h, o;
+  size_t status, logits, idx, w, gate, mask, base, counts, offsets, sorted, pos, blocks, nblocks, h, o;
   size_t dec_logits, dec_idx, dec_w, dec_g, dec_h, dec_counter, x_stage, y_stage, total;
 };
 
@@ -46,6 +46,7 @@ WsLayout make_layout(const moe_config &c) {
   L.logits = take(Tc * E * 4);
   L.idx = take(Tc * k * 4);
   L.w = take(Tc * k * 4);
+  L.gate = take(Tc * 4);
   L.mask = take(static_cast<size_t>(L.nblk) * E * 4);
   L.base = take(static_cast<size_t>(L.nblk) * E * 4);
   L.counts = take(E * 4);
@@ -301,7 +302,10 @@ moe_status enqueue_route(moe_ctx *ctx, const LayerSlot &ls, const void *x, int T
   int32_t *base = ctx->at<int32_t>(L.base);
   {
     ProfScope ps(ctx, K_TOPK, s);
-    st = launched(ctx, launch_topk(logits, T, c.n_experts, c.top_k, idx, w, mask, s), "topk launch");
+    st = launched(ctx,
+                  launch_topk(logits, x, ls.w.sh_gate_w, T, c.n_experts, c.top_k, c.hidden, idx, w,
+                              mask, ctx->at<float>(L.gate), s),
+                  "topk launch");
   }
   if (st) return st;
   const int nblk = (T + kRouteBlockTokens - 1) / kRouteBlockTokens;
@@ -397,7 +401,7 @@ moe_status enqueue_prefill_chunk(moe_ctx *ctx, const LayerSlot &ls, const void *
   {
     ProfScope ps(ctx, K_COMBINE, s);
     st = launched(ctx,
-                  launch_combine(x, ls.w.sh_gate_w, ctx->at<void>(L.o), pos, w, T, c.hidden,
+                  launch_combine(ctx->at<float>(L.gate), ctx->at<void>(L.o), pos, w, T, c.hidden,
                                  c.top_k, y, s),
                   "combine launch");
   }

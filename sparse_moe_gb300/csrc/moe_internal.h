@@ -66,8 +66,9 @@ cudaError_t launch_tc_gemm(const CUtensorMap &a_routed, const CUtensorMap &a_sha
                            const GemmParams &p, int conv, int grid, cudaStream_t stream);
 
 // Routing: top-k + masks, block scan + block map, stable scatter.
-cudaError_t launch_topk(const float *logits, int T, int E, int k, int32_t *idx, float *w,
-                        uint32_t *blk_mask, cudaStream_t stream);
+cudaError_t launch_topk(const float *logits, const void *x, const void *wsg, int T, int E, int k,
+                        int H, int32_t *idx, float *w, uint32_t *blk_mask, float *gate,
+                        cudaStream_t stream);
 cudaError_t launch_scan(const uint32_t *blk_mask, int nblk, int T, int E, int k,
                         int32_t *counts, int32_t *offsets, int32_t *blk_base, int4 *blocks,
                         int32_t *n_blocks, cudaStream_t stream);
@@ -75,10 +76,9 @@ cudaError_t launch_scatter(const int32_t *idx, const uint32_t *blk_mask, const i
                            const int32_t *offsets, int T, int E, int k, int32_t *sorted_rows,
                            int32_t *pos_of_assign, cudaStream_t stream);
 
-// y[t] = sum_j w[t,j] o[pos(t,j)] + sigmoid(x[t].w_sg) o[T*k + t]
-cudaError_t launch_combine(const void *x, const void *sh_gate_w, const void *o,
-                           const int32_t *pos, const float *w, int T, int H, int k, void *y,
-                           cudaStream_t stream);
+// y[t] = sum_j w[t,j] o[pos(t,j)] + g[t] o[T*k + t]
+cudaError_t launch_combine(const float *gate, const void *o, const int32_t *pos, const float *w,
+                           int T, int H, int k, void *y, cudaStream_t stream);
 
 // Batch-1 decode.
 struct DecodeParams {

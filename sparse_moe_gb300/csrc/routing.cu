@@ -16,57 +16,76 @@
 namespace moe {
 
 // ----------------------------------------------------------------- top-k --
+// One routing block of 32 tokens per CTA, one token per warp: top-k and
+// weights of the token, its bit in the block's per-expert masks, and the
+// shared-expert gate g[t] = sigmoid(x[t] . w_sg) for the combine.
+constexpr int kTopkThreads = 32 * kRouteBlockTokens;
+
 template <int R>
-__global__ void __launch_bounds__(256) topk_kernel(const float *__restrict__ logits, int T, int E,
-                                                   int k, int32_t *__restrict__ idx,
-                                                   float *__restrict__ w,
-                                                   uint32_t *__restrict__ blk_mask) {
+__global__ void __launch_bounds__(kTopkThreads) topk_kernel(
+    const float *__restrict__ logits, const __nv_bfloat16 *__restrict__ x,
+    const __nv_bfloat16 *__restrict__ wsg, int T, int E, int k, int H, int32_t *__restrict__ idx,
+    float *__restrict__ w, uint32_t *__restrict__ blk_mask, float *__restrict__ gate) {
   __shared__ uint32_t mask_s[1024];
   for (int e = threadIdx.x; e < E; e += blockDim.x) mask_s[e] = 0;
   __syncthreads();
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  constexpr int kTokPerWarp = kRouteBlockTokens / 8;
-  for (int i = 0; i < kTokPerWarp; ++i) {
-    const int tl = warp * kTokPerWarp + i;
-    const int t = blockIdx.x * kRouteBlockTokens + tl;
-    if (t >= T) break;
+  const int tl = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * kRouteBlockTokens + tl;
+  if (t < T) {
     float v[R];
     const float *row = logits + static_cast<size_t>(t) * E;
 #pragma unroll
     for (int r = 0; r < R; ++r) {
       const int e = lane + 32 * r;
-      v[r] = (e < E) ? row[e] : -INFINITY;
+      v[r] = (e < E) ? __ldcs(row + e) : 0.0f;
     }
-    float sv, sw;
+    // the shared gate's dot product, loads in flight with the logits
+    const uint4 *x4 = reinterpret_cast<const uint4 *>(x + static_cast<size_t>(t) * H);
+    const uint4 *g4 = reinterpret_cast<const uint4 *>(wsg);
+    float d = 0.0f;
+    for (int c = lane; c < H / 8; c += 32) {
+      const uint4 xv = x4[c], gv = __ldg(g4 + c);
+      const uint32_t xa[4] = {xv.x, xv.y, xv.z, xv.w}, ga[4] = {gv.x, gv.y, gv.z, gv.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        d = fmaf(bf16_lo(xa[i]), bf16_lo(ga[i]), d);
+        d = fmaf(bf16_hi(xa[i]), bf16_hi(ga[i]), d);
+      }
+    }
     int se;
-    warp_topk<R>(v, E, k, sv, se, sw);
+    float sw;
+    warp_topk_redux<R>(v, E, k, se, sw);
     if (lane < k) {
       idx[static_cast<size_t>(t) * k + lane] = se;
       w[static_cast<size_t>(t) * k + lane] = sw;
       atomicOr(&mask_s[se], 1u << tl);
     }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
+    if (lane == 0) gate[t] = sigmoid_f(d);
   }
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += blockDim.x)
     blk_mask[static_cast<size_t>(blockIdx.x) * E + e] = mask_s[e];
 }
 
-cudaError_t launch_topk(const float *logits, int T, int E, int k, int32_t *idx, float *w,
-                        uint32_t *blk_mask, cudaStream_t stream) {
+cudaError_t launch_topk(const float *logits, const void *x, const void *wsg, int T, int E, int k,
+                        int H, int32_t *idx, float *w, uint32_t *blk_mask, float *gate,
+                        cudaStream_t stream) {
   const int nblk = (T + kRouteBlockTokens - 1) / kRouteBlockTokens;
   const int R = (E + 31) / 32;
-  if (R <= 1)
-    topk_kernel<1><<<nblk, 256, 0, stream>>>(logits, T, E, k, idx, w, blk_mask);
-  else if (R <= 2)
-    topk_kernel<2><<<nblk, 256, 0, stream>>>(logits, T, E, k, idx, w, blk_mask);
-  else if (R <= 4)
-    topk_kernel<4><<<nblk, 256, 0, stream>>>(logits, T, E, k, idx, w, blk_mask);
-  else if (R <= 8)
-    topk_kernel<8><<<nblk, 256, 0, stream>>>(logits, T, E, k, idx, w, blk_mask);
-  else if (R <= 16)
-    topk_kernel<16><<<nblk, 256, 0, stream>>>(logits, T, E, k, idx, w, blk_mask);
-  else
-    topk_kernel<32><<<nblk, 256, 0, stream>>>(logits, T, E, k, idx, w, blk_mask);
+  const __nv_bfloat16 *xb = static_cast<const __nv_bfloat16 *>(x);
+  const __nv_bfloat16 *gb = static_cast<const __nv_bfloat16 *>(wsg);
+#define MOE_TOPK(RR)                                                                     \
+  topk_kernel<RR><<<nblk, kTopkThreads, 0, stream>>>(logits, xb, gb, T, E, k, H, idx, w, \
+                                                     blk_mask, gate)
+  if (R <= 1) MOE_TOPK(1);
+  else if (R <= 2) MOE_TOPK(2);
+  else if (R <= 4) MOE_TOPK(4);
+  else if (R <= 8) MOE_TOPK(8);
+  else if (R <= 16) MOE_TOPK(16);
+  else MOE_TOPK(32);
+#undef MOE_TOPK
   return cudaGetLastError();
 }
 
@@ -119,6 +138,7 @@ __global__ void __launch_bounds__(1024) scan_kernel(const uint32_t *__restrict__
   const int b1 = active ? static_cast<int>((static_cast<long long>(nblk) * (pi + 1)) / P) : 0;
   // 1. histogram: rows of expert e in my range of routing blocks
   int s = 0;
+#pragma unroll 8
   for (int b = b0; b < b1; ++b) s += __popc(blk_mask[static_cast<size_t>(b) * E + e]);
   part[tid] = s;
   __syncthreads();
@@ -137,6 +157,7 @@ __global__ void __launch_bounds__(1024) scan_kernel(const uint32_t *__restrict__
   // 3. per-block bases inside each expert segment
   if (active) {
     int run = part[tid];
+#pragma unroll 8
     for (int b = b0; b < b1; ++b) {
       blk_base[static_cast<size_t>(b) * E + e] = run;
       run += __popc(blk_mask[static_cast<size_t>(b) * E + e]);
@@ -205,17 +226,18 @@ cudaError_t launch_scatter(const int32_t *idx, const uint32_t *blk_mask, const i
 }
 
 // --------------------------------------------------------------- combine --
-// y[t] = sum_j w[t,j] * o[pos(t,j)] + sigmoid(x[t] . w_sg) * o[T*k + t], fp32
-// accumulation in fixed slot order (o holds the per-expert outputs in fp16) (section "Reduce intermediate and state
-// traffic": the output projection combined with its routing score and the
-// shared-expert result).  No atomics: each output element is written once.
-__global__ void __launch_bounds__(256) combine_kernel(const __nv_bfloat16 *__restrict__ x,
-                                                      const __nv_bfloat16 *__restrict__ wsg,
+// y[t] = sum_j w[t,j] * o[pos(t,j)] + g[t] * o[T*k + t], fp32 accumulation in
+// fixed slot order (o holds the per-expert outputs in fp16; g[t] comes from
+// the top-k kernel) (section "Reduce intermediate and state traffic": the
+// output projection combined with its routing score and the shared-expert
+// result).  No atomics: each output element is written once.  For k <= KF
+// all of a chunk's loads are issued before its arithmetic.
+template <int KF>
+__global__ void __launch_bounds__(256) combine_kernel(const float *__restrict__ gate,
                                                       const __half *__restrict__ o,
                                                       const int32_t *__restrict__ pos,
                                                       const float *__restrict__ w, int T, int H,
                                                       int k, __nv_bfloat16 *__restrict__ y) {
-  __shared__ float red[8];
   __shared__ int pos_s[32];
   __shared__ float w_s[32];
   const int t = blockIdx.x;
@@ -224,65 +246,60 @@ __global__ void __launch_bounds__(256) combine_kernel(const __nv_bfloat16 *__res
     pos_s[threadIdx.x] = pos[static_cast<size_t>(t) * k + threadIdx.x];
     w_s[threadIdx.x] = w[static_cast<size_t>(t) * k + threadIdx.x];
   }
-  // shared-expert gate: sigmoid(x[t] . w_sg)
-  const uint4 *x4 = reinterpret_cast<const uint4 *>(x + static_cast<size_t>(t) * H);
-  const uint4 *g4 = reinterpret_cast<const uint4 *>(wsg);
-  float d = 0.0f;
-  for (int c = threadIdx.x; c < nchunk; c += blockDim.x) {
-    const uint4 xv = x4[c], gv = __ldg(g4 + c);
-    const uint32_t xa[4] = {xv.x, xv.y, xv.z, xv.w}, ga[4] = {gv.x, gv.y, gv.z, gv.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      d = fmaf(bf16_lo(xa[i]), bf16_lo(ga[i]), d);
-      d = fmaf(bf16_hi(xa[i]), bf16_hi(ga[i]), d);
-    }
-  }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = d;
   __syncthreads();
-  float dot = 0.0f;
-  for (int i = 0; i < static_cast<int>(blockDim.x >> 5); ++i) dot += red[i];
-  const float gate = sigmoid_f(dot);
-
+  const float g = __ldg(gate + t);
   const size_t shared_row = static_cast<size_t>(T) * k + t;
   for (int c = threadIdx.x; c < nchunk; c += blockDim.x) {
     float acc[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
-    for (int j = 0; j < k; ++j) {
-      const uint4 ov = *reinterpret_cast<const uint4 *>(o + static_cast<size_t>(pos_s[j]) * H + c * 8);
-      const float wj = w_s[j];
-      const uint32_t oa[4] = {ov.x, ov.y, ov.z, ov.w};
+    uint4 ov[KF > 0 ? KF : 1];
+    if constexpr (KF > 0) {
+#pragma unroll
+      for (int j = 0; j < KF; ++j)
+        ov[j] = j < k ? __ldcs(reinterpret_cast<const uint4 *>(o + static_cast<size_t>(pos_s[j]) * H + c * 8))
+                      : make_uint4(0, 0, 0, 0);
+    }
+    const uint4 sv = __ldcs(reinterpret_cast<const uint4 *>(o + shared_row * H + c * 8));
+    auto add = [&](const uint4 oj, float wj) {
+      const uint32_t oa[4] = {oj.x, oj.y, oj.z, oj.w};
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const float2 f = half2_to_float2(oa[i]);
         acc[2 * i] = fmaf(wj, f.x, acc[2 * i]);
         acc[2 * i + 1] = fmaf(wj, f.y, acc[2 * i + 1]);
       }
+    };
+    if constexpr (KF > 0) {
+#pragma unroll
+      for (int j = 0; j < KF; ++j)
+        if (j < k) add(ov[j], w_s[j]);
+    } else {
+      for (int j = 0; j < k; ++j)
+        add(*reinterpret_cast<const uint4 *>(o + static_cast<size_t>(pos_s[j]) * H + c * 8), w_s[j]);
     }
-    const uint4 sv = *reinterpret_cast<const uint4 *>(o + shared_row * H + c * 8);
     const uint32_t sa[4] = {sv.x, sv.y, sv.z, sv.w};
     uint4 out;
     uint32_t *oo = reinterpret_cast<uint32_t *>(&out);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const float2 f = half2_to_float2(sa[i]);
-      const float lo = fmaf(gate, f.x, acc[2 * i]);
-      const float hi = fmaf(gate, f.y, acc[2 * i + 1]);
+      const float lo = fmaf(g, f.x, acc[2 * i]);
+      const float hi = fmaf(g, f.y, acc[2 * i + 1]);
       oo[i] = pack_bf16x2(lo, hi);
     }
     *reinterpret_cast<uint4 *>(y + static_cast<size_t>(t) * H + c * 8) = out;
   }
 }
 
-cudaError_t launch_combine(const void *x, const void *sh_gate_w, const void *o,
-                           const int32_t *pos, const float *w, int T, int H, int k, void *y,
-                           cudaStream_t stream) {
-  combine_kernel<<<T, 256, 0, stream>>>(
-      reinterpret_cast<const __nv_bfloat16 *>(x), reinterpret_cast<const __nv_bfloat16 *>(sh_gate_w),
-      reinterpret_cast<const __half *>(o), pos, w, T, H, k,
-      reinterpret_cast<__nv_bfloat16 *>(y));
+cudaError_t launch_combine(const float *gate, const void *o, const int32_t *pos, const float *w,
+                           int T, int H, int k, void *y, cudaStream_t stream) {
+  const __half *oh = reinterpret_cast<const __half *>(o);
+  __nv_bfloat16 *yb = reinterpret_cast<__nv_bfloat16 *>(y);
+  if (k <= 8)
+    combine_kernel<8><<<T, 256, 0, stream>>>(gate, oh, pos, w, T, H, k, yb);
+  else
+    combine_kernel<0><<<T, 256, 0, stream>>>(gate, oh, pos, w, T, H, k, yb);
   return cudaGetLastError();
 }
 

@@ -2,62 +2,62 @@
 // softmax ("Qwen creates three distinct workload shapes": the router scores
 // every expert and selects k; the weights are a softmax over all experts
 // renormalised over the selected ones, which equals a softmax over the
-// selected logits).
+// selected logits).  Used by the prefill routing and by the decode kernel.
 #pragma once
-#include <cfloat>
-#include <climits>
 #include "moe_common.cuh"
 
 namespace moe {
 
-// Total order used for selection: larger logit first, equal logits -> lower
-// expert index first.  `eb == INT_MAX` marks "no candidate".
-__device__ __forceinline__ bool topk_better(float va, int ea, float vb, int eb) {
-  return (va > vb) || (va == vb && ea < eb);
+// Order-preserving 32-bit key of a logit (-0 folded into +0 so that equal
+// values compare equal, as floats do).
+__device__ __forceinline__ uint32_t logit_key(float v) {
+  const uint32_t u = __float_as_uint(v + 0.0f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key_logit(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
 }
 
-// Lane l holds logits of experts l, l+32, ... (v[r] for expert l + 32r).
-// After the call, lane j < k holds the j-th selection (value, expert) and
-// its renormalised weight.  Deterministic: the reductions are fixed
-// butterflies, every lane computes the same result.
+// Top-k of the E logits (lane l holds experts l + 32 r in v[r]) in the order
+// larger logit first, equal logits -> lower expert first; then the weights
+// softmax(selected logits), which equal the softmax over all E logits
+// renormalised over the selection ("Qwen creates three distinct workload
+// shapes").  Lane j < k receives selection j: expert sel_e and weight sel_w.
+// Each round takes the warp maximum of the lanes' best keys and the lowest
+// expert holding it with two redux.sync reductions; every lane computes the
+// same result.
 template <int R>
-__device__ __forceinline__ void warp_topk(const float (&v)[R], int E, int k, float &sel_v,
-                                          int &sel_e, float &sel_w) {
+__device__ __forceinline__ void warp_topk_redux(const float (&v)[R], int E, int k, int &sel_e,
+                                                float &sel_w) {
   const int lane = threadIdx.x & 31;
-  uint32_t taken = 0;
+  uint32_t key[R];
 #pragma unroll
-  for (int r = 0; r < R; ++r)
-    if (lane + 32 * r >= E) taken |= 1u << r;
-  sel_v = -FLT_MAX;
+  for (int r = 0; r < R; ++r) key[r] = (lane + 32 * r < E) ? logit_key(v[r]) : 0u;
+  uint32_t sel_key = 0;
   sel_e = 0;
   for (int j = 0; j < k; ++j) {
-    float bv = -INFINITY;
-    int be = INT_MAX;
+    uint32_t bk = key[0];
+    int br = 0;
 #pragma unroll
-    for (int r = 0; r < R; ++r) {
-      const int e = lane + 32 * r;
-      if (!((taken >> r) & 1u) && topk_better(v[r], e, bv, be)) {
-        bv = v[r];
-        be = e;
+    for (int r = 1; r < R; ++r)
+      if (key[r] > bk) {
+        bk = key[r];
+        br = r;
       }
-    }
+    const uint32_t m = __reduce_max_sync(0xffffffffu, bk);
+    const uint32_t e = __reduce_min_sync(0xffffffffu, bk == m ? static_cast<uint32_t>(lane + 32 * br)
+                                                              : 0xffffffffu);
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-      const int oe = __shfl_xor_sync(0xffffffffu, be, off);
-      if (topk_better(ov, oe, bv, be)) {
-        bv = ov;
-        be = oe;
-      }
-    }
-    if ((be & 31) == lane) taken |= 1u << (be >> 5);
+    for (int r = 0; r < R; ++r)
+      key[r] = (e == static_cast<uint32_t>(lane + 32 * r)) ? 0u : key[r];
     if (lane == j) {
-      sel_v = bv;
-      sel_e = be;
+      sel_key = m;
+      sel_e = static_cast<int>(e);
     }
   }
-  const float vmax = __shfl_sync(0xffffffffu, sel_v, 0);
-  const float ex = (lane < k) ? expf(sel_v - vmax) : 0.0f;
+  const float sv = key_logit(sel_key);
+  const float vmax = __shfl_sync(0xffffffffu, sv, 0);
+  const float ex = (lane < k) ? expf(sv - vmax) : 0.0f;
   float sum = ex;
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
