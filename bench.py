@@ -119,6 +119,13 @@ class ClockSampler:
                 "window_s": (t1 - t0) if self.t0 is not None and self.t1 is not None else None}
 
 
+# DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) of
+# the kernels the roofline lines name, from one ncu capture of the current
+# kernels (the summaries under profiles/): gate/up 625.0 + 33.1 MB at the
+# T=4096 prefill workload, decode layer 57.77 + 0.28 MB.
+TRAFFIC_BYTES = {"gateup_swiglu_gemm": 658.1e6, "decode_layer": 58.05e6}
+
+
 # ------------------------------------------------------------- workload --
 def algorithmic(s: moe_synth.Shape, T: int):
     H, E, k, I, Is = s.hidden, s.n_experts, s.top_k, s.inter, s.shared_inter
@@ -332,7 +339,8 @@ def bench_decode(args, dev, stream, hbm, int4=None):
         "expert_stream_frac_of_hbm": nb["expert_stream"] / (us_layer * 1e-6) / 1e9 / hbm,
         "bytes_per_layer": nb["total"],
         "roofline": {"kernel": "decode_layer", "bound": "hbm", "achieved": achieved,
-                     "peak": hbm, "unit": "GB/s", "frac": achieved / hbm, "traffic": None,
+                     "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                     "traffic": None if int4 else TRAFFIC_BYTES["decode_layer"],
                      "algorithmic_bytes_per_launch": nb["total"],
                      "launch_us_eager": lay_us},
         "kernels_eager_us": {k: v[1] * 1e3 / max(1, v[0]) for k, v in prof.items()},
@@ -463,7 +471,8 @@ def main(args):
     dn_us = kern.get("down_gemm", {}).get("avg_us", float("nan"))
     achieved = gu_f / (gu_us * 1e-6) / 1e12
     roofline = {"kernel": "gateup_swiglu_gemm", "bound": "tensor", "achieved": achieved,
-                "peak": tf_burst, "unit": "TFLOP/s", "frac": achieved / tf_burst, "traffic": None,
+                "peak": tf_burst, "unit": "TFLOP/s", "frac": achieved / tf_burst,
+                "traffic": TRAFFIC_BYTES["gateup_swiglu_gemm"],
                 "peak_source": f"{peak_src} bf16 burst",
                 "algorithmic_flops_per_launch": gu_f,
                 "down_gemm_TFLOPs": dn_f / (dn_us * 1e-6) / 1e12,
