@@ -120,6 +120,15 @@ typedef struct {       /* device pointers, borrowed (see Ownership above)      *
   const void  *sh_down;           /* bf16 [H, Is]    | uint8 [H, Is/2]         */
   const void  *sh_down_scale;     /* NULL (bf16)     | bf16  [H, Is/64]        */
   const void  *sh_gate_w;         /* bf16 [H]                                  */
+  /* Optional (bf16 format only; both or neither, else NULL): fp16 copies of
+   * down and sh_down, same shapes, each value the round-to-nearest fp16 of
+   * the bf16 one (moe_convert_bf16_to_f16 writes them).  The prefill down
+   * projection runs on fp16 operands (h is stored in fp16 for its 11
+   * significant bits); given these copies its weight tiles go from TMA
+   * straight to the tensor cores instead of being converted in shared memory
+   * first, with bit-identical results.  Decode never reads them. */
+  const void  *down_f16;          /* fp16 [E, H, I] or NULL                    */
+  const void  *sh_down_f16;       /* fp16 [H, Is]   or NULL                    */
 } moe_weights;
 
 /* Bytes of device workspace a context with this config needs (host only). */
@@ -207,6 +216,15 @@ moe_status moe_forward_decode_host(moe_ctx *ctx, int layer, const void *x_host,
  * shapes the decode kernels do not take, MOE_ERR_CUDA if a CUDA call fails. */
 moe_status moe_forward_decode_noalloc(const moe_config *cfg, const moe_weights *w,
                                       const void *x, void *y, void *stream);
+
+/* dst[i] = fp16(src[i]) for 0 <= i < n: bf16 -> fp16 with round-to-nearest-
+ * even (values beyond the fp16 range become +-inf, bf16 NaN stays NaN), on
+ * the current device, asynchronously on `stream`.  src and dst are device
+ * arrays of n 2-byte elements, 16-byte aligned, not overlapping.  Meant for
+ * the optional down_f16 / sh_down_f16 weight copies.  Returns
+ * MOE_ERR_INVALID_ARG for a null or misaligned pointer with n > 0 (nothing
+ * is launched), MOE_ERR_CUDA if the launch fails; n = 0 is a no-op. */
+moe_status moe_convert_bf16_to_f16(const void *src, void *dst, size_t n, void *stream);
 
 /* Synchronises the device, reads and clears the device status word: MOE_OK,
  * or MOE_ERR_DEVICE_TIMEOUT (a bounded wait ran out; *code, if non-NULL,

@@ -13,7 +13,8 @@ import torch
 
 from . import _abi
 
-__all__ = ["MoEError", "MoEContext", "library", "WFMT"]
+__all__ = ["MoEError", "MoEContext", "library", "WFMT", "convert_bf16_to_f16",
+           "with_f16_down"]
 
 WFMT = {"bf16": _abi.MOE_W_BF16, "int4_sym_g64": _abi.MOE_W_INT4_SYM_G64}
 
@@ -37,6 +38,29 @@ def _stream_handle(stream, device):
     if stream is None:
         stream = torch.cuda.current_stream(device)
     return ctypes.c_void_p(stream.cuda_stream)
+
+
+def convert_bf16_to_f16(src: torch.Tensor, stream=None) -> torch.Tensor:
+    """fp16 copy of a contiguous bf16 CUDA tensor, written by the library's
+    conversion kernel (round to nearest even)."""
+    if src.dtype != torch.bfloat16 or not src.is_cuda or not src.is_contiguous():
+        raise ValueError("src must be a contiguous bf16 CUDA tensor")
+    dst = torch.empty(src.shape, dtype=torch.float16, device=src.device)
+    st = library().moe_convert_bf16_to_f16(_ptr(src), _ptr(dst), src.numel(),
+                                           _stream_handle(stream, src.device))
+    if st != 0:
+        raise MoEError(st, "moe_convert_bf16_to_f16")
+    return dst
+
+
+def with_f16_down(w: dict, stream=None) -> dict:
+    """`w` plus the optional fp16 copies of the bf16 down projections
+    (down_f16, sh_down_f16) that let the prefill down GEMM skip its in-kernel
+    weight conversion."""
+    out = dict(w)
+    out["down_f16"] = convert_bf16_to_f16(w["down"], stream)
+    out["sh_down_f16"] = convert_bf16_to_f16(w["sh_down"], stream)
+    return out
 
 
 class MoEContext:
@@ -91,7 +115,8 @@ class MoEContext:
     def load_weights(self, layer: int, w: dict):
         """`w` holds device tensors in the layout of include/sparse_moe.h
         (keys: router_w, router_b, gate_up, gate_up_scale, down, down_scale,
-        sh_gate_up, sh_gate_up_scale, sh_down, sh_down_scale, sh_gate_w).
+        sh_gate_up, sh_gate_up_scale, sh_down, sh_down_scale, sh_gate_w, and
+        the optional down_f16, sh_down_f16).
         The context borrows them; a reference is kept here."""
         for k, v in w.items():
             if v is not None and (not v.is_cuda or not v.is_contiguous()):

@@ -32,7 +32,8 @@ class MoeConfig(ctypes.Structure):
 class MoeWeights(ctypes.Structure):
     _fields_ = [("router_w", vp), ("router_b", vp), ("gate_up", vp), ("gate_up_scale", vp),
                 ("down", vp), ("down_scale", vp), ("sh_gate_up", vp), ("sh_gate_up_scale", vp),
-                ("sh_down", vp), ("sh_down_scale", vp), ("sh_gate_w", vp)]
+                ("sh_down", vp), ("sh_down_scale", vp), ("sh_gate_w", vp),
+                ("down_f16", vp), ("sh_down_f16", vp)]
 
 
 class MoeKernelStat(ctypes.Structure):
@@ -53,6 +54,7 @@ SIGNATURES = {
     "moe_forward_decode_host": (i32, [vp, i32, vp, vp, vp]),
     "moe_forward_decode_noalloc": (i32, [ctypes.POINTER(MoeConfig), ctypes.POINTER(MoeWeights), vp,
                                          vp, vp]),
+    "moe_convert_bf16_to_f16": (i32, [vp, vp, ctypes.c_size_t, vp]),
     "moe_check_device": (i32, [vp, ctypes.POINTER(ctypes.c_int32)]),
     "moe_profile_enable": (i32, [vp, i32]),
     "moe_profile_read": (i32, [vp, ctypes.POINTER(MoeKernelStat), i32, ctypes.POINTER(i32)]),

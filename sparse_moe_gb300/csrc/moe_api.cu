@@ -89,17 +89,19 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// 2-D bf16 matrix [outer, inner] (inner contiguous), 128-byte swizzled boxes
-// of {64, box_rows} elements: the K-major weight tiles of the grouped GEMMs.
+// 2-D bf16 (or fp16) matrix [outer, inner] (inner contiguous), 128-byte
+// swizzled boxes of {64, box_rows} elements: the K-major weight tiles of the
+// grouped GEMMs.
 bool encode_weight_map(CUtensorMap *m, const void *ptr, uint64_t inner, uint64_t outer,
-                       uint32_t box_rows) {
+                       uint32_t box_rows, bool f16 = false) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   const cuuint64_t dims[2] = {inner, outer};
   const cuuint64_t strides[1] = {inner * 2};
   const cuuint32_t box[2] = {64, box_rows};
   const cuuint32_t es[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, es,
+  return fn(m, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+            const_cast<void *>(ptr), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -134,6 +136,7 @@ const char *kKernelNames[K_COUNT] = {
 
 struct LayerSlot {
   bool loaded = false;
+  bool down_f16 = false;   // caller-supplied fp16 copies of down / sh_down
   moe_weights w{};
   // TMA descriptors of the weight (A) operands, encoded at load time
   CUtensorMap map_router, map_gu, map_gu_sh, map_dn, map_dn_sh;
@@ -377,8 +380,9 @@ moe_status enqueue_prefill_chunk(moe_ctx *ctx, const LayerSlot &ls, const void *
   if (st) return st;
   // down -> o
   gp.mode = MODE_DOWN;
-  gp.a_routed = ls.w.down;
-  gp.a_shared = ls.w.sh_down;
+  gp.a_routed = ls.down_f16 ? ls.w.down_f16 : ls.w.down;
+  gp.a_shared = ls.down_f16 ? ls.w.sh_down_f16 : ls.w.sh_down;
+  gp.ab_f16 = ls.down_f16 ? 1 : 0;
   gp.lda_routed = c.inter;
   gp.lda_shared = c.shared_inter;
   gp.a_rows_routed = c.n_experts * c.hidden;
@@ -394,7 +398,9 @@ moe_status enqueue_prefill_chunk(moe_ctx *ctx, const LayerSlot &ls, const void *
     ProfScope ps(ctx, K_DOWN_GEMM, s);
     st = launched(ctx,
                   launch_tc_gemm(ls.map_dn, ls.map_dn_sh, gp,
-                                 int4 ? CONV_INT4_TO_F16 : CONV_BF16_TO_F16, ctx->gemm_grid, s),
+                                 int4 ? CONV_INT4_TO_F16
+                                      : (ls.down_f16 ? CONV_NONE : CONV_BF16_TO_F16),
+                                 ctx->gemm_grid, s),
                   "down gemm launch");
   }
   if (st) return st;
@@ -551,17 +557,27 @@ moe_status moe_load_weights(moe_ctx *ctx, int layer, const moe_weights *w) {
       if (!p || (reinterpret_cast<uintptr_t>(p) & 1))
         return fail(ctx, MOE_ERR_INVALID_ARG, "int4 format needs all four scale pointers");
   }
+  const bool f16_down = w->down_f16 != nullptr || w->sh_down_f16 != nullptr;
+  if (f16_down) {
+    if (int4) return fail(ctx, MOE_ERR_INVALID_ARG, "fp16 down copies apply to bf16 weights only");
+    if (!w->down_f16 || !w->sh_down_f16)
+      return fail(ctx, MOE_ERR_INVALID_ARG, "down_f16 and sh_down_f16 go together");
+    if (!aligned16(w->down_f16) || !aligned16(w->sh_down_f16))
+      return fail(ctx, MOE_ERR_INVALID_ARG, "fp16 down copies not 16-byte aligned");
+  }
   LayerSlot &ls = ctx->layers[layer];
   ls.loaded = false;
   ls.w = *w;
+  ls.down_f16 = f16_down;
   bool ok = encode_weight_map(&ls.map_router, w->router_w, c.hidden, c.n_experts, 128);
   if (!int4) {
     ok = ok && encode_weight_map(&ls.map_gu, w->gate_up, c.hidden,
                                  static_cast<uint64_t>(c.n_experts) * 2 * c.inter, 64);
     ok = ok && encode_weight_map(&ls.map_gu_sh, w->sh_gate_up, c.hidden, 2 * c.shared_inter, 64);
-    ok = ok && encode_weight_map(&ls.map_dn, w->down, c.inter,
-                                 static_cast<uint64_t>(c.n_experts) * c.hidden, 128);
-    ok = ok && encode_weight_map(&ls.map_dn_sh, w->sh_down, c.shared_inter, c.hidden, 128);
+    ok = ok && encode_weight_map(&ls.map_dn, f16_down ? w->down_f16 : w->down, c.inter,
+                                 static_cast<uint64_t>(c.n_experts) * c.hidden, 128, f16_down);
+    ok = ok && encode_weight_map(&ls.map_dn_sh, f16_down ? w->sh_down_f16 : w->sh_down,
+                                 c.shared_inter, c.hidden, 128, f16_down);
   } else {
     ok = ok && encode_code_map(&ls.map_gu, w->gate_up, c.hidden / 2,
                                static_cast<uint64_t>(c.n_experts) * 2 * c.inter, 64);
@@ -693,6 +709,17 @@ moe_status moe_forward_decode_host(moe_ctx *ctx, int layer, const void *x_host, 
   if (st) return st;
   e = cudaMemcpyAsync(y_host, ys, bytes, cudaMemcpyDeviceToHost, s);
   return e == cudaSuccess ? MOE_OK : cuda_fail(ctx, e, "device-to-host copy");
+}
+
+moe_status moe_convert_bf16_to_f16(const void *src, void *dst, size_t n, void *stream) {
+  if (n == 0) return MOE_OK;
+  if (!src || !dst || !aligned16(src) || !aligned16(dst)) return MOE_ERR_INVALID_ARG;
+  const char *a = static_cast<const char *>(src);
+  const char *b = static_cast<const char *>(dst);
+  if (a < b + 2 * n && b < a + 2 * n) return MOE_ERR_INVALID_ARG;   // overlap
+  return launch_convert_bf16_to_f16(src, dst, n, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? MOE_OK
+             : MOE_ERR_CUDA;
 }
 
 moe_status moe_check_device(moe_ctx *ctx, int32_t *code) {

@@ -55,6 +55,7 @@ struct GemmParams {
   int prefetch;              // bit 1: L2-prefetch the next tile's token rows
   const void *a_scale_routed;   // int4 weights: bf16 scales [rows, K/64] (else null)
   const void *a_scale_shared;
+  int ab_f16;                // CONV_NONE only: A and B are fp16 (else bf16)
 };
 
 cudaError_t gemm_configure();
@@ -79,6 +80,9 @@ cudaError_t launch_scatter(const int32_t *idx, const uint32_t *blk_mask, const i
 // y[t] = sum_j w[t,j] o[pos(t,j)] + g[t] o[T*k + t]
 cudaError_t launch_combine(const float *gate, const void *o, const int32_t *pos, const float *w,
                            int T, int H, int k, void *y, cudaStream_t stream);
+
+// dst[i] = fp16(src[i]) (round to nearest even), n elements, 16-byte aligned.
+cudaError_t launch_convert_bf16_to_f16(const void *src, void *dst, size_t n, cudaStream_t stream);
 
 // Batch-1 decode.
 struct DecodeParams {

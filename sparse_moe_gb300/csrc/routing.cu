@@ -11,6 +11,8 @@
 //     offsets[e] + (rows of e in earlier blocks) + popc(mask & lower bits),
 // i.e. segments are ordered by ascending token index.
 #include "moe_internal.h"
+
+#include <algorithm>
 #include "warp_topk.cuh"
 
 namespace moe {
@@ -300,6 +302,45 @@ cudaError_t launch_combine(const float *gate, const void *o, const int32_t *pos,
     combine_kernel<8><<<T, 256, 0, stream>>>(gate, oh, pos, w, T, H, k, yb);
   else
     combine_kernel<0><<<T, 256, 0, stream>>>(gate, oh, pos, w, T, H, k, yb);
+  return cudaGetLastError();
+}
+
+// bf16 -> fp16 copy of a weight array, 8 elements (16 bytes) per thread and
+// step; the last n % 8 elements one by one.  Each pair is widened to fp32
+// exactly and narrowed with cvt.rn.f16x2.f32, the conversion the down GEMM
+// applies to weight tiles in shared memory when no copy is supplied.
+__global__ void __launch_bounds__(256) convert_bf16_to_f16_kernel(const uint4 *__restrict__ src,
+                                                                  uint4 *__restrict__ dst,
+                                                                  size_t nvec, size_t n) {
+  const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
+  for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < nvec; i += stride) {
+    const uint4 v = __ldg(src + i);
+    const uint32_t wi[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      asm("cvt.rn.f16x2.f32 %0, %1, %2;"
+          : "=r"(o[j])
+          : "f"(__uint_as_float(wi[j] & 0xffff0000u)), "f"(__uint_as_float(wi[j] << 16)));
+    dst[i] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+  if (blockIdx.x == 0 && threadIdx.x < n - nvec * 8) {
+    const size_t e = nvec * 8 + threadIdx.x;
+    const uint16_t b = reinterpret_cast<const uint16_t *>(src)[e];
+    reinterpret_cast<__half *>(dst)[e] = __float2half_rn(__uint_as_float(static_cast<uint32_t>(b) << 16));
+  }
+}
+
+cudaError_t launch_convert_bf16_to_f16(const void *src, void *dst, size_t n, cudaStream_t stream) {
+  int dev = 0, sms = 0;
+  cudaError_t e;
+  if ((e = cudaGetDevice(&dev)) || (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)))
+    return e;
+  const size_t nvec = n / 8;
+  const size_t want = (nvec + 255) / 256;
+  const int grid = static_cast<int>(std::max<size_t>(1, std::min<size_t>(want, static_cast<size_t>(sms) * 8)));
+  convert_bf16_to_f16_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint4 *>(src),
+                                                       static_cast<uint4 *>(dst), nvec, n);
   return cudaGetLastError();
 }
 

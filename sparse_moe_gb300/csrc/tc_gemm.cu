@@ -640,9 +640,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
           }
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + acc * ACC_COLS;
-          const uint32_t idesc = (CONV == CONV_BF16_TO_F16 || CONV == CONV_INT4_TO_F16)
-                                     ? idesc_f16_f32(PAIR_M, t.nmma)
-                                     : idesc_bf16_f32(PAIR_M, t.nmma);
+          const bool f16 = CONV == CONV_BF16_TO_F16 || CONV == CONV_INT4_TO_F16 ||
+                           (CONV == CONV_NONE && p.ab_f16);
+          const uint32_t idesc = f16 ? idesc_f16_f32(PAIR_M, t.nmma) : idesc_bf16_f32(PAIR_M, t.nmma);
           for (int ks = 0; ks < t.nk; ++ks) {
             MOE_T0();
             // unconverted modes: both CTAs' producers signal this CTA's full

@@ -8,6 +8,7 @@ import torch
 import moe_synth
 from gpu_helpers import assert_layer_close, check_routing, host_layer, make_ctx
 from oracle import moe_oracle as orc
+from sparse_moe_gb300 import MoEError, convert_bf16_to_f16, with_f16_down
 
 pytestmark = pytest.mark.gpu
 
@@ -133,6 +134,48 @@ def test_prefill_host_buffers_match_device_path():
     ctx.forward_prefill_host(0, x_h, y_h)
     torch.cuda.synchronize()
     assert torch.equal(y_h, y_dev.cpu())
+
+
+# ---- optional fp16 copies of the down weights: the down GEMM then feeds its
+# weight tiles straight to the tensor cores instead of converting them in
+# shared memory; the conversion is the same, so the output must not change.
+
+@pytest.mark.parametrize("n", [0, 1, 7, 8, 9, 1000, (1 << 20) + 5])
+def test_convert_bf16_to_f16_matches_torch(n):
+    g = torch.Generator(device="cuda").manual_seed(n)
+    src = (torch.randn(n, device="cuda", generator=g) * 0.05).to(torch.bfloat16)
+    if n >= 9:
+        # specials: +-inf, NaN, beyond the fp16 range, fp16 subnormals and below
+        src[:9] = torch.tensor([float("inf"), -float("inf"), float("nan"), 7.0e4, -1.0e5,
+                                6.0e-6, -3.0e-8, 1.0e-9, 65504.0], device="cuda").to(torch.bfloat16)
+    got = convert_bf16_to_f16(src)
+    ref = src.to(torch.float16)
+    torch.cuda.synchronize()
+    nan = torch.isnan(ref)
+    assert torch.equal(torch.isnan(got), nan)
+    assert torch.equal(got[~nan].view(torch.int16), ref[~nan].view(torch.int16))
+
+
+@pytest.mark.parametrize("wl", [moe_synth.TINY_LAYER, _wl(moe_synth.QWEN, 300, bias=1.5, seed=7),
+                                moe_synth.PREFILL_BF16], ids=["tiny", "qwen300", "qwen4096"])
+def test_prefill_f16_down_copies_bit_identical(wl):
+    ctx, (w,) = make_ctx(wl, max_chunk_rows=max(64, wl.T))
+    x = moe_synth.make_x(wl, device="cuda")
+    y_conv = ctx.forward_prefill(0, x)
+    ctx.load_weights(0, with_f16_down(w))
+    y_f16 = ctx.forward_prefill(0, x)
+    torch.cuda.synchronize()
+    assert torch.equal(y_conv, y_f16)
+    assert ctx.check_device() == 0
+
+
+def test_load_weights_rejects_lone_f16_down_copy():
+    wl = moe_synth.TINY_LAYER
+    ctx, (w,) = make_ctx(wl, max_chunk_rows=64)
+    w2 = dict(w)
+    w2["down_f16"] = convert_bf16_to_f16(w["down"])
+    with pytest.raises(MoEError):
+        ctx.load_weights(0, w2)
 
 
 # ---- int4 weights (symmetric, group 64): dequantised inside the GEMMs; the
