@@ -79,15 +79,6 @@ __device__ __forceinline__ const char *line_of(const char *p) {
   return reinterpret_cast<const char *>(reinterpret_cast<uintptr_t>(p) & ~uintptr_t(127));
 }
 
-// Programmatic dependent launch: let the next kernel in the stream be
-// scheduled (its CTAs start as SMs free up), and wait until the previous one
-// has completed with its memory visible.  Both are no-ops without the launch
-// attribute.
-__device__ __forceinline__ void pdl_trigger() {
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-
 // This warp's L2 prefetch of `bytes` of one weight row.
 __device__ __forceinline__ void prefetch_row_l2(const void *row, size_t bytes) {
   const char *b = static_cast<const char *>(row);

@@ -148,6 +148,8 @@ struct moe_ctx {
   int num_sms = 0;
   int gemm_grid = 0;   // CTAs of the persistent grouped-GEMM grid (whole pairs)
   int gemm_prefetch = 0;   // GEMM L2 prefetch bits (MOE_GEMM_PREFETCH; see GemmParams)
+  int router_split = 1;    // router GEMM split-K parts (router_split())
+  bool prefill_pdl = true; // programmatic dependent launch between prefill kernels (MOE_PREFILL_PDL)
   int decode_grid = 0;     // CTAs of the cooperative decode launch
   int decode_smem = 0;     // dynamic shared-memory limit of the decode kernel
   bool decode_pdl = true;  // decode launches overlap the previous kernel's tail
@@ -256,16 +258,33 @@ moe_status launched(moe_ctx *ctx, cudaError_t e, const char *what) {
   return MOE_OK;
 }
 
-// Token rows per router tile: enough tiles for every CTA pair, at least 32.
-int router_block_rows(const moe_ctx *ctx, int T) {
-  const int mt = (ctx->cfg.n_experts + gemm_pair_rows() - 1) / gemm_pair_rows();
-  const int pairs = std::max(1, ctx->num_sms / 2);
-  int br = (T * mt + pairs - 1) / pairs;
-  br = (br + 31) & ~31;
-  return std::min(kBlockRowsMax, std::max(32, br));
+// Router GEMM split-K parts S (4, 2 or 1: the largest dividing H / 64 whose
+// parts fit the scratch).  S depends on the configuration only, so every
+// token's logits are summed in the same order whatever the chunk length
+// ("Bound temporary memory with prompt chunking": chunking leaves the output
+// bit for bit unchanged).  With S > 1 the parts go to scratch space of
+// S * T * E floats (the o buffer, which a chunk does not use until its down
+// projection) and the top-k kernel adds them in part order.
+int router_split(const moe_config &c, const WsLayout &L) {
+  const int nk = c.hidden / 64;
+  const size_t scratch_floats = static_cast<size_t>(L.R) * c.hidden / 2;
+  for (int S = 4; S > 1; S /= 2)
+    if (nk % S == 0 && static_cast<size_t>(S) * L.Tc * c.n_experts <= scratch_floats) return S;
+  return 1;
 }
 
-// Router GEMM, top-k, histogram/scan/block map, scatter for T <= Tc tokens.
+// Token rows per router tile: enough tiles (with the split-K parts) for every
+// CTA pair, 32..256 rows.
+int router_block_rows(const moe_ctx *ctx, int T) {
+  const long long mt = (ctx->cfg.n_experts + gemm_pair_rows() - 1) / gemm_pair_rows();
+  const long long pairs = std::max(1, ctx->num_sms / 2);
+  long long br = (static_cast<long long>(T) * mt * ctx->router_split + pairs - 1) / pairs;
+  br = (br + 31) & ~31LL;
+  return static_cast<int>(std::min<long long>(kBlockRowsMax, std::max<long long>(32, br)));
+}
+
+// Router GEMM, top-k, histogram/scan/block map, scatter for T <= Tc tokens;
+// the summed logits go to `logits` when it is non-null.
 moe_status enqueue_route(moe_ctx *ctx, const LayerSlot &ls, const void *x, int T, float *logits,
                          int32_t *idx, float *w, int32_t *counts, int32_t *offsets,
                          int32_t *sorted_rows, int32_t *pos, cudaStream_t s) {
@@ -279,6 +298,7 @@ moe_status enqueue_route(moe_ctx *ctx, const LayerSlot &ls, const void *x, int T
   gp.b = x;
   gp.ldb = c.hidden;
   gp.block_rows = router_block_rows(ctx, T);
+  gp.k_split = ctx->router_split;
   gp.n_blocks_host = (T + gp.block_rows - 1) / gp.block_rows;
   gp.T = T;
   gp.m_tiles = (c.n_experts + gemm_pair_rows() - 1) / gemm_pair_rows();
@@ -287,17 +307,21 @@ moe_status enqueue_route(moe_ctx *ctx, const LayerSlot &ls, const void *x, int T
   gp.inter_routed = c.inter;
   gp.inter_shared = c.shared_inter;
   gp.k_routed = c.hidden;
-  gp.out = logits;
+  // one part: logits straight into the caller's buffer (or the workspace's);
+  // several: parts in the o scratch, summed by the top-k kernel
+  float *part = gp.k_split > 1 ? ctx->at<float>(L.o) : (logits ? logits : ctx->at<float>(L.logits));
+  gp.out = part;
+  gp.out_split_stride = static_cast<size_t>(T) * c.n_experts;
   gp.out_ld = c.n_experts;
   gp.bias = ls.w.router_b;
   gp.status = ctx->status();
   gp.prefetch = ctx->gemm_prefetch;
-  const int tiles = gp.n_blocks_host * gp.m_tiles;
+  const int tiles = gp.n_blocks_host * gp.m_tiles * gp.k_split;
   moe_status st;
   {
     ProfScope ps(ctx, K_ROUTER_GEMM, s);
     st = launched(ctx, launch_tc_gemm(ls.map_router, ls.map_router, gp, CONV_NONE,
-                                      std::min(ctx->gemm_grid, 2 * tiles), s),
+                                      std::min(ctx->gemm_grid, 2 * tiles), ctx->prefill_pdl, s),
                   "router gemm launch");
   }
   if (st) return st;
@@ -306,8 +330,10 @@ moe_status enqueue_route(moe_ctx *ctx, const LayerSlot &ls, const void *x, int T
   {
     ProfScope ps(ctx, K_TOPK, s);
     st = launched(ctx,
-                  launch_topk(logits, x, ls.w.sh_gate_w, T, c.n_experts, c.top_k, c.hidden, idx, w,
-                              mask, ctx->at<float>(L.gate), s),
+                  launch_topk(part, gp.k_split, gp.out_split_stride,
+                              gp.k_split > 1 ? logits : nullptr, x, ls.w.sh_gate_w, T,
+                              c.n_experts, c.top_k, c.hidden, idx, w, mask,
+                              ctx->at<float>(L.gate), ctx->prefill_pdl, s),
                   "topk launch");
   }
   if (st) return st;
@@ -316,7 +342,8 @@ moe_status enqueue_route(moe_ctx *ctx, const LayerSlot &ls, const void *x, int T
     ProfScope ps(ctx, K_SCAN, s);
     st = launched(ctx,
                   launch_scan(mask, nblk, T, c.n_experts, c.top_k, counts, offsets, base,
-                              ctx->at<int4>(L.blocks), ctx->at<int32_t>(L.nblocks), s),
+                              ctx->at<int4>(L.blocks), ctx->at<int32_t>(L.nblocks), ctx->prefill_pdl,
+                              s),
                   "scan launch");
   }
   if (st) return st;
@@ -324,7 +351,7 @@ moe_status enqueue_route(moe_ctx *ctx, const LayerSlot &ls, const void *x, int T
     ProfScope ps(ctx, K_SCATTER, s);
     st = launched(ctx,
                   launch_scatter(idx, mask, base, offsets, T, c.n_experts, c.top_k, sorted_rows,
-                                 pos, s),
+                                 pos, ctx->prefill_pdl, s),
                   "scatter launch");
   }
   return st;
@@ -338,7 +365,7 @@ moe_status enqueue_prefill_chunk(moe_ctx *ctx, const LayerSlot &ls, const void *
   float *w = ctx->at<float>(L.w);
   int32_t *sorted = ctx->at<int32_t>(L.sorted);
   int32_t *pos = ctx->at<int32_t>(L.pos);
-  moe_status st = enqueue_route(ctx, ls, x, T, ctx->at<float>(L.logits), idx, w,
+  moe_status st = enqueue_route(ctx, ls, x, T, nullptr, idx, w,
                                 ctx->at<int32_t>(L.counts), ctx->at<int32_t>(L.offsets), sorted,
                                 pos, s);
   if (st) return st;
@@ -374,7 +401,7 @@ moe_status enqueue_prefill_chunk(moe_ctx *ctx, const LayerSlot &ls, const void *
     ProfScope ps(ctx, K_GATEUP_GEMM, s);
     st = launched(ctx,
                   launch_tc_gemm(ls.map_gu, ls.map_gu_sh, gp, int4 ? CONV_INT4_TO_BF16 : CONV_NONE,
-                                 ctx->gemm_grid, s),
+                                 ctx->gemm_grid, ctx->prefill_pdl, s),
                   "gate/up gemm launch");
   }
   if (st) return st;
@@ -400,7 +427,7 @@ moe_status enqueue_prefill_chunk(moe_ctx *ctx, const LayerSlot &ls, const void *
                   launch_tc_gemm(ls.map_dn, ls.map_dn_sh, gp,
                                  int4 ? CONV_INT4_TO_F16
                                       : (ls.down_f16 ? CONV_NONE : CONV_BF16_TO_F16),
-                                 ctx->gemm_grid, s),
+                                 ctx->gemm_grid, ctx->prefill_pdl, s),
                   "down gemm launch");
   }
   if (st) return st;
@@ -408,7 +435,7 @@ moe_status enqueue_prefill_chunk(moe_ctx *ctx, const LayerSlot &ls, const void *
     ProfScope ps(ctx, K_COMBINE, s);
     st = launched(ctx,
                   launch_combine(ctx->at<float>(L.gate), ctx->at<void>(L.o), pos, w, T, c.hidden,
-                                 c.top_k, y, s),
+                                 c.top_k, y, ctx->prefill_pdl, s),
                   "combine launch");
   }
   return st;
@@ -514,9 +541,11 @@ moe_status moe_ctx_create(const moe_config *cfg, int device, void *workspace, si
     return MOE_ERR_CUDA;
   }
   ctx->gemm_grid = gemm_max_grid(sms);
+  ctx->router_split = router_split(ctx->cfg, ctx->L);
   ctx->decode_grid = decode_layer_grid(sms);
   if (const char *env = std::getenv("MOE_GEMM_PREFETCH")) ctx->gemm_prefetch = std::atoi(env);
   if (const char *env = std::getenv("MOE_DECODE_PDL")) ctx->decode_pdl = std::atoi(env) != 0;
+  if (const char *env = std::getenv("MOE_PREFILL_PDL")) ctx->prefill_pdl = std::atoi(env) != 0;
   if (
       (e = decode_configure(&ctx->decode_smem)) != cudaSuccess ||
       (e = cudaMemset(ctx->ws + L.status, 0, 256)) != cudaSuccess ||
@@ -604,8 +633,7 @@ moe_status moe_route(moe_ctx *ctx, int layer, const void *x, int T, float *logit
       !pos_of_assign)
     return fail(ctx, MOE_ERR_INVALID_ARG, "null or misaligned routing buffer");
   if ((st = ensure_device(ctx))) return st;
-  float *lg = logits ? logits : ctx->at<float>(ctx->L.logits);
-  return enqueue_route(ctx, ctx->layers[layer], x, T, lg, topk_idx, topk_w, counts, offsets,
+  return enqueue_route(ctx, ctx->layers[layer], x, T, logits, topk_idx, topk_w, counts, offsets,
                        sorted_rows, pos_of_assign, static_cast<cudaStream_t>(stream));
 }
 

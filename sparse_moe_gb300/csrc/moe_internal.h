@@ -56,6 +56,8 @@ struct GemmParams {
   const void *a_scale_routed;   // int4 weights: bf16 scales [rows, K/64] (else null)
   const void *a_scale_shared;
   int ab_f16;                // CONV_NONE only: A and B are fp16 (else bf16)
+  int k_split;               // router: split-K parts (>= 1); part s writes out + s * out_split_stride
+  size_t out_split_stride;   // router: floats between split-K parts of `out`
 };
 
 cudaError_t gemm_configure();
@@ -63,23 +65,28 @@ cudaError_t gemm_configure();
 int gemm_pair_rows();
 // Largest persistent grid (CTAs, whole pairs) whose clusters are co-resident.
 int gemm_max_grid(int num_sms);
+// `pdl` (here and below): programmatic dependent launch on the previous
+// kernel of the stream (the kernel waits for it before reading its inputs).
 cudaError_t launch_tc_gemm(const CUtensorMap &a_routed, const CUtensorMap &a_shared,
-                           const GemmParams &p, int conv, int grid, cudaStream_t stream);
+                           const GemmParams &p, int conv, int grid, bool pdl,
+                           cudaStream_t stream);
 
 // Routing: top-k + masks, block scan + block map, stable scatter.
-cudaError_t launch_topk(const float *logits, const void *x, const void *wsg, int T, int E, int k,
-                        int H, int32_t *idx, float *w, uint32_t *blk_mask, float *gate,
-                        cudaStream_t stream);
+// Top-k over logits = sum of nsplit parts (part s at partial + s * split_stride,
+// summed in order s = 0, 1, ...); writes the sums to logits_out if non-null.
+cudaError_t launch_topk(const float *partial, int nsplit, size_t split_stride, float *logits_out,
+                        const void *x, const void *wsg, int T, int E, int k, int H, int32_t *idx,
+                        float *w, uint32_t *blk_mask, float *gate, bool pdl, cudaStream_t stream);
 cudaError_t launch_scan(const uint32_t *blk_mask, int nblk, int T, int E, int k,
                         int32_t *counts, int32_t *offsets, int32_t *blk_base, int4 *blocks,
-                        int32_t *n_blocks, cudaStream_t stream);
+                        int32_t *n_blocks, bool pdl, cudaStream_t stream);
 cudaError_t launch_scatter(const int32_t *idx, const uint32_t *blk_mask, const int32_t *blk_base,
                            const int32_t *offsets, int T, int E, int k, int32_t *sorted_rows,
-                           int32_t *pos_of_assign, cudaStream_t stream);
+                           int32_t *pos_of_assign, bool pdl, cudaStream_t stream);
 
 // y[t] = sum_j w[t,j] o[pos(t,j)] + g[t] o[T*k + t]
 cudaError_t launch_combine(const float *gate, const void *o, const int32_t *pos, const float *w,
-                           int T, int H, int k, void *y, cudaStream_t stream);
+                           int T, int H, int k, void *y, bool pdl, cudaStream_t stream);
 
 // dst[i] = fp16(src[i]) (round to nearest even), n elements, 16-byte aligned.
 cudaError_t launch_convert_bf16_to_f16(const void *src, void *dst, size_t n, cudaStream_t stream);

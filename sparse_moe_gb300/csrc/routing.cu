@@ -18,28 +18,46 @@
 namespace moe {
 
 // ----------------------------------------------------------------- top-k --
-// One routing block of 32 tokens per CTA, one token per warp: top-k and
-// weights of the token, its bit in the block's per-expert masks, and the
+// One routing block of 32 tokens per CTA, one token per warp: the token's
+// logits (the sum of the router GEMM's split-K parts, in part order), its
+// top-k and weights, its bit in the block's per-expert masks, and the
 // shared-expert gate g[t] = sigmoid(x[t] . w_sg) for the combine.
 constexpr int kTopkThreads = 32 * kRouteBlockTokens;
 
 template <int R>
 __global__ void __launch_bounds__(kTopkThreads) topk_kernel(
-    const float *__restrict__ logits, const __nv_bfloat16 *__restrict__ x,
+    const float *__restrict__ partial, int nsplit, size_t split_stride, float *__restrict__ logits_out,
+    const __nv_bfloat16 *__restrict__ x,
     const __nv_bfloat16 *__restrict__ wsg, int T, int E, int k, int H, int32_t *__restrict__ idx,
     float *__restrict__ w, uint32_t *__restrict__ blk_mask, float *__restrict__ gate) {
   __shared__ uint32_t mask_s[1024];
+  pdl_trigger();
   for (int e = threadIdx.x; e < E; e += blockDim.x) mask_s[e] = 0;
   __syncthreads();
+  pdl_wait();
   const int tl = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * kRouteBlockTokens + tl;
   if (t < T) {
     float v[R];
-    const float *row = logits + static_cast<size_t>(t) * E;
+    const float *row = partial + static_cast<size_t>(t) * E;
 #pragma unroll
     for (int r = 0; r < R; ++r) {
       const int e = lane + 32 * r;
       v[r] = (e < E) ? __ldcs(row + e) : 0.0f;
+    }
+    for (int sp = 1; sp < nsplit; ++sp) {
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        const int e = lane + 32 * r;
+        if (e < E) v[r] += __ldcs(row + sp * split_stride + e);
+      }
+    }
+    if (logits_out != nullptr) {
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        const int e = lane + 32 * r;
+        if (e < E) logits_out[static_cast<size_t>(t) * E + e] = v[r];
+      }
     }
     // the shared gate's dot product, loads in flight with the logits
     const uint4 *x4 = reinterpret_cast<const uint4 *>(x + static_cast<size_t>(t) * H);
@@ -71,16 +89,17 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(
     blk_mask[static_cast<size_t>(blockIdx.x) * E + e] = mask_s[e];
 }
 
-cudaError_t launch_topk(const float *logits, const void *x, const void *wsg, int T, int E, int k,
-                        int H, int32_t *idx, float *w, uint32_t *blk_mask, float *gate,
-                        cudaStream_t stream) {
+cudaError_t launch_topk(const float *partial, int nsplit, size_t split_stride, float *logits_out,
+                        const void *x, const void *wsg, int T, int E, int k, int H, int32_t *idx,
+                        float *w, uint32_t *blk_mask, float *gate, bool pdl, cudaStream_t stream) {
   const int nblk = (T + kRouteBlockTokens - 1) / kRouteBlockTokens;
   const int R = (E + 31) / 32;
   const __nv_bfloat16 *xb = static_cast<const __nv_bfloat16 *>(x);
   const __nv_bfloat16 *gb = static_cast<const __nv_bfloat16 *>(wsg);
-#define MOE_TOPK(RR)                                                                     \
-  topk_kernel<RR><<<nblk, kTopkThreads, 0, stream>>>(logits, xb, gb, T, E, k, H, idx, w, \
-                                                     blk_mask, gate)
+  cudaError_t e;
+#define MOE_TOPK(RR)                                                                            \
+  e = launch_kernel(topk_kernel<RR>, dim3(nblk), dim3(kTopkThreads), 0, stream, pdl, partial,  \
+                    nsplit, split_stride, logits_out, xb, gb, T, E, k, H, idx, w, blk_mask, gate)
   if (R <= 1) MOE_TOPK(1);
   else if (R <= 2) MOE_TOPK(2);
   else if (R <= 4) MOE_TOPK(4);
@@ -88,7 +107,7 @@ cudaError_t launch_topk(const float *logits, const void *x, const void *wsg, int
   else if (R <= 16) MOE_TOPK(16);
   else MOE_TOPK(32);
 #undef MOE_TOPK
-  return cudaGetLastError();
+  return e;
 }
 
 // ------------------------------------------------------------------ scan --
@@ -131,6 +150,8 @@ __global__ void __launch_bounds__(1024) scan_kernel(const uint32_t *__restrict__
   __shared__ int part[1024];
   __shared__ int warp_tot[33];
   __shared__ int cnt_s[1024];
+  pdl_trigger();
+  pdl_wait();
   const int tid = threadIdx.x;
   const int P = max(1, 1024 / E);     // parts of the block range per expert
   const int e = tid % E;
@@ -192,10 +213,9 @@ __global__ void __launch_bounds__(1024) scan_kernel(const uint32_t *__restrict__
 
 cudaError_t launch_scan(const uint32_t *blk_mask, int nblk, int T, int E, int k,
                         int32_t *counts, int32_t *offsets, int32_t *blk_base, int4 *blocks,
-                        int32_t *n_blocks, cudaStream_t stream) {
-  scan_kernel<<<1, 1024, 0, stream>>>(blk_mask, nblk, T, E, k, counts, offsets, blk_base, blocks,
-                                      n_blocks);
-  return cudaGetLastError();
+                        int32_t *n_blocks, bool pdl, cudaStream_t stream) {
+  return launch_kernel(scan_kernel, dim3(1), dim3(1024), 0, stream, pdl, blk_mask, nblk, T, E, k,
+                       counts, offsets, blk_base, blocks, n_blocks);
 }
 
 // --------------------------------------------------------------- scatter --
@@ -204,6 +224,8 @@ __global__ void scatter_kernel(const int32_t *__restrict__ idx, const uint32_t *
                                const int32_t *__restrict__ offsets, int T, int E, int k,
                                int32_t *__restrict__ sorted_rows,
                                int32_t *__restrict__ pos_of_assign) {
+  pdl_trigger();
+  pdl_wait();
   const int tl = threadIdx.x / k;
   const int j = threadIdx.x - tl * k;
   const int b = blockIdx.x;
@@ -220,11 +242,10 @@ __global__ void scatter_kernel(const int32_t *__restrict__ idx, const uint32_t *
 
 cudaError_t launch_scatter(const int32_t *idx, const uint32_t *blk_mask, const int32_t *blk_base,
                            const int32_t *offsets, int T, int E, int k, int32_t *sorted_rows,
-                           int32_t *pos_of_assign, cudaStream_t stream) {
+                           int32_t *pos_of_assign, bool pdl, cudaStream_t stream) {
   const int nblk = (T + kRouteBlockTokens - 1) / kRouteBlockTokens;
-  scatter_kernel<<<nblk, kRouteBlockTokens * k, 0, stream>>>(idx, blk_mask, blk_base, offsets, T, E,
-                                                             k, sorted_rows, pos_of_assign);
-  return cudaGetLastError();
+  return launch_kernel(scatter_kernel, dim3(nblk), dim3(kRouteBlockTokens * k), 0, stream, pdl, idx,
+                       blk_mask, blk_base, offsets, T, E, k, sorted_rows, pos_of_assign);
 }
 
 // --------------------------------------------------------------- combine --
@@ -242,6 +263,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const float *__restrict__ 
                                                       int k, __nv_bfloat16 *__restrict__ y) {
   __shared__ int pos_s[32];
   __shared__ float w_s[32];
+  pdl_trigger();
+  pdl_wait();
   const int t = blockIdx.x;
   const int nchunk = H / 8;
   if (threadIdx.x < k) {
@@ -295,14 +318,14 @@ __global__ void __launch_bounds__(256) combine_kernel(const float *__restrict__ 
 }
 
 cudaError_t launch_combine(const float *gate, const void *o, const int32_t *pos, const float *w,
-                           int T, int H, int k, void *y, cudaStream_t stream) {
+                           int T, int H, int k, void *y, bool pdl, cudaStream_t stream) {
   const __half *oh = reinterpret_cast<const __half *>(o);
   __nv_bfloat16 *yb = reinterpret_cast<__nv_bfloat16 *>(y);
   if (k <= 8)
-    combine_kernel<8><<<T, 256, 0, stream>>>(gate, oh, pos, w, T, H, k, yb);
-  else
-    combine_kernel<0><<<T, 256, 0, stream>>>(gate, oh, pos, w, T, H, k, yb);
-  return cudaGetLastError();
+    return launch_kernel(combine_kernel<8>, dim3(T), dim3(256), 0, stream, pdl, gate, oh, pos, w, T,
+                         H, k, yb);
+  return launch_kernel(combine_kernel<0>, dim3(T), dim3(256), 0, stream, pdl, gate, oh, pos, w, T, H,
+                       k, yb);
 }
 
 // bf16 -> fp16 copy of a weight array, 8 elements (16 bytes) per thread and

@@ -128,6 +128,8 @@ struct Tile {
   int valid;
   int row0, nrows, nmma;
   int nk;
+  int k0;              // first k-step (router split-K: split * nk)
+  int split;           // router split-K part of this tile
   int m;
   int shared;
   int a_row, a_row2;   // this CTA's first A row (a_row2: first up row for gate/up)
@@ -138,6 +140,12 @@ struct Tile {
 
 __device__ __forceinline__ Tile decode_tile(const GemmParams &p, int tile, int rank) {
   Tile t;
+  t.k0 = 0;
+  t.split = 0;
+  if (p.mode == MODE_ROUTER) {   // router tiles: (block, m, split), split fastest
+    t.split = tile % p.k_split;
+    tile /= p.k_split;
+  }
   const int b = tile / p.m_tiles;
   t.m = tile - b * p.m_tiles;
   int e = 0;
@@ -155,7 +163,8 @@ __device__ __forceinline__ Tile decode_tile(const GemmParams &p, int tile, int r
   t.nmma = max(32, (t.nrows + 31) & ~31);
   t.valid = t.nrows > 0;
   if (p.mode == MODE_ROUTER) {
-    t.nk = p.k_routed / BK;
+    t.nk = p.k_routed / BK / p.k_split;
+    t.k0 = t.split * t.nk;
     t.out_base = t.m * PAIR_M + rank * BM;
     t.out_limit = p.n_experts;
     t.a_row = t.out_base;
@@ -181,8 +190,8 @@ __device__ __forceinline__ Tile decode_tile(const GemmParams &p, int tile, int r
 }
 
 __device__ __forceinline__ int num_tiles(const GemmParams &p) {
-  const int nb = (p.mode == MODE_ROUTER) ? p.n_blocks_host : *p.n_blocks_dev;
-  return nb * p.m_tiles;
+  if (p.mode == MODE_ROUTER) return p.n_blocks_host * p.m_tiles * p.k_split;
+  return *p.n_blocks_dev * p.m_tiles;
 }
 
 // Row of the B operand (x for router and gate/up, h for down) feeding row r
@@ -389,6 +398,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
   int *row_tab = reinterpret_cast<int *>(epi_stage + EPI_STAGE_BYTES);
   SmemTail *tail = reinterpret_cast<SmemTail *>(row_tab + B_WARPS * kRowTab);
   volatile int *abort_flag = &tail->abort_flag;
+  pdl_trigger();   // the next kernel may start its set-up as SMs free up
 
   const int warp = threadIdx.x >> 5;
   const int lane = lane_id();
@@ -423,6 +433,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
   __syncthreads();
   cluster_sync_all();   // both CTAs' barriers exist before any remote arrive
   tc_fence_after();
+  pdl_wait();   // inputs (block list, token rows) written by earlier kernels
   const uint32_t tmem_base = tail->tmem_base;
   const int ntiles = num_tiles(p);
 #ifdef MOE_TRACE
@@ -464,10 +475,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
           if constexpr (INT4) {
             mbar_arrive_expect_tx(full_bar, A_CODE_BYTES);
             if (p.mode == MODE_GATEUP) {
-              tma_load_2d(a_dst + CODE_OFF, amap, ks * kx, t.a_row, full_bar);
-              tma_load_2d(a_dst + CODE_OFF + A_CODE_BYTES / 2, amap, ks * kx, t.a_row2, full_bar);
+              tma_load_2d(a_dst + CODE_OFF, amap, (t.k0 + ks) * kx, t.a_row, full_bar);
+              tma_load_2d(a_dst + CODE_OFF + A_CODE_BYTES / 2, amap, (t.k0 + ks) * kx, t.a_row2, full_bar);
             } else {
-              tma_load_2d(a_dst + CODE_OFF, amap, ks * kx, t.a_row, full_bar);
+              tma_load_2d(a_dst + CODE_OFF, amap, (t.k0 + ks) * kx, t.a_row, full_bar);
             }
           } else if constexpr (CONV == CONV_NONE) {
             // Both CTAs' boxes complete on the leader's full barrier, which
@@ -475,18 +486,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
             const uint32_t lead_full = mapa_shared(full_bar, 0);
             if (rank == 0) mbar_arrive_expect_tx(full_bar, 2 * A_BYTES);
             if (p.mode == MODE_GATEUP) {
-              tma_load_2d_pair(a_dst, amap, ks * kx, t.a_row, lead_full);
-              tma_load_2d_pair(a_dst + A_BYTES / 2, amap, ks * kx, t.a_row2, lead_full);
+              tma_load_2d_pair(a_dst, amap, (t.k0 + ks) * kx, t.a_row, lead_full);
+              tma_load_2d_pair(a_dst + A_BYTES / 2, amap, (t.k0 + ks) * kx, t.a_row2, lead_full);
             } else {
-              tma_load_2d_pair(a_dst, amap, ks * kx, t.a_row, lead_full);
+              tma_load_2d_pair(a_dst, amap, (t.k0 + ks) * kx, t.a_row, lead_full);
             }
           } else {
             mbar_arrive_expect_tx(full_bar, A_BYTES);
             if (p.mode == MODE_GATEUP) {
-              tma_load_2d(a_dst, amap, ks * kx, t.a_row, full_bar);
-              tma_load_2d(a_dst + A_BYTES / 2, amap, ks * kx, t.a_row2, full_bar);
+              tma_load_2d(a_dst, amap, (t.k0 + ks) * kx, t.a_row, full_bar);
+              tma_load_2d(a_dst + A_BYTES / 2, amap, (t.k0 + ks) * kx, t.a_row2, full_bar);
             } else {
-              tma_load_2d(a_dst, amap, ks * kx, t.a_row, full_bar);
+              tma_load_2d(a_dst, amap, (t.k0 + ks) * kx, t.a_row, full_bar);
             }
           }
           // (the peer's boxes in the unconverted modes complete on the
@@ -539,7 +550,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       const int half = u.nmma / 2;
       for (int rb = btid; rb < half; rb += B_WARPS * 32) {
         const int r = rank * half + rb;
-        if (r < u.nrows) prefetch_l2_bulk(bsrc + static_cast<size_t>(b_row(p, u, r)) * p.ldb, kbytes);
+        if (r < u.nrows)
+          prefetch_l2_bulk(bsrc + static_cast<size_t>(b_row(p, u, r)) * p.ldb + u.k0 * BK, kbytes);
       }
     };
     if (pair_id < ntiles) prefetch_b(pair_id);
@@ -578,7 +590,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
 #ifdef MOE_TRACE
         const long long tb1 = clock64();
 #endif
-        const int kc = ks * BK + c * 8;
+        const int kc = (t.k0 + ks) * BK + c * 8;
         for (int j = gq, e = rsub; j < nquads; j += B_WARPS_PER_STAGE, e += 4) {
           const int r = 4 * j + rsub;
           const uint32_t dst = stage_b + r * 128 + static_cast<uint32_t>((c ^ (r & 7)) << 4);
@@ -812,10 +824,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
                     __float2half_rn(__uint_as_float(r[cc]));
           }
         }
-      } else {  // MODE_ROUTER: fp32 logits, 128 contiguous bytes per column
+      } else {  // MODE_ROUTER: fp32 logits (split-K part t.split), 128 contiguous bytes per column
         const int e = t.out_base + q * 32 + lane;
-        float *lout = reinterpret_cast<float *>(p.out);
-        const float bias = (p.bias != nullptr && e < p.n_experts) ? __ldg(p.bias + e) : 0.0f;
+        float *lout = reinterpret_cast<float *>(p.out) + t.split * p.out_split_stride;
+        const float bias =
+            (p.bias != nullptr && e < p.n_experts && t.split == 0) ? __ldg(p.bias + e) : 0.0f;
         for (int c0 = 0; c0 < t.nmma; c0 += 16) {
           uint32_t r[16];
           tmem_ld16(tacc + c0, r);
@@ -902,27 +915,25 @@ int gemm_max_grid(int num_sms) {
 }
 
 cudaError_t launch_tc_gemm(const CUtensorMap &a_routed, const CUtensorMap &a_shared,
-                           const GemmParams &p, int conv, int grid, cudaStream_t stream) {
+                           const GemmParams &p, int conv, int grid, bool pdl,
+                           cudaStream_t stream) {
   grid &= ~1;   // whole CTA pairs
   if (grid < 2) grid = 2;
+  const dim3 g(grid), b(NUM_THREADS);
   switch (conv) {
     case CONV_BF16_TO_F16:
-      tc_gemm_kernel<CONV_BF16_TO_F16>
-          <<<grid, NUM_THREADS, kGemmSmemBytes, stream>>>(a_routed, a_shared, p);
-      break;
+      return launch_kernel(tc_gemm_kernel<CONV_BF16_TO_F16>, g, b, kGemmSmemBytes, stream, pdl,
+                           a_routed, a_shared, p);
     case CONV_INT4_TO_BF16:
-      tc_gemm_kernel<CONV_INT4_TO_BF16>
-          <<<grid, NUM_THREADS, kGemmSmemBytes, stream>>>(a_routed, a_shared, p);
-      break;
+      return launch_kernel(tc_gemm_kernel<CONV_INT4_TO_BF16>, g, b, kGemmSmemBytes, stream, pdl,
+                           a_routed, a_shared, p);
     case CONV_INT4_TO_F16:
-      tc_gemm_kernel<CONV_INT4_TO_F16>
-          <<<grid, NUM_THREADS, kGemmSmemBytes, stream>>>(a_routed, a_shared, p);
-      break;
+      return launch_kernel(tc_gemm_kernel<CONV_INT4_TO_F16>, g, b, kGemmSmemBytes, stream, pdl,
+                           a_routed, a_shared, p);
     default:
-      tc_gemm_kernel<CONV_NONE>
-          <<<grid, NUM_THREADS, kGemmSmemBytes, stream>>>(a_routed, a_shared, p);
+      return launch_kernel(tc_gemm_kernel<CONV_NONE>, g, b, kGemmSmemBytes, stream, pdl, a_routed,
+                           a_shared, p);
   }
-  return cudaGetLastError();
 }
 
 }  // namespace moe
