@@ -149,6 +149,7 @@ struct moe_ctx {
   int gemm_grid = 0;   // CTAs of the persistent grouped-GEMM grid (whole pairs)
   int gemm_prefetch = 0;   // GEMM L2 prefetch bits (MOE_GEMM_PREFETCH; see GemmParams)
   int router_split = 1;    // router GEMM split-K parts (router_split())
+  CUtensorMap map_h;       // h [R, Imax] fp16 in the workspace: the down GEMM's token rows
   bool prefill_pdl = true; // programmatic dependent launch between prefill kernels (MOE_PREFILL_PDL)
   int decode_grid = 0;     // CTAs of the cooperative decode launch
   int decode_smem = 0;     // dynamic shared-memory limit of the decode kernel
@@ -320,7 +321,7 @@ moe_status enqueue_route(moe_ctx *ctx, const LayerSlot &ls, const void *x, int T
   moe_status st;
   {
     ProfScope ps(ctx, K_ROUTER_GEMM, s);
-    st = launched(ctx, launch_tc_gemm(ls.map_router, ls.map_router, gp, CONV_NONE,
+    st = launched(ctx, launch_tc_gemm(ls.map_router, ls.map_router, ls.map_router, gp, CONV_NONE,
                                       std::min(ctx->gemm_grid, 2 * tiles), ctx->prefill_pdl, s),
                   "router gemm launch");
   }
@@ -400,7 +401,8 @@ moe_status enqueue_prefill_chunk(moe_ctx *ctx, const LayerSlot &ls, const void *
   {
     ProfScope ps(ctx, K_GATEUP_GEMM, s);
     st = launched(ctx,
-                  launch_tc_gemm(ls.map_gu, ls.map_gu_sh, gp, int4 ? CONV_INT4_TO_BF16 : CONV_NONE,
+                  launch_tc_gemm(ls.map_gu, ls.map_gu_sh, ls.map_gu, gp,
+                                 int4 ? CONV_INT4_TO_BF16 : CONV_NONE,
                                  ctx->gemm_grid, ctx->prefill_pdl, s),
                   "gate/up gemm launch");
   }
@@ -410,6 +412,7 @@ moe_status enqueue_prefill_chunk(moe_ctx *ctx, const LayerSlot &ls, const void *
   gp.a_routed = ls.down_f16 ? ls.w.down_f16 : ls.w.down;
   gp.a_shared = ls.down_f16 ? ls.w.sh_down_f16 : ls.w.sh_down;
   gp.ab_f16 = ls.down_f16 ? 1 : 0;
+  gp.b_tma = 1;   // h rows of a block are consecutive: TMA boxes
   gp.lda_routed = c.inter;
   gp.lda_shared = c.shared_inter;
   gp.a_rows_routed = c.n_experts * c.hidden;
@@ -424,7 +427,7 @@ moe_status enqueue_prefill_chunk(moe_ctx *ctx, const LayerSlot &ls, const void *
   {
     ProfScope ps(ctx, K_DOWN_GEMM, s);
     st = launched(ctx,
-                  launch_tc_gemm(ls.map_dn, ls.map_dn_sh, gp,
+                  launch_tc_gemm(ls.map_dn, ls.map_dn_sh, ctx->map_h, gp,
                                  int4 ? CONV_INT4_TO_F16
                                       : (ls.down_f16 ? CONV_NONE : CONV_BF16_TO_F16),
                                  ctx->gemm_grid, ctx->prefill_pdl, s),
@@ -542,6 +545,11 @@ moe_status moe_ctx_create(const moe_config *cfg, int device, void *workspace, si
   }
   ctx->gemm_grid = gemm_max_grid(sms);
   ctx->router_split = router_split(ctx->cfg, ctx->L);
+  if (!encode_weight_map(&ctx->map_h, ctx->ws + L.h, L.Imax, static_cast<uint64_t>(L.R), kBTmaRows,
+                         true)) {
+    delete ctx;
+    return MOE_ERR_CUDA;
+  }
   ctx->decode_grid = decode_layer_grid(sms);
   if (const char *env = std::getenv("MOE_GEMM_PREFETCH")) ctx->gemm_prefetch = std::atoi(env);
   if (const char *env = std::getenv("MOE_DECODE_PDL")) ctx->decode_pdl = std::atoi(env) != 0;

@@ -56,6 +56,8 @@ struct GemmParams {
   const void *a_scale_routed;   // int4 weights: bf16 scales [rows, K/64] (else null)
   const void *a_scale_shared;
   int ab_f16;                // CONV_NONE only: A and B are fp16 (else bf16)
+  int b_tma;                 // down: B rows are consecutive (h in grouped order) and come by
+                             // TMA with the weight tile (map_b), not from the row producers
   int k_split;               // router: split-K parts (>= 1); part s writes out + s * out_split_stride
   size_t out_split_stride;   // router: floats between split-K parts of `out`
 };
@@ -68,8 +70,10 @@ int gemm_max_grid(int num_sms);
 // `pdl` (here and below): programmatic dependent launch on the previous
 // kernel of the stream (the kernel waits for it before reading its inputs).
 cudaError_t launch_tc_gemm(const CUtensorMap &a_routed, const CUtensorMap &a_shared,
-                           const GemmParams &p, int conv, int grid, bool pdl,
+                           const CUtensorMap &b, const GemmParams &p, int conv, int grid, bool pdl,
                            cudaStream_t stream);
+// Token-row boxes of the down GEMM's B operand: 16 rows x 64 fp16.
+constexpr int kBTmaRows = 16;
 
 // Routing: top-k + masks, block scan + block map, stable scatter.
 // Top-k over logits = sum of nsplit parts (part s at partial + s * split_stride,

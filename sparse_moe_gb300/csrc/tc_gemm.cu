@@ -389,7 +389,8 @@ __device__ __forceinline__ void warp_store_rows_f16(const uint8_t *stage, int ro
 template <int CONV>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a_routed,
-                       const __grid_constant__ CUtensorMap map_a_shared, const GemmParams p) {
+                       const __grid_constant__ CUtensorMap map_a_shared,
+                       const __grid_constant__ CUtensorMap map_b, const GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
@@ -424,6 +425,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     fence_mbarrier_init();
     prefetch_tensormap(&map_a_routed);
     prefetch_tensormap(&map_a_shared);
+    if (p.b_tma) prefetch_tensormap(&map_b);
   }
   if (warp == MMA_WARP) {
     tmem_alloc_pair(smem_u32(&tail->tmem_base), TMEM_COLS);
@@ -472,8 +474,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
           MOE_TADD(0);
           const uint32_t full_bar = smem_u32(&tail->full[stage]);
           const uint32_t a_dst = smem_base + stage * STAGE_BYTES;
+          // b_tma: this CTA's nmma / 2 token rows, in boxes of kBTmaRows
+          const int b_boxes = p.b_tma ? t.nmma / 2 / kBTmaRows : 0;
+          const uint32_t b_bytes = static_cast<uint32_t>(b_boxes * kBTmaRows * BK * 2);
+          const int b_row0 = t.row0 + rank * (t.nmma / 2);
           if constexpr (INT4) {
-            mbar_arrive_expect_tx(full_bar, A_CODE_BYTES);
+            mbar_arrive_expect_tx(full_bar, A_CODE_BYTES + b_bytes);
+            for (int i = 0; i < b_boxes; ++i)
+              tma_load_2d(a_dst + A_BYTES + i * kBTmaRows * 128, &map_b, (t.k0 + ks) * BK,
+                          b_row0 + i * kBTmaRows, full_bar);
             if (p.mode == MODE_GATEUP) {
               tma_load_2d(a_dst + CODE_OFF, amap, (t.k0 + ks) * kx, t.a_row, full_bar);
               tma_load_2d(a_dst + CODE_OFF + A_CODE_BYTES / 2, amap, (t.k0 + ks) * kx, t.a_row2, full_bar);
@@ -484,7 +493,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
             // Both CTAs' boxes complete on the leader's full barrier, which
             // expects the pair's bytes: no relay from the peer is needed.
             const uint32_t lead_full = mapa_shared(full_bar, 0);
-            if (rank == 0) mbar_arrive_expect_tx(full_bar, 2 * A_BYTES);
+            if (rank == 0) mbar_arrive_expect_tx(full_bar, 2 * (A_BYTES + b_bytes));
+            for (int i = 0; i < b_boxes; ++i)
+              tma_load_2d_pair(a_dst + A_BYTES + i * kBTmaRows * 128, &map_b, (t.k0 + ks) * BK,
+                               b_row0 + i * kBTmaRows, lead_full);
             if (p.mode == MODE_GATEUP) {
               tma_load_2d_pair(a_dst, amap, (t.k0 + ks) * kx, t.a_row, lead_full);
               tma_load_2d_pair(a_dst + A_BYTES / 2, amap, (t.k0 + ks) * kx, t.a_row2, lead_full);
@@ -492,7 +504,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
               tma_load_2d_pair(a_dst, amap, (t.k0 + ks) * kx, t.a_row, lead_full);
             }
           } else {
-            mbar_arrive_expect_tx(full_bar, A_BYTES);
+            mbar_arrive_expect_tx(full_bar, A_BYTES + b_bytes);
+            for (int i = 0; i < b_boxes; ++i)
+              tma_load_2d(a_dst + A_BYTES + i * kBTmaRows * 128, &map_b, (t.k0 + ks) * BK,
+                          b_row0 + i * kBTmaRows, full_bar);
             if (p.mode == MODE_GATEUP) {
               tma_load_2d(a_dst, amap, (t.k0 + ks) * kx, t.a_row, full_bar);
               tma_load_2d(a_dst + A_BYTES / 2, amap, (t.k0 + ks) * kx, t.a_row2, full_bar);
@@ -591,7 +606,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         const long long tb1 = clock64();
 #endif
         const int kc = (t.k0 + ks) * BK + c * 8;
-        for (int j = gq, e = rsub; j < nquads; j += B_WARPS_PER_STAGE, e += 4) {
+        for (int j = gq, e = rsub; j < (p.b_tma ? 0 : nquads); j += B_WARPS_PER_STAGE, e += 4) {
           const int r = 4 * j + rsub;
           const uint32_t dst = stage_b + r * 128 + static_cast<uint32_t>((c ^ (r & 7)) << 4);
           cp_async16(dst, bsrc + rows_tab[e] + kc, 16u);
@@ -915,24 +930,24 @@ int gemm_max_grid(int num_sms) {
 }
 
 cudaError_t launch_tc_gemm(const CUtensorMap &a_routed, const CUtensorMap &a_shared,
-                           const GemmParams &p, int conv, int grid, bool pdl,
+                           const CUtensorMap &b, const GemmParams &p, int conv, int grid, bool pdl,
                            cudaStream_t stream) {
   grid &= ~1;   // whole CTA pairs
   if (grid < 2) grid = 2;
-  const dim3 g(grid), b(NUM_THREADS);
+  const dim3 g(grid), bl(NUM_THREADS);
   switch (conv) {
     case CONV_BF16_TO_F16:
-      return launch_kernel(tc_gemm_kernel<CONV_BF16_TO_F16>, g, b, kGemmSmemBytes, stream, pdl,
-                           a_routed, a_shared, p);
+      return launch_kernel(tc_gemm_kernel<CONV_BF16_TO_F16>, g, bl, kGemmSmemBytes, stream, pdl,
+                           a_routed, a_shared, b, p);
     case CONV_INT4_TO_BF16:
-      return launch_kernel(tc_gemm_kernel<CONV_INT4_TO_BF16>, g, b, kGemmSmemBytes, stream, pdl,
-                           a_routed, a_shared, p);
+      return launch_kernel(tc_gemm_kernel<CONV_INT4_TO_BF16>, g, bl, kGemmSmemBytes, stream, pdl,
+                           a_routed, a_shared, b, p);
     case CONV_INT4_TO_F16:
-      return launch_kernel(tc_gemm_kernel<CONV_INT4_TO_F16>, g, b, kGemmSmemBytes, stream, pdl,
-                           a_routed, a_shared, p);
+      return launch_kernel(tc_gemm_kernel<CONV_INT4_TO_F16>, g, bl, kGemmSmemBytes, stream, pdl,
+                           a_routed, a_shared, b, p);
     default:
-      return launch_kernel(tc_gemm_kernel<CONV_NONE>, g, b, kGemmSmemBytes, stream, pdl, a_routed,
-                           a_shared, p);
+      return launch_kernel(tc_gemm_kernel<CONV_NONE>, g, bl, kGemmSmemBytes, stream, pdl, a_routed,
+                           a_shared, b, p);
   }
 }
 
