@@ -170,6 +170,8 @@ struct moe_ctx {
 
   template <class T> T *at(size_t off) const { return reinterpret_cast<T *>(ws + off); }
   int *status() const { return at<int>(L.status); }
+  // the routing scan's completion ticket (zeroed with the status region)
+  unsigned int *scan_ticket() const { return at<unsigned int>(L.status + 64); }
 };
 
 namespace {
@@ -343,8 +345,8 @@ moe_status enqueue_route(moe_ctx *ctx, const LayerSlot &ls, const void *x, int T
     ProfScope ps(ctx, K_SCAN, s);
     st = launched(ctx,
                   launch_scan(mask, nblk, T, c.n_experts, c.top_k, counts, offsets, base,
-                              ctx->at<int4>(L.blocks), ctx->at<int32_t>(L.nblocks), ctx->prefill_pdl,
-                              s),
+                              ctx->at<int4>(L.blocks), ctx->at<int32_t>(L.nblocks),
+                              ctx->scan_ticket(), ctx->prefill_pdl, s),
                   "scan launch");
   }
   if (st) return st;

@@ -81,9 +81,10 @@ constexpr int kBTmaRows = 16;
 cudaError_t launch_topk(const float *partial, int nsplit, size_t split_stride, float *logits_out,
                         const void *x, const void *wsg, int T, int E, int k, int H, int32_t *idx,
                         float *w, uint32_t *blk_mask, float *gate, bool pdl, cudaStream_t stream);
+// `ticket`: a zeroed counter in device memory (left zeroed on return).
 cudaError_t launch_scan(const uint32_t *blk_mask, int nblk, int T, int E, int k,
                         int32_t *counts, int32_t *offsets, int32_t *blk_base, int4 *blocks,
-                        int32_t *n_blocks, bool pdl, cudaStream_t stream);
+                        int32_t *n_blocks, unsigned int *ticket, bool pdl, cudaStream_t stream);
 cudaError_t launch_scatter(const int32_t *idx, const uint32_t *blk_mask, const int32_t *blk_base,
                            const int32_t *offsets, int T, int E, int k, int32_t *sorted_rows,
                            int32_t *pos_of_assign, bool pdl, cudaStream_t stream);

@@ -24,7 +24,7 @@ namespace moe {
 // shared-expert gate g[t] = sigmoid(x[t] . w_sg) for the combine.
 constexpr int kTopkThreads = 32 * kRouteBlockTokens;
 
-template <int R>
+template <int R, int SP>
 __global__ void __launch_bounds__(kTopkThreads) topk_kernel(
     const float *__restrict__ partial, int nsplit, size_t split_stride, float *__restrict__ logits_out,
     const __nv_bfloat16 *__restrict__ x,
@@ -40,16 +40,35 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(
   if (t < T) {
     float v[R];
     const float *row = partial + static_cast<size_t>(t) * E;
+    if constexpr (SP > 0) {
+      // up to SP parts' loads in flight together, then the sums in part order
+      float pv[SP][R];
 #pragma unroll
-    for (int r = 0; r < R; ++r) {
-      const int e = lane + 32 * r;
-      v[r] = (e < E) ? __ldcs(row + e) : 0.0f;
-    }
-    for (int sp = 1; sp < nsplit; ++sp) {
+      for (int sp = 0; sp < SP; ++sp)
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+          const int e = lane + 32 * r;
+          pv[sp][r] = (e < E && sp < nsplit) ? __ldcs(row + sp * split_stride + e) : 0.0f;
+        }
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        v[r] = pv[0][r];
+#pragma unroll
+        for (int sp = 1; sp < SP; ++sp)
+          if (sp < nsplit) v[r] += pv[sp][r];
+      }
+    } else {
 #pragma unroll
       for (int r = 0; r < R; ++r) {
         const int e = lane + 32 * r;
-        if (e < E) v[r] += __ldcs(row + sp * split_stride + e);
+        v[r] = (e < E) ? __ldcs(row + e) : 0.0f;
+      }
+      for (int sp = 1; sp < nsplit; ++sp) {
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+          const int e = lane + 32 * r;
+          if (e < E) v[r] += __ldcs(row + sp * split_stride + e);
+        }
       }
     }
     if (logits_out != nullptr) {
@@ -63,6 +82,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(
     const uint4 *x4 = reinterpret_cast<const uint4 *>(x + static_cast<size_t>(t) * H);
     const uint4 *g4 = reinterpret_cast<const uint4 *>(wsg);
     float d = 0.0f;
+#pragma unroll 4
     for (int c = lane; c < H / 8; c += 32) {
       const uint4 xv = x4[c], gv = __ldg(g4 + c);
       const uint32_t xa[4] = {xv.x, xv.y, xv.z, xv.w}, ga[4] = {gv.x, gv.y, gv.z, gv.w};
@@ -96,16 +116,22 @@ cudaError_t launch_topk(const float *partial, int nsplit, size_t split_stride, f
   const int R = (E + 31) / 32;
   const __nv_bfloat16 *xb = static_cast<const __nv_bfloat16 *>(x);
   const __nv_bfloat16 *gb = static_cast<const __nv_bfloat16 *>(wsg);
-  cudaError_t e;
-#define MOE_TOPK(RR)                                                                            \
-  e = launch_kernel(topk_kernel<RR>, dim3(nblk), dim3(kTopkThreads), 0, stream, pdl, partial,  \
+  // SP: parts loaded together (up to 4 parts for E <= 256), 0: part by part
+  cudaError_t e = cudaSuccess;
+#define MOE_TOPK(RR, SS)                                                                        \
+  e = launch_kernel(topk_kernel<RR, SS>, dim3(nblk), dim3(kTopkThreads), 0, stream, pdl, partial, \
                     nsplit, split_stride, logits_out, xb, gb, T, E, k, H, idx, w, blk_mask, gate)
-  if (R <= 1) MOE_TOPK(1);
-  else if (R <= 2) MOE_TOPK(2);
-  else if (R <= 4) MOE_TOPK(4);
-  else if (R <= 8) MOE_TOPK(8);
-  else if (R <= 16) MOE_TOPK(16);
-  else MOE_TOPK(32);
+#define MOE_TOPK_R(RR)                        \
+  if (nsplit == 1) MOE_TOPK(RR, 1);           \
+  else if (nsplit <= 4) MOE_TOPK(RR, 4);      \
+  else MOE_TOPK(RR, 0)
+  if (R <= 1) { MOE_TOPK_R(1); }
+  else if (R <= 2) { MOE_TOPK_R(2); }
+  else if (R <= 4) { MOE_TOPK_R(4); }
+  else if (R <= 8) { MOE_TOPK_R(8); }
+  else if (R <= 16) { MOE_TOPK(16, 0); }
+  else { MOE_TOPK(32, 0); }
+#undef MOE_TOPK_R
 #undef MOE_TOPK
   return e;
 }
@@ -140,58 +166,97 @@ __device__ __forceinline__ int block_excl_scan_1024(int v, int *warp_tot, int &t
   return excl;
 }
 
+// Experts per scan CTA: each CTA counts and places the routing blocks of its
+// experts; the CTA that finishes last (an atomic ticket) turns the counts into
+// segment offsets and writes the block map.  Results do not depend on which
+// CTA is last.
+constexpr int kScanExperts = 32;
+
 __global__ void __launch_bounds__(1024) scan_kernel(const uint32_t *__restrict__ blk_mask,
                                                     int nblk, int T, int E, int k,
                                                     int32_t *__restrict__ counts,
                                                     int32_t *__restrict__ offsets,
                                                     int32_t *__restrict__ blk_base,
                                                     int4 *__restrict__ blocks,
-                                                    int32_t *__restrict__ n_blocks) {
+                                                    int32_t *__restrict__ n_blocks,
+                                                    unsigned int *__restrict__ ticket) {
   __shared__ int part[1024];
   __shared__ int warp_tot[33];
-  __shared__ int cnt_s[1024];
+  __shared__ int is_last;
   pdl_trigger();
   pdl_wait();
   const int tid = threadIdx.x;
-  const int P = max(1, 1024 / E);     // parts of the block range per expert
-  const int e = tid % E;
-  const int pi = tid / E;
-  const bool active = tid < P * E;
+  const int e0 = blockIdx.x * kScanExperts;
+  const int Ec = min(kScanExperts, E - e0);   // experts of this CTA
+  const int P = 1024 / kScanExperts;         // parts of the block range per expert
+  const int el = tid % kScanExperts;
+  const int e = e0 + el;
+  const int pi = tid / kScanExperts;
+  const bool active = el < Ec;
   const int b0 = active ? static_cast<int>((static_cast<long long>(nblk) * pi) / P) : 0;
   const int b1 = active ? static_cast<int>((static_cast<long long>(nblk) * (pi + 1)) / P) : 0;
-  // 1. histogram: rows of expert e in my range of routing blocks
-  int s = 0;
+  // 1. histogram: rows of expert e in my range of routing blocks (ranges of
+  //    up to kScanRegs blocks keep their counts in registers for step 3)
+  constexpr int kScanRegs = 8;
+  const bool in_regs = b1 - b0 <= kScanRegs;
+  int cnt[kScanRegs];
+  int sum = 0;
+  if (in_regs) {
+#pragma unroll
+    for (int i = 0; i < kScanRegs; ++i)
+      cnt[i] = (b0 + i < b1) ? __popc(blk_mask[static_cast<size_t>(b0 + i) * E + e]) : 0;
+#pragma unroll
+    for (int i = 0; i < kScanRegs; ++i) sum += cnt[i];
+  } else {
 #pragma unroll 8
-  for (int b = b0; b < b1; ++b) s += __popc(blk_mask[static_cast<size_t>(b) * E + e]);
-  part[tid] = s;
+    for (int b = b0; b < b1; ++b) sum += __popc(blk_mask[static_cast<size_t>(b) * E + e]);
+  }
+  part[tid] = sum;
   __syncthreads();
   // 2. exclusive scan over the parts of each expert
-  if (tid < E) {
+  if (tid < Ec) {
     int run = 0;
     for (int pp = 0; pp < P; ++pp) {
-      const int v = part[pp * E + tid];
-      part[pp * E + tid] = run;
+      const int v = part[pp * kScanExperts + tid];
+      part[pp * kScanExperts + tid] = run;
       run += v;
     }
-    cnt_s[tid] = run;
-    counts[tid] = run;
+    counts[e0 + tid] = run;
   }
   __syncthreads();
   // 3. per-block bases inside each expert segment
   if (active) {
     int run = part[tid];
+    if (in_regs) {
+#pragma unroll
+      for (int i = 0; i < kScanRegs; ++i)
+        if (b0 + i < b1) {
+          blk_base[static_cast<size_t>(b0 + i) * E + e] = run;
+          run += cnt[i];
+        }
+    } else {
 #pragma unroll 8
-    for (int b = b0; b < b1; ++b) {
-      blk_base[static_cast<size_t>(b) * E + e] = run;
-      run += __popc(blk_mask[static_cast<size_t>(b) * E + e]);
+      for (int b = b0; b < b1; ++b) {
+        blk_base[static_cast<size_t>(b) * E + e] = run;
+        run += __popc(blk_mask[static_cast<size_t>(b) * E + e]);
+      }
     }
   }
-  // 4. exclusive scan of the counts -> segment offsets
+  // 4. the last CTA: exclusive scan of all counts -> segment offsets, block map
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) is_last = atomicAdd(ticket, 1u) == gridDim.x - 1;
+  __syncthreads();
+  if (!is_last) return;
+  __threadfence();
+  const int c = (tid < E) ? __ldcg(counts + tid) : 0;
   int total = 0;
-  const int c = (tid < E) ? cnt_s[tid] : 0;
   const int off = block_excl_scan_1024(c, warp_tot, total);
   if (tid < E) offsets[tid] = off;
-  if (tid == 0) offsets[E] = total;   // = T * k
+  if (tid == 0) {
+    offsets[E] = total;   // = T * k
+    *ticket = 0u;         // ready for the next launch
+  }
   // 5. block map: ceil(count / kBlockRowsMax) blocks per expert, then the
   //    shared expert's T rows at grouped row T*k.
   const int nb = (c + kBlockRowsMax - 1) / kBlockRowsMax;
@@ -213,9 +278,10 @@ __global__ void __launch_bounds__(1024) scan_kernel(const uint32_t *__restrict__
 
 cudaError_t launch_scan(const uint32_t *blk_mask, int nblk, int T, int E, int k,
                         int32_t *counts, int32_t *offsets, int32_t *blk_base, int4 *blocks,
-                        int32_t *n_blocks, bool pdl, cudaStream_t stream) {
-  return launch_kernel(scan_kernel, dim3(1), dim3(1024), 0, stream, pdl, blk_mask, nblk, T, E, k,
-                       counts, offsets, blk_base, blocks, n_blocks);
+                        int32_t *n_blocks, unsigned int *ticket, bool pdl, cudaStream_t stream) {
+  return launch_kernel(scan_kernel, dim3((E + kScanExperts - 1) / kScanExperts), dim3(1024), 0,
+                       stream, pdl, blk_mask, nblk, T, E, k, counts, offsets, blk_base, blocks,
+                       n_blocks, ticket);
 }
 
 // --------------------------------------------------------------- scatter --
