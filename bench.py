@@ -121,9 +121,9 @@ class ClockSampler:
 
 # DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) of
 # the kernels the roofline lines name, from one ncu capture of the current
-# kernels (the summaries under profiles/): gate/up 625.0 + 33.1 MB at the
-# T=4096 prefill workload, decode layer 57.77 + 0.28 MB.
-TRAFFIC_BYTES = {"gateup_swiglu_gemm": 658.1e6, "decode_layer": 58.05e6}
+# kernels (the summaries under profiles/): gate/up 625.5 + 33.0 MB at the
+# T=4096 prefill workload, decode layer 57.76 + 0.29 MB.
+TRAFFIC_BYTES = {"gateup_swiglu_gemm": 658.5e6, "decode_layer": 58.05e6}
 
 
 # ------------------------------------------------------------- workload --
