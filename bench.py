@@ -326,6 +326,18 @@ def bench_decode(args, dev, stream, hbm, int4=None):
         b.record(stream)
     torch.cuda.synchronize()
     us_layer = a.elapsed_time(b) * 1e3 / (reps * L)
+    # the same L layers in one persistent launch (moe_forward_decode_layers):
+    # a grid barrier between layers instead of a kernel boundary
+    for _ in range(max(3, args.warmup)):
+        ctx.forward_decode_layers(0, xs, ys, stream=stream)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        a.record(stream)
+        for _ in range(reps):
+            ctx.forward_decode_layers(0, xs, ys, stream=stream)
+        b.record(stream)
+    torch.cuda.synchronize()
+    us_layer_ml = a.elapsed_time(b) * 1e3 / (reps * L)
     # end to end from host memory: one token per layer call, copies included
     for _ in range(3):
         ctx.forward_decode_host(0, x_h, y_h, stream=stream)
@@ -355,6 +367,14 @@ def bench_decode(args, dev, stream, hbm, int4=None):
                      "timing": "graph replays of L layers, CUDA events on the launch stream; "
                                "launch_us_eager: events around single eager launches",
                      "launch_us_eager": lay_us},
+        "multi_layer": {
+            "value": us_layer_ml, "unit": "us/layer",
+            "how": f"moe_forward_decode_layers: all {L} layers in one persistent launch, "
+                   "grid barrier between layers, next layer's shared weights fetched ahead",
+            "roofline": {"kernel": "decode_layers", "bound": "hbm",
+                         "achieved": nb["total"] / (us_layer_ml * 1e-6) / 1e9, "peak": hbm,
+                         "unit": "GB/s",
+                         "frac": nb["total"] / (us_layer_ml * 1e-6) / 1e9 / hbm}},
         "kernels_eager_us": {k: v[1] * 1e3 / max(1, v[0]) for k, v in prof.items()},
         "e2e": {"value": e2e_us, "unit": "us/token (one layer, host buffers, synchronous)",
                 "h2d_bytes_per_step": s.hidden * 2, "d2h_bytes_per_step": s.hidden * 2},

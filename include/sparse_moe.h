@@ -175,6 +175,24 @@ moe_status moe_forward_prefill(moe_ctx *ctx, int layer, const void *x, int T,
 moe_status moe_forward_decode(moe_ctx *ctx, int layer, const void *x, void *y,
                               void *stream);
 
+/* Batch-1 decode of layer slots first_layer .. first_layer + n_layers - 1 in
+ * order, for a caller that has their inputs at hand (or chains them), in one
+ * persistent launch per up to 48 layers instead of one per layer: layer l
+ * reads x + l * x_stride and writes y + l * y_stride (device bf16 rows of H;
+ * strides in elements, multiples of 8, 0 allowed for x).  It computes exactly
+ * what moe_forward_decode computes for each layer, with the same arithmetic.
+ * Layer l + 1 starts only after every CTA has written layer l's output (a
+ * grid barrier), so its input may be layer l's output (x + (l + 1) *
+ * x_stride == y + l * y_stride): a layer's output is written after its last
+ * read of its input.  Only the next layer's weights (its router, shared gate
+ * and shared expert, which do not depend on the routing) are fetched ahead,
+ * during the current layer's output projection.  Layers must be loaded;
+ * n_layers = 0 is a no-op.  Afterwards moe_decode_routing reports the last
+ * layer's routing. */
+moe_status moe_forward_decode_layers(moe_ctx *ctx, int first_layer, int n_layers,
+                                     const void *x, size_t x_stride, void *y,
+                                     size_t y_stride, void *stream);
+
 /* Routing of the most recent moe_forward_decode on this context, copied
  * (asynchronously, on `stream`) to device buffers: logits fp32 [E] (may be
  * NULL), idx int32 [k], w fp32 [k] (either may be NULL). */

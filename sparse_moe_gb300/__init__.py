@@ -165,6 +165,29 @@ class MoEContext:
         self._check(st, "moe_forward_decode")
         return y
 
+    def forward_decode_layers(self, first_layer: int, x: torch.Tensor, y: torch.Tensor,
+                              chained: bool = False, stream=None) -> torch.Tensor:
+        """Layers first_layer .. first_layer + n - 1 in one launch per up to 48
+        layers.  Independent inputs: x and y are [n, H] (layer l reads x[l],
+        writes y[l]).  chained=True: y is [n, H] and x is [1, H]; layer 0 reads
+        x, layer l > 0 reads y[l - 1]."""
+        H = self.hidden
+        if chained:
+            n = y.shape[0]
+            buf = torch.empty((n + 1, H), dtype=torch.bfloat16, device=y.device)
+            buf[0].copy_(x.reshape(H))
+            st = self.lib.moe_forward_decode_layers(self.handle, first_layer, n, _ptr(buf), H,
+                                                    ctypes.c_void_p(buf[1:].data_ptr()), H,
+                                                    _stream_handle(stream, self.device))
+            self._check(st, "moe_forward_decode_layers")
+            y.copy_(buf[1:])
+            return y
+        n = x.shape[0]
+        st = self.lib.moe_forward_decode_layers(self.handle, first_layer, n, _ptr(x), H, _ptr(y), H,
+                                                _stream_handle(stream, self.device))
+        self._check(st, "moe_forward_decode_layers")
+        return y
+
     def decode_routing(self, stream=None) -> dict:
         dev = self.device
         out = dict(logits=torch.empty((self.n_experts,), dtype=torch.float32, device=dev),

@@ -49,6 +49,8 @@ SIGNATURES = {
     "moe_route": (i32, [vp, i32, vp, i32, vp, vp, vp, vp, vp, vp, vp, vp]),
     "moe_forward_prefill": (i32, [vp, i32, vp, i32, vp, vp]),
     "moe_forward_decode": (i32, [vp, i32, vp, vp, vp]),
+    "moe_forward_decode_layers": (i32, [vp, i32, i32, vp, ctypes.c_size_t, vp, ctypes.c_size_t,
+                                        vp]),
     "moe_decode_routing": (i32, [vp, vp, vp, vp, vp]),
     "moe_forward_prefill_host": (i32, [vp, i32, vp, i32, vp, vp]),
     "moe_forward_decode_host": (i32, [vp, i32, vp, vp, vp]),

@@ -359,58 +359,44 @@ __device__ __forceinline__ void run_slot_task(const DecodeParams &p, int j, int 
   else slot_task<WF, false>(p, j, t0, n0, nrows, expert, part, w3, w3_sh);
 }
 
-// Persistent cooperative kernel, one CTA per SM (see the top of this file).
-template <int WF, int R>
-__global__ void __launch_bounds__(kDecLayerThreads, 1) decode_layer_kernel(const DecodeParams p) {
-  extern __shared__ __align__(128) unsigned char dsm[];
-  __shared__ __align__(8) uint64_t mbar[2];   // [0] shared expert rows, [1] routed rows
-  __shared__ int idx_s[32];
-  __shared__ float w_s[33];                   // routing weights, then the shared gate
+// Per-CTA state shared by every layer of a launch: the shared-memory carve-up
+// (part, staged output-projection rows), the CTA's output rows and its two
+// mbarriers (shared-expert rows, routed rows; one phase per layer).
+struct DecCta {
+  float *part;
+  unsigned char *w3, *w3_sh;
+  int n0, n1, nrows, ngroups;
+  uint32_t mb_sh, mb_rt;
+};
+
+template <int WF>
+__device__ __forceinline__ DecCta make_dec_cta(const DecodeParams &p, unsigned char *dsm,
+                                               uint64_t *mbar) {
   const DecSmem S = dec_smem<WF>(p.k, p.I, p.Is, p.p3_rows);
-  float *part = reinterpret_cast<float *>(dsm);
-  unsigned char *w3 = dsm + S.w3;
-  unsigned char *w3_sh = dsm + S.w3_sh;
-  const __nv_bfloat16 *x = reinterpret_cast<const __nv_bfloat16 *>(p.x);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int G = gridDim.x;
-  // warps numbered across CTAs first, so that a partly filled phase spreads
-  // over every SM
-  const int gw = warp * G + blockIdx.x;
-  const int nw = G * kDecWarps;
-  float *hg = p.h;   // [k+1][h_ld]: h of the k experts, then of the shared expert
-  // this CTA's output rows
-  const int n0 = static_cast<int>((static_cast<long long>(blockIdx.x) * p.H) / G);
-  const int n1 = static_cast<int>((static_cast<long long>(blockIdx.x + 1) * p.H) / G);
-  const int nrows = n1 - n0;
-  const int ngroups = (nrows + 7) / 8;
-  const size_t rbI = row_bytes<WF>(p.I), rbS = row_bytes<WF>(p.Is);
-  const uint32_t mb_sh = smem_u32(&mbar[0]), mb_rt = smem_u32(&mbar[1]);
+  DecCta c;
+  c.part = reinterpret_cast<float *>(dsm);
+  c.w3 = dsm + S.w3;
+  c.w3_sh = dsm + S.w3_sh;
+  c.n0 = static_cast<int>((static_cast<long long>(blockIdx.x) * p.H) / gridDim.x);
+  c.n1 = static_cast<int>((static_cast<long long>(blockIdx.x + 1) * p.H) / gridDim.x);
+  c.nrows = c.n1 - c.n0;
+  c.ngroups = (c.nrows + 7) / 8;
+  c.mb_sh = smem_u32(&mbar[0]);
+  c.mb_rt = smem_u32(&mbar[1]);
+  return c;
+}
 
-  DEC_MARK(0);
-#ifdef MOE_TRACE
-  const unsigned long long gt_start = gtimer();
-#endif
-  unsigned long long base = 0;   // barrier counter at launch (used by thread 0)
-  if (threadIdx.x == 0) {
-    // With a programmatic launch this CTA can start while the previous
-    // layer's CTAs finish, but only after the one on this SM exited, i.e.
-    // after that layer's last barrier completed: the counter is final.
-    const unsigned long long v = ld_acquire_u64(p.bar);
-    base = v - v % static_cast<unsigned long long>(G);
-    if (p.p3_stage) {
-      mbar_init(mb_sh, 1);
-      mbar_init(mb_rt, 1);
-      fence_mbarrier_init();
-      // the shared expert's output rows n0..n1 are needed whatever the routing
-      const uint32_t bytes = static_cast<uint32_t>(nrows * rbS);
-      mbar_arrive_expect_tx(mb_sh, bytes);
-      if (bytes) bulk_copy_g2s(smem_u32(w3_sh), row_ptr<WF>(p.sh_down, n0, p.Is), bytes, mb_sh);
-    }
+// Routing-independent weight traffic of layer p, which may start before the
+// layer's input is ready: thread 0 bulk-copies the CTA's rows of the shared
+// expert's output projection into shared memory (one phase of mb_sh), and
+// warp gw (numbered across CTAs) prefetches phase-A row gw into L2.
+template <int WF>
+__device__ __forceinline__ void layer_prefetch(const DecodeParams &p, const DecCta &c, int gw) {
+  if (threadIdx.x == 0 && p.p3_stage) {
+    const uint32_t bytes = static_cast<uint32_t>(c.nrows * row_bytes<WF>(p.Is));
+    mbar_arrive_expect_tx(c.mb_sh, bytes);
+    if (bytes) bulk_copy_g2s(smem_u32(c.w3_sh), row_ptr<WF>(p.sh_down, c.n0, p.Is), bytes, c.mb_sh);
   }
-
-  pdl_trigger();
-  // Everything above and the prefetch below read only weights; x, and every
-  // buffer this kernel writes, may still be in use by the previous layer.
   const int nA = p.E + 1 + p.Is;
   if (gw < nA) {
     if (gw < p.E) prefetch_row_l2(row_ptr<0>(p.router_w, gw, p.H), row_bytes<0>(p.H));
@@ -420,11 +406,35 @@ __global__ void __launch_bounds__(kDecLayerThreads, 1) decode_layer_kernel(const
       prefetch_row_l2(row_ptr<WF>(p.sh_gate_up, p.Is + gw - p.E - 1, p.H), row_bytes<WF>(p.H));
     }
   }
-  pdl_wait();
-#ifdef MOE_TRACE
-  const unsigned long long gt_wait = gtimer();
-#endif
+}
 
+// One decode layer, phases A to C (see the top of this file), after
+// layer_prefetch(p) has been issued and the layer's input is ready.  `par`
+// is the parity of this layer's mbarrier phases, bar_base the barrier
+// counter its two grid barriers count from (thread 0 only); `next`, if not
+// null, is the following layer, whose layer_prefetch is issued after this
+// layer's second grid barrier.
+template <int WF, int R>
+__device__ __forceinline__ void decode_layer(const DecodeParams &p, const DecCta &c, uint32_t par,
+                                             unsigned long long bar_base, const DecodeParams *next,
+                                             int *idx_s, float *w_s) {
+  float *part = c.part;
+  unsigned char *w3 = c.w3;
+  unsigned char *w3_sh = c.w3_sh;
+  const int n0 = c.n0, n1 = c.n1, nrows = c.nrows, ngroups = c.ngroups;
+  const uint32_t mb_sh = c.mb_sh, mb_rt = c.mb_rt;
+  const __nv_bfloat16 *x = reinterpret_cast<const __nv_bfloat16 *>(p.x);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = gridDim.x;
+  // warps numbered across CTAs first, so that a partly filled phase spreads
+  // over every SM
+  const int gw = warp * G + blockIdx.x;
+  const int nw = G * kDecWarps;
+  float *hg = p.h;   // [k+1][h_ld]: h of the k experts, then of the shared expert
+  const size_t rbI = row_bytes<WF>(p.I);
+  const int nA = p.E + 1 + p.Is;   // phase-A items: router rows, the gate row, shared pairs
+  (void)n1;
+  (void)lane;
   // ---- phase A: router rows, the shared gate row, shared-expert row pairs
   for (int it = gw; it < nA; it += nw) {
     if (it <= p.E) {
@@ -448,7 +458,7 @@ __global__ void __launch_bounds__(kDecLayerThreads, 1) decode_layer_kernel(const
     }
   }
   DEC_MARK(1);
-  grid_sync(p.bar, base + G, p.status);
+  grid_sync(p.bar, bar_base + G, p.status);
   DEC_MARK(2);
 
   // ---- top-k (one warp per CTA; the logits are in L2)
@@ -520,19 +530,29 @@ __global__ void __launch_bounds__(kDecLayerThreads, 1) decode_layer_kernel(const
   for (int s = kDecWarps - 1 - warp; s < ngroups; s += kDecWarps) {
     if (p.p3_stage) {
       volatile int no_abort = 0;
-      mbar_wait_bounded(mb_sh, 0, &no_abort, p.status, DEV_TIMEOUT_STAGE);
+      mbar_wait_bounded(mb_sh, par, &no_abort, p.status, DEV_TIMEOUT_STAGE);
     }
     run_slot_task<WF>(p, p.k, 8 * s, n0, nrows, 0, part, w3, w3_sh);
   }
   DEC_MARK(5);
-  grid_sync(p.bar, base + 2 * static_cast<unsigned long long>(G), p.status);
+  grid_sync(p.bar, bar_base + 2 * static_cast<unsigned long long>(G), p.status);
   DEC_MARK(6);
+  // The next layer's routing-independent weight traffic can start now: this
+  // layer's shared-expert rows are consumed (phase B) and DRAM is idle from
+  // here on.
+  if (next != nullptr) {
+    if (threadIdx.x == 0 && p.p3_stage) {
+      volatile int no_abort = 0;   // this layer's phase of mb_sh is complete
+      mbar_wait_bounded(mb_sh, par, &no_abort, p.status, DEV_TIMEOUT_STAGE);
+    }
+    layer_prefetch<WF>(*next, c, gw);
+  }
 
   // ---- phase C: the routed slots, one (slot j, group of 8 rows) per warp
   if (p.p3_stage) {
     // the staged rows must have landed before this thread reads them
     volatile int no_abort = 0;
-    mbar_wait_bounded(mb_rt, 0, &no_abort, p.status, DEV_TIMEOUT_STAGE);
+    mbar_wait_bounded(mb_rt, par, &no_abort, p.status, DEV_TIMEOUT_STAGE);
   }
   DEC_MARK(7);
   for (int task = warp; task < p.k * ngroups; task += kDecWarps) {
@@ -558,40 +578,141 @@ __global__ void __launch_bounds__(kDecLayerThreads, 1) decode_layer_kernel(const
     }
     reinterpret_cast<__nv_bfloat16 *>(p.y)[n0 + t] = __float2bfloat16_rn(y);
   }
+}
+
+// Persistent cooperative kernel, one CTA per SM (see the top of this file):
+// one layer.
+template <int WF, int R>
+__global__ void __launch_bounds__(kDecLayerThreads, 1) decode_layer_kernel(const DecodeParams p) {
+  extern __shared__ __align__(128) unsigned char dsm[];
+  __shared__ __align__(8) uint64_t mbar[2];   // [0] shared expert rows, [1] routed rows
+  __shared__ int idx_s[32];
+  __shared__ float w_s[33];                   // routing weights, then the shared gate
+  const DecCta c = make_dec_cta<WF>(p, dsm, mbar);
+  const int G = gridDim.x;
+  const int gw = (threadIdx.x >> 5) * G + blockIdx.x;
+
+  DEC_MARK(0);
+#ifdef MOE_TRACE
+  const unsigned long long gt_start = gtimer();
+#endif
+  unsigned long long base = 0;   // barrier counter at launch (used by thread 0)
+  if (threadIdx.x == 0) {
+    // With a programmatic launch this CTA can start while the previous
+    // layer's CTAs finish, but only after the one on this SM exited, i.e.
+    // after that layer's last barrier completed: the counter is final.
+    const unsigned long long v = ld_acquire_u64(p.bar);
+    base = v - v % static_cast<unsigned long long>(G);
+    if (p.p3_stage) {
+      mbar_init(c.mb_sh, 1);
+      mbar_init(c.mb_rt, 1);
+      fence_mbarrier_init();
+    }
+  }
+  // Only weights are read before the wait below: x, and every buffer this
+  // kernel writes, may still be in use by the previous layer.
+  layer_prefetch<WF>(p, c, gw);
+  pdl_trigger();
+  pdl_wait();
+  decode_layer<WF, R>(p, c, 0u, base, nullptr, idx_s, w_s);
   DEC_MARK(9);
   DEC_MARK(10);
 #ifdef MOE_TRACE
   if (threadIdx.x == 0 && blockIdx.x < 160) {
     const int slot = static_cast<int>((base / (2ull * G)) % 64);
     g_dec_gt[slot][blockIdx.x][0] = gt_start;
-    g_dec_gt[slot][blockIdx.x][1] = gt_wait;
     g_dec_gt[slot][blockIdx.x][2] = gtimer();
   }
-#endif
-#ifdef MOE_TRACE
   if (threadIdx.x == 0) g_dec_trace[blockIdx.x & 1023][15] = p.p3_stage + 10 * p.p3_rows;
 #endif
 }
 
+// The same for n consecutive layers in one launch (P.layer[0..n-1], same
+// shapes): layer l + 1 starts after a grid barrier that follows layer l's
+// last write (so its input may be layer l's output), and its
+// routing-independent weight traffic starts during layer l's output
+// projection.  The barrier counter advances by 3 n - 1 grid widths.
 template <int WF, int R>
-static cudaError_t launch_layer(DecodeParams p, int grid, int smem_limit, bool pdl,
-                                cudaStream_t stream) {
+__global__ void __launch_bounds__(kDecLayerThreads, 1)
+    decode_layers_kernel(const __grid_constant__ DecodeLayersParams P) {
+  extern __shared__ __align__(128) unsigned char dsm[];
+  __shared__ __align__(8) uint64_t mbar[2];
+  __shared__ int idx_s[32];
+  __shared__ float w_s[33];
+  const DecodeParams &p0 = P.layer[0];
+  const DecCta c = make_dec_cta<WF>(p0, dsm, mbar);
+  const int G = gridDim.x;
+  const int gw = (threadIdx.x >> 5) * G + blockIdx.x;
+  unsigned long long base = 0;
+  if (threadIdx.x == 0) {
+    const unsigned long long v = ld_acquire_u64(p0.bar);
+    base = v - v % static_cast<unsigned long long>(G);
+    if (p0.p3_stage) {
+      mbar_init(c.mb_sh, 1);
+      mbar_init(c.mb_rt, 1);
+      fence_mbarrier_init();
+    }
+  }
+  layer_prefetch<WF>(p0, c, gw);
+  pdl_trigger();
+  pdl_wait();
+  for (int l = 0; l < P.n; ++l) {
+    const DecodeParams &p = P.layer[l];
+    const unsigned long long lb = base + 3ull * static_cast<unsigned long long>(l) * G;
+    decode_layer<WF, R>(p, c, static_cast<uint32_t>(l & 1), lb,
+                        l + 1 < P.n ? &P.layer[l + 1] : nullptr, idx_s, w_s);
+    // layer l's outputs are complete before layer l + 1 reads its input
+    if (l + 1 < P.n) grid_sync(p.bar, lb + 3ull * G, p.status);
+  }
+}
+
+template <int WF>
+static void set_p3(DecodeParams &p, int grid, int smem_limit, size_t *smem) {
   p.p3_rows = (p.H + grid - 1) / grid;
   const DecSmem S = dec_smem<WF>(p.k, p.I, p.Is, p.p3_rows);
   p.p3_stage = S.staged <= static_cast<size_t>(smem_limit) ? 1 : 0;
+  *smem = p.p3_stage ? S.staged : S.unstaged;
+}
+
+static cudaLaunchConfig_t dec_config(int grid, size_t smem, bool pdl, cudaStream_t stream,
+                                     cudaLaunchAttribute (&attr)[2]) {
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeCooperative;
   attr[0].val.cooperative = 1;
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.gridDim = dim3(grid, 1, 1);
   cfg.blockDim = dim3(kDecLayerThreads, 1, 1);
-  cfg.dynamicSmemBytes = p.p3_stage ? S.staged : S.unstaged;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 2 : 1;
+  return cfg;
+}
+
+template <int WF, int R>
+static cudaError_t launch_layer(DecodeParams p, int grid, int smem_limit, bool pdl,
+                                cudaStream_t stream) {
+  size_t smem = 0;
+  set_p3<WF>(p, grid, smem_limit, &smem);
+  cudaLaunchAttribute attr[2];
+  const cudaLaunchConfig_t cfg = dec_config(grid, smem, pdl, stream, attr);
   return cudaLaunchKernelEx(&cfg, decode_layer_kernel<WF, R>, p);
+}
+
+template <int WF, int R>
+static cudaError_t launch_layers(const DecodeParams *layers, int n, int grid, int smem_limit,
+                                 bool pdl, cudaStream_t stream) {
+  DecodeLayersParams P;
+  size_t smem = 0;
+  P.n = n;
+  for (int l = 0; l < n; ++l) {
+    P.layer[l] = layers[l];
+    set_p3<WF>(P.layer[l], grid, smem_limit, &smem);
+  }
+  cudaLaunchAttribute attr[2];
+  const cudaLaunchConfig_t cfg = dec_config(grid, smem, pdl, stream, attr);
+  return cudaLaunchKernelEx(&cfg, decode_layers_kernel<WF, R>, P);
 }
 
 cudaError_t launch_decode_layer(const DecodeParams &p, int grid, int smem_limit, bool pdl,
@@ -601,6 +722,17 @@ cudaError_t launch_decode_layer(const DecodeParams &p, int grid, int smem_limit,
                       : launch_layer<0, 32>(p, grid, smem_limit, pdl, stream);
   return p.E <= 256 ? launch_layer<1, 8>(p, grid, smem_limit, pdl, stream)
                     : launch_layer<1, 32>(p, grid, smem_limit, pdl, stream);
+}
+
+cudaError_t launch_decode_layers(const DecodeParams *layers, int n, int grid, int smem_limit,
+                                 bool pdl, cudaStream_t stream) {
+  if (n < 1 || n > kMaxDecodeLayers) return cudaErrorInvalidValue;
+  const DecodeParams &p = layers[0];
+  if (p.wfmt == 0)
+    return p.E <= 256 ? launch_layers<0, 8>(layers, n, grid, smem_limit, pdl, stream)
+                      : launch_layers<0, 32>(layers, n, grid, smem_limit, pdl, stream);
+  return p.E <= 256 ? launch_layers<1, 8>(layers, n, grid, smem_limit, pdl, stream)
+                    : launch_layers<1, 32>(layers, n, grid, smem_limit, pdl, stream);
 }
 
 cudaError_t decode_configure(int *smem_limit) {
@@ -620,6 +752,14 @@ cudaError_t decode_configure(int *smem_limit) {
       (e = cudaFuncSetAttribute(decode_layer_kernel<1, 8>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) ||
       (e = cudaFuncSetAttribute(decode_layer_kernel<1, 32>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) ||
+      (e = cudaFuncSetAttribute(decode_layers_kernel<0, 8>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) ||
+      (e = cudaFuncSetAttribute(decode_layers_kernel<0, 32>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) ||
+      (e = cudaFuncSetAttribute(decode_layers_kernel<1, 8>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) ||
+      (e = cudaFuncSetAttribute(decode_layers_kernel<1, 32>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)))
     return e;
   *smem_limit = bytes;

@@ -126,11 +126,11 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 
 
 enum KernelId : int {
   K_ROUTER_GEMM = 0, K_TOPK, K_SCAN, K_SCATTER, K_GATEUP_GEMM, K_DOWN_GEMM, K_COMBINE,
-  K_DEC_LAYER, K_H2D, K_D2H, K_COUNT
+  K_DEC_LAYER, K_H2D, K_D2H, K_DEC_LAYERS, K_COUNT
 };
 const char *kKernelNames[K_COUNT] = {
     "router_gemm", "topk", "route_scan", "route_scatter", "gateup_swiglu_gemm", "down_gemm",
-    "combine", "decode_layer", "h2d_copy", "d2h_copy"};
+    "combine", "decode_layer", "h2d_copy", "d2h_copy", "decode_layers"};
 
 }  // namespace
 
@@ -454,8 +454,7 @@ moe_status check_layer(moe_ctx *ctx, int layer) {
   return MOE_OK;
 }
 
-moe_status enqueue_decode(moe_ctx *ctx, const LayerSlot &ls, const void *x, void *y,
-                          cudaStream_t s) {
+DecodeParams decode_params(const moe_ctx *ctx, const LayerSlot &ls, const void *x, void *y) {
   const moe_config &c = ctx->cfg;
   const WsLayout &L = ctx->L;
   DecodeParams p{};
@@ -486,6 +485,12 @@ moe_status enqueue_decode(moe_ctx *ctx, const LayerSlot &ls, const void *x, void
   p.h_ld = L.Imax;
   p.bar = ctx->at<unsigned long long>(L.dec_counter);
   p.status = ctx->status();
+  return p;
+}
+
+moe_status enqueue_decode(moe_ctx *ctx, const LayerSlot &ls, const void *x, void *y,
+                          cudaStream_t s) {
+  const DecodeParams p = decode_params(ctx, ls, x, y);
   ProfScope ps(ctx, K_DEC_LAYER, s);
   return launched(ctx, launch_decode_layer(p, ctx->decode_grid, ctx->decode_smem, ctx->decode_pdl, s),
                   "decode layer launch");
@@ -678,6 +683,42 @@ moe_status moe_forward_decode(moe_ctx *ctx, int layer, const void *x, void *y, v
     return fail(ctx, MOE_ERR_INVALID_ARG, "x/y null or not 16-byte aligned");
   if ((st = ensure_device(ctx))) return st;
   return enqueue_decode(ctx, ctx->layers[layer], x, y, static_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_forward_decode_layers(moe_ctx *ctx, int first_layer, int n_layers, const void *x,
+                                     size_t x_stride, void *y, size_t y_stride, void *stream) {
+  if (!ctx) return MOE_ERR_INVALID_ARG;
+  if (n_layers < 0 || first_layer < 0 || first_layer + n_layers > ctx->cfg.n_layers)
+    return fail(ctx, MOE_ERR_INVALID_ARG, "layers [%d, %d) outside the context's %d slots",
+                first_layer, first_layer + n_layers, ctx->cfg.n_layers);
+  if (n_layers == 0) return MOE_OK;
+  if (!x || !y || !aligned16(x) || !aligned16(y) || (x_stride & 7) || (y_stride & 7))
+    return fail(ctx, MOE_ERR_INVALID_ARG, "x/y null or rows not 16-byte aligned");
+  for (int l = first_layer; l < first_layer + n_layers; ++l) {
+    moe_status st = check_layer(ctx, l);
+    if (st) return st;
+  }
+  moe_status st = ensure_device(ctx);
+  if (st) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const char *xb = static_cast<const char *>(x);
+  char *yb = static_cast<char *>(y);
+  DecodeParams ps[kMaxDecodeLayers];
+  for (int l0 = 0; l0 < n_layers; l0 += kMaxDecodeLayers) {
+    const int n = std::min(kMaxDecodeLayers, n_layers - l0);
+    for (int i = 0; i < n; ++i) {
+      const size_t l = static_cast<size_t>(l0 + i);
+      ps[i] = decode_params(ctx, ctx->layers[first_layer + l0 + i], xb + l * x_stride * 2,
+                            yb + l * y_stride * 2);
+    }
+    ProfScope pr(ctx, K_DEC_LAYERS, s);
+    st = launched(ctx,
+                  launch_decode_layers(ps, n, ctx->decode_grid, ctx->decode_smem, ctx->decode_pdl,
+                                       s),
+                  "multi-layer decode launch");
+    if (st) return st;
+  }
+  return MOE_OK;
 }
 
 moe_status moe_decode_routing(moe_ctx *ctx, float *logits, int32_t *idx, float *w, void *stream) {

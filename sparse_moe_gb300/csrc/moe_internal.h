@@ -116,6 +116,12 @@ struct DecodeParams {
   int *status;               // device status word
   int p3_rows, p3_stage;     // set by launch_decode_layer
 };
+// Up to kMaxDecodeLayers layers (same shapes) for one multi-layer decode launch.
+constexpr int kMaxDecodeLayers = 48;
+struct DecodeLayersParams {
+  DecodeParams layer[kMaxDecodeLayers];
+  int n;
+};
 // Floats of the h region a decode needs.
 inline size_t decode_h_floats(int k, int h_ld) { return (static_cast<size_t>(k) + 1) * h_ld; }
 // Raises the decode kernel's dynamic shared-memory limit on the current
@@ -128,5 +134,9 @@ int decode_layer_grid(int num_sms);
 // start while the previous kernel in the stream finishes.
 cudaError_t launch_decode_layer(const DecodeParams &p, int grid, int smem_limit, bool pdl,
                                 cudaStream_t stream);
+// n consecutive layers (1 <= n <= kMaxDecodeLayers) in one launch of the
+// same grid: layer l + 1 starts after a grid barrier behind layer l's outputs.
+cudaError_t launch_decode_layers(const DecodeParams *layers, int n, int grid, int smem_limit,
+                                 bool pdl, cudaStream_t stream);
 
 }  // namespace moe

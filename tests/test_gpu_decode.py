@@ -1,5 +1,7 @@
 """Batch-1 decode GEMV path (bf16 and int4) against the fp64 oracle, which
 selects experts from the decode router's own fp32 logits."""
+import ctypes
+
 import numpy as np
 import pytest
 import torch
@@ -7,6 +9,7 @@ import torch
 import moe_synth
 from gpu_helpers import assert_layer_close, host_layer, logits_bound, make_ctx
 from oracle import moe_oracle as orc
+from sparse_moe_gb300 import MoEError, _abi
 
 pytestmark = pytest.mark.gpu
 
@@ -103,3 +106,78 @@ def test_decode_int4_tiny():
     wl = moe_synth.Workload("d4", moe_synth.TINY, T=1, wfmt=moe_synth.WFMT_INT4, seed=12)
     ctx, (w,) = make_ctx(wl, max_chunk_rows=16)
     _check_decode(ctx, w, moe_synth.make_x(wl, device="cuda"), int4=True)
+
+
+# ---- several layers in one persistent launch: the same arithmetic as one
+# launch per layer, so the outputs must match bit for bit, with independent
+# inputs and with each layer's output feeding the next layer.
+
+def _layers_ctx(wl, n):
+    return make_ctx(wl, n_layers=n, max_chunk_rows=16, seed_layers=list(range(n)))
+
+
+@pytest.mark.parametrize("wl", [moe_synth.DECODE_BF16, moe_synth.DECODE_INT4],
+                         ids=["bf16", "int4"])
+def test_decode_layers_independent_inputs_match_single_launches(wl):
+    n = 3
+    ctx, _ = _layers_ctx(wl, n)
+    xs = torch.cat([moe_synth.make_x(wl, layer=l, device="cuda") for l in range(n)])
+    ref = torch.stack([ctx.forward_decode(l, xs[l:l + 1])[0] for l in range(n)])
+    y = torch.empty_like(xs)
+    ctx.forward_decode_layers(0, xs, y)
+    torch.cuda.synchronize()
+    assert torch.equal(y, ref)
+    assert ctx.check_device() == 0
+
+
+def test_decode_layers_chained_match_single_launches(decode_bf16):
+    wl, ctx, layers = decode_bf16
+    x0 = moe_synth.make_x(wl, layer=5, device="cuda")
+    ref, x = [], x0
+    for l in range(2):
+        x = ctx.forward_decode(l, x)
+        ref.append(x[0].clone())
+    y = torch.empty((2, wl.shape.hidden), dtype=torch.bfloat16, device="cuda")
+    ctx.forward_decode_layers(0, x0, y, chained=True)
+    torch.cuda.synchronize()
+    assert torch.equal(y, torch.stack(ref))
+    # the last layer's routing is the one reported
+    r = ctx.decode_routing()
+    lg = r["logits"].cpu().numpy()[None, :]
+    o = orc.route(lg, ctx.top_k)
+    np.testing.assert_array_equal(r["topk_idx"].cpu().numpy(), o["topk_idx"][0])
+
+
+def test_decode_layers_more_than_one_launch_and_oracle():
+    """50 tiny layers (two launches of at most 48), chained; the first layer's
+    output (equal to the multi-layer one) is also checked against the oracle.
+    (Chained through 50 random layers the signal fades towards zero, so the
+    relative error of a late layer is not a meaningful check.)"""
+    wl = moe_synth.Workload("dl", moe_synth.TINY, T=1, seed=13)
+    n = 50
+    ctx, layers = _layers_ctx(wl, n)
+    x0 = moe_synth.make_x(wl, device="cuda")
+    ref, x = [], x0
+    for l in range(n):
+        x = ctx.forward_decode(l, x)
+        ref.append(x[0].clone())
+    y = torch.empty((n, wl.shape.hidden), dtype=torch.bfloat16, device="cuda")
+    ctx.forward_decode_layers(0, x0, y, chained=True)
+    torch.cuda.synchronize()
+    assert torch.equal(y, torch.stack(ref))
+    y0, _ = _check_decode(ctx, layers[0], x0, layer=0)
+    assert torch.equal(y0[0], y[0])
+
+
+def test_decode_layers_rejects_bad_arguments(decode_bf16):
+    wl, ctx, _ = decode_bf16
+    H = wl.shape.hidden
+    x = torch.zeros((3, H), dtype=torch.bfloat16, device="cuda")
+    y = torch.empty_like(x)
+    with pytest.raises(MoEError):
+        ctx.forward_decode_layers(0, x, y)          # slots 0..2 of a 2-slot context
+    lib = ctx.lib
+    st = lib.moe_forward_decode_layers(ctx.handle, 0, 2, ctypes.c_void_p(x.data_ptr()), 3,
+                                       ctypes.c_void_p(y.data_ptr()), H, None)
+    assert st == _abi.MOE_ERR_INVALID_ARG             # stride not a multiple of 8
+    assert lib.moe_forward_decode_layers(ctx.handle, 0, 0, None, 0, None, 0, None) == _abi.MOE_OK
