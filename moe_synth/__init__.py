@@ -28,6 +28,16 @@ int4 symmetric, group 64 along K (the compressed variant):
     <name>_scale  bf16  [rows, K/64]
 
 Codes are drawn uniformly from [-7, 7]; scales are |N(0, 0.02)| / 7.
+
+int4 affine, group 64 along K (the checkpoint format of section "Dequantize
+weights during matrix multiplication": a bf16 scale and a bf16 bias per group):
+    <name>        uint8 [rows, K/2]    unsigned codes in [0, 15], same packing
+    <name>_scale  bf16  [rows, K/64]
+    <name>_bias   bf16  [rows, K/64]   (weight = scale * code + bias)
+
+Codes are drawn uniformly from [0, 15]; scales are |N(0, 0.02)| / 7 and biases
+-scale * (7.5 + N(0, 0.5)), so each group spans about the range a min-max
+quantiser of N(0, 0.02) weights would give it.
 """
 from __future__ import annotations
 
@@ -38,6 +48,7 @@ import torch
 
 WFMT_BF16 = "bf16"
 WFMT_INT4 = "int4_sym_g64"
+WFMT_INT4_AFFINE = "int4_affine_g64"
 
 GROUP = 64
 
@@ -80,6 +91,11 @@ DECODE_INT4 = Workload("decode_T1_H2048_E256_k8_I512_int4g64_40layers", QWEN, T=
                        wfmt=WFMT_INT4, seed=2000, n_layers=40)
 PREFILL_INT4 = Workload("prefill_T4096_H2048_E256_k8_I512_int4g64_bias1.5", QWEN,
                         T=4096, wfmt=WFMT_INT4, bias_std=1.5, seed=1)
+# The affine int4 format of the page's checkpoint (a scale and a bias per 64).
+DECODE_INT4_AFFINE = Workload("decode_T1_H2048_E256_k8_I512_int4affg64_40layers", QWEN, T=1,
+                              wfmt=WFMT_INT4_AFFINE, seed=3000, n_layers=40)
+PREFILL_INT4_AFFINE = Workload("prefill_T4096_H2048_E256_k8_I512_int4affg64_bias1.5", QWEN,
+                               T=4096, wfmt=WFMT_INT4_AFFINE, bias_std=1.5, seed=3)
 SWEEP_T = (256, 512, 1024, 2048, 4096, 8192, 16384, 32768, 65536, 131072)
 
 
@@ -117,6 +133,27 @@ def pack_int4(codes: torch.Tensor) -> torch.Tensor:
     """Pack signed codes in [-8, 7] (last dim even) two per byte, even index low."""
     c = codes.to(torch.int16) & 0xF
     return (c[..., 0::2] | (c[..., 1::2] << 4)).to(torch.uint8)
+
+
+def _int4_affine_weight(shape, std, g, device):
+    """Random affine int4 weight: packed codes U{0..15}, |N(0,std)|/7 scales and
+    biases -scale * (7.5 + N(0, 0.5)), all per group of 64 along K."""
+    *lead, K = shape
+    assert K % GROUP == 0
+    packed = torch.empty(tuple(lead) + (K // 2,), dtype=torch.uint8, device=device)
+    rows = packed.view(-1, K // 2)
+    step = 1 << 14
+    for r0 in range(0, rows.shape[0], step):
+        r1 = min(rows.shape[0], r0 + step)
+        codes = torch.randint(0, 16, (r1 - r0, K), generator=g, device=device, dtype=torch.int16)
+        rows[r0:r1] = pack_int4(codes)
+    gshape = tuple(lead) + (K // GROUP,)
+    scale32 = torch.randn(gshape, generator=g, device=device, dtype=torch.float32).abs_().mul_(
+        std / 7.0)
+    scale = scale32.to(torch.bfloat16)
+    z = torch.randn(gshape, generator=g, device=device, dtype=torch.float32).mul_(0.5).add_(7.5)
+    bias = (-scale.float() * z).to(torch.bfloat16)
+    return packed, scale, bias
 
 
 def _int4_weight(shape, std, g, device):
@@ -174,6 +211,11 @@ def make_layer(wl: Workload, layer: int = 0, device="cpu") -> dict:
             (2 * Is, H), std, _gen(wl.seed, "sh_gate_up", layer, device), device)
         out["sh_down"], out["sh_down_scale"] = _int4_weight(
             (H, Is), std, _gen(wl.seed, "sh_down", layer, device), device)
+    elif wl.wfmt == WFMT_INT4_AFFINE:
+        for name, shape in (("gate_up", (E, 2 * I, H)), ("down", (E, H, I)),
+                            ("sh_gate_up", (2 * Is, H)), ("sh_down", (H, Is))):
+            out[name], out[name + "_scale"], out[name + "_bias"] = _int4_affine_weight(
+                shape, std, _gen(wl.seed, name, layer, device), device)
     else:
         raise ValueError(wl.wfmt)
     out["sh_gate_w"] = _normal_bf16((H,), std, _gen(wl.seed, "sh_gate_w", layer, device), device)
@@ -197,7 +239,7 @@ def expert_slice(layer: dict, experts) -> dict:
     """Subset of the routed-expert tensors (host copies), for sampled checks at full size."""
     idx = torch.as_tensor(list(experts), dtype=torch.long, device=layer["gate_up"].device)
     out = dict(layer)
-    for k in ("gate_up", "gate_up_scale", "down", "down_scale"):
-        if layer[k] is not None:
+    for k in ("gate_up", "gate_up_scale", "gate_up_bias", "down", "down_scale", "down_bias"):
+        if layer.get(k) is not None:
             out[k] = layer[k].index_select(0, idx)
     return out

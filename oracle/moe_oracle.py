@@ -29,8 +29,10 @@ Readings of what the page leaves open (each one is stated where it is used):
   * the gated activation is SwiGLU: silu(gate) * up, silu(z) = z / (1 + e^-z);
   * the shared expert's output is scaled by sigmoid(x . w_sg), a scalar per
     token, and is not renormalised with the routed weights;
-  * the int4 format is symmetric: w = scale * q, q the two's-complement
-    nibble in [-8, 7], element 2m in the low nibble of byte m;
+  * the int4 formats: symmetric, w = scale * q with q the two's-complement
+    nibble in [-8, 7]; and affine (the page's checkpoint format: a bf16 scale
+    and a bf16 bias per group of 64), w = scale * q + bias with q the unsigned
+    nibble in [0, 15]; element 2m in the low nibble of byte m in both;
   * inside an expert's group, rows are ordered by ascending token index.
 
 Everything is evaluated in float64 with no intermediate rounding.
@@ -63,6 +65,24 @@ def dequant_int4_sym_g64(packed, scale) -> np.ndarray:
     return np.repeat(s, GROUP, axis=-1) * q
 
 
+def dequant_int4_affine_g64(packed, scale, bias) -> np.ndarray:
+    """Affine int4, group 64 along K: w[r, k] = scale[r, k // 64] * q[r, k] +
+    bias[r, k // 64], q the unsigned code in [0, 15] (same packing as the
+    symmetric format).  Section "Dequantize weights during matrix
+    multiplication": each weight is a 4-bit integer code, and every group of 64
+    weights shares a bfloat16 scale and bias that reconstruct its values.
+    """
+    packed = np.asarray(packed, dtype=np.uint8)
+    K = packed.shape[-1] * 2
+    q = np.empty(packed.shape[:-1] + (K,), dtype=np.int64)
+    q[..., 0::2] = packed & 0x0F
+    q[..., 1::2] = packed >> 4
+    s = np.asarray(scale, dtype=np.float64)
+    b = np.asarray(bias, dtype=np.float64)
+    assert s.shape[-1] * GROUP == K and b.shape == s.shape, "one scale and bias per 64 along K"
+    return np.repeat(s, GROUP, axis=-1) * q + np.repeat(b, GROUP, axis=-1)
+
+
 def _f64(a) -> np.ndarray:
     return np.asarray(a, dtype=np.float64)
 
@@ -71,11 +91,15 @@ def _matrix(layer: dict, name: str, index=None) -> np.ndarray:
     """A weight matrix (or one expert's slice of it) in float64."""
     w = layer[name]
     s = layer.get(name + "_scale")
+    b = layer.get(name + "_bias")
     if index is not None:
         w = w[index]
         s = None if s is None else s[index]
+        b = None if b is None else b[index]
     if s is None:
         return _f64(w)
+    if b is not None:
+        return dequant_int4_affine_g64(w, s, b)
     return dequant_int4_sym_g64(w, s)
 
 

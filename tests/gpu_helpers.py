@@ -15,8 +15,9 @@ import moe_synth
 from oracle import moe_oracle as orc
 from sparse_moe_gb300 import MoEContext
 
-WEIGHT_KEYS = ("router_w", "router_b", "gate_up", "gate_up_scale", "down", "down_scale",
-               "sh_gate_up", "sh_gate_up_scale", "sh_down", "sh_down_scale", "sh_gate_w")
+WEIGHT_KEYS = ("router_w", "router_b", "gate_up", "gate_up_scale", "gate_up_bias", "down",
+               "down_scale", "down_bias", "sh_gate_up", "sh_gate_up_scale", "sh_gate_up_bias",
+               "sh_down", "sh_down_scale", "sh_down_bias", "sh_gate_w")
 
 
 def make_ctx(wl, n_layers=1, max_chunk_rows=4096, seed_layers=None):
@@ -51,7 +52,7 @@ def host_layer(w: dict) -> dict:
         v = w.get(k)
         if v is None:
             out[k] = None
-        elif k in ("gate_up", "gate_up_scale", "down", "down_scale"):
+        elif k in ("gate_up", "gate_up_scale", "gate_up_bias", "down", "down_scale", "down_bias"):
             out[k] = _LazyExperts(v)
         else:
             out[k] = v.float().cpu().numpy() if v.dtype == torch.bfloat16 else v.cpu().numpy()

@@ -364,3 +364,80 @@ def test_generator_distributions():
     # same seed, same bytes
     again = moe_synth.to_numpy(moe_synth.make_layer(wl4))
     assert np.array_equal(again["down"], L4["down"])
+
+
+# --------------------------------------------------------- int4 affine --
+
+def test_int4_affine_nibble_decoding_golden():
+    """Unsigned codes, low nibble first, from hand-decoded bytes; all 16 codes
+    appear; scale 1 and bias 0 return the codes themselves."""
+    gold = json.load(open(os.path.join(GOLDEN, "int4_affine_nibbles.json")))
+    byts = np.array([[int(c["byte"], 16) for c in gold["cases"]]], dtype=np.uint8)
+    codes = np.array([c["codes"] for c in gold["cases"]]).reshape(1, -1)
+    K = byts.shape[1] * 2
+    pad = (-K) % 64
+    byts = np.concatenate([byts, np.zeros((1, pad // 2), np.uint8)], 1)
+    G = byts.shape[1] * 2 // 64
+    w = orc.dequant_int4_affine_g64(byts, np.ones((1, G)), np.zeros((1, G)))
+    assert w[0, :K].tolist() == codes[0].tolist()
+    assert sorted(set(codes[0].tolist())) == list(range(16))
+
+
+def test_int4_affine_with_bias_minus_8_scale_is_symmetric_format():
+    """Closed form linking the two formats: for any bytes, flipping the top bit
+    of every nibble (u -> u ^ 8) maps the unsigned code u to the two's-complement
+    code q with u ^ 8 - 8 = q, so affine(bytes ^ 0x88, s, -8 s) == symmetric(bytes, s)."""
+    rng = np.random.default_rng(7)
+    byts = rng.integers(0, 256, size=(5, 96), dtype=np.uint8)
+    # dyadic scales (small integer times a power of two): every product and
+    # sum below is exact in fp64, so the two sides must agree bit for bit
+    s = rng.choice([-1.0, 1.0], (5, 3)) * rng.integers(1, 64, (5, 3)) * 2.0 ** -rng.integers(
+        4, 12, (5, 3)).astype(np.float64)
+    sym = orc.dequant_int4_sym_g64(byts, s)
+    aff = orc.dequant_int4_affine_g64(byts ^ np.uint8(0x88), s, -8.0 * s)
+    np.testing.assert_array_equal(aff, sym)
+
+
+def test_int4_affine_onehot_gemv_returns_dequantised_column():
+    """x = e_k through a GEMV picks column k: scale * code + bias of group
+    k // 64, exactly (dyadic scales and biases)."""
+    R, K = 3, 192
+    codes = np.array([[(r * 7 + k * 5) % 16 for k in range(K)] for r in range(R)])
+    scales = np.array([[2.0 ** -(r + g + 2) for g in range(K // 64)] for r in range(R)])
+    biases = np.array([[-(g + 1) * 2.0 ** -(r + 1) for g in range(K // 64)] for r in range(R)])
+    packed = (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)
+    W = orc.dequant_int4_affine_g64(packed, scales, biases)
+    for k in (0, 1, 63, 64, 65, 127, 128, 191):
+        x = np.zeros(K)
+        x[k] = 1.0
+        col = W @ x
+        for r in range(R):
+            g = k // 64
+            assert col[r] == codes[r, k] * 2.0 ** -(r + g + 2) - (g + 1) * 2.0 ** -(r + 1)
+
+
+def test_int4_affine_layer_equals_layer_on_dequantised_weights():
+    wl = moe_synth.Workload("tiny_int4a", moe_synth.TINY, T=8, wfmt=moe_synth.WFMT_INT4_AFFINE,
+                            seed=4)
+    x = moe_synth.make_x(wl).float().numpy()
+    layer = moe_synth.to_numpy(moe_synth.make_layer(wl))
+    deq = dict(layer)
+    for name in ("gate_up", "down", "sh_gate_up", "sh_down"):
+        deq[name] = orc.dequant_int4_affine_g64(layer[name], layer[name + "_scale"],
+                                                layer[name + "_bias"])
+        deq[name + "_scale"] = deq[name + "_bias"] = None
+    np.testing.assert_allclose(orc.moe_layer(x, layer, 2), orc.moe_layer(x, deq, 2),
+                               rtol=1e-13, atol=1e-16)
+
+
+def test_generator_affine_distribution():
+    wl = moe_synth.Workload("g4a", moe_synth.TINY, T=4, wfmt=moe_synth.WFMT_INT4_AFFINE, seed=5)
+    L = moe_synth.to_numpy(moe_synth.make_layer(wl))
+    G = L["gate_up_scale"].shape
+    q = orc.dequant_int4_affine_g64(L["gate_up"], np.ones(G), np.zeros(G))
+    assert q.min() == 0 and q.max() == 15
+    s, b = L["gate_up_scale"], L["gate_up_bias"]
+    assert np.all(s > 0) and np.all(b < 0)
+    assert abs(np.median(-b / s) - 7.5) < 0.1
+    w = orc.dequant_int4_affine_g64(L["gate_up"], s, b)
+    assert abs(w.mean()) < 1e-3 and 0.01 < w.std() < 0.04
