@@ -135,10 +135,11 @@ def algorithmic(s: moe_synth.Shape, T: int):
     return gateup_flops, down_flops, router_flops
 
 
-def decode_bytes(s: moe_synth.Shape, int4: bool):
+def decode_bytes(s: moe_synth.Shape, int4: bool, affine: bool = False):
     H, E, k, I, Is = s.hidden, s.n_experts, s.top_k, s.inter, s.shared_inter
     if int4:
-        per = lambda rows, K: rows * K // 2 + rows * (K // 64) * 2  # noqa: E731
+        ng = 2 if affine else 1   # scales, and biases for the affine format
+        per = lambda rows, K: rows * K // 2 + ng * rows * (K // 64) * 2  # noqa: E731
     else:
         per = lambda rows, K: rows * K * 2  # noqa: E731
     routed_gu = k * per(2 * I, H)
@@ -201,11 +202,10 @@ def run_prefill_e2e(ctx, x_h, y_h, steps, warmup, flush, stream):
     return float(np.sum([a.elapsed_time(b) for a, b in zip(starts, ends)]))
 
 
-def bench_prefill_int4(args, dev, stream, flush, tf_burst):
-    """The int4 (symmetric, group 64) prefill workload at T=4096: weights are
-    dequantised tile by tile inside the grouped GEMMs."""
+def bench_prefill_int4(args, dev, stream, flush, tf_burst, wl=moe_synth.PREFILL_INT4):
+    """An int4 prefill workload at T=4096 (symmetric, or affine with a bias
+    per group): weights are dequantised tile by tile inside the grouped GEMMs."""
     from sparse_moe_gb300 import MoEContext
-    wl = moe_synth.PREFILL_INT4
     s = wl.shape
     ctx = MoEContext(s.hidden, s.n_experts, s.top_k, s.inter, s.shared_inter, n_layers=1,
                      max_chunk_rows=4096, wfmt=wl.wfmt, device=dev.index)
@@ -277,12 +277,14 @@ def bench_sweep(args, dev, stream, flush, tf_burst, hbm):
     return out
 
 
-def bench_decode(args, dev, stream, hbm, int4=None):
+def bench_decode(args, dev, stream, hbm, int4=None, wl=None):
     """40 independent decode layers replayed as one CUDA graph."""
     from sparse_moe_gb300 import MoEContext
-    if int4 is None:
-        int4 = args.decode_int4
-    wl = moe_synth.DECODE_INT4 if int4 else moe_synth.DECODE_BF16
+    if wl is None:
+        if int4 is None:
+            int4 = args.decode_int4
+        wl = moe_synth.DECODE_INT4 if int4 else moe_synth.DECODE_BF16
+    int4 = wl.wfmt != moe_synth.WFMT_BF16
     s = wl.shape
     L = args.decode_layers or wl.n_layers
     ctx = MoEContext(s.hidden, s.n_experts, s.top_k, s.inter, s.shared_inter, n_layers=L,
@@ -348,7 +350,7 @@ def bench_decode(args, dev, stream, hbm, int4=None):
         ctx.forward_decode_host(i % L, x_h, y_h, stream=stream)
         stream.synchronize()
     e2e_us = (time.perf_counter() - t0) * 1e6 / n_e2e
-    nb = decode_bytes(s, wl.wfmt == moe_synth.WFMT_INT4)
+    nb = decode_bytes(s, int4, affine=wl.wfmt == moe_synth.WFMT_INT4_AFFINE)
     lay = prof.get("decode_layer", (1, float("nan")))
     lay_us = lay[1] * 1e3 / max(1, lay[0])
     # one launch per layer: its average duration in the timed graph replays
@@ -543,8 +545,12 @@ def main(args):
         line["sweep"] = bench_sweep(args, dev, stream, flush, tf_burst, hbm)
     if rank == 0 and not args.skip_int4:
         line["prefill_int4"] = bench_prefill_int4(args, dev, stream, flush, tf_burst)
+        line["prefill_int4_affine"] = bench_prefill_int4(args, dev, stream, flush, tf_burst,
+                                                         wl=moe_synth.PREFILL_INT4_AFFINE)
         if not args.skip_decode and not args.decode_int4:
             line["decode_int4"] = bench_decode(args, dev, stream, hbm, int4=True)
+            line["decode_int4_affine"] = bench_decode(args, dev, stream, hbm,
+                                                      wl=moe_synth.DECODE_INT4_AFFINE)
     if rank == 0 and not args.skip_cpu:
         line["cpu_baseline"] = cpu_baseline_prefill(x.cpu(), w, s.top_k)
     if rank == 0:

@@ -43,7 +43,14 @@
  *                                    element 2m+1 in the high nibble, each a
  *                                    two's-complement code q in [-8, 7]
  *   <w>_scale     bf16  [rows, K/64] weight = scale[r, k/64] * q[r, k]
- * The router and sh_gate_w stay bf16 in both formats.
+ * int4 affine group-64 format (wfmt = MOE_W_INT4_AFFINE_G64), the checkpoint
+ * format of "Dequantize weights during matrix multiplication" (a bf16 scale
+ * and a bf16 bias per group of 64 weights), same tensors plus:
+ *   <w>           uint8 [rows, K/2]  as above, but each code an unsigned q in
+ *                                    [0, 15]
+ *   <w>_bias      bf16  [rows, K/64] weight = scale[r, k/64] * q[r, k]
+ *                                             + bias[r, k/64]
+ * The router and sh_gate_w stay bf16 in every format.
  *
  * Routing outputs (moe_route), per chunk of T tokens, assignment a = t*k + j:
  *   counts[e]          number of assignments to expert e             int32 [E]
@@ -93,7 +100,8 @@ typedef enum {
 
 typedef enum {
   MOE_W_BF16 = 0,              /* all weights bf16                                */
-  MOE_W_INT4_SYM_G64 = 1       /* expert + shared-expert weights int4, group 64   */
+  MOE_W_INT4_SYM_G64 = 1,      /* expert + shared-expert weights int4, group 64   */
+  MOE_W_INT4_AFFINE_G64 = 2    /* the same, unsigned codes with a scale and bias  */
 } moe_wfmt;
 
 typedef struct {
@@ -129,6 +137,12 @@ typedef struct {       /* device pointers, borrowed (see Ownership above)      *
    * first, with bit-identical results.  Decode never reads them. */
   const void  *down_f16;          /* fp16 [E, H, I] or NULL                    */
   const void  *sh_down_f16;       /* fp16 [H, Is]   or NULL                    */
+  /* Affine int4 only (else NULL): the per-group biases, bf16 [rows, K/64] of
+   * gate_up, down, sh_gate_up, sh_down. */
+  const void  *gate_up_bias;
+  const void  *down_bias;
+  const void  *sh_gate_up_bias;
+  const void  *sh_down_bias;
 } moe_weights;
 
 /* Bytes of device workspace a context with this config needs (host only). */

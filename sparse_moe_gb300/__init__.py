@@ -16,7 +16,8 @@ from . import _abi
 __all__ = ["MoEError", "MoEContext", "library", "WFMT", "convert_bf16_to_f16",
            "with_f16_down"]
 
-WFMT = {"bf16": _abi.MOE_W_BF16, "int4_sym_g64": _abi.MOE_W_INT4_SYM_G64}
+WFMT = {"bf16": _abi.MOE_W_BF16, "int4_sym_g64": _abi.MOE_W_INT4_SYM_G64,
+        "int4_affine_g64": _abi.MOE_W_INT4_AFFINE_G64}
 
 
 class MoEError(RuntimeError):
@@ -115,8 +116,9 @@ class MoEContext:
     def load_weights(self, layer: int, w: dict):
         """`w` holds device tensors in the layout of include/sparse_moe.h
         (keys: router_w, router_b, gate_up, gate_up_scale, down, down_scale,
-        sh_gate_up, sh_gate_up_scale, sh_down, sh_down_scale, sh_gate_w, and
-        the optional down_f16, sh_down_f16).
+        sh_gate_up, sh_gate_up_scale, sh_down, sh_down_scale, sh_gate_w, the
+        optional down_f16, sh_down_f16, and for affine int4 gate_up_bias,
+        down_bias, sh_gate_up_bias, sh_down_bias).
         The context borrows them; a reference is kept here."""
         for k, v in w.items():
             if v is not None and (not v.is_cuda or not v.is_contiguous()):

@@ -16,6 +16,7 @@ MOE_ERR_DEVICE_TIMEOUT = 6
 
 MOE_W_BF16 = 0
 MOE_W_INT4_SYM_G64 = 1
+MOE_W_INT4_AFFINE_G64 = 2
 
 # Every function the header declares, with its C signature.
 vp = ctypes.c_void_p
@@ -33,7 +34,9 @@ class MoeWeights(ctypes.Structure):
     _fields_ = [("router_w", vp), ("router_b", vp), ("gate_up", vp), ("gate_up_scale", vp),
                 ("down", vp), ("down_scale", vp), ("sh_gate_up", vp), ("sh_gate_up_scale", vp),
                 ("sh_down", vp), ("sh_down_scale", vp), ("sh_gate_w", vp),
-                ("down_f16", vp), ("sh_down_f16", vp)]
+                ("down_f16", vp), ("sh_down_f16", vp),
+                ("gate_up_bias", vp), ("down_bias", vp), ("sh_gate_up_bias", vp),
+                ("sh_down_bias", vp)]
 
 
 class MoeKernelStat(ctypes.Structure):

@@ -151,12 +151,48 @@ __device__ __forceinline__ float dot32_int4_f32(const uint4 wv, const float (&xs
   return a;
 }
 
+// Unsigned code of nibble n (0..7) of a 32-bit word (affine int4).
+__device__ __forceinline__ float nibu(uint32_t word, int n) {
+  return static_cast<float>((word >> (4 * n)) & 15u);
+}
+
+// Affine int4: 32 unsigned codes . 32 bf16 activations (sum q * x), and the
+// sum of those activations (for the group bias).
+__device__ __forceinline__ float dot32_u4_bf16(const uint4 wv, const uint4 (&xv)[4], float &xsum) {
+  const uint32_t words[4] = {wv.x, wv.y, wv.z, wv.w};
+  float a = 0.0f, sx = 0.0f;
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    const uint32_t xs[4] = {xv[w].x, xv[w].y, xv[w].z, xv[w].w};
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      a = fmaf(nibu(words[w], 2 * m), bf16_lo(xs[m]), a);
+      a = fmaf(nibu(words[w], 2 * m + 1), bf16_hi(xs[m]), a);
+      sx += bf16_lo(xs[m]) + bf16_hi(xs[m]);
+    }
+  }
+  xsum = sx;
+  return a;
+}
+
+// Same with 32 fp32 activations held in registers (their sum passed in).
+__device__ __forceinline__ float dot32_u4_f32(const uint4 wv, const float (&xs)[32]) {
+  const uint32_t words[4] = {wv.x, wv.y, wv.z, wv.w};
+  float a = 0.0f;
+#pragma unroll
+  for (int w = 0; w < 4; ++w)
+#pragma unroll
+    for (int n = 0; n < 8; ++n) a = fmaf(nibu(words[w], n), xs[8 * w + n], a);
+  return a;
+}
+
 // Chunking of one weight row for a warp: 16-byte chunks of EPC elements;
 // lane l takes chunks l + 32 u.  A segment is U chunks per lane (2048
 // elements for both formats), whose x slice is U * XPC 16-byte bf16 chunks.
 template <int WF> struct Fmt;
 template <> struct Fmt<0> { static constexpr int EPC = 8, XPC = 1, U = 8; };
 template <> struct Fmt<1> { static constexpr int EPC = 32, XPC = 4, U = 2; };
+template <> struct Fmt<2> : Fmt<1> {};   // affine int4: the same packing
 
 // Bytes of one weight row of K elements.
 template <int WF> __host__ __device__ __forceinline__ size_t row_bytes(int K) {
@@ -168,7 +204,8 @@ template <int WF> __host__ __device__ __forceinline__ size_t row_bytes(int K) {
 // issued before any arithmetic.
 template <int WF, int NR>
 __device__ __forceinline__ void warp_dots_x(const void *const (&rows)[NR],
-                                            const __nv_bfloat16 *const (&srows)[NR], int K,
+                                            const __nv_bfloat16 *const (&srows)[NR],
+                                            const __nv_bfloat16 *const (&brows)[NR], int K,
                                             const __nv_bfloat16 *x, float (&out)[NR]) {
   using F = Fmt<WF>;
   const int lane = threadIdx.x & 31;
@@ -180,7 +217,7 @@ __device__ __forceinline__ void warp_dots_x(const void *const (&rows)[NR],
   for (int c0 = 0; c0 < nchunk; c0 += 32 * F::U) {
     uint4 wv[NR][F::U];
     uint4 xv[F::U][F::XPC];
-    float sv[NR][F::U];
+    float sv[NR][F::U], bv[NR][F::U];
 #pragma unroll
     for (int r = 0; r < NR; ++r)
 #pragma unroll
@@ -188,7 +225,8 @@ __device__ __forceinline__ void warp_dots_x(const void *const (&rows)[NR],
         const int c = c0 + lane + 32 * u;
         wv[r][u] = (c < nchunk) ? ld_stream(reinterpret_cast<const uint4 *>(rows[r]) + c)
                                 : make_uint4(0, 0, 0, 0);
-        if constexpr (WF == 1) sv[r][u] = (c < nchunk) ? __bfloat162float(__ldg(srows[r] + (c >> 1))) : 0.0f;
+        if constexpr (WF != 0) sv[r][u] = (c < nchunk) ? __bfloat162float(__ldg(srows[r] + (c >> 1))) : 0.0f;
+        if constexpr (WF == 2) bv[r][u] = (c < nchunk) ? __bfloat162float(__ldg(brows[r] + (c >> 1))) : 0.0f;
       }
 #pragma unroll
     for (int u = 0; u < F::U; ++u)
@@ -203,8 +241,15 @@ __device__ __forceinline__ void warp_dots_x(const void *const (&rows)[NR],
     for (int r = 0; r < NR; ++r)
 #pragma unroll
       for (int u = 0; u < F::U; ++u) {
-        if constexpr (WF == 0) acc[r] += dot8_bf16_bf16(wv[r][u], xv[u][0]);
-        else acc[r] = fmaf(sv[r][u], dot32_int4_bf16(wv[r][u], xv[u]), acc[r]);
+        if constexpr (WF == 0) {
+          acc[r] += dot8_bf16_bf16(wv[r][u], xv[u][0]);
+        } else if constexpr (WF == 1) {
+          acc[r] = fmaf(sv[r][u], dot32_int4_bf16(wv[r][u], xv[u]), acc[r]);
+        } else {   // scale * (sum q x) + bias * (sum x)
+          float xs;
+          const float qx = dot32_u4_bf16(wv[r][u], xv[u], xs);
+          acc[r] = fmaf(sv[r][u], qx, fmaf(bv[r][u], xs, acc[r]));
+        }
       }
   }
 #pragma unroll
@@ -299,7 +344,10 @@ __device__ __forceinline__ void slot_task(const DecodeParams &p, int j, int t0, 
   else
     wrow = static_cast<const unsigned char *>(sh ? p.sh_down : p.down) + r0 * rb;
   const __nv_bfloat16 *srow =
-      WF == 1 ? static_cast<const __nv_bfloat16 *>(sh ? p.sh_down_scale : p.down_scale) + r0 * ng
+      WF != 0 ? static_cast<const __nv_bfloat16 *>(sh ? p.sh_down_scale : p.down_scale) + r0 * ng
+              : nullptr;
+  const __nv_bfloat16 *brow =
+      WF == 2 ? static_cast<const __nv_bfloat16 *>(sh ? p.sh_down_bias : p.down_bias) + r0 * ng
               : nullptr;
   // bf16 rows: two chunks per lane per pass, so that both h loads (from L2)
   // are in flight together
@@ -325,6 +373,14 @@ __device__ __forceinline__ void slot_task(const DecodeParams &p, int j, int t0, 
     // rows past the CTA's last repeat that row (their sums are dropped) and
     // chunks past the row end hold zero h: no branches, so the chains of the
     // eight rows interleave
+    float hs[CU];   // affine: the sum of each chunk's h values (for the group bias)
+#pragma unroll
+    for (int u = 0; u < CU; ++u) {
+      hs[u] = 0.0f;
+      if constexpr (WF == 2)
+#pragma unroll
+        for (int e = 0; e < F::EPC; ++e) hs[u] += hv[u][e];
+    }
 #pragma unroll
     for (int u = 0; u < CU; ++u) {
       const int c = min(c0 + 32 * u, nch - 1);
@@ -334,9 +390,13 @@ __device__ __forceinline__ void slot_task(const DecodeParams &p, int j, int t0, 
         const uint4 wv = reinterpret_cast<const uint4 *>(wrow + rr * rb)[c];
         if constexpr (WF == 0) {
           acc[r] += dot8_bf16_f32(wv, hv[u]);
-        } else {
+        } else if constexpr (WF == 1) {
           const float sc = __bfloat162float(__ldg(srow + rr * ng + (c >> 1)));
           acc[r] = fmaf(sc, dot32_int4_f32(wv, hv[u]), acc[r]);
+        } else {
+          const float sc = __bfloat162float(__ldg(srow + rr * ng + (c >> 1)));
+          const float bc = __bfloat162float(__ldg(brow + rr * ng + (c >> 1)));
+          acc[r] = fmaf(sc, dot32_u4_f32(wv, hv[u]), fmaf(bc, hs[u], acc[r]));
         }
       }
     }
@@ -441,7 +501,7 @@ __device__ __forceinline__ void decode_layer(const DecodeParams &p, const DecCta
       const void *rows[1] = {it < p.E ? row_ptr<0>(p.router_w, it, p.H) : p.sh_gate_w};
       const __nv_bfloat16 *sr[1] = {nullptr};
       float d[1];
-      warp_dots_x<0, 1>(rows, sr, p.H, x, d);
+      warp_dots_x<0, 1>(rows, sr, sr, p.H, x, d);
       if (lane == 0) {
         if (it < p.E) p.logits[it] = d[0] + (p.router_b ? p.router_b[it] : 0.0f);
         else *p.g = sigmoid_f(d[0]);
@@ -452,8 +512,10 @@ __device__ __forceinline__ void decode_layer(const DecodeParams &p, const DecCta
                              row_ptr<WF>(p.sh_gate_up, p.Is + i, p.H)};
       const __nv_bfloat16 *sr[2] = {scale_row(p.sh_gate_up_scale, i, p.H),
                                     scale_row(p.sh_gate_up_scale, p.Is + i, p.H)};
+      const __nv_bfloat16 *br[2] = {scale_row(p.sh_gate_up_bias, i, p.H),
+                                    scale_row(p.sh_gate_up_bias, p.Is + i, p.H)};
       float d[2];
-      warp_dots_x<WF, 2>(rows, sr, p.H, x, d);
+      warp_dots_x<WF, 2>(rows, sr, br, p.H, x, d);
       if (lane == 0) hg[static_cast<size_t>(p.k) * p.h_ld + i] = silu_f(d[0]) * d[1];
     }
   }
@@ -499,16 +561,19 @@ __device__ __forceinline__ void decode_layer(const DecodeParams &p, const DecCta
                         mb_rt);
     }
   }
-  if (WF == 1 && warp == kDecWarps - 2 && nrows > 0) {
-    // int4 group scales of those rows, into L2 for phase C
+  if (WF != 0 && warp == kDecWarps - 2 && nrows > 0) {
+    // int4 group scales (and affine biases) of those rows, into L2 for phase C
     for (int j = 0; j <= p.k; ++j) {
       const bool sh = (j == p.k);
       const size_t r0 = sh ? 0 : static_cast<size_t>(idx_s[j]) * p.H;
       const int K = sh ? p.Is : p.I;
-      const void *sb = sh ? p.sh_down_scale : p.down_scale;
-      const char *s0 = reinterpret_cast<const char *>(scale_row(sb, r0 + n0, K));
-      const char *s1 = reinterpret_cast<const char *>(scale_row(sb, r0 + n1, K));
-      for (const char *a = line_of(s0) + lane * 128; a < s1; a += 32 * 128) prefetch_l2_line(a);
+      for (int t = 0; t < (WF == 2 ? 2 : 1); ++t) {
+        const void *sb = t == 0 ? (sh ? p.sh_down_scale : p.down_scale)
+                                : (sh ? p.sh_down_bias : p.down_bias);
+        const char *s0 = reinterpret_cast<const char *>(scale_row(sb, r0 + n0, K));
+        const char *s1 = reinterpret_cast<const char *>(scale_row(sb, r0 + n1, K));
+        for (const char *a = line_of(s0) + lane * 128; a < s1; a += 32 * 128) prefetch_l2_line(a);
+      }
     }
   }
   DEC_MARK(4);
@@ -521,8 +586,10 @@ __device__ __forceinline__ void decode_layer(const DecodeParams &p, const DecCta
     const void *rows[2] = {row_ptr<WF>(p.gate_up, rg, p.H), row_ptr<WF>(p.gate_up, rg + p.I, p.H)};
     const __nv_bfloat16 *sr[2] = {scale_row(p.gate_up_scale, rg, p.H),
                                   scale_row(p.gate_up_scale, rg + p.I, p.H)};
+    const __nv_bfloat16 *br[2] = {scale_row(p.gate_up_bias, rg, p.H),
+                                  scale_row(p.gate_up_bias, rg + p.I, p.H)};
     float d[2];
-    warp_dots_x<WF, 2>(rows, sr, p.H, x, d);
+    warp_dots_x<WF, 2>(rows, sr, br, p.H, x, d);
     if (lane == 0) hg[static_cast<size_t>(j) * p.h_ld + i] = silu_f(d[0]) * d[1];
   }
   // The shared expert's slot needs only h_s (complete since the first
@@ -720,6 +787,9 @@ cudaError_t launch_decode_layer(const DecodeParams &p, int grid, int smem_limit,
   if (p.wfmt == 0)
     return p.E <= 256 ? launch_layer<0, 8>(p, grid, smem_limit, pdl, stream)
                       : launch_layer<0, 32>(p, grid, smem_limit, pdl, stream);
+  if (p.wfmt == 2)
+    return p.E <= 256 ? launch_layer<2, 8>(p, grid, smem_limit, pdl, stream)
+                      : launch_layer<2, 32>(p, grid, smem_limit, pdl, stream);
   return p.E <= 256 ? launch_layer<1, 8>(p, grid, smem_limit, pdl, stream)
                     : launch_layer<1, 32>(p, grid, smem_limit, pdl, stream);
 }
@@ -731,6 +801,9 @@ cudaError_t launch_decode_layers(const DecodeParams *layers, int n, int grid, in
   if (p.wfmt == 0)
     return p.E <= 256 ? launch_layers<0, 8>(layers, n, grid, smem_limit, pdl, stream)
                       : launch_layers<0, 32>(layers, n, grid, smem_limit, pdl, stream);
+  if (p.wfmt == 2)
+    return p.E <= 256 ? launch_layers<2, 8>(layers, n, grid, smem_limit, pdl, stream)
+                      : launch_layers<2, 32>(layers, n, grid, smem_limit, pdl, stream);
   return p.E <= 256 ? launch_layers<1, 8>(layers, n, grid, smem_limit, pdl, stream)
                     : launch_layers<1, 32>(layers, n, grid, smem_limit, pdl, stream);
 }
@@ -745,23 +818,23 @@ cudaError_t decode_configure(int *smem_limit) {
       cudaSuccess)
     return e;
   const int bytes = optin - 1024;   // room for the kernel's static shared memory
-  if ((e = cudaFuncSetAttribute(decode_layer_kernel<0, 8>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) ||
-      (e = cudaFuncSetAttribute(decode_layer_kernel<0, 32>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) ||
-      (e = cudaFuncSetAttribute(decode_layer_kernel<1, 8>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) ||
-      (e = cudaFuncSetAttribute(decode_layer_kernel<1, 32>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) ||
-      (e = cudaFuncSetAttribute(decode_layers_kernel<0, 8>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) ||
-      (e = cudaFuncSetAttribute(decode_layers_kernel<0, 32>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) ||
-      (e = cudaFuncSetAttribute(decode_layers_kernel<1, 8>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) ||
-      (e = cudaFuncSetAttribute(decode_layers_kernel<1, 32>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)))
-    return e;
+  const void *kernels[] = {
+      reinterpret_cast<const void *>(decode_layer_kernel<0, 8>),
+      reinterpret_cast<const void *>(decode_layer_kernel<0, 32>),
+      reinterpret_cast<const void *>(decode_layer_kernel<1, 8>),
+      reinterpret_cast<const void *>(decode_layer_kernel<1, 32>),
+      reinterpret_cast<const void *>(decode_layer_kernel<2, 8>),
+      reinterpret_cast<const void *>(decode_layer_kernel<2, 32>),
+      reinterpret_cast<const void *>(decode_layers_kernel<0, 8>),
+      reinterpret_cast<const void *>(decode_layers_kernel<0, 32>),
+      reinterpret_cast<const void *>(decode_layers_kernel<1, 8>),
+      reinterpret_cast<const void *>(decode_layers_kernel<1, 32>),
+      reinterpret_cast<const void *>(decode_layers_kernel<2, 8>),
+      reinterpret_cast<const void *>(decode_layers_kernel<2, 32>)};
+  for (const void *k : kernels)
+    if ((e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) !=
+        cudaSuccess)
+      return e;
   *smem_limit = bytes;
   return cudaSuccess;
 }

@@ -61,7 +61,8 @@ bool config_ok(const moe_config *c) {
   if (c->top_k < 1 || c->top_k > c->n_experts || c->top_k > 32) return false;
   if (c->inter < 64 || c->inter % 64 || c->shared_inter < 64 || c->shared_inter % 64) return false;
   if (c->inter > 16384 || c->shared_inter > 16384) return false;
-  if (c->wfmt != MOE_W_BF16 && c->wfmt != MOE_W_INT4_SYM_G64) return false;
+  if (c->wfmt != MOE_W_BF16 && c->wfmt != MOE_W_INT4_SYM_G64 && c->wfmt != MOE_W_INT4_AFFINE_G64)
+    return false;
   return true;
 }
 
@@ -76,8 +77,11 @@ extern "C" moe_status moe_forward_decode_noalloc(const moe_config *cfg, const mo
   const void *req[] = {w->router_w, w->gate_up, w->down, w->sh_gate_up, w->sh_down, w->sh_gate_w};
   for (const void *p : req)
     if (!p || !aligned16(p)) return MOE_ERR_INVALID_ARG;
-  if (cfg->wfmt == MOE_W_INT4_SYM_G64 &&
+  if (cfg->wfmt != MOE_W_BF16 &&
       (!w->gate_up_scale || !w->down_scale || !w->sh_gate_up_scale || !w->sh_down_scale))
+    return MOE_ERR_INVALID_ARG;
+  if (cfg->wfmt == MOE_W_INT4_AFFINE_G64 &&
+      (!w->gate_up_bias || !w->down_bias || !w->sh_gate_up_bias || !w->sh_down_bias))
     return MOE_ERR_INVALID_ARG;
   const ScratchLayout L = scratch_layout(*cfg);
   if (L.total > kNoAllocScratchBytes) return MOE_ERR_WORKSPACE;   // beyond the fixed scratch
@@ -138,6 +142,10 @@ extern "C" moe_status moe_forward_decode_noalloc(const moe_config *cfg, const mo
   p.sh_down = w->sh_down;
   p.sh_down_scale = w->sh_down_scale;
   p.sh_gate_w = w->sh_gate_w;
+  p.gate_up_bias = w->gate_up_bias;
+  p.down_bias = w->down_bias;
+  p.sh_gate_up_bias = w->sh_gate_up_bias;
+  p.sh_down_bias = w->sh_down_bias;
   p.logits = reinterpret_cast<float *>(base + L.logits);
   p.idx = reinterpret_cast<int32_t *>(base + L.idx);
   p.w = reinterpret_cast<float *>(base + L.w);

@@ -202,7 +202,8 @@ moe_status check_config(const moe_config *c) {
   if (c->inter > 16384 || c->shared_inter > 16384) return MOE_ERR_INVALID_ARG;
   if (c->n_layers < 1 || c->n_layers > 4096) return MOE_ERR_INVALID_ARG;
   if (c->max_chunk_rows < 1 || c->max_chunk_rows > 65536) return MOE_ERR_INVALID_ARG;
-  if (c->wfmt != MOE_W_BF16 && c->wfmt != MOE_W_INT4_SYM_G64) return MOE_ERR_INVALID_ARG;
+  if (c->wfmt != MOE_W_BF16 && c->wfmt != MOE_W_INT4_SYM_G64 && c->wfmt != MOE_W_INT4_AFFINE_G64)
+    return MOE_ERR_INVALID_ARG;
   const size_t imax = std::max(c->inter, c->shared_inter);
   // the GEMM producers address operand rows with 32-bit element offsets
   const size_t lim = size_t(1) << 31;
@@ -385,7 +386,8 @@ moe_status enqueue_prefill_chunk(moe_ctx *ctx, const LayerSlot &ls, const void *
   gp.sorted_rows = sorted;
   gp.status = ctx->status();
   gp.prefetch = ctx->gemm_prefetch;
-  const bool int4 = c.wfmt == MOE_W_INT4_SYM_G64;
+  const bool int4 = c.wfmt != MOE_W_BF16;
+  const bool aff = c.wfmt == MOE_W_INT4_AFFINE_G64;
   // gate/up + SwiGLU -> h
   gp.mode = MODE_GATEUP;
   gp.m_tiles = (L.Imax + gemm_pair_rows() / 2 - 1) / (gemm_pair_rows() / 2);   // 128 SwiGLU outputs per pair
@@ -400,11 +402,13 @@ moe_status enqueue_prefill_chunk(moe_ctx *ctx, const LayerSlot &ls, const void *
   gp.out_ld = L.Imax;
   gp.a_scale_routed = int4 ? ls.w.gate_up_scale : nullptr;
   gp.a_scale_shared = int4 ? ls.w.sh_gate_up_scale : nullptr;
+  gp.a_bias_routed = aff ? ls.w.gate_up_bias : nullptr;
+  gp.a_bias_shared = aff ? ls.w.sh_gate_up_bias : nullptr;
   {
     ProfScope ps(ctx, K_GATEUP_GEMM, s);
     st = launched(ctx,
                   launch_tc_gemm(ls.map_gu, ls.map_gu_sh, ls.map_gu, gp,
-                                 int4 ? CONV_INT4_TO_BF16 : CONV_NONE,
+                                 aff ? CONV_INT4A_TO_BF16 : int4 ? CONV_INT4_TO_BF16 : CONV_NONE,
                                  ctx->gemm_grid, ctx->prefill_pdl, s),
                   "gate/up gemm launch");
   }
@@ -426,11 +430,13 @@ moe_status enqueue_prefill_chunk(moe_ctx *ctx, const LayerSlot &ls, const void *
   gp.out_ld = c.hidden;
   gp.a_scale_routed = int4 ? ls.w.down_scale : nullptr;
   gp.a_scale_shared = int4 ? ls.w.sh_down_scale : nullptr;
+  gp.a_bias_routed = aff ? ls.w.down_bias : nullptr;
+  gp.a_bias_shared = aff ? ls.w.sh_down_bias : nullptr;
   {
     ProfScope ps(ctx, K_DOWN_GEMM, s);
     st = launched(ctx,
                   launch_tc_gemm(ls.map_dn, ls.map_dn_sh, ctx->map_h, gp,
-                                 int4 ? CONV_INT4_TO_F16
+                                 aff ? CONV_INT4A_TO_F16 : int4 ? CONV_INT4_TO_F16
                                       : (ls.down_f16 ? CONV_NONE : CONV_BF16_TO_F16),
                                  ctx->gemm_grid, ctx->prefill_pdl, s),
                   "down gemm launch");
@@ -477,6 +483,10 @@ DecodeParams decode_params(const moe_ctx *ctx, const LayerSlot &ls, const void *
   p.sh_down = ls.w.sh_down;
   p.sh_down_scale = ls.w.sh_down_scale;
   p.sh_gate_w = ls.w.sh_gate_w;
+  p.gate_up_bias = ls.w.gate_up_bias;
+  p.down_bias = ls.w.down_bias;
+  p.sh_gate_up_bias = ls.w.sh_gate_up_bias;
+  p.sh_down_bias = ls.w.sh_down_bias;
   p.logits = ctx->at<float>(L.dec_logits);
   p.idx = ctx->at<int32_t>(L.dec_idx);
   p.w = ctx->at<float>(L.dec_w);
@@ -589,7 +599,8 @@ moe_status moe_load_weights(moe_ctx *ctx, int layer, const moe_weights *w) {
   if (layer < 0 || layer >= ctx->cfg.n_layers)
     return fail(ctx, MOE_ERR_INVALID_ARG, "layer %d out of range", layer);
   const moe_config &c = ctx->cfg;
-  const bool int4 = c.wfmt == MOE_W_INT4_SYM_G64;
+  const bool int4 = c.wfmt != MOE_W_BF16;
+  const bool aff = c.wfmt == MOE_W_INT4_AFFINE_G64;
   const void *req[] = {w->router_w, w->gate_up, w->down, w->sh_gate_up, w->sh_down, w->sh_gate_w};
   for (const void *p : req)
     if (!p || !aligned16(p)) return fail(ctx, MOE_ERR_INVALID_ARG, "weight pointer null or not 16-byte aligned");
@@ -600,6 +611,12 @@ moe_status moe_load_weights(moe_ctx *ctx, int layer, const moe_weights *w) {
     for (const void *p : sc)
       if (!p || (reinterpret_cast<uintptr_t>(p) & 1))
         return fail(ctx, MOE_ERR_INVALID_ARG, "int4 format needs all four scale pointers");
+  }
+  const void *bi[] = {w->gate_up_bias, w->down_bias, w->sh_gate_up_bias, w->sh_down_bias};
+  for (const void *p : bi) {
+    if (aff && (!p || (reinterpret_cast<uintptr_t>(p) & 1)))
+      return fail(ctx, MOE_ERR_INVALID_ARG, "affine int4 format needs all four bias pointers");
+    if (!aff && p) return fail(ctx, MOE_ERR_INVALID_ARG, "bias pointers apply to affine int4 only");
   }
   const bool f16_down = w->down_f16 != nullptr || w->sh_down_f16 != nullptr;
   if (f16_down) {

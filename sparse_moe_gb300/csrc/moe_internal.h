@@ -16,14 +16,21 @@ constexpr int kRouteBlockTokens = 32;
 
 enum GemmMode : int { MODE_ROUTER = 0, MODE_GATEUP = 1, MODE_DOWN = 2 };
 // In-shared-memory conversion of the weight (A) tile before the MMA: none,
-// bf16 -> fp16 in place, or int4 codes (symmetric, one bf16 scale per 64
-// along K) -> bf16 / fp16.
+// bf16 -> fp16 in place, or int4 codes -> bf16 / fp16, symmetric (one bf16
+// scale per 64 along K) or affine (a bf16 scale and bias per 64).
 enum GemmConv : int {
   CONV_NONE = 0,
   CONV_BF16_TO_F16 = 1,
   CONV_INT4_TO_BF16 = 2,
-  CONV_INT4_TO_F16 = 3
+  CONV_INT4_TO_F16 = 3,
+  CONV_INT4A_TO_BF16 = 4,
+  CONV_INT4A_TO_F16 = 5
 };
+__host__ __device__ constexpr bool conv_int4(int c) { return c >= CONV_INT4_TO_BF16; }
+__host__ __device__ constexpr bool conv_affine(int c) { return c >= CONV_INT4A_TO_BF16; }
+__host__ __device__ constexpr bool conv_to_f16(int c) {
+  return c == CONV_BF16_TO_F16 || c == CONV_INT4_TO_F16 || c == CONV_INT4A_TO_F16;
+}
 
 struct GemmParams {
   int mode;
@@ -55,6 +62,8 @@ struct GemmParams {
   int prefetch;              // bit 1: L2-prefetch the next tile's token rows
   const void *a_scale_routed;   // int4 weights: bf16 scales [rows, K/64] (else null)
   const void *a_scale_shared;
+  const void *a_bias_routed;    // affine int4 weights: bf16 biases [rows, K/64] (else null)
+  const void *a_bias_shared;
   int ab_f16;                // CONV_NONE only: A and B are fp16 (else bf16)
   int b_tma;                 // down: B rows are consecutive (h in grouped order) and come by
                              // TMA with the weight tile (map_b), not from the row producers
@@ -106,6 +115,8 @@ struct DecodeParams {
   const void *gate_up, *gate_up_scale, *down, *down_scale;
   const void *sh_gate_up, *sh_gate_up_scale, *sh_down, *sh_down_scale;
   const void *sh_gate_w;
+  // affine int4 (wfmt 2): bf16 biases [rows, K/64] beside the scales (else null)
+  const void *gate_up_bias, *down_bias, *sh_gate_up_bias, *sh_down_bias;
   float *logits;             // [E]
   int32_t *idx;              // [k]
   float *w;                  // [k]

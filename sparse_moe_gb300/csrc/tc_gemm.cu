@@ -239,6 +239,28 @@ __device__ __forceinline__ uint32_t dq_pair(uint32_t lo_nib, uint32_t hi_nib, in
   return r;
 }
 
+// Affine codes, two values per 32-bit word: with u in [0, 15] the pattern
+// M | u is M + u exactly, so one packed subtract of M gives u and one packed
+// fma u * s + b rounds the weight once.
+template <bool F16>
+__device__ __forceinline__ uint32_t dq_pair_affine(uint32_t lo_nib, uint32_t hi_nib, int h,
+                                                   uint32_t s2, uint32_t b2) {
+  const uint32_t sel = static_cast<uint32_t>(h) | (static_cast<uint32_t>(h + 4) << 8);
+  const uint32_t b = __byte_perm(lo_nib, hi_nib, sel) & 0x00FF00FFu;
+  const uint32_t v = b | (F16 ? 0x64006400u : 0x43004300u);
+  uint32_t r;
+  if constexpr (F16) {
+    asm("{\n .reg .b32 t;\n sub.f16x2 t, %1, %2;\n fma.rn.f16x2 %0, t, %3, %4;\n}"
+        : "=r"(r)
+        : "r"(v), "r"(0x64006400u), "r"(s2), "r"(b2));
+  } else {
+    asm("{\n .reg .b32 t;\n sub.rn.bf16x2 t, %1, %2;\n fma.rn.bf16x2 %0, t, %3, %4;\n}"
+        : "=r"(r)
+        : "r"(v), "r"(0x43004300u), "r"(s2), "r"(b2));
+  }
+  return r;
+}
+
 // In-place dequantisation of one stage's A tile by one warp: row r's int4
 // codes (32 bytes = 64 K values, element 2m in the low nibble of byte m, two's
 // complement) at tile + CODE_OFF + 32 r become q * s_r in bf16 (or fp16) in
@@ -250,8 +272,9 @@ __device__ __forceinline__ uint32_t dq_pair(uint32_t lo_nib, uint32_t hi_nib, in
 // the last batch overwrites codes, all of which every lane has read by then
 // (the __syncwarp before it).
 //
-template <bool F16>
-__device__ __forceinline__ void dequant_tile_int4(uint32_t tile, const float (&sreg)[4], int lane) {
+template <bool F16, bool AFF>
+__device__ __forceinline__ void dequant_tile_int4(uint32_t tile, const float (&sreg)[4],
+                                                  const float (&breg)[4], int lane) {
   const int c = lane & 7, rs = lane >> 3;
   const uint32_t code0 = tile + CODE_OFF + rs * 32 + c * 4;   // + 1024 j + 128 m
   uint32_t cur[8], nxt[8];
@@ -276,11 +299,22 @@ __device__ __forceinline__ void dequant_tile_int4(uint32_t tile, const float (&s
       if constexpr (F16) asm("cvt.rn.f16x2.f32 %0, %1, %1;" : "=r"(s2) : "f"(s));
       else asm("cvt.rn.bf16x2.f32 %0, %1, %1;" : "=r"(s2) : "f"(s));
       const uint32_t w = cur[m];
-      const uint32_t lo = (w & 0x0F0F0F0Fu) ^ 0x08080808u;          // elements 0, 2, 4, 6
-      const uint32_t hi = ((w >> 4) & 0x0F0F0F0Fu) ^ 0x08080808u;   // elements 1, 3, 5, 7
       uint32_t o[4];
+      if constexpr (AFF) {
+        const float bf = __shfl_sync(0xffffffffu, breg[j], 4 * m + rs);
+        uint32_t b2;
+        if constexpr (F16) asm("cvt.rn.f16x2.f32 %0, %1, %1;" : "=r"(b2) : "f"(bf));
+        else asm("cvt.rn.bf16x2.f32 %0, %1, %1;" : "=r"(b2) : "f"(bf));
+        const uint32_t lo = w & 0x0F0F0F0Fu;           // elements 0, 2, 4, 6
+        const uint32_t hi = (w >> 4) & 0x0F0F0F0Fu;    // elements 1, 3, 5, 7
 #pragma unroll
-      for (int h = 0; h < 4; ++h) o[h] = dq_pair<F16>(lo, hi, h, s2);
+        for (int h = 0; h < 4; ++h) o[h] = dq_pair_affine<F16>(lo, hi, h, s2, b2);
+      } else {
+        const uint32_t lo = (w & 0x0F0F0F0Fu) ^ 0x08080808u;          // elements 0, 2, 4, 6
+        const uint32_t hi = ((w >> 4) & 0x0F0F0F0Fu) ^ 0x08080808u;   // elements 1, 3, 5, 7
+#pragma unroll
+        for (int h = 0; h < 4; ++h) o[h] = dq_pair<F16>(lo, hi, h, s2);
+      }
       asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(tile + r * 128 + ((c ^ (r & 7)) << 4)),
                    "r"(o[0]), "r"(o[1]), "r"(o[2]), "r"(o[3])
                    : "memory");
@@ -331,17 +365,23 @@ __device__ __forceinline__ void tile_scale_rows(const GemmParams &p, const Tile 
   }
 }
 
-// int4: the scales of this k-step for A rows 32 j + lane (0 past the end).
+// int4: the scales (and affine biases) of this k-step for A rows 32 j + lane
+// (0 past the end).
+template <bool AFF>
 __device__ __forceinline__ void load_stage_scales(const GemmParams &p, const Tile &t, int ks,
-                                                  int lane, float (&sreg)[4]) {
+                                                  int lane, float (&sreg)[4], float (&breg)[4]) {
   int srow[4];
   tile_scale_rows(p, t, lane, srow);
   const __nv_bfloat16 *sbase =
       static_cast<const __nv_bfloat16 *>(t.shared ? p.a_scale_shared : p.a_scale_routed);
+  const __nv_bfloat16 *bbase =
+      static_cast<const __nv_bfloat16 *>(t.shared ? p.a_bias_shared : p.a_bias_routed);
 #pragma unroll
-  for (int j = 0; j < 4; ++j)
-    sreg[j] = srow[j] >= 0 ? __bfloat162float(__ldg(sbase + static_cast<size_t>(srow[j]) * t.nk + ks))
-                           : 0.0f;
+  for (int j = 0; j < 4; ++j) {
+    const size_t off = static_cast<size_t>(srow[j]) * t.nk + ks;
+    sreg[j] = srow[j] >= 0 ? __bfloat162float(__ldg(sbase + off)) : 0.0f;
+    if constexpr (AFF) breg[j] = srow[j] >= 0 ? __bfloat162float(__ldg(bbase + off)) : 0.0f;
+  }
 }
 
 // Team warp q's part of a converting stage: a bounded wait for the stage to
@@ -349,10 +389,11 @@ __device__ __forceinline__ void load_stage_scales(const GemmParams &p, const Til
 // earlier by the caller), and its arrival on the pair leader's ready barrier.
 // Returns false on a timeout or abort.
 template <int CONV>
-__device__ __forceinline__ bool convert_stage(const GemmParams &p, const float (&sreg)[4], int stage,
+__device__ __forceinline__ bool convert_stage(const GemmParams &p, const float (&sreg)[4],
+                                              const float (&breg)[4], int stage,
                                               uint32_t phase, int q, int rank, uint32_t smem_base,
                                               SmemTail *tail, volatile int *abort_flag, int lane) {
-  constexpr bool INT4 = (CONV == CONV_INT4_TO_BF16 || CONV == CONV_INT4_TO_F16);
+  constexpr bool INT4 = conv_int4(CONV);
   int got = 1;
   if (lane == 0)
     got = mbar_wait_bounded(smem_u32(&tail->full[stage]), phase, abort_flag, p.status,
@@ -362,7 +403,7 @@ __device__ __forceinline__ bool convert_stage(const GemmParams &p, const float (
   if constexpr (CONV == CONV_BF16_TO_F16) {
     convert_share_bf16_to_f16(tile, q, lane);
   } else if constexpr (INT4) {
-    dequant_tile_int4<CONV == CONV_INT4_TO_F16>(tile, sreg, lane);
+    dequant_tile_int4<conv_to_f16(CONV), conv_affine(CONV)>(tile, sreg, breg, lane);
   }
   fence_proxy_async_smem();
   __syncwarp();
@@ -451,7 +492,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     // ahead of the boxes, by TMA or by plain prefetches, and loading part or
     // all of the weight tile with cp.async from the stage producers -- each
     // was slower than plain TMA boxes.)
-    constexpr bool INT4 = (CONV == CONV_INT4_TO_BF16 || CONV == CONV_INT4_TO_F16);
+    constexpr bool INT4 = conv_int4(CONV);
     constexpr int kx = INT4 ? BK / 2 : BK;   // box x extent per k-step (bytes / elements)
     int stage = 0;
     uint32_t phase = 0;
@@ -634,7 +675,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         if constexpr (CONV == CONV_BF16_TO_F16) {
           // this warp's share of the stage's conversion (team warps 1, 2)
           const float sreg[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-          if (!convert_stage<CONV>(p, sreg, g, phase, 1 + gq, rank, smem_base, tail, abort_flag,
+          if (!convert_stage<CONV>(p, sreg, sreg, g, phase, 1 + gq, rank, smem_base, tail, abort_flag,
                                    lane)) {
             ok = false;
             break;
@@ -667,8 +708,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
           }
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + acc * ACC_COLS;
-          const bool f16 = CONV == CONV_BF16_TO_F16 || CONV == CONV_INT4_TO_F16 ||
-                           (CONV == CONV_NONE && p.ab_f16);
+          const bool f16 = conv_to_f16(CONV) || (CONV == CONV_NONE && p.ab_f16);
           const uint32_t idesc = f16 ? idesc_f16_f32(PAIR_M, t.nmma) : idesc_bf16_f32(PAIR_M, t.nmma);
           for (int ks = 0; ks < t.nk; ++ks) {
             MOE_T0();
@@ -740,9 +780,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         if ((it % STAGES) != f) continue;
         const uint32_t phase = static_cast<uint32_t>(it / STAGES) & 1u;
         float sreg[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-        if constexpr (CONV == CONV_INT4_TO_BF16 || CONV == CONV_INT4_TO_F16)
-          load_stage_scales(p, t, ks, lane, sreg);
-        if (!convert_stage<CONV>(p, sreg, f, phase, 0, rank, smem_base, tail, abort_flag, lane)) {
+        float breg[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        if constexpr (conv_int4(CONV)) load_stage_scales<conv_affine(CONV)>(p, t, ks, lane, sreg, breg);
+        if (!convert_stage<CONV>(p, sreg, breg, f, phase, 0, rank, smem_base, tail, abort_flag,
+                                 lane)) {
           ok = false;
           break;
         }
@@ -900,6 +941,10 @@ cudaError_t gemm_configure() {
       (e = cudaFuncSetAttribute(tc_gemm_kernel<CONV_INT4_TO_BF16>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) ||
       (e = cudaFuncSetAttribute(tc_gemm_kernel<CONV_INT4_TO_F16>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) ||
+      (e = cudaFuncSetAttribute(tc_gemm_kernel<CONV_INT4A_TO_BF16>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) ||
+      (e = cudaFuncSetAttribute(tc_gemm_kernel<CONV_INT4A_TO_F16>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)))
     return e;
   return cudaSuccess;
@@ -944,6 +989,12 @@ cudaError_t launch_tc_gemm(const CUtensorMap &a_routed, const CUtensorMap &a_sha
                            a_routed, a_shared, b, p);
     case CONV_INT4_TO_F16:
       return launch_kernel(tc_gemm_kernel<CONV_INT4_TO_F16>, g, bl, kGemmSmemBytes, stream, pdl,
+                           a_routed, a_shared, b, p);
+    case CONV_INT4A_TO_BF16:
+      return launch_kernel(tc_gemm_kernel<CONV_INT4A_TO_BF16>, g, bl, kGemmSmemBytes, stream, pdl,
+                           a_routed, a_shared, b, p);
+    case CONV_INT4A_TO_F16:
+      return launch_kernel(tc_gemm_kernel<CONV_INT4A_TO_F16>, g, bl, kGemmSmemBytes, stream, pdl,
                            a_routed, a_shared, b, p);
     default:
       return launch_kernel(tc_gemm_kernel<CONV_NONE>, g, bl, kGemmSmemBytes, stream, pdl, a_routed,

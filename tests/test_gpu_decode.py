@@ -108,6 +108,30 @@ def test_decode_int4_tiny():
     _check_decode(ctx, w, moe_synth.make_x(wl, device="cuda"), int4=True)
 
 
+def test_decode_int4_affine_qwen():
+    wl = moe_synth.DECODE_INT4_AFFINE
+    ctx, (w,) = make_ctx(wl, max_chunk_rows=16)
+    x = moe_synth.make_x(wl, device="cuda")
+    _check_decode(ctx, w, x, int4=True)
+
+
+def test_decode_int4_affine_tiny():
+    wl = moe_synth.Workload("d4a", moe_synth.TINY, T=1, wfmt=moe_synth.WFMT_INT4_AFFINE, seed=14)
+    ctx, (w,) = make_ctx(wl, max_chunk_rows=16)
+    _check_decode(ctx, w, moe_synth.make_x(wl, device="cuda"), int4=True)
+
+
+def test_decode_int4_affine_matches_prefill_one_token():
+    wl = moe_synth.Workload("d4a1", moe_synth.QWEN, T=1, wfmt=moe_synth.WFMT_INT4_AFFINE, seed=15)
+    ctx, (w,) = make_ctx(wl, max_chunk_rows=16)
+    x = moe_synth.make_x(wl, device="cuda")
+    yd = ctx.forward_decode(0, x)
+    yp = ctx.forward_prefill(0, x)
+    torch.cuda.synchronize()
+    err = (yd.float() - yp.float()).abs().max().item()
+    assert err <= 2e-2 * yp.float().abs().max().item()
+
+
 # ---- several layers in one persistent launch: the same arithmetic as one
 # launch per layer, so the outputs must match bit for bit, with independent
 # inputs and with each layer's output feeding the next layer.

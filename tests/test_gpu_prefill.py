@@ -223,3 +223,56 @@ def test_prefill_int4_4096_sampled_tokens():
     y2 = ctx.forward_prefill(0, x)
     torch.cuda.synchronize()
     assert torch.equal(y, y2)
+
+
+# ---- affine int4 (the checkpoint format: a scale and a bias per 64 along K,
+# unsigned codes): dequantised inside the GEMMs with one fused multiply-add
+# per weight; the oracle applies w = scale * code + bias in fp64.
+
+def _wl4a(shape, T, bias=None, seed=0):
+    return moe_synth.Workload("t4a", shape, T=T, bias_std=bias, seed=seed,
+                              wfmt=moe_synth.WFMT_INT4_AFFINE)
+
+
+@pytest.mark.parametrize("T", [1, 16, 1000])
+def test_prefill_int4_affine_tiny(T):
+    wl = _wl4a(moe_synth.TINY, T, bias=1.5 if T > 16 else None, seed=60 + T)
+    ctx, (w,) = make_ctx(wl, max_chunk_rows=1024)
+    x = moe_synth.make_x(wl, device="cuda")
+    y = ctx.forward_prefill(0, x)
+    torch.cuda.synchronize()
+    assert_layer_close(y.float().cpu().numpy(), _oracle_y(ctx, w, x), int4=True,
+                       what=f"tiny int4 affine T={T}")
+
+
+def test_prefill_int4_affine_qwen_ragged_full():
+    wl = _wl4a(moe_synth.QWEN, 300, bias=1.5, seed=19)
+    ctx, (w,) = make_ctx(wl)
+    x = moe_synth.make_x(wl, device="cuda")
+    y = ctx.forward_prefill(0, x)
+    torch.cuda.synchronize()
+    assert_layer_close(y.float().cpu().numpy(), _oracle_y(ctx, w, x), int4=True,
+                       what="qwen int4 affine T=300")
+
+
+def test_prefill_int4_affine_4096_sampled_tokens():
+    wl = moe_synth.PREFILL_INT4_AFFINE
+    ctx, (w,) = make_ctx(wl)
+    x = moe_synth.make_x(wl, device="cuda")
+    y = ctx.forward_prefill(0, x)
+    torch.cuda.synchronize()
+    check_routing(ctx, w, x)
+    rng = np.random.default_rng(3)
+    tokens = np.unique(np.concatenate([[0, 4095], rng.choice(4096, 30, replace=False)]))
+    ref = _oracle_y(ctx, w, x, tokens=tokens)
+    assert_layer_close(y[tokens].float().cpu().numpy(), ref, int4=True,
+                       what="qwen int4 affine T=4096 sampled")
+
+
+def test_load_weights_affine_needs_biases():
+    wl = _wl4a(moe_synth.TINY, 4, seed=5)
+    ctx, (w,) = make_ctx(wl, max_chunk_rows=16)
+    w2 = dict(w)
+    w2["down_bias"] = None
+    with pytest.raises(MoEError):
+        ctx.load_weights(0, w2)

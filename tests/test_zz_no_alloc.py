@@ -21,17 +21,20 @@ def _ptr(t):
 
 
 @pytest.mark.parametrize("wl", [moe_synth.Workload("na_tiny", moe_synth.TINY, T=1, seed=21),
-                                moe_synth.DECODE_BF16, moe_synth.DECODE_INT4],
-                         ids=["tiny", "qwen_bf16", "qwen_int4"])
+                                moe_synth.DECODE_BF16, moe_synth.DECODE_INT4,
+                                moe_synth.DECODE_INT4_AFFINE],
+                         ids=["tiny", "qwen_bf16", "qwen_int4", "qwen_int4_affine"])
 def test_noalloc_decode_matches_context_decode(wl):
     lib = _abi.load()
     ctx, (w,) = make_ctx(wl, max_chunk_rows=16)
     s = wl.shape
     cfg = _abi.MoeConfig(s.hidden, s.n_experts, s.top_k, s.inter, s.shared_inter, 1, 16,
-                         _abi.MOE_W_BF16 if wl.wfmt == moe_synth.WFMT_BF16 else _abi.MOE_W_INT4_SYM_G64)
+                         {moe_synth.WFMT_BF16: _abi.MOE_W_BF16,
+                          moe_synth.WFMT_INT4: _abi.MOE_W_INT4_SYM_G64,
+                          moe_synth.WFMT_INT4_AFFINE: _abi.MOE_W_INT4_AFFINE_G64}[wl.wfmt])
     mw = _abi.MoeWeights(*[_ptr(w.get(n)) for n, _ in _abi.MoeWeights._fields_])
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
-    tol = 2e-2 if wl.wfmt == moe_synth.WFMT_INT4 else 1e-2
+    tol = 1e-2 if wl.wfmt == moe_synth.WFMT_BF16 else 2e-2
     for call in range(2):                       # two calls in a row share the scratch
         x = moe_synth.make_x(wl, layer=call, device="cuda")
         y_ref = ctx.forward_decode(0, x)
