@@ -15,6 +15,7 @@ machine's cores, and the SM clocks seen during the run.
 from __future__ import annotations
 
 import argparse
+import ctypes
 import json
 import os
 import subprocess
@@ -227,6 +228,126 @@ def bench_prefill_int4(args, dev, stream, flush, tf_burst, wl=moe_synth.PREFILL_
            "gpu_launches": launches}
     ctx.close()
     del w
+    torch.cuda.empty_cache()
+    return out
+
+
+def _time_steps(fn, steps, warmup, flush, stream):
+    """ms per call of fn() (one layer pass), CUDA events around each call on
+    `stream`, L2 flushed before each."""
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    with torch.cuda.stream(stream):
+        for a, b in ev:
+            flush.zero_()
+            a.record(stream)
+            fn()
+            b.record(stream)
+    torch.cuda.synchronize()
+    return float(np.mean([a.elapsed_time(b) for a, b in ev]))
+
+
+def bench_ablations(args, dev, stream, flush):
+    """The page's prefill ablations on GB300, each undoing one mechanism of the
+    layer at the prompt length the page measured it at: routing kept on the GPU
+    vs a host that waits for the routing before the grouped GEMMs ("Keep
+    expert routing on the GPU", 512 tokens); tile shape from the expert's load
+    vs a fixed tile ("Match tile size to expert load", 2K tokens: every block
+    at the full 256-row MMA N, and blocks of at most 16 rows); weights expanded
+    inside the GEMMs vs by a separate kernel into a bf16/fp16 array that the
+    GEMMs read back ("Dequantize weights during matrix multiplication", 512
+    tokens, the affine int4 format).  Layer time here, not the page's
+    end-to-end prefill."""
+    from sparse_moe_gb300 import MoEContext, dequant_int4, with_f16_down
+    steps = max(10, min(args.steps, 40))
+    out = {}
+
+    def layer_ms(wl, env=None):
+        old = {k: os.environ.get(k) for k in (env or {})}
+        os.environ.update(env or {})
+        try:
+            s = wl.shape
+            ctx = MoEContext(s.hidden, s.n_experts, s.top_k, s.inter, s.shared_inter,
+                             max_chunk_rows=4096, wfmt=wl.wfmt, device=dev.index)
+        finally:
+            for k, v in old.items():
+                if v is None:
+                    os.environ.pop(k, None)
+                else:
+                    os.environ[k] = v
+        w = moe_synth.make_layer(wl, device=dev)
+        ctx.load_weights(0, with_f16_down(w) if wl.wfmt == moe_synth.WFMT_BF16 else w)
+        x = moe_synth.make_x(wl, device=dev)
+        y = torch.empty_like(x)
+        ms = _time_steps(lambda: ctx.forward_prefill(0, x, y, stream=stream), steps, args.warmup,
+                         flush, stream)
+        ctx.close()
+        return ms
+
+    def entry(base_ms, abl_ms, what, page):
+        return {"layer_ms": base_ms, "ablated_layer_ms": abl_ms, "ablated": what,
+                "gain_of_mechanism": abl_ms / base_ms - 1.0, "page_end_to_end_gain": page}
+
+    wl512 = moe_synth.sweep_workload(512)
+    base512 = layer_ms(wl512)
+    out["gpu_routing_vs_host_sync_T512"] = entry(
+        base512, layer_ms(wl512, {"MOE_ABLATE_HOST_ROUTING": "1"}),
+        "host waits for the routing (block count read back) before the grouped GEMMs", 0.89)
+    wl2k = moe_synth.sweep_workload(2048)
+    base2k = layer_ms(wl2k)
+    out["adaptive_tile_vs_fixed_n256_T2048"] = entry(
+        base2k, layer_ms(wl2k, {"MOE_ABLATE_TILE": "fixed256"}),
+        "every block runs the full 256-row MMA N", 0.132)
+    out["adaptive_tile_vs_16_row_blocks_T2048"] = entry(
+        base2k, layer_ms(wl2k, {"MOE_ABLATE_TILE": "rows16"}),
+        "blocks of at most 16 rows (the weights re-read per 16 rows; MMA N 32)", 0.132)
+
+    # fused vs separate dequantisation, affine int4 at T=512
+    wl4 = moe_synth.Workload("ablation_dequant_T512_int4affg64_bias1.5", moe_synth.QWEN, T=512,
+                             wfmt=moe_synth.WFMT_INT4_AFFINE, bias_std=1.5, seed=512)
+    fused = layer_ms(wl4)
+    s4 = wl4.shape
+    w4 = moe_synth.make_layer(wl4, device=dev)
+    ctxb = MoEContext(s4.hidden, s4.n_experts, s4.top_k, s4.inter, s4.shared_inter,
+                      max_chunk_rows=4096, device=dev.index)
+    exp = {}
+    for name in ("gate_up", "sh_gate_up", "down", "sh_down"):
+        exp[name] = dequant_int4(w4[name], w4[name + "_scale"], w4[name + "_bias"])
+    for name in ("down", "sh_down"):
+        exp[name + "_f16"] = dequant_int4(w4[name], w4[name + "_scale"], w4[name + "_bias"],
+                                          out_dtype=torch.float16)
+    ctxb.load_weights(0, {"router_w": w4["router_w"], "router_b": w4["router_b"],
+                          "sh_gate_w": w4["sh_gate_w"], **exp})
+    x4 = moe_synth.make_x(wl4, device=dev)
+    y4 = torch.empty_like(x4)
+    from sparse_moe_gb300 import library, _abi
+    lib = library()
+
+    def separate():
+        # expand every expert's weights, then run the bf16/fp16 layer on them
+        h = ctypes.c_void_p(stream.cuda_stream)
+        for name, dst in (("gate_up", exp["gate_up"]), ("sh_gate_up", exp["sh_gate_up"]),
+                          ("down", exp["down_f16"]), ("sh_down", exp["sh_down_f16"])):
+            c = w4[name]
+            K = c.shape[-1] * 2
+            st = lib.moe_dequant_int4(ctypes.c_void_p(c.data_ptr()),
+                                      ctypes.c_void_p(w4[name + "_scale"].data_ptr()),
+                                      ctypes.c_void_p(w4[name + "_bias"].data_ptr()),
+                                      ctypes.c_void_p(dst.data_ptr()), c.numel() * 2 // K, K,
+                                      _abi.MOE_W_INT4_AFFINE_G64,
+                                      int(dst.dtype == torch.float16), h)
+            assert st == 0
+        ctxb.forward_prefill(0, x4, y4, stream=stream)
+
+    out["fused_vs_separate_dequant_T512_int4_affine"] = entry(
+        fused, _time_steps(separate, steps, args.warmup, flush, stream),
+        "a separate kernel expands all expert weights (bf16 gate/up, fp16 down) that the "
+        "bf16/fp16 GEMMs then read", 0.774)
+    ctxb.close()
+    del w4, exp
     torch.cuda.empty_cache()
     return out
 
@@ -543,6 +664,8 @@ def main(args):
         line["decode"] = bench_decode(args, dev, stream, hbm)
     if rank == 0 and not args.skip_sweep:
         line["sweep"] = bench_sweep(args, dev, stream, flush, tf_burst, hbm)
+    if rank == 0 and not args.skip_ablations:
+        line["ablations"] = bench_ablations(args, dev, stream, flush)
     if rank == 0 and not args.skip_int4:
         line["prefill_int4"] = bench_prefill_int4(args, dev, stream, flush, tf_burst)
         line["prefill_int4_affine"] = bench_prefill_int4(args, dev, stream, flush, tf_burst,
@@ -575,6 +698,8 @@ if __name__ == "__main__":
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--skip-sweep", action="store_true",
                     help="skip the prompt-length sweep (T = 256 .. 128K)")
+    ap.add_argument("--skip-ablations", action="store_true",
+                    help="skip the ablations (GPU routing, tile shape, fused dequantisation)")
     ap.add_argument("--skip-int4", action="store_true",
                     help="skip the int4 prefill and decode measurements")
     ap.add_argument("--skip-prefill", action="store_true",

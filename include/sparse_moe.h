@@ -258,6 +258,20 @@ moe_status moe_forward_decode_noalloc(const moe_config *cfg, const moe_weights *
  * is launched), MOE_ERR_CUDA if the launch fails; n = 0 is a no-op. */
 moe_status moe_convert_bf16_to_f16(const void *src, void *dst, size_t n, void *stream);
 
+/* Expands int4 weights (wfmt MOE_W_INT4_SYM_G64 or MOE_W_INT4_AFFINE_G64;
+ * codes uint8 [rows, K/2], scale bf16 [rows, K/64], bias bf16 [rows, K/64]
+ * for the affine format, else ignored) into dst [rows, K], bf16 (out_f16 = 0)
+ * or fp16 (out_f16 = 1), on the current device, asynchronously on `stream`.
+ * Each value is rounded exactly as the grouped GEMMs round it when they expand
+ * a weight tile in shared memory, so a bf16/fp16 layer on the expanded arrays
+ * computes what the int4 layer computes.  This is the separate dequantisation
+ * that "Dequantize weights during matrix multiplication" measures its fused
+ * expansion against.  codes and dst 16-byte aligned; K a multiple of 64.
+ * Returns MOE_ERR_INVALID_ARG for bad arguments (nothing launched),
+ * MOE_ERR_CUDA if the launch fails; rows = 0 is a no-op. */
+moe_status moe_dequant_int4(const void *codes, const void *scale, const void *bias, void *dst,
+                            size_t rows, int K, int wfmt, int out_f16, void *stream);
+
 /* Synchronises the device, reads and clears the device status word: MOE_OK,
  * or MOE_ERR_DEVICE_TIMEOUT (a bounded wait ran out; *code, if non-NULL,
  * receives the site code), or MOE_ERR_CUDA. */

@@ -14,7 +14,7 @@ import torch
 from . import _abi
 
 __all__ = ["MoEError", "MoEContext", "library", "WFMT", "convert_bf16_to_f16",
-           "with_f16_down"]
+           "with_f16_down", "dequant_int4"]
 
 WFMT = {"bf16": _abi.MOE_W_BF16, "int4_sym_g64": _abi.MOE_W_INT4_SYM_G64,
         "int4_affine_g64": _abi.MOE_W_INT4_AFFINE_G64}
@@ -51,6 +51,23 @@ def convert_bf16_to_f16(src: torch.Tensor, stream=None) -> torch.Tensor:
                                            _stream_handle(stream, src.device))
     if st != 0:
         raise MoEError(st, "moe_convert_bf16_to_f16")
+    return dst
+
+
+def dequant_int4(codes: torch.Tensor, scale: torch.Tensor, bias: Optional[torch.Tensor] = None,
+                 out_dtype=torch.bfloat16, stream=None) -> torch.Tensor:
+    """Expanded copy of int4 weights (codes uint8 [..., K/2], bf16 scale and,
+    for the affine format, bias [..., K/64]) in bf16 or fp16, rounded as the
+    grouped GEMMs round them; written by the library's kernel."""
+    K = codes.shape[-1] * 2
+    rows = codes.numel() * 2 // K
+    dst = torch.empty(tuple(codes.shape[:-1]) + (K,), dtype=out_dtype, device=codes.device)
+    fmt = _abi.MOE_W_INT4_AFFINE_G64 if bias is not None else _abi.MOE_W_INT4_SYM_G64
+    st = library().moe_dequant_int4(_ptr(codes), _ptr(scale), _ptr(bias), _ptr(dst), rows, K, fmt,
+                                    int(out_dtype == torch.float16),
+                                    _stream_handle(stream, codes.device))
+    if st != 0:
+        raise MoEError(st, "moe_dequant_int4")
     return dst
 
 

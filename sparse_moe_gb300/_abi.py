@@ -60,6 +60,7 @@ SIGNATURES = {
     "moe_forward_decode_noalloc": (i32, [ctypes.POINTER(MoeConfig), ctypes.POINTER(MoeWeights), vp,
                                          vp, vp]),
     "moe_convert_bf16_to_f16": (i32, [vp, vp, ctypes.c_size_t, vp]),
+    "moe_dequant_int4": (i32, [vp, vp, vp, vp, ctypes.c_size_t, i32, i32, i32, vp]),
     "moe_check_device": (i32, [vp, ctypes.POINTER(ctypes.c_int32)]),
     "moe_profile_enable": (i32, [vp, i32]),
     "moe_profile_read": (i32, [vp, ctypes.POINTER(MoeKernelStat), i32, ctypes.POINTER(i32)]),

@@ -33,8 +33,8 @@ WsLayout make_layout(const moe_config &c) {
   L.nblk = (L.Tc + kRouteBlockTokens - 1) / kRouteBlockTokens;
   L.R = L.Tc * c.top_k + L.Tc;
   L.Imax = std::max(c.inter, c.shared_inter);
-  L.max_blocks = (L.Tc * c.top_k) / kBlockRowsMax + c.n_experts +
-                 (L.Tc + kBlockRowsMax - 1) / kBlockRowsMax + 1;
+  L.max_blocks = (L.Tc * c.top_k) / kBlockRowsMin + c.n_experts +
+                 (L.Tc + kBlockRowsMin - 1) / kBlockRowsMin + 1;
   size_t off = 0;
   auto take = [&](size_t bytes) {
     const size_t at = off;
@@ -151,6 +151,16 @@ struct moe_ctx {
   int router_split = 1;    // router GEMM split-K parts (router_split())
   CUtensorMap map_h;       // h [R, Imax] fp16 in the workspace: the down GEMM's token rows
   bool prefill_pdl = true; // programmatic dependent launch between prefill kernels (MOE_PREFILL_PDL)
+  // Measurement options (environment, read at creation; off by default), each
+  // undoing one mechanism of the page to measure what it is worth here:
+  //   MOE_ABLATE_HOST_ROUTING=1  the host waits for the routing and reads the
+  //                              block count before the grouped GEMMs launch;
+  //   MOE_ABLATE_TILE=fixed256   every block runs the full 256-row MMA N;
+  //   MOE_ABLATE_TILE=rows<n>    blocks of at most n rows (16 <= n <= 256).
+  bool ablate_host_routing = false;
+  int ablate_fixed_n = 0;
+  int block_rows = kBlockRowsMax;
+  int32_t host_nblocks = 0;
   int decode_grid = 0;     // CTAs of the cooperative decode launch
   int decode_smem = 0;     // dynamic shared-memory limit of the decode kernel
   bool decode_pdl = true;  // decode launches overlap the previous kernel's tail
@@ -347,7 +357,7 @@ moe_status enqueue_route(moe_ctx *ctx, const LayerSlot &ls, const void *x, int T
     st = launched(ctx,
                   launch_scan(mask, nblk, T, c.n_experts, c.top_k, counts, offsets, base,
                               ctx->at<int4>(L.blocks), ctx->at<int32_t>(L.nblocks),
-                              ctx->scan_ticket(), ctx->prefill_pdl, s),
+                              ctx->scan_ticket(), ctx->block_rows, ctx->prefill_pdl, s),
                   "scan launch");
   }
   if (st) return st;
@@ -373,7 +383,16 @@ moe_status enqueue_prefill_chunk(moe_ctx *ctx, const LayerSlot &ls, const void *
                                 ctx->at<int32_t>(L.counts), ctx->at<int32_t>(L.offsets), sorted,
                                 pos, s);
   if (st) return st;
+  if (ctx->ablate_host_routing) {
+    // measurement option: the CPU waits for the routing and inspects it
+    // before it submits the grouped GEMMs
+    cudaError_t e = cudaMemcpyAsync(&ctx->host_nblocks, ctx->at<int32_t>(L.nblocks), 4,
+                                    cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "host routing read-back");
+  }
   GemmParams gp{};
+  gp.fixed_n = ctx->ablate_fixed_n;
   gp.blocks = ctx->at<int4>(L.blocks);
   gp.n_blocks_dev = ctx->at<int32_t>(L.nblocks);
   gp.T = T;
@@ -571,6 +590,13 @@ moe_status moe_ctx_create(const moe_config *cfg, int device, void *workspace, si
   if (const char *env = std::getenv("MOE_GEMM_PREFETCH")) ctx->gemm_prefetch = std::atoi(env);
   if (const char *env = std::getenv("MOE_DECODE_PDL")) ctx->decode_pdl = std::atoi(env) != 0;
   if (const char *env = std::getenv("MOE_PREFILL_PDL")) ctx->prefill_pdl = std::atoi(env) != 0;
+  if (const char *env = std::getenv("MOE_ABLATE_HOST_ROUTING"))
+    ctx->ablate_host_routing = std::atoi(env) != 0;
+  if (const char *env = std::getenv("MOE_ABLATE_TILE")) {
+    if (std::strcmp(env, "fixed256") == 0) ctx->ablate_fixed_n = 1;
+    if (std::strncmp(env, "rows", 4) == 0)
+      ctx->block_rows = std::min(kBlockRowsMax, std::max(kBlockRowsMin, std::atoi(env + 4)));
+  }
   if (
       (e = decode_configure(&ctx->decode_smem)) != cudaSuccess ||
       (e = cudaMemset(ctx->ws + L.status, 0, 256)) != cudaSuccess ||
@@ -814,6 +840,21 @@ moe_status moe_convert_bf16_to_f16(const void *src, void *dst, size_t n, void *s
   const char *b = static_cast<const char *>(dst);
   if (a < b + 2 * n && b < a + 2 * n) return MOE_ERR_INVALID_ARG;   // overlap
   return launch_convert_bf16_to_f16(src, dst, n, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? MOE_OK
+             : MOE_ERR_CUDA;
+}
+
+moe_status moe_dequant_int4(const void *codes, const void *scale, const void *bias, void *dst,
+                            size_t rows, int K, int wfmt, int out_f16, void *stream) {
+  if (rows == 0) return MOE_OK;
+  if (wfmt != MOE_W_INT4_SYM_G64 && wfmt != MOE_W_INT4_AFFINE_G64) return MOE_ERR_INVALID_ARG;
+  if (K < 64 || K % 64 || !codes || !scale || !dst || !aligned16(codes) || !aligned16(dst) ||
+      (reinterpret_cast<uintptr_t>(scale) & 1))
+    return MOE_ERR_INVALID_ARG;
+  const bool aff = wfmt == MOE_W_INT4_AFFINE_G64;
+  if (aff && (!bias || (reinterpret_cast<uintptr_t>(bias) & 1))) return MOE_ERR_INVALID_ARG;
+  return launch_dequant_int4(codes, scale, aff ? bias : nullptr, dst, rows, K, aff, out_f16 != 0,
+                             static_cast<cudaStream_t>(stream)) == cudaSuccess
              ? MOE_OK
              : MOE_ERR_CUDA;
 }

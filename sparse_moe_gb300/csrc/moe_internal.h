@@ -11,6 +11,9 @@ namespace moe {
 // becomes ceil(c / kBlockRowsMax) blocks; each block's MMA N is its row count
 // rounded up to 16.
 constexpr int kBlockRowsMax = 256;
+// Smallest block of the grouped GEMMs' block list (a measurement option;
+// the MMA N of such a block is still at least 32).
+constexpr int kBlockRowsMin = 16;
 // Tokens per routing block (one 32-bit mask word per expert per block).
 constexpr int kRouteBlockTokens = 32;
 
@@ -65,6 +68,7 @@ struct GemmParams {
   const void *a_bias_routed;    // affine int4 weights: bf16 biases [rows, K/64] (else null)
   const void *a_bias_shared;
   int ab_f16;                // CONV_NONE only: A and B are fp16 (else bf16)
+  int fixed_n;               // grouped modes: MMA N = kBlockRowsMax for every block (measurement)
   int b_tma;                 // down: B rows are consecutive (h in grouped order) and come by
                              // TMA with the weight tile (map_b), not from the row producers
   int k_split;               // router: split-K parts (>= 1); part s writes out + s * out_split_stride
@@ -90,10 +94,12 @@ constexpr int kBTmaRows = 16;
 cudaError_t launch_topk(const float *partial, int nsplit, size_t split_stride, float *logits_out,
                         const void *x, const void *wsg, int T, int E, int k, int H, int32_t *idx,
                         float *w, uint32_t *blk_mask, float *gate, bool pdl, cudaStream_t stream);
-// `ticket`: a zeroed counter in device memory (left zeroed on return).
+// `ticket`: a zeroed counter in device memory (left zeroed on return);
+// block_rows (kBlockRowsMin..kBlockRowsMax): rows per grouped-GEMM block.
 cudaError_t launch_scan(const uint32_t *blk_mask, int nblk, int T, int E, int k,
                         int32_t *counts, int32_t *offsets, int32_t *blk_base, int4 *blocks,
-                        int32_t *n_blocks, unsigned int *ticket, bool pdl, cudaStream_t stream);
+                        int32_t *n_blocks, unsigned int *ticket, int block_rows, bool pdl,
+                        cudaStream_t stream);
 cudaError_t launch_scatter(const int32_t *idx, const uint32_t *blk_mask, const int32_t *blk_base,
                            const int32_t *offsets, int T, int E, int k, int32_t *sorted_rows,
                            int32_t *pos_of_assign, bool pdl, cudaStream_t stream);
@@ -102,6 +108,11 @@ cudaError_t launch_scatter(const int32_t *idx, const uint32_t *blk_mask, const i
 cudaError_t launch_combine(const float *gate, const void *o, const int32_t *pos, const float *w,
                            int T, int H, int k, void *y, bool pdl, cudaStream_t stream);
 
+// int4 codes [rows, K/2] (+ bf16 scales, and biases if affine, [rows, K/64])
+// -> bf16 or fp16 weights [rows, K], rounded as the grouped GEMMs round them.
+cudaError_t launch_dequant_int4(const void *codes, const void *scale, const void *bias, void *dst,
+                                size_t rows, int K, bool affine, bool out_f16,
+                                cudaStream_t stream);
 // dst[i] = fp16(src[i]) (round to nearest even), n elements, 16-byte aligned.
 cudaError_t launch_convert_bf16_to_f16(const void *src, void *dst, size_t n, cudaStream_t stream);
 

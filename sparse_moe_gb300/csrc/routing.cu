@@ -179,7 +179,8 @@ __global__ void __launch_bounds__(1024) scan_kernel(const uint32_t *__restrict__
                                                     int32_t *__restrict__ blk_base,
                                                     int4 *__restrict__ blocks,
                                                     int32_t *__restrict__ n_blocks,
-                                                    unsigned int *__restrict__ ticket) {
+                                                    unsigned int *__restrict__ ticket,
+                                                    int block_rows) {
   __shared__ int part[1024];
   __shared__ int warp_tot[33];
   __shared__ int is_last;
@@ -257,31 +258,32 @@ __global__ void __launch_bounds__(1024) scan_kernel(const uint32_t *__restrict__
     offsets[E] = total;   // = T * k
     *ticket = 0u;         // ready for the next launch
   }
-  // 5. block map: ceil(count / kBlockRowsMax) blocks per expert, then the
+  // 5. block map: ceil(count / block_rows) blocks per expert, then the
   //    shared expert's T rows at grouped row T*k.
-  const int nb = (c + kBlockRowsMax - 1) / kBlockRowsMax;
+  const int nb = (c + block_rows - 1) / block_rows;
   int nb_total = 0;
   const int bstart = block_excl_scan_1024(nb, warp_tot, nb_total);
   if (tid < E) {
     for (int i = 0; i < nb; ++i) {
-      const int r0 = i * kBlockRowsMax;
-      blocks[bstart + i] = make_int4(tid, off + r0, min(kBlockRowsMax, c - r0), 0);
+      const int r0 = i * block_rows;
+      blocks[bstart + i] = make_int4(tid, off + r0, min(block_rows, c - r0), 0);
     }
   }
-  const int nb_sh = (T + kBlockRowsMax - 1) / kBlockRowsMax;
+  const int nb_sh = (T + block_rows - 1) / block_rows;
   for (int i = tid; i < nb_sh; i += blockDim.x) {
-    const int r0 = i * kBlockRowsMax;
-    blocks[nb_total + i] = make_int4(E, T * k + r0, min(kBlockRowsMax, T - r0), 0);
+    const int r0 = i * block_rows;
+    blocks[nb_total + i] = make_int4(E, T * k + r0, min(block_rows, T - r0), 0);
   }
   if (tid == 0) *n_blocks = nb_total + nb_sh;
 }
 
 cudaError_t launch_scan(const uint32_t *blk_mask, int nblk, int T, int E, int k,
                         int32_t *counts, int32_t *offsets, int32_t *blk_base, int4 *blocks,
-                        int32_t *n_blocks, unsigned int *ticket, bool pdl, cudaStream_t stream) {
+                        int32_t *n_blocks, unsigned int *ticket, int block_rows, bool pdl,
+                        cudaStream_t stream) {
   return launch_kernel(scan_kernel, dim3((E + kScanExperts - 1) / kScanExperts), dim3(1024), 0,
                        stream, pdl, blk_mask, nblk, T, E, k, counts, offsets, blk_base, blocks,
-                       n_blocks, ticket);
+                       n_blocks, ticket, block_rows);
 }
 
 // --------------------------------------------------------------- scatter --

@@ -160,7 +160,7 @@ __device__ __forceinline__ Tile decode_tile(const GemmParams &p, int tile, int r
     t.nrows = blk.z;
     t.shared = (e == p.n_experts);
   }
-  t.nmma = max(32, (t.nrows + 31) & ~31);
+  t.nmma = p.fixed_n && p.mode != MODE_ROUTER ? BN_MAX : max(32, (t.nrows + 31) & ~31);
   t.valid = t.nrows > 0;
   if (p.mode == MODE_ROUTER) {
     t.nk = p.k_routed / BK / p.k_split;
@@ -930,6 +930,69 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
   if (warp == MMA_WARP) tmem_dealloc_pair(tmem_base, TMEM_COLS);
 }
 
+
+// Stand-alone dequantisation of int4 weights into a bf16 (or fp16) array,
+// with the same per-pair arithmetic as the GEMMs' in-shared-memory expansion
+// (so a GEMM on the expanded array sees the same operands).  One thread turns
+// 4 code bytes (8 weights of one group) into one 16-byte output chunk.
+template <bool F16, bool AFF>
+__global__ void __launch_bounds__(256) dequant_int4_kernel(const uint32_t *__restrict__ codes,
+                                                           const __nv_bfloat16 *__restrict__ scale,
+                                                           const __nv_bfloat16 *__restrict__ bias,
+                                                           uint4 *__restrict__ dst, size_t rows,
+                                                           int K) {
+  const size_t per_row = static_cast<size_t>(K) / 8;   // chunks of 8 weights
+  const size_t total = rows * per_row;
+  const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
+  for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total; i += stride) {
+    const size_t r = i / per_row, c = i - r * per_row;
+    const size_t g = r * (K / 64) + c / 8;
+    const uint32_t w = __ldg(codes + i);
+    uint32_t s2, b2 = 0;
+    const float sf = __bfloat162float(scale[g]);
+    if constexpr (F16) asm("cvt.rn.f16x2.f32 %0, %1, %1;" : "=r"(s2) : "f"(sf));
+    else asm("cvt.rn.bf16x2.f32 %0, %1, %1;" : "=r"(s2) : "f"(sf));
+    uint32_t o[4];
+    if constexpr (AFF) {
+      const float bf = __bfloat162float(bias[g]);
+      if constexpr (F16) asm("cvt.rn.f16x2.f32 %0, %1, %1;" : "=r"(b2) : "f"(bf));
+      else asm("cvt.rn.bf16x2.f32 %0, %1, %1;" : "=r"(b2) : "f"(bf));
+      const uint32_t lo = w & 0x0F0F0F0Fu, hi = (w >> 4) & 0x0F0F0F0Fu;
+#pragma unroll
+      for (int h = 0; h < 4; ++h) o[h] = dq_pair_affine<F16>(lo, hi, h, s2, b2);
+    } else {
+      const uint32_t lo = (w & 0x0F0F0F0Fu) ^ 0x08080808u;
+      const uint32_t hi = ((w >> 4) & 0x0F0F0F0Fu) ^ 0x08080808u;
+#pragma unroll
+      for (int h = 0; h < 4; ++h) o[h] = dq_pair<F16>(lo, hi, h, s2);
+    }
+    dst[i] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
+cudaError_t launch_dequant_int4(const void *codes, const void *scale, const void *bias, void *dst,
+                                size_t rows, int K, bool affine, bool out_f16,
+                                cudaStream_t stream) {
+  int dev = 0, sms = 0;
+  cudaError_t e;
+  if ((e = cudaGetDevice(&dev)) || (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)))
+    return e;
+  const size_t total = rows * static_cast<size_t>(K) / 8;
+  const int grid = static_cast<int>(std::max<size_t>(1, std::min<size_t>((total + 255) / 256,
+                                                                          static_cast<size_t>(sms) * 8)));
+  const auto *cw = static_cast<const uint32_t *>(codes);
+  const auto *sc = static_cast<const __nv_bfloat16 *>(scale);
+  const auto *bi = static_cast<const __nv_bfloat16 *>(bias);
+  auto *d = static_cast<uint4 *>(dst);
+  if (affine) {
+    if (out_f16) dequant_int4_kernel<true, true><<<grid, 256, 0, stream>>>(cw, sc, bi, d, rows, K);
+    else dequant_int4_kernel<false, true><<<grid, 256, 0, stream>>>(cw, sc, bi, d, rows, K);
+  } else {
+    if (out_f16) dequant_int4_kernel<true, false><<<grid, 256, 0, stream>>>(cw, sc, bi, d, rows, K);
+    else dequant_int4_kernel<false, false><<<grid, 256, 0, stream>>>(cw, sc, bi, d, rows, K);
+  }
+  return cudaGetLastError();
+}
 
 cudaError_t gemm_configure() {
   const int bytes = static_cast<int>(kGemmSmemBytes);

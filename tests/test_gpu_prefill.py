@@ -8,7 +8,7 @@ import torch
 import moe_synth
 from gpu_helpers import assert_layer_close, check_routing, host_layer, make_ctx
 from oracle import moe_oracle as orc
-from sparse_moe_gb300 import MoEError, convert_bf16_to_f16, with_f16_down
+from sparse_moe_gb300 import MoEContext, MoEError, convert_bf16_to_f16, dequant_int4, with_f16_down
 
 pytestmark = pytest.mark.gpu
 
@@ -276,3 +276,58 @@ def test_load_weights_affine_needs_biases():
     w2["down_bias"] = None
     with pytest.raises(MoEError):
         ctx.load_weights(0, w2)
+
+
+# ---- stand-alone dequantisation (the page's "separate dequantization"
+# ablation): rounded exactly as the fused expansion, so a bf16 layer on the
+# expanded weights equals the int4 layer bit for bit.
+
+@pytest.mark.parametrize("wfmt", [moe_synth.WFMT_INT4, moe_synth.WFMT_INT4_AFFINE])
+@pytest.mark.parametrize("out", [torch.bfloat16, torch.float16])
+def test_dequant_int4_rounds_once(wfmt, out):
+    wl = moe_synth.Workload("dq", moe_synth.TINY, T=1, wfmt=wfmt, seed=31)
+    w = moe_synth.make_layer(wl, device="cuda")
+    got = dequant_int4(w["down"], w["down_scale"], w.get("down_bias"), out_dtype=out)
+    torch.cuda.synchronize()
+    L = moe_synth.to_numpy(w)
+    if out == torch.float16:
+        # fp16 operands: the bf16 scale and bias become fp16 values first
+        # (exact unless below fp16's normal range, where they round)
+        for name in ("down_scale", "down_bias"):
+            if name in w and w[name] is not None:
+                L[name] = w[name].cpu().half().double().numpy()
+    exact = (orc.dequant_int4_affine_g64(L["down"], L["down_scale"], L["down_bias"])
+             if wfmt == moe_synth.WFMT_INT4_AFFINE else
+             orc.dequant_int4_sym_g64(L["down"], L["down_scale"]))
+    g = got.double().cpu().numpy()
+    # then correctly rounded: within half a unit in the last place of the format
+    mant = 8 if out == torch.bfloat16 else 11
+    e = np.floor(np.log2(np.maximum(np.abs(exact), 2.0 ** -120)))
+    half_ulp = 2.0 ** (e - mant)
+    if out == torch.float16:
+        half_ulp = np.maximum(half_ulp, 2.0 ** -25)   # fp16 subnormal spacing / 2
+    assert np.all(np.abs(g - exact) <= half_ulp)
+    if wfmt == moe_synth.WFMT_INT4:   # q * s is exact in fp32: one rounding in torch too
+        ref = torch.from_numpy(exact.astype(np.float32)).to(out)
+        assert torch.equal(got.cpu(), ref)
+
+
+@pytest.mark.parametrize("wfmt", [moe_synth.WFMT_INT4, moe_synth.WFMT_INT4_AFFINE])
+def test_prefill_on_dequantised_weights_equals_fused_int4(wfmt):
+    wl = moe_synth.Workload("dqp", moe_synth.QWEN, T=300, bias_std=1.5, wfmt=wfmt, seed=33)
+    ctx4, (w,) = make_ctx(wl)
+    x = moe_synth.make_x(wl, device="cuda")
+    y4 = ctx4.forward_prefill(0, x)
+    s = wl.shape
+    ctxb = MoEContext(s.hidden, s.n_experts, s.top_k, s.inter, s.shared_inter)
+    wb = {"router_w": w["router_w"], "router_b": w["router_b"], "sh_gate_w": w["sh_gate_w"]}
+    for name in ("gate_up", "sh_gate_up", "down", "sh_down"):
+        wb[name] = dequant_int4(w[name], w[name + "_scale"], w.get(name + "_bias"))
+    wb["down_f16"] = dequant_int4(w["down"], w["down_scale"], w.get("down_bias"),
+                                  out_dtype=torch.float16)
+    wb["sh_down_f16"] = dequant_int4(w["sh_down"], w["sh_down_scale"], w.get("sh_down_bias"),
+                                     out_dtype=torch.float16)
+    ctxb.load_weights(0, wb)
+    yb = ctxb.forward_prefill(0, x)
+    torch.cuda.synchronize()
+    assert torch.equal(y4, yb)
