@@ -91,25 +91,30 @@ constexpr int B_WARP0 = 1;                                   // warps 1..12
 constexpr int B_WARPS = STAGES * B_WARPS_PER_STAGE;
 constexpr int MMA_WARP = B_WARP0 + B_WARPS;                  // warp 13
 constexpr int EPI_WARP0 = MMA_WARP + 1;                      // warps 14..17
-constexpr int FIN_WARP0 = EPI_WARP0 + 4;                     // warps 18..23: one per stage
-constexpr int NUM_THREADS = (FIN_WARP0 + STAGES) * 32;
+constexpr int FIN_WARP0 = EPI_WARP0 + 4;                     // warps 18..25: finishers
+constexpr int FIN_WARPS = 8;
+constexpr int NUM_THREADS = (FIN_WARP0 + FIN_WARPS) * 32;
 constexpr int XCH_FLOATS = 2 * 2 * 2 * 8 * 32;  // [buf][pair][dir][8 cols][32 lanes]
 constexpr int EPI_STAGE_BYTES = 4 * 16 * 64;    // per epilogue warp: 16 rows x 64 bytes
 // Per B producer warp: offsets of the token rows it copies (every
 // B_WARPS_PER_STAGE-th group of four rows of up to 128).
 constexpr int kRowTab = 4 * ((BN_HALF / 4 + B_WARPS_PER_STAGE - 1) / B_WARPS_PER_STAGE);
 
-// Warps that convert one stage's weight tile: for bf16 -> fp16 the stage's
-// finisher and its two token-row producers (each a share of the chunks); for
-// int4 the finisher alone (splitting the in-place dequantisation measured
-// slower).
+// Warps that convert one stage's weight tile, per CTA: for bf16 -> fp16 the
+// stage's finisher (finisher f owns stage f) and its two token-row producers,
+// each a share of the chunks; for int4 four finishers, one per 32 weight rows
+// (finishers 0-3 take the even k-steps, 4-7 the odd ones).
 constexpr int kConvTeam = 1 + B_WARPS_PER_STAGE;
+constexpr int kInt4Warps = 4;
+static_assert(2 * kInt4Warps == FIN_WARPS && STAGES % 2 == 0, "int4 finisher groups");
 template <int CONV> __host__ __device__ constexpr int conv_team() {
-  return CONV == CONV_BF16_TO_F16 ? kConvTeam : 1;
+  return CONV == CONV_BF16_TO_F16 ? kConvTeam : conv_int4(CONV) ? kInt4Warps : 1;
 }
 
 struct SmemTail {
-  uint64_t full[STAGES];        // local: TMA (A) + this CTA's B warps
+  uint64_t full[STAGES];        // local: TMA (A; int4: token-row boxes only) + this CTA's B warps
+  uint64_t cfull[STAGES];       // local, int4: the stage's weight codes (TMA)
+  uint64_t cread[STAGES];       // local, int4: converters 0-2 hold their codes in registers
   uint64_t ready[STAGES];       // leader: both CTAs' conversion teams
   uint64_t empty[STAGES];       // local: arrives from the leader's commit
   uint64_t tmem_full[2];        // local: arrives from the leader's commit
@@ -261,68 +266,55 @@ __device__ __forceinline__ uint32_t dq_pair_affine(uint32_t lo_nib, uint32_t hi_
   return r;
 }
 
-// In-place dequantisation of one stage's A tile by one warp: row r's int4
-// codes (32 bytes = 64 K values, element 2m in the low nibble of byte m, two's
-// complement) at tile + CODE_OFF + 32 r become q * s_r in bf16 (or fp16) in
-// the 128-byte-swizzled K-major layout the MMA reads.  sreg[j] holds, in lane
-// l, the scale of row 32 j + l.  Lane l writes 16-byte chunk l % 8 (K values
-// 8 (l % 8) .. +7) of rows 32 j + 4 m + l / 8, m = 0..7, batch j = 0..3, and
-// reads batch j + 1's codes before writing batch j.  Batch j's outputs cover
-// bytes [4096 j, 4096 j + 4096) and codes start at CODE_OFF = 12288, so only
-// the last batch overwrites codes, all of which every lane has read by then
-// (the __syncwarp before it).
-//
-template <bool F16, bool AFF>
-__device__ __forceinline__ void dequant_tile_int4(uint32_t tile, const float (&sreg)[4],
-                                                  const float (&breg)[4], int lane) {
-  const int c = lane & 7, rs = lane >> 3;
-  const uint32_t code0 = tile + CODE_OFF + rs * 32 + c * 4;   // + 1024 j + 128 m
-  uint32_t cur[8], nxt[8];
+// In-place dequantisation of rows 32 j .. 32 j + 31 of one stage's A tile by
+// one warp.  Row r's int4 codes (32 bytes = 64 K values, element 2m in the
+// low nibble of byte m) sit at tile + CODE_OFF + 32 r; they become q * s_r
+// (+ b_r) in bf16 (or fp16) in the 128-byte-swizzled K-major layout the MMA
+// reads.  Lane l handles 16-byte chunk l % 8 (K values 8 (l % 8) .. +7) of
+// rows 32 j + 4 m + l / 8, m = 0..7: load_codes_int4 reads its 8 code words,
+// expand_rows_int4 writes the outputs, bytes [4096 j, 4096 j + 4096) of the
+// tile.  Only batch j = 3 overwrites codes (CODE_OFF = 12288), so its warp
+// waits until the other three hold theirs in registers.
+__device__ __forceinline__ void load_codes_int4(uint32_t tile, int j, int lane,
+                                                uint32_t (&w)[8]) {
+  const uint32_t code0 = tile + CODE_OFF + 1024 * j + (lane >> 3) * 32 + (lane & 7) * 4;
 #pragma unroll
   for (int m = 0; m < 8; ++m)
-    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(cur[m]) : "r"(code0 + 128 * m));
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(w[m]) : "r"(code0 + 128 * m));
+}
+
+// s_lane, b_lane: the scale (and affine bias) of row 32 j + lane.
+template <bool F16, bool AFF>
+__device__ __forceinline__ void expand_rows_int4(uint32_t tile, const uint32_t (&w)[8], int j,
+                                                 float s_lane, float b_lane, int lane) {
+  const int c = lane & 7, rs = lane >> 3;
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    if (j < 3) {
+  for (int m = 0; m < 8; ++m) {
+    const int r = 32 * j + 4 * m + rs;
+    // the row's scale (held by lane 4 m + l / 8) as a packed pair
+    const float sv = __shfl_sync(0xffffffffu, s_lane, 4 * m + rs);
+    uint32_t s2;
+    if constexpr (F16) asm("cvt.rn.f16x2.f32 %0, %1, %1;" : "=r"(s2) : "f"(sv));
+    else asm("cvt.rn.bf16x2.f32 %0, %1, %1;" : "=r"(s2) : "f"(sv));
+    uint32_t o[4];
+    if constexpr (AFF) {
+      const float bv = __shfl_sync(0xffffffffu, b_lane, 4 * m + rs);
+      uint32_t b2;
+      if constexpr (F16) asm("cvt.rn.f16x2.f32 %0, %1, %1;" : "=r"(b2) : "f"(bv));
+      else asm("cvt.rn.bf16x2.f32 %0, %1, %1;" : "=r"(b2) : "f"(bv));
+      const uint32_t lo = w[m] & 0x0F0F0F0Fu;           // elements 0, 2, 4, 6
+      const uint32_t hi = (w[m] >> 4) & 0x0F0F0F0Fu;    // elements 1, 3, 5, 7
 #pragma unroll
-      for (int m = 0; m < 8; ++m)
-        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(nxt[m]) : "r"(code0 + 1024 * (j + 1) + 128 * m));
+      for (int h = 0; h < 4; ++h) o[h] = dq_pair_affine<F16>(lo, hi, h, s2, b2);
     } else {
-      __syncwarp();
+      const uint32_t lo = (w[m] & 0x0F0F0F0Fu) ^ 0x08080808u;          // elements 0, 2, 4, 6
+      const uint32_t hi = ((w[m] >> 4) & 0x0F0F0F0Fu) ^ 0x08080808u;   // elements 1, 3, 5, 7
+#pragma unroll
+      for (int h = 0; h < 4; ++h) o[h] = dq_pair<F16>(lo, hi, h, s2);
     }
-#pragma unroll
-    for (int m = 0; m < 8; ++m) {
-      const int r = 32 * j + 4 * m + rs;
-      // the row's scale (held by lane 4 m + l / 8) as a packed pair
-      const float s = __shfl_sync(0xffffffffu, sreg[j], 4 * m + rs);
-      uint32_t s2;
-      if constexpr (F16) asm("cvt.rn.f16x2.f32 %0, %1, %1;" : "=r"(s2) : "f"(s));
-      else asm("cvt.rn.bf16x2.f32 %0, %1, %1;" : "=r"(s2) : "f"(s));
-      const uint32_t w = cur[m];
-      uint32_t o[4];
-      if constexpr (AFF) {
-        const float bf = __shfl_sync(0xffffffffu, breg[j], 4 * m + rs);
-        uint32_t b2;
-        if constexpr (F16) asm("cvt.rn.f16x2.f32 %0, %1, %1;" : "=r"(b2) : "f"(bf));
-        else asm("cvt.rn.bf16x2.f32 %0, %1, %1;" : "=r"(b2) : "f"(bf));
-        const uint32_t lo = w & 0x0F0F0F0Fu;           // elements 0, 2, 4, 6
-        const uint32_t hi = (w >> 4) & 0x0F0F0F0Fu;    // elements 1, 3, 5, 7
-#pragma unroll
-        for (int h = 0; h < 4; ++h) o[h] = dq_pair_affine<F16>(lo, hi, h, s2, b2);
-      } else {
-        const uint32_t lo = (w & 0x0F0F0F0Fu) ^ 0x08080808u;          // elements 0, 2, 4, 6
-        const uint32_t hi = ((w >> 4) & 0x0F0F0F0Fu) ^ 0x08080808u;   // elements 1, 3, 5, 7
-#pragma unroll
-        for (int h = 0; h < 4; ++h) o[h] = dq_pair<F16>(lo, hi, h, s2);
-      }
-      asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(tile + r * 128 + ((c ^ (r & 7)) << 4)),
-                   "r"(o[0]), "r"(o[1]), "r"(o[2]), "r"(o[3])
-                   : "memory");
-    }
-    if (j < 3) {
-#pragma unroll
-      for (int m = 0; m < 8; ++m) cur[m] = nxt[m];
-    }
+    asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(tile + r * 128 + ((c ^ (r & 7)) << 4)),
+                 "r"(o[0]), "r"(o[1]), "r"(o[2]), "r"(o[3])
+                 : "memory");
   }
 }
 
@@ -365,54 +357,94 @@ __device__ __forceinline__ void tile_scale_rows(const GemmParams &p, const Tile 
   }
 }
 
-// int4: the scales (and affine biases) of this k-step for A rows 32 j + lane
-// (0 past the end).
+// int4: the scale (and affine bias) of this k-step for A row 32 j + lane (0
+// past the operator's end).
 template <bool AFF>
-__device__ __forceinline__ void load_stage_scales(const GemmParams &p, const Tile &t, int ks,
-                                                  int lane, float (&sreg)[4], float (&breg)[4]) {
+__device__ __forceinline__ void load_row_scale(const GemmParams &p, const Tile &t, int ks, int j,
+                                               int lane, float &sv, float &bv) {
   int srow[4];
   tile_scale_rows(p, t, lane, srow);
+  int row = srow[0];
+#pragma unroll
+  for (int q = 1; q < 4; ++q)
+    if (j == q) row = srow[q];
   const __nv_bfloat16 *sbase =
       static_cast<const __nv_bfloat16 *>(t.shared ? p.a_scale_shared : p.a_scale_routed);
   const __nv_bfloat16 *bbase =
       static_cast<const __nv_bfloat16 *>(t.shared ? p.a_bias_shared : p.a_bias_routed);
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const size_t off = static_cast<size_t>(srow[j]) * t.nk + ks;
-    sreg[j] = srow[j] >= 0 ? __bfloat162float(__ldg(sbase + off)) : 0.0f;
-    if constexpr (AFF) breg[j] = srow[j] >= 0 ? __bfloat162float(__ldg(bbase + off)) : 0.0f;
-  }
+  const size_t off = static_cast<size_t>(row) * t.nk + ks;
+  sv = row >= 0 ? __bfloat162float(__ldg(sbase + off)) : 0.0f;
+  bv = 0.0f;
+  if constexpr (AFF) bv = row >= 0 ? __bfloat162float(__ldg(bbase + off)) : 0.0f;
 }
 
-// Team warp q's part of a converting stage: a bounded wait for the stage to
-// be full, its share of the conversion (int4: with the scales in sreg, loaded
-// earlier by the caller), and its arrival on the pair leader's ready barrier.
-// Returns false on a timeout or abort.
-template <int CONV>
-__device__ __forceinline__ bool convert_stage(const GemmParams &p, const float (&sreg)[4],
-                                              const float (&breg)[4], int stage,
-                                              uint32_t phase, int q, int rank, uint32_t smem_base,
-                                              SmemTail *tail, volatile int *abort_flag, int lane) {
-  constexpr bool INT4 = conv_int4(CONV);
+// Arrival of one converting warp on the pair leader's ready barrier of
+// `stage` (after its writes are fenced for the tensor core).
+__device__ __forceinline__ void arrive_ready(SmemTail *tail, int stage, int rank) {
+  const uint32_t ready = smem_u32(&tail->ready[stage]);
+  if (rank == 0) mbar_arrive(ready);
+  else mbar_arrive_cluster(mapa_shared(ready, 0));
+}
+
+// bf16 -> fp16 team warp q's part of a converting stage: a bounded wait for
+// the stage to be full, its share of the conversion, and its arrival on the
+// pair leader's ready barrier.  Returns false on a timeout or abort.
+__device__ __forceinline__ bool convert_stage_bf16(const GemmParams &p, int stage, uint32_t phase,
+                                                   int q, int rank, uint32_t smem_base,
+                                                   SmemTail *tail, volatile int *abort_flag,
+                                                   int lane) {
   int got = 1;
   if (lane == 0)
     got = mbar_wait_bounded(smem_u32(&tail->full[stage]), phase, abort_flag, p.status,
                             DEV_TIMEOUT_CONVERTER);
   if (!__shfl_sync(0xffffffffu, got, 0)) return false;
+  convert_share_bf16_to_f16(smem_base + stage * STAGE_BYTES, q, lane);
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) arrive_ready(tail, stage, rank);
+  return true;
+}
+
+// int4 converter j (0..3) of a stage: expands weight rows 32 j .. 32 j + 31
+// once the codes have landed (cfull; the token rows may still be in flight),
+// then (the last converter) waits for the token rows (full) and arrives on
+// the leader's ready barrier.  sv, bv: this lane's row scale and bias, loaded by the caller
+// before the wait.  Returns false on a timeout or abort.
+template <int CONV>
+__device__ __forceinline__ bool convert_stage_int4(const GemmParams &p, int j, float sv, float bv,
+                                                   int stage, uint32_t phase, int rank,
+                                                   uint32_t smem_base, SmemTail *tail,
+                                                   volatile int *abort_flag, int lane) {
   const uint32_t tile = smem_base + stage * STAGE_BYTES;
-  if constexpr (CONV == CONV_BF16_TO_F16) {
-    convert_share_bf16_to_f16(tile, q, lane);
-  } else if constexpr (INT4) {
-    dequant_tile_int4<conv_to_f16(CONV), conv_affine(CONV)>(tile, sreg, breg, lane);
+  int got = 1;
+  if (lane == 0)
+    got = mbar_wait_bounded(smem_u32(&tail->cfull[stage]), phase, abort_flag, p.status,
+                            DEV_TIMEOUT_CONVERTER);
+  if (!__shfl_sync(0xffffffffu, got, 0)) return false;
+  uint32_t w[8];
+  load_codes_int4(tile, j, lane, w);
+  __syncwarp();
+  if (j < kInt4Warps - 1) {
+    if (lane == 0) mbar_arrive(smem_u32(&tail->cread[stage]));
+  } else {
+    // the last batch's outputs cover all codes: wait until the others hold theirs
+    if (lane == 0)
+      got = mbar_wait_bounded(smem_u32(&tail->cread[stage]), phase, abort_flag, p.status,
+                              DEV_TIMEOUT_CONVERTER);
+    if (!__shfl_sync(0xffffffffu, got, 0)) return false;
   }
+  expand_rows_int4<conv_to_f16(CONV), conv_affine(CONV)>(tile, w, j, sv, bv, lane);
   fence_proxy_async_smem();
   __syncwarp();
   if (lane == 0) {
-    const uint32_t ready = smem_u32(&tail->ready[stage]);
-    if (rank == 0) mbar_arrive(ready);
-    else mbar_arrive_cluster(mapa_shared(ready, 0));
+    // one converter per CTA checks the token rows: the leader's ready phase
+    // needs every converter's arrival
+    if (j == kInt4Warps - 1)
+      got = mbar_wait_bounded(smem_u32(&tail->full[stage]), phase, abort_flag, p.status,
+                              DEV_TIMEOUT_CONVERTER);
+    if (got) arrive_ready(tail, stage, rank);
   }
-  return true;
+  return __shfl_sync(0xffffffffu, got, 0) != 0;
 }
 
 // One warp stores a [rows x 32] block of fp16 values (row-major, 64 bytes per
@@ -456,6 +488,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
                 CONV == CONV_NONE ? 1 + 2 * B_WARPS_PER_STAGE : 1 + B_WARPS_PER_STAGE);
       mbar_init(smem_u32(&tail->ready[s]), 2 * conv_team<CONV>());
       mbar_init(smem_u32(&tail->empty[s]), 1);
+      mbar_init(smem_u32(&tail->cfull[s]), 1);
+      mbar_init(smem_u32(&tail->cread[s]), kInt4Warps - 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(smem_u32(&tail->tmem_full[a]), 1);
@@ -520,16 +554,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
           const uint32_t b_bytes = static_cast<uint32_t>(b_boxes * kBTmaRows * BK * 2);
           const int b_row0 = t.row0 + rank * (t.nmma / 2);
           if constexpr (INT4) {
-            mbar_arrive_expect_tx(full_bar, A_CODE_BYTES + b_bytes);
+            // codes on their own barrier (the converters start on them), the
+            // token-row boxes (if any) on the stage's full barrier
+            const uint32_t cfull_bar = smem_u32(&tail->cfull[stage]);
+            mbar_arrive_expect_tx(cfull_bar, A_CODE_BYTES);
+            if (p.mode == MODE_GATEUP) {
+              tma_load_2d(a_dst + CODE_OFF, amap, (t.k0 + ks) * kx, t.a_row, cfull_bar);
+              tma_load_2d(a_dst + CODE_OFF + A_CODE_BYTES / 2, amap, (t.k0 + ks) * kx, t.a_row2, cfull_bar);
+            } else {
+              tma_load_2d(a_dst + CODE_OFF, amap, (t.k0 + ks) * kx, t.a_row, cfull_bar);
+            }
+            mbar_arrive_expect_tx(full_bar, b_bytes);
             for (int i = 0; i < b_boxes; ++i)
               tma_load_2d(a_dst + A_BYTES + i * kBTmaRows * 128, &map_b, (t.k0 + ks) * BK,
                           b_row0 + i * kBTmaRows, full_bar);
-            if (p.mode == MODE_GATEUP) {
-              tma_load_2d(a_dst + CODE_OFF, amap, (t.k0 + ks) * kx, t.a_row, full_bar);
-              tma_load_2d(a_dst + CODE_OFF + A_CODE_BYTES / 2, amap, (t.k0 + ks) * kx, t.a_row2, full_bar);
-            } else {
-              tma_load_2d(a_dst + CODE_OFF, amap, (t.k0 + ks) * kx, t.a_row, full_bar);
-            }
           } else if constexpr (CONV == CONV_NONE) {
             // Both CTAs' boxes complete on the leader's full barrier, which
             // expects the pair's bytes: no relay from the peer is needed.
@@ -571,9 +609,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       // Wait (bounded) for copies still in flight before the CTA exits.
       for (int s2 = 0; s2 < STAGES; ++s2)
         if (issued_parity[s2] >= 0) {
-          const long long t0 = cycles_now();
-          while (!mbar_try_wait(smem_u32(&tail->full[s2]), static_cast<uint32_t>(issued_parity[s2])) &&
+          const uint32_t par = static_cast<uint32_t>(issued_parity[s2]);
+          long long t0 = cycles_now();
+          while (!mbar_try_wait(smem_u32(&tail->full[s2]), par) &&
                  cycles_now() - t0 < kWaitLimitCycles) {
+          }
+          if constexpr (INT4) {
+            t0 = cycles_now();
+            while (!mbar_try_wait(smem_u32(&tail->cfull[s2]), par) &&
+                   cycles_now() - t0 < kWaitLimitCycles) {
+            }
           }
         }
     }
@@ -674,9 +719,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         }
         if constexpr (CONV == CONV_BF16_TO_F16) {
           // this warp's share of the stage's conversion (team warps 1, 2)
-          const float sreg[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-          if (!convert_stage<CONV>(p, sreg, sreg, g, phase, 1 + gq, rank, smem_base, tail, abort_flag,
-                                   lane)) {
+          if (!convert_stage_bf16(p, g, phase, 1 + gq, rank, smem_base, tail, abort_flag, lane)) {
             ok = false;
             break;
           }
@@ -764,11 +807,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     __syncwarp();
   } else if (warp >= FIN_WARP0) {
     // --------------------------------------------------- stage finishers --
-    // Finisher warp f owns pipeline stage f.  In the converting modes it is
-    // warp 0 of the stage's conversion team (with the stage's two token-row
+    // bf16 -> fp16: finisher warp f < STAGES owns pipeline stage f and is warp
+    // 0 of the stage's conversion team (with the stage's two token-row
     // producers): once this CTA's stage is full it converts its share of the
     // weight tile in place and arrives on the pair leader's ready barrier.
-    // Unconverted modes need no finisher: the producers signal the leader.
+    // int4: finishers 4 G .. 4 G + 3 take the k-steps with it % 2 == G, warp j
+    // expanding weight rows 32 j .. 32 j + 31 as soon as the codes land, so a
+    // stage's dequantisation takes a quarter of one warp's time and overlaps
+    // the token-row copies.  Unconverted modes need no finisher: the
+    // producers signal the leader.
     const int f = warp - FIN_WARP0;
     const int ntiles_fin = CONV == CONV_NONE ? 0 : ntiles;
     int it = 0;
@@ -777,16 +824,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       const Tile t = decode_tile(p, tile, rank);
       if (!t.valid) continue;
       for (int ks = 0; ks < t.nk; ++ks, ++it) {
-        if ((it % STAGES) != f) continue;
+        const int stage = it % STAGES;
         const uint32_t phase = static_cast<uint32_t>(it / STAGES) & 1u;
-        float sreg[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-        float breg[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-        if constexpr (conv_int4(CONV)) load_stage_scales<conv_affine(CONV)>(p, t, ks, lane, sreg, breg);
-        if (!convert_stage<CONV>(p, sreg, breg, f, phase, 0, rank, smem_base, tail, abort_flag,
-                                 lane)) {
-          ok = false;
-          break;
+        if constexpr (conv_int4(CONV)) {
+          if ((it & 1) != f / kInt4Warps) continue;
+          const int j = f % kInt4Warps;
+          float sv, bv;
+          load_row_scale<conv_affine(CONV)>(p, t, ks, j, lane, sv, bv);
+          ok = convert_stage_int4<CONV>(p, j, sv, bv, stage, phase, rank, smem_base, tail,
+                                        abort_flag, lane);
+        } else {
+          if (stage != f) continue;
+          ok = convert_stage_bf16(p, stage, phase, 0, rank, smem_base, tail, abort_flag, lane);
         }
+        if (!ok) break;
       }
     }
   } else {
