@@ -80,8 +80,8 @@ constexpr int B_BYTES = BN_HALF * BK * 2;       // 16 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // 32 KB
 // int4 weights: the TMA puts a stage's packed codes (BM rows x BK/2 bytes) in
 // the last 4 KB of the A region, where the finisher dequantises them in place.
-constexpr int A_CODE_BYTES = BM * BK / 2;       // 4 KB
-constexpr int CODE_OFF = A_BYTES - A_CODE_BYTES;
+constexpr int A_CODE_BYTES = BM * BK / 2;       // 4 KB: one k-step's int4 codes
+constexpr int kCodeSlots = 4;                   // int4 code ring (ahead of the stages)
 constexpr int ACC_COLS = 256;                   // one accumulator buffer
 constexpr int TMEM_COLS = 512;                  // two buffers
 // Warp roles (identical in both CTAs of a pair).
@@ -112,9 +112,9 @@ template <int CONV> __host__ __device__ constexpr int conv_team() {
 }
 
 struct SmemTail {
-  uint64_t full[STAGES];        // local: TMA (A; int4: token-row boxes only) + this CTA's B warps
-  uint64_t cfull[STAGES];       // local, int4: the stage's weight codes (TMA)
-  uint64_t cread[STAGES];       // local, int4: converters 0-2 hold their codes in registers
+  uint64_t full[STAGES];        // local: TMA (A, or int4: the producers' token-row boxes) + this CTA's B warps
+  uint64_t cfull[kCodeSlots];   // local, int4: a k-step's weight codes landed in the ring (TMA)
+  uint64_t cempty[kCodeSlots];  // local, int4: the k-step's converters hold their codes
   uint64_t ready[STAGES];       // leader: both CTAs' conversion teams
   uint64_t empty[STAGES];       // local: arrives from the leader's commit
   uint64_t tmem_full[2];        // local: arrives from the leader's commit
@@ -127,7 +127,8 @@ struct SmemTail {
 
 constexpr size_t kGemmSmemBytes = 1024 /*align slack*/ + STAGES * STAGE_BYTES +
                                   XCH_FLOATS * sizeof(float) + EPI_STAGE_BYTES +
-                                  B_WARPS * kRowTab * sizeof(int) + sizeof(SmemTail);
+                                  B_WARPS * kRowTab * sizeof(int) + sizeof(SmemTail) +
+                                  128 /*ring alignment*/ + kCodeSlots * A_CODE_BYTES;
 
 struct Tile {
   int valid;
@@ -266,18 +267,17 @@ __device__ __forceinline__ uint32_t dq_pair_affine(uint32_t lo_nib, uint32_t hi_
   return r;
 }
 
-// In-place dequantisation of rows 32 j .. 32 j + 31 of one stage's A tile by
-// one warp.  Row r's int4 codes (32 bytes = 64 K values, element 2m in the
-// low nibble of byte m) sit at tile + CODE_OFF + 32 r; they become q * s_r
-// (+ b_r) in bf16 (or fp16) in the 128-byte-swizzled K-major layout the MMA
-// reads.  Lane l handles 16-byte chunk l % 8 (K values 8 (l % 8) .. +7) of
-// rows 32 j + 4 m + l / 8, m = 0..7: load_codes_int4 reads its 8 code words,
-// expand_rows_int4 writes the outputs, bytes [4096 j, 4096 j + 4096) of the
-// tile.  Only batch j = 3 overwrites codes (CODE_OFF = 12288), so its warp
-// waits until the other three hold theirs in registers.
-__device__ __forceinline__ void load_codes_int4(uint32_t tile, int j, int lane,
+// Dequantisation of rows 32 j .. 32 j + 31 of one stage's A tile by one
+// warp.  Row r's int4 codes (32 bytes = 64 K values, element 2m in the low
+// nibble of byte m) sit at codes + 32 r in a slot of the code ring; they
+// become q * s_r (+ b_r) in bf16 (or fp16) in the 128-byte-swizzled K-major
+// layout the MMA reads.  Lane l handles 16-byte chunk l % 8 (K values
+// 8 (l % 8) .. +7) of rows 32 j + 4 m + l / 8, m = 0..7: load_codes_int4
+// reads its 8 code words, expand_rows_int4 writes the outputs, bytes
+// [4096 j, 4096 j + 4096) of the tile.
+__device__ __forceinline__ void load_codes_int4(uint32_t codes, int j, int lane,
                                                 uint32_t (&w)[8]) {
-  const uint32_t code0 = tile + CODE_OFF + 1024 * j + (lane >> 3) * 32 + (lane & 7) * 4;
+  const uint32_t code0 = codes + 1024 * j + (lane >> 3) * 32 + (lane & 7) * 4;
 #pragma unroll
   for (int m = 0; m < 8; ++m)
     asm volatile("ld.shared.u32 %0, [%1];" : "=r"(w[m]) : "r"(code0 + 128 * m));
@@ -405,34 +405,36 @@ __device__ __forceinline__ bool convert_stage_bf16(const GemmParams &p, int stag
   return true;
 }
 
-// int4 converter j (0..3) of a stage: expands weight rows 32 j .. 32 j + 31
-// once the codes have landed (cfull; the token rows may still be in flight),
-// then (the last converter) waits for the token rows (full) and arrives on
-// the leader's ready barrier.  sv, bv: this lane's row scale and bias, loaded by the caller
-// before the wait.  Returns false on a timeout or abort.
+// int4 converter j (0..3) of k-step `it` (stage it % STAGES, ring slot
+// it % kCodeSlots): takes its codes from the ring as soon as they land and
+// frees its share of the slot, waits until the MMA has released the stage's
+// A region, expands weight rows 32 j .. 32 j + 31 into it, and arrives on the
+// leader's ready barrier (the last converter only after the stage's token
+// rows have landed).  sv, bv: this lane's row scale and bias, loaded by the
+// caller before the waits.  Returns false on a timeout or abort.
 template <int CONV>
 __device__ __forceinline__ bool convert_stage_int4(const GemmParams &p, int j, float sv, float bv,
-                                                   int stage, uint32_t phase, int rank,
-                                                   uint32_t smem_base, SmemTail *tail,
+                                                   int it, int rank, uint32_t smem_base,
+                                                   uint32_t code_ring, SmemTail *tail,
                                                    volatile int *abort_flag, int lane) {
+  const int stage = it % STAGES, slot = it % kCodeSlots;
+  const uint32_t sph = static_cast<uint32_t>(it / STAGES) & 1u;
+  const uint32_t cph = static_cast<uint32_t>(it / kCodeSlots) & 1u;
   const uint32_t tile = smem_base + stage * STAGE_BYTES;
   int got = 1;
   if (lane == 0)
-    got = mbar_wait_bounded(smem_u32(&tail->cfull[stage]), phase, abort_flag, p.status,
+    got = mbar_wait_bounded(smem_u32(&tail->cfull[slot]), cph, abort_flag, p.status,
                             DEV_TIMEOUT_CONVERTER);
   if (!__shfl_sync(0xffffffffu, got, 0)) return false;
   uint32_t w[8];
-  load_codes_int4(tile, j, lane, w);
+  load_codes_int4(code_ring + slot * A_CODE_BYTES, j, lane, w);
   __syncwarp();
-  if (j < kInt4Warps - 1) {
-    if (lane == 0) mbar_arrive(smem_u32(&tail->cread[stage]));
-  } else {
-    // the last batch's outputs cover all codes: wait until the others hold theirs
-    if (lane == 0)
-      got = mbar_wait_bounded(smem_u32(&tail->cread[stage]), phase, abort_flag, p.status,
-                              DEV_TIMEOUT_CONVERTER);
-    if (!__shfl_sync(0xffffffffu, got, 0)) return false;
+  if (lane == 0) {
+    mbar_arrive(smem_u32(&tail->cempty[slot]));
+    got = mbar_wait_bounded(smem_u32(&tail->empty[stage]), sph ^ 1, abort_flag, p.status,
+                            DEV_TIMEOUT_CONVERTER);
   }
+  if (!__shfl_sync(0xffffffffu, got, 0)) return false;
   expand_rows_int4<conv_to_f16(CONV), conv_affine(CONV)>(tile, w, j, sv, bv, lane);
   fence_proxy_async_smem();
   __syncwarp();
@@ -440,7 +442,7 @@ __device__ __forceinline__ bool convert_stage_int4(const GemmParams &p, int j, f
     // one converter per CTA checks the token rows: the leader's ready phase
     // needs every converter's arrival
     if (j == kInt4Warps - 1)
-      got = mbar_wait_bounded(smem_u32(&tail->full[stage]), phase, abort_flag, p.status,
+      got = mbar_wait_bounded(smem_u32(&tail->full[stage]), sph, abort_flag, p.status,
                               DEV_TIMEOUT_CONVERTER);
     if (got) arrive_ready(tail, stage, rank);
   }
@@ -471,6 +473,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
   uint8_t *epi_stage = reinterpret_cast<uint8_t *>(xch + XCH_FLOATS);
   int *row_tab = reinterpret_cast<int *>(epi_stage + EPI_STAGE_BYTES);
   SmemTail *tail = reinterpret_cast<SmemTail *>(row_tab + B_WARPS * kRowTab);
+  const uint32_t code_ring = (smem_u32(tail + 1) + 127u) & ~127u;   // int4: kCodeSlots x 4 KB
   volatile int *abort_flag = &tail->abort_flag;
   pdl_trigger();   // the next kernel may start its set-up as SMs free up
 
@@ -488,8 +491,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
                 CONV == CONV_NONE ? 1 + 2 * B_WARPS_PER_STAGE : 1 + B_WARPS_PER_STAGE);
       mbar_init(smem_u32(&tail->ready[s]), 2 * conv_team<CONV>());
       mbar_init(smem_u32(&tail->empty[s]), 1);
+    }
+    for (int s = 0; s < kCodeSlots; ++s) {
       mbar_init(smem_u32(&tail->cfull[s]), 1);
-      mbar_init(smem_u32(&tail->cread[s]), kInt4Warps - 1);
+      mbar_init(smem_u32(&tail->cempty[s]), kInt4Warps);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(smem_u32(&tail->tmem_full[a]), 1);
@@ -520,15 +525,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
   if (warp == TMA_WARP) {
     // ------------------------------------------------ weight tiles (TMA) --
     // Lane 0 loads each k-step's 128 weight rows of this CTA with TMA into
-    // the stage's A region (complete_tx on the local full barrier); int4
-    // codes land packed at CODE_OFF for the stage finisher to expand.
+    // the stage's A region (complete_tx on the local full barrier).  int4
+    // codes go to the code ring instead (slot it % kCodeSlots, complete_tx
+    // on cfull), paced by the converters freeing slots, not by the MMA.
     // (Measured on GB300 and not kept: prefetching the weight rows into L2
     // ahead of the boxes, by TMA or by plain prefetches, and loading part or
     // all of the weight tile with cp.async from the stage producers -- each
     // was slower than plain TMA boxes.)
     constexpr bool INT4 = conv_int4(CONV);
     constexpr int kx = INT4 ? BK / 2 : BK;   // box x extent per k-step (bytes / elements)
-    int stage = 0;
+    constexpr int kBufs = INT4 ? kCodeSlots : STAGES;
+    static_assert(kCodeSlots <= STAGES, "issued_parity covers the code ring");
+    int stage = 0;   // int4: ring slot
     uint32_t phase = 0;
     int issued_parity[STAGES];
 #pragma unroll
@@ -541,8 +549,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         const CUtensorMap *amap = t.shared ? &map_a_shared : &map_a_routed;
         for (int ks = 0; ks < t.nk; ++ks) {
           MOE_T0();
-          if (!mbar_wait_bounded(smem_u32(&tail->empty[stage]), phase ^ 1, abort_flag, p.status,
-                                 DEV_TIMEOUT_PRODUCER)) {
+          const uint32_t free_bar = INT4 ? smem_u32(&tail->cempty[stage]) : smem_u32(&tail->empty[stage]);
+          if (!mbar_wait_bounded(free_bar, phase ^ 1, abort_flag, p.status, DEV_TIMEOUT_PRODUCER)) {
             ok = 0;
             break;
           }
@@ -554,20 +562,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
           const uint32_t b_bytes = static_cast<uint32_t>(b_boxes * kBTmaRows * BK * 2);
           const int b_row0 = t.row0 + rank * (t.nmma / 2);
           if constexpr (INT4) {
-            // codes on their own barrier (the converters start on them), the
-            // token-row boxes (if any) on the stage's full barrier
+            // codes only (the stage's token-row boxes, if any, come from its
+            // producer warps)
             const uint32_t cfull_bar = smem_u32(&tail->cfull[stage]);
+            const uint32_t c_dst = code_ring + stage * A_CODE_BYTES;
             mbar_arrive_expect_tx(cfull_bar, A_CODE_BYTES);
             if (p.mode == MODE_GATEUP) {
-              tma_load_2d(a_dst + CODE_OFF, amap, (t.k0 + ks) * kx, t.a_row, cfull_bar);
-              tma_load_2d(a_dst + CODE_OFF + A_CODE_BYTES / 2, amap, (t.k0 + ks) * kx, t.a_row2, cfull_bar);
+              tma_load_2d(c_dst, amap, (t.k0 + ks) * kx, t.a_row, cfull_bar);
+              tma_load_2d(c_dst + A_CODE_BYTES / 2, amap, (t.k0 + ks) * kx, t.a_row2, cfull_bar);
             } else {
-              tma_load_2d(a_dst + CODE_OFF, amap, (t.k0 + ks) * kx, t.a_row, cfull_bar);
+              tma_load_2d(c_dst, amap, (t.k0 + ks) * kx, t.a_row, cfull_bar);
             }
-            mbar_arrive_expect_tx(full_bar, b_bytes);
-            for (int i = 0; i < b_boxes; ++i)
-              tma_load_2d(a_dst + A_BYTES + i * kBTmaRows * 128, &map_b, (t.k0 + ks) * BK,
-                          b_row0 + i * kBTmaRows, full_bar);
           } else if constexpr (CONV == CONV_NONE) {
             // Both CTAs' boxes complete on the leader's full barrier, which
             // expects the pair's bytes: no relay from the peer is needed.
@@ -597,7 +602,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
           // (the peer's boxes in the unconverted modes complete on the
           // leader's barrier: nothing local to wait for on abort)
           if (!(CONV == CONV_NONE && rank == 1)) issued_parity[stage] = static_cast<int>(phase);
-          if (++stage == STAGES) {
+          if (++stage == kBufs) {
             stage = 0;
             phase ^= 1;
           }
@@ -607,18 +612,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     }
     if (!ok && lane == 0) {
       // Wait (bounded) for copies still in flight before the CTA exits.
-      for (int s2 = 0; s2 < STAGES; ++s2)
+      for (int s2 = 0; s2 < kBufs; ++s2)
         if (issued_parity[s2] >= 0) {
-          const uint32_t par = static_cast<uint32_t>(issued_parity[s2]);
-          long long t0 = cycles_now();
-          while (!mbar_try_wait(smem_u32(&tail->full[s2]), par) &&
+          const uint32_t bar = INT4 ? smem_u32(&tail->cfull[s2]) : smem_u32(&tail->full[s2]);
+          const long long t0 = cycles_now();
+          while (!mbar_try_wait(bar, static_cast<uint32_t>(issued_parity[s2])) &&
                  cycles_now() - t0 < kWaitLimitCycles) {
-          }
-          if constexpr (INT4) {
-            t0 = cycles_now();
-            while (!mbar_try_wait(smem_u32(&tail->cfull[s2]), par) &&
-                   cycles_now() - t0 < kWaitLimitCycles) {
-            }
           }
         }
     }
@@ -658,6 +657,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     if (pair_id < ntiles) prefetch_b(pair_id);
     int it = 0;   // k-step counter over all tiles of this CTA
     bool ok = true;
+    int boxes_parity = -1;   // int4, b_tma: phase of this warp's last token-row boxes
     for (int tile = pair_id; tile < ntiles && ok; tile += num_pairs) {
       const Tile t = decode_tile(p, tile, rank);
       prefetch_b(tile + num_pairs);
@@ -691,6 +691,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
 #ifdef MOE_TRACE
         const long long tb1 = clock64();
 #endif
+        if (conv_int4(CONV) && gq == 0 && lane == 0) {
+          // int4: the TMA warp streams codes only; this CTA's token-row boxes
+          // (down: h rows, consecutive) come from here, on the full barrier
+          const int b_boxes = p.b_tma ? t.nmma / 2 / kBTmaRows : 0;
+          mbar_arrive_expect_tx(full_bar, static_cast<uint32_t>(b_boxes * kBTmaRows * BK * 2));
+          const int b_row0 = t.row0 + rank * (t.nmma / 2);
+          for (int i = 0; i < b_boxes; ++i)
+            tma_load_2d(stage_b + i * kBTmaRows * 128, &map_b, (t.k0 + ks) * BK,
+                        b_row0 + i * kBTmaRows, full_bar);
+          if (b_boxes > 0) boxes_parity = static_cast<int>(phase);
+        }
         const int kc = (t.k0 + ks) * BK + c * 8;
         for (int j = gq, e = rsub; j < (p.b_tma ? 0 : nquads); j += B_WARPS_PER_STAGE, e += 4) {
           const int r = 4 * j + rsub;
@@ -724,6 +735,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
             break;
           }
         }
+      }
+    }
+    if (!ok && boxes_parity >= 0) {
+      // Wait (bounded) for this warp's boxes still in flight before the CTA exits.
+      const long long t0 = cycles_now();
+      while (!mbar_try_wait(full_bar, static_cast<uint32_t>(boxes_parity)) &&
+             cycles_now() - t0 < kWaitLimitCycles) {
       }
     }
     __syncwarp();
@@ -814,7 +832,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     // int4: finishers 4 G .. 4 G + 3 take the k-steps with it % 2 == G, warp j
     // expanding weight rows 32 j .. 32 j + 31 as soon as the codes land, so a
     // stage's dequantisation takes a quarter of one warp's time and overlaps
-    // the token-row copies.  Unconverted modes need no finisher: the
+    // the token-row copies; the codes run up to kCodeSlots k-steps ahead in
+    // their own ring.  Unconverted modes need no finisher: the
     // producers signal the leader.
     const int f = warp - FIN_WARP0;
     const int ntiles_fin = CONV == CONV_NONE ? 0 : ntiles;
@@ -831,7 +850,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
           const int j = f % kInt4Warps;
           float sv, bv;
           load_row_scale<conv_affine(CONV)>(p, t, ks, j, lane, sv, bv);
-          ok = convert_stage_int4<CONV>(p, j, sv, bv, stage, phase, rank, smem_base, tail,
+          ok = convert_stage_int4<CONV>(p, j, sv, bv, it, rank, smem_base, code_ring, tail,
                                         abort_flag, lane);
         } else {
           if (stage != f) continue;
