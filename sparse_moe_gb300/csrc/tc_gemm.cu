@@ -64,9 +64,15 @@ __device__ unsigned long long g_moe_trace[3][1024][16];
 #define MOE_TADD(slot)                                        \
   atomicAdd(&g_moe_trace[p.mode][blockIdx.x & 1023][slot], \
             static_cast<unsigned long long>(clock64() - _t0))
+#define MOE_TSTAMP(var) const long long var = clock64()
+#define MOE_TSPAN(slot, a, b)                                  \
+  atomicAdd(&g_moe_trace[p.mode][blockIdx.x & 1023][slot], \
+            static_cast<unsigned long long>((b) - (a)))
 #else
 #define MOE_T0()
 #define MOE_TADD(slot)
+#define MOE_TSTAMP(var)
+#define MOE_TSPAN(slot, a, b)
 #endif
 
 constexpr int BM = 128;                 // A rows per CTA (MMA M = 256 per pair)
@@ -110,11 +116,19 @@ static_assert(2 * kInt4Warps == FIN_WARPS && STAGES % 2 == 0, "int4 finisher gro
 template <int CONV> __host__ __device__ constexpr int conv_team() {
   return CONV == CONV_BF16_TO_F16 ? kConvTeam : conv_int4(CONV) ? kInt4Warps : 1;
 }
+// Arrivals on the leader's ready barrier per k-step: both CTAs' conversion
+// teams, except for int4, where the peer's four converters arrive on a local
+// barrier (cdone) and one relay thread forwards a single cluster-scope arrival
+// (a cluster-scope release costs each arriving thread about a thousand cycles).
+template <int CONV> __host__ __device__ constexpr int ready_count() {
+  return conv_int4(CONV) ? kInt4Warps + 1 : 2 * conv_team<CONV>();
+}
 
 struct SmemTail {
   uint64_t full[STAGES];        // local: TMA (A, or int4: the producers' token-row boxes) + this CTA's B warps
   uint64_t cfull[kCodeSlots];   // local, int4: a k-step's weight codes landed in the ring (TMA)
   uint64_t cempty[kCodeSlots];  // local, int4: the k-step's converters hold their codes
+  uint64_t cdone[STAGES];       // peer, int4: its four converters are done (relayed to ready)
   uint64_t ready[STAGES];       // leader: both CTAs' conversion teams
   uint64_t empty[STAGES];       // local: arrives from the leader's commit
   uint64_t tmem_full[2];        // local: arrives from the leader's commit
@@ -409,8 +423,8 @@ __device__ __forceinline__ bool convert_stage_bf16(const GemmParams &p, int stag
 // it % kCodeSlots): takes its codes from the ring as soon as they land and
 // frees its share of the slot, waits until the MMA has released the stage's
 // A region, expands weight rows 32 j .. 32 j + 31 into it, and arrives on the
-// leader's ready barrier (the last converter only after the stage's token
-// rows have landed).  sv, bv: this lane's row scale and bias, loaded by the
+// leader's ready barrier, or in the peer on its local cdone barrier (the last
+// converter only after the stage's token rows have landed).  sv, bv: this lane's row scale and bias, loaded by the
 // caller before the waits.  Returns false on a timeout or abort.
 template <int CONV>
 __device__ __forceinline__ bool convert_stage_int4(const GemmParams &p, int j, float sv, float bv,
@@ -422,10 +436,12 @@ __device__ __forceinline__ bool convert_stage_int4(const GemmParams &p, int j, f
   const uint32_t cph = static_cast<uint32_t>(it / kCodeSlots) & 1u;
   const uint32_t tile = smem_base + stage * STAGE_BYTES;
   int got = 1;
+  MOE_TSTAMP(tc0);
   if (lane == 0)
     got = mbar_wait_bounded(smem_u32(&tail->cfull[slot]), cph, abort_flag, p.status,
                             DEV_TIMEOUT_CONVERTER);
   if (!__shfl_sync(0xffffffffu, got, 0)) return false;
+  MOE_TSTAMP(tc1);
   uint32_t w[8];
   load_codes_int4(code_ring + slot * A_CODE_BYTES, j, lane, w);
   __syncwarp();
@@ -435,17 +451,31 @@ __device__ __forceinline__ bool convert_stage_int4(const GemmParams &p, int j, f
                             DEV_TIMEOUT_CONVERTER);
   }
   if (!__shfl_sync(0xffffffffu, got, 0)) return false;
+  MOE_TSTAMP(tc2);
   expand_rows_int4<conv_to_f16(CONV), conv_affine(CONV)>(tile, w, j, sv, bv, lane);
   fence_proxy_async_smem();
   __syncwarp();
+  MOE_TSTAMP(tc3);
   if (lane == 0) {
     // one converter per CTA checks the token rows: the leader's ready phase
     // needs every converter's arrival
     if (j == kInt4Warps - 1)
       got = mbar_wait_bounded(smem_u32(&tail->full[stage]), sph, abort_flag, p.status,
                               DEV_TIMEOUT_CONVERTER);
-    if (got) arrive_ready(tail, stage, rank);
+    if (got) {
+      if (rank == 0) mbar_arrive(smem_u32(&tail->ready[stage]));
+      else mbar_arrive(smem_u32(&tail->cdone[stage]));   // relayed by the peer's MMA warp
+    }
   }
+#ifdef MOE_TRACE
+  if (lane == 0) {
+    MOE_TSTAMP(tc4);
+    MOE_TSPAN(12, tc0, tc1);   // wait for codes
+    MOE_TSPAN(13, tc1, tc2);   // codes to registers + wait for the stage's A region
+    MOE_TSPAN(14, tc2, tc3);   // expansion
+    MOE_TSPAN(15, tc3, tc4);   // (last converter) wait for token rows
+  }
+#endif
   return __shfl_sync(0xffffffffu, got, 0) != 0;
 }
 
@@ -489,7 +519,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       // producers (and both CTAs' TMA bytes); otherwise each CTA's own
       mbar_init(smem_u32(&tail->full[s]),
                 CONV == CONV_NONE ? 1 + 2 * B_WARPS_PER_STAGE : 1 + B_WARPS_PER_STAGE);
-      mbar_init(smem_u32(&tail->ready[s]), 2 * conv_team<CONV>());
+      mbar_init(smem_u32(&tail->ready[s]), ready_count<CONV>());
+      mbar_init(smem_u32(&tail->cdone[s]), kInt4Warps);
       mbar_init(smem_u32(&tail->empty[s]), 1);
     }
     for (int s = 0; s < kCodeSlots; ++s) {
@@ -821,6 +852,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
           }
         }
       }
+    } else if (conv_int4(CONV) && lane == 0) {
+      // ------------------------------------------- int4 readiness relay (peer) --
+      // Once this CTA's four converters of a k-step are done (cdone, a
+      // CTA-scope acquire), one cluster-scope release-arrive tells the leader.
+      int it = 0;
+      bool ok = true;
+      for (int tile = pair_id; tile < ntiles && ok; tile += num_pairs) {
+        const Tile t = decode_tile(p, tile, rank);
+        if (!t.valid) continue;
+        for (int ks = 0; ks < t.nk; ++ks, ++it) {
+          const int stage = it % STAGES;
+          if (!mbar_wait_bounded(smem_u32(&tail->cdone[stage]),
+                                 static_cast<uint32_t>(it / STAGES) & 1u, abort_flag, p.status,
+                                 DEV_TIMEOUT_RELAY)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_cluster(mapa_shared(smem_u32(&tail->ready[stage]), 0));
+        }
+      }
     }
     __syncwarp();
   } else if (warp >= FIN_WARP0) {
@@ -839,6 +890,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     const int ntiles_fin = CONV == CONV_NONE ? 0 : ntiles;
     int it = 0;
     bool ok = true;
+    // int4: every tile's nk is even, so group G's k-steps are ks = G, G + 2, ...
+    // of each tile; the row scales of the group's next k-step in the tile are
+    // loaded while this one converts (a global load's latency would otherwise
+    // sit inside every expansion).
+    float sv_next = 0.0f, bv_next = 0.0f;
+    bool have_next = false;
     for (int tile = pair_id; tile < ntiles_fin && ok; tile += num_pairs) {
       const Tile t = decode_tile(p, tile, rank);
       if (!t.valid) continue;
@@ -848,8 +905,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         if constexpr (conv_int4(CONV)) {
           if ((it & 1) != f / kInt4Warps) continue;
           const int j = f % kInt4Warps;
-          float sv, bv;
-          load_row_scale<conv_affine(CONV)>(p, t, ks, j, lane, sv, bv);
+          float sv = sv_next, bv = bv_next;
+          if (!have_next) load_row_scale<conv_affine(CONV)>(p, t, ks, j, lane, sv, bv);
+          have_next = ks + 2 < t.nk;
+          if (have_next) load_row_scale<conv_affine(CONV)>(p, t, ks + 2, j, lane, sv_next, bv_next);
           ok = convert_stage_int4<CONV>(p, j, sv, bv, it, rank, smem_base, code_ring, tail,
                                         abort_flag, lane);
         } else {
