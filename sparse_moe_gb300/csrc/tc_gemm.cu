@@ -108,11 +108,25 @@ constexpr int kRowTab = 4 * ((BN_HALF / 4 + B_WARPS_PER_STAGE - 1) / B_WARPS_PER
 
 // Warps that convert one stage's weight tile, per CTA: for bf16 -> fp16 the
 // stage's finisher (finisher f owns stage f) and its two token-row producers,
-// each a share of the chunks; for int4 four finishers, one per 32 weight rows
-// (finishers 0-3 take the even k-steps, 4-7 the odd ones).
+// each a share of the chunks; for int4 kInt4Warps finishers, each expanding
+// kInt4Batches batches of 32 weight rows, the finishers forming kInt4Groups
+// teams that take k-steps in turn (team g: it % kInt4Groups == g).  Measured
+// at T=4096: four warps of 32 rows per k-step (two teams) beat two of 64 rows
+// (four teams) by 20 %.
+//
+// A team's next k-step is kInt4Groups k-steps later; its parity waits on the
+// stage and code-ring barriers stay unambiguous only if no team can reach a
+// barrier phase two ahead of the completed one: every ring slot is used by
+// one team (kCodeSlots a multiple of kInt4Groups) and a team's previous
+// k-step already waited for the stage's previous use (kInt4Groups <= STAGES).
 constexpr int kConvTeam = 1 + B_WARPS_PER_STAGE;
 constexpr int kInt4Warps = 4;
-static_assert(2 * kInt4Warps == FIN_WARPS && STAGES % 2 == 0, "int4 finisher groups");
+constexpr int kInt4Batches = (BM / 32) / kInt4Warps;
+constexpr int kInt4Groups = FIN_WARPS / kInt4Warps;
+static_assert(kInt4Warps * kInt4Batches * 32 == BM && kInt4Groups * kInt4Warps == FIN_WARPS,
+              "int4 finisher teams");
+static_assert(kCodeSlots % kInt4Groups == 0 && kInt4Groups <= STAGES,
+              "int4 teams must not alias barrier phases");
 template <int CONV> __host__ __device__ constexpr int conv_team() {
   return CONV == CONV_BF16_TO_F16 ? kConvTeam : conv_int4(CONV) ? kInt4Warps : 1;
 }
@@ -419,16 +433,19 @@ __device__ __forceinline__ bool convert_stage_bf16(const GemmParams &p, int stag
   return true;
 }
 
-// int4 converter j (0..3) of k-step `it` (stage it % STAGES, ring slot
-// it % kCodeSlots): takes its codes from the ring as soon as they land and
-// frees its share of the slot, waits until the MMA has released the stage's
-// A region, expands weight rows 32 j .. 32 j + 31 into it, and arrives on the
-// leader's ready barrier, or in the peer on its local cdone barrier (the last
-// converter only after the stage's token rows have landed).  sv, bv: this lane's row scale and bias, loaded by the
-// caller before the waits.  Returns false on a timeout or abort.
+// int4 converter q (0 .. kInt4Warps - 1) of k-step `it` (stage it % STAGES,
+// ring slot it % kCodeSlots): takes its codes (batches q * kInt4Batches + b)
+// from the ring as soon as they land and frees its share of the slot, waits
+// until the MMA has released the stage's A region, expands its weight rows
+// into it, and arrives on the leader's ready barrier, or in the peer on its
+// local cdone barrier (the last converter only after the stage's token rows
+// have landed).  sv, bv: this lane's row scales and biases, one per batch,
+// loaded by the caller before the waits.  Returns false on a timeout or abort.
 template <int CONV>
-__device__ __forceinline__ bool convert_stage_int4(const GemmParams &p, int j, float sv, float bv,
-                                                   int it, int rank, uint32_t smem_base,
+__device__ __forceinline__ bool convert_stage_int4(const GemmParams &p, int q,
+                                                   const float (&sv)[kInt4Batches],
+                                                   const float (&bv)[kInt4Batches], int it,
+                                                   int rank, uint32_t smem_base,
                                                    uint32_t code_ring, SmemTail *tail,
                                                    volatile int *abort_flag, int lane) {
   const int stage = it % STAGES, slot = it % kCodeSlots;
@@ -442,8 +459,10 @@ __device__ __forceinline__ bool convert_stage_int4(const GemmParams &p, int j, f
                             DEV_TIMEOUT_CONVERTER);
   if (!__shfl_sync(0xffffffffu, got, 0)) return false;
   MOE_TSTAMP(tc1);
-  uint32_t w[8];
-  load_codes_int4(code_ring + slot * A_CODE_BYTES, j, lane, w);
+  uint32_t w[kInt4Batches][8];
+#pragma unroll
+  for (int b = 0; b < kInt4Batches; ++b)
+    load_codes_int4(code_ring + slot * A_CODE_BYTES, q * kInt4Batches + b, lane, w[b]);
   __syncwarp();
   if (lane == 0) {
     mbar_arrive(smem_u32(&tail->cempty[slot]));
@@ -452,14 +471,17 @@ __device__ __forceinline__ bool convert_stage_int4(const GemmParams &p, int j, f
   }
   if (!__shfl_sync(0xffffffffu, got, 0)) return false;
   MOE_TSTAMP(tc2);
-  expand_rows_int4<conv_to_f16(CONV), conv_affine(CONV)>(tile, w, j, sv, bv, lane);
+#pragma unroll
+  for (int b = 0; b < kInt4Batches; ++b)
+    expand_rows_int4<conv_to_f16(CONV), conv_affine(CONV)>(tile, w[b], q * kInt4Batches + b,
+                                                           sv[b], bv[b], lane);
   fence_proxy_async_smem();
   __syncwarp();
   MOE_TSTAMP(tc3);
   if (lane == 0) {
     // one converter per CTA checks the token rows: the leader's ready phase
     // needs every converter's arrival
-    if (j == kInt4Warps - 1)
+    if (q == kInt4Warps - 1)
       got = mbar_wait_bounded(smem_u32(&tail->full[stage]), sph, abort_flag, p.status,
                               DEV_TIMEOUT_CONVERTER);
     if (got) {
@@ -880,21 +902,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     // 0 of the stage's conversion team (with the stage's two token-row
     // producers): once this CTA's stage is full it converts its share of the
     // weight tile in place and arrives on the pair leader's ready barrier.
-    // int4: finishers 4 G .. 4 G + 3 take the k-steps with it % 2 == G, warp j
-    // expanding weight rows 32 j .. 32 j + 31 as soon as the codes land, so a
-    // stage's dequantisation takes a quarter of one warp's time and overlaps
-    // the token-row copies; the codes run up to kCodeSlots k-steps ahead in
-    // their own ring.  Unconverted modes need no finisher: the
-    // producers signal the leader.
+    // int4: team g (finishers kInt4Warps g ..) takes the k-steps with
+    // it % kInt4Groups == g, each warp expanding its share of the weight rows
+    // as soon as the codes land and the stage is free, overlapping the
+    // token-row copies; the codes run up to kCodeSlots k-steps ahead in their
+    // own ring.  Unconverted modes need no finisher: the producers signal the
+    // leader.
     const int f = warp - FIN_WARP0;
     const int ntiles_fin = CONV == CONV_NONE ? 0 : ntiles;
     int it = 0;
     bool ok = true;
-    // int4: every tile's nk is even, so group G's k-steps are ks = G, G + 2, ...
-    // of each tile; the row scales of the group's next k-step in the tile are
-    // loaded while this one converts (a global load's latency would otherwise
-    // sit inside every expansion).
-    float sv_next = 0.0f, bv_next = 0.0f;
+    // int4: the row scales of the team's next k-step in the tile (ks +
+    // kInt4Groups) are loaded while this one converts (a global load's latency
+    // would otherwise sit inside every expansion).
+    float sv_next[kInt4Batches] = {}, bv_next[kInt4Batches] = {};
     bool have_next = false;
     for (int tile = pair_id; tile < ntiles_fin && ok; tile += num_pairs) {
       const Tile t = decode_tile(p, tile, rank);
@@ -903,13 +924,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         const int stage = it % STAGES;
         const uint32_t phase = static_cast<uint32_t>(it / STAGES) & 1u;
         if constexpr (conv_int4(CONV)) {
-          if ((it & 1) != f / kInt4Warps) continue;
-          const int j = f % kInt4Warps;
-          float sv = sv_next, bv = bv_next;
-          if (!have_next) load_row_scale<conv_affine(CONV)>(p, t, ks, j, lane, sv, bv);
-          have_next = ks + 2 < t.nk;
-          if (have_next) load_row_scale<conv_affine(CONV)>(p, t, ks + 2, j, lane, sv_next, bv_next);
-          ok = convert_stage_int4<CONV>(p, j, sv, bv, it, rank, smem_base, code_ring, tail,
+          if (it % kInt4Groups != f / kInt4Warps) continue;
+          const int q = f % kInt4Warps;
+          float sv[kInt4Batches], bv[kInt4Batches];
+#pragma unroll
+          for (int b = 0; b < kInt4Batches; ++b) {
+            sv[b] = sv_next[b];
+            bv[b] = bv_next[b];
+            if (!have_next)
+              load_row_scale<conv_affine(CONV)>(p, t, ks, q * kInt4Batches + b, lane, sv[b], bv[b]);
+          }
+          have_next = ks + kInt4Groups < t.nk;
+          if (have_next) {
+#pragma unroll
+            for (int b = 0; b < kInt4Batches; ++b)
+              load_row_scale<conv_affine(CONV)>(p, t, ks + kInt4Groups, q * kInt4Batches + b, lane,
+                                                sv_next[b], bv_next[b]);
+          }
+          ok = convert_stage_int4<CONV>(p, q, sv, bv, it, rank, smem_base, code_ring, tail,
                                         abort_flag, lane);
         } else {
           if (stage != f) continue;
