@@ -352,50 +352,61 @@ def bench_ablations(args, dev, stream, flush):
     return out
 
 
+def _sweep_point(T, dev, stream, flush, tf_burst, hbm, steps):
+    """One prefill-path point of the sweep workload at T tokens (seed = T,
+    router bias 1.5, 4096-row chunks)."""
+    from sparse_moe_gb300 import MoEContext, with_f16_down
+    wl = moe_synth.sweep_workload(T)
+    s = wl.shape
+    ctx = MoEContext(s.hidden, s.n_experts, s.top_k, s.inter, s.shared_inter, n_layers=1,
+                     max_chunk_rows=4096, device=dev.index)
+    w = moe_synth.make_layer(wl, device=dev)
+    ctx.load_weights(0, with_f16_down(w))
+    x = moe_synth.make_x(wl, device=dev)
+    y = torch.empty_like(x)
+    touched = 0
+    for c0 in range(0, T, 4096):
+        cnt = ctx.route(0, x[c0:c0 + 4096])["counts"]
+        touched += int((cnt > 0).sum().item()) + 1   # + the shared expert
+    for _ in range(2):
+        ctx.forward_prefill(0, x, y, stream=stream)
+    torch.cuda.synchronize()
+    a = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    b = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    with torch.cuda.stream(stream):
+        for i in range(steps):
+            flush.zero_()
+            a[i].record(stream)
+            ctx.forward_prefill(0, x, y, stream=stream)
+            b[i].record(stream)
+    torch.cuda.synchronize()
+    ms = float(np.mean([e0.elapsed_time(e1) for e0, e1 in zip(a, b)]))
+    gu_f, dn_f, rt_f = algorithmic(s, T)
+    wbytes = touched * 3 * s.inter * s.hidden * 2 + s.n_experts * s.hidden * 2
+    ctx.close()
+    del w, x, y
+    torch.cuda.empty_cache()
+    return {"T": T, "tokens_per_s": T / (ms * 1e-3), "ms": ms, "chunks": (T + 4095) // 4096,
+            "tensor_frac": (gu_f + dn_f + rt_f) / (ms * 1e-3) / 1e12 / tf_burst,
+            "hbm_frac_expert_weights": wbytes / (ms * 1e-3) / 1e9 / hbm,
+            "experts_touched_per_chunk": touched / ((T + 4095) // 4096)}
+
+
 def bench_sweep(args, dev, stream, flush, tf_burst, hbm):
     """Prefill over the prompt-length sweep (T = 256 .. 128K, seed = T, router
     bias 1.5), long prompts in 4096-row chunks: tokens/s, and the fraction of
     the tensor peak (algorithmic FLOPs) and of the HBM peak (expert weights
     the chunks touch, each counted once per chunk) that the layer reaches."""
-    from sparse_moe_gb300 import MoEContext, with_f16_down
-    out = []
-    for T in moe_synth.SWEEP_T:
-        wl = moe_synth.sweep_workload(T)
-        s = wl.shape
-        ctx = MoEContext(s.hidden, s.n_experts, s.top_k, s.inter, s.shared_inter, n_layers=1,
-                         max_chunk_rows=4096, device=dev.index)
-        w = moe_synth.make_layer(wl, device=dev)
-        ctx.load_weights(0, with_f16_down(w))
-        x = moe_synth.make_x(wl, device=dev)
-        y = torch.empty_like(x)
-        touched = 0
-        for c0 in range(0, T, 4096):
-            cnt = ctx.route(0, x[c0:c0 + 4096])["counts"]
-            touched += int((cnt > 0).sum().item()) + 1   # + the shared expert
-        steps = 3 if T >= 32768 else 5
-        for _ in range(2):
-            ctx.forward_prefill(0, x, y, stream=stream)
-        torch.cuda.synchronize()
-        a = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
-        b = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
-        with torch.cuda.stream(stream):
-            for i in range(steps):
-                flush.zero_()
-                a[i].record(stream)
-                ctx.forward_prefill(0, x, y, stream=stream)
-                b[i].record(stream)
-        torch.cuda.synchronize()
-        ms = float(np.mean([e0.elapsed_time(e1) for e0, e1 in zip(a, b)]))
-        gu_f, dn_f, rt_f = algorithmic(s, T)
-        wbytes = touched * 3 * s.inter * s.hidden * 2 + s.n_experts * s.hidden * 2
-        out.append({"T": T, "tokens_per_s": T / (ms * 1e-3), "ms": ms, "chunks": (T + 4095) // 4096,
-                    "tensor_frac": (gu_f + dn_f + rt_f) / (ms * 1e-3) / 1e12 / tf_burst,
-                    "hbm_frac_expert_weights": wbytes / (ms * 1e-3) / 1e9 / hbm,
-                    "experts_touched_per_chunk": touched / ((T + 4095) // 4096)})
-        ctx.close()
-        del w, x, y
-        torch.cuda.empty_cache()
-    return out
+    return [_sweep_point(T, dev, stream, flush, tf_burst, hbm, 3 if T >= 32768 else 5)
+            for T in moe_synth.SWEEP_T]
+
+
+def bench_small_m(args, dev, stream, flush, tf_burst, hbm):
+    """Small row counts (2 - 16 rows, the page's speculative-verification
+    shapes) through the prefill path, whose grouped GEMMs run each expert's
+    block at MMA N = 32: each point reads the weights of every expert it
+    touches once, so the HBM fraction over those weights is the figure."""
+    return [_sweep_point(T, dev, stream, flush, tf_burst, hbm, 20) for T in (2, 4, 8, 16)]
 
 
 def bench_decode(args, dev, stream, hbm, int4=None, wl=None):
@@ -664,6 +675,7 @@ def main(args):
         line["decode"] = bench_decode(args, dev, stream, hbm)
     if rank == 0 and not args.skip_sweep:
         line["sweep"] = bench_sweep(args, dev, stream, flush, tf_burst, hbm)
+        line["small_m"] = bench_small_m(args, dev, stream, flush, tf_burst, hbm)
     if rank == 0 and not args.skip_ablations:
         line["ablations"] = bench_ablations(args, dev, stream, flush)
     if rank == 0 and not args.skip_int4:

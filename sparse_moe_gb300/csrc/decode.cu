@@ -117,73 +117,69 @@ __device__ __forceinline__ float dot8_bf16_f32(const uint4 wv, const float (&xs)
   return a;
 }
 
-// Signed code of nibble n (0..7) of a 32-bit word.
-__device__ __forceinline__ float nib(uint32_t word, int n) {
-  return static_cast<float>(static_cast<int>(word << (28 - 4 * n)) >> 28);
+// int4 dot products on packed fp16 pairs.  For a 32-bit word of eight codes
+// (element n in nibble n), ((word >> 4 k) & 0x000F000F) | 0x6400_6400 is the
+// fp16 pair (1024 + u_k, 1024 + u_{k+4}) exactly (fp16 has unit spacing on
+// [1024, 2048)), so one packed subtract gives the codes (u - 8 for the
+// signed format, whose nibbles are first flipped to u = q + 8; u for the
+// affine one) and one packed fma multiplies them by the activation pair
+// (x_k, x_{k+4}).  Per 32-code chunk the products are summed in fp16 (eight
+// per half), then in fp32: about three instructions per weight instead of
+// five for a convert-and-fma per code.
+
+// fp16 pair (lo, hi), round to nearest even.
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
 }
 
-// 32 int4 codes (one 16-byte chunk; element n of word w is nibble n) . 32
-// bf16 activations (four 16-byte chunks).  Returns sum q * x without the
-// group scale.
-__device__ __forceinline__ float dot32_int4_bf16(const uint4 wv, const uint4 (&xv)[4]) {
-  const uint32_t words[4] = {wv.x, wv.y, wv.z, wv.w};
-  float a = 0.0f;
+// The activation pairs of one code word from 8 bf16 values (one 16-byte
+// chunk): pair k = (x_k, x_{k+4}).
+__device__ __forceinline__ void xpairs_bf16(const uint4 xv, uint32_t (&h)[4]) {
+  h[0] = pack_f16x2(bf16_lo(xv.x), bf16_lo(xv.z));
+  h[1] = pack_f16x2(bf16_hi(xv.x), bf16_hi(xv.z));
+  h[2] = pack_f16x2(bf16_lo(xv.y), bf16_lo(xv.w));
+  h[3] = pack_f16x2(bf16_hi(xv.y), bf16_hi(xv.w));
+}
+
+// Same from 8 fp32 values.
+__device__ __forceinline__ void xpairs_f32(const float *x8, uint32_t (&h)[4]) {
 #pragma unroll
-  for (int w = 0; w < 4; ++w) {
-    const uint32_t xs[4] = {xv[w].x, xv[w].y, xv[w].z, xv[w].w};
+  for (int k = 0; k < 4; ++k) h[k] = pack_f16x2(x8[k], x8[k + 4]);
+}
+
+// acc + (q_k x_k, q_{k+4} x_{k+4}) summed over k, packed fp16.
+template <bool SIGNED>
+__device__ __forceinline__ uint32_t hdot8(uint32_t word, const uint32_t (&h)[4], uint32_t acc) {
+  if (SIGNED) word ^= 0x88888888u;
 #pragma unroll
-    for (int m = 0; m < 4; ++m) {
-      a = fmaf(nib(words[w], 2 * m), bf16_lo(xs[m]), a);
-      a = fmaf(nib(words[w], 2 * m + 1), bf16_hi(xs[m]), a);
-    }
+  for (int k = 0; k < 4; ++k) {
+    const uint32_t v = ((word >> (4 * k)) & 0x000F000Fu) | 0x64006400u;
+    asm("{\n .reg .b32 t;\n sub.f16x2 t, %1, %2;\n fma.rn.f16x2 %0, t, %3, %0;\n}"
+        : "+r"(acc)
+        : "r"(v), "r"(SIGNED ? 0x64086408u : 0x64006400u), "r"(h[k]));
   }
-  return a;
+  return acc;
 }
 
-// Same with 32 fp32 activations held in registers.
-__device__ __forceinline__ float dot32_int4_f32(const uint4 wv, const float (&xs)[32]) {
-  const uint32_t words[4] = {wv.x, wv.y, wv.z, wv.w};
-  float a = 0.0f;
-#pragma unroll
-  for (int w = 0; w < 4; ++w)
-#pragma unroll
-    for (int n = 0; n < 8; ++n) a = fmaf(nib(words[w], n), xs[8 * w + n], a);
-  return a;
+// fp32 sum of the four halves of two fp16 pairs.
+__device__ __forceinline__ float hsum4(uint32_t a, uint32_t b) {
+  const float2 fa = __half22float2(*reinterpret_cast<const __half2 *>(&a));
+  const float2 fb = __half22float2(*reinterpret_cast<const __half2 *>(&b));
+  return (fa.x + fa.y) + (fb.x + fb.y);
 }
 
-// Unsigned code of nibble n (0..7) of a 32-bit word (affine int4).
-__device__ __forceinline__ float nibu(uint32_t word, int n) {
-  return static_cast<float>((word >> (4 * n)) & 15u);
-}
-
-// Affine int4: 32 unsigned codes . 32 bf16 activations (sum q * x), and the
-// sum of those activations (for the group bias).
-__device__ __forceinline__ float dot32_u4_bf16(const uint4 wv, const uint4 (&xv)[4], float &xsum) {
-  const uint32_t words[4] = {wv.x, wv.y, wv.z, wv.w};
-  float a = 0.0f, sx = 0.0f;
-#pragma unroll
-  for (int w = 0; w < 4; ++w) {
-    const uint32_t xs[4] = {xv[w].x, xv[w].y, xv[w].z, xv[w].w};
-#pragma unroll
-    for (int m = 0; m < 4; ++m) {
-      a = fmaf(nibu(words[w], 2 * m), bf16_lo(xs[m]), a);
-      a = fmaf(nibu(words[w], 2 * m + 1), bf16_hi(xs[m]), a);
-      sx += bf16_lo(xs[m]) + bf16_hi(xs[m]);
-    }
-  }
-  xsum = sx;
-  return a;
-}
-
-// Same with 32 fp32 activations held in registers (their sum passed in).
-__device__ __forceinline__ float dot32_u4_f32(const uint4 wv, const float (&xs)[32]) {
-  const uint32_t words[4] = {wv.x, wv.y, wv.z, wv.w};
-  float a = 0.0f;
-#pragma unroll
-  for (int w = 0; w < 4; ++w)
-#pragma unroll
-    for (int n = 0; n < 8; ++n) a = fmaf(nibu(words[w], n), xs[8 * w + n], a);
-  return a;
+// 32 codes (one 16-byte chunk; word w holds elements 8 w .. 8 w + 7) . the
+// activation pairs of their four words: sum q * x without the group scale.
+template <bool SIGNED>
+__device__ __forceinline__ float dot32_int4(const uint4 wv, const uint32_t (&h)[4][4]) {
+  uint32_t a0 = 0u, a1 = 0u;
+  a0 = hdot8<SIGNED>(wv.x, h[0], a0);
+  a1 = hdot8<SIGNED>(wv.y, h[1], a1);
+  a0 = hdot8<SIGNED>(wv.z, h[2], a0);
+  a1 = hdot8<SIGNED>(wv.w, h[3], a1);
+  return hsum4(a0, a1);
 }
 
 // Chunking of one weight row for a warp: 16-byte chunks of EPC elements;
@@ -199,18 +195,22 @@ template <int WF> __host__ __device__ __forceinline__ size_t row_bytes(int K) {
   return WF == 0 ? static_cast<size_t>(K) * 2 : static_cast<size_t>(K) / 2;
 }
 
-// Dot products of NR weight rows of length K with the bf16 vector x (global
-// memory), by one warp.  All loads of a segment (weights first, then x) are
-// issued before any arithmetic.
+// Dot products of NR weight rows of length K with the bf16 vector x, by one
+// warp.  x is in shared memory (xs), filled by a bulk copy that completes
+// phase `par` of the mbarrier mb_x: the weight loads of a segment are issued
+// first, then the wait, then the x loads and the arithmetic.  (Every warp
+// reading x from L2 instead moved more bytes into the SMs than the weights
+// themselves for int4 rows.)
 template <int WF, int NR>
 __device__ __forceinline__ void warp_dots_x(const void *const (&rows)[NR],
                                             const __nv_bfloat16 *const (&srows)[NR],
                                             const __nv_bfloat16 *const (&brows)[NR], int K,
-                                            const __nv_bfloat16 *x, float (&out)[NR]) {
+                                            const uint4 *xs, uint32_t mb_x, uint32_t par,
+                                            int *status, float (&out)[NR]) {
   using F = Fmt<WF>;
   const int lane = threadIdx.x & 31;
   const int nchunk = K / F::EPC;
-  const uint4 *xg = reinterpret_cast<const uint4 *>(x);
+  const uint4 *xg = xs;
   float acc[NR];
 #pragma unroll
   for (int r = 0; r < NR; ++r) acc[r] = 0.0f;
@@ -228,29 +228,51 @@ __device__ __forceinline__ void warp_dots_x(const void *const (&rows)[NR],
         if constexpr (WF != 0) sv[r][u] = (c < nchunk) ? __bfloat162float(__ldg(srows[r] + (c >> 1))) : 0.0f;
         if constexpr (WF == 2) bv[r][u] = (c < nchunk) ? __bfloat162float(__ldg(brows[r] + (c >> 1))) : 0.0f;
       }
+    {
+      volatile int no_abort = 0;
+      mbar_wait_bounded(mb_x, par, &no_abort, status, DEV_TIMEOUT_STAGE);
+    }
 #pragma unroll
     for (int u = 0; u < F::U; ++u)
 #pragma unroll
       for (int q = 0; q < F::XPC; ++q) {
         const int c = c0 + lane + 32 * u;
-        xv[u][q] = (c < nchunk) ? __ldg(xg + c * F::XPC + q) : make_uint4(0, 0, 0, 0);
+        xv[u][q] = (c < nchunk) ? xg[c * F::XPC + q] : make_uint4(0, 0, 0, 0);
       }
     // chunks past the row end were loaded as zeros and add nothing: no
     // branches, so the NR * U dot chains interleave
+    if constexpr (WF == 0) {
 #pragma unroll
-    for (int r = 0; r < NR; ++r)
+      for (int r = 0; r < NR; ++r)
+#pragma unroll
+        for (int u = 0; u < F::U; ++u) acc[r] += dot8_bf16_bf16(wv[r][u], xv[u][0]);
+    } else {
+      // the activation pairs (and, affine, the sum) of each chunk, once for
+      // all NR rows
+      uint32_t xh[F::U][4][4];
+      float xs[F::U];
 #pragma unroll
       for (int u = 0; u < F::U; ++u) {
-        if constexpr (WF == 0) {
-          acc[r] += dot8_bf16_bf16(wv[r][u], xv[u][0]);
-        } else if constexpr (WF == 1) {
-          acc[r] = fmaf(sv[r][u], dot32_int4_bf16(wv[r][u], xv[u]), acc[r]);
-        } else {   // scale * (sum q x) + bias * (sum x)
-          float xs;
-          const float qx = dot32_u4_bf16(wv[r][u], xv[u], xs);
-          acc[r] = fmaf(sv[r][u], qx, fmaf(bv[r][u], xs, acc[r]));
+        xs[u] = 0.0f;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          xpairs_bf16(xv[u][q], xh[u][q]);
+          if constexpr (WF == 2)
+            xs[u] += (bf16_lo(xv[u][q].x) + bf16_hi(xv[u][q].x)) +
+                     (bf16_lo(xv[u][q].y) + bf16_hi(xv[u][q].y)) +
+                     (bf16_lo(xv[u][q].z) + bf16_hi(xv[u][q].z)) +
+                     (bf16_lo(xv[u][q].w) + bf16_hi(xv[u][q].w));
         }
       }
+#pragma unroll
+      for (int r = 0; r < NR; ++r)
+#pragma unroll
+        for (int u = 0; u < F::U; ++u) {
+          const float qx = dot32_int4<WF == 1>(wv[r][u], xh[u]);
+          if constexpr (WF == 1) acc[r] = fmaf(sv[r][u], qx, acc[r]);
+          else acc[r] = fmaf(sv[r][u], qx, fmaf(bv[r][u], xs[u], acc[r]));   // s * sum q x + b * sum x
+        }
+    }
   }
 #pragma unroll
   for (int r = 0; r < NR; ++r) out[r] = warp_sum(acc[r]);
@@ -304,16 +326,18 @@ __device__ __forceinline__ void grid_sync(unsigned long long *bar, unsigned long
 
 // ------------------------------------------------- one decode layer --
 // Dynamic shared memory of one CTA, in this order:
+//   x     [H] bf16               the layer's input (one bulk copy per layer)
 //   part  [(k+1) p3_rows] fp32   per-slot dot products of the CTA's output rows
 //   w3    the CTA's output-projection rows (p3_stage only): k slots of p3_rows
 //         rows of I for the routed experts, then one of p3_rows rows of Is
 struct DecSmem {
-  size_t w3, w3_sh, unstaged, staged;
+  size_t part, w3, w3_sh, unstaged, staged;
 };
 template <int WF>
-__host__ __device__ __forceinline__ DecSmem dec_smem(int k, int I, int Is, int rows) {
+__host__ __device__ __forceinline__ DecSmem dec_smem(int k, int I, int Is, int rows, int H) {
   DecSmem L{};
-  L.w3 = (static_cast<size_t>(k + 1) * rows * sizeof(float) + 127) / 128 * 128;
+  L.part = (static_cast<size_t>(H) * 2 + 127) / 128 * 128;   // x (bf16) first
+  L.w3 = L.part + (static_cast<size_t>(k + 1) * rows * sizeof(float) + 127) / 128 * 128;
   L.unstaged = L.w3;
   L.w3_sh = L.w3 + static_cast<size_t>(k) * rows * row_bytes<WF>(I);
   L.staged = L.w3_sh + static_cast<size_t>(rows) * row_bytes<WF>(Is);
@@ -384,6 +408,11 @@ __device__ __forceinline__ void slot_task(const DecodeParams &p, int j, int t0, 
 #pragma unroll
     for (int u = 0; u < CU; ++u) {
       const int c = min(c0 + 32 * u, nch - 1);
+      uint32_t hh[4][4];   // int4: h as the fp16 pairs of the chunk's four code words
+      if constexpr (WF != 0) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) xpairs_f32(&hv[u][8 * q], hh[q]);
+      }
 #pragma unroll
       for (int r = 0; r < 8; ++r) {
         const int rr = min(r, nrows - 1 - t0);
@@ -392,11 +421,11 @@ __device__ __forceinline__ void slot_task(const DecodeParams &p, int j, int t0, 
           acc[r] += dot8_bf16_f32(wv, hv[u]);
         } else if constexpr (WF == 1) {
           const float sc = __bfloat162float(__ldg(srow + rr * ng + (c >> 1)));
-          acc[r] = fmaf(sc, dot32_int4_f32(wv, hv[u]), acc[r]);
+          acc[r] = fmaf(sc, dot32_int4<true>(wv, hh), acc[r]);
         } else {
           const float sc = __bfloat162float(__ldg(srow + rr * ng + (c >> 1)));
           const float bc = __bfloat162float(__ldg(brow + rr * ng + (c >> 1)));
-          acc[r] = fmaf(sc, dot32_u4_f32(wv, hv[u]), fmaf(bc, hs[u], acc[r]));
+          acc[r] = fmaf(sc, dot32_int4<false>(wv, hh), fmaf(bc, hs[u], acc[r]));
         }
       }
     }
@@ -425,16 +454,18 @@ __device__ __forceinline__ void run_slot_task(const DecodeParams &p, int j, int 
 struct DecCta {
   float *part;
   unsigned char *w3, *w3_sh;
+  const uint4 *x_s;   // the layer input in shared memory
   int n0, n1, nrows, ngroups;
-  uint32_t mb_sh, mb_rt;
+  uint32_t mb_sh, mb_rt, mb_x;
 };
 
 template <int WF>
 __device__ __forceinline__ DecCta make_dec_cta(const DecodeParams &p, unsigned char *dsm,
                                                uint64_t *mbar) {
-  const DecSmem S = dec_smem<WF>(p.k, p.I, p.Is, p.p3_rows);
+  const DecSmem S = dec_smem<WF>(p.k, p.I, p.Is, p.p3_rows, p.H);
   DecCta c;
-  c.part = reinterpret_cast<float *>(dsm);
+  c.x_s = reinterpret_cast<const uint4 *>(dsm);
+  c.part = reinterpret_cast<float *>(dsm + S.part);
   c.w3 = dsm + S.w3;
   c.w3_sh = dsm + S.w3_sh;
   c.n0 = static_cast<int>((static_cast<long long>(blockIdx.x) * p.H) / gridDim.x);
@@ -443,6 +474,7 @@ __device__ __forceinline__ DecCta make_dec_cta(const DecodeParams &p, unsigned c
   c.ngroups = (c.nrows + 7) / 8;
   c.mb_sh = smem_u32(&mbar[0]);
   c.mb_rt = smem_u32(&mbar[1]);
+  c.mb_x = smem_u32(&mbar[2]);
   return c;
 }
 
@@ -482,7 +514,7 @@ __device__ __forceinline__ void decode_layer(const DecodeParams &p, const DecCta
   unsigned char *w3 = c.w3;
   unsigned char *w3_sh = c.w3_sh;
   const int n0 = c.n0, n1 = c.n1, nrows = c.nrows, ngroups = c.ngroups;
-  const uint32_t mb_sh = c.mb_sh, mb_rt = c.mb_rt;
+  const uint32_t mb_sh = c.mb_sh, mb_rt = c.mb_rt, mb_x = c.mb_x;
   const __nv_bfloat16 *x = reinterpret_cast<const __nv_bfloat16 *>(p.x);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = gridDim.x;
@@ -495,13 +527,23 @@ __device__ __forceinline__ void decode_layer(const DecodeParams &p, const DecCta
   const int nA = p.E + 1 + p.Is;   // phase-A items: router rows, the gate row, shared pairs
   (void)n1;
   (void)lane;
+  (void)x;
+  if (threadIdx.x == 0) {
+    // the layer input into shared memory (x was written by generic stores of
+    // the previous kernel or layer, acquired before this point)
+    const uint32_t xbytes = static_cast<uint32_t>(p.H) * 2;
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    fence_proxy_async_smem();   // the previous layer's reads of x_s come first
+    mbar_arrive_expect_tx(mb_x, xbytes);
+    bulk_copy_g2s(smem_u32(c.x_s), p.x, xbytes, mb_x);
+  }
   // ---- phase A: router rows, the shared gate row, shared-expert row pairs
   for (int it = gw; it < nA; it += nw) {
     if (it <= p.E) {
       const void *rows[1] = {it < p.E ? row_ptr<0>(p.router_w, it, p.H) : p.sh_gate_w};
       const __nv_bfloat16 *sr[1] = {nullptr};
       float d[1];
-      warp_dots_x<0, 1>(rows, sr, sr, p.H, x, d);
+      warp_dots_x<0, 1>(rows, sr, sr, p.H, c.x_s, c.mb_x, par, p.status, d);
       if (lane == 0) {
         if (it < p.E) p.logits[it] = d[0] + (p.router_b ? p.router_b[it] : 0.0f);
         else *p.g = sigmoid_f(d[0]);
@@ -515,7 +557,7 @@ __device__ __forceinline__ void decode_layer(const DecodeParams &p, const DecCta
       const __nv_bfloat16 *br[2] = {scale_row(p.sh_gate_up_bias, i, p.H),
                                     scale_row(p.sh_gate_up_bias, p.Is + i, p.H)};
       float d[2];
-      warp_dots_x<WF, 2>(rows, sr, br, p.H, x, d);
+      warp_dots_x<WF, 2>(rows, sr, br, p.H, c.x_s, c.mb_x, par, p.status, d);
       if (lane == 0) hg[static_cast<size_t>(p.k) * p.h_ld + i] = silu_f(d[0]) * d[1];
     }
   }
@@ -589,7 +631,7 @@ __device__ __forceinline__ void decode_layer(const DecodeParams &p, const DecCta
     const __nv_bfloat16 *br[2] = {scale_row(p.gate_up_bias, rg, p.H),
                                   scale_row(p.gate_up_bias, rg + p.I, p.H)};
     float d[2];
-    warp_dots_x<WF, 2>(rows, sr, br, p.H, x, d);
+    warp_dots_x<WF, 2>(rows, sr, br, p.H, c.x_s, c.mb_x, par, p.status, d);
     if (lane == 0) hg[static_cast<size_t>(j) * p.h_ld + i] = silu_f(d[0]) * d[1];
   }
   // The shared expert's slot needs only h_s (complete since the first
@@ -652,7 +694,7 @@ __device__ __forceinline__ void decode_layer(const DecodeParams &p, const DecCta
 template <int WF, int R>
 __global__ void __launch_bounds__(kDecLayerThreads, 1) decode_layer_kernel(const DecodeParams p) {
   extern __shared__ __align__(128) unsigned char dsm[];
-  __shared__ __align__(8) uint64_t mbar[2];   // [0] shared expert rows, [1] routed rows
+  __shared__ __align__(8) uint64_t mbar[3];   // shared expert rows, routed rows, x
   __shared__ int idx_s[32];
   __shared__ float w_s[33];                   // routing weights, then the shared gate
   const DecCta c = make_dec_cta<WF>(p, dsm, mbar);
@@ -673,9 +715,11 @@ __global__ void __launch_bounds__(kDecLayerThreads, 1) decode_layer_kernel(const
     if (p.p3_stage) {
       mbar_init(c.mb_sh, 1);
       mbar_init(c.mb_rt, 1);
-      fence_mbarrier_init();
     }
+    mbar_init(c.mb_x, 1);
+    fence_mbarrier_init();
   }
+  __syncthreads();   // the barriers exist before any thread waits on mb_x
   // Only weights are read before the wait below: x, and every buffer this
   // kernel writes, may still be in use by the previous layer.
   layer_prefetch<WF>(p, c, gw);
@@ -703,7 +747,7 @@ template <int WF, int R>
 __global__ void __launch_bounds__(kDecLayerThreads, 1)
     decode_layers_kernel(const __grid_constant__ DecodeLayersParams P) {
   extern __shared__ __align__(128) unsigned char dsm[];
-  __shared__ __align__(8) uint64_t mbar[2];
+  __shared__ __align__(8) uint64_t mbar[3];
   __shared__ int idx_s[32];
   __shared__ float w_s[33];
   const DecodeParams &p0 = P.layer[0];
@@ -717,9 +761,11 @@ __global__ void __launch_bounds__(kDecLayerThreads, 1)
     if (p0.p3_stage) {
       mbar_init(c.mb_sh, 1);
       mbar_init(c.mb_rt, 1);
-      fence_mbarrier_init();
     }
+    mbar_init(c.mb_x, 1);
+    fence_mbarrier_init();
   }
+  __syncthreads();   // the barriers exist before any thread waits on mb_x
   layer_prefetch<WF>(p0, c, gw);
   pdl_trigger();
   pdl_wait();
@@ -736,7 +782,7 @@ __global__ void __launch_bounds__(kDecLayerThreads, 1)
 template <int WF>
 static void set_p3(DecodeParams &p, int grid, int smem_limit, size_t *smem) {
   p.p3_rows = (p.H + grid - 1) / grid;
-  const DecSmem S = dec_smem<WF>(p.k, p.I, p.Is, p.p3_rows);
+  const DecSmem S = dec_smem<WF>(p.k, p.I, p.Is, p.p3_rows, p.H);
   p.p3_stage = S.staged <= static_cast<size_t>(smem_limit) ? 1 : 0;
   *smem = p.p3_stage ? S.staged : S.unstaged;
 }
