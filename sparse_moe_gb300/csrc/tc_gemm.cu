@@ -36,9 +36,12 @@
 //    conversion (router, bf16 gate/up) both CTAs' TMA boxes complete on the
 //    leader's full barrier (cta_group::2 loads) and the peer's token-row
 //    warps arrive on it remotely, so readiness needs no relay; when the
-//    weight tile must be converted first (down, int4), a finisher warp per
-//    stage and CTA converts it and forwards readiness to the leader, the
-//    peer's with a cluster-scope release-arrive;
+//    weight tile must be converted first, converting warps arrive on the
+//    leader's ready barrier: for bf16 -> fp16 (down without fp16 copies) a
+//    team per stage, each member with a cluster-scope arrival from the peer;
+//    for int4 four converter warps per k-step, whose codes come through
+//    their own ring, and in the peer one relay thread forwards a single
+//    cluster-scope arrival per k-step once its four converters are done;
 //    four epilogue warps
 //    per CTA drain their half of the double-buffered TMEM accumulator while
 //    the next tile computes, and transpose each 32x16 piece through shared
