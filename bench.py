@@ -401,12 +401,54 @@ def bench_sweep(args, dev, stream, flush, tf_burst, hbm):
             for T in moe_synth.SWEEP_T]
 
 
+def _rows_point(T, dev, stream, flush, hbm, steps):
+    """moe_forward_rows on the sweep workload's first T rows: layer time and
+    the HBM fraction over the weights it must read (router, shared expert and
+    the union of the selected experts, each once)."""
+    from sparse_moe_gb300 import MoEContext
+    wl = moe_synth.sweep_workload(T)
+    s = wl.shape
+    ctx = MoEContext(s.hidden, s.n_experts, s.top_k, s.inter, s.shared_inter, n_layers=1,
+                     max_chunk_rows=16, device=dev.index)
+    w = moe_synth.make_layer(wl, device=dev)
+    ctx.load_weights(0, w)
+    x = moe_synth.make_x(wl, device=dev)
+    y = torch.empty_like(x)
+    ctx.forward_rows(0, x, y, stream=stream)
+    torch.cuda.synchronize()
+    union = int(torch.unique(ctx.rows_routing(T)["topk_idx"]).numel())
+    for _ in range(3):
+        ctx.forward_rows(0, x, y, stream=stream)
+    torch.cuda.synchronize()
+    a = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    b = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    with torch.cuda.stream(stream):
+        for i in range(steps):
+            flush.zero_()
+            a[i].record(stream)
+            ctx.forward_rows(0, x, y, stream=stream)
+            b[i].record(stream)
+    torch.cuda.synchronize()
+    ms = float(np.mean([e0.elapsed_time(e1) for e0, e1 in zip(a, b)]))
+    wbytes = (union + 1) * 3 * s.inter * s.hidden * 2 + s.n_experts * s.hidden * 2 + s.hidden * 2
+    ctx.close()
+    del w, x, y
+    torch.cuda.empty_cache()
+    return {"rows_ms": ms, "rows_hbm_frac": wbytes / (ms * 1e-3) / 1e9 / hbm, "union_experts": union,
+            "rows_gpu_launches": 1}
+
+
 def bench_small_m(args, dev, stream, flush, tf_burst, hbm):
     """Small row counts (2 - 16 rows, the page's speculative-verification
-    shapes) through the prefill path, whose grouped GEMMs run each expert's
-    block at MMA N = 32: each point reads the weights of every expert it
-    touches once, so the HBM fraction over those weights is the figure."""
-    return [_sweep_point(T, dev, stream, flush, tf_burst, hbm, 20) for T in (2, 4, 8, 16)]
+    shapes): the prefill path (grouped GEMMs at MMA N = 32) and the
+    decode-style rows path (moe_forward_rows), each against the HBM time of
+    the weights the rows need."""
+    out = []
+    for T in (2, 4, 8, 16):
+        pt = _sweep_point(T, dev, stream, flush, tf_burst, hbm, 20)
+        pt.update(_rows_point(T, dev, stream, flush, hbm, 20))
+        out.append(pt)
+    return out
 
 
 def bench_decode(args, dev, stream, hbm, int4=None, wl=None):

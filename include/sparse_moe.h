@@ -213,6 +213,28 @@ moe_status moe_forward_decode_layers(moe_ctx *ctx, int first_layer, int n_layers
 moe_status moe_decode_routing(moe_ctx *ctx, float *logits, int32_t *idx, float *w,
                               void *stream);
 
+/* A few rows through the decode-style path: y[T, H] = MoE(x[T, H]) for
+ * 1 <= T <= 16 (and T <= the context's max_chunk_rows), device bf16, 16-byte
+ * aligned, in one cooperative launch of the decode grid.  Section "Limits of
+ * further optimization": verifying drafted tokens processes groups of two to
+ * five rows that often select different experts, so the weights read grow
+ * with the union of the rows' experts.  Here every weight row in that union
+ * (and of the router and the shared expert) is read from HBM once for all
+ * the rows that need it; the prefill path would instead run its routing and
+ * grouped GEMMs for a handful of rows.  Same arithmetic and tolerances as
+ * moe_forward_decode (rows are independent: row t's result does not depend
+ * on the other rows).  Uses the workspace's prefill regions: do not overlap
+ * with a prefill call on the same context.  Errors: MOE_ERR_INVALID_ARG for
+ * T out of range or misaligned buffers. */
+moe_status moe_forward_rows(moe_ctx *ctx, int layer, const void *x, int T, void *y,
+                            void *stream);
+
+/* Routing of the most recent moe_forward_rows (T rows) on this context,
+ * copied asynchronously on `stream` to device buffers: logits fp32 [T, E],
+ * idx int32 [T, k], w fp32 [T, k] (any may be NULL).  Valid until the next
+ * prefill or rows call; MOE_ERR_INVALID_ARG before the first rows call. */
+moe_status moe_rows_routing(moe_ctx *ctx, float *logits, int32_t *idx, float *w, void *stream);
+
 /* End-to-end prefill from HOST memory: copies x_host [T, H] bf16 to the
  * device chunk by chunk, runs the prefill path and copies y back into y_host
  * [T, H].  Pinned host buffers make the copies asynchronous; the call returns

@@ -207,6 +207,29 @@ class MoEContext:
         self._check(st, "moe_forward_decode_layers")
         return y
 
+    def forward_rows(self, layer: int, x: torch.Tensor, y: Optional[torch.Tensor] = None,
+                     stream=None) -> torch.Tensor:
+        """y[T, H] for x[T, H] (device bf16, 1 <= T <= 16) through the
+        decode-style path that reads each needed weight row once for all T
+        rows (moe_forward_rows)."""
+        if y is None:
+            y = torch.empty_like(x)
+        st = self.lib.moe_forward_rows(self.handle, layer, _ptr(x), x.shape[0], _ptr(y),
+                                       _stream_handle(stream, self.device))
+        self._check(st, "moe_forward_rows")
+        return y
+
+    def rows_routing(self, T: int, stream=None) -> dict:
+        """Routing of the last forward_rows call (T rows)."""
+        dev = self.device
+        out = dict(logits=torch.empty((T, self.n_experts), dtype=torch.float32, device=dev),
+                   topk_idx=torch.empty((T, self.top_k), dtype=torch.int32, device=dev),
+                   topk_w=torch.empty((T, self.top_k), dtype=torch.float32, device=dev))
+        st = self.lib.moe_rows_routing(self.handle, _ptr(out["logits"]), _ptr(out["topk_idx"]),
+                                       _ptr(out["topk_w"]), _stream_handle(stream, dev))
+        self._check(st, "moe_rows_routing")
+        return out
+
     def decode_routing(self, stream=None) -> dict:
         dev = self.device
         out = dict(logits=torch.empty((self.n_experts,), dtype=torch.float32, device=dev),

@@ -55,6 +55,8 @@ SIGNATURES = {
     "moe_forward_decode_layers": (i32, [vp, i32, i32, vp, ctypes.c_size_t, vp, ctypes.c_size_t,
                                         vp]),
     "moe_decode_routing": (i32, [vp, vp, vp, vp, vp]),
+    "moe_forward_rows": (i32, [vp, i32, vp, i32, vp, vp]),
+    "moe_rows_routing": (i32, [vp, vp, vp, vp, vp]),
     "moe_forward_prefill_host": (i32, [vp, i32, vp, i32, vp, vp]),
     "moe_forward_decode_host": (i32, [vp, i32, vp, vp, vp]),
     "moe_forward_decode_noalloc": (i32, [ctypes.POINTER(MoeConfig), ctypes.POINTER(MoeWeights), vp,

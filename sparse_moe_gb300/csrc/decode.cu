@@ -195,13 +195,93 @@ template <int WF> __host__ __device__ __forceinline__ size_t row_bytes(int K) {
   return WF == 0 ? static_cast<size_t>(K) * 2 : static_cast<size_t>(K) / 2;
 }
 
+// One segment of a warp's dot products: lane l takes 16-byte chunks
+// c0 + l + 32 u (u < U) of NR weight rows (seg_load_w) and the matching
+// chunks of x (seg_load_x, from shared memory); seg_dots adds the chunks'
+// dot products to acc.  Chunks past the row end load as zeros and add
+// nothing: no branches, so the NR * U dot chains interleave.
+template <int WF, int NR, bool L1>
+__device__ __forceinline__ void seg_load_w(const void *const (&rows)[NR],
+                                           const __nv_bfloat16 *const (&srows)[NR],
+                                           const __nv_bfloat16 *const (&brows)[NR], int nchunk,
+                                           int c0, int lane, uint4 (&wv)[NR][Fmt<WF>::U],
+                                           float (&sv)[NR][Fmt<WF>::U],
+                                           float (&bv)[NR][Fmt<WF>::U]) {
+  using F = Fmt<WF>;
+#pragma unroll
+  for (int r = 0; r < NR; ++r)
+#pragma unroll
+    for (int u = 0; u < F::U; ++u) {
+      const int c = c0 + lane + 32 * u;
+      const uint4 *wp = reinterpret_cast<const uint4 *>(rows[r]) + c;
+      wv[r][u] = (c < nchunk) ? (L1 ? __ldg(wp) : ld_stream(wp)) : make_uint4(0, 0, 0, 0);
+      if constexpr (WF != 0) sv[r][u] = (c < nchunk) ? __bfloat162float(__ldg(srows[r] + (c >> 1))) : 0.0f;
+      if constexpr (WF == 2) bv[r][u] = (c < nchunk) ? __bfloat162float(__ldg(brows[r] + (c >> 1))) : 0.0f;
+    }
+}
+
+template <int WF>
+__device__ __forceinline__ void seg_load_x(const uint4 *xs, int nchunk, int c0, int lane,
+                                           uint4 (&xv)[Fmt<WF>::U][Fmt<WF>::XPC]) {
+  using F = Fmt<WF>;
+#pragma unroll
+  for (int u = 0; u < F::U; ++u)
+#pragma unroll
+    for (int q = 0; q < F::XPC; ++q) {
+      const int c = c0 + lane + 32 * u;
+      xv[u][q] = (c < nchunk) ? xs[c * F::XPC + q] : make_uint4(0, 0, 0, 0);
+    }
+}
+
+template <int WF, int NR>
+__device__ __forceinline__ void seg_dots(const uint4 (&wv)[NR][Fmt<WF>::U],
+                                         const float (&sv)[NR][Fmt<WF>::U],
+                                         const float (&bv)[NR][Fmt<WF>::U],
+                                         const uint4 (&xv)[Fmt<WF>::U][Fmt<WF>::XPC],
+                                         float (&acc)[NR]) {
+  using F = Fmt<WF>;
+  if constexpr (WF == 0) {
+#pragma unroll
+    for (int r = 0; r < NR; ++r)
+#pragma unroll
+      for (int u = 0; u < F::U; ++u) acc[r] += dot8_bf16_bf16(wv[r][u], xv[u][0]);
+  } else {
+    // the activation pairs (and, affine, the sum) of each chunk, once for
+    // all NR rows
+    uint32_t xh[F::U][4][4];
+    float xs[F::U];
+#pragma unroll
+    for (int u = 0; u < F::U; ++u) {
+      xs[u] = 0.0f;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        xpairs_bf16(xv[u][q], xh[u][q]);
+        if constexpr (WF == 2)
+          xs[u] += (bf16_lo(xv[u][q].x) + bf16_hi(xv[u][q].x)) +
+                   (bf16_lo(xv[u][q].y) + bf16_hi(xv[u][q].y)) +
+                   (bf16_lo(xv[u][q].z) + bf16_hi(xv[u][q].z)) +
+                   (bf16_lo(xv[u][q].w) + bf16_hi(xv[u][q].w));
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < NR; ++r)
+#pragma unroll
+      for (int u = 0; u < F::U; ++u) {
+        const float qx = dot32_int4<WF == 1>(wv[r][u], xh[u]);
+        if constexpr (WF == 1) acc[r] = fmaf(sv[r][u], qx, acc[r]);
+        else acc[r] = fmaf(sv[r][u], qx, fmaf(bv[r][u], xs[u], acc[r]));   // s * sum q x + b * sum x
+      }
+  }
+}
+
 // Dot products of NR weight rows of length K with the bf16 vector x, by one
 // warp.  x is in shared memory (xs), filled by a bulk copy that completes
 // phase `par` of the mbarrier mb_x: the weight loads of a segment are issued
 // first, then the wait, then the x loads and the arithmetic.  (Every warp
 // reading x from L2 instead moved more bytes into the SMs than the weights
-// themselves for int4 rows.)
-template <int WF, int NR>
+// themselves for int4 rows.)  L1: weights through L1, for rows that the
+// caller reads again soon.
+template <int WF, int NR, bool L1 = false>
 __device__ __forceinline__ void warp_dots_x(const void *const (&rows)[NR],
                                             const __nv_bfloat16 *const (&srows)[NR],
                                             const __nv_bfloat16 *const (&brows)[NR], int K,
@@ -210,7 +290,6 @@ __device__ __forceinline__ void warp_dots_x(const void *const (&rows)[NR],
   using F = Fmt<WF>;
   const int lane = threadIdx.x & 31;
   const int nchunk = K / F::EPC;
-  const uint4 *xg = xs;
   float acc[NR];
 #pragma unroll
   for (int r = 0; r < NR; ++r) acc[r] = 0.0f;
@@ -218,64 +297,35 @@ __device__ __forceinline__ void warp_dots_x(const void *const (&rows)[NR],
     uint4 wv[NR][F::U];
     uint4 xv[F::U][F::XPC];
     float sv[NR][F::U], bv[NR][F::U];
-#pragma unroll
-    for (int r = 0; r < NR; ++r)
-#pragma unroll
-      for (int u = 0; u < F::U; ++u) {
-        const int c = c0 + lane + 32 * u;
-        wv[r][u] = (c < nchunk) ? ld_stream(reinterpret_cast<const uint4 *>(rows[r]) + c)
-                                : make_uint4(0, 0, 0, 0);
-        if constexpr (WF != 0) sv[r][u] = (c < nchunk) ? __bfloat162float(__ldg(srows[r] + (c >> 1))) : 0.0f;
-        if constexpr (WF == 2) bv[r][u] = (c < nchunk) ? __bfloat162float(__ldg(brows[r] + (c >> 1))) : 0.0f;
-      }
+    seg_load_w<WF, NR, L1>(rows, srows, brows, nchunk, c0, lane, wv, sv, bv);
     {
       volatile int no_abort = 0;
       mbar_wait_bounded(mb_x, par, &no_abort, status, DEV_TIMEOUT_STAGE);
     }
-#pragma unroll
-    for (int u = 0; u < F::U; ++u)
-#pragma unroll
-      for (int q = 0; q < F::XPC; ++q) {
-        const int c = c0 + lane + 32 * u;
-        xv[u][q] = (c < nchunk) ? xg[c * F::XPC + q] : make_uint4(0, 0, 0, 0);
-      }
-    // chunks past the row end were loaded as zeros and add nothing: no
-    // branches, so the NR * U dot chains interleave
-    if constexpr (WF == 0) {
-#pragma unroll
-      for (int r = 0; r < NR; ++r)
-#pragma unroll
-        for (int u = 0; u < F::U; ++u) acc[r] += dot8_bf16_bf16(wv[r][u], xv[u][0]);
-    } else {
-      // the activation pairs (and, affine, the sum) of each chunk, once for
-      // all NR rows
-      uint32_t xh[F::U][4][4];
-      float xs[F::U];
-#pragma unroll
-      for (int u = 0; u < F::U; ++u) {
-        xs[u] = 0.0f;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          xpairs_bf16(xv[u][q], xh[u][q]);
-          if constexpr (WF == 2)
-            xs[u] += (bf16_lo(xv[u][q].x) + bf16_hi(xv[u][q].x)) +
-                     (bf16_lo(xv[u][q].y) + bf16_hi(xv[u][q].y)) +
-                     (bf16_lo(xv[u][q].z) + bf16_hi(xv[u][q].z)) +
-                     (bf16_lo(xv[u][q].w) + bf16_hi(xv[u][q].w));
-        }
-      }
-#pragma unroll
-      for (int r = 0; r < NR; ++r)
-#pragma unroll
-        for (int u = 0; u < F::U; ++u) {
-          const float qx = dot32_int4<WF == 1>(wv[r][u], xh[u]);
-          if constexpr (WF == 1) acc[r] = fmaf(sv[r][u], qx, acc[r]);
-          else acc[r] = fmaf(sv[r][u], qx, fmaf(bv[r][u], xs[u], acc[r]));   // s * sum q x + b * sum x
-        }
-    }
+    seg_load_x<WF>(xs, nchunk, c0, lane, xv);
+    seg_dots<WF, NR>(wv, sv, bv, xv, acc);
   }
 #pragma unroll
   for (int r = 0; r < NR; ++r) out[r] = warp_sum(acc[r]);
+}
+
+// The same for several activation rows: row t (bit t of `users`) is at
+// xs + t * xq, and out(t, d) receives its NR sums (in every lane).  One
+// warp_dots_x per user, the weights through L1, so that a row comes from HBM
+// once.  (Keeping the weights in registers across the users instead measured
+// slower: the kernel then spills.)
+template <int WF, int NR, class Out>
+__device__ __forceinline__ void warp_dots_users(const void *const (&rows)[NR],
+                                                const __nv_bfloat16 *const (&srows)[NR],
+                                                const __nv_bfloat16 *const (&brows)[NR], int K,
+                                                const uint4 *xs, int xq, unsigned int users,
+                                                uint32_t mb_x, int *status, Out out) {
+  for (unsigned int m = users; m != 0u; m &= m - 1u) {
+    const int t = __ffs(m) - 1;
+    float d[NR];
+    warp_dots_x<WF, NR, true>(rows, srows, brows, K, xs + t * xq, mb_x, 0u, status, d);
+    out(t, d);
+  }
 }
 
 // Row r of a K-major matrix with K columns, bf16 or packed int4.
@@ -346,20 +396,20 @@ __host__ __device__ __forceinline__ DecSmem dec_smem(int k, int I, int Is, int r
 
 // One phase-C task: part[j][t0 + r] = (output-projection row n0 + t0 + r of
 // slot j) . h_j for r < 8, slot j < k a routed expert and j = k the shared
-// one.  The rows come from shared memory (STAGED) or global memory; h_j comes
+// one; h_j = hbase + j h_ld.  The rows come from shared memory (STAGED) or global memory; h_j comes
 // from global memory (L2).  Lane l takes 16-byte chunks l + 32 m and keeps
 // the matching h elements in registers across the eight rows.
 template <int WF, bool STAGED>
-__device__ __forceinline__ void slot_task(const DecodeParams &p, int j, int t0, int n0, int nrows,
-                                          int expert, float *part, const unsigned char *w3,
-                                          const unsigned char *w3_sh) {
+__device__ __forceinline__ void slot_task(const DecodeParams &p, const float *hbase, int j, int t0,
+                                          int n0, int nrows, int expert, float *part,
+                                          const unsigned char *w3, const unsigned char *w3_sh) {
   using F = Fmt<WF>;
   const int lane = threadIdx.x & 31;
   const bool sh = (j == p.k);
   const int K = sh ? p.Is : p.I;
   const int nch = K / F::EPC, ng = K / 64;
   const size_t rb = row_bytes<WF>(K);
-  const float *hj = p.h + static_cast<size_t>(j) * p.h_ld;
+  const float *hj = hbase + static_cast<size_t>(j) * p.h_ld;
   const size_t r0 = (sh ? 0 : static_cast<size_t>(expert) * p.H) + n0 + t0;   // global row
   const unsigned char *wrow;   // row t0 of the group
   if constexpr (STAGED)
@@ -439,13 +489,29 @@ __device__ __forceinline__ void slot_task(const DecodeParams &p, int j, int t0, 
   }
 }
 
+// slot_task for several activation rows: users (bit t) of one output
+// projection (the shared one if sh), row t's h at h0 + t * hrow + j(t) h_ld
+// and its parts at part0 + t * pstride; one slot_task per user, whose weight
+// rows come from L1 after the first.
+template <int WF, class SlotOf>
+__device__ __forceinline__ void slot_task_users(const DecodeParams &p, const float *h0, size_t hrow,
+                                                unsigned int users, SlotOf slot_of_t, int t0,
+                                                int n0, int nrows, int expert, float *part0,
+                                                size_t pstride) {
+  for (unsigned int m = users; m != 0u; m &= m - 1u) {
+    const int t = __ffs(m) - 1;
+    slot_task<WF, false>(p, h0 + t * hrow, slot_of_t(t), t0, n0, nrows, expert, part0 + t * pstride,
+                         nullptr, nullptr);
+  }
+}
+
 template <int WF>
 __device__ __forceinline__ void run_slot_task(const DecodeParams &p, int j, int t0, int n0,
                                               int nrows, int expert, float *part,
                                               const unsigned char *w3,
                                               const unsigned char *w3_sh) {
-  if (p.p3_stage) slot_task<WF, true>(p, j, t0, n0, nrows, expert, part, w3, w3_sh);
-  else slot_task<WF, false>(p, j, t0, n0, nrows, expert, part, w3, w3_sh);
+  if (p.p3_stage) slot_task<WF, true>(p, p.h, j, t0, n0, nrows, expert, part, w3, w3_sh);
+  else slot_task<WF, false>(p, p.h, j, t0, n0, nrows, expert, part, w3, w3_sh);
 }
 
 // Per-CTA state shared by every layer of a launch: the shared-memory carve-up
@@ -779,6 +845,221 @@ __global__ void __launch_bounds__(kDecLayerThreads, 1)
   }
 }
 
+// ------------------------------------------------------------ a few rows --
+// T = 1 .. kSmallMaxRows rows of one layer ("Limits of further optimization":
+// verifying drafted tokens processes groups of two to five rows, which often
+// select different experts).  The decode layer's structure, with every weight
+// row streamed once for all the rows that use it:
+//   A. router rows, the shared gate row and the shared expert's row pairs,
+//      each dotted with all T inputs (x [T, H] staged in shared memory);
+//   B. per-row top-k (warp t of every CTA for row t), the union of the
+//      selected experts in ascending expert order, then items (u, i): the
+//      gate/up row pair i of union expert u with every row that selected u;
+//   C. each CTA's output rows n0..n1 of every union expert and of the shared
+//      expert (tasks of 8 rows) with the h of each user row, then
+//      y[t][n] = sum_j w[t][j] part[t][j][n] + g[t] part[t][k][n] in fixed j
+//      order.
+// A row read for several users comes from HBM once and from L1 after that.
+// Phase C reads its rows from global memory (no staging: the union holds up
+// to T k experts).
+//
+// Dynamic shared memory: x [T][H] bf16, then part [T][k + 1][p3_rows] fp32.
+struct RowsSmem {
+  size_t part, total;
+};
+__host__ __device__ __forceinline__ RowsSmem rows_smem(int T, int k, int H, int rows) {
+  RowsSmem L{};
+  L.part = (static_cast<size_t>(T) * H * 2 + 127) / 128 * 128;
+  L.total = L.part + static_cast<size_t>(T) * (k + 1) * rows * sizeof(float);
+  return L;
+}
+constexpr int kRowsMaxUnion = kSmallMaxRows * 32;   // T k with k <= 32
+
+template <int WF, int R>
+__global__ void __launch_bounds__(kDecLayerThreads, 1) rows_kernel(const DecodeParams p) {
+  extern __shared__ __align__(128) unsigned char dsm[];
+  __shared__ __align__(8) uint64_t mb_x_store;
+  __shared__ int idx_s[kSmallMaxRows * 32];
+  __shared__ float w_s[kSmallMaxRows * 32];
+  __shared__ float g_s[kSmallMaxRows];
+  __shared__ short umap[1024];                      // expert -> union index
+  __shared__ short ue[kRowsMaxUnion];               // union index -> expert
+  __shared__ unsigned int users[kRowsMaxUnion];     // bit t: row t selected the expert
+  __shared__ signed char slot_of[kRowsMaxUnion][kSmallMaxRows];
+  __shared__ int n_union;
+  const int T = p.T, H = p.H, E = p.E, k = p.k;
+  const RowsSmem S = rows_smem(T, k, H, p.p3_rows);
+  const uint4 *x_s = reinterpret_cast<const uint4 *>(dsm);
+  float *part = reinterpret_cast<float *>(dsm + S.part);
+  const uint32_t mb_x = smem_u32(&mb_x_store);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = gridDim.x;
+  const int gw = warp * G + blockIdx.x;
+  const int nw = G * kDecWarps;
+  const int n0 = static_cast<int>((static_cast<long long>(blockIdx.x) * H) / G);
+  const int n1 = static_cast<int>((static_cast<long long>(blockIdx.x + 1) * H) / G);
+  const int nrows = n1 - n0, ngroups = (nrows + 7) / 8;
+  const size_t hrow = static_cast<size_t>(k + 1) * p.h_ld;   // h floats per row t
+  const uint32_t all_rows = T >= 32 ? 0xffffffffu : (1u << T) - 1u;
+
+  unsigned long long base = 0;
+  if (threadIdx.x == 0) {
+    const unsigned long long v = ld_acquire_u64(p.bar);
+    base = v - v % static_cast<unsigned long long>(G);
+    mbar_init(mb_x, 1);
+    fence_mbarrier_init();
+  }
+  __syncthreads();
+  // only weights before the wait: x and the scratch may still be in use
+  layer_prefetch<WF>(p, DecCta{}, gw);
+  pdl_trigger();
+  pdl_wait();
+  if (threadIdx.x == 0) {
+    const uint32_t xbytes = static_cast<uint32_t>(T) * H * 2;
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    mbar_arrive_expect_tx(mb_x, xbytes);
+    bulk_copy_g2s(smem_u32(x_s), p.x, xbytes, mb_x);
+  }
+  const int xq = H / 8;   // uint4 per x row
+
+  // ---- A: router rows, the gate row, shared pairs; all T rows
+  const int nA = E + 1 + p.Is;
+  for (int it = gw; it < nA; it += nw) {
+    if (it <= E) {
+      const void *rows[1] = {it < E ? row_ptr<0>(p.router_w, it, H) : p.sh_gate_w};
+      const __nv_bfloat16 *sr[1] = {nullptr};
+      warp_dots_users<0, 1>(rows, sr, sr, H, x_s, xq, all_rows, mb_x, p.status,
+                            [&](int t, const float (&d)[1]) {
+                              if (lane == 0) {
+                                if (it < E)
+                                  p.logits[static_cast<size_t>(t) * E + it] =
+                                      d[0] + (p.router_b ? p.router_b[it] : 0.0f);
+                                else
+                                  p.g[t] = sigmoid_f(d[0]);
+                              }
+                            });
+    } else {
+      const int i = it - E - 1;
+      const void *rows[2] = {row_ptr<WF>(p.sh_gate_up, i, H), row_ptr<WF>(p.sh_gate_up, p.Is + i, H)};
+      const __nv_bfloat16 *sr[2] = {scale_row(p.sh_gate_up_scale, i, H),
+                                    scale_row(p.sh_gate_up_scale, p.Is + i, H)};
+      const __nv_bfloat16 *br[2] = {scale_row(p.sh_gate_up_bias, i, H),
+                                    scale_row(p.sh_gate_up_bias, p.Is + i, H)};
+      warp_dots_users<WF, 2>(rows, sr, br, H, x_s, xq, all_rows, mb_x, p.status,
+                             [&](int t, const float (&d)[2]) {
+                               if (lane == 0)
+                                 p.h[t * hrow + static_cast<size_t>(k) * p.h_ld + i] = silu_f(d[0]) * d[1];
+                             });
+    }
+  }
+  grid_sync(p.bar, base + G, p.status);
+
+  // ---- top-k per row (warps 0..T-1 of every CTA), then the union
+  if (warp < T) {
+    float v[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      const int e = lane + 32 * r;
+      v[r] = (e < E) ? __ldcg(p.logits + static_cast<size_t>(warp) * E + e) : 0.0f;
+    }
+    int sel_e;
+    float sel_w;
+    warp_topk_redux<R>(v, E, k, sel_e, sel_w);
+    sel_e = min(max(sel_e, 0), E - 1);
+    if (lane < k) {
+      idx_s[warp * 32 + lane] = sel_e;
+      w_s[warp * 32 + lane] = sel_w;
+      if (blockIdx.x == 0) {
+        p.idx[warp * k + lane] = sel_e;
+        p.w[warp * k + lane] = sel_w;
+      }
+    }
+    if (lane == 0) g_s[warp] = __ldcg(p.g + warp);
+  }
+  for (int e = threadIdx.x; e < E; e += kDecLayerThreads) umap[e] = 0;
+  __syncthreads();
+  for (int q = threadIdx.x; q < T * k; q += kDecLayerThreads) umap[idx_s[(q / k) * 32 + q % k]] = 1;
+  __syncthreads();
+  if (warp == 0) {
+    // union in ascending expert order: rank = number of marked experts below
+    int nu = 0;
+    for (int e0 = 0; e0 < E; e0 += 32) {
+      const int e = e0 + lane;
+      const bool f = e < E && umap[e] != 0;
+      const unsigned int b = __ballot_sync(0xffffffffu, f);
+      const int rank = nu + __popc(b & ((1u << lane) - 1u));
+      __syncwarp();
+      if (f) {
+        umap[e] = static_cast<short>(rank);
+        ue[rank] = static_cast<short>(e);
+      }
+      nu += __popc(b);
+    }
+    if (lane == 0) n_union = nu;
+  }
+  for (int u = threadIdx.x; u < kRowsMaxUnion; u += kDecLayerThreads) users[u] = 0u;
+  __syncthreads();
+  const int U = n_union;
+  for (int q = threadIdx.x; q < T * k; q += kDecLayerThreads) {
+    const int t = q / k, j = q - (q / k) * k;
+    const int u = umap[idx_s[t * 32 + j]];
+    atomicOr(&users[u], 1u << t);
+    slot_of[u][t] = static_cast<signed char>(j);
+  }
+  __syncthreads();
+  if (warp == kDecWarps - 1 && nrows > 0) {
+    // this CTA's output rows of the union experts (and their int4 scales and
+    // biases) into L2 while phase B streams the gate/up rows
+    const size_t rbI = row_bytes<WF>(p.I);
+    for (int u = 0; u < U; ++u) {
+      const size_t r0 = static_cast<size_t>(ue[u]) * H + n0;
+      prefetch_row_l2(row_ptr<WF>(p.down, r0, p.I), nrows * rbI);
+      if (WF != 0) prefetch_row_l2(scale_row(p.down_scale, r0, p.I), nrows * (p.I / 64) * 2);
+      if (WF == 2) prefetch_row_l2(scale_row(p.down_bias, r0, p.I), nrows * (p.I / 64) * 2);
+    }
+  }
+
+  // ---- B: union gate/up row pairs with their user rows -> h
+  const int nB = U * p.I;
+  for (int q = gw; q < nB; q += nw) {
+    const int u = q / p.I, i = q - u * p.I;
+    const size_t rg = static_cast<size_t>(ue[u]) * 2 * p.I + i;
+    const void *rows[2] = {row_ptr<WF>(p.gate_up, rg, H), row_ptr<WF>(p.gate_up, rg + p.I, H)};
+    const __nv_bfloat16 *sr[2] = {scale_row(p.gate_up_scale, rg, H),
+                                  scale_row(p.gate_up_scale, rg + p.I, H)};
+    const __nv_bfloat16 *br[2] = {scale_row(p.gate_up_bias, rg, H),
+                                  scale_row(p.gate_up_bias, rg + p.I, H)};
+    warp_dots_users<WF, 2>(rows, sr, br, H, x_s, xq, users[u], mb_x, p.status,
+                           [&](int t, const float (&d)[2]) {
+                             if (lane == 0)
+                               p.h[t * hrow + static_cast<size_t>(slot_of[u][t]) * p.h_ld + i] =
+                                   silu_f(d[0]) * d[1];
+                           });
+  }
+  grid_sync(p.bar, base + 2 * static_cast<unsigned long long>(G), p.status);
+
+  // ---- C: output rows n0..n1 of the union experts (u < U) and the shared
+  // expert (u = U), 8 rows per task, for each user row
+  const size_t pstride = static_cast<size_t>(k + 1) * p.p3_rows;   // part floats per row t
+  for (int task = warp; task < (U + 1) * ngroups; task += kDecWarps) {
+    const int u = task / ngroups, t0 = (task - u * ngroups) * 8;
+    const bool sh = (u == U);
+    slot_task_users<WF>(p, p.h, hrow, sh ? all_rows : users[u],
+                        [&](int t) { return sh ? k : static_cast<int>(slot_of[u][t]); }, t0, n0,
+                        nrows, sh ? 0 : ue[u], part, pstride);
+  }
+  __syncthreads();
+  // y[t][n] = sum_j w[t][j] part[t][j][n] + g[t] part[t][k][n], in that order
+  for (int q = threadIdx.x; q < T * nrows; q += kDecLayerThreads) {
+    const int t = q / nrows, n = q - t * nrows;
+    const float *pt = part + t * pstride;
+    float y = 0.0f;
+    for (int j = 0; j < k; ++j) y = fmaf(w_s[t * 32 + j], pt[j * p.p3_rows + n], y);
+    y = fmaf(g_s[t], pt[k * p.p3_rows + n], y);
+    reinterpret_cast<__nv_bfloat16 *>(p.y)[static_cast<size_t>(t) * H + n0 + n] = __float2bfloat16_rn(y);
+  }
+}
+
 template <int WF>
 static void set_p3(DecodeParams &p, int grid, int smem_limit, size_t *smem) {
   p.p3_rows = (p.H + grid - 1) / grid;
@@ -854,6 +1135,36 @@ cudaError_t launch_decode_layers(const DecodeParams *layers, int n, int grid, in
                     : launch_layers<1, 32>(layers, n, grid, smem_limit, pdl, stream);
 }
 
+// Largest dynamic shared memory of the rows kernels (the device's opt-in
+// limit less their static shared memory), set by decode_configure.
+static int g_rows_smem_limit = 0;
+
+template <int WF, int R>
+static cudaError_t launch_rows_t(DecodeParams p, int grid, int smem_limit, bool pdl,
+                                 cudaStream_t stream) {
+  p.p3_rows = (p.H + grid - 1) / grid;
+  p.p3_stage = 0;
+  const RowsSmem S = rows_smem(p.T, p.k, p.H, p.p3_rows);
+  (void)smem_limit;
+  if (S.total > static_cast<size_t>(g_rows_smem_limit)) return cudaErrorInvalidValue;
+  cudaLaunchAttribute attr[2];
+  const cudaLaunchConfig_t cfg = dec_config(grid, S.total, pdl, stream, attr);
+  return cudaLaunchKernelEx(&cfg, rows_kernel<WF, R>, p);
+}
+
+cudaError_t launch_rows(const DecodeParams &p, int grid, int smem_limit, bool pdl,
+                        cudaStream_t stream) {
+  if (p.T < 1 || p.T > kSmallMaxRows || p.k > 32 || p.E > 1024) return cudaErrorInvalidValue;
+  if (p.wfmt == 0)
+    return p.E <= 256 ? launch_rows_t<0, 8>(p, grid, smem_limit, pdl, stream)
+                      : launch_rows_t<0, 32>(p, grid, smem_limit, pdl, stream);
+  if (p.wfmt == 2)
+    return p.E <= 256 ? launch_rows_t<2, 8>(p, grid, smem_limit, pdl, stream)
+                      : launch_rows_t<2, 32>(p, grid, smem_limit, pdl, stream);
+  return p.E <= 256 ? launch_rows_t<1, 8>(p, grid, smem_limit, pdl, stream)
+                    : launch_rows_t<1, 32>(p, grid, smem_limit, pdl, stream);
+}
+
 cudaError_t decode_configure(int *smem_limit) {
   // Opt every instantiation into the device's largest dynamic shared memory;
   // each launch then asks for what its shape needs.
@@ -881,6 +1192,26 @@ cudaError_t decode_configure(int *smem_limit) {
     if ((e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) !=
         cudaSuccess)
       return e;
+  // the rows kernels hold about 17 KB of static shared memory (the union
+  // tables): each may ask for the opt-in limit less that
+  const void *rows_kernels[] = {
+      reinterpret_cast<const void *>(rows_kernel<0, 8>),
+      reinterpret_cast<const void *>(rows_kernel<0, 32>),
+      reinterpret_cast<const void *>(rows_kernel<1, 8>),
+      reinterpret_cast<const void *>(rows_kernel<1, 32>),
+      reinterpret_cast<const void *>(rows_kernel<2, 8>),
+      reinterpret_cast<const void *>(rows_kernel<2, 32>)};
+  int rows_limit = bytes;
+  for (const void *k : rows_kernels) {
+    cudaFuncAttributes a{};
+    if ((e = cudaFuncGetAttributes(&a, k)) != cudaSuccess) return e;
+    const int dyn = optin - static_cast<int>(a.sharedSizeBytes) - 1024;
+    if ((e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn)) !=
+        cudaSuccess)
+      return e;
+    rows_limit = dyn < rows_limit ? dyn : rows_limit;
+  }
+  g_rows_smem_limit = rows_limit;
   *smem_limit = bytes;
   return cudaSuccess;
 }

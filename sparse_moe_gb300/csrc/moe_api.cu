@@ -126,11 +126,11 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 
 
 enum KernelId : int {
   K_ROUTER_GEMM = 0, K_TOPK, K_SCAN, K_SCATTER, K_GATEUP_GEMM, K_DOWN_GEMM, K_COMBINE,
-  K_DEC_LAYER, K_H2D, K_D2H, K_DEC_LAYERS, K_COUNT
+  K_DEC_LAYER, K_H2D, K_D2H, K_DEC_LAYERS, K_ROWS, K_COUNT
 };
 const char *kKernelNames[K_COUNT] = {
     "router_gemm", "topk", "route_scan", "route_scatter", "gateup_swiglu_gemm", "down_gemm",
-    "combine", "decode_layer", "h2d_copy", "d2h_copy", "decode_layers"};
+    "combine", "decode_layer", "h2d_copy", "d2h_copy", "decode_layers", "rows"};
 
 }  // namespace
 
@@ -162,6 +162,7 @@ struct moe_ctx {
   int block_rows = kBlockRowsMax;
   int32_t host_nblocks = 0;
   int decode_grid = 0;     // CTAs of the cooperative decode launch
+  int last_rows = 0;       // rows of the last moe_forward_rows (its routing is in the prefill regions)
   int decode_smem = 0;     // dynamic shared-memory limit of the decode kernel
   bool decode_pdl = true;  // decode launches overlap the previous kernel's tail
   char *ws = nullptr;
@@ -762,6 +763,55 @@ moe_status moe_forward_decode_layers(moe_ctx *ctx, int first_layer, int n_layers
     if (st) return st;
   }
   return MOE_OK;
+}
+
+moe_status moe_forward_rows(moe_ctx *ctx, int layer, const void *x, int T, void *y,
+                            void *stream) {
+  moe_status st = check_layer(ctx, layer);
+  if (st) return st;
+  const moe_config &c = ctx->cfg;
+  const WsLayout &L = ctx->L;
+  if (T < 1 || T > kSmallMaxRows || T > L.Tc)
+    return fail(ctx, MOE_ERR_INVALID_ARG, "T = %d outside 1..%d (and the context's max_chunk_rows %d)",
+                T, kSmallMaxRows, L.Tc);
+  if (!x || !y || !aligned16(x) || !aligned16(y))
+    return fail(ctx, MOE_ERR_INVALID_ARG, "x/y null or not 16-byte aligned");
+  // h [T][k + 1][Imax] fp32 lives in the o region ([R, H] fp16)
+  if (static_cast<size_t>(T) * (c.top_k + 1) * L.Imax * 4 > static_cast<size_t>(L.R) * c.hidden * 2)
+    return fail(ctx, MOE_ERR_UNSUPPORTED, "rows scratch does not fit the workspace");
+  if ((st = ensure_device(ctx))) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  DecodeParams p = decode_params(ctx, ctx->layers[layer], x, y);
+  p.T = T;
+  p.logits = ctx->at<float>(L.logits);
+  p.idx = ctx->at<int32_t>(L.idx);
+  p.w = ctx->at<float>(L.w);
+  p.g = ctx->at<float>(L.gate);
+  p.h = ctx->at<float>(L.o);
+  ProfScope ps(ctx, K_ROWS, s);
+  st = launched(ctx, launch_rows(p, ctx->decode_grid, ctx->decode_smem, ctx->decode_pdl, s),
+                "rows launch");
+  if (st == MOE_OK) ctx->last_rows = T;
+  return st;
+}
+
+moe_status moe_rows_routing(moe_ctx *ctx, float *logits, int32_t *idx, float *w, void *stream) {
+  if (!ctx) return MOE_ERR_INVALID_ARG;
+  if (ctx->last_rows < 1) return fail(ctx, MOE_ERR_INVALID_ARG, "no moe_forward_rows call yet");
+  moe_status st = ensure_device(ctx);
+  if (st) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const moe_config &c = ctx->cfg;
+  const size_t T = static_cast<size_t>(ctx->last_rows);
+  cudaError_t e = cudaSuccess;
+  if (logits)
+    e = cudaMemcpyAsync(logits, ctx->ws + ctx->L.logits, T * c.n_experts * 4,
+                        cudaMemcpyDeviceToDevice, s);
+  if (e == cudaSuccess && idx)
+    e = cudaMemcpyAsync(idx, ctx->ws + ctx->L.idx, T * c.top_k * 4, cudaMemcpyDeviceToDevice, s);
+  if (e == cudaSuccess && w)
+    e = cudaMemcpyAsync(w, ctx->ws + ctx->L.w, T * c.top_k * 4, cudaMemcpyDeviceToDevice, s);
+  return e == cudaSuccess ? MOE_OK : cuda_fail(ctx, e, "rows routing copy");
 }
 
 moe_status moe_decode_routing(moe_ctx *ctx, float *logits, int32_t *idx, float *w, void *stream) {

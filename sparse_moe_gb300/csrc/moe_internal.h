@@ -137,6 +137,8 @@ struct DecodeParams {
   unsigned long long *bar;   // grid-barrier arrival counter (16-byte slot, zeroed once)
   int *status;               // device status word
   int p3_rows, p3_stage;     // set by launch_decode_layer
+  int T;                     // launch_rows: rows of x and y (x, y [T, H]; logits [T, E];
+                             // idx, w [T, k]; g [T]; h [T][k + 1][h_ld]); 1 otherwise
 };
 // Up to kMaxDecodeLayers layers (same shapes) for one multi-layer decode launch.
 constexpr int kMaxDecodeLayers = 48;
@@ -160,5 +162,11 @@ cudaError_t launch_decode_layer(const DecodeParams &p, int grid, int smem_limit,
 // same grid: layer l + 1 starts after a grid barrier behind layer l's outputs.
 cudaError_t launch_decode_layers(const DecodeParams *layers, int n, int grid, int smem_limit,
                                  bool pdl, cudaStream_t stream);
+// A few rows (1 <= p.T <= kSmallMaxRows) of one layer in one cooperative
+// launch of the decode grid: every weight row the rows need is streamed once
+// for all of them (see decode.cu).
+constexpr int kSmallMaxRows = 16;
+cudaError_t launch_rows(const DecodeParams &p, int grid, int smem_limit, bool pdl,
+                        cudaStream_t stream);
 
 }  // namespace moe

@@ -331,3 +331,25 @@ def test_prefill_on_dequantised_weights_equals_fused_int4(wfmt):
     yb = ctxb.forward_prefill(0, x)
     torch.cuda.synchronize()
     assert torch.equal(y4, yb)
+
+
+# ---- the ablation switches (measurement options read at context creation)
+# change how the work is scheduled, never a result: each output row is the
+# same dot products in the same order whatever block it lands in.
+
+@pytest.mark.parametrize("env", [{"MOE_ABLATE_HOST_ROUTING": "1"}, {"MOE_ABLATE_TILE": "fixed256"},
+                                 {"MOE_ABLATE_TILE": "rows16"}, {"MOE_ABLATE_TILE": "rows48"}])
+def test_ablation_switches_change_no_result(env, monkeypatch):
+    wl = _wl(moe_synth.QWEN, 700, bias=1.5, seed=41)
+    ctx, (w,) = make_ctx(wl)
+    x = moe_synth.make_x(wl, device="cuda")
+    y0 = ctx.forward_prefill(0, x)
+    for k, v in env.items():
+        monkeypatch.setenv(k, v)
+    s = wl.shape
+    ctx2 = MoEContext(s.hidden, s.n_experts, s.top_k, s.inter, s.shared_inter)
+    ctx2.load_weights(0, w)
+    y1 = ctx2.forward_prefill(0, x)
+    torch.cuda.synchronize()
+    assert torch.equal(y0, y1)
+    assert ctx2.check_device() == 0
