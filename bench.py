@@ -122,9 +122,11 @@ class ClockSampler:
 
 # DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) of
 # the kernels the roofline lines name, from one ncu capture of the current
-# kernels (the summaries under profiles/): gate/up 625.5 + 33.0 MB at the
-# T=4096 prefill workload, decode layer 57.76 + 0.29 MB.
-TRAFFIC_BYTES = {"gateup_swiglu_gemm": 658.5e6, "decode_layer": 58.05e6}
+# kernels (the summaries under profiles/): gate/up 624.3 + 33.0 MB at the
+# T=4096 prefill workload, decode layer 57.76 + 0.33 MB (bf16) and
+# 16.19 + 0.00 MB (symmetric int4).  The affine int4 decode was not captured.
+TRAFFIC_BYTES = {"gateup_swiglu_gemm": 657.4e6, "decode_layer": 58.09e6,
+                 "decode_layer_int4_sym": 16.19e6}
 
 
 # ------------------------------------------------------------- workload --
@@ -537,7 +539,9 @@ def bench_decode(args, dev, stream, hbm, int4=None, wl=None):
         "bytes_per_layer": nb["total"],
         "roofline": {"kernel": "decode_layer", "bound": "hbm", "achieved": achieved,
                      "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                     "traffic": None if int4 else TRAFFIC_BYTES["decode_layer"],
+                     "traffic": (TRAFFIC_BYTES["decode_layer"] if not int4 else
+                                 TRAFFIC_BYTES["decode_layer_int4_sym"]
+                                 if wl.wfmt == moe_synth.WFMT_INT4 else None),
                      "algorithmic_bytes_per_launch": nb["total"],
                      "launch_us_timed": us_layer,
                      "timing": "graph replays of L layers, CUDA events on the launch stream; "
