@@ -287,9 +287,16 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
   return r;
 }
-// Release-arrive on an mbarrier anywhere in the cluster.
+// Arrive on an mbarrier anywhere in the cluster (the pair leader's), with
+// the default CTA-scope release.  Every producer that uses it has completed
+// its writes to its own shared memory before the arrive (cp.async.wait_group,
+// or st.shared in program order) and made them visible to the tensor core
+// (fence.proxy.async), or has finished its TMEM reads (tcgen05.wait::ld); the
+// data is then in place when the leader observes the phase.  A cluster-scope
+// release cost each arriving thread about a thousand cycles on GB300 (the
+// grouped GEMMs: 11 % on bf16 gate/up, 10 % on int4).
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+  asm volatile("mbarrier.arrive.release.cta.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
                : "memory");
 }
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {

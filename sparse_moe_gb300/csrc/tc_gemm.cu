@@ -40,8 +40,7 @@
 //    leader's ready barrier: for bf16 -> fp16 (down without fp16 copies) a
 //    team per stage, each member with a cluster-scope arrival from the peer;
 //    for int4 four converter warps per k-step, whose codes come through
-//    their own ring, and in the peer one relay thread forwards a single
-//    cluster-scope arrival per k-step once its four converters are done;
+//    their own ring;
 //    four epilogue warps
 //    per CTA drain their half of the double-buffered TMEM accumulator while
 //    the next tile computes, and transpose each 32x16 piece through shared
@@ -133,19 +132,11 @@ static_assert(kCodeSlots % kInt4Groups == 0 && kInt4Groups <= STAGES,
 template <int CONV> __host__ __device__ constexpr int conv_team() {
   return CONV == CONV_BF16_TO_F16 ? kConvTeam : conv_int4(CONV) ? kInt4Warps : 1;
 }
-// Arrivals on the leader's ready barrier per k-step: both CTAs' conversion
-// teams, except for int4, where the peer's four converters arrive on a local
-// barrier (cdone) and one relay thread forwards a single cluster-scope arrival
-// (a cluster-scope release costs each arriving thread about a thousand cycles).
-template <int CONV> __host__ __device__ constexpr int ready_count() {
-  return conv_int4(CONV) ? kInt4Warps + 1 : 2 * conv_team<CONV>();
-}
 
 struct SmemTail {
   uint64_t full[STAGES];        // local: TMA (A, or int4: the producers' token-row boxes) + this CTA's B warps
   uint64_t cfull[kCodeSlots];   // local, int4: a k-step's weight codes landed in the ring (TMA)
   uint64_t cempty[kCodeSlots];  // local, int4: the k-step's converters hold their codes
-  uint64_t cdone[STAGES];       // peer, int4: its four converters are done (relayed to ready)
   uint64_t ready[STAGES];       // leader: both CTAs' conversion teams
   uint64_t empty[STAGES];       // local: arrives from the leader's commit
   uint64_t tmem_full[2];        // local: arrives from the leader's commit
@@ -440,9 +431,8 @@ __device__ __forceinline__ bool convert_stage_bf16(const GemmParams &p, int stag
 // ring slot it % kCodeSlots): takes its codes (batches q * kInt4Batches + b)
 // from the ring as soon as they land and frees its share of the slot, waits
 // until the MMA has released the stage's A region, expands its weight rows
-// into it, and arrives on the leader's ready barrier, or in the peer on its
-// local cdone barrier (the last converter only after the stage's token rows
-// have landed).  sv, bv: this lane's row scales and biases, one per batch,
+// into it, and arrives on the pair leader's ready barrier (the last converter
+// only after the stage's token rows have landed).  sv, bv: this lane's row scales and biases, one per batch,
 // loaded by the caller before the waits.  Returns false on a timeout or abort.
 template <int CONV>
 __device__ __forceinline__ bool convert_stage_int4(const GemmParams &p, int q,
@@ -487,10 +477,7 @@ __device__ __forceinline__ bool convert_stage_int4(const GemmParams &p, int q,
     if (q == kInt4Warps - 1)
       got = mbar_wait_bounded(smem_u32(&tail->full[stage]), sph, abort_flag, p.status,
                               DEV_TIMEOUT_CONVERTER);
-    if (got) {
-      if (rank == 0) mbar_arrive(smem_u32(&tail->ready[stage]));
-      else mbar_arrive(smem_u32(&tail->cdone[stage]));   // relayed by the peer's MMA warp
-    }
+    if (got) arrive_ready(tail, stage, rank);
   }
 #ifdef MOE_TRACE
   if (lane == 0) {
@@ -544,8 +531,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       // producers (and both CTAs' TMA bytes); otherwise each CTA's own
       mbar_init(smem_u32(&tail->full[s]),
                 CONV == CONV_NONE ? 1 + 2 * B_WARPS_PER_STAGE : 1 + B_WARPS_PER_STAGE);
-      mbar_init(smem_u32(&tail->ready[s]), ready_count<CONV>());
-      mbar_init(smem_u32(&tail->cdone[s]), kInt4Warps);
+      mbar_init(smem_u32(&tail->ready[s]), 2 * conv_team<CONV>());
       mbar_init(smem_u32(&tail->empty[s]), 1);
     }
     for (int s = 0; s < kCodeSlots; ++s) {
@@ -875,26 +861,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
             atomicExch(p.status, DEV_TIMEOUT_DRAIN);
             break;
           }
-        }
-      }
-    } else if (conv_int4(CONV) && lane == 0) {
-      // ------------------------------------------- int4 readiness relay (peer) --
-      // Once this CTA's four converters of a k-step are done (cdone, a
-      // CTA-scope acquire), one cluster-scope release-arrive tells the leader.
-      int it = 0;
-      bool ok = true;
-      for (int tile = pair_id; tile < ntiles && ok; tile += num_pairs) {
-        const Tile t = decode_tile(p, tile, rank);
-        if (!t.valid) continue;
-        for (int ks = 0; ks < t.nk; ++ks, ++it) {
-          const int stage = it % STAGES;
-          if (!mbar_wait_bounded(smem_u32(&tail->cdone[stage]),
-                                 static_cast<uint32_t>(it / STAGES) & 1u, abort_flag, p.status,
-                                 DEV_TIMEOUT_RELAY)) {
-            ok = false;
-            break;
-          }
-          mbar_arrive_cluster(mapa_shared(smem_u32(&tail->ready[stage]), 0));
         }
       }
     }
