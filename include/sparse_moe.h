@@ -238,7 +238,15 @@ moe_status moe_rows_routing(moe_ctx *ctx, float *logits, int32_t *idx, float *w,
 /* End-to-end prefill from HOST memory: copies x_host [T, H] bf16 to the
  * device chunk by chunk, runs the prefill path and copies y back into y_host
  * [T, H].  Pinned host buffers make the copies asynchronous; the call returns
- * once the work is enqueued (synchronise `stream` before reading y_host). */
+ * once the work is enqueued (synchronise `stream` before reading y_host).
+ * The input copies run on the context's own copy stream through two staging
+ * slots, so that a chunk's input copy overlaps the previous chunk's (or the
+ * previous call's) compute.  A page-locked y_host is written directly by the
+ * combine kernel (it is addressable from the device); a pageable one through
+ * a staging slot and an output copy on a second copy stream, which overlaps
+ * the next chunk's compute.  The layer's kernels are ordered after earlier
+ * work on `stream`, but the input copy is not: x_host must hold the input
+ * when the call is made. */
 moe_status moe_forward_prefill_host(moe_ctx *ctx, int layer, const void *x_host,
                                     int T, void *y_host, void *stream);
 

@@ -24,7 +24,8 @@ size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 struct WsLayout {
   int Tc, nblk, R, Imax, max_blocks;
   size_t status, logits, idx, w, gate, mask, base, counts, offsets, sorted, pos, blocks, nblocks, h, o;
-  size_t dec_logits, dec_idx, dec_w, dec_g, dec_h, dec_counter, x_stage, y_stage, total;
+  size_t dec_logits, dec_idx, dec_w, dec_g, dec_h, dec_counter, x_stage, y_stage, dec_x_stage,
+      dec_y_stage, total;
 };
 
 WsLayout make_layout(const moe_config &c) {
@@ -63,8 +64,10 @@ WsLayout make_layout(const moe_config &c) {
   L.dec_g = take(4);
   L.dec_h = take(decode_h_floats(c.top_k, L.Imax) * 4);
   L.dec_counter = take(16);
-  L.x_stage = take(Tc * H * 2);
-  L.y_stage = take(Tc * H * 2);
+  L.x_stage = take(2 * Tc * H * 2);   // two slots: see moe_forward_prefill_host
+  L.y_stage = take(2 * Tc * H * 2);
+  L.dec_x_stage = take(H * 2);   // moe_forward_decode_host (apart from the prefill slots,
+  L.dec_y_stage = take(H * 2);   // whose input copies do not wait for the caller's stream)
   L.total = off;
   return L;
 }
@@ -163,6 +166,11 @@ struct moe_ctx {
   int32_t host_nblocks = 0;
   int decode_grid = 0;     // CTAs of the cooperative decode launch
   int last_rows = 0;       // rows of the last moe_forward_rows (its routing is in the prefill regions)
+  // moe_forward_prefill_host: copy streams and the events of the two staging
+  // slots (created on first use)
+  cudaStream_t copy_in = nullptr, copy_out = nullptr;
+  cudaEvent_t ev_x[2] = {}, ev_y[2] = {}, ev_out[2] = {};
+  int host_slot = 0;
   int decode_smem = 0;     // dynamic shared-memory limit of the decode kernel
   bool decode_pdl = true;  // decode launches overlap the previous kernel's tail
   char *ws = nullptr;
@@ -617,6 +625,13 @@ moe_status moe_ctx_destroy(moe_ctx *ctx) {
     cudaEventDestroy(r.b);
   }
   for (auto e : ctx->event_pool) cudaEventDestroy(e);
+  for (int i = 0; i < 2; ++i) {
+    if (ctx->ev_x[i]) cudaEventDestroy(ctx->ev_x[i]);
+    if (ctx->ev_y[i]) cudaEventDestroy(ctx->ev_y[i]);
+    if (ctx->ev_out[i]) cudaEventDestroy(ctx->ev_out[i]);
+  }
+  if (ctx->copy_in) cudaStreamDestroy(ctx->copy_in);
+  if (ctx->copy_out) cudaStreamDestroy(ctx->copy_out);
   delete ctx;
   return MOE_OK;
 }
@@ -839,29 +854,73 @@ moe_status moe_forward_prefill_host(moe_ctx *ctx, int layer, const void *x_host,
     return fail(ctx, MOE_ERR_INVALID_ARG, "bad host buffers or T");
   if (T == 0) return MOE_OK;
   if ((st = ensure_device(ctx))) return st;
+  cudaError_t e = cudaSuccess;
+  if (!ctx->copy_in) {
+    if ((e = cudaStreamCreateWithFlags(&ctx->copy_in, cudaStreamNonBlocking)) != cudaSuccess ||
+        (e = cudaStreamCreateWithFlags(&ctx->copy_out, cudaStreamNonBlocking)) != cudaSuccess)
+      return cuda_fail(ctx, e, "copy stream creation");
+    for (int i = 0; i < 2; ++i)
+      if ((e = cudaEventCreateWithFlags(&ctx->ev_x[i], cudaEventDisableTiming)) != cudaSuccess ||
+          (e = cudaEventCreateWithFlags(&ctx->ev_y[i], cudaEventDisableTiming)) != cudaSuccess ||
+          (e = cudaEventCreateWithFlags(&ctx->ev_out[i], cudaEventDisableTiming)) != cudaSuccess)
+        return cuda_fail(ctx, e, "copy event creation");
+  }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const size_t row_bytes = static_cast<size_t>(ctx->cfg.hidden) * 2;
-  void *xs = ctx->ws + ctx->L.x_stage;
-  void *ys = ctx->ws + ctx->L.y_stage;
+  const size_t slot_bytes = static_cast<size_t>(ctx->L.Tc) * row_bytes;
   const LayerSlot &ls = ctx->layers[layer];
+  // Page-locked y_host is directly addressable by the device: the combine
+  // kernel then writes y into it (over the CPU-GPU link) and no output copy
+  // or staging is needed.
+  char *y_direct = nullptr;
+  {
+    cudaPointerAttributes pa{};
+    if (cudaPointerGetAttributes(&pa, y_host) == cudaSuccess && pa.type == cudaMemoryTypeHost &&
+        pa.devicePointer != nullptr && aligned16(pa.devicePointer))
+      y_direct = static_cast<char *>(pa.devicePointer);
+    else
+      cudaGetLastError();   // pageable memory: not an error here
+  }
+  // Chunk c uses staging slot c % 2 (alternating across calls too): its
+  // input copy runs on copy_in once the slot's previous use is over, so it
+  // overlaps the previous chunk's (or call's) compute; its output copy, if
+  // any, runs on copy_out and overlaps the next chunk's compute.  `stream`
+  // waits for the last output copies at the end, so synchronising it covers
+  // y_host.
+  bool used[2] = {false, false};
   for (int c0 = 0; c0 < T; c0 += ctx->cfg.max_chunk_rows) {
     const int n = std::min(ctx->cfg.max_chunk_rows, T - c0);
-    cudaError_t e;
-    {
-      ProfScope ps(ctx, K_H2D, s);
+    const int slot = ctx->host_slot;
+    ctx->host_slot ^= 1;
+    used[slot] = true;
+    void *xs = ctx->ws + ctx->L.x_stage + slot * slot_bytes;
+    void *ys = ctx->ws + ctx->L.y_stage + slot * slot_bytes;
+    if ((e = cudaStreamWaitEvent(ctx->copy_in, ctx->ev_out[slot], 0)) == cudaSuccess) {
+      ProfScope ps(ctx, K_H2D, ctx->copy_in);
       e = cudaMemcpyAsync(xs, static_cast<const char *>(x_host) + c0 * row_bytes, n * row_bytes,
-                          cudaMemcpyHostToDevice, s);
+                          cudaMemcpyHostToDevice, ctx->copy_in);
     }
+    if (e == cudaSuccess) e = cudaEventRecord(ctx->ev_x[slot], ctx->copy_in);
     if (e != cudaSuccess) return cuda_fail(ctx, e, "host-to-device copy");
-    st = enqueue_prefill_chunk(ctx, ls, xs, n, ys, s);
+    if ((e = cudaStreamWaitEvent(s, ctx->ev_x[slot], 0)) != cudaSuccess)
+      return cuda_fail(ctx, e, "stream wait");
+    st = enqueue_prefill_chunk(ctx, ls, xs, n, y_direct ? y_direct + c0 * row_bytes : ys, s);
     if (st) return st;
-    {
-      ProfScope ps(ctx, K_D2H, s);
+    // the slot's input is free once this chunk's kernels are done
+    if ((e = cudaEventRecord(y_direct ? ctx->ev_out[slot] : ctx->ev_y[slot], s)) != cudaSuccess)
+      return cuda_fail(ctx, e, "event record");
+    if (y_direct) continue;
+    if ((e = cudaStreamWaitEvent(ctx->copy_out, ctx->ev_y[slot], 0)) == cudaSuccess) {
+      ProfScope ps(ctx, K_D2H, ctx->copy_out);
       e = cudaMemcpyAsync(static_cast<char *>(y_host) + c0 * row_bytes, ys, n * row_bytes,
-                          cudaMemcpyDeviceToHost, s);
+                          cudaMemcpyDeviceToHost, ctx->copy_out);
     }
+    if (e == cudaSuccess) e = cudaEventRecord(ctx->ev_out[slot], ctx->copy_out);
     if (e != cudaSuccess) return cuda_fail(ctx, e, "device-to-host copy");
   }
+  for (int i = 0; i < 2; ++i)
+    if (used[i] && (e = cudaStreamWaitEvent(s, ctx->ev_out[i], 0)) != cudaSuccess)
+      return cuda_fail(ctx, e, "stream wait");
   return MOE_OK;
 }
 
@@ -873,8 +932,8 @@ moe_status moe_forward_decode_host(moe_ctx *ctx, int layer, const void *x_host, 
   if ((st = ensure_device(ctx))) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const size_t bytes = static_cast<size_t>(ctx->cfg.hidden) * 2;
-  void *xs = ctx->ws + ctx->L.x_stage;
-  void *ys = ctx->ws + ctx->L.y_stage;
+  void *xs = ctx->ws + ctx->L.dec_x_stage;
+  void *ys = ctx->ws + ctx->L.dec_y_stage;
   cudaError_t e = cudaMemcpyAsync(xs, x_host, bytes, cudaMemcpyHostToDevice, s);
   if (e != cudaSuccess) return cuda_fail(ctx, e, "host-to-device copy");
   st = enqueue_decode(ctx, ctx->layers[layer], xs, ys, s);

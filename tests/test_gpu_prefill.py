@@ -136,6 +136,34 @@ def test_prefill_host_buffers_match_device_path():
     assert torch.equal(y_h, y_dev.cpu())
 
 
+@pytest.mark.parametrize("pinned_out", [True, False])
+def test_prefill_host_back_to_back_calls_match_device_path(pinned_out):
+    # consecutive calls without a synchronisation in between: their copies
+    # run on the context's copy streams through alternating staging slots,
+    # overlapping each other's compute; a decode from host buffers in between.
+    # Page-locked outputs are written by the combine kernel directly, pageable
+    # ones through the staging slots and an output copy.
+    wl = _wl(moe_synth.QWEN, 300, bias=1.5, seed=10)
+    ctx, (w,) = make_ctx(wl, max_chunk_rows=256)      # two chunks per call
+    base = moe_synth.make_x(wl, device="cuda")
+    xs = [base, torch.flip(base, dims=[0]).contiguous(), (base.float() * 0.5).to(torch.bfloat16)]
+    ys_dev = [ctx.forward_prefill(0, x) for x in xs]
+    yd_dev = ctx.forward_decode(0, base[:1].contiguous())
+    torch.cuda.synchronize()
+    xh = [x.cpu().pin_memory() for x in xs]
+    yh = [torch.empty_like(x).pin_memory() if pinned_out else torch.empty_like(x) for x in xh]
+    xdh = base[:1].cpu().pin_memory()
+    ydh = torch.empty_like(xdh).pin_memory()
+    for i in range(3):
+        ctx.forward_prefill_host(0, xh[i], yh[i])
+        if i == 1:
+            ctx.forward_decode_host(0, xdh, ydh)
+    torch.cuda.synchronize()
+    for i in range(3):
+        assert torch.equal(yh[i], ys_dev[i].cpu())
+    assert torch.equal(ydh, yd_dev.cpu())
+
+
 # ---- optional fp16 copies of the down weights: the down GEMM then feeds its
 # weight tiles straight to the tensor cores instead of converting them in
 # shared memory; the conversion is the same, so the output must not change.
