@@ -250,7 +250,8 @@ moe_status moe_rows_routing(moe_ctx *ctx, float *logits, int32_t *idx, float *w,
 moe_status moe_forward_prefill_host(moe_ctx *ctx, int layer, const void *x_host,
                                     int T, void *y_host, void *stream);
 
-/* Same for one decode token (x_host, y_host: bf16 [H] in host memory). */
+/* Same for one decode token (x_host, y_host: bf16 [H] in host memory); a
+ * page-locked y_host is written by the decode kernel directly. */
 moe_status moe_forward_decode_host(moe_ctx *ctx, int layer, const void *x_host,
                                    void *y_host, void *stream);
 

@@ -934,10 +934,21 @@ moe_status moe_forward_decode_host(moe_ctx *ctx, int layer, const void *x_host, 
   const size_t bytes = static_cast<size_t>(ctx->cfg.hidden) * 2;
   void *xs = ctx->ws + ctx->L.dec_x_stage;
   void *ys = ctx->ws + ctx->L.dec_y_stage;
+  // a page-locked y_host is written by the kernel directly (as in
+  // moe_forward_prefill_host)
+  void *y_direct = nullptr;
+  {
+    cudaPointerAttributes pa{};
+    if (cudaPointerGetAttributes(&pa, y_host) == cudaSuccess && pa.type == cudaMemoryTypeHost &&
+        pa.devicePointer != nullptr && aligned16(pa.devicePointer))
+      y_direct = pa.devicePointer;
+    else
+      cudaGetLastError();
+  }
   cudaError_t e = cudaMemcpyAsync(xs, x_host, bytes, cudaMemcpyHostToDevice, s);
   if (e != cudaSuccess) return cuda_fail(ctx, e, "host-to-device copy");
-  st = enqueue_decode(ctx, ctx->layers[layer], xs, ys, s);
-  if (st) return st;
+  st = enqueue_decode(ctx, ctx->layers[layer], xs, y_direct ? y_direct : ys, s);
+  if (st || y_direct) return st;
   e = cudaMemcpyAsync(y_host, ys, bytes, cudaMemcpyDeviceToHost, s);
   return e == cudaSuccess ? MOE_OK : cuda_fail(ctx, e, "device-to-host copy");
 }

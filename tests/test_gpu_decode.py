@@ -84,12 +84,15 @@ def test_decode_matches_prefill_one_token(decode_bf16):
     assert err <= 1e-2 * np.abs(ref).max()
 
 
-def test_decode_host_buffers_match_device_path(decode_bf16):
+@pytest.mark.parametrize("pinned_out", [True, False])
+def test_decode_host_buffers_match_device_path(decode_bf16, pinned_out):
+    # a page-locked output is written by the kernel directly, a pageable one
+    # through the staging buffer and a copy
     wl, ctx, layers = decode_bf16
     x = moe_synth.make_x(wl, layer=0, device="cuda")
     yd = ctx.forward_decode(0, x)
     x_h = x.cpu().pin_memory()
-    y_h = torch.empty_like(x_h).pin_memory()
+    y_h = torch.empty_like(x_h).pin_memory() if pinned_out else torch.empty_like(x_h)
     ctx.forward_decode_host(0, x_h, y_h)
     torch.cuda.synchronize()
     assert torch.equal(y_h, yd.cpu())
