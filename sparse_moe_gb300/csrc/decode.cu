@@ -429,6 +429,55 @@ __device__ __forceinline__ void slot_task(const DecodeParams &p, const float *hb
   float acc[8];
 #pragma unroll
   for (int r = 0; r < 8; ++r) acc[r] = 0.0f;
+  if constexpr (WF != 0) {
+    if (nch <= 16) {
+      // int4 rows of at most 16 chunks (K <= 512): two lanes per chunk, 16
+      // codes (two words) each, so that every lane works
+      const int hc = lane;                       // half chunk: codes 16 hc .. 16 hc + 15
+      const bool act = hc < 2 * nch;
+      float hv[16];
+#pragma unroll
+      for (int e = 0; e < 16; e += 4) {
+        const float4 h4 = act ? __ldcg(reinterpret_cast<const float4 *>(hj + hc * 16 + e))
+                              : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        hv[e] = h4.x;
+        hv[e + 1] = h4.y;
+        hv[e + 2] = h4.z;
+        hv[e + 3] = h4.w;
+      }
+      float hs = 0.0f;
+      if constexpr (WF == 2)
+#pragma unroll
+        for (int e = 0; e < 16; ++e) hs += hv[e];
+      uint32_t hh[2][4];
+      xpairs_f32(&hv[0], hh[0]);
+      xpairs_f32(&hv[8], hh[1]);
+      const int hcc = act ? hc : 0;   // inactive lanes read a valid word and add 0 (h = 0)
+#pragma unroll
+      for (int r = 0; r < 8; ++r) {
+        const int rr = min(r, nrows - 1 - t0);
+        const uint2 wv = reinterpret_cast<const uint2 *>(wrow + rr * rb)[hcc];
+        uint32_t a0 = hdot8<WF == 1>(wv.x, hh[0], 0u);
+        uint32_t a1 = hdot8<WF == 1>(wv.y, hh[1], 0u);
+        const float qx = hsum4(a0, a1);
+        const float sc = __bfloat162float(__ldg(srow + rr * ng + (hcc >> 2)));
+        if constexpr (WF == 1) {
+          acc[r] = fmaf(sc, qx, acc[r]);
+        } else {
+          const float bc = __bfloat162float(__ldg(brow + rr * ng + (hcc >> 2)));
+          acc[r] = fmaf(sc, qx, fmaf(bc, hs, acc[r]));
+        }
+      }
+#pragma unroll
+      for (int r = 0; r < 8; ++r) acc[r] = warp_sum(acc[r]);
+      if (lane == 0) {
+#pragma unroll
+        for (int r = 0; r < 8; ++r)
+          if (t0 + r < nrows) part[j * p.p3_rows + t0 + r] = acc[r];
+      }
+      return;
+    }
+  }
   for (int c0 = lane; c0 < nch; c0 += 32 * CU) {
     float hv[CU][F::EPC];
 #pragma unroll
