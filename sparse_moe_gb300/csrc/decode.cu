@@ -380,8 +380,11 @@ __device__ __forceinline__ void grid_sync(unsigned long long *bar, unsigned long
 //   part  [(k+1) p3_rows] fp32   per-slot dot products of the CTA's output rows
 //   w3    the CTA's output-projection rows (p3_stage only): k slots of p3_rows
 //         rows of I for the routed experts, then one of p3_rows rows of Is
+//   ws    int4 (p3_scales only): the bf16 group scales of those rows, then
+//         (affine) their biases, in the same order
 struct DecSmem {
   size_t part, w3, w3_sh, unstaged, staged;
+  size_t ws, ws_sh, wb, wb_sh, scaled;
 };
 template <int WF>
 __host__ __device__ __forceinline__ DecSmem dec_smem(int k, int I, int Is, int rows, int H) {
@@ -391,8 +394,26 @@ __host__ __device__ __forceinline__ DecSmem dec_smem(int k, int I, int Is, int r
   L.unstaged = L.w3;
   L.w3_sh = L.w3 + static_cast<size_t>(k) * rows * row_bytes<WF>(I);
   L.staged = L.w3_sh + static_cast<size_t>(rows) * row_bytes<WF>(Is);
+  const size_t sI = static_cast<size_t>(rows) * (I / 64) * 2, sIs = static_cast<size_t>(rows) * (Is / 64) * 2;
+  L.ws = (L.staged + 127) / 128 * 128;
+  L.ws_sh = L.ws + k * sI;
+  L.wb = L.ws_sh + sIs;
+  L.wb_sh = L.wb + (WF == 2 ? k * sI : 0);
+  L.scaled = L.wb_sh + (WF == 2 ? sIs : 0);
   return L;
 }
+
+// Per-CTA state shared by every layer of a launch: the shared-memory carve-up
+// (part, staged output-projection rows), the CTA's output rows and its two
+// mbarriers (shared-expert rows, routed rows; one phase per layer).
+struct DecCta {
+  float *part;
+  unsigned char *w3, *w3_sh;
+  unsigned char *ws, *ws_sh, *wb, *wb_sh;   // staged int4 scales / biases (p3_scales)
+  const uint4 *x_s;   // the layer input in shared memory
+  int n0, n1, nrows, ngroups;
+  uint32_t mb_sh, mb_rt, mb_x;
+};
 
 // One phase-C task: part[j][t0 + r] = (output-projection row n0 + t0 + r of
 // slot j) . h_j for r < 8, slot j < k a routed expert and j = k the shared
@@ -402,7 +423,8 @@ __host__ __device__ __forceinline__ DecSmem dec_smem(int k, int I, int Is, int r
 template <int WF, bool STAGED>
 __device__ __forceinline__ void slot_task(const DecodeParams &p, const float *hbase, int j, int t0,
                                           int n0, int nrows, int expert, float *part,
-                                          const unsigned char *w3, const unsigned char *w3_sh) {
+                                          const unsigned char *w3, const unsigned char *w3_sh,
+                                          const DecCta *cs = nullptr) {
   using F = Fmt<WF>;
   const int lane = threadIdx.x & 31;
   const bool sh = (j == p.k);
@@ -423,6 +445,12 @@ __device__ __forceinline__ void slot_task(const DecodeParams &p, const float *hb
   const __nv_bfloat16 *brow =
       WF == 2 ? static_cast<const __nv_bfloat16 *>(sh ? p.sh_down_bias : p.down_bias) + r0 * ng
               : nullptr;
+  if (STAGED && WF != 0 && cs != nullptr && p.p3_scales) {
+    // the scales (and biases) staged in shared memory beside the rows
+    const size_t so = (sh ? static_cast<size_t>(t0) : static_cast<size_t>(j) * p.p3_rows + t0) * ng * 2;
+    srow = reinterpret_cast<const __nv_bfloat16 *>((sh ? cs->ws_sh : cs->ws) + so);
+    if (WF == 2) brow = reinterpret_cast<const __nv_bfloat16 *>((sh ? cs->wb_sh : cs->wb) + so);
+  }
   // bf16 rows: two chunks per lane per pass, so that both h loads (from L2)
   // are in flight together
   constexpr int CU = WF == 0 ? 2 : 1;
@@ -460,11 +488,11 @@ __device__ __forceinline__ void slot_task(const DecodeParams &p, const float *hb
         uint32_t a0 = hdot8<WF == 1>(wv.x, hh[0], 0u);
         uint32_t a1 = hdot8<WF == 1>(wv.y, hh[1], 0u);
         const float qx = hsum4(a0, a1);
-        const float sc = __bfloat162float(__ldg(srow + rr * ng + (hcc >> 2)));
+        const float sc = __bfloat162float(srow[rr * ng + (hcc >> 2)]);
         if constexpr (WF == 1) {
           acc[r] = fmaf(sc, qx, acc[r]);
         } else {
-          const float bc = __bfloat162float(__ldg(brow + rr * ng + (hcc >> 2)));
+          const float bc = __bfloat162float(brow[rr * ng + (hcc >> 2)]);
           acc[r] = fmaf(sc, qx, fmaf(bc, hs, acc[r]));
         }
       }
@@ -519,11 +547,11 @@ __device__ __forceinline__ void slot_task(const DecodeParams &p, const float *hb
         if constexpr (WF == 0) {
           acc[r] += dot8_bf16_f32(wv, hv[u]);
         } else if constexpr (WF == 1) {
-          const float sc = __bfloat162float(__ldg(srow + rr * ng + (c >> 1)));
+          const float sc = __bfloat162float(srow[rr * ng + (c >> 1)]);
           acc[r] = fmaf(sc, dot32_int4<true>(wv, hh), acc[r]);
         } else {
-          const float sc = __bfloat162float(__ldg(srow + rr * ng + (c >> 1)));
-          const float bc = __bfloat162float(__ldg(brow + rr * ng + (c >> 1)));
+          const float sc = __bfloat162float(srow[rr * ng + (c >> 1)]);
+          const float bc = __bfloat162float(brow[rr * ng + (c >> 1)]);
           acc[r] = fmaf(sc, dot32_int4<false>(wv, hh), fmaf(bc, hs[u], acc[r]));
         }
       }
@@ -558,21 +586,10 @@ template <int WF>
 __device__ __forceinline__ void run_slot_task(const DecodeParams &p, int j, int t0, int n0,
                                               int nrows, int expert, float *part,
                                               const unsigned char *w3,
-                                              const unsigned char *w3_sh) {
-  if (p.p3_stage) slot_task<WF, true>(p, p.h, j, t0, n0, nrows, expert, part, w3, w3_sh);
+                                              const unsigned char *w3_sh, const DecCta *cs) {
+  if (p.p3_stage) slot_task<WF, true>(p, p.h, j, t0, n0, nrows, expert, part, w3, w3_sh, cs);
   else slot_task<WF, false>(p, p.h, j, t0, n0, nrows, expert, part, w3, w3_sh);
 }
-
-// Per-CTA state shared by every layer of a launch: the shared-memory carve-up
-// (part, staged output-projection rows), the CTA's output rows and its two
-// mbarriers (shared-expert rows, routed rows; one phase per layer).
-struct DecCta {
-  float *part;
-  unsigned char *w3, *w3_sh;
-  const uint4 *x_s;   // the layer input in shared memory
-  int n0, n1, nrows, ngroups;
-  uint32_t mb_sh, mb_rt, mb_x;
-};
 
 template <int WF>
 __device__ __forceinline__ DecCta make_dec_cta(const DecodeParams &p, unsigned char *dsm,
@@ -583,6 +600,10 @@ __device__ __forceinline__ DecCta make_dec_cta(const DecodeParams &p, unsigned c
   c.part = reinterpret_cast<float *>(dsm + S.part);
   c.w3 = dsm + S.w3;
   c.w3_sh = dsm + S.w3_sh;
+  c.ws = dsm + S.ws;
+  c.ws_sh = dsm + S.ws_sh;
+  c.wb = dsm + S.wb;
+  c.wb_sh = dsm + S.wb_sh;
   c.n0 = static_cast<int>((static_cast<long long>(blockIdx.x) * p.H) / gridDim.x);
   c.n1 = static_cast<int>((static_cast<long long>(blockIdx.x + 1) * p.H) / gridDim.x);
   c.nrows = c.n1 - c.n0;
@@ -601,8 +622,14 @@ template <int WF>
 __device__ __forceinline__ void layer_prefetch(const DecodeParams &p, const DecCta &c, int gw) {
   if (threadIdx.x == 0 && p.p3_stage) {
     const uint32_t bytes = static_cast<uint32_t>(c.nrows * row_bytes<WF>(p.Is));
-    mbar_arrive_expect_tx(c.mb_sh, bytes);
+    const uint32_t sbytes = p.p3_scales ? static_cast<uint32_t>(c.nrows * (p.Is / 64) * 2) : 0u;
+    mbar_arrive_expect_tx(c.mb_sh, bytes + (WF == 2 ? 2 : 1) * sbytes);
     if (bytes) bulk_copy_g2s(smem_u32(c.w3_sh), row_ptr<WF>(p.sh_down, c.n0, p.Is), bytes, c.mb_sh);
+    if (sbytes) {
+      bulk_copy_g2s(smem_u32(c.ws_sh), scale_row(p.sh_down_scale, c.n0, p.Is), sbytes, c.mb_sh);
+      if (WF == 2)
+        bulk_copy_g2s(smem_u32(c.wb_sh), scale_row(p.sh_down_bias, c.n0, p.Is), sbytes, c.mb_sh);
+    }
   }
   const int nA = p.E + 1 + p.Is;
   if (gw < nA) {
@@ -709,16 +736,24 @@ __device__ __forceinline__ void decode_layer(const DecodeParams &p, const DecCta
   if (warp == kDecWarps - 1 && p.p3_stage) {
     // the k routed experts' output rows n0..n1, one bulk copy per expert
     const uint32_t bytes = static_cast<uint32_t>(nrows * rbI);
+    const uint32_t sbytes = p.p3_scales ? static_cast<uint32_t>(nrows * (p.I / 64) * 2) : 0u;
     if (lane == 0) {
-      mbar_arrive_expect_tx(mb_rt, bytes * p.k);
+      mbar_arrive_expect_tx(mb_rt, (bytes + (WF == 2 ? 2 : 1) * sbytes) * p.k);
       if (bytes)
-        for (int j = 0; j < p.k; ++j)
+        for (int j = 0; j < p.k; ++j) {
+          const size_t r0 = static_cast<size_t>(idx_s[j]) * p.H + n0;
           bulk_copy_g2s(smem_u32(w3 + static_cast<size_t>(j) * p.p3_rows * rbI),
-                        row_ptr<WF>(p.down, static_cast<size_t>(idx_s[j]) * p.H + n0, p.I), bytes,
-                        mb_rt);
+                        row_ptr<WF>(p.down, r0, p.I), bytes, mb_rt);
+          if (sbytes) {
+            const size_t so = static_cast<size_t>(j) * p.p3_rows * (p.I / 64) * 2;
+            bulk_copy_g2s(smem_u32(c.ws + so), scale_row(p.down_scale, r0, p.I), sbytes, mb_rt);
+            if (WF == 2)
+              bulk_copy_g2s(smem_u32(c.wb + so), scale_row(p.down_bias, r0, p.I), sbytes, mb_rt);
+          }
+        }
     }
   }
-  if (WF != 0 && warp == kDecWarps - 2 && nrows > 0) {
+  if (WF != 0 && !p.p3_scales && warp == kDecWarps - 2 && nrows > 0) {
     // int4 group scales (and affine biases) of those rows, into L2 for phase C
     for (int j = 0; j <= p.k; ++j) {
       const bool sh = (j == p.k);
@@ -756,7 +791,7 @@ __device__ __forceinline__ void decode_layer(const DecodeParams &p, const DecCta
       volatile int no_abort = 0;
       mbar_wait_bounded(mb_sh, par, &no_abort, p.status, DEV_TIMEOUT_STAGE);
     }
-    run_slot_task<WF>(p, p.k, 8 * s, n0, nrows, 0, part, w3, w3_sh);
+    run_slot_task<WF>(p, p.k, 8 * s, n0, nrows, 0, part, w3, w3_sh, &c);
   }
   DEC_MARK(5);
   grid_sync(p.bar, bar_base + 2 * static_cast<unsigned long long>(G), p.status);
@@ -781,7 +816,7 @@ __device__ __forceinline__ void decode_layer(const DecodeParams &p, const DecCta
   DEC_MARK(7);
   for (int task = warp; task < p.k * ngroups; task += kDecWarps) {
     const int j = task / ngroups, t0 = (task - j * ngroups) * 8;
-    run_slot_task<WF>(p, j, t0, n0, nrows, idx_s[j], part, w3, w3_sh);
+    run_slot_task<WF>(p, j, t0, n0, nrows, idx_s[j], part, w3, w3_sh, &c);
   }
   __syncthreads();
   DEC_MARK(8);
@@ -1114,7 +1149,17 @@ static void set_p3(DecodeParams &p, int grid, int smem_limit, size_t *smem) {
   p.p3_rows = (p.H + grid - 1) / grid;
   const DecSmem S = dec_smem<WF>(p.k, p.I, p.Is, p.p3_rows, p.H);
   p.p3_stage = S.staged <= static_cast<size_t>(smem_limit) ? 1 : 0;
-  *smem = p.p3_stage ? S.staged : S.unstaged;
+  // int4: stage the rows' scales (and biases) too when their row slices are
+  // whole 16-byte bulk copies (I and Is multiples of 512, 16-byte aligned
+  // bases) and they fit
+  auto a16 = [](const void *q) { return (reinterpret_cast<uintptr_t>(q) & 15) == 0; };
+  const bool aligned = a16(p.down_scale) && a16(p.sh_down_scale) &&
+                       (WF != 2 || (a16(p.down_bias) && a16(p.sh_down_bias)));
+  p.p3_scales = WF != 0 && p.p3_stage && p.I % 512 == 0 && p.Is % 512 == 0 && aligned &&
+                        S.scaled <= static_cast<size_t>(smem_limit)
+                    ? 1
+                    : 0;
+  *smem = p.p3_scales ? S.scaled : p.p3_stage ? S.staged : S.unstaged;
 }
 
 static cudaLaunchConfig_t dec_config(int grid, size_t smem, bool pdl, cudaStream_t stream,
@@ -1193,6 +1238,7 @@ static cudaError_t launch_rows_t(DecodeParams p, int grid, int smem_limit, bool 
                                  cudaStream_t stream) {
   p.p3_rows = (p.H + grid - 1) / grid;
   p.p3_stage = 0;
+  p.p3_scales = 0;
   const RowsSmem S = rows_smem(p.T, p.k, p.H, p.p3_rows);
   (void)smem_limit;
   if (S.total > static_cast<size_t>(g_rows_smem_limit)) return cudaErrorInvalidValue;

@@ -137,6 +137,7 @@ struct DecodeParams {
   unsigned long long *bar;   // grid-barrier arrival counter (16-byte slot, zeroed once)
   int *status;               // device status word
   int p3_rows, p3_stage;     // set by launch_decode_layer
+  int p3_scales;             // set by launch_decode_layer: int4 scales (biases) staged too
   int T;                     // launch_rows: rows of x and y (x, y [T, H]; logits [T, E];
                              // idx, w [T, k]; g [T]; h [T][k + 1][h_ld]); 1 otherwise
 };
