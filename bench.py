@@ -122,10 +122,10 @@ class ClockSampler:
 
 # DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) of
 # the kernels the roofline lines name, from one ncu capture of the current
-# kernels (the summaries under profiles/): gate/up 625.7 + 33.1 MB at the
-# T=4096 prefill workload, decode layer 57.76 + 0.33 MB (bf16) and
+# kernels (the summaries under profiles/): gate/up 628.0 + 33.0 MB at the
+# T=4096 prefill workload, decode layer 57.76 + 0.42 MB (bf16) and
 # 16.19 + 0.00 MB (symmetric int4).  The affine int4 decode was not captured.
-TRAFFIC_BYTES = {"gateup_swiglu_gemm": 658.8e6, "decode_layer": 58.09e6,
+TRAFFIC_BYTES = {"gateup_swiglu_gemm": 661.0e6, "decode_layer": 58.18e6,
                  "decode_layer_int4_sym": 16.19e6}
 
 
