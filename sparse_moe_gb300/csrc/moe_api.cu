@@ -340,11 +340,16 @@ moe_status enqueue_route(moe_ctx *ctx, const LayerSlot &ls, const void *x, int T
   gp.status = ctx->status();
   gp.prefetch = ctx->gemm_prefetch;
   const int tiles = gp.n_blocks_host * gp.m_tiles * gp.k_split;
+  // The token rows of a router tile are consecutive rows of x: they come by
+  // TMA boxes with the weight tile instead of cp.async gathers.
+  CUtensorMap map_x;
+  gp.b_tma = encode_weight_map(&map_x, x, c.hidden, static_cast<uint64_t>(T), kBTmaRows) ? 1 : 0;
   moe_status st;
   {
     ProfScope ps(ctx, K_ROUTER_GEMM, s);
-    st = launched(ctx, launch_tc_gemm(ls.map_router, ls.map_router, ls.map_router, gp, CONV_NONE,
-                                      std::min(ctx->gemm_grid, 2 * tiles), ctx->prefill_pdl, s),
+    st = launched(ctx, launch_tc_gemm(ls.map_router, ls.map_router, gp.b_tma ? map_x : ls.map_router,
+                                      gp, CONV_NONE, std::min(ctx->gemm_grid, 2 * tiles),
+                                      ctx->prefill_pdl, s),
                   "router gemm launch");
   }
   if (st) return st;
