@@ -24,10 +24,12 @@
 //    the epilogue pairs them through a small shared-memory exchange;
 //  * the weight tile (A) of each k-step is one or two TMA boxes (128-byte
 //    swizzle; an L2 prefetch of the next tile's boxes exists but is off by
-//    default, as it measured slower); the token rows (B) are
-//    gathered by a group of warps per pipeline stage with 16-byte cp.async
-//    copies written straight into the same 128-byte-swizzled K-major layout,
-//    so no permuted copy of x is ever written.  (Measured on GB300: TMA
+//    default, as it measured slower); the gate/up GEMM's token rows (B)
+//    are gathered by a group of warps per pipeline stage with 16-byte
+//    cp.async copies written straight into the same 128-byte-swizzled
+//    K-major layout, so no permuted copy of x is ever written; the router's
+//    (x in token order) and the down GEMM's (h in grouped order) are
+//    consecutive rows and come by TMA boxes with the weight tile.  (Measured on GB300: TMA
 //    gather4 moves 512 bytes per request and tops out near 7-18 bytes/clock
 //    per SM; one warp of cp.async sustains about 7 bytes/clock; a single-SM
 //    128 x 256 tile would need 96 bytes/clock, the pair needs 64.)
