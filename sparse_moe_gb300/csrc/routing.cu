@@ -329,59 +329,82 @@ __global__ void __launch_bounds__(256) combine_kernel(const float *__restrict__ 
                                                       const int32_t *__restrict__ pos,
                                                       const float *__restrict__ w, int T, int H,
                                                       int k, __nv_bfloat16 *__restrict__ y) {
-  __shared__ int pos_s[32];
-  __shared__ float w_s[32];
+  // rows and weights of the CTA's current token (buffer it & 1) and of its
+  // next one (k <= 32)
+  __shared__ int pos_s[2][32];
+  __shared__ float w_s[2][32];
   pdl_trigger();
   pdl_wait();
-  const int t = blockIdx.x;
   const int nchunk = H / 8;
-  if (threadIdx.x < k) {
-    pos_s[threadIdx.x] = pos[static_cast<size_t>(t) * k + threadIdx.x];
-    w_s[threadIdx.x] = w[static_cast<size_t>(t) * k + threadIdx.x];
+  const int tid = threadIdx.x;
+  int t = blockIdx.x;
+  if (t < T && tid < k) {
+    pos_s[0][tid] = pos[static_cast<size_t>(t) * k + tid];
+    w_s[0][tid] = w[static_cast<size_t>(t) * k + tid];
   }
   __syncthreads();
-  const float g = __ldg(gate + t);
-  const size_t shared_row = static_cast<size_t>(T) * k + t;
-  for (int c = threadIdx.x; c < nchunk; c += blockDim.x) {
-    float acc[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
-    uint4 ov[KF > 0 ? KF : 1];
-    if constexpr (KF > 0) {
-#pragma unroll
-      for (int j = 0; j < KF; ++j)
-        ov[j] = j < k ? __ldcs(reinterpret_cast<const uint4 *>(o + static_cast<size_t>(pos_s[j]) * H + c * 8))
-                      : make_uint4(0, 0, 0, 0);
+  // tokens t = blockIdx.x, + gridDim.x, ...: one resident wave of CTAs; the
+  // next token's rows are read while this token's outputs stream
+  for (int it = 0; t < T; t += gridDim.x, ++it) {
+    const int buf = it & 1;
+    const int tn = t + gridDim.x;
+    const bool pre = tn < T && tid < k;
+    int pos_n = 0;
+    float w_n = 0.0f;
+    if (pre) {
+      pos_n = __ldg(pos + static_cast<size_t>(tn) * k + tid);
+      w_n = __ldg(w + static_cast<size_t>(tn) * k + tid);
     }
-    const uint4 sv = __ldcs(reinterpret_cast<const uint4 *>(o + shared_row * H + c * 8));
-    auto add = [&](const uint4 oj, float wj) {
-      const uint32_t oa[4] = {oj.x, oj.y, oj.z, oj.w};
+    const float g = __ldg(gate + t);
+    const size_t shared_row = static_cast<size_t>(T) * k + t;
+    for (int c = tid; c < nchunk; c += blockDim.x) {
+      float acc[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+      uint4 ov[KF > 0 ? KF : 1];
+      if constexpr (KF > 0) {
+#pragma unroll
+        for (int j = 0; j < KF; ++j)
+          ov[j] = j < k ? __ldcs(reinterpret_cast<const uint4 *>(o + static_cast<size_t>(pos_s[buf][j]) * H + c * 8))
+                        : make_uint4(0, 0, 0, 0);
+      }
+      const uint4 sv = __ldcs(reinterpret_cast<const uint4 *>(o + shared_row * H + c * 8));
+      auto add = [&](const uint4 oj, float wj) {
+        const uint32_t oa[4] = {oj.x, oj.y, oj.z, oj.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float2 f = half2_to_float2(oa[i]);
+          acc[2 * i] = fmaf(wj, f.x, acc[2 * i]);
+          acc[2 * i + 1] = fmaf(wj, f.y, acc[2 * i + 1]);
+        }
+      };
+      if constexpr (KF > 0) {
+#pragma unroll
+        for (int j = 0; j < KF; ++j)
+          if (j < k) add(ov[j], w_s[buf][j]);
+      } else {
+        for (int j = 0; j < k; ++j)
+          add(*reinterpret_cast<const uint4 *>(o + static_cast<size_t>(pos_s[buf][j]) * H + c * 8),
+              w_s[buf][j]);
+      }
+      const uint32_t sa[4] = {sv.x, sv.y, sv.z, sv.w};
+      uint4 out;
+      uint32_t *oo = reinterpret_cast<uint32_t *>(&out);
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const float2 f = half2_to_float2(oa[i]);
-        acc[2 * i] = fmaf(wj, f.x, acc[2 * i]);
-        acc[2 * i + 1] = fmaf(wj, f.y, acc[2 * i + 1]);
+        const float2 f = half2_to_float2(sa[i]);
+        const float lo = fmaf(g, f.x, acc[2 * i]);
+        const float hi = fmaf(g, f.y, acc[2 * i + 1]);
+        oo[i] = pack_bf16x2(lo, hi);
       }
-    };
-    if constexpr (KF > 0) {
-#pragma unroll
-      for (int j = 0; j < KF; ++j)
-        if (j < k) add(ov[j], w_s[j]);
-    } else {
-      for (int j = 0; j < k; ++j)
-        add(*reinterpret_cast<const uint4 *>(o + static_cast<size_t>(pos_s[j]) * H + c * 8), w_s[j]);
+      *reinterpret_cast<uint4 *>(y + static_cast<size_t>(t) * H + c * 8) = out;
     }
-    const uint32_t sa[4] = {sv.x, sv.y, sv.z, sv.w};
-    uint4 out;
-    uint32_t *oo = reinterpret_cast<uint32_t *>(&out);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float2 f = half2_to_float2(sa[i]);
-      const float lo = fmaf(g, f.x, acc[2 * i]);
-      const float hi = fmaf(g, f.y, acc[2 * i + 1]);
-      oo[i] = pack_bf16x2(lo, hi);
+    // buffer buf ^ 1 was last read before the previous iteration's barrier
+    if (pre) {
+      pos_s[buf ^ 1][tid] = pos_n;
+      w_s[buf ^ 1][tid] = w_n;
     }
-    *reinterpret_cast<uint4 *>(y + static_cast<size_t>(t) * H + c * 8) = out;
+    __syncthreads();
   }
 }
 
@@ -389,11 +412,28 @@ cudaError_t launch_combine(const float *gate, const void *o, const int32_t *pos,
                            int T, int H, int k, void *y, bool pdl, cudaStream_t stream) {
   const __half *oh = reinterpret_cast<const __half *>(o);
   __nv_bfloat16 *yb = reinterpret_cast<__nv_bfloat16 *>(y);
+  // one resident wave: SMs x CTAs of this kernel per SM (cached per device)
+  static int waves[64][2] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const int kf = k <= 8 ? 0 : 1;
+  int &wave = waves[dev & 63][kf];
+  if (wave == 0) {
+    int sms = 0, per_sm = 0;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+      return e;
+    e = kf == 0 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, combine_kernel<8>, 256, 0)
+                : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, combine_kernel<0>, 256, 0);
+    if (e != cudaSuccess) return e;
+    wave = std::max(1, sms * per_sm);
+  }
+  const int grid = std::max(1, std::min(T, wave));
   if (k <= 8)
-    return launch_kernel(combine_kernel<8>, dim3(T), dim3(256), 0, stream, pdl, gate, oh, pos, w, T,
-                         H, k, yb);
-  return launch_kernel(combine_kernel<0>, dim3(T), dim3(256), 0, stream, pdl, gate, oh, pos, w, T, H,
-                       k, yb);
+    return launch_kernel(combine_kernel<8>, dim3(grid), dim3(256), 0, stream, pdl, gate, oh, pos, w,
+                         T, H, k, yb);
+  return launch_kernel(combine_kernel<0>, dim3(grid), dim3(256), 0, stream, pdl, gate, oh, pos, w, T,
+                       H, k, yb);
 }
 
 // bf16 -> fp16 copy of a weight array, 8 elements (16 bytes) per thread and
