@@ -1016,15 +1016,39 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
           }
         }
       } else {  // MODE_ROUTER: fp32 logits (split-K part t.split), 128 contiguous bytes per column
-        const int e = t.out_base + q * 32 + lane;
+        const int e0 = t.out_base + q * 32;   // the warp's 32 experts, one per lane
+        const int e = e0 + lane;
         float *lout = reinterpret_cast<float *>(p.out) + t.split * p.out_split_stride;
         const float bias =
             (p.bias != nullptr && e < p.n_experts && t.split == 0) ? __ldg(p.bias + e) : 0.0f;
+        // 8 tokens x 32 experts at a time through the warp's staging area,
+        // then 16-byte stores: a quarter of the store instructions of one
+        // 4-byte store per lane and token
+        const bool vec = e0 + 32 <= p.n_experts && (p.out_ld & 3) == 0 &&
+                         (reinterpret_cast<uintptr_t>(lout) & 15) == 0;
+        float *sf = reinterpret_cast<float *>(my_stage);   // [8 tokens][32 experts]
         for (int c0 = 0; c0 < t.nmma; c0 += 16) {
           uint32_t r[16];
           tmem_ld16(tacc + c0, r);
           tmem_ld_wait();
-          if (e < p.n_experts) {
+          if (vec) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+#pragma unroll
+              for (int cc = 0; cc < 8; ++cc) sf[cc * 32 + lane] = __uint_as_float(r[h * 8 + cc]) + bias;
+              __syncwarp();
+#pragma unroll
+              for (int i = 0; i < 2; ++i) {
+                const int f = i * 32 + lane;            // float4 f of the 8 x 32 tile
+                const int row = f >> 3, col = (f & 7) * 4;
+                const int tok = c0 + h * 8 + row;
+                if (tok < t.nrows)
+                  *reinterpret_cast<float4 *>(lout + static_cast<size_t>(t.row0 + tok) * p.out_ld + e0 + col) =
+                      *reinterpret_cast<const float4 *>(sf + row * 32 + col);
+              }
+              __syncwarp();
+            }
+          } else if (e < p.n_experts) {
 #pragma unroll
             for (int cc = 0; cc < 16; ++cc)
               if (c0 + cc < t.nrows)
