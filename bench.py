@@ -125,7 +125,7 @@ class ClockSampler:
 # kernels (the summaries under profiles/): gate/up 628.0 + 33.0 MB at the
 # T=4096 prefill workload, decode layer 57.76 + 0.42 MB (bf16) and
 # 16.19 + 0.00 MB (symmetric int4).  The affine int4 decode was not captured.
-TRAFFIC_BYTES = {"gateup_swiglu_gemm": 661.0e6, "decode_layer": 58.18e6,
+TRAFFIC_BYTES = {"gateup_swiglu_gemm": 661.4e6, "decode_layer": 58.18e6,
                  "decode_layer_int4_sym": 16.19e6}
 
 
