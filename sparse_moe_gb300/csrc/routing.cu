@@ -412,22 +412,22 @@ cudaError_t launch_combine(const float *gate, const void *o, const int32_t *pos,
                            int T, int H, int k, void *y, bool pdl, cudaStream_t stream) {
   const __half *oh = reinterpret_cast<const __half *>(o);
   __nv_bfloat16 *yb = reinterpret_cast<__nv_bfloat16 *>(y);
-  // one resident wave: SMs x CTAs of this kernel per SM (cached per device)
-  static int waves[64][2] = {};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  const int kf = k <= 8 ? 0 : 1;
-  int &wave = waves[dev & 63][kf];
-  if (wave == 0) {
-    int sms = 0, per_sm = 0;
-    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
-      return e;
-    e = kf == 0 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, combine_kernel<8>, 256, 0)
-                : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, combine_kernel<0>, 256, 0);
-    if (e != cudaSuccess) return e;
-    wave = std::max(1, sms * per_sm);
-  }
+  // one resident wave: SMs x CTAs of the kernel per SM (the latter depends
+  // only on the kernel and the architecture; computed once, thread-safely)
+  static const int per_sm8 = [] {
+    int n = 0;
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, combine_kernel<8>, 256, 0) == cudaSuccess ? n : 1;
+  }();
+  static const int per_sm0 = [] {
+    int n = 0;
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, combine_kernel<0>, 256, 0) == cudaSuccess ? n : 1;
+  }();
+  int dev = 0, sms = 0;
+  cudaError_t e;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess ||
+      (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+    return e;
+  const int wave = std::max(1, sms * std::max(1, k <= 8 ? per_sm8 : per_sm0));
   const int grid = std::max(1, std::min(T, wave));
   if (k <= 8)
     return launch_kernel(combine_kernel<8>, dim3(grid), dim3(256), 0, stream, pdl, gate, oh, pos, w,
