@@ -23,6 +23,14 @@ def test_route_tiny_shapes(T):
     check_routing(ctx, w, x)
 
 
+def test_route_qwen_8192_row_chunk():
+    # one chunk of 8192 rows: 256 routing blocks, twice the default chunk's
+    wl = _wl(moe_synth.QWEN, 8192, bias=1.5, seed=81)
+    ctx, (w,) = make_ctx(wl, max_chunk_rows=8192)
+    x = moe_synth.make_x(wl, device="cuda")
+    check_routing(ctx, w, x)
+
+
 @pytest.mark.parametrize("T", [1, 300, 4096])
 def test_route_qwen_shape(T):
     wl = moe_synth.PREFILL_BF16 if T == 4096 else _wl(moe_synth.QWEN, T, bias=1.5, seed=T)
