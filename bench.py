@@ -636,6 +636,17 @@ def main_reference(args):
     return 0
 
 
+def replicas_rate(total_ms, world, tokens_per_step, steps, device):
+    """Whole-job rate of `world` independent replicas: the slowest rank's
+    timed region (max over ranks) and all ranks' tokens over it.  Returns
+    (max total ms, tokens/s)."""
+    if world > 1:
+        t = torch.tensor([float(total_ms)], dtype=torch.float64, device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    return total_ms, world * tokens_per_step * steps / (total_ms * 1e-3)
+
+
 def main(args):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -675,13 +686,9 @@ def main(args):
     total_ms, prof, launches = run_prefill(ctx, x, y, args.steps, args.warmup, flush, stream,
                                            clocks)
     torch.cuda.synchronize()
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms, value = replicas_rate(total_ms, world, wl.T, args.steps, dev)
     clk = clocks.stop()
     ms_step = total_ms / args.steps
-    value = world * wl.T * args.steps / (total_ms * 1e-3)
 
     gu_f, dn_f, rt_f = algorithmic(s, wl.T)
     kern = {k: {"launches": v[0], "avg_us": v[1] * 1e3 / max(1, v[0])} for k, v in prof.items()}
