@@ -33,25 +33,6 @@ namespace moe {
 constexpr int kDecLayerThreads = 512;
 constexpr int kDecWarps = kDecLayerThreads / 32;
 
-// Optional phase timestamps (compiled only with -DMOE_TRACE): per CTA, clock64
-// at each phase boundary of the last decode launch, read back with
-// moe_debug_read_decode_trace().
-#ifdef MOE_TRACE
-__device__ long long g_dec_trace[1024][16];
-// global-timer stamps per launch (ring of 64 launches, by barrier epoch):
-// [start, after the programmatic-launch wait, end] per CTA
-__device__ unsigned long long g_dec_gt[64][160][3];
-__device__ __forceinline__ unsigned long long gtimer() {
-  unsigned long long t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-#define DEC_MARK(i) \
-  if (threadIdx.x == 0) g_dec_trace[blockIdx.x & 1023][i] = clock64()
-#else
-#define DEC_MARK(i)
-#endif
-
 __device__ __forceinline__ uint4 ld_stream(const void *p) {
   uint4 v;
   asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
@@ -703,9 +684,7 @@ __device__ __forceinline__ void decode_layer(const DecodeParams &p, const DecCta
       if (lane == 0) hg[static_cast<size_t>(p.k) * p.h_ld + i] = silu_f(d[0]) * d[1];
     }
   }
-  DEC_MARK(1);
   grid_sync(p.bar, bar_base + G, p.status);
-  DEC_MARK(2);
 
   // ---- top-k (one warp per CTA; the logits are in L2)
   if (warp == 0) {
@@ -731,7 +710,6 @@ __device__ __forceinline__ void decode_layer(const DecodeParams &p, const DecCta
     if (lane == 0) w_s[32] = g;
   }
   __syncthreads();
-  DEC_MARK(3);
   // The last warps have the fewest phase-B rows: they issue the copies.
   if (warp == kDecWarps - 1 && p.p3_stage) {
     // the k routed experts' output rows n0..n1, one bulk copy per expert
@@ -768,7 +746,6 @@ __device__ __forceinline__ void decode_layer(const DecodeParams &p, const DecCta
       }
     }
   }
-  DEC_MARK(4);
 
   // ---- phase B: routed gate/up row pairs -> h
   const int nB = p.k * p.I;
@@ -793,9 +770,7 @@ __device__ __forceinline__ void decode_layer(const DecodeParams &p, const DecCta
     }
     run_slot_task<WF>(p, p.k, 8 * s, n0, nrows, 0, part, w3, w3_sh, &c);
   }
-  DEC_MARK(5);
   grid_sync(p.bar, bar_base + 2 * static_cast<unsigned long long>(G), p.status);
-  DEC_MARK(6);
   // The next layer's routing-independent weight traffic can start now: this
   // layer's shared-expert rows are consumed (phase B) and DRAM is idle from
   // here on.
@@ -813,13 +788,11 @@ __device__ __forceinline__ void decode_layer(const DecodeParams &p, const DecCta
     volatile int no_abort = 0;
     mbar_wait_bounded(mb_rt, par, &no_abort, p.status, DEV_TIMEOUT_STAGE);
   }
-  DEC_MARK(7);
   for (int task = warp; task < p.k * ngroups; task += kDecWarps) {
     const int j = task / ngroups, t0 = (task - j * ngroups) * 8;
     run_slot_task<WF>(p, j, t0, n0, nrows, idx_s[j], part, w3, w3_sh, &c);
   }
   __syncthreads();
-  DEC_MARK(8);
   // y[n] = sum_j w_j part[j] + g part[k], in that order
   for (int t = threadIdx.x; t < nrows; t += kDecLayerThreads) {
     float y = 0.0f;
@@ -851,10 +824,6 @@ __global__ void __launch_bounds__(kDecLayerThreads, 1) decode_layer_kernel(const
   const int G = gridDim.x;
   const int gw = (threadIdx.x >> 5) * G + blockIdx.x;
 
-  DEC_MARK(0);
-#ifdef MOE_TRACE
-  const unsigned long long gt_start = gtimer();
-#endif
   unsigned long long base = 0;   // barrier counter at launch (used by thread 0)
   if (threadIdx.x == 0) {
     // With a programmatic launch this CTA can start while the previous
@@ -876,16 +845,6 @@ __global__ void __launch_bounds__(kDecLayerThreads, 1) decode_layer_kernel(const
   pdl_trigger();
   pdl_wait();
   decode_layer<WF, R>(p, c, 0u, base, nullptr, idx_s, w_s);
-  DEC_MARK(9);
-  DEC_MARK(10);
-#ifdef MOE_TRACE
-  if (threadIdx.x == 0 && blockIdx.x < 160) {
-    const int slot = static_cast<int>((base / (2ull * G)) % 64);
-    g_dec_gt[slot][blockIdx.x][0] = gt_start;
-    g_dec_gt[slot][blockIdx.x][2] = gtimer();
-  }
-  if (threadIdx.x == 0) g_dec_trace[blockIdx.x & 1023][15] = p.p3_stage + 10 * p.p3_rows;
-#endif
 }
 
 // The same for n consecutive layers in one launch (P.layer[0..n-1], same
@@ -1317,13 +1276,3 @@ int decode_layer_grid(int num_sms) {
 
 }  // namespace moe
 
-#ifdef MOE_TRACE
-extern "C" int moe_debug_read_decode_gt(void *dst, size_t bytes) {
-  size_t n = bytes < sizeof(moe::g_dec_gt) ? bytes : sizeof(moe::g_dec_gt);
-  return cudaMemcpyFromSymbol(dst, moe::g_dec_gt, n) == cudaSuccess ? 0 : 1;
-}
-extern "C" int moe_debug_read_decode_trace(void *dst, size_t bytes) {
-  size_t n = bytes < sizeof(moe::g_dec_trace) ? bytes : sizeof(moe::g_dec_trace);
-  return cudaMemcpyFromSymbol(dst, moe::g_dec_trace, n) == cudaSuccess ? 0 : 1;
-}
-#endif

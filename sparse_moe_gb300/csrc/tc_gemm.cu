@@ -59,26 +59,6 @@
 
 namespace moe {
 
-// Optional wait-time tracing (compiled only with -DMOE_TRACE): per CTA, clock
-// cycles each role spends waiting on each barrier, read back with
-// moe_debug_read_trace().
-#ifdef MOE_TRACE
-__device__ unsigned long long g_moe_trace[3][1024][16];
-#define MOE_T0() const long long _t0 = clock64()
-#define MOE_TADD(slot)                                        \
-  atomicAdd(&g_moe_trace[p.mode][blockIdx.x & 1023][slot], \
-            static_cast<unsigned long long>(clock64() - _t0))
-#define MOE_TSTAMP(var) const long long var = clock64()
-#define MOE_TSPAN(slot, a, b)                                  \
-  atomicAdd(&g_moe_trace[p.mode][blockIdx.x & 1023][slot], \
-            static_cast<unsigned long long>((b) - (a)))
-#else
-#define MOE_T0()
-#define MOE_TADD(slot)
-#define MOE_TSTAMP(var)
-#define MOE_TSPAN(slot, a, b)
-#endif
-
 constexpr int BM = 128;                 // A rows per CTA (MMA M = 256 per pair)
 constexpr int PAIR_M = 2 * BM;
 constexpr int BK = 64;                  // K per pipeline stage (128-byte rows)
@@ -448,12 +428,10 @@ __device__ __forceinline__ bool convert_stage_int4(const GemmParams &p, int q,
   const uint32_t cph = static_cast<uint32_t>(it / kCodeSlots) & 1u;
   const uint32_t tile = smem_base + stage * STAGE_BYTES;
   int got = 1;
-  MOE_TSTAMP(tc0);
   if (lane == 0)
     got = mbar_wait_bounded(smem_u32(&tail->cfull[slot]), cph, abort_flag, p.status,
                             DEV_TIMEOUT_CONVERTER);
   if (!__shfl_sync(0xffffffffu, got, 0)) return false;
-  MOE_TSTAMP(tc1);
   uint32_t w[kInt4Batches][8];
 #pragma unroll
   for (int b = 0; b < kInt4Batches; ++b)
@@ -465,14 +443,12 @@ __device__ __forceinline__ bool convert_stage_int4(const GemmParams &p, int q,
                             DEV_TIMEOUT_CONVERTER);
   }
   if (!__shfl_sync(0xffffffffu, got, 0)) return false;
-  MOE_TSTAMP(tc2);
 #pragma unroll
   for (int b = 0; b < kInt4Batches; ++b)
     expand_rows_int4<conv_to_f16(CONV), conv_affine(CONV)>(tile, w[b], q * kInt4Batches + b,
                                                            sv[b], bv[b], lane);
   fence_proxy_async_smem();
   __syncwarp();
-  MOE_TSTAMP(tc3);
   if (lane == 0) {
     // one converter per CTA checks the token rows: the leader's ready phase
     // needs every converter's arrival
@@ -481,15 +457,6 @@ __device__ __forceinline__ bool convert_stage_int4(const GemmParams &p, int q,
                               DEV_TIMEOUT_CONVERTER);
     if (got) arrive_ready(tail, stage, rank);
   }
-#ifdef MOE_TRACE
-  if (lane == 0) {
-    MOE_TSTAMP(tc4);
-    MOE_TSPAN(12, tc0, tc1);   // wait for codes
-    MOE_TSPAN(13, tc1, tc2);   // codes to registers + wait for the stage's A region
-    MOE_TSPAN(14, tc2, tc3);   // expansion
-    MOE_TSPAN(15, tc3, tc4);   // (last converter) wait for token rows
-  }
-#endif
   return __shfl_sync(0xffffffffu, got, 0) != 0;
 }
 
@@ -562,9 +529,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
   pdl_wait();   // inputs (block list, token rows) written by earlier kernels
   const uint32_t tmem_base = tail->tmem_base;
   const int ntiles = num_tiles(p);
-#ifdef MOE_TRACE
-  const long long t_kernel0 = clock64();
-#endif
 
   if (warp == TMA_WARP) {
     // ------------------------------------------------ weight tiles (TMA) --
@@ -592,13 +556,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       if (lane == 0) {
         const CUtensorMap *amap = t.shared ? &map_a_shared : &map_a_routed;
         for (int ks = 0; ks < t.nk; ++ks) {
-          MOE_T0();
           const uint32_t free_bar = INT4 ? smem_u32(&tail->cempty[stage]) : smem_u32(&tail->empty[stage]);
           if (!mbar_wait_bounded(free_bar, phase ^ 1, abort_flag, p.status, DEV_TIMEOUT_PRODUCER)) {
             ok = 0;
             break;
           }
-          MOE_TADD(0);
           const uint32_t full_bar = smem_u32(&tail->full[stage]);
           const uint32_t a_dst = smem_base + stage * STAGE_BYTES;
           // b_tma: this CTA's nmma / 2 token rows, in boxes of kBTmaRows
@@ -722,9 +684,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         }
         const uint32_t phase = static_cast<uint32_t>(it / STAGES) & 1u;
         int got = 1;
-#ifdef MOE_TRACE
-        const long long tb0 = clock64();
-#endif
         if (lane == 0)
           got = mbar_wait_bounded(empty_bar, phase ^ 1, abort_flag, p.status, DEV_TIMEOUT_PRODUCER);
         got = __shfl_sync(0xffffffffu, got, 0);
@@ -732,9 +691,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
           ok = false;
           break;
         }
-#ifdef MOE_TRACE
-        const long long tb1 = clock64();
-#endif
         if (conv_int4(CONV) && gq == 0 && lane == 0) {
           // int4: the TMA warp streams codes only; this CTA's token-row boxes
           // (down: h rows, consecutive) come from here, on the full barrier
@@ -753,19 +709,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
           cp_async16(dst, bsrc + rows_tab[e] + kc, 16u);
         }
         cp_async_commit();
-#ifdef MOE_TRACE
-        const long long tb2 = clock64();
-#endif
         cp_async_wait<0>();
-#ifdef MOE_TRACE
-        if (lane == 0) {
-          const long long tb3 = clock64();
-          atomicAdd(&g_moe_trace[p.mode][blockIdx.x & 1023][8], static_cast<unsigned long long>(tb1 - tb0));
-          atomicAdd(&g_moe_trace[p.mode][blockIdx.x & 1023][9], static_cast<unsigned long long>(tb2 - tb1));
-          atomicAdd(&g_moe_trace[p.mode][blockIdx.x & 1023][10], static_cast<unsigned long long>(tb3 - tb2));
-          atomicAdd(&g_moe_trace[p.mode][blockIdx.x & 1023][11], 1ull);
-        }
-#endif
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
@@ -802,10 +746,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
           const Tile t = decode_tile(p, tile, 0);
           if (!t.valid) continue;
           {
-            MOE_T0();
             const bool w_ok = mbar_wait_bounded_cluster(smem_u32(&tail->tmem_empty[acc]), aphase ^ 1,
                                                         abort_flag, p.status, DEV_TIMEOUT_MMA);
-            MOE_TADD(3);
             if (!w_ok) {
               ok = false;
               break;
@@ -816,7 +758,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
           const bool f16 = conv_to_f16(CONV) || (CONV == CONV_NONE && p.ab_f16);
           const uint32_t idesc = f16 ? idesc_f16_f32(PAIR_M, t.nmma) : idesc_bf16_f32(PAIR_M, t.nmma);
           for (int ks = 0; ks < t.nk; ++ks) {
-            MOE_T0();
             // unconverted modes: both CTAs' producers signal this CTA's full
             // barrier directly; otherwise the stage finishers' ready barrier
             const uint32_t stage_bar = CONV == CONV_NONE ? smem_u32(&tail->full[stage])
@@ -826,15 +767,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
             // than a cluster-scope acquire)
             const bool r_ok = mbar_wait_bounded(stage_bar, phase, abort_flag, p.status,
                                                 DEV_TIMEOUT_MMA);
-            MOE_TADD(2);
             if (!r_ok) {
               ok = false;
               break;
             }
             tc_fence_after();
-#ifdef MOE_TRACE
-            const long long _ti = clock64();
-#endif
             const uint32_t a_addr = smem_base + stage * STAGE_BYTES;
             const uint64_t a_desc = smem_desc_sw128(a_addr);
             const uint64_t b_desc = smem_desc_sw128(a_addr + A_BYTES);
@@ -842,10 +779,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
             for (int kk = 0; kk < BK / 16; ++kk)
               tc_mma_pair(d_tmem, a_desc + 2 * kk, b_desc + 2 * kk, idesc, (ks | kk) != 0);
             tc_commit_pair_mc(smem_u32(&tail->empty[stage]), 0x3);
-#ifdef MOE_TRACE
-            atomicAdd(&g_moe_trace[p.mode][blockIdx.x & 1023][1],
-                      static_cast<unsigned long long>(clock64() - _ti));
-#endif
             if (++stage == STAGES) {
               stage = 0;
               phase ^= 1;
@@ -937,10 +870,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       if (!t.valid) continue;
       int got = 1;
       if (lane == 0) {
-        MOE_T0();
         got = mbar_wait_bounded(smem_u32(&tail->tmem_full[acc]), aphase, abort_flag, p.status,
                                 DEV_TIMEOUT_EPILOGUE);
-        if (ew == 0) MOE_TADD(4);
       }
       got = __shfl_sync(0xffffffffu, got, 0);
       // Agree across the four epilogue warps before any named barrier.
@@ -951,9 +882,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       if (!all_ok) break;
       tc_fence_after();
       const uint32_t tacc = tmem_base + acc * ACC_COLS + (static_cast<uint32_t>(q * 32) << 16);
-#ifdef MOE_TRACE
-      const long long _te = clock64();
-#endif
 
       if (p.mode == MODE_GATEUP) {
         // Lanes 0..63 of this CTA's accumulator hold gate rows, 64..127 the
@@ -1059,11 +987,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       }
       tc_fence_before();
       __syncwarp();
-#ifdef MOE_TRACE
-      if (lane == 0 && ew == 0)
-        atomicAdd(&g_moe_trace[p.mode][blockIdx.x & 1023][5],
-                  static_cast<unsigned long long>(clock64() - _te));
-#endif
       if (lane == 0) {
         if (rank == 0) mbar_arrive(smem_u32(&tail->tmem_empty[acc]));
         else mbar_arrive_cluster(tmem_empty0 + acc * 8);
@@ -1079,13 +1002,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
   __syncthreads();
   cluster_sync_all();   // the pair's MMAs and epilogues are done in both CTAs
   tc_fence_after();
-#ifdef MOE_TRACE
-  if (threadIdx.x == 0) {
-    atomicAdd(&g_moe_trace[p.mode][blockIdx.x & 1023][6],
-              static_cast<unsigned long long>(clock64() - t_kernel0));
-    atomicAdd(&g_moe_trace[p.mode][blockIdx.x & 1023][7], 1ull);
-  }
-#endif
   if (warp == MMA_WARP) tmem_dealloc_pair(tmem_base, TMEM_COLS);
 }
 
@@ -1226,14 +1142,3 @@ cudaError_t launch_tc_gemm(const CUtensorMap &a_routed, const CUtensorMap &a_sha
 
 }  // namespace moe
 
-#ifdef MOE_TRACE
-extern "C" int moe_debug_read_trace(void *dst, size_t bytes, int clear) {
-  size_t n = bytes < sizeof(moe::g_moe_trace) ? bytes : sizeof(moe::g_moe_trace);
-  if (cudaMemcpyFromSymbol(dst, moe::g_moe_trace, n) != cudaSuccess) return 1;
-  if (clear) {
-    static unsigned long long zeros[3][1024][16];
-    if (cudaMemcpyToSymbol(moe::g_moe_trace, zeros, sizeof(zeros)) != cudaSuccess) return 2;
-  }
-  return 0;
-}
-#endif
