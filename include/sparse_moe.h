@@ -272,9 +272,19 @@ moe_status moe_forward_decode_host(moe_ctx *ctx, int layer, const void *x_host,
  *   Set-up: the first call on each device looks up the array's device
  *   address (with that device current) and raises the decode kernel's
  *   shared-memory limit; make that first call before any stream capture.
+ *   The cached set-up belongs to the device's primary context: it assumes
+ *   one primary context per device for the life of the process (no
+ *   cudaDeviceReset between calls).
  *   Sharing: every call uses the same array, which keeps the previous call's
  *   contents; calls that overlap on the GPU (different streams, or several
  *   host threads) race on it, so serialise them.
+ *   Launch: programmatic dependent launch is on unless the environment
+ *   variable MOE_DECODE_PDL is 0 when the first call on a device is made, the
+ *   same switch as a context's decode launches.
+ *   Device waits: the call returns before its kernel runs, so a bounded wait
+ *   that runs out cannot change its return value; the kernel records the
+ *   site in a status word inside the array, which moe_check_device(NULL,
+ *   &code) reads and clears.
  * Returns MOE_ERR_INVALID_ARG for bad arguments, MOE_ERR_UNSUPPORTED for
  * shapes the decode kernels do not take, MOE_ERR_CUDA if a CUDA call fails. */
 moe_status moe_forward_decode_noalloc(const moe_config *cfg, const moe_weights *w,
@@ -305,7 +315,9 @@ moe_status moe_dequant_int4(const void *codes, const void *scale, const void *bi
 
 /* Synchronises the device, reads and clears the device status word: MOE_OK,
  * or MOE_ERR_DEVICE_TIMEOUT (a bounded wait ran out; *code, if non-NULL,
- * receives the site code), or MOE_ERR_CUDA. */
+ * receives the site code), or MOE_ERR_CUDA.  With ctx = NULL it does the
+ * same for the status word of moe_forward_decode_noalloc on the current
+ * device. */
 moe_status moe_check_device(moe_ctx *ctx, int32_t *code);
 
 /* Per-kernel timing with CUDA events recorded on the launching stream. */

@@ -10,6 +10,7 @@
 // words) live in one file-scope device array instead of a workspace.  The
 // array is part of the loaded library: every device that loads it holds
 // kNoAllocScratchBytes until the process exits.
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -27,12 +28,17 @@ std::mutex g_setup_mutex;
 unsigned char *g_scratch_addr[kMaxDevices] = {};   // device address of the array, per device
 int g_grid[kMaxDevices] = {};                       // cooperative decode grid, per device
 int g_smem_limit[kMaxDevices] = {};                 // decode kernel's shared-memory limit, per device
+int g_pdl[kMaxDevices] = {};                        // 1 + programmatic dependent launch flag, per device
 
 size_t align256(size_t v) { return (v + 255) / 256 * 256; }
 
 struct ScratchLayout {
   size_t logits, idx, w, g, h, counter, status, total;
 };
+
+// The status word sits at a fixed offset (the start of the array), whatever
+// the shape of the call that wrote it, so that it can be read without one.
+constexpr size_t kStatusOffset = 0;
 
 ScratchLayout scratch_layout(const moe_config &c) {
   ScratchLayout L{};
@@ -43,13 +49,13 @@ ScratchLayout scratch_layout(const moe_config &c) {
     return at;
   };
   const size_t imax = static_cast<size_t>(c.inter > c.shared_inter ? c.inter : c.shared_inter);
+  L.status = take(16);
   L.logits = take(static_cast<size_t>(c.n_experts) * 4);
   L.idx = take(static_cast<size_t>(c.top_k) * 4);
   L.w = take(static_cast<size_t>(c.top_k) * 4);
   L.g = take(4);
   L.h = take(moe::decode_h_floats(c.top_k, static_cast<int>(imax)) * 4);
   L.counter = take(16);
-  L.status = take(16);
   L.total = off;
   return L;
 }
@@ -92,9 +98,13 @@ extern "C" moe_status moe_forward_decode_noalloc(const moe_config *cfg, const mo
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
   unsigned char *base = nullptr;
   int grid = 0, smem_limit = 0;
+  bool pdl = true;
   {
     // Set-up, once per device and with that device current: the host-side
     // name of the array is not a device address, so ask the runtime for it.
+    // What is cached here (the address, the grid, the shared-memory opt-in)
+    // belongs to the device's primary context: it stays valid as long as the
+    // process keeps that context (no cudaDeviceReset in between).
     std::lock_guard<std::mutex> lock(g_setup_mutex);
     if (!g_scratch_addr[dev]) {
       void *ptr = nullptr;
@@ -112,9 +122,16 @@ extern "C" moe_status moe_forward_decode_noalloc(const moe_config *cfg, const mo
       if (moe::decode_configure(&limit) != cudaSuccess) return MOE_ERR_CUDA;
       g_smem_limit[dev] = limit;
     }
+    if (!g_pdl[dev]) {
+      // the same switch as a context's decode launches (MOE_DECODE_PDL=0
+      // turns programmatic dependent launch off), read once per device
+      const char *env = std::getenv("MOE_DECODE_PDL");
+      g_pdl[dev] = 1 + ((env && std::atoi(env) == 0) ? 0 : 1);
+    }
     base = g_scratch_addr[dev];
     grid = g_grid[dev];
     smem_limit = g_smem_limit[dev];
+    pdl = g_pdl[dev] == 2;
   }
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -154,6 +171,30 @@ extern "C" moe_status moe_forward_decode_noalloc(const moe_config *cfg, const mo
   p.h_ld = imax;
   p.bar = reinterpret_cast<unsigned long long *>(base + L.counter);
   p.status = reinterpret_cast<int *>(base + L.status);
-  if (moe::launch_decode_layer(p, grid, smem_limit, true, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (moe::launch_decode_layer(p, grid, smem_limit, pdl, s) != cudaSuccess) return MOE_ERR_CUDA;
   return MOE_OK;
 }
+
+namespace moe {
+
+// Status word of the allocation-free decode on the current device (see
+// moe_check_device with a null context): waits for the device, then reads
+// the word and clears it.  (The grid-barrier counter needs no clearing: every
+// call zeroes it before its launch.)  Returns false if a CUDA call fails.
+bool noalloc_status_read_clear(int32_t *code) {
+  *code = 0;
+  if (cudaDeviceSynchronize() != cudaSuccess) return false;
+  int32_t v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_decode_scratch, sizeof(v), kStatusOffset) != cudaSuccess)
+    return false;
+  if (v != 0) {
+    const int32_t zero = 0;
+    if (cudaMemcpyToSymbol(g_decode_scratch, &zero, sizeof(zero), kStatusOffset) != cudaSuccess ||
+        cudaDeviceSynchronize() != cudaSuccess)
+      return false;
+  }
+  *code = v;
+  return true;
+}
+
+}  // namespace moe

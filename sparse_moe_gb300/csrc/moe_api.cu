@@ -23,7 +23,8 @@ size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 struct WsLayout {
   int Tc, nblk, R, Imax, max_blocks;
-  size_t status, logits, idx, w, gate, mask, base, counts, offsets, sorted, pos, blocks, nblocks, h, o;
+  size_t status, logits, idx, w, gate, mask, base, counts, offsets, sorted, pos, blocks, nblocks, xg, h,
+      o;
   size_t dec_logits, dec_idx, dec_w, dec_g, dec_h, dec_counter, x_stage, y_stage, dec_x_stage,
       dec_y_stage, total;
 };
@@ -56,6 +57,7 @@ WsLayout make_layout(const moe_config &c) {
   L.pos = take(Tc * k * 4);
   L.blocks = take(static_cast<size_t>(L.max_blocks) * 16);
   L.nblocks = take(16);
+  L.xg = take(Tc * k * H * 2);
   L.h = take(static_cast<size_t>(L.R) * L.Imax * 2);
   L.o = take(static_cast<size_t>(L.R) * H * 2);
   L.dec_logits = take(E * 4);
@@ -109,6 +111,33 @@ bool encode_weight_map(CUtensorMap *m, const void *ptr, uint64_t inner, uint64_t
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The four token-row maps of a 2-D bf16 (or fp16) matrix [rows, inner]:
+// boxes of {64, 16 << i} elements, 128-byte swizzled (the grouped GEMMs' B
+// operand, one or two boxes per stage chosen from the block's size).
+bool encode_row_maps(CUtensorMap (&m)[4], const void *ptr, uint64_t inner, uint64_t rows,
+                     bool f16 = false) {
+  for (int i = 0; i < 4; ++i)
+    if (!encode_weight_map(&m[i], ptr, inner, rows, 16u << i, f16)) return false;
+  return true;
+}
+
+// The gate/up weights [experts, 2 inter, K] as a 3-D bf16 tensor {K, inter,
+// 2 experts}: a box {64, 64, 2} holds 64 gate rows followed by the matching
+// 64 up rows of one expert, 128-byte swizzled (one TMA box per CTA and
+// k-step).
+bool encode_gateup_map(CUtensorMap *m, const void *ptr, uint64_t K, uint64_t inter,
+                       uint64_t experts) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {K, inter, 2 * experts};
+  const cuuint64_t strides[2] = {K * 2, inter * K * 2};
+  const cuuint32_t box[3] = {64, 64, 2};
+  const cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // 2-D matrix of packed int4 codes [outer rows, inner bytes] (two codes per
 // byte along K), unswizzled boxes of {32 bytes (64 codes), box_rows}: the
 // int4 weight tiles, dequantised in shared memory by the GEMM.
@@ -150,9 +179,9 @@ struct moe_ctx {
   int device = 0;
   int num_sms = 0;
   int gemm_grid = 0;   // CTAs of the persistent grouped-GEMM grid (whole pairs)
-  int gemm_prefetch = 0;   // GEMM L2 prefetch bits (MOE_GEMM_PREFETCH; see GemmParams)
   int router_split = 1;    // router GEMM split-K parts (router_split())
-  CUtensorMap map_h;       // h [R, Imax] fp16 in the workspace: the down GEMM's token rows
+  CUtensorMap map_h[4];    // h [R, Imax] fp16 in the workspace: the down GEMM's token rows
+  CUtensorMap map_xg[4];   // x in grouped order [Tc k, H] bf16: the routed gate/up token rows
   bool prefill_pdl = true; // programmatic dependent launch between prefill kernels (MOE_PREFILL_PDL)
   // Measurement options (environment, read at creation; off by default), each
   // undoing one mechanism of the page to measure what it is worth here:
@@ -307,10 +336,13 @@ int router_block_rows(const moe_ctx *ctx, int T) {
 }
 
 // Router GEMM, top-k, histogram/scan/block map, scatter for T <= Tc tokens;
-// the summed logits go to `logits` when it is non-null.
+// the summed logits go to `logits` when it is non-null.  map_x: the token-row
+// maps of x (T rows); with_xg: the scatter also writes x in grouped order
+// into the workspace (the routed gate/up GEMM's token rows).
 moe_status enqueue_route(moe_ctx *ctx, const LayerSlot &ls, const void *x, int T, float *logits,
                          int32_t *idx, float *w, int32_t *counts, int32_t *offsets,
-                         int32_t *sorted_rows, int32_t *pos, cudaStream_t s) {
+                         int32_t *sorted_rows, int32_t *pos, const CUtensorMap (&map_x)[4],
+                         bool with_xg, cudaStream_t s) {
   const moe_config &c = ctx->cfg;
   const WsLayout &L = ctx->L;
   GemmParams gp{};
@@ -318,8 +350,6 @@ moe_status enqueue_route(moe_ctx *ctx, const LayerSlot &ls, const void *x, int T
   gp.a_routed = gp.a_shared = ls.w.router_w;
   gp.lda_routed = gp.lda_shared = c.hidden;
   gp.a_rows_routed = gp.a_rows_shared = c.n_experts;
-  gp.b = x;
-  gp.ldb = c.hidden;
   gp.block_rows = router_block_rows(ctx, T);
   gp.k_split = ctx->router_split;
   gp.n_blocks_host = (T + gp.block_rows - 1) / gp.block_rows;
@@ -338,18 +368,12 @@ moe_status enqueue_route(moe_ctx *ctx, const LayerSlot &ls, const void *x, int T
   gp.out_ld = c.n_experts;
   gp.bias = ls.w.router_b;
   gp.status = ctx->status();
-  gp.prefetch = ctx->gemm_prefetch;
   const int tiles = gp.n_blocks_host * gp.m_tiles * gp.k_split;
-  // The token rows of a router tile are consecutive rows of x: they come by
-  // TMA boxes with the weight tile instead of cp.async gathers.
-  CUtensorMap map_x;
-  gp.b_tma = encode_weight_map(&map_x, x, c.hidden, static_cast<uint64_t>(T), kBTmaRows) ? 1 : 0;
   moe_status st;
   {
     ProfScope ps(ctx, K_ROUTER_GEMM, s);
-    st = launched(ctx, launch_tc_gemm(ls.map_router, ls.map_router, gp.b_tma ? map_x : ls.map_router,
-                                      gp, CONV_NONE, std::min(ctx->gemm_grid, 2 * tiles),
-                                      ctx->prefill_pdl, s),
+    st = launched(ctx, launch_tc_gemm(ls.map_router, ls.map_router, map_x, map_x, gp, CONV_NONE,
+                                      std::min(ctx->gemm_grid, 2 * tiles), ctx->prefill_pdl, s),
                   "router gemm launch");
   }
   if (st) return st;
@@ -379,7 +403,8 @@ moe_status enqueue_route(moe_ctx *ctx, const LayerSlot &ls, const void *x, int T
     ProfScope ps(ctx, K_SCATTER, s);
     st = launched(ctx,
                   launch_scatter(idx, mask, base, offsets, T, c.n_experts, c.top_k, sorted_rows,
-                                 pos, ctx->prefill_pdl, s),
+                                 pos, x, with_xg ? ctx->at<void>(L.xg) : nullptr, c.hidden,
+                                 ctx->prefill_pdl, s),
                   "scatter launch");
   }
   return st;
@@ -393,9 +418,14 @@ moe_status enqueue_prefill_chunk(moe_ctx *ctx, const LayerSlot &ls, const void *
   float *w = ctx->at<float>(L.w);
   int32_t *sorted = ctx->at<int32_t>(L.sorted);
   int32_t *pos = ctx->at<int32_t>(L.pos);
+  // token-row maps of this call's x (the router's, and the shared expert's
+  // gate/up token rows)
+  CUtensorMap map_x[4];
+  if (!encode_row_maps(map_x, x, c.hidden, static_cast<uint64_t>(T)))
+    return fail(ctx, MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed for x");
   moe_status st = enqueue_route(ctx, ls, x, T, nullptr, idx, w,
                                 ctx->at<int32_t>(L.counts), ctx->at<int32_t>(L.offsets), sorted,
-                                pos, s);
+                                pos, map_x, true, s);
   if (st) return st;
   if (ctx->ablate_host_routing) {
     // measurement option: the CPU waits for the routing and inspects it
@@ -416,9 +446,7 @@ moe_status enqueue_prefill_chunk(moe_ctx *ctx, const LayerSlot &ls, const void *
   gp.inter_shared = c.shared_inter;
   gp.k_routed = c.hidden;
   gp.shared_row0 = T * c.top_k;
-  gp.sorted_rows = sorted;
   gp.status = ctx->status();
-  gp.prefetch = ctx->gemm_prefetch;
   const bool int4 = c.wfmt != MOE_W_BF16;
   const bool aff = c.wfmt == MOE_W_INT4_AFFINE_G64;
   // gate/up + SwiGLU -> h
@@ -429,8 +457,6 @@ moe_status enqueue_prefill_chunk(moe_ctx *ctx, const LayerSlot &ls, const void *
   gp.lda_routed = gp.lda_shared = c.hidden;
   gp.a_rows_routed = c.n_experts * 2 * c.inter;
   gp.a_rows_shared = 2 * c.shared_inter;
-  gp.b = x;
-  gp.ldb = c.hidden;
   gp.out = ctx->at<void>(L.h);
   gp.out_ld = L.Imax;
   gp.a_scale_routed = int4 ? ls.w.gate_up_scale : nullptr;
@@ -440,7 +466,7 @@ moe_status enqueue_prefill_chunk(moe_ctx *ctx, const LayerSlot &ls, const void *
   {
     ProfScope ps(ctx, K_GATEUP_GEMM, s);
     st = launched(ctx,
-                  launch_tc_gemm(ls.map_gu, ls.map_gu_sh, ls.map_gu, gp,
+                  launch_tc_gemm(ls.map_gu, ls.map_gu_sh, ctx->map_xg, map_x, gp,
                                  aff ? CONV_INT4A_TO_BF16 : int4 ? CONV_INT4_TO_BF16 : CONV_NONE,
                                  ctx->gemm_grid, ctx->prefill_pdl, s),
                   "gate/up gemm launch");
@@ -451,13 +477,10 @@ moe_status enqueue_prefill_chunk(moe_ctx *ctx, const LayerSlot &ls, const void *
   gp.a_routed = ls.down_f16 ? ls.w.down_f16 : ls.w.down;
   gp.a_shared = ls.down_f16 ? ls.w.sh_down_f16 : ls.w.sh_down;
   gp.ab_f16 = ls.down_f16 ? 1 : 0;
-  gp.b_tma = 1;   // h rows of a block are consecutive: TMA boxes
   gp.lda_routed = c.inter;
   gp.lda_shared = c.shared_inter;
   gp.a_rows_routed = c.n_experts * c.hidden;
   gp.a_rows_shared = c.hidden;
-  gp.b = ctx->at<void>(L.h);
-  gp.ldb = L.Imax;
   gp.m_tiles = (c.hidden + gemm_pair_rows() - 1) / gemm_pair_rows();
   gp.out = ctx->at<void>(L.o);
   gp.out_ld = c.hidden;
@@ -468,7 +491,7 @@ moe_status enqueue_prefill_chunk(moe_ctx *ctx, const LayerSlot &ls, const void *
   {
     ProfScope ps(ctx, K_DOWN_GEMM, s);
     st = launched(ctx,
-                  launch_tc_gemm(ls.map_dn, ls.map_dn_sh, ctx->map_h, gp,
+                  launch_tc_gemm(ls.map_dn, ls.map_dn_sh, ctx->map_h, ctx->map_h, gp,
                                  aff ? CONV_INT4A_TO_F16 : int4 ? CONV_INT4_TO_F16
                                       : (ls.down_f16 ? CONV_NONE : CONV_BF16_TO_F16),
                                  ctx->gemm_grid, ctx->prefill_pdl, s),
@@ -595,13 +618,13 @@ moe_status moe_ctx_create(const moe_config *cfg, int device, void *workspace, si
   }
   ctx->gemm_grid = gemm_max_grid(sms);
   ctx->router_split = router_split(ctx->cfg, ctx->L);
-  if (!encode_weight_map(&ctx->map_h, ctx->ws + L.h, L.Imax, static_cast<uint64_t>(L.R), kBTmaRows,
-                         true)) {
+  if (!encode_row_maps(ctx->map_h, ctx->ws + L.h, L.Imax, static_cast<uint64_t>(L.R), true) ||
+      !encode_row_maps(ctx->map_xg, ctx->ws + L.xg, cfg->hidden,
+                       static_cast<uint64_t>(L.Tc) * cfg->top_k)) {
     delete ctx;
     return MOE_ERR_CUDA;
   }
   ctx->decode_grid = decode_layer_grid(sms);
-  if (const char *env = std::getenv("MOE_GEMM_PREFETCH")) ctx->gemm_prefetch = std::atoi(env);
   if (const char *env = std::getenv("MOE_DECODE_PDL")) ctx->decode_pdl = std::atoi(env) != 0;
   if (const char *env = std::getenv("MOE_PREFILL_PDL")) ctx->prefill_pdl = std::atoi(env) != 0;
   if (const char *env = std::getenv("MOE_ABLATE_HOST_ROUTING"))
@@ -679,9 +702,8 @@ moe_status moe_load_weights(moe_ctx *ctx, int layer, const moe_weights *w) {
   ls.down_f16 = f16_down;
   bool ok = encode_weight_map(&ls.map_router, w->router_w, c.hidden, c.n_experts, 128);
   if (!int4) {
-    ok = ok && encode_weight_map(&ls.map_gu, w->gate_up, c.hidden,
-                                 static_cast<uint64_t>(c.n_experts) * 2 * c.inter, 64);
-    ok = ok && encode_weight_map(&ls.map_gu_sh, w->sh_gate_up, c.hidden, 2 * c.shared_inter, 64);
+    ok = ok && encode_gateup_map(&ls.map_gu, w->gate_up, c.hidden, c.inter, c.n_experts);
+    ok = ok && encode_gateup_map(&ls.map_gu_sh, w->sh_gate_up, c.hidden, c.shared_inter, 1);
     ok = ok && encode_weight_map(&ls.map_dn, f16_down ? w->down_f16 : w->down, c.inter,
                                  static_cast<uint64_t>(c.n_experts) * c.hidden, 128, f16_down);
     ok = ok && encode_weight_map(&ls.map_dn_sh, f16_down ? w->sh_down_f16 : w->sh_down,
@@ -712,8 +734,11 @@ moe_status moe_route(moe_ctx *ctx, int layer, const void *x, int T, float *logit
       !pos_of_assign)
     return fail(ctx, MOE_ERR_INVALID_ARG, "null or misaligned routing buffer");
   if ((st = ensure_device(ctx))) return st;
+  CUtensorMap map_x[4];
+  if (!encode_row_maps(map_x, x, ctx->cfg.hidden, static_cast<uint64_t>(T)))
+    return fail(ctx, MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed for x");
   return enqueue_route(ctx, ctx->layers[layer], x, T, logits, topk_idx, topk_w, counts, offsets,
-                       sorted_rows, pos_of_assign, static_cast<cudaStream_t>(stream));
+                       sorted_rows, pos_of_assign, map_x, false, static_cast<cudaStream_t>(stream));
 }
 
 moe_status moe_forward_prefill(moe_ctx *ctx, int layer, const void *x, int T, void *y,
@@ -985,7 +1010,14 @@ moe_status moe_dequant_int4(const void *codes, const void *scale, const void *bi
 }
 
 moe_status moe_check_device(moe_ctx *ctx, int32_t *code) {
-  if (!ctx) return MOE_ERR_INVALID_ARG;
+  if (!ctx) {
+    // no context: the status word of moe_forward_decode_noalloc on the
+    // current device
+    int32_t v = 0;
+    if (!noalloc_status_read_clear(&v)) return MOE_ERR_CUDA;
+    if (code) *code = v;
+    return v != 0 ? MOE_ERR_DEVICE_TIMEOUT : MOE_OK;
+  }
   moe_status st = ensure_device(ctx);
   if (st) return st;
   cudaError_t e = cudaDeviceSynchronize();

@@ -43,8 +43,6 @@ struct GemmParams {
   int lda_shared;
   int a_rows_routed;         // rows of the A tensors (rows past them read as zeros)
   int a_rows_shared;
-  const void *b;             // B rows (K-major): x (router, gate/up) or h (down)
-  int ldb;                   // elements per B row
   const int4 *blocks;        // grouped modes: {expert (E = shared), row_start, n_rows, 0}
   const int *n_blocks_dev;   // grouped modes: block count in device memory
   int n_blocks_host;         // router: token blocks
@@ -57,20 +55,16 @@ struct GemmParams {
   int inter_shared;          // Is
   int k_routed;              // reduction length (router, gate/up: H)
   int shared_row0;           // first grouped row of the shared expert (T*k)
-  const int *sorted_rows;    // token of each grouped row
   void *out;                 // router: fp32 [T,E]; gate/up: fp16 h [R,ld]; down: fp16 o [R,H]
   int out_ld;                // elements per output row
   const float *bias;         // router bias or null
   int *status;               // device status word
-  int prefetch;              // bit 1: L2-prefetch the next tile's token rows
   const void *a_scale_routed;   // int4 weights: bf16 scales [rows, K/64] (else null)
   const void *a_scale_shared;
   const void *a_bias_routed;    // affine int4 weights: bf16 biases [rows, K/64] (else null)
   const void *a_bias_shared;
   int ab_f16;                // CONV_NONE only: A and B are fp16 (else bf16)
   int fixed_n;               // grouped modes: MMA N = kBlockRowsMax for every block (measurement)
-  int b_tma;                 // down: B rows are consecutive (h in grouped order) and come by
-                             // TMA with the weight tile (map_b), not from the row producers
   int k_split;               // router: split-K parts (>= 1); part s writes out + s * out_split_stride
   size_t out_split_stride;   // router: floats between split-K parts of `out`
 };
@@ -82,11 +76,15 @@ int gemm_pair_rows();
 int gemm_max_grid(int num_sms);
 // `pdl` (here and below): programmatic dependent launch on the previous
 // kernel of the stream (the kernel waits for it before reading its inputs).
+// a_routed, a_shared: the weight maps (router: 2-D {K, E}, box {64, 128};
+// gate/up: 3-D {K, I, 2 E} (2 for the shared expert), box {64, 64, 2}; down:
+// 2-D {K, rows}, box {64, 128}; int4: 2-D code maps, box {32 bytes, 64 or
+// 128}).  b, b2: token-row maps of one matrix each, boxes of 64 elements x
+// (16 << i) rows for i = 0..3 (b: x for the router, x in grouped order for
+// gate/up, h for down; b2: x, for the shared expert's gate/up tiles).
 cudaError_t launch_tc_gemm(const CUtensorMap &a_routed, const CUtensorMap &a_shared,
-                           const CUtensorMap &b, const GemmParams &p, int conv, int grid, bool pdl,
-                           cudaStream_t stream);
-// Token-row boxes of the down GEMM's B operand: 16 rows x 64 fp16.
-constexpr int kBTmaRows = 16;
+                           const CUtensorMap (&b)[4], const CUtensorMap (&b2)[4],
+                           const GemmParams &p, int conv, int grid, bool pdl, cudaStream_t stream);
 
 // Routing: top-k + masks, block scan + block map, stable scatter.
 // Top-k over logits = sum of nsplit parts (part s at partial + s * split_stride,
@@ -100,9 +98,13 @@ cudaError_t launch_scan(const uint32_t *blk_mask, int nblk, int T, int E, int k,
                         int32_t *counts, int32_t *offsets, int32_t *blk_base, int4 *blocks,
                         int32_t *n_blocks, unsigned int *ticket, int block_rows, bool pdl,
                         cudaStream_t stream);
+// With xg non-null, also writes xg[pos(t, j)] = x[t] (x [T, H] bf16, xg
+// [T * k, H] bf16: the token rows in grouped order, the routed gate/up
+// GEMM's B operand).
 cudaError_t launch_scatter(const int32_t *idx, const uint32_t *blk_mask, const int32_t *blk_base,
                            const int32_t *offsets, int T, int E, int k, int32_t *sorted_rows,
-                           int32_t *pos_of_assign, bool pdl, cudaStream_t stream);
+                           int32_t *pos_of_assign, const void *x, void *xg, int H, bool pdl,
+                           cudaStream_t stream);
 
 // y[t] = sum_j w[t,j] o[pos(t,j)] + g[t] o[T*k + t]
 cudaError_t launch_combine(const float *gate, const void *o, const int32_t *pos, const float *w,
@@ -169,5 +171,10 @@ cudaError_t launch_decode_layers(const DecodeParams *layers, int n, int grid, in
 constexpr int kSmallMaxRows = 16;
 cudaError_t launch_rows(const DecodeParams &p, int grid, int smem_limit, bool pdl,
                         cudaStream_t stream);
+
+// Reads and clears the device status word of moe_forward_decode_noalloc on
+// the current device, after waiting for the device (decode_noalloc.cu).
+// Returns false if a CUDA call fails.
+bool noalloc_status_read_clear(int32_t *code);
 
 }  // namespace moe

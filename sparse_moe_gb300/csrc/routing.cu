@@ -287,33 +287,75 @@ cudaError_t launch_scan(const uint32_t *blk_mask, int nblk, int T, int E, int k,
 }
 
 // --------------------------------------------------------------- scatter --
+// One routing block of 32 tokens per CTA, one thread per assignment (t, j):
+// pos(t, j) = offsets[e] + (rows of e in earlier blocks) + (lower tokens of
+// this block that chose e), sorted_rows[pos] = t.  With xg, the CTA then
+// copies each of its tokens' x row to the token's k positions of xg (one warp
+// per token at a time: the row is read once, into registers, and written k
+// times), so that the grouped GEMM reads its token rows as consecutive rows.
+constexpr int kScatterChunks = 8;   // 16-byte chunks of a row per lane and pass
+
 __global__ void scatter_kernel(const int32_t *__restrict__ idx, const uint32_t *__restrict__ blk_mask,
                                const int32_t *__restrict__ blk_base,
                                const int32_t *__restrict__ offsets, int T, int E, int k,
                                int32_t *__restrict__ sorted_rows,
-                               int32_t *__restrict__ pos_of_assign) {
+                               int32_t *__restrict__ pos_of_assign, const uint4 *__restrict__ x,
+                               uint4 *__restrict__ xg, int H) {
+  __shared__ int pos_s[kRouteBlockTokens * 32];   // [token][slot], k <= 32
   pdl_trigger();
   pdl_wait();
   const int tl = threadIdx.x / k;
   const int j = threadIdx.x - tl * k;
   const int b = blockIdx.x;
   const int t = b * kRouteBlockTokens + tl;
-  if (tl >= kRouteBlockTokens || t >= T) return;
-  const int a = t * k + j;
-  const int e = idx[a];
-  const uint32_t m = blk_mask[static_cast<size_t>(b) * E + e];
-  const int rank = __popc(m & ((1u << tl) - 1u));
-  const int p = offsets[e] + blk_base[static_cast<size_t>(b) * E + e] + rank;
-  pos_of_assign[a] = p;
-  sorted_rows[p] = t;
+  if (tl < kRouteBlockTokens && t < T) {
+    const int a = t * k + j;
+    const int e = idx[a];
+    const uint32_t m = blk_mask[static_cast<size_t>(b) * E + e];
+    const int rank = __popc(m & ((1u << tl) - 1u));
+    const int p = offsets[e] + blk_base[static_cast<size_t>(b) * E + e] + rank;
+    pos_of_assign[a] = p;
+    sorted_rows[p] = t;
+    pos_s[tl * k + j] = p;
+  }
+  if (xg == nullptr) return;
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nwarps = blockDim.x >> 5;
+  const int nch = H / 8;   // 16-byte chunks per row
+  for (int u = warp; u < kRouteBlockTokens; u += nwarps) {
+    const int tt = b * kRouteBlockTokens + u;
+    if (tt >= T) break;
+    const uint4 *src = x + static_cast<size_t>(tt) * nch;
+    for (int c0 = 0; c0 < nch; c0 += 32 * kScatterChunks) {
+      uint4 v[kScatterChunks];
+#pragma unroll
+      for (int i = 0; i < kScatterChunks; ++i) {
+        const int c = c0 + lane + 32 * i;
+        if (c < nch) v[i] = __ldg(src + c);
+      }
+      for (int jj = 0; jj < k; ++jj) {
+        uint4 *dst = xg + static_cast<size_t>(pos_s[u * k + jj]) * nch;
+#pragma unroll
+        for (int i = 0; i < kScatterChunks; ++i) {
+          const int c = c0 + lane + 32 * i;
+          if (c < nch) dst[c] = v[i];
+        }
+      }
+    }
+  }
 }
 
 cudaError_t launch_scatter(const int32_t *idx, const uint32_t *blk_mask, const int32_t *blk_base,
                            const int32_t *offsets, int T, int E, int k, int32_t *sorted_rows,
-                           int32_t *pos_of_assign, bool pdl, cudaStream_t stream) {
+                           int32_t *pos_of_assign, const void *x, void *xg, int H, bool pdl,
+                           cudaStream_t stream) {
   const int nblk = (T + kRouteBlockTokens - 1) / kRouteBlockTokens;
-  return launch_kernel(scatter_kernel, dim3(nblk), dim3(kRouteBlockTokens * k), 0, stream, pdl, idx,
-                       blk_mask, blk_base, offsets, T, E, k, sorted_rows, pos_of_assign);
+  // at least four warps per CTA for the row copies
+  const int threads = std::max(128, (kRouteBlockTokens * k + 31) / 32 * 32);
+  return launch_kernel(scatter_kernel, dim3(nblk), dim3(threads), 0, stream, pdl, idx, blk_mask,
+                       blk_base, offsets, T, E, k, sorted_rows, pos_of_assign,
+                       static_cast<const uint4 *>(x), static_cast<uint4 *>(xg), H);
 }
 
 // --------------------------------------------------------------- combine --

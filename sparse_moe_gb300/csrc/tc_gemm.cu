@@ -2,11 +2,13 @@
 // for the prefill path:
 //
 //   router:  l[t, e]  = sum_h x[t,h] Wr[e,h] (+ b[e])              -> fp32
-//   gate/up: h[p, i]  = silu(sum_h x[tok(p),h] Wg[e,i,h]) *
-//                       sum_h x[tok(p),h] Wu[e,i,h]                 -> fp16
+//   gate/up: h[p, i]  = silu(sum_h xg[p,h] Wg[e,i,h]) *
+//                       sum_h xg[p,h] Wu[e,i,h]                     -> fp16
 //   down:    o[p, n]  = sum_i h[p,i] Wd[e,n,i]                      -> fp16
 //
-// (sections "Dequantize weights during matrix multiplication", "Keep expert
+// where p runs over the rows routed to expert e in grouped order and xg is x
+// in that order (written by the routing's scatter step).
+// (Sections "Dequantize weights during matrix multiplication", "Keep expert
 // routing on the GPU" and "Match tile size to expert load" of "Optimizing
 // On-Device Inference for Apple Silicon": grouped GEMM over the rows routed
 // to each expert, fp32 accumulation, tile shape from the expert's row count.)
@@ -15,43 +17,40 @@
 //  * a pair of CTAs on two SMs (a cluster of 2) runs one 256 x N tile with
 //    tcgen05.mma.cta_group::2: weights on the MMA M side (each CTA stages its
 //    own 128 rows) and the routed token rows on the N side (each CTA stages
-//    half of them), so every SM moves 32 KB per 64-deep k-step for 2 x 128 x
-//    N x 64 multiply-adds.  N is the block's row count rounded up to 32 (at
-//    most 256): an expert with 5 rows runs a 256x32 MMA, not a padded 256-row
-//    token tile;
-//  * the gate/up tile stacks, in each CTA, 64 gate rows over the 64 matching
-//    up rows, so one MMA produces both halves of 64 SwiGLU outputs per CTA;
-//    the epilogue pairs them through a small shared-memory exchange;
-//  * the weight tile (A) of each k-step is one or two TMA boxes (128-byte
-//    swizzle; an L2 prefetch of the next tile's boxes exists but is off by
-//    default, as it measured slower); the gate/up GEMM's token rows (B)
-//    are gathered by a group of warps per pipeline stage with 16-byte
-//    cp.async copies written straight into the same 128-byte-swizzled
-//    K-major layout, so no permuted copy of x is ever written; the router's
-//    (x in token order) and the down GEMM's (h in grouped order) are
-//    consecutive rows and come by TMA boxes with the weight tile.  (Measured on GB300: TMA
-//    gather4 moves 512 bytes per request and tops out near 7-18 bytes/clock
-//    per SM; one warp of cp.async sustains about 7 bytes/clock; a single-SM
-//    128 x 256 tile would need 96 bytes/clock, the pair needs 64.)
+//    half of them), so every SM takes in up to 32 KB per 64-deep k-step for
+//    2 x 128 x N x 64 multiply-adds.  N is the block's row count rounded up
+//    to 32 (at most 256): an expert with 5 rows runs a 256x32 MMA, not a
+//    padded 256-row token tile;
+//  * both operands come by TMA with 128-byte swizzle.  Each CTA's share of a
+//    stage is one weight box (the gate/up tile as a 3-D box that stacks 64
+//    gate rows over the matching 64 up rows, so one MMA yields both halves of
+//    64 SwiGLU outputs) and one or two token-row boxes of 16..128 rows chosen
+//    from the block's size, all consecutive rows: x for the router and the
+//    shared expert, x in grouped order for the routed gate/up tiles, h (in
+//    grouped order) for the down projection;
+//  * two producer threads fill alternate stages.  (Measured on GB300 with
+//    every SM streaming from L2: one thread issuing one 16 KB box per stage
+//    moves about 23-28 bytes/clock per SM whatever the pipeline depth; two
+//    threads issuing 32 KB stages move about 78.  The tiles need about 64 at
+//    the tensor cores' full rate.  cp.async gathers of scattered rows reach
+//    about 28 and TMA gather4 about 3, which is why the gate/up token rows
+//    are read from a grouped copy of x rather than gathered.)
 //  * the pair's CTAs walk the device-built tile list persistently; one thread
 //    of the leader issues the MMAs once both CTAs' stage is ready.  Without a
-//    conversion (router, bf16 gate/up) both CTAs' TMA boxes complete on the
-//    leader's full barrier (cta_group::2 loads) and the peer's token-row
-//    warps arrive on it remotely, so readiness needs no relay; when the
-//    weight tile must be converted first, converting warps arrive on the
-//    leader's ready barrier: for bf16 -> fp16 (down without fp16 copies) a
-//    team per stage, each member with a cluster-scope arrival from the peer;
-//    for int4 four converter warps per k-step, whose codes come through
-//    their own ring;
-//    four epilogue warps
-//    per CTA drain their half of the double-buffered TMEM accumulator while
-//    the next tile computes, and transpose each 32x16 piece through shared
-//    memory so global stores are 16-byte vectors;
+//    conversion (router, bf16 gate/up, down on fp16 weights) both CTAs' boxes
+//    complete on the leader's full barrier (cta_group::2 loads), so readiness
+//    needs no relay; when the weight tile must be converted first (int4
+//    codes, or bf16 down weights without fp16 copies), a team of four
+//    converter warps per k-step arrives on the leader's ready barrier;
+//    four epilogue warps per CTA drain their half of the double-buffered
+//    TMEM accumulator while the next tile computes, and transpose each 32x16
+//    piece through shared memory so global stores are 16-byte vectors;
 //  * the down projection runs with fp16 operands: the gate/up epilogue stores
-//    h in fp16 (11 significant bits instead of bf16's 8), and the stage
-//    finisher warps turn each bf16 weight tile into fp16 in place in shared memory
-//    before the MMA reads it (exact for |w| >= 2^-17; the swizzled layout is
-//    unchanged since both types are 2 bytes).  o is stored in fp16.
+//    h in fp16 (11 significant bits instead of bf16's 8), and bf16 weight
+//    tiles are turned into fp16 in place in shared memory before the MMA
+//    reads them (exact for |w| >= 2^-17; the swizzled layout is unchanged
+//    since both types are 2 bytes) unless the caller supplies fp16 copies.
+//    o is stored in fp16.
 #include "moe_common.cuh"
 #include "moe_internal.h"
 
@@ -64,59 +63,53 @@ constexpr int PAIR_M = 2 * BM;
 constexpr int BK = 64;                  // K per pipeline stage (128-byte rows)
 constexpr int BN_MAX = kBlockRowsMax;   // max MMA N (tokens per tile)
 constexpr int BN_HALF = BN_MAX / 2;     // token rows staged per CTA
-constexpr int STAGES = 6;
+constexpr int STAGES = 6;               // even: producer p fills the stages it % 2 == p
 constexpr int A_BYTES = BM * BK * 2;            // 16 KB
 constexpr int B_BYTES = BN_HALF * BK * 2;       // 16 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // 32 KB
-// int4 weights: the TMA puts a stage's packed codes (BM rows x BK/2 bytes) in
-// the last 4 KB of the A region, where the finisher dequantises them in place.
+// int4 weights: a k-step's packed codes (BM rows x BK/2 bytes) land in a ring
+// of their own, from which the converter warps expand them into the stage.
 constexpr int A_CODE_BYTES = BM * BK / 2;       // 4 KB: one k-step's int4 codes
 constexpr int kCodeSlots = 4;                   // int4 code ring (ahead of the stages)
 constexpr int ACC_COLS = 256;                   // one accumulator buffer
 constexpr int TMEM_COLS = 512;                  // two buffers
 // Warp roles (identical in both CTAs of a pair).
-constexpr int B_WARPS_PER_STAGE = 2;
-constexpr int TMA_WARP = 0;                                  // warp 0
-constexpr int B_WARP0 = 1;                                   // warps 1..12
-constexpr int B_WARPS = STAGES * B_WARPS_PER_STAGE;
-constexpr int MMA_WARP = B_WARP0 + B_WARPS;                  // warp 13
-constexpr int EPI_WARP0 = MMA_WARP + 1;                      // warps 14..17
-constexpr int FIN_WARP0 = EPI_WARP0 + 4;                     // warps 18..25: finishers
+constexpr int kProducers = 2;                   // warps 0, 1: stage producers (lane 0)
+constexpr int CODE_WARP = 2;                    // int4 code ring producer (lane 0)
+constexpr int MMA_WARP = 3;
+constexpr int EPI_WARP0 = 4;                    // warps 4..7 (TMEM lane quarter = warp % 4)
+constexpr int FIN_WARP0 = EPI_WARP0 + 4;        // warps 8..15: converters
 constexpr int FIN_WARPS = 8;
 constexpr int NUM_THREADS = (FIN_WARP0 + FIN_WARPS) * 32;
 constexpr int XCH_FLOATS = 2 * 2 * 2 * 8 * 32;  // [buf][pair][dir][8 cols][32 lanes]
 constexpr int EPI_STAGE_BYTES = 4 * 16 * 64;    // per epilogue warp: 16 rows x 64 bytes
-// Per B producer warp: offsets of the token rows it copies (every
-// B_WARPS_PER_STAGE-th group of four rows of up to 128).
-constexpr int kRowTab = 4 * ((BN_HALF / 4 + B_WARPS_PER_STAGE - 1) / B_WARPS_PER_STAGE);
+static_assert(STAGES % kProducers == 0, "each stage has one producer");
+static_assert(EPI_WARP0 % 4 == 0, "epilogue warp q reads TMEM lanes 32 q .. 32 q + 31");
 
-// Warps that convert one stage's weight tile, per CTA: for bf16 -> fp16 the
-// stage's finisher (finisher f owns stage f) and its two token-row producers,
-// each a share of the chunks; for int4 kInt4Warps finishers, each expanding
-// kInt4Batches batches of 32 weight rows, the finishers forming kInt4Groups
-// teams that take k-steps in turn (team g: it % kInt4Groups == g).  Measured
-// at T=4096: four warps of 32 rows per k-step (two teams) beat two of 64 rows
-// (four teams) by 20 %.
+// Warps that convert one stage's weight tile, per CTA: kInt4Warps converter
+// warps, each handling kInt4Batches batches of 32 weight rows (int4: expanding
+// codes from the ring; bf16 -> fp16: converting the landed tile in place), the
+// converters forming kInt4Groups teams that take k-steps in turn (team g:
+// it % kInt4Groups == g).  Measured at T=4096 (int4): four warps of 32 rows
+// per k-step (two teams) beat two of 64 rows (four teams) by 20 %.
 //
 // A team's next k-step is kInt4Groups k-steps later; its parity waits on the
 // stage and code-ring barriers stay unambiguous only if no team can reach a
-// barrier phase two ahead of the completed one: every ring slot is used by
-// one team (kCodeSlots a multiple of kInt4Groups) and a team's previous
-// k-step already waited for the stage's previous use (kInt4Groups <= STAGES).
-constexpr int kConvTeam = 1 + B_WARPS_PER_STAGE;
+// barrier phase two ahead of the completed one: every ring slot and every
+// stage is used by one team (kCodeSlots and STAGES multiples of kInt4Groups).
 constexpr int kInt4Warps = 4;
 constexpr int kInt4Batches = (BM / 32) / kInt4Warps;
 constexpr int kInt4Groups = FIN_WARPS / kInt4Warps;
 static_assert(kInt4Warps * kInt4Batches * 32 == BM && kInt4Groups * kInt4Warps == FIN_WARPS,
-              "int4 finisher teams");
-static_assert(kCodeSlots % kInt4Groups == 0 && kInt4Groups <= STAGES,
-              "int4 teams must not alias barrier phases");
+              "converter teams");
+static_assert(kCodeSlots % kInt4Groups == 0 && STAGES % kInt4Groups == 0,
+              "converter teams must not alias barrier phases");
 template <int CONV> __host__ __device__ constexpr int conv_team() {
-  return CONV == CONV_BF16_TO_F16 ? kConvTeam : conv_int4(CONV) ? kInt4Warps : 1;
+  return CONV == CONV_NONE ? 1 : kInt4Warps;
 }
 
 struct SmemTail {
-  uint64_t full[STAGES];        // local: TMA (A, or int4: the producers' token-row boxes) + this CTA's B warps
+  uint64_t full[STAGES];        // unconverted: leader's, both CTAs' boxes; else local (A + B or B)
   uint64_t cfull[kCodeSlots];   // local, int4: a k-step's weight codes landed in the ring (TMA)
   uint64_t cempty[kCodeSlots];  // local, int4: the k-step's converters hold their codes
   uint64_t ready[STAGES];       // leader: both CTAs' conversion teams
@@ -131,8 +124,8 @@ struct SmemTail {
 
 constexpr size_t kGemmSmemBytes = 1024 /*align slack*/ + STAGES * STAGE_BYTES +
                                   XCH_FLOATS * sizeof(float) + EPI_STAGE_BYTES +
-                                  B_WARPS * kRowTab * sizeof(int) + sizeof(SmemTail) +
-                                  128 /*ring alignment*/ + kCodeSlots * A_CODE_BYTES;
+                                  sizeof(SmemTail) + 128 /*ring alignment*/ +
+                                  kCodeSlots * A_CODE_BYTES;
 
 struct Tile {
   int valid;
@@ -141,6 +134,7 @@ struct Tile {
   int k0;              // first k-step (router split-K: split * nk)
   int split;           // router split-K part of this tile
   int m;
+  int e;               // expert (E: the shared expert; router: 0)
   int shared;
   int a_row, a_row2;   // this CTA's first A row (a_row2: first up row for gate/up)
   int a_valid_rows;    // this CTA's A rows at or beyond this index are not outputs
@@ -170,6 +164,7 @@ __device__ __forceinline__ Tile decode_tile(const GemmParams &p, int tile, int r
     t.nrows = blk.z;
     t.shared = (e == p.n_experts);
   }
+  t.e = e;
   t.nmma = p.fixed_n && p.mode != MODE_ROUTER ? BN_MAX : max(32, (t.nrows + 31) & ~31);
   t.valid = t.nrows > 0;
   if (p.mode == MODE_ROUTER) {
@@ -204,22 +199,31 @@ __device__ __forceinline__ int num_tiles(const GemmParams &p) {
   return *p.n_blocks_dev * p.m_tiles;
 }
 
-// Row of the B operand (x for router and gate/up, h for down) feeding row r
-// of a tile; rows past the tile's end repeat its last row.
-__device__ __forceinline__ int b_row(const GemmParams &p, const Tile &t, int r) {
-  const int pr = t.row0 + min(r, t.nrows - 1);
-  if (p.mode != MODE_GATEUP) return pr;
-  return t.shared ? pr - p.shared_row0 : __ldg(p.sorted_rows + pr);
-}
-
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint32_t src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+// The token-row boxes of one CTA's share of a stage: `rows` (a multiple of
+// 16, at most BN_HALF) rows as at most two boxes of 16 << i rows (map i of
+// the GemmMaps row-box sets), covering them with at most 16 rows to spare.
+struct BBoxes {
+  int n;
+  int map[2];
+  int rows[2];
+};
+__device__ __forceinline__ BBoxes b_boxes(int rows) {
+  BBoxes b;
+  const int u = rows >> 4;   // 1 .. 8
+  if (u >= 7) {
+    b.n = 1; b.map[0] = 3; b.rows[0] = 128;
+  } else if (u == 5 || u == 6) {
+    b.n = 2; b.map[0] = 2; b.rows[0] = 64; b.map[1] = u - 5; b.rows[1] = 16 << (u - 5);
+  } else if (u == 4) {
+    b.n = 1; b.map[0] = 2; b.rows[0] = 64;
+  } else if (u == 3) {
+    b.n = 2; b.map[0] = 1; b.rows[0] = 32; b.map[1] = 0; b.rows[1] = 16;
+  } else {
+    b.n = 1; b.map[0] = u - 1; b.rows[0] = 16 * u;
+  }
+  b.map[1] = b.n > 1 ? b.map[1] : 0;
+  b.rows[1] = b.n > 1 ? b.rows[1] : 0;
+  return b;
 }
 
 // Conversion, two values per 32-bit word: with u = q + 8 in [0, 15], the
@@ -322,11 +326,12 @@ __device__ __forceinline__ void expand_rows_int4(uint32_t tile, const uint32_t (
   }
 }
 
-// Warp q's share of the in-place bf16 -> fp16 conversion of one stage's A
-// tile (16-byte chunks q * 32 + lane, stepping kConvTeam * 32).
-__device__ __forceinline__ void convert_share_bf16_to_f16(uint32_t tile, int q, int lane) {
-  for (int i = q * 32 + lane; i < A_BYTES / 16; i += kConvTeam * 32) {
-    const uint32_t addr = tile + i * 16;
+// Converter q's share of the in-place bf16 -> fp16 conversion of one stage's
+// A tile: rows 32 q .. 32 q + 31 (4 KB, 16-byte chunks q * 256 + lane + 32 m).
+__device__ __forceinline__ void convert_rows_bf16_to_f16(uint32_t tile, int q, int lane) {
+#pragma unroll
+  for (int m = 0; m < 8; ++m) {
+    const uint32_t addr = tile + (q * 256 + lane + 32 * m) * 16;
     uint32_t w0, w1, w2, w3;
     asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
                  : "=r"(w0), "=r"(w1), "=r"(w2), "=r"(w3)
@@ -390,19 +395,21 @@ __device__ __forceinline__ void arrive_ready(SmemTail *tail, int stage, int rank
   else mbar_arrive_cluster(mapa_shared(ready, 0));
 }
 
-// bf16 -> fp16 team warp q's part of a converting stage: a bounded wait for
-// the stage to be full, its share of the conversion, and its arrival on the
-// pair leader's ready barrier.  Returns false on a timeout or abort.
-__device__ __forceinline__ bool convert_stage_bf16(const GemmParams &p, int stage, uint32_t phase,
-                                                   int q, int rank, uint32_t smem_base,
-                                                   SmemTail *tail, volatile int *abort_flag,
-                                                   int lane) {
+// bf16 -> fp16 converter q of k-step `it` (stage it % STAGES): a bounded wait
+// for the stage's boxes (weights and token rows) to land in this CTA, its 32
+// rows converted in place, and its arrival on the pair leader's ready
+// barrier.  Returns false on a timeout or abort.
+__device__ __forceinline__ bool convert_stage_bf16(const GemmParams &p, int q, int it, int rank,
+                                                   uint32_t smem_base, SmemTail *tail,
+                                                   volatile int *abort_flag, int lane) {
+  const int stage = it % STAGES;
+  const uint32_t phase = static_cast<uint32_t>(it / STAGES) & 1u;
   int got = 1;
   if (lane == 0)
     got = mbar_wait_bounded(smem_u32(&tail->full[stage]), phase, abort_flag, p.status,
                             DEV_TIMEOUT_CONVERTER);
   if (!__shfl_sync(0xffffffffu, got, 0)) return false;
-  convert_share_bf16_to_f16(smem_base + stage * STAGE_BYTES, q, lane);
+  convert_rows_bf16_to_f16(smem_base + stage * STAGE_BYTES, q, lane);
   fence_proxy_async_smem();
   __syncwarp();
   if (lane == 0) arrive_ready(tail, stage, rank);
@@ -472,18 +479,25 @@ __device__ __forceinline__ void warp_store_rows_f16(const uint8_t *stage, int ro
   }
 }
 
+// TMA descriptors of one grouped-GEMM launch: the weight tiles (routed
+// experts, shared expert) and two sets of token-row maps whose boxes are
+// 16, 32, 64 and 128 rows of 64 elements: b for the router (x), the routed
+// gate/up tiles (x in grouped order) and the down projection (h); b2 for the
+// shared expert's gate/up tiles (x).
+struct GemmMaps {
+  CUtensorMap a_routed, a_shared;
+  CUtensorMap b[4], b2[4];
+};
+
 template <int CONV>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
-    tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a_routed,
-                       const __grid_constant__ CUtensorMap map_a_shared,
-                       const __grid_constant__ CUtensorMap map_b, const GemmParams p) {
+    tc_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
   float *xch = reinterpret_cast<float *>(smem + STAGES * STAGE_BYTES);
   uint8_t *epi_stage = reinterpret_cast<uint8_t *>(xch + XCH_FLOATS);
-  int *row_tab = reinterpret_cast<int *>(epi_stage + EPI_STAGE_BYTES);
-  SmemTail *tail = reinterpret_cast<SmemTail *>(row_tab + B_WARPS * kRowTab);
+  SmemTail *tail = reinterpret_cast<SmemTail *>(epi_stage + EPI_STAGE_BYTES);
   const uint32_t code_ring = (smem_u32(tail + 1) + 127u) & ~127u;   // int4: kCodeSlots x 4 KB
   volatile int *abort_flag = &tail->abort_flag;
   pdl_trigger();   // the next kernel may start its set-up as SMs free up
@@ -496,10 +510,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
   const int num_pairs = gridDim.x >> 1;
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      // unconverted modes: the leader's full barrier also counts the peer's
-      // producers (and both CTAs' TMA bytes); otherwise each CTA's own
-      mbar_init(smem_u32(&tail->full[s]),
-                CONV == CONV_NONE ? 1 + 2 * B_WARPS_PER_STAGE : 1 + B_WARPS_PER_STAGE);
+      // one arrival per phase: the stage producer's arrive.expect_tx (the
+      // leader's, covering both CTAs' bytes, in the unconverted modes)
+      mbar_init(smem_u32(&tail->full[s]), 1);
       mbar_init(smem_u32(&tail->ready[s]), 2 * conv_team<CONV>());
       mbar_init(smem_u32(&tail->empty[s]), 1);
     }
@@ -514,9 +527,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     mbar_init(smem_u32(&tail->drain), 1);
     tail->abort_flag = 0;
     fence_mbarrier_init();
-    prefetch_tensormap(&map_a_routed);
-    prefetch_tensormap(&map_a_shared);
-    if (p.b_tma) prefetch_tensormap(&map_b);
+  }
+  if (warp < kProducers && lane == 0) {
+    prefetch_tensormap(&maps.a_routed);
+    prefetch_tensormap(&maps.a_shared);
+    for (int i = 0; i < 4; ++i) prefetch_tensormap(&maps.b[i]);
   }
   if (warp == MMA_WARP) {
     tmem_alloc_pair(smem_u32(&tail->tmem_base), TMEM_COLS);
@@ -530,206 +545,136 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
   const uint32_t tmem_base = tail->tmem_base;
   const int ntiles = num_tiles(p);
 
-  if (warp == TMA_WARP) {
-    // ------------------------------------------------ weight tiles (TMA) --
-    // Lane 0 loads each k-step's 128 weight rows of this CTA with TMA into
-    // the stage's A region (complete_tx on the local full barrier).  int4
-    // codes go to the code ring instead (slot it % kCodeSlots, complete_tx
-    // on cfull), paced by the converters freeing slots, not by the MMA.
-    // (Measured on GB300 and not kept: prefetching the weight rows into L2
-    // ahead of the boxes, by TMA or by plain prefetches, and loading part or
-    // all of the weight tile with cp.async from the stage producers -- each
-    // was slower than plain TMA boxes.)
+  if (warp < kProducers) {
+    // ------------------------------------------------- stage producers --
+    // Lane 0 of producer warp pp fills the stages of the k-steps it with
+    // it % kProducers == pp: it waits until the MMA has released the stage,
+    // then issues this CTA's boxes: the weight box (unless the weights are
+    // int4 codes, which come through the code ring) and the token-row boxes.
+    // Unconverted modes: both CTAs' boxes complete on the leader's full
+    // barrier, which expects the pair's bytes (cta_group::2 loads).
     constexpr bool INT4 = conv_int4(CONV);
-    constexpr int kx = INT4 ? BK / 2 : BK;   // box x extent per k-step (bytes / elements)
-    constexpr int kBufs = INT4 ? kCodeSlots : STAGES;
-    static_assert(kCodeSlots <= STAGES, "issued_parity covers the code ring");
-    int stage = 0;   // int4: ring slot
-    uint32_t phase = 0;
+    const int pp = warp;
     int issued_parity[STAGES];
 #pragma unroll
     for (int s2 = 0; s2 < STAGES; ++s2) issued_parity[s2] = -1;
-    int ok = 1;
-    for (int tile = pair_id; tile < ntiles && ok; tile += num_pairs) {
-      const Tile t = decode_tile(p, tile, rank);
-      if (!t.valid) continue;
-      if (lane == 0) {
-        const CUtensorMap *amap = t.shared ? &map_a_shared : &map_a_routed;
-        for (int ks = 0; ks < t.nk; ++ks) {
-          const uint32_t free_bar = INT4 ? smem_u32(&tail->cempty[stage]) : smem_u32(&tail->empty[stage]);
-          if (!mbar_wait_bounded(free_bar, phase ^ 1, abort_flag, p.status, DEV_TIMEOUT_PRODUCER)) {
-            ok = 0;
+    bool ok = true;
+    if (lane == 0) {
+      int it = 0;
+      for (int tile = pair_id; tile < ntiles && ok; tile += num_pairs) {
+        const Tile t = decode_tile(p, tile, rank);
+        if (!t.valid) continue;
+        const CUtensorMap *amap = t.shared ? &maps.a_shared : &maps.a_routed;
+        const bool b_from_x = p.mode == MODE_GATEUP && t.shared;   // shared expert: x rows
+        const CUtensorMap *bmaps = b_from_x ? maps.b2 : maps.b;
+        const int half = t.nmma / 2;
+        const BBoxes bb = b_boxes(half);
+        const int b_row0 = (b_from_x ? t.row0 - p.shared_row0 : t.row0) + rank * half;
+        const uint32_t b_bytes = static_cast<uint32_t>((bb.rows[0] + bb.rows[1]) * BK * 2);
+        for (int ks = 0; ks < t.nk; ++ks, ++it) {
+          if (it % kProducers != pp) continue;
+          const int stage = it % STAGES;
+          const uint32_t phase = static_cast<uint32_t>(it / STAGES) & 1u;
+          if (!mbar_wait_bounded(smem_u32(&tail->empty[stage]), phase ^ 1, abort_flag, p.status,
+                                 DEV_TIMEOUT_PRODUCER)) {
+            ok = false;
             break;
           }
           const uint32_t full_bar = smem_u32(&tail->full[stage]);
           const uint32_t a_dst = smem_base + stage * STAGE_BYTES;
-          // b_tma: this CTA's nmma / 2 token rows, in boxes of kBTmaRows
-          const int b_boxes = p.b_tma ? t.nmma / 2 / kBTmaRows : 0;
-          const uint32_t b_bytes = static_cast<uint32_t>(b_boxes * kBTmaRows * BK * 2);
-          const int b_row0 = t.row0 + rank * (t.nmma / 2);
-          if constexpr (INT4) {
-            // codes only (the stage's token-row boxes, if any, come from its
-            // producer warps)
-            const uint32_t cfull_bar = smem_u32(&tail->cfull[stage]);
-            const uint32_t c_dst = code_ring + stage * A_CODE_BYTES;
-            mbar_arrive_expect_tx(cfull_bar, A_CODE_BYTES);
-            if (p.mode == MODE_GATEUP) {
-              tma_load_2d(c_dst, amap, (t.k0 + ks) * kx, t.a_row, cfull_bar);
-              tma_load_2d(c_dst + A_CODE_BYTES / 2, amap, (t.k0 + ks) * kx, t.a_row2, cfull_bar);
-            } else {
-              tma_load_2d(c_dst, amap, (t.k0 + ks) * kx, t.a_row, cfull_bar);
-            }
-          } else if constexpr (CONV == CONV_NONE) {
-            // Both CTAs' boxes complete on the leader's full barrier, which
-            // expects the pair's bytes: no relay from the peer is needed.
+          const uint32_t b_dst = a_dst + A_BYTES;
+          const int kx = (t.k0 + ks) * BK;
+          if constexpr (CONV == CONV_NONE) {
             const uint32_t lead_full = mapa_shared(full_bar, 0);
             if (rank == 0) mbar_arrive_expect_tx(full_bar, 2 * (A_BYTES + b_bytes));
-            for (int i = 0; i < b_boxes; ++i)
-              tma_load_2d_pair(a_dst + A_BYTES + i * kBTmaRows * 128, &map_b, (t.k0 + ks) * BK,
-                               b_row0 + i * kBTmaRows, lead_full);
-            if (p.mode == MODE_GATEUP) {
-              tma_load_2d_pair(a_dst, amap, (t.k0 + ks) * kx, t.a_row, lead_full);
-              tma_load_2d_pair(a_dst + A_BYTES / 2, amap, (t.k0 + ks) * kx, t.a_row2, lead_full);
-            } else {
-              tma_load_2d_pair(a_dst, amap, (t.k0 + ks) * kx, t.a_row, lead_full);
-            }
+            if (p.mode == MODE_GATEUP)
+              tma_load_3d_pair(a_dst, amap, kx, t.out_base, t.shared ? 0 : 2 * t.e, lead_full);
+            else
+              tma_load_2d_pair(a_dst, amap, kx, t.a_row, lead_full);
+            tma_load_2d_pair(b_dst, &bmaps[bb.map[0]], kx, b_row0, lead_full);
+            if (bb.n > 1)
+              tma_load_2d_pair(b_dst + bb.rows[0] * 128, &bmaps[bb.map[1]], kx, b_row0 + bb.rows[0],
+                               lead_full);
+            // (the peer's boxes complete on the leader's barrier: the leader's
+            // producers wait for them on abort)
+            if (rank == 0) issued_parity[stage] = static_cast<int>(phase);
           } else {
-            mbar_arrive_expect_tx(full_bar, A_BYTES + b_bytes);
-            for (int i = 0; i < b_boxes; ++i)
-              tma_load_2d(a_dst + A_BYTES + i * kBTmaRows * 128, &map_b, (t.k0 + ks) * BK,
-                          b_row0 + i * kBTmaRows, full_bar);
-            if (p.mode == MODE_GATEUP) {
-              tma_load_2d(a_dst, amap, (t.k0 + ks) * kx, t.a_row, full_bar);
-              tma_load_2d(a_dst + A_BYTES / 2, amap, (t.k0 + ks) * kx, t.a_row2, full_bar);
-            } else {
-              tma_load_2d(a_dst, amap, (t.k0 + ks) * kx, t.a_row, full_bar);
+            mbar_arrive_expect_tx(full_bar, (INT4 ? 0u : static_cast<uint32_t>(A_BYTES)) + b_bytes);
+            if constexpr (!INT4) {
+              if (p.mode == MODE_GATEUP)
+                tma_load_3d(a_dst, amap, kx, t.out_base, t.shared ? 0 : 2 * t.e, full_bar);
+              else
+                tma_load_2d(a_dst, amap, kx, t.a_row, full_bar);
+            }
+            tma_load_2d(b_dst, &bmaps[bb.map[0]], kx, b_row0, full_bar);
+            if (bb.n > 1)
+              tma_load_2d(b_dst + bb.rows[0] * 128, &bmaps[bb.map[1]], kx, b_row0 + bb.rows[0],
+                          full_bar);
+            issued_parity[stage] = static_cast<int>(phase);
+          }
+        }
+      }
+      if (!ok) {
+        // Wait (bounded) for this thread's copies still in flight before the CTA exits.
+        for (int s2 = 0; s2 < STAGES; ++s2)
+          if (issued_parity[s2] >= 0) {
+            const uint32_t bar = smem_u32(&tail->full[s2]);
+            const long long t0 = cycles_now();
+            while (!mbar_try_wait(bar, static_cast<uint32_t>(issued_parity[s2])) &&
+                   cycles_now() - t0 < kWaitLimitCycles) {
             }
           }
-          // (the peer's boxes in the unconverted modes complete on the
-          // leader's barrier: nothing local to wait for on abort)
-          if (!(CONV == CONV_NONE && rank == 1)) issued_parity[stage] = static_cast<int>(phase);
-          if (++stage == kBufs) {
-            stage = 0;
+      }
+    }
+    __syncwarp();
+  } else if (warp == CODE_WARP) {
+    // ------------------------------------------- int4 codes (code ring) --
+    // Lane 0 loads each k-step's packed codes (128 rows x 32 bytes) into ring
+    // slot it % kCodeSlots (complete_tx on cfull), paced by the converters
+    // freeing slots, not by the MMA.
+    if (conv_int4(CONV) && lane == 0) {
+      int slot = 0;
+      uint32_t phase = 0;
+      int issued_parity[kCodeSlots];
+#pragma unroll
+      for (int s2 = 0; s2 < kCodeSlots; ++s2) issued_parity[s2] = -1;
+      bool ok = true;
+      for (int tile = pair_id; tile < ntiles && ok; tile += num_pairs) {
+        const Tile t = decode_tile(p, tile, rank);
+        if (!t.valid) continue;
+        const CUtensorMap *amap = t.shared ? &maps.a_shared : &maps.a_routed;
+        for (int ks = 0; ks < t.nk; ++ks) {
+          if (!mbar_wait_bounded(smem_u32(&tail->cempty[slot]), phase ^ 1, abort_flag, p.status,
+                                 DEV_TIMEOUT_PRODUCER)) {
+            ok = false;
+            break;
+          }
+          const uint32_t cfull_bar = smem_u32(&tail->cfull[slot]);
+          const uint32_t c_dst = code_ring + slot * A_CODE_BYTES;
+          const int kx = (t.k0 + ks) * (BK / 2);
+          mbar_arrive_expect_tx(cfull_bar, A_CODE_BYTES);
+          if (p.mode == MODE_GATEUP) {
+            tma_load_2d(c_dst, amap, kx, t.a_row, cfull_bar);
+            tma_load_2d(c_dst + A_CODE_BYTES / 2, amap, kx, t.a_row2, cfull_bar);
+          } else {
+            tma_load_2d(c_dst, amap, kx, t.a_row, cfull_bar);
+          }
+          issued_parity[slot] = static_cast<int>(phase);
+          if (++slot == kCodeSlots) {
+            slot = 0;
             phase ^= 1;
           }
         }
       }
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-    }
-    if (!ok && lane == 0) {
-      // Wait (bounded) for copies still in flight before the CTA exits.
-      for (int s2 = 0; s2 < kBufs; ++s2)
-        if (issued_parity[s2] >= 0) {
-          const uint32_t bar = INT4 ? smem_u32(&tail->cfull[s2]) : smem_u32(&tail->full[s2]);
-          const long long t0 = cycles_now();
-          while (!mbar_try_wait(bar, static_cast<uint32_t>(issued_parity[s2])) &&
-                 cycles_now() - t0 < kWaitLimitCycles) {
+      if (!ok) {
+        for (int s2 = 0; s2 < kCodeSlots; ++s2)
+          if (issued_parity[s2] >= 0) {
+            const uint32_t bar = smem_u32(&tail->cfull[s2]);
+            const long long t0 = cycles_now();
+            while (!mbar_try_wait(bar, static_cast<uint32_t>(issued_parity[s2])) &&
+                   cycles_now() - t0 < kWaitLimitCycles) {
+            }
           }
-        }
-    }
-    __syncwarp();
-  } else if (warp >= B_WARP0 && warp < B_WARP0 + B_WARPS) {
-    // ------------------------------------------------- token rows (cp.async) --
-    // Warp group g owns pipeline stage g: for every k-step that lands in its
-    // stage it copies this CTA's half of the B slice (nmma / 2 rows of 128
-    // bytes), each warp of the group every B_WARPS_PER_STAGE-th group of four
-    // rows, waits for its own copies, fences them for the tensor core and
-    // arrives on the stage's full barrier.  Lane l copies 16-byte chunk l % 8
-    // of rows 4 j + l / 8.  (Weight tiles stay on TMA: loading them with
-    // cp.async from these warps measured 1.6x slower.)
-    const int bw = warp - B_WARP0;
-    const int g = bw / B_WARPS_PER_STAGE;
-    const int gq = bw - g * B_WARPS_PER_STAGE;
-    int *rows_tab = row_tab + bw * kRowTab;          // my rows' element offsets
-    const int c = lane & 7;
-    const int rsub = lane >> 3;
-    const __nv_bfloat16 *bsrc = reinterpret_cast<const __nv_bfloat16 *>(p.b);
-    const uint32_t stage_b = smem_base + g * STAGE_BYTES + A_BYTES;
-    const uint32_t full_bar = smem_u32(&tail->full[g]);
-    const uint32_t empty_bar = smem_u32(&tail->empty[g]);
-    const int btid = bw * 32 + lane;
-    auto prefetch_b = [&](int tile_id) {
-      if (!(p.prefetch & 2) || tile_id >= ntiles) return;
-      const Tile u = decode_tile(p, tile_id, rank);
-      if (!u.valid) return;
-      const uint32_t kbytes = static_cast<uint32_t>(u.nk * BK * 2);
-      const int half = u.nmma / 2;
-      for (int rb = btid; rb < half; rb += B_WARPS * 32) {
-        const int r = rank * half + rb;
-        if (r < u.nrows)
-          prefetch_l2_bulk(bsrc + static_cast<size_t>(b_row(p, u, r)) * p.ldb + u.k0 * BK, kbytes);
-      }
-    };
-    if (pair_id < ntiles) prefetch_b(pair_id);
-    int it = 0;   // k-step counter over all tiles of this CTA
-    bool ok = true;
-    int boxes_parity = -1;   // int4, b_tma: phase of this warp's last token-row boxes
-    for (int tile = pair_id; tile < ntiles && ok; tile += num_pairs) {
-      const Tile t = decode_tile(p, tile, rank);
-      prefetch_b(tile + num_pairs);
-      if (!t.valid) continue;
-      bool table_ready = false;
-      const int half = t.nmma / 2;
-      const int nquads = half / 4;
-      for (int ks = 0; ks < t.nk; ++ks, ++it) {
-        if ((it % STAGES) != g) continue;
-        if (!table_ready) {
-          __syncwarp();   // previous tile's table no longer read
-          for (int e = lane; e < kRowTab; e += 32) {
-            const int r = 4 * (gq + B_WARPS_PER_STAGE * (e >> 2)) + (e & 3);
-            rows_tab[e] = (r < half) ? b_row(p, t, rank * half + r) * p.ldb : 0;
-          }
-          __syncwarp();
-          table_ready = true;
-        }
-        const uint32_t phase = static_cast<uint32_t>(it / STAGES) & 1u;
-        int got = 1;
-        if (lane == 0)
-          got = mbar_wait_bounded(empty_bar, phase ^ 1, abort_flag, p.status, DEV_TIMEOUT_PRODUCER);
-        got = __shfl_sync(0xffffffffu, got, 0);
-        if (!got) {
-          ok = false;
-          break;
-        }
-        if (conv_int4(CONV) && gq == 0 && lane == 0) {
-          // int4: the TMA warp streams codes only; this CTA's token-row boxes
-          // (down: h rows, consecutive) come from here, on the full barrier
-          const int b_boxes = p.b_tma ? t.nmma / 2 / kBTmaRows : 0;
-          mbar_arrive_expect_tx(full_bar, static_cast<uint32_t>(b_boxes * kBTmaRows * BK * 2));
-          const int b_row0 = t.row0 + rank * (t.nmma / 2);
-          for (int i = 0; i < b_boxes; ++i)
-            tma_load_2d(stage_b + i * kBTmaRows * 128, &map_b, (t.k0 + ks) * BK,
-                        b_row0 + i * kBTmaRows, full_bar);
-          if (b_boxes > 0) boxes_parity = static_cast<int>(phase);
-        }
-        const int kc = (t.k0 + ks) * BK + c * 8;
-        for (int j = gq, e = rsub; j < (p.b_tma ? 0 : nquads); j += B_WARPS_PER_STAGE, e += 4) {
-          const int r = 4 * j + rsub;
-          const uint32_t dst = stage_b + r * 128 + static_cast<uint32_t>((c ^ (r & 7)) << 4);
-          cp_async16(dst, bsrc + rows_tab[e] + kc, 16u);
-        }
-        cp_async_commit();
-        cp_async_wait<0>();
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          if (CONV == CONV_NONE && rank == 1) mbar_arrive_cluster(mapa_shared(full_bar, 0));
-          else mbar_arrive(full_bar);
-        }
-        if constexpr (CONV == CONV_BF16_TO_F16) {
-          // this warp's share of the stage's conversion (team warps 1, 2)
-          if (!convert_stage_bf16(p, g, phase, 1 + gq, rank, smem_base, tail, abort_flag, lane)) {
-            ok = false;
-            break;
-          }
-        }
-      }
-    }
-    if (!ok && boxes_parity >= 0) {
-      // Wait (bounded) for this warp's boxes still in flight before the CTA exits.
-      const long long t0 = cycles_now();
-      while (!mbar_try_wait(full_bar, static_cast<uint32_t>(boxes_parity)) &&
-             cycles_now() - t0 < kWaitLimitCycles) {
       }
     }
     __syncwarp();
@@ -745,29 +690,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         for (int tile = pair_id; tile < ntiles && ok; tile += num_pairs) {
           const Tile t = decode_tile(p, tile, 0);
           if (!t.valid) continue;
-          {
-            const bool w_ok = mbar_wait_bounded_cluster(smem_u32(&tail->tmem_empty[acc]), aphase ^ 1,
-                                                        abort_flag, p.status, DEV_TIMEOUT_MMA);
-            if (!w_ok) {
-              ok = false;
-              break;
-            }
+          if (!mbar_wait_bounded_cluster(smem_u32(&tail->tmem_empty[acc]), aphase ^ 1, abort_flag,
+                                         p.status, DEV_TIMEOUT_MMA)) {
+            ok = false;
+            break;
           }
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + acc * ACC_COLS;
           const bool f16 = conv_to_f16(CONV) || (CONV == CONV_NONE && p.ab_f16);
           const uint32_t idesc = f16 ? idesc_f16_f32(PAIR_M, t.nmma) : idesc_bf16_f32(PAIR_M, t.nmma);
           for (int ks = 0; ks < t.nk; ++ks) {
-            // unconverted modes: both CTAs' producers signal this CTA's full
-            // barrier directly; otherwise the stage finishers' ready barrier
+            // unconverted modes: both CTAs' boxes complete on this CTA's full
+            // barrier; otherwise the converter teams' ready barrier (CTA-scope
+            // acquire, as the converters' arrivals are CTA-scope releases:
+            // measured 2-3 % faster than a cluster-scope acquire)
             const uint32_t stage_bar = CONV == CONV_NONE ? smem_u32(&tail->full[stage])
                                                          : smem_u32(&tail->ready[stage]);
-            // (CTA-scope acquire, as the producers' arrivals are CTA-scope
-            // releases: measured 2-3 % faster on the down and int4 GEMMs
-            // than a cluster-scope acquire)
-            const bool r_ok = mbar_wait_bounded(stage_bar, phase, abort_flag, p.status,
-                                                DEV_TIMEOUT_MMA);
-            if (!r_ok) {
+            if (!mbar_wait_bounded(stage_bar, phase, abort_flag, p.status, DEV_TIMEOUT_MMA)) {
               ok = false;
               break;
             }
@@ -804,19 +743,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     }
     __syncwarp();
   } else if (warp >= FIN_WARP0) {
-    // --------------------------------------------------- stage finishers --
-    // bf16 -> fp16: finisher warp f < STAGES owns pipeline stage f and is warp
-    // 0 of the stage's conversion team (with the stage's two token-row
-    // producers): once this CTA's stage is full it converts its share of the
-    // weight tile in place and arrives on the pair leader's ready barrier.
-    // int4: team g (finishers kInt4Warps g ..) takes the k-steps with
-    // it % kInt4Groups == g, each warp expanding its share of the weight rows
-    // as soon as the codes land and the stage is free, overlapping the
+    // ------------------------------------------------------- converters --
+    // Team g (converters kInt4Warps g ..) takes the k-steps with
+    // it % kInt4Groups == g.  int4: each warp expands its share of the weight
+    // rows as soon as the codes land and the stage is free, overlapping the
     // token-row copies; the codes run up to kCodeSlots k-steps ahead in their
-    // own ring.  Unconverted modes need no finisher: the producers signal the
-    // leader.
+    // own ring.  bf16 -> fp16: each warp converts its 32 rows once the stage's
+    // boxes have landed.  Unconverted modes need no converter.
     const int f = warp - FIN_WARP0;
     const int ntiles_fin = CONV == CONV_NONE ? 0 : ntiles;
+    const int q = f % kInt4Warps;
     int it = 0;
     bool ok = true;
     // int4: the row scales of the team's next k-step in the tile (ks +
@@ -828,11 +764,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       const Tile t = decode_tile(p, tile, rank);
       if (!t.valid) continue;
       for (int ks = 0; ks < t.nk; ++ks, ++it) {
-        const int stage = it % STAGES;
-        const uint32_t phase = static_cast<uint32_t>(it / STAGES) & 1u;
+        if (it % kInt4Groups != f / kInt4Warps) continue;
         if constexpr (conv_int4(CONV)) {
-          if (it % kInt4Groups != f / kInt4Warps) continue;
-          const int q = f % kInt4Warps;
           float sv[kInt4Batches], bv[kInt4Batches];
 #pragma unroll
           for (int b = 0; b < kInt4Batches; ++b) {
@@ -851,8 +784,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
           ok = convert_stage_int4<CONV>(p, q, sv, bv, it, rank, smem_base, code_ring, tail,
                                         abort_flag, lane);
         } else {
-          if (stage != f) continue;
-          ok = convert_stage_bf16(p, stage, phase, 0, rank, smem_base, tail, abort_flag, lane);
+          ok = convert_stage_bf16(p, q, it, rank, smem_base, tail, abort_flag, lane);
         }
         if (!ok) break;
       }
@@ -1005,7 +937,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
   if (warp == MMA_WARP) tmem_dealloc_pair(tmem_base, TMEM_COLS);
 }
 
-
 // Stand-alone dequantisation of int4 weights into a bf16 (or fp16) array,
 // with the same per-pair arithmetic as the GEMMs' in-shared-memory expansion
 // (so a GEMM on the expanded array sees the same operands).  One thread turns
@@ -1113,32 +1044,37 @@ int gemm_max_grid(int num_sms) {
 }
 
 cudaError_t launch_tc_gemm(const CUtensorMap &a_routed, const CUtensorMap &a_shared,
-                           const CUtensorMap &b, const GemmParams &p, int conv, int grid, bool pdl,
-                           cudaStream_t stream) {
+                           const CUtensorMap (&b)[4], const CUtensorMap (&b2)[4],
+                           const GemmParams &p, int conv, int grid, bool pdl, cudaStream_t stream) {
   grid &= ~1;   // whole CTA pairs
   if (grid < 2) grid = 2;
+  GemmMaps maps;
+  maps.a_routed = a_routed;
+  maps.a_shared = a_shared;
+  for (int i = 0; i < 4; ++i) {
+    maps.b[i] = b[i];
+    maps.b2[i] = b2[i];
+  }
   const dim3 g(grid), bl(NUM_THREADS);
   switch (conv) {
     case CONV_BF16_TO_F16:
       return launch_kernel(tc_gemm_kernel<CONV_BF16_TO_F16>, g, bl, kGemmSmemBytes, stream, pdl,
-                           a_routed, a_shared, b, p);
+                           maps, p);
     case CONV_INT4_TO_BF16:
       return launch_kernel(tc_gemm_kernel<CONV_INT4_TO_BF16>, g, bl, kGemmSmemBytes, stream, pdl,
-                           a_routed, a_shared, b, p);
+                           maps, p);
     case CONV_INT4_TO_F16:
       return launch_kernel(tc_gemm_kernel<CONV_INT4_TO_F16>, g, bl, kGemmSmemBytes, stream, pdl,
-                           a_routed, a_shared, b, p);
+                           maps, p);
     case CONV_INT4A_TO_BF16:
       return launch_kernel(tc_gemm_kernel<CONV_INT4A_TO_BF16>, g, bl, kGemmSmemBytes, stream, pdl,
-                           a_routed, a_shared, b, p);
+                           maps, p);
     case CONV_INT4A_TO_F16:
       return launch_kernel(tc_gemm_kernel<CONV_INT4A_TO_F16>, g, bl, kGemmSmemBytes, stream, pdl,
-                           a_routed, a_shared, b, p);
+                           maps, p);
     default:
-      return launch_kernel(tc_gemm_kernel<CONV_NONE>, g, bl, kGemmSmemBytes, stream, pdl, a_routed,
-                           a_shared, b, p);
+      return launch_kernel(tc_gemm_kernel<CONV_NONE>, g, bl, kGemmSmemBytes, stream, pdl, maps, p);
   }
 }
 
 }  // namespace moe
-
