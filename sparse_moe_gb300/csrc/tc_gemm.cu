@@ -60,13 +60,15 @@ namespace moe {
 
 constexpr int BM = 128;                 // A rows per CTA (MMA M = 256 per pair)
 constexpr int PAIR_M = 2 * BM;
-constexpr int BK = 64;                  // K per pipeline stage (128-byte rows)
+constexpr int BK = 64;                  // K per k-step (128-byte rows): one half of a stage
+constexpr int HALVES = 2;               // k-steps per pipeline stage
 constexpr int BN_MAX = kBlockRowsMax;   // max MMA N (tokens per tile)
 constexpr int BN_HALF = BN_MAX / 2;     // token rows staged per CTA
-constexpr int STAGES = 6;               // even: producer p fills the stages it % 2 == p
+constexpr int STAGES = 3;               // pipeline stages of HALVES k-steps each
 constexpr int A_BYTES = BM * BK * 2;            // 16 KB
 constexpr int B_BYTES = BN_HALF * BK * 2;       // 16 KB
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // 32 KB
+constexpr int SLOT_BYTES = A_BYTES + B_BYTES;   // 32 KB: one k-step (A, then B)
+constexpr int STAGE_BYTES = HALVES * SLOT_BYTES;
 // int4 weights: a k-step's packed codes (BM rows x BK/2 bytes) land in a ring
 // of their own, from which the converter warps expand them into the stage.
 constexpr int A_CODE_BYTES = BM * BK / 2;       // 4 KB: one k-step's int4 codes
@@ -77,60 +79,79 @@ constexpr int TMEM_COLS = 512;                  // two buffers
 constexpr int kProducers = 2;                   // warps 0, 1: stage producers (lane 0)
 constexpr int CODE_WARP = 2;                    // int4 code ring producer (lane 0)
 constexpr int MMA_WARP = 3;
-constexpr int EPI_WARP0 = 4;                    // warps 4..7 (TMEM lane quarter = warp % 4)
-constexpr int FIN_WARP0 = EPI_WARP0 + 4;        // warps 8..15: converters
-constexpr int FIN_WARPS = 8;
-constexpr int NUM_THREADS = (FIN_WARP0 + FIN_WARPS) * 32;
-constexpr int XCH_FLOATS = 2 * 2 * 2 * 8 * 32;  // [buf][pair][dir][8 cols][32 lanes]
-constexpr int EPI_STAGE_BYTES = 4 * 16 * 64;    // per epilogue warp: 16 rows x 64 bytes
-static_assert(STAGES % kProducers == 0, "each stage has one producer");
+constexpr int EPI_WARP0 = 4;                    // epilogue groups of four warps from warp 4
+constexpr int FIN_WARPS = 8;                    // converters (after the epilogue warps)
+constexpr int XCH_FLOATS = 2 * 2 * 2 * 8 * 32;  // per group: [buf][pair][dir][8 cols][32 lanes]
+constexpr int EPI_WARP_STAGE_BYTES = 16 * 64;   // per epilogue warp: 16 rows x 64 bytes
 static_assert(EPI_WARP0 % 4 == 0, "epilogue warp q reads TMEM lanes 32 q .. 32 q + 31");
 
-// Warps that convert one stage's weight tile, per CTA: kInt4Warps converter
-// warps, each handling kInt4Batches batches of 32 weight rows (int4: expanding
-// codes from the ring; bf16 -> fp16: converting the landed tile in place), the
-// converters forming kInt4Groups teams that take k-steps in turn (team g:
-// it % kInt4Groups == g).  Measured at T=4096 (int4): four warps of 32 rows
-// per k-step (two teams) beat two of 64 rows (four teams) by 20 %.
+// Epilogue groups: four warps (one per TMEM lane quarter) each; group g
+// drains the 16-column chunks g, g + G, g + 2G, ... of a tile.  Without a
+// conversion the converter warps are not needed and a second group takes
+// their place (the epilogue of a 256-column gate/up tile otherwise takes
+// longer than the tile's MMAs).
+template <int CONV> __host__ __device__ constexpr int epi_groups() { return CONV == CONV_NONE ? 2 : 1; }
+template <int CONV> __host__ __device__ constexpr int fin_warp0() {
+  return EPI_WARP0 + 4 * epi_groups<CONV>();
+}
+template <int CONV> __host__ __device__ constexpr int num_threads() {
+  return (fin_warp0<CONV>() + (CONV == CONV_NONE ? 0 : FIN_WARPS)) * 32;
+}
+
+// Warps that convert one stage's weight tiles, per CTA: kInt4Warps converter
+// warps per k-step, each handling kInt4Batches batches of 32 weight rows (int4:
+// expanding codes from the ring; bf16 -> fp16: converting the landed tile in
+// place).  The converters form kInt4Groups = HALVES teams: team h takes half
+// h of every stage.  Measured at T=4096 (int4): four warps of 32 rows per
+// k-step beat two of 64 rows by 20 %.
 //
-// A team's next k-step is kInt4Groups k-steps later; its parity waits on the
-// stage and code-ring barriers stay unambiguous only if no team can reach a
-// barrier phase two ahead of the completed one: every ring slot and every
-// stage is used by one team (kCodeSlots and STAGES multiples of kInt4Groups).
+// A team's next k-step is in the next stage; its parity waits on the stage
+// and code-ring barriers stay unambiguous only if no team can reach a barrier
+// phase two ahead of the completed one: every ring slot belongs to one team
+// (kCodeSlots a multiple of HALVES, ring slot = half-slot counter % kCodeSlots)
+// and a team waits for a stage's release before each use.
 constexpr int kInt4Warps = 4;
 constexpr int kInt4Batches = (BM / 32) / kInt4Warps;
 constexpr int kInt4Groups = FIN_WARPS / kInt4Warps;
 static_assert(kInt4Warps * kInt4Batches * 32 == BM && kInt4Groups * kInt4Warps == FIN_WARPS,
               "converter teams");
-static_assert(kCodeSlots % kInt4Groups == 0 && STAGES % kInt4Groups == 0,
+static_assert(kInt4Groups == HALVES && kCodeSlots % HALVES == 0,
               "converter teams must not alias barrier phases");
 template <int CONV> __host__ __device__ constexpr int conv_team() {
-  return CONV == CONV_NONE ? 1 : kInt4Warps;
+  return CONV == CONV_NONE ? 1 : HALVES * kInt4Warps;
 }
 
 struct SmemTail {
   uint64_t full[STAGES];        // unconverted: leader's, both CTAs' boxes; else local (A + B or B)
   uint64_t cfull[kCodeSlots];   // local, int4: a k-step's weight codes landed in the ring (TMA)
   uint64_t cempty[kCodeSlots];  // local, int4: the k-step's converters hold their codes
-  uint64_t ready[STAGES];       // leader: both CTAs' conversion teams
+  uint64_t ready[STAGES];       // leader: both CTAs' converter teams (both halves)
   uint64_t empty[STAGES];       // local: arrives from the leader's commit
   uint64_t tmem_full[2];        // local: arrives from the leader's commit
-  uint64_t tmem_empty[2];       // leader: 4 + 4 epilogue warps
+  uint64_t tmem_empty[2];       // leader: every epilogue warp of both CTAs
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
-  int vote[4];
+  int vote[8];
 };
 
-constexpr size_t kGemmSmemBytes = 1024 /*align slack*/ + STAGES * STAGE_BYTES +
-                                  XCH_FLOATS * sizeof(float) + EPI_STAGE_BYTES +
-                                  sizeof(SmemTail) + 128 /*ring alignment*/ +
-                                  kCodeSlots * A_CODE_BYTES;
+// Shared memory: the stages, the epilogue groups' exchange buffers and
+// staging rows, the barriers, and (int4) the code ring.
+template <int CONV> __host__ __device__ constexpr size_t gemm_smem_bytes() {
+  return 1024 /*align slack*/ + STAGES * STAGE_BYTES +
+         epi_groups<CONV>() * (XCH_FLOATS * sizeof(float) + 4 * EPI_WARP_STAGE_BYTES) +
+         sizeof(SmemTail) + (conv_int4(CONV) ? 128 /*ring alignment*/ + kCodeSlots * A_CODE_BYTES : 0);
+}
+static_assert(gemm_smem_bytes<CONV_NONE>() <= 227 * 1024 &&
+                  gemm_smem_bytes<CONV_INT4_TO_BF16>() <= 227 * 1024 &&
+                  gemm_smem_bytes<CONV_BF16_TO_F16>() <= 227 * 1024,
+              "shared memory per CTA");
 
 struct Tile {
   int valid;
   int row0, nrows, nmma;
-  int nk;
+  int nk;              // k-steps (of BK)
+  int ns;              // pipeline stages (HALVES k-steps each; the last may hold one)
   int k0;              // first k-step (router split-K: split * nk)
   int split;           // router split-K part of this tile
   int m;
@@ -191,6 +212,7 @@ __device__ __forceinline__ Tile decode_tile(const GemmParams &p, int tile, int r
     t.a_row2 = 0;
   }
   t.a_valid_rows = t.out_limit - t.out_base;
+  t.ns = (t.nk + HALVES - 1) / HALVES;
   return t;
 }
 
@@ -395,54 +417,71 @@ __device__ __forceinline__ void arrive_ready(SmemTail *tail, int stage, int rank
   else mbar_arrive_cluster(mapa_shared(ready, 0));
 }
 
-// bf16 -> fp16 converter q of k-step `it` (stage it % STAGES): a bounded wait
-// for the stage's boxes (weights and token rows) to land in this CTA, its 32
-// rows converted in place, and its arrival on the pair leader's ready
-// barrier.  Returns false on a timeout or abort.
-__device__ __forceinline__ bool convert_stage_bf16(const GemmParams &p, int q, int it, int rank,
-                                                   uint32_t smem_base, SmemTail *tail,
+// Where converter work sits in the pipeline: stage counter st (stage st %
+// STAGES, phase (st / STAGES) & 1), half h of the stage (k-step slot
+// (st % STAGES) * HALVES + h of the shared memory), and the half-slot counter
+// hs = HALVES * st + h (int4 code ring slot hs % kCodeSlots, phase
+// (hs / kCodeSlots) & 1).  `real`: the tile has a k-step in this half (the
+// second half of a tile's last stage is empty when its k-step count is odd;
+// the converters still take part in its barriers, so that every phase sees
+// the same arrivals).
+struct ConvPos {
+  int st, h, hs;
+  bool real;
+};
+
+// bf16 -> fp16 converter q of one half-stage: a bounded wait for the stage's
+// boxes (weights and token rows) to land in this CTA, its 32 rows converted
+// in place, and its arrival on the pair leader's ready barrier.  Returns false
+// on a timeout or abort.
+__device__ __forceinline__ bool convert_stage_bf16(const GemmParams &p, int q, const ConvPos &c,
+                                                   int rank, uint32_t smem_base, SmemTail *tail,
                                                    volatile int *abort_flag, int lane) {
-  const int stage = it % STAGES;
-  const uint32_t phase = static_cast<uint32_t>(it / STAGES) & 1u;
+  const int stage = c.st % STAGES;
+  const uint32_t phase = static_cast<uint32_t>(c.st / STAGES) & 1u;
   int got = 1;
   if (lane == 0)
     got = mbar_wait_bounded(smem_u32(&tail->full[stage]), phase, abort_flag, p.status,
                             DEV_TIMEOUT_CONVERTER);
   if (!__shfl_sync(0xffffffffu, got, 0)) return false;
-  convert_rows_bf16_to_f16(smem_base + stage * STAGE_BYTES, q, lane);
-  fence_proxy_async_smem();
+  if (c.real) {
+    convert_rows_bf16_to_f16(smem_base + (stage * HALVES + c.h) * SLOT_BYTES, q, lane);
+    fence_proxy_async_smem();
+  }
   __syncwarp();
   if (lane == 0) arrive_ready(tail, stage, rank);
   return true;
 }
 
-// int4 converter q (0 .. kInt4Warps - 1) of k-step `it` (stage it % STAGES,
-// ring slot it % kCodeSlots): takes its codes (batches q * kInt4Batches + b)
-// from the ring as soon as they land and frees its share of the slot, waits
-// until the MMA has released the stage's A region, expands its weight rows
-// into it, and arrives on the pair leader's ready barrier (the last converter
-// only after the stage's token rows have landed).  sv, bv: this lane's row scales and biases, one per batch,
-// loaded by the caller before the waits.  Returns false on a timeout or abort.
+// int4 converter q (0 .. kInt4Warps - 1) of one half-stage: takes its codes
+// (batches q * kInt4Batches + b) from the ring as soon as they land and frees
+// its share of the slot, waits until the MMA has released the stage, expands
+// its weight rows into the half's A region, and arrives on the pair leader's
+// ready barrier (the last converter only after the stage's token rows have
+// landed).  sv, bv: this lane's row scales and biases, one per batch, loaded
+// by the caller before the waits.  Returns false on a timeout or abort.
 template <int CONV>
 __device__ __forceinline__ bool convert_stage_int4(const GemmParams &p, int q,
                                                    const float (&sv)[kInt4Batches],
-                                                   const float (&bv)[kInt4Batches], int it,
-                                                   int rank, uint32_t smem_base,
+                                                   const float (&bv)[kInt4Batches],
+                                                   const ConvPos &c, int rank, uint32_t smem_base,
                                                    uint32_t code_ring, SmemTail *tail,
                                                    volatile int *abort_flag, int lane) {
-  const int stage = it % STAGES, slot = it % kCodeSlots;
-  const uint32_t sph = static_cast<uint32_t>(it / STAGES) & 1u;
-  const uint32_t cph = static_cast<uint32_t>(it / kCodeSlots) & 1u;
-  const uint32_t tile = smem_base + stage * STAGE_BYTES;
+  const int stage = c.st % STAGES, slot = c.hs % kCodeSlots;
+  const uint32_t sph = static_cast<uint32_t>(c.st / STAGES) & 1u;
+  const uint32_t cph = static_cast<uint32_t>(c.hs / kCodeSlots) & 1u;
+  const uint32_t tile = smem_base + (stage * HALVES + c.h) * SLOT_BYTES;
   int got = 1;
   if (lane == 0)
     got = mbar_wait_bounded(smem_u32(&tail->cfull[slot]), cph, abort_flag, p.status,
                             DEV_TIMEOUT_CONVERTER);
   if (!__shfl_sync(0xffffffffu, got, 0)) return false;
   uint32_t w[kInt4Batches][8];
+  if (c.real) {
 #pragma unroll
-  for (int b = 0; b < kInt4Batches; ++b)
-    load_codes_int4(code_ring + slot * A_CODE_BYTES, q * kInt4Batches + b, lane, w[b]);
+    for (int b = 0; b < kInt4Batches; ++b)
+      load_codes_int4(code_ring + slot * A_CODE_BYTES, q * kInt4Batches + b, lane, w[b]);
+  }
   __syncwarp();
   if (lane == 0) {
     mbar_arrive(smem_u32(&tail->cempty[slot]));
@@ -450,15 +489,17 @@ __device__ __forceinline__ bool convert_stage_int4(const GemmParams &p, int q,
                             DEV_TIMEOUT_CONVERTER);
   }
   if (!__shfl_sync(0xffffffffu, got, 0)) return false;
+  if (c.real) {
 #pragma unroll
-  for (int b = 0; b < kInt4Batches; ++b)
-    expand_rows_int4<conv_to_f16(CONV), conv_affine(CONV)>(tile, w[b], q * kInt4Batches + b,
-                                                           sv[b], bv[b], lane);
-  fence_proxy_async_smem();
+    for (int b = 0; b < kInt4Batches; ++b)
+      expand_rows_int4<conv_to_f16(CONV), conv_affine(CONV)>(tile, w[b], q * kInt4Batches + b,
+                                                             sv[b], bv[b], lane);
+    fence_proxy_async_smem();
+  }
   __syncwarp();
   if (lane == 0) {
-    // one converter per CTA checks the token rows: the leader's ready phase
-    // needs every converter's arrival
+    // one converter per CTA and half checks the token rows: the leader's
+    // ready phase needs every converter's arrival
     if (q == kInt4Warps - 1)
       got = mbar_wait_bounded(smem_u32(&tail->full[stage]), sph, abort_flag, p.status,
                               DEV_TIMEOUT_CONVERTER);
@@ -490,14 +531,16 @@ struct GemmMaps {
 };
 
 template <int CONV>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(num_threads<CONV>(), 1)
     tc_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
+  constexpr int G = epi_groups<CONV>();
+  constexpr int FIN_WARP0 = fin_warp0<CONV>();
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
-  float *xch = reinterpret_cast<float *>(smem + STAGES * STAGE_BYTES);
-  uint8_t *epi_stage = reinterpret_cast<uint8_t *>(xch + XCH_FLOATS);
-  SmemTail *tail = reinterpret_cast<SmemTail *>(epi_stage + EPI_STAGE_BYTES);
+  float *xch_all = reinterpret_cast<float *>(smem + STAGES * STAGE_BYTES);   // [G][XCH_FLOATS]
+  uint8_t *epi_stage = reinterpret_cast<uint8_t *>(xch_all + G * XCH_FLOATS);
+  SmemTail *tail = reinterpret_cast<SmemTail *>(epi_stage + 4 * G * EPI_WARP_STAGE_BYTES);
   const uint32_t code_ring = (smem_u32(tail + 1) + 127u) & ~127u;   // int4: kCodeSlots x 4 KB
   volatile int *abort_flag = &tail->abort_flag;
   pdl_trigger();   // the next kernel may start its set-up as SMs free up
@@ -522,7 +565,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(smem_u32(&tail->tmem_full[a]), 1);
-      mbar_init(smem_u32(&tail->tmem_empty[a]), 8);
+      mbar_init(smem_u32(&tail->tmem_empty[a]), 2 * 4 * G);
     }
     mbar_init(smem_u32(&tail->drain), 1);
     tail->abort_flag = 0;
@@ -547,12 +590,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
 
   if (warp < kProducers) {
     // ------------------------------------------------- stage producers --
-    // Lane 0 of producer warp pp fills the stages of the k-steps it with
-    // it % kProducers == pp: it waits until the MMA has released the stage,
-    // then issues this CTA's boxes: the weight box (unless the weights are
-    // int4 codes, which come through the code ring) and the token-row boxes.
-    // Unconverted modes: both CTAs' boxes complete on the leader's full
-    // barrier, which expects the pair's bytes (cta_group::2 loads).
+    // Lane 0 of producer warp pp fills the stages st with st % kProducers ==
+    // pp (st counts this CTA's stages over all its tiles): it waits until the
+    // MMA has released the stage, then issues this CTA's boxes for each of the
+    // stage's k-steps: the weight box (unless the weights are int4 codes,
+    // which come through the code ring) and the token-row boxes.  Unconverted
+    // modes: both CTAs' boxes complete on the leader's full barrier, which
+    // expects the pair's bytes (cta_group::2 loads).
     constexpr bool INT4 = conv_int4(CONV);
     const int pp = warp;
     int issued_parity[STAGES];
@@ -560,7 +604,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     for (int s2 = 0; s2 < STAGES; ++s2) issued_parity[s2] = -1;
     bool ok = true;
     if (lane == 0) {
-      int it = 0;
+      int st = 0;
       for (int tile = pair_id; tile < ntiles && ok; tile += num_pairs) {
         const Tile t = decode_tile(p, tile, rank);
         if (!t.valid) continue;
@@ -571,45 +615,54 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         const BBoxes bb = b_boxes(half);
         const int b_row0 = (b_from_x ? t.row0 - p.shared_row0 : t.row0) + rank * half;
         const uint32_t b_bytes = static_cast<uint32_t>((bb.rows[0] + bb.rows[1]) * BK * 2);
-        for (int ks = 0; ks < t.nk; ++ks, ++it) {
-          if (it % kProducers != pp) continue;
-          const int stage = it % STAGES;
-          const uint32_t phase = static_cast<uint32_t>(it / STAGES) & 1u;
+        for (int j = 0; j < t.ns; ++j, ++st) {
+          if (st % kProducers != pp) continue;
+          const int stage = st % STAGES;
+          const uint32_t phase = static_cast<uint32_t>(st / STAGES) & 1u;
           if (!mbar_wait_bounded(smem_u32(&tail->empty[stage]), phase ^ 1, abort_flag, p.status,
                                  DEV_TIMEOUT_PRODUCER)) {
             ok = false;
             break;
           }
+          const int nh = min(HALVES, t.nk - j * HALVES);   // k-steps in this stage
           const uint32_t full_bar = smem_u32(&tail->full[stage]);
-          const uint32_t a_dst = smem_base + stage * STAGE_BYTES;
-          const uint32_t b_dst = a_dst + A_BYTES;
-          const int kx = (t.k0 + ks) * BK;
           if constexpr (CONV == CONV_NONE) {
             const uint32_t lead_full = mapa_shared(full_bar, 0);
-            if (rank == 0) mbar_arrive_expect_tx(full_bar, 2 * (A_BYTES + b_bytes));
-            if (p.mode == MODE_GATEUP)
-              tma_load_3d_pair(a_dst, amap, kx, t.out_base, t.shared ? 0 : 2 * t.e, lead_full);
-            else
-              tma_load_2d_pair(a_dst, amap, kx, t.a_row, lead_full);
-            tma_load_2d_pair(b_dst, &bmaps[bb.map[0]], kx, b_row0, lead_full);
-            if (bb.n > 1)
-              tma_load_2d_pair(b_dst + bb.rows[0] * 128, &bmaps[bb.map[1]], kx, b_row0 + bb.rows[0],
-                               lead_full);
+            if (rank == 0) mbar_arrive_expect_tx(full_bar, 2 * nh * (A_BYTES + b_bytes));
+            for (int h = 0; h < nh; ++h) {
+              const uint32_t a_dst = smem_base + (stage * HALVES + h) * SLOT_BYTES;
+              const uint32_t b_dst = a_dst + A_BYTES;
+              const int kx = (t.k0 + j * HALVES + h) * BK;
+              if (p.mode == MODE_GATEUP)
+                tma_load_3d_pair(a_dst, amap, kx, t.out_base, t.shared ? 0 : 2 * t.e, lead_full);
+              else
+                tma_load_2d_pair(a_dst, amap, kx, t.a_row, lead_full);
+              tma_load_2d_pair(b_dst, &bmaps[bb.map[0]], kx, b_row0, lead_full);
+              if (bb.n > 1)
+                tma_load_2d_pair(b_dst + bb.rows[0] * 128, &bmaps[bb.map[1]], kx,
+                                 b_row0 + bb.rows[0], lead_full);
+            }
             // (the peer's boxes complete on the leader's barrier: the leader's
             // producers wait for them on abort)
             if (rank == 0) issued_parity[stage] = static_cast<int>(phase);
           } else {
-            mbar_arrive_expect_tx(full_bar, (INT4 ? 0u : static_cast<uint32_t>(A_BYTES)) + b_bytes);
-            if constexpr (!INT4) {
-              if (p.mode == MODE_GATEUP)
-                tma_load_3d(a_dst, amap, kx, t.out_base, t.shared ? 0 : 2 * t.e, full_bar);
-              else
-                tma_load_2d(a_dst, amap, kx, t.a_row, full_bar);
+            mbar_arrive_expect_tx(full_bar,
+                                  nh * ((INT4 ? 0u : static_cast<uint32_t>(A_BYTES)) + b_bytes));
+            for (int h = 0; h < nh; ++h) {
+              const uint32_t a_dst = smem_base + (stage * HALVES + h) * SLOT_BYTES;
+              const uint32_t b_dst = a_dst + A_BYTES;
+              const int kx = (t.k0 + j * HALVES + h) * BK;
+              if constexpr (!INT4) {
+                if (p.mode == MODE_GATEUP)
+                  tma_load_3d(a_dst, amap, kx, t.out_base, t.shared ? 0 : 2 * t.e, full_bar);
+                else
+                  tma_load_2d(a_dst, amap, kx, t.a_row, full_bar);
+              }
+              tma_load_2d(b_dst, &bmaps[bb.map[0]], kx, b_row0, full_bar);
+              if (bb.n > 1)
+                tma_load_2d(b_dst + bb.rows[0] * 128, &bmaps[bb.map[1]], kx, b_row0 + bb.rows[0],
+                            full_bar);
             }
-            tma_load_2d(b_dst, &bmaps[bb.map[0]], kx, b_row0, full_bar);
-            if (bb.n > 1)
-              tma_load_2d(b_dst + bb.rows[0] * 128, &bmaps[bb.map[1]], kx, b_row0 + bb.rows[0],
-                          full_bar);
             issued_parity[stage] = static_cast<int>(phase);
           }
         }
@@ -630,8 +683,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
   } else if (warp == CODE_WARP) {
     // ------------------------------------------- int4 codes (code ring) --
     // Lane 0 loads each k-step's packed codes (128 rows x 32 bytes) into ring
-    // slot it % kCodeSlots (complete_tx on cfull), paced by the converters
-    // freeing slots, not by the MMA.
+    // slot hs % kCodeSlots (complete_tx on cfull; hs counts half-stages,
+    // including the empty second half of a tile's last stage, whose slot phase
+    // completes with a plain arrival), paced by the converters freeing slots,
+    // not by the MMA.
     if (conv_int4(CONV) && lane == 0) {
       int slot = 0;
       uint32_t phase = 0;
@@ -643,23 +698,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         const Tile t = decode_tile(p, tile, rank);
         if (!t.valid) continue;
         const CUtensorMap *amap = t.shared ? &maps.a_shared : &maps.a_routed;
-        for (int ks = 0; ks < t.nk; ++ks) {
+        for (int ks = 0; ks < t.ns * HALVES; ++ks) {
           if (!mbar_wait_bounded(smem_u32(&tail->cempty[slot]), phase ^ 1, abort_flag, p.status,
                                  DEV_TIMEOUT_PRODUCER)) {
             ok = false;
             break;
           }
           const uint32_t cfull_bar = smem_u32(&tail->cfull[slot]);
-          const uint32_t c_dst = code_ring + slot * A_CODE_BYTES;
-          const int kx = (t.k0 + ks) * (BK / 2);
-          mbar_arrive_expect_tx(cfull_bar, A_CODE_BYTES);
-          if (p.mode == MODE_GATEUP) {
-            tma_load_2d(c_dst, amap, kx, t.a_row, cfull_bar);
-            tma_load_2d(c_dst + A_CODE_BYTES / 2, amap, kx, t.a_row2, cfull_bar);
+          if (ks < t.nk) {
+            const uint32_t c_dst = code_ring + slot * A_CODE_BYTES;
+            const int kx = (t.k0 + ks) * (BK / 2);
+            mbar_arrive_expect_tx(cfull_bar, A_CODE_BYTES);
+            if (p.mode == MODE_GATEUP) {
+              tma_load_2d(c_dst, amap, kx, t.a_row, cfull_bar);
+              tma_load_2d(c_dst + A_CODE_BYTES / 2, amap, kx, t.a_row2, cfull_bar);
+            } else {
+              tma_load_2d(c_dst, amap, kx, t.a_row, cfull_bar);
+            }
+            issued_parity[slot] = static_cast<int>(phase);
           } else {
-            tma_load_2d(c_dst, amap, kx, t.a_row, cfull_bar);
+            mbar_arrive(cfull_bar);   // an empty half: no codes
+            issued_parity[slot] = -1;
           }
-          issued_parity[slot] = static_cast<int>(phase);
           if (++slot == kCodeSlots) {
             slot = 0;
             phase ^= 1;
@@ -699,11 +759,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
           const uint32_t d_tmem = tmem_base + acc * ACC_COLS;
           const bool f16 = conv_to_f16(CONV) || (CONV == CONV_NONE && p.ab_f16);
           const uint32_t idesc = f16 ? idesc_f16_f32(PAIR_M, t.nmma) : idesc_bf16_f32(PAIR_M, t.nmma);
-          for (int ks = 0; ks < t.nk; ++ks) {
+          for (int j = 0; j < t.ns; ++j) {
             // unconverted modes: both CTAs' boxes complete on this CTA's full
             // barrier; otherwise the converter teams' ready barrier (CTA-scope
             // acquire, as the converters' arrivals are CTA-scope releases:
-            // measured 2-3 % faster than a cluster-scope acquire)
+            // measured 2-3 % faster than a cluster-scope acquire).  One wait
+            // per stage of HALVES k-steps: a barrier wait in the issuing thread
+            // costs about as long as four MMAs of N = 256 (measured), so
+            // waiting once per k-step held small tiles to a fraction of the
+            // tensor cores' rate.
             const uint32_t stage_bar = CONV == CONV_NONE ? smem_u32(&tail->full[stage])
                                                          : smem_u32(&tail->ready[stage]);
             if (!mbar_wait_bounded(stage_bar, phase, abort_flag, p.status, DEV_TIMEOUT_MMA)) {
@@ -711,12 +775,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
               break;
             }
             tc_fence_after();
-            const uint32_t a_addr = smem_base + stage * STAGE_BYTES;
-            const uint64_t a_desc = smem_desc_sw128(a_addr);
-            const uint64_t b_desc = smem_desc_sw128(a_addr + A_BYTES);
+            const int nh = min(HALVES, t.nk - j * HALVES);
+            for (int h = 0; h < nh; ++h) {
+              const uint32_t a_addr = smem_base + (stage * HALVES + h) * SLOT_BYTES;
+              const uint64_t a_desc = smem_desc_sw128(a_addr);
+              const uint64_t b_desc = smem_desc_sw128(a_addr + A_BYTES);
 #pragma unroll
-            for (int kk = 0; kk < BK / 16; ++kk)
-              tc_mma_pair(d_tmem, a_desc + 2 * kk, b_desc + 2 * kk, idesc, (ks | kk) != 0);
+              for (int kk = 0; kk < BK / 16; ++kk)
+                tc_mma_pair(d_tmem, a_desc + 2 * kk, b_desc + 2 * kk, idesc,
+                            (j | h | kk) != 0);
+            }
             tc_commit_pair_mc(smem_u32(&tail->empty[stage]), 0x3);
             if (++stage == STAGES) {
               stage = 0;
@@ -744,47 +812,49 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     __syncwarp();
   } else if (warp >= FIN_WARP0) {
     // ------------------------------------------------------- converters --
-    // Team g (converters kInt4Warps g ..) takes the k-steps with
-    // it % kInt4Groups == g.  int4: each warp expands its share of the weight
-    // rows as soon as the codes land and the stage is free, overlapping the
-    // token-row copies; the codes run up to kCodeSlots k-steps ahead in their
-    // own ring.  bf16 -> fp16: each warp converts its 32 rows once the stage's
-    // boxes have landed.  Unconverted modes need no converter.
+    // Team h (converters kInt4Warps h ..) takes half h of every stage.  int4:
+    // each warp expands its share of the weight rows as soon as the codes land
+    // and the stage is free, overlapping the token-row copies; the codes run
+    // up to kCodeSlots k-steps ahead in their own ring.  bf16 -> fp16: each
+    // warp converts its 32 rows once the stage's boxes have landed.  An empty
+    // half (odd k-step count) only takes part in the barriers.  Unconverted
+    // modes have no converter warps.
     const int f = warp - FIN_WARP0;
-    const int ntiles_fin = CONV == CONV_NONE ? 0 : ntiles;
+    const int h = f / kInt4Warps;
     const int q = f % kInt4Warps;
-    int it = 0;
+    int st = 0;
     bool ok = true;
     // int4: the row scales of the team's next k-step in the tile (ks +
-    // kInt4Groups) are loaded while this one converts (a global load's latency
+    // HALVES) are loaded while this one converts (a global load's latency
     // would otherwise sit inside every expansion).
     float sv_next[kInt4Batches] = {}, bv_next[kInt4Batches] = {};
     bool have_next = false;
-    for (int tile = pair_id; tile < ntiles_fin && ok; tile += num_pairs) {
+    for (int tile = pair_id; tile < ntiles && ok; tile += num_pairs) {
       const Tile t = decode_tile(p, tile, rank);
       if (!t.valid) continue;
-      for (int ks = 0; ks < t.nk; ++ks, ++it) {
-        if (it % kInt4Groups != f / kInt4Warps) continue;
+      for (int jj = 0; jj < t.ns; ++jj, ++st) {
+        const int ks = jj * HALVES + h;
+        const ConvPos pos{st, h, HALVES * st + h, ks < t.nk};
         if constexpr (conv_int4(CONV)) {
           float sv[kInt4Batches], bv[kInt4Batches];
 #pragma unroll
           for (int b = 0; b < kInt4Batches; ++b) {
             sv[b] = sv_next[b];
             bv[b] = bv_next[b];
-            if (!have_next)
+            if (!have_next && pos.real)
               load_row_scale<conv_affine(CONV)>(p, t, ks, q * kInt4Batches + b, lane, sv[b], bv[b]);
           }
-          have_next = ks + kInt4Groups < t.nk;
+          have_next = ks + HALVES < t.nk;
           if (have_next) {
 #pragma unroll
             for (int b = 0; b < kInt4Batches; ++b)
-              load_row_scale<conv_affine(CONV)>(p, t, ks + kInt4Groups, q * kInt4Batches + b, lane,
+              load_row_scale<conv_affine(CONV)>(p, t, ks + HALVES, q * kInt4Batches + b, lane,
                                                 sv_next[b], bv_next[b]);
           }
-          ok = convert_stage_int4<CONV>(p, q, sv, bv, it, rank, smem_base, code_ring, tail,
+          ok = convert_stage_int4<CONV>(p, q, sv, bv, pos, rank, smem_base, code_ring, tail,
                                         abort_flag, lane);
         } else {
-          ok = convert_stage_bf16(p, q, it, rank, smem_base, tail, abort_flag, lane);
+          ok = convert_stage_bf16(p, q, pos, rank, smem_base, tail, abort_flag, lane);
         }
         if (!ok) break;
       }
@@ -792,8 +862,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
   } else {
     // ----------------------------------------------------------- epilogue --
     const int q = warp & 3;               // TMEM lane quarter this warp may access
-    const int ew = warp - EPI_WARP0;      // 0..3
-    uint8_t *my_stage = epi_stage + ew * (16 * 64);
+    const int ew = warp - EPI_WARP0;      // 0 .. 4 G - 1
+    const int grp = ew >> 2;              // epilogue group: column chunks grp, grp + G, ...
+    const int bar_id = 1 + grp;           // the group's named barrier (128 threads)
+    float *xch = xch_all + grp * XCH_FLOATS;
+    uint8_t *my_stage = epi_stage + ew * EPI_WARP_STAGE_BYTES;
     const uint32_t tmem_empty0 = mapa_shared(smem_u32(&tail->tmem_empty[0]), 0);
     int acc = 0;
     uint32_t aphase = 0;
@@ -806,11 +879,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
                                 DEV_TIMEOUT_EPILOGUE);
       }
       got = __shfl_sync(0xffffffffu, got, 0);
-      // Agree across the four epilogue warps before any named barrier.
+      // Agree across the group's four warps before any named barrier.
       if (lane == 0) tail->vote[ew] = got;
-      named_bar_sync(1, 128);
-      const int all_ok = tail->vote[0] & tail->vote[1] & tail->vote[2] & tail->vote[3];
-      named_bar_sync(1, 128);
+      named_bar_sync(bar_id, 128);
+      const int v0 = grp * 4;
+      const int all_ok = tail->vote[v0] & tail->vote[v0 + 1] & tail->vote[v0 + 2] & tail->vote[v0 + 3];
+      named_bar_sync(bar_id, 128);
       if (!all_ok) break;
       tc_fence_after();
       const uint32_t tacc = tmem_base + acc * ACC_COLS + (static_cast<uint32_t>(q * 32) << 16);
@@ -827,7 +901,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         __half *hout = reinterpret_cast<__half *>(p.out) + i0;
         __half *sh = reinterpret_cast<__half *>(my_stage);
         int buf = 0;
-        for (int c0 = 0; c0 < t.nmma; c0 += 16) {
+        for (int c0 = 16 * grp; c0 < t.nmma; c0 += 16 * G) {
           uint32_t r[16];
           tmem_ld16(tacc + c0, r);
           tmem_ld_wait();
@@ -836,7 +910,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
           for (int cc = 0; cc < 8; ++cc)
             mine_to[cc * 32 + lane] = __uint_as_float(r[is_gate ? 8 + cc : cc]);
-          named_bar_sync(1, 128);
+          named_bar_sync(bar_id, 128);
 #pragma unroll
           for (int cc = 0; cc < 8; ++cc) {
             const float g = is_gate ? __uint_as_float(r[cc]) : from[cc * 32 + lane];
@@ -856,7 +930,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         __half *oout = reinterpret_cast<__half *>(p.out) + n0;
         __half *sh = reinterpret_cast<__half *>(my_stage);
         const bool full_rows = n0 + 32 <= p.hidden;
-        for (int c0 = 0; c0 < t.nmma; c0 += 16) {
+        for (int c0 = 16 * grp; c0 < t.nmma; c0 += 16 * G) {
           uint32_t r[16];
           tmem_ld16(tacc + c0, r);
           tmem_ld_wait();
@@ -887,7 +961,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         const bool vec = e0 + 32 <= p.n_experts && (p.out_ld & 3) == 0 &&
                          (reinterpret_cast<uintptr_t>(lout) & 15) == 0;
         float *sf = reinterpret_cast<float *>(my_stage);   // [8 tokens][32 experts]
-        for (int c0 = 0; c0 < t.nmma; c0 += 16) {
+        for (int c0 = 16 * grp; c0 < t.nmma; c0 += 16 * G) {
           uint32_t r[16];
           tmem_ld16(tacc + c0, r);
           tmem_ld_wait();
@@ -1000,29 +1074,25 @@ cudaError_t launch_dequant_int4(const void *codes, const void *scale, const void
   return cudaGetLastError();
 }
 
+template <int CONV> cudaError_t gemm_configure_one() {
+  return cudaFuncSetAttribute(tc_gemm_kernel<CONV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              static_cast<int>(gemm_smem_bytes<CONV>()));
+}
+
 cudaError_t gemm_configure() {
-  const int bytes = static_cast<int>(kGemmSmemBytes);
   cudaError_t e;
-  if ((e = cudaFuncSetAttribute(tc_gemm_kernel<CONV_NONE>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) ||
-      (e = cudaFuncSetAttribute(tc_gemm_kernel<CONV_BF16_TO_F16>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) ||
-      (e = cudaFuncSetAttribute(tc_gemm_kernel<CONV_INT4_TO_BF16>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) ||
-      (e = cudaFuncSetAttribute(tc_gemm_kernel<CONV_INT4_TO_F16>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) ||
-      (e = cudaFuncSetAttribute(tc_gemm_kernel<CONV_INT4A_TO_BF16>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) ||
-      (e = cudaFuncSetAttribute(tc_gemm_kernel<CONV_INT4A_TO_F16>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)))
+  if ((e = gemm_configure_one<CONV_NONE>()) || (e = gemm_configure_one<CONV_BF16_TO_F16>()) ||
+      (e = gemm_configure_one<CONV_INT4_TO_BF16>()) || (e = gemm_configure_one<CONV_INT4_TO_F16>()) ||
+      (e = gemm_configure_one<CONV_INT4A_TO_BF16>()) || (e = gemm_configure_one<CONV_INT4A_TO_F16>()))
     return e;
   return cudaSuccess;
 }
 
 int gemm_pair_rows() { return PAIR_M; }
 
-int gemm_max_grid(int num_sms) {
-  int grid = num_sms & ~1;
+// Co-resident pairs of one kernel instance (both instances used here take
+// one CTA per SM).
+template <int CONV> int max_clusters(int grid) {
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -1030,17 +1100,30 @@ int gemm_max_grid(int num_sms) {
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.gridDim = dim3(grid, 1, 1);
-  cfg.blockDim = dim3(NUM_THREADS, 1, 1);
-  cfg.dynamicSmemBytes = kGemmSmemBytes;
+  cfg.blockDim = dim3(num_threads<CONV>(), 1, 1);
+  cfg.dynamicSmemBytes = gemm_smem_bytes<CONV>();
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int clusters = 0;
-  if (cudaOccupancyMaxActiveClusters(&clusters, tc_gemm_kernel<CONV_BF16_TO_F16>, &cfg) ==
-          cudaSuccess &&
-      clusters > 0)
-    grid = std::min(grid, 2 * clusters);
+  if (cudaOccupancyMaxActiveClusters(&clusters, tc_gemm_kernel<CONV>, &cfg) != cudaSuccess)
+    clusters = 0;
   cudaGetLastError();
+  return clusters;
+}
+
+int gemm_max_grid(int num_sms) {
+  int grid = num_sms & ~1;
+  const int c0 = max_clusters<CONV_NONE>(grid), c1 = max_clusters<CONV_INT4_TO_BF16>(grid);
+  const int clusters = std::min(c0 > 0 ? c0 : grid / 2, c1 > 0 ? c1 : grid / 2);
+  grid = std::min(grid, 2 * clusters);
   return grid > 2 ? grid : 2;
+}
+
+template <int CONV>
+cudaError_t launch_one(dim3 g, const GemmMaps &maps, const GemmParams &p, bool pdl,
+                       cudaStream_t stream) {
+  return launch_kernel(tc_gemm_kernel<CONV>, g, dim3(num_threads<CONV>()), gemm_smem_bytes<CONV>(),
+                       stream, pdl, maps, p);
 }
 
 cudaError_t launch_tc_gemm(const CUtensorMap &a_routed, const CUtensorMap &a_shared,
@@ -1055,25 +1138,14 @@ cudaError_t launch_tc_gemm(const CUtensorMap &a_routed, const CUtensorMap &a_sha
     maps.b[i] = b[i];
     maps.b2[i] = b2[i];
   }
-  const dim3 g(grid), bl(NUM_THREADS);
+  const dim3 g(grid);
   switch (conv) {
-    case CONV_BF16_TO_F16:
-      return launch_kernel(tc_gemm_kernel<CONV_BF16_TO_F16>, g, bl, kGemmSmemBytes, stream, pdl,
-                           maps, p);
-    case CONV_INT4_TO_BF16:
-      return launch_kernel(tc_gemm_kernel<CONV_INT4_TO_BF16>, g, bl, kGemmSmemBytes, stream, pdl,
-                           maps, p);
-    case CONV_INT4_TO_F16:
-      return launch_kernel(tc_gemm_kernel<CONV_INT4_TO_F16>, g, bl, kGemmSmemBytes, stream, pdl,
-                           maps, p);
-    case CONV_INT4A_TO_BF16:
-      return launch_kernel(tc_gemm_kernel<CONV_INT4A_TO_BF16>, g, bl, kGemmSmemBytes, stream, pdl,
-                           maps, p);
-    case CONV_INT4A_TO_F16:
-      return launch_kernel(tc_gemm_kernel<CONV_INT4A_TO_F16>, g, bl, kGemmSmemBytes, stream, pdl,
-                           maps, p);
-    default:
-      return launch_kernel(tc_gemm_kernel<CONV_NONE>, g, bl, kGemmSmemBytes, stream, pdl, maps, p);
+    case CONV_BF16_TO_F16: return launch_one<CONV_BF16_TO_F16>(g, maps, p, pdl, stream);
+    case CONV_INT4_TO_BF16: return launch_one<CONV_INT4_TO_BF16>(g, maps, p, pdl, stream);
+    case CONV_INT4_TO_F16: return launch_one<CONV_INT4_TO_F16>(g, maps, p, pdl, stream);
+    case CONV_INT4A_TO_BF16: return launch_one<CONV_INT4A_TO_BF16>(g, maps, p, pdl, stream);
+    case CONV_INT4A_TO_F16: return launch_one<CONV_INT4A_TO_F16>(g, maps, p, pdl, stream);
+    default: return launch_one<CONV_NONE>(g, maps, p, pdl, stream);
   }
 }
 
