@@ -95,7 +95,8 @@ typedef enum {
   MOE_ERR_WORKSPACE = 3,       /* workspace missing, too small or misaligned     */
   MOE_ERR_CUDA = 4,            /* a CUDA runtime/driver call failed              */
   MOE_ERR_NOT_LOADED = 5,      /* weights of the requested layer slot not loaded */
-  MOE_ERR_DEVICE_TIMEOUT = 6   /* a bounded device-side wait ran out             */
+  MOE_ERR_DEVICE_TIMEOUT = 6,  /* a bounded device-side wait ran out             */
+  MOE_ERR_RANGE = 7            /* a prefill intermediate left the fp16 range     */
 } moe_status;
 
 typedef enum {
@@ -181,7 +182,16 @@ moe_status moe_route(moe_ctx *ctx, int layer, const void *x, int T,
  * ("Bound temporary memory with prompt chunking").  With int4 weights the
  * grouped GEMMs dequantise each weight tile in shared memory right before its
  * MMA ("Dequantize weights during matrix multiplication"): no expanded copy
- * of the weights is ever written. */
+ * of the weights is ever written.
+ *   Range: the prefill path keeps the two per-row intermediates in fp16 (11
+ *   significant bits, finite up to 65504): h = silu(gate) * up of every
+ *   routed and shared expert, and o, each expert's output row.  The kernels
+ *   check both as they store them; if one is not finite or beyond 65504 in
+ *   magnitude (activations about 70 times larger than unit-variance inputs
+ *   through N(0, 0.02) weights), y is not valid and moe_check_device()
+ *   reports MOE_ERR_RANGE.  The decode and few-rows paths keep these values
+ *   in fp32 and have no such limit.  Down-projection weights below 2^-17 in
+ *   magnitude keep fewer than 8 significant bits in the fp16 operands. */
 moe_status moe_forward_prefill(moe_ctx *ctx, int layer, const void *x, int T,
                                void *y, void *stream);
 
@@ -314,8 +324,10 @@ moe_status moe_dequant_int4(const void *codes, const void *scale, const void *bi
                             size_t rows, int K, int wfmt, int out_f16, void *stream);
 
 /* Synchronises the device, reads and clears the device status word: MOE_OK,
- * or MOE_ERR_DEVICE_TIMEOUT (a bounded wait ran out; *code, if non-NULL,
- * receives the site code), or MOE_ERR_CUDA.  With ctx = NULL it does the
+ * MOE_ERR_DEVICE_TIMEOUT (a bounded wait ran out; *code, if non-NULL,
+ * receives the site code), MOE_ERR_RANGE (a prefill intermediate left the
+ * fp16 range since the last check; *code receives 0x201 for h, 0x202 for o),
+ * or MOE_ERR_CUDA.  With ctx = NULL it does the
  * same for the status word of moe_forward_decode_noalloc on the current
  * device. */
 moe_status moe_check_device(moe_ctx *ctx, int32_t *code);

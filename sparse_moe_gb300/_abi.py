@@ -13,6 +13,7 @@ MOE_ERR_WORKSPACE = 3
 MOE_ERR_CUDA = 4
 MOE_ERR_NOT_LOADED = 5
 MOE_ERR_DEVICE_TIMEOUT = 6
+MOE_ERR_RANGE = 7
 
 MOE_W_BF16 = 0
 MOE_W_INT4_SYM_G64 = 1

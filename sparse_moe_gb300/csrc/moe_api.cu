@@ -575,6 +575,7 @@ const char *moe_status_string(moe_status s) {
     case MOE_ERR_CUDA: return "CUDA error";
     case MOE_ERR_NOT_LOADED: return "layer weights not loaded";
     case MOE_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
+    case MOE_ERR_RANGE: return "prefill intermediate outside the fp16 range";
   }
   return "unknown status";
 }
@@ -1030,6 +1031,8 @@ moe_status moe_check_device(moe_ctx *ctx, int32_t *code) {
     cudaMemset(ctx->status(), 0, 4);
     cudaMemset(ctx->ws + ctx->L.dec_counter, 0, 16);   // a timed-out grid barrier
     cudaDeviceSynchronize();
+    if (v == kDevRangeH || v == kDevRangeO)
+      return fail(ctx, MOE_ERR_RANGE, "prefill %s outside the fp16 range", v == kDevRangeH ? "h" : "o");
     return fail(ctx, MOE_ERR_DEVICE_TIMEOUT, "device wait timed out (site 0x%x)", v);
   }
   return MOE_OK;

@@ -8,6 +8,8 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include "moe_internal.h"
+
 namespace moe {
 
 // ---------------------------------------------------------------- status --
@@ -22,6 +24,8 @@ enum : int {
   DEV_TIMEOUT_RELAY = 0x106,
   DEV_TIMEOUT_GRID = 0x107,
   DEV_TIMEOUT_STAGE = 0x108,
+  DEV_RANGE_H = kDevRangeH,  // a prefill h value left the fp16 range
+  DEV_RANGE_O = kDevRangeO,  // a prefill o value left the fp16 range
 };
 
 // A wait that has not completed within this many SM clock cycles gives up
@@ -141,6 +145,27 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
       *abort_flag = 1;
       atomicExch(status, code);
       return false;
+    }
+  }
+}
+
+// The same without sleeping between polls, checking the abort flag and the
+// cycle limit only every 64 polls: for the thread that issues the MMAs, whose
+// every memory access (a poll included) stalls it for hundreds of cycles
+// after MMAs have been issued.
+__device__ __forceinline__ bool mbar_wait_spin_bounded(uint32_t bar, uint32_t parity,
+                                                       volatile int *abort_flag, int *status,
+                                                       int code) {
+  const long long t0 = cycles_now();
+  for (int i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 63) == 0) {
+      if (*abort_flag) return false;
+      if (cycles_now() - t0 > kWaitLimitCycles) {
+        *abort_flag = 1;
+        atomicExch(status, code);
+        return false;
+      }
     }
   }
 }

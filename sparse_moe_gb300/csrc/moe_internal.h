@@ -17,6 +17,11 @@ constexpr int kBlockRowsMin = 16;
 // Tokens per routing block (one 32-bit mask word per expert per block).
 constexpr int kRouteBlockTokens = 32;
 
+// Device status codes of a prefill intermediate (h, o) outside the fp16
+// range (the bounded-wait timeout codes are 0x1xx).
+constexpr int kDevRangeH = 0x201;
+constexpr int kDevRangeO = 0x202;
+
 enum GemmMode : int { MODE_ROUTER = 0, MODE_GATEUP = 1, MODE_DOWN = 2 };
 // In-shared-memory conversion of the weight (A) tile before the MMA: none,
 // bf16 -> fp16 in place, or int4 codes -> bf16 / fp16, symmetric (one bf16

@@ -747,8 +747,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(num_threads<CONV>(),
         int acc = 0;
         uint32_t aphase = 0;
         bool ok = true;
+        // descriptors of k-step slot 0 (A and B); slot s adds s * SLOT_BYTES
+        // to the start-address field (addresses >> 4, 14 bits: no carry below
+        // 256 KB)
+        const uint64_t a_desc0 = smem_desc_sw128(smem_base);
+        const uint64_t b_desc0 = smem_desc_sw128(smem_base + A_BYTES);
+        // the next tile's block-list entry is read one tile ahead
+        Tile tn = decode_tile(p, pair_id < ntiles ? pair_id : 0, 0);
         for (int tile = pair_id; tile < ntiles && ok; tile += num_pairs) {
-          const Tile t = decode_tile(p, tile, 0);
+          const Tile t = tn;
+          if (tile + num_pairs < ntiles) tn = decode_tile(p, tile + num_pairs, 0);
           if (!t.valid) continue;
           if (!mbar_wait_bounded_cluster(smem_u32(&tail->tmem_empty[acc]), aphase ^ 1, abort_flag,
                                          p.status, DEV_TIMEOUT_MMA)) {
@@ -770,20 +778,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(num_threads<CONV>(),
             // tensor cores' rate.
             const uint32_t stage_bar = CONV == CONV_NONE ? smem_u32(&tail->full[stage])
                                                          : smem_u32(&tail->ready[stage]);
-            if (!mbar_wait_bounded(stage_bar, phase, abort_flag, p.status, DEV_TIMEOUT_MMA)) {
+            if (!mbar_wait_spin_bounded(stage_bar, phase, abort_flag, p.status, DEV_TIMEOUT_MMA)) {
               ok = false;
               break;
             }
             tc_fence_after();
             const int nh = min(HALVES, t.nk - j * HALVES);
-            for (int h = 0; h < nh; ++h) {
-              const uint32_t a_addr = smem_base + (stage * HALVES + h) * SLOT_BYTES;
-              const uint64_t a_desc = smem_desc_sw128(a_addr);
-              const uint64_t b_desc = smem_desc_sw128(a_addr + A_BYTES);
 #pragma unroll
-              for (int kk = 0; kk < BK / 16; ++kk)
-                tc_mma_pair(d_tmem, a_desc + 2 * kk, b_desc + 2 * kk, idesc,
-                            (j | h | kk) != 0);
+            for (int h = 0; h < HALVES; ++h) {
+              if (h < nh) {
+                const uint64_t off = static_cast<uint64_t>((stage * HALVES + h) * (SLOT_BYTES >> 4));
+                const uint64_t a_desc = a_desc0 + off, b_desc = b_desc0 + off;
+#pragma unroll
+                for (int kk = 0; kk < BK / 16; ++kk)
+                  tc_mma_pair(d_tmem, a_desc + 2 * kk, b_desc + 2 * kk, idesc,
+                              (j | h | kk) != 0);
+              }
             }
             tc_commit_pair_mc(smem_u32(&tail->empty[stage]), 0x3);
             if (++stage == STAGES) {
@@ -870,6 +880,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(num_threads<CONV>(),
     const uint32_t tmem_empty0 = mapa_shared(smem_u32(&tail->tmem_empty[0]), 0);
     int acc = 0;
     uint32_t aphase = 0;
+    bool range_bad = false;   // a stored h or o value outside the fp16 range
     for (int tile = pair_id; tile < ntiles; tile += num_pairs) {
       const Tile t = decode_tile(p, tile, rank);
       if (!t.valid) continue;
@@ -915,7 +926,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(num_threads<CONV>(),
           for (int cc = 0; cc < 8; ++cc) {
             const float g = is_gate ? __uint_as_float(r[cc]) : from[cc * 32 + lane];
             const float u = is_gate ? from[cc * 32 + lane] : __uint_as_float(r[8 + cc]);
-            sh[cc * 32 + lane] = __float2half_rn(silu_f(g) * u);
+            const float hv = silu_f(g) * u;
+            // fp16 range check of the stored values (token columns that exist)
+            range_bad |= live && (c0 + (is_gate ? 0 : 8) + cc < t.nrows) && !(fabsf(hv) <= 65504.0f);
+            sh[cc * 32 + lane] = __float2half_rn(hv);
           }
           __syncwarp();
           const int col0 = c0 + (is_gate ? 0 : 8);
@@ -936,7 +950,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(num_threads<CONV>(),
           tmem_ld_wait();
           if (full_rows) {
 #pragma unroll
-            for (int cc = 0; cc < 16; ++cc) sh[cc * 32 + lane] = __float2half_rn(__uint_as_float(r[cc]));
+            for (int cc = 0; cc < 16; ++cc) {
+              const float ov = __uint_as_float(r[cc]);
+              range_bad |= (c0 + cc < t.nrows) && !(fabsf(ov) <= 65504.0f);
+              sh[cc * 32 + lane] = __float2half_rn(ov);
+            }
             __syncwarp();
             warp_store_rows_f16(my_stage, 16, t.nrows - c0,
                                 oout + static_cast<size_t>(t.row0 + c0) * p.out_ld, p.out_ld, lane);
@@ -944,9 +962,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(num_threads<CONV>(),
           } else if (n0 + lane < p.hidden) {
 #pragma unroll
             for (int cc = 0; cc < 16; ++cc)
-              if (c0 + cc < t.nrows)
-                oout[static_cast<size_t>(t.row0 + c0 + cc) * p.out_ld + lane] =
-                    __float2half_rn(__uint_as_float(r[cc]));
+              if (c0 + cc < t.nrows) {
+                const float ov = __uint_as_float(r[cc]);
+                range_bad |= !(fabsf(ov) <= 65504.0f);
+                oout[static_cast<size_t>(t.row0 + c0 + cc) * p.out_ld + lane] = __float2half_rn(ov);
+              }
           }
         }
       } else {  // MODE_ROUTER: fp32 logits (split-K part t.split), 128 contiguous bytes per column
@@ -1002,6 +1022,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(num_threads<CONV>(),
         aphase ^= 1;
       }
     }
+    // h or o outside the fp16 range: recorded once per warp (a timeout code
+    // already there is kept)
+    if (__any_sync(0xffffffffu, range_bad) && lane == 0 && p.mode != MODE_ROUTER)
+      atomicCAS(p.status, 0, p.mode == MODE_GATEUP ? DEV_RANGE_H : DEV_RANGE_O);
   }
 
   tc_fence_before();
