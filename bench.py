@@ -591,6 +591,86 @@ def cpu_baseline_prefill(x_cpu, w_dev, k, min_seconds=10.0, max_passes=32):
             "seconds": dt}
 
 
+def cpu_oracle_worker(threads: int) -> dict:
+    """The fp64 oracle, as it stands, on bounded samples of each configured
+    workload, timed in this process (started with the BLAS thread count set
+    to `threads`).  Weights are regenerated on the host from the workloads'
+    seeds (the host generator draws other numbers than the device one; the
+    shapes, distributions and routing skew are the same)."""
+    from oracle import moe_oracle as orc
+    out = {"threads": threads}
+
+    def timed(fn, min_s=0.5, max_reps=50):
+        fn()   # first pass: warm caches and allocations
+        t0 = time.perf_counter()
+        n = 0
+        while n < max_reps and (n == 0 or time.perf_counter() - t0 < min_s):
+            fn()
+            n += 1
+        return (time.perf_counter() - t0) / n
+
+    def host(wl):
+        return moe_synth.to_numpy(moe_synth.make_layer(wl, device="cpu")), \
+            moe_synth.make_x(wl, device="cpu").float().numpy()
+
+    w, x = host(moe_synth.TINY_LAYER)
+    dt = timed(lambda: orc.moe_layer(x, w, moe_synth.TINY.top_k))
+    out["tiny_T16"] = {"tokens_per_s": 16 / dt, "sample": "all 16 tokens"}
+    wl = moe_synth.PREFILL_BF16
+    w, x = host(wl)
+    k = wl.shape.top_k
+    dt = timed(lambda: orc.moe_layer(x[:1], w, k))
+    out["decode_bf16_T1"] = {"us_per_layer": dt * 1e6, "tokens_per_s_40_layers": 1.0 / (40 * dt),
+                             "sample": "one token through one layer of the prefill workload's "
+                                       "weights (8 routed experts + shared; the decode "
+                                       "workload's shapes)"}
+    S = 512
+    dt = timed(lambda: orc.moe_layer(x[:S], w, k), min_s=0.0, max_reps=1)
+    out["prefill_bf16_T4096"] = {"tokens_per_s": S / dt,
+                                 "sample": f"first {S} tokens of the T=4096 workload"}
+    lens = {}
+    per_tok = None
+    for T in moe_synth.SWEEP_T:
+        if T <= 512:
+            xs = moe_synth.make_x(moe_synth.sweep_workload(T), device="cpu").float().numpy()
+            dts = timed(lambda: orc.moe_layer(xs, w, k), min_s=0.0, max_reps=1)
+            per_tok = dts / T
+            lens[str(T)] = {"seconds": dts, "tokens_per_s": T / dts, "how": "measured, all rows"}
+        else:
+            lens[str(T)] = {"seconds": T * per_tok, "tokens_per_s": 1.0 / per_tok,
+                            "how": "extrapolated from the T=512 measurement (cost per token)"}
+    out["prompt_sweep"] = lens
+    del w
+    wl4 = moe_synth.PREFILL_INT4
+    w4, x4 = host(wl4)
+    dt = timed(lambda: orc.moe_layer(x4[:1], w4, k))
+    out["decode_int4_T1"] = {"us_per_layer": dt * 1e6, "sample": "one token, symmetric int4 G64"}
+    S = 256
+    dt = timed(lambda: orc.moe_layer(x4[:S], w4, k), min_s=0.0, max_reps=1)
+    out["prefill_int4_T4096"] = {"tokens_per_s": S / dt,
+                                 "sample": f"first {S} tokens of the int4 T=4096 workload"}
+    return out
+
+
+def cpu_baselines_by_threads() -> dict:
+    """cpu_oracle_worker with one thread and with all host cores, each in a
+    subprocess whose BLAS thread count is fixed before numpy loads."""
+    res = {}
+    for threads in (1, os.cpu_count() or 1):
+        env = dict(os.environ)
+        for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+            env[v] = str(threads)
+        env["CUDA_VISIBLE_DEVICES"] = ""
+        try:
+            r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-oracle-worker",
+                                str(threads)], env=env, capture_output=True, text=True,
+                               timeout=600)
+            res[f"threads_{threads}"] = json.loads(r.stdout.strip().splitlines()[-1])
+        except Exception as e:   # reported, not fatal: the GPU numbers stand
+            res[f"threads_{threads}"] = {"error": f"{type(e).__name__}: {e}"[:300]}
+    return res
+
+
 def main_reference(args):
     """The oracle as the reference arm, on the host cores."""
     rank = int(os.environ.get("RANK", "0"))
@@ -747,6 +827,8 @@ def main(args):
                                                       wl=moe_synth.DECODE_INT4_AFFINE)
     if rank == 0 and not args.skip_cpu:
         line["cpu_baseline"] = cpu_baseline_prefill(x.cpu(), w, s.top_k)
+        if not args.skip_cpu_configs:
+            line["cpu_baseline"]["per_config"] = cpu_baselines_by_threads()
     if rank == 0:
         print(json.dumps(line))
     if world > 1:
@@ -777,7 +859,14 @@ if __name__ == "__main__":
                     help="decode measurements only (diagnostic; not the benchmark line)")
     ap.add_argument("--decode-layers", type=int, default=0,
                     help="layers in the decode graph (default: the workload's 40)")
+    ap.add_argument("--cpu-oracle-worker", type=int, default=0,
+                    help=argparse.SUPPRESS)   # internal: one thread setting of the CPU baseline
+    ap.add_argument("--skip-cpu-configs", action="store_true",
+                    help="skip the per-configuration oracle timings (1 thread and all cores)")
     a = ap.parse_args()
+    if a.cpu_oracle_worker:
+        print(json.dumps(cpu_oracle_worker(a.cpu_oracle_worker)))
+        sys.exit(0)
     if a.warmup < 3 and a.impl == "ours":
         a.warmup = 3
     sys.exit(main_reference(a) if a.impl == "reference" else main(a))
