@@ -122,10 +122,10 @@ class ClockSampler:
 
 # DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) of
 # the kernels the roofline lines name, from one ncu capture of the current
-# kernels (the summaries under profiles/): gate/up 628.0 + 33.0 MB at the
+# kernels (the summaries under profiles/): gate/up 705.0 + 34.0 MB at the
 # T=4096 prefill workload, decode layer 57.76 + 0.42 MB (bf16) and
 # 16.19 + 0.00 MB (symmetric int4).  The affine int4 decode was not captured.
-TRAFFIC_BYTES = {"gateup_swiglu_gemm": 661.4e6, "decode_layer": 58.18e6,
+TRAFFIC_BYTES = {"gateup_swiglu_gemm": 739.1e6, "decode_layer": 58.18e6,
                  "decode_layer_int4_sym": 16.19e6}
 
 
@@ -136,6 +136,28 @@ def algorithmic(s: moe_synth.Shape, T: int):
     down_flops = 2.0 * I * H * T * k + 2.0 * Is * H * T
     router_flops = 2.0 * H * E * T
     return gateup_flops, down_flops, router_flops
+
+
+def routing_bytes(s: moe_synth.Shape, T: int, k_split: int = 4):
+    """Bytes each routing kernel must move at T tokens (what the step reads
+    and writes, not what a cache hierarchy adds): router GEMM x, Wr and its
+    split-K logit parts; top-k the parts, x (for the shared gate) and its
+    outputs (indices, weights, per-32-token expert masks, gates); scan the
+    masks in, counts, offsets, bases and the block list out; scatter its
+    index inputs, the two permutation arrays, and x read once and written k
+    times in grouped order."""
+    H, E, k = s.hidden, s.n_experts, s.top_k
+    nblk = (T + 31) // 32
+    x = T * H * 2
+    parts = k_split * T * E * 4
+    masks = nblk * E * 4
+    return {
+        "router_gemm": x + E * H * 2 + parts,
+        "topk": parts + x + H * 2 + T * k * 8 + masks + T * 4,
+        "route_scan": masks + 2 * masks + 3 * E * 4,
+        "route_scatter": T * k * 4 + 2 * masks + E * 4 + 2 * T * k * 4 + x + T * k * H * 2,
+        "combine": (T * k + T) * H * 2 + T * k * 8 + T * 4 + x,
+    }
 
 
 def decode_bytes(s: moe_synth.Shape, int4: bool, affine: bool = False):
@@ -772,6 +794,13 @@ def main(args):
 
     gu_f, dn_f, rt_f = algorithmic(s, wl.T)
     kern = {k: {"launches": v[0], "avg_us": v[1] * 1e3 / max(1, v[0])} for k, v in prof.items()}
+    # achieved bandwidth of the HBM/latency-bound kernels (algorithmic bytes
+    # per launch over the launch's CUDA-event time)
+    for name, nbytes in routing_bytes(s, wl.T).items():
+        if name in kern:
+            kern[name]["algorithmic_bytes"] = nbytes
+            kern[name]["achieved_GBps"] = nbytes / (kern[name]["avg_us"] * 1e-6) / 1e9
+            kern[name]["frac_of_hbm"] = kern[name]["achieved_GBps"] / hbm
     gu_us = kern.get("gateup_swiglu_gemm", {}).get("avg_us", float("nan"))
     dn_us = kern.get("down_gemm", {}).get("avg_us", float("nan"))
     achieved = gu_f / (gu_us * 1e-6) / 1e12
@@ -801,6 +830,21 @@ def main(args):
         "clocks": clk,
     }
 
+    if rank == 0 and not args.skip_int4:
+        # the same layer with only the bf16 down weights (no fp16 copies): the
+        # down GEMM then converts each weight tile in shared memory
+        ctx_b = MoEContext(s.hidden, s.n_experts, s.top_k, s.inter, s.shared_inter, n_layers=1,
+                           max_chunk_rows=4096, device=local)
+        ctx_b.load_weights(0, w)
+        steps_b = max(5, args.steps // 4)
+        tot_b, prof_b, _ = run_prefill(ctx_b, x, y, steps_b, args.warmup, flush, stream)
+        dn_b = prof_b.get("down_gemm", (1, float("nan")))
+        line["prefill_bf16_down_only"] = {
+            "value": wl.T * steps_b / (tot_b * 1e-3), "unit": "tokens/s",
+            "ms_per_step": tot_b / steps_b, "steps": steps_b,
+            "down_gemm_us": dn_b[1] * 1e3 / max(1, dn_b[0]),
+            "how": "bf16 down weights only, converted to fp16 tile by tile in the GEMM"}
+        ctx_b.close()
     if rank == 0 and not args.skip_e2e:
         x_h = x.cpu().pin_memory()
         y_h = torch.empty_like(x_h).pin_memory()
