@@ -123,10 +123,10 @@ class ClockSampler:
 # DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) of
 # the kernels the roofline lines name, from one ncu capture of the current
 # kernels (the summaries under profiles/): gate/up 705.0 + 34.0 MB at the
-# T=4096 prefill workload, decode layer 57.76 + 0.42 MB (bf16) and
-# 16.19 + 0.00 MB (symmetric int4).  The affine int4 decode was not captured.
+# T=4096 prefill workload, decode layer 57.76 + 0.42 MB (bf16),
+# 16.19 + 0.00 MB (symmetric int4) and 17.09 + 0.00 MB (affine int4).
 TRAFFIC_BYTES = {"gateup_swiglu_gemm": 739.1e6, "decode_layer": 58.18e6,
-                 "decode_layer_int4_sym": 16.19e6}
+                 "decode_layer_int4_sym": 16.19e6, "decode_layer_int4_affine": 17.09e6}
 
 
 # ------------------------------------------------------------- workload --
@@ -567,7 +567,8 @@ def bench_decode(args, dev, stream, hbm, int4=None, wl=None):
                      "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
                      "traffic": (TRAFFIC_BYTES["decode_layer"] if not int4 else
                                  TRAFFIC_BYTES["decode_layer_int4_sym"]
-                                 if wl.wfmt == moe_synth.WFMT_INT4 else None),
+                                 if wl.wfmt == moe_synth.WFMT_INT4 else
+                                 TRAFFIC_BYTES["decode_layer_int4_affine"]),
                      "algorithmic_bytes_per_launch": nb["total"],
                      "launch_us_timed": us_layer,
                      "timing": "graph replays of L layers, CUDA events on the launch stream; "
@@ -761,7 +762,8 @@ def main(args):
 
     if args.skip_prefill:
         # decode only (a diagnostic mode: e.g. a small decode case for a profiler)
-        out = bench_decode(args, dev, torch.cuda.Stream(device=dev), hbm)
+        out = bench_decode(args, dev, torch.cuda.Stream(device=dev), hbm,
+                           wl=moe_synth.DECODE_INT4_AFFINE if args.decode_affine else None)
         if rank == 0:
             print(json.dumps({"metric": METRIC, "value": out["value"], "unit": out["unit"],
                               "n_gpus": world, "higher_is_better": False, "decode": out}))
@@ -890,6 +892,8 @@ if __name__ == "__main__":
     ap.add_argument("--ref-sample", type=int, default=128,
                     help="tokens per step of the reference arm (the oracle on the host cores)")
     ap.add_argument("--decode-int4", action="store_true")
+    ap.add_argument("--decode-affine", action="store_true",
+                    help="with --skip-prefill: the affine int4 decode workload")
     ap.add_argument("--skip-decode", action="store_true")
     ap.add_argument("--skip-e2e", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
