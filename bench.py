@@ -1,7 +1,8 @@
 """Benchmark of the sparse MoE layer on one GB300 (or N replicas).
 
-One step = one prefill pass of the whole layer (router GEMM, top-k, histogram,
-scan, scatter, gate/up+SwiGLU and down grouped GEMMs, combine) over T=4096
+One step = one prefill pass of the whole layer (router GEMM, top-k, placement:
+histogram, scan, block map and scatter, gate/up+SwiGLU and down grouped GEMMs,
+combine) over T=4096
 synthetic tokens of the Qwen3.6-35B-A3B MoE shape (H=2048, 256 experts, top-8,
 I=512, one shared expert, bf16, router bias ~N(0,1.5)), inputs resident in HBM,
 L2 flushed between timed steps.  The same JSON line carries the batch-1 decode
@@ -142,10 +143,10 @@ def routing_bytes(s: moe_synth.Shape, T: int, k_split: int = 4):
     """Bytes each routing kernel must move at T tokens (what the step reads
     and writes, not what a cache hierarchy adds): router GEMM x, Wr and its
     split-K logit parts; top-k the parts, x (for the shared gate) and its
-    outputs (indices, weights, per-32-token expert masks, gates); scan the
-    masks in, counts, offsets, bases and the block list out; scatter its
-    index inputs, the two permutation arrays, and x read once and written k
-    times in grouped order."""
+    outputs (indices, weights, per-32-token expert masks, gates); placement
+    the indices and masks in, counts, offsets, the two permutation arrays
+    and the block list out, and x read once and written k times in grouped
+    order."""
     H, E, k = s.hidden, s.n_experts, s.top_k
     nblk = (T + 31) // 32
     x = T * H * 2
@@ -154,8 +155,7 @@ def routing_bytes(s: moe_synth.Shape, T: int, k_split: int = 4):
     return {
         "router_gemm": x + E * H * 2 + parts,
         "topk": parts + x + H * 2 + T * k * 8 + masks + T * 4,
-        "route_scan": masks + 2 * masks + 3 * E * 4,
-        "route_scatter": T * k * 4 + 2 * masks + E * 4 + 2 * T * k * 4 + x + T * k * H * 2,
+        "route_place": T * k * 4 + masks + 2 * E * 4 + 2 * T * k * 4 + x + T * k * H * 2,
         "combine": (T * k + T) * H * 2 + T * k * 8 + T * 4 + x,
     }
 

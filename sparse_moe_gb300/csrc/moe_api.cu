@@ -23,7 +23,7 @@ size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 struct WsLayout {
   int Tc, nblk, R, Imax, max_blocks;
-  size_t status, logits, idx, w, gate, mask, base, counts, offsets, sorted, pos, blocks, nblocks, xg, h,
+  size_t status, logits, idx, w, gate, mask, counts, offsets, sorted, pos, blocks, nblocks, xg, h,
       o;
   size_t dec_logits, dec_idx, dec_w, dec_g, dec_h, dec_counter, x_stage, y_stage, dec_x_stage,
       dec_y_stage, total;
@@ -50,7 +50,6 @@ WsLayout make_layout(const moe_config &c) {
   L.w = take(Tc * k * 4);
   L.gate = take(Tc * 4);
   L.mask = take(static_cast<size_t>(L.nblk) * E * 4);
-  L.base = take(static_cast<size_t>(L.nblk) * E * 4);
   L.counts = take(E * 4);
   L.offsets = take((E + 1) * 4);
   L.sorted = take(Tc * k * 4);
@@ -157,11 +156,11 @@ bool encode_code_map(CUtensorMap *m, const void *ptr, uint64_t inner_bytes, uint
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
 enum KernelId : int {
-  K_ROUTER_GEMM = 0, K_TOPK, K_SCAN, K_SCATTER, K_GATEUP_GEMM, K_DOWN_GEMM, K_COMBINE,
+  K_ROUTER_GEMM = 0, K_TOPK, K_PLACE, K_GATEUP_GEMM, K_DOWN_GEMM, K_COMBINE,
   K_DEC_LAYER, K_H2D, K_D2H, K_DEC_LAYERS, K_ROWS, K_COUNT
 };
 const char *kKernelNames[K_COUNT] = {
-    "router_gemm", "topk", "route_scan", "route_scatter", "gateup_swiglu_gemm", "down_gemm",
+    "router_gemm", "topk", "route_place", "gateup_swiglu_gemm", "down_gemm",
     "combine", "decode_layer", "h2d_copy", "d2h_copy", "decode_layers", "rows"};
 
 }  // namespace
@@ -218,8 +217,6 @@ struct moe_ctx {
 
   template <class T> T *at(size_t off) const { return reinterpret_cast<T *>(ws + off); }
   int *status() const { return at<int>(L.status); }
-  // the routing scan's completion ticket (zeroed with the status region)
-  unsigned int *scan_ticket() const { return at<unsigned int>(L.status + 64); }
 };
 
 namespace {
@@ -378,7 +375,6 @@ moe_status enqueue_route(moe_ctx *ctx, const LayerSlot &ls, const void *x, int T
   }
   if (st) return st;
   uint32_t *mask = ctx->at<uint32_t>(L.mask);
-  int32_t *base = ctx->at<int32_t>(L.base);
   {
     ProfScope ps(ctx, K_TOPK, s);
     st = launched(ctx,
@@ -389,23 +385,15 @@ moe_status enqueue_route(moe_ctx *ctx, const LayerSlot &ls, const void *x, int T
                   "topk launch");
   }
   if (st) return st;
-  const int nblk = (T + kRouteBlockTokens - 1) / kRouteBlockTokens;
   {
-    ProfScope ps(ctx, K_SCAN, s);
+    ProfScope ps(ctx, K_PLACE, s);
     st = launched(ctx,
-                  launch_scan(mask, nblk, T, c.n_experts, c.top_k, counts, offsets, base,
-                              ctx->at<int4>(L.blocks), ctx->at<int32_t>(L.nblocks),
-                              ctx->scan_ticket(), ctx->block_rows, ctx->prefill_pdl, s),
-                  "scan launch");
-  }
-  if (st) return st;
-  {
-    ProfScope ps(ctx, K_SCATTER, s);
-    st = launched(ctx,
-                  launch_scatter(idx, mask, base, offsets, T, c.n_experts, c.top_k, sorted_rows,
-                                 pos, x, with_xg ? ctx->at<void>(L.xg) : nullptr, c.hidden,
-                                 ctx->prefill_pdl, s),
-                  "scatter launch");
+                  launch_place(idx, mask, T, c.n_experts, c.top_k, counts, offsets,
+                               ctx->at<int4>(L.blocks), ctx->at<int32_t>(L.nblocks),
+                               ctx->block_rows, sorted_rows, pos, x,
+                               with_xg ? ctx->at<void>(L.xg) : nullptr, c.hidden,
+                               ctx->prefill_pdl, s),
+                  "placement launch");
   }
   return st;
 }

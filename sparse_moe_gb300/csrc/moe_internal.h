@@ -97,19 +97,17 @@ cudaError_t launch_tc_gemm(const CUtensorMap &a_routed, const CUtensorMap &a_sha
 cudaError_t launch_topk(const float *partial, int nsplit, size_t split_stride, float *logits_out,
                         const void *x, const void *wsg, int T, int E, int k, int H, int32_t *idx,
                         float *w, uint32_t *blk_mask, float *gate, bool pdl, cudaStream_t stream);
-// `ticket`: a zeroed counter in device memory (left zeroed on return);
-// block_rows (kBlockRowsMin..kBlockRowsMax): rows per grouped-GEMM block.
-cudaError_t launch_scan(const uint32_t *blk_mask, int nblk, int T, int E, int k,
-                        int32_t *counts, int32_t *offsets, int32_t *blk_base, int4 *blocks,
-                        int32_t *n_blocks, unsigned int *ticket, int block_rows, bool pdl,
-                        cudaStream_t stream);
-// With xg non-null, also writes xg[pos(t, j)] = x[t] (x [T, H] bf16, xg
-// [T * k, H] bf16: the token rows in grouped order, the routed gate/up
-// GEMM's B operand).
-cudaError_t launch_scatter(const int32_t *idx, const uint32_t *blk_mask, const int32_t *blk_base,
-                           const int32_t *offsets, int T, int E, int k, int32_t *sorted_rows,
-                           int32_t *pos_of_assign, const void *x, void *xg, int H, bool pdl,
-                           cudaStream_t stream);
+// After the top-k kernel: the per-expert counts and segment offsets
+// (offsets[E] = T * k), each assignment's grouped row (pos_of_assign) and
+// its inverse (sorted_rows), and the block map of the grouped GEMMs
+// (block_rows in kBlockRowsMin..kBlockRowsMax rows per block).  With xg
+// non-null, also writes xg[pos(t, j)] = x[t] (x [T, H] bf16, xg [T * k, H]
+// bf16: the token rows in grouped order, the routed gate/up GEMM's B
+// operand).
+cudaError_t launch_place(const int32_t *idx, const uint32_t *blk_mask, int T, int E, int k,
+                         int32_t *counts, int32_t *offsets, int4 *blocks, int32_t *n_blocks,
+                         int block_rows, int32_t *sorted_rows, int32_t *pos_of_assign,
+                         const void *x, void *xg, int H, bool pdl, cudaStream_t stream);
 
 // y[t] = sum_j w[t,j] o[pos(t,j)] + g[t] o[T*k + t]
 cudaError_t launch_combine(const float *gate, const void *o, const int32_t *pos, const float *w,

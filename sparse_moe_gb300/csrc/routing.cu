@@ -136,7 +136,32 @@ cudaError_t launch_topk(const float *partial, int nsplit, size_t split_stride, f
   return e;
 }
 
-// ------------------------------------------------------------------ scan --
+// ------------------------------------------------------------- placement --
+// One routing block of 32 tokens per CTA (1024 threads), after the top-k
+// kernel has written every block's per-expert masks:
+//  1. every CTA counts, for each expert e, its rows in all blocks (total[e])
+//     and in the blocks before its own (before[e]): 128 KB of masks at
+//     T = 4096, read by each CTA from L2 (parts of the block range per
+//     thread, summed in a fixed order);
+//  2. the exclusive scan of the totals gives the segment offsets (identical
+//     in every CTA: integer sums);
+//  3. one thread per assignment (t, j) of the block: pos(t, j) = offsets[e] +
+//     before[e] + (lower tokens of this block that chose e), sorted_rows[pos]
+//     = t;
+//  4. the block map the grouped GEMMs walk: ceil(total[e] / block_rows)
+//     blocks per expert in expert order, then the shared expert's T rows at
+//     grouped row T * k; each CTA writes the blocks of the experts e with
+//     e % gridDim.x == blockIdx.x, CTA 0 the counts, offsets, shared blocks and
+//     block count;
+//  5. with xg, each token's x row is copied to its k positions of xg (one
+//     warp per token: the row is read once, into registers, and written k
+//     times), so that the grouped gate/up GEMM reads its token rows as
+//     consecutive rows.
+// Every result is an integer function of the masks and indices: independent
+// of thread timing and of which CTA computes it.
+constexpr int kPlaceThreads = 1024;
+constexpr int kScatterChunks = 8;   // 16-byte chunks of a row per lane and pass
+
 // Exclusive scan of one int per thread over a 1024-thread block.
 __device__ __forceinline__ int block_excl_scan_1024(int v, int *warp_tot, int &total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -166,161 +191,112 @@ __device__ __forceinline__ int block_excl_scan_1024(int v, int *warp_tot, int &t
   return excl;
 }
 
-// Experts per scan CTA: each CTA counts and places the routing blocks of its
-// experts; the CTA that finishes last (an atomic ticket) turns the counts into
-// segment offsets and writes the block map.  Results do not depend on which
-// CTA is last.
-constexpr int kScanExperts = 32;
-
-__global__ void __launch_bounds__(1024) scan_kernel(const uint32_t *__restrict__ blk_mask,
-                                                    int nblk, int T, int E, int k,
-                                                    int32_t *__restrict__ counts,
-                                                    int32_t *__restrict__ offsets,
-                                                    int32_t *__restrict__ blk_base,
-                                                    int4 *__restrict__ blocks,
-                                                    int32_t *__restrict__ n_blocks,
-                                                    unsigned int *__restrict__ ticket,
-                                                    int block_rows) {
-  __shared__ int part[1024];
+__global__ void __launch_bounds__(kPlaceThreads) place_kernel(
+    const int32_t *__restrict__ idx, const uint32_t *__restrict__ blk_mask, int nblk, int T, int E,
+    int k, int32_t *__restrict__ counts, int32_t *__restrict__ offsets, int4 *__restrict__ blocks,
+    int32_t *__restrict__ n_blocks, int block_rows, int32_t *__restrict__ sorted_rows,
+    int32_t *__restrict__ pos_of_assign, const uint4 *__restrict__ x, uint4 *__restrict__ xg,
+    int H) {
+  __shared__ int tot_s[kPlaceThreads];    // per (part, expert), then per expert
+  __shared__ int bef_s[kPlaceThreads];
+  __shared__ int off_s[kPlaceThreads];
   __shared__ int warp_tot[33];
-  __shared__ int is_last;
-  pdl_trigger();
-  pdl_wait();
-  const int tid = threadIdx.x;
-  const int e0 = blockIdx.x * kScanExperts;
-  const int Ec = min(kScanExperts, E - e0);   // experts of this CTA
-  const int P = 1024 / kScanExperts;         // parts of the block range per expert
-  const int el = tid % kScanExperts;
-  const int e = e0 + el;
-  const int pi = tid / kScanExperts;
-  const bool active = el < Ec;
-  const int b0 = active ? static_cast<int>((static_cast<long long>(nblk) * pi) / P) : 0;
-  const int b1 = active ? static_cast<int>((static_cast<long long>(nblk) * (pi + 1)) / P) : 0;
-  // 1. histogram: rows of expert e in my range of routing blocks (ranges of
-  //    up to kScanRegs blocks keep their counts in registers for step 3)
-  constexpr int kScanRegs = 8;
-  const bool in_regs = b1 - b0 <= kScanRegs;
-  int cnt[kScanRegs];
-  int sum = 0;
-  if (in_regs) {
-#pragma unroll
-    for (int i = 0; i < kScanRegs; ++i)
-      cnt[i] = (b0 + i < b1) ? __popc(blk_mask[static_cast<size_t>(b0 + i) * E + e]) : 0;
-#pragma unroll
-    for (int i = 0; i < kScanRegs; ++i) sum += cnt[i];
-  } else {
-#pragma unroll 8
-    for (int b = b0; b < b1; ++b) sum += __popc(blk_mask[static_cast<size_t>(b) * E + e]);
-  }
-  part[tid] = sum;
-  __syncthreads();
-  // 2. exclusive scan over the parts of each expert
-  if (tid < Ec) {
-    int run = 0;
-    for (int pp = 0; pp < P; ++pp) {
-      const int v = part[pp * kScanExperts + tid];
-      part[pp * kScanExperts + tid] = run;
-      run += v;
-    }
-    counts[e0 + tid] = run;
-  }
-  __syncthreads();
-  // 3. per-block bases inside each expert segment
-  if (active) {
-    int run = part[tid];
-    if (in_regs) {
-#pragma unroll
-      for (int i = 0; i < kScanRegs; ++i)
-        if (b0 + i < b1) {
-          blk_base[static_cast<size_t>(b0 + i) * E + e] = run;
-          run += cnt[i];
-        }
-    } else {
-#pragma unroll 8
-      for (int b = b0; b < b1; ++b) {
-        blk_base[static_cast<size_t>(b) * E + e] = run;
-        run += __popc(blk_mask[static_cast<size_t>(b) * E + e]);
-      }
-    }
-  }
-  // 4. the last CTA: exclusive scan of all counts -> segment offsets, block map
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) is_last = atomicAdd(ticket, 1u) == gridDim.x - 1;
-  __syncthreads();
-  if (!is_last) return;
-  __threadfence();
-  const int c = (tid < E) ? __ldcg(counts + tid) : 0;
-  int total = 0;
-  const int off = block_excl_scan_1024(c, warp_tot, total);
-  if (tid < E) offsets[tid] = off;
-  if (tid == 0) {
-    offsets[E] = total;   // = T * k
-    *ticket = 0u;         // ready for the next launch
-  }
-  // 5. block map: ceil(count / block_rows) blocks per expert, then the
-  //    shared expert's T rows at grouped row T*k.
-  const int nb = (c + block_rows - 1) / block_rows;
-  int nb_total = 0;
-  const int bstart = block_excl_scan_1024(nb, warp_tot, nb_total);
-  if (tid < E) {
-    for (int i = 0; i < nb; ++i) {
-      const int r0 = i * block_rows;
-      blocks[bstart + i] = make_int4(tid, off + r0, min(block_rows, c - r0), 0);
-    }
-  }
-  const int nb_sh = (T + block_rows - 1) / block_rows;
-  for (int i = tid; i < nb_sh; i += blockDim.x) {
-    const int r0 = i * block_rows;
-    blocks[nb_total + i] = make_int4(E, T * k + r0, min(block_rows, T - r0), 0);
-  }
-  if (tid == 0) *n_blocks = nb_total + nb_sh;
-}
-
-cudaError_t launch_scan(const uint32_t *blk_mask, int nblk, int T, int E, int k,
-                        int32_t *counts, int32_t *offsets, int32_t *blk_base, int4 *blocks,
-                        int32_t *n_blocks, unsigned int *ticket, int block_rows, bool pdl,
-                        cudaStream_t stream) {
-  return launch_kernel(scan_kernel, dim3((E + kScanExperts - 1) / kScanExperts), dim3(1024), 0,
-                       stream, pdl, blk_mask, nblk, T, E, k, counts, offsets, blk_base, blocks,
-                       n_blocks, ticket, block_rows);
-}
-
-// --------------------------------------------------------------- scatter --
-// One routing block of 32 tokens per CTA, one thread per assignment (t, j):
-// pos(t, j) = offsets[e] + (rows of e in earlier blocks) + (lower tokens of
-// this block that chose e), sorted_rows[pos] = t.  With xg, the CTA then
-// copies each of its tokens' x row to the token's k positions of xg (one warp
-// per token at a time: the row is read once, into registers, and written k
-// times), so that the grouped GEMM reads its token rows as consecutive rows.
-constexpr int kScatterChunks = 8;   // 16-byte chunks of a row per lane and pass
-
-__global__ void scatter_kernel(const int32_t *__restrict__ idx, const uint32_t *__restrict__ blk_mask,
-                               const int32_t *__restrict__ blk_base,
-                               const int32_t *__restrict__ offsets, int T, int E, int k,
-                               int32_t *__restrict__ sorted_rows,
-                               int32_t *__restrict__ pos_of_assign, const uint4 *__restrict__ x,
-                               uint4 *__restrict__ xg, int H) {
   __shared__ int pos_s[kRouteBlockTokens * 32];   // [token][slot], k <= 32
   pdl_trigger();
   pdl_wait();
-  const int tl = threadIdx.x / k;
-  const int j = threadIdx.x - tl * k;
+  const int tid = threadIdx.x;
   const int b = blockIdx.x;
+  // 1. counts: P parts of the block range per expert (Ep = E rounded up to a
+  //    power of two, P = 1024 / Ep)
+  int Ep = 1;
+  while (Ep < E) Ep <<= 1;
+  const int P = kPlaceThreads / Ep;
+  {
+    const int e = tid & (Ep - 1), part = tid / Ep;
+    const int b0 = static_cast<int>((static_cast<long long>(nblk) * part) / P);
+    const int b1 = static_cast<int>((static_cast<long long>(nblk) * (part + 1)) / P);
+    int tot = 0, bef = 0;
+    if (e < E) {
+      const uint32_t *col = blk_mask + e;
+      int bb = b0;
+      for (; bb + 8 <= b1; bb += 8) {
+        uint32_t m[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) m[i] = __ldcg(col + static_cast<size_t>(bb + i) * E);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int c = __popc(m[i]);
+          tot += c;
+          bef += (bb + i < b) ? c : 0;
+        }
+      }
+      for (; bb < b1; ++bb) {
+        const int c = __popc(__ldcg(col + static_cast<size_t>(bb) * E));
+        tot += c;
+        bef += (bb < b) ? c : 0;
+      }
+    }
+    tot_s[tid] = tot;
+    bef_s[tid] = bef;
+  }
+  __syncthreads();
+  int total_e = 0, before_e = 0;
+  if (tid < E) {
+    for (int part = 0; part < P; ++part) {
+      total_e += tot_s[part * Ep + tid];
+      before_e += bef_s[part * Ep + tid];
+    }
+  }
+  // 2. segment offsets
+  int all = 0;
+  const int off = block_excl_scan_1024(total_e, warp_tot, all);   // all = T * k
+  if (tid < E) {
+    off_s[tid] = off;
+    bef_s[tid] = before_e;   // (read only after the barrier below)
+  }
+  // 4a. block counts and starts (every CTA computes them; the scan's
+  //     barriers order the writes above)
+  const int nb = (tid < E) ? (total_e + block_rows - 1) / block_rows : 0;
+  int nb_total = 0;
+  const int bstart = block_excl_scan_1024(nb, warp_tot, nb_total);
+  // 3. positions of this block's assignments
+  const int tl = tid / k;
+  const int j = tid - tl * k;
   const int t = b * kRouteBlockTokens + tl;
   if (tl < kRouteBlockTokens && t < T) {
     const int a = t * k + j;
     const int e = idx[a];
-    const uint32_t m = blk_mask[static_cast<size_t>(b) * E + e];
+    const uint32_t m = __ldcg(blk_mask + static_cast<size_t>(b) * E + e);
     const int rank = __popc(m & ((1u << tl) - 1u));
-    const int p = offsets[e] + blk_base[static_cast<size_t>(b) * E + e] + rank;
+    const int p = off_s[e] + bef_s[e] + rank;
     pos_of_assign[a] = p;
     sorted_rows[p] = t;
     pos_s[tl * k + j] = p;
   }
+  // 4b. this CTA's share of the block map
+  if (tid < E && (tid % gridDim.x) == b) {
+    for (int i = 0; i < nb; ++i) {
+      const int r0 = i * block_rows;
+      blocks[bstart + i] = make_int4(tid, off + r0, min(block_rows, total_e - r0), 0);
+    }
+  }
+  if (b == 0) {
+    if (tid < E) {
+      counts[tid] = total_e;
+      offsets[tid] = off;
+    }
+    if (tid == 0) offsets[E] = all;
+    const int nb_sh = (T + block_rows - 1) / block_rows;
+    for (int i = tid; i < nb_sh; i += blockDim.x) {
+      const int r0 = i * block_rows;
+      blocks[nb_total + i] = make_int4(E, T * k + r0, min(block_rows, T - r0), 0);
+    }
+    if (tid == 0) *n_blocks = nb_total + nb_sh;
+  }
   if (xg == nullptr) return;
   __syncthreads();
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // 5. the token rows in grouped order
+  const int warp = tid >> 5, lane = tid & 31;
   const int nwarps = blockDim.x >> 5;
   const int nch = H / 8;   // 16-byte chunks per row
   for (int u = warp; u < kRouteBlockTokens; u += nwarps) {
@@ -346,16 +322,15 @@ __global__ void scatter_kernel(const int32_t *__restrict__ idx, const uint32_t *
   }
 }
 
-cudaError_t launch_scatter(const int32_t *idx, const uint32_t *blk_mask, const int32_t *blk_base,
-                           const int32_t *offsets, int T, int E, int k, int32_t *sorted_rows,
-                           int32_t *pos_of_assign, const void *x, void *xg, int H, bool pdl,
-                           cudaStream_t stream) {
+cudaError_t launch_place(const int32_t *idx, const uint32_t *blk_mask, int T, int E, int k,
+                         int32_t *counts, int32_t *offsets, int4 *blocks, int32_t *n_blocks,
+                         int block_rows, int32_t *sorted_rows, int32_t *pos_of_assign,
+                         const void *x, void *xg, int H, bool pdl, cudaStream_t stream) {
   const int nblk = (T + kRouteBlockTokens - 1) / kRouteBlockTokens;
-  // at least four warps per CTA for the row copies
-  const int threads = std::max(128, (kRouteBlockTokens * k + 31) / 32 * 32);
-  return launch_kernel(scatter_kernel, dim3(nblk), dim3(threads), 0, stream, pdl, idx, blk_mask,
-                       blk_base, offsets, T, E, k, sorted_rows, pos_of_assign,
-                       static_cast<const uint4 *>(x), static_cast<uint4 *>(xg), H);
+  return launch_kernel(place_kernel, dim3(nblk), dim3(kPlaceThreads), 0, stream, pdl, idx,
+                       blk_mask, nblk, T, E, k, counts, offsets, blocks, n_blocks, block_rows,
+                       sorted_rows, pos_of_assign, static_cast<const uint4 *>(x),
+                       static_cast<uint4 *>(xg), H);
 }
 
 // --------------------------------------------------------------- combine --
