@@ -142,11 +142,11 @@ def algorithmic(s: moe_synth.Shape, T: int):
 def routing_bytes(s: moe_synth.Shape, T: int, k_split: int = 4):
     """Bytes each routing kernel must move at T tokens (what the step reads
     and writes, not what a cache hierarchy adds): router GEMM x, Wr and its
-    split-K logit parts; top-k the parts, x (for the shared gate) and its
-    outputs (indices, weights, per-32-token expert masks, gates); placement
-    the indices and masks in, counts, offsets, the two permutation arrays
-    and the block list out, and x read once and written k times in grouped
-    order."""
+    split-K logit parts; top-k the parts and its outputs (indices, weights,
+    per-32-token expert masks); placement the indices and masks in, counts,
+    offsets, the two permutation arrays and the block list out, x and the
+    shared gate's weights read once, the gates out, and x written k times in
+    grouped order."""
     H, E, k = s.hidden, s.n_experts, s.top_k
     nblk = (T + 31) // 32
     x = T * H * 2
@@ -154,8 +154,9 @@ def routing_bytes(s: moe_synth.Shape, T: int, k_split: int = 4):
     masks = nblk * E * 4
     return {
         "router_gemm": x + E * H * 2 + parts,
-        "topk": parts + x + H * 2 + T * k * 8 + masks + T * 4,
-        "route_place": T * k * 4 + masks + 2 * E * 4 + 2 * T * k * 4 + x + T * k * H * 2,
+        "topk": parts + T * k * 8 + masks,
+        "route_place": T * k * 4 + masks + 2 * E * 4 + 2 * T * k * 4 + x + H * 2 + T * 4
+        + T * k * H * 2,
         "combine": (T * k + T) * H * 2 + T * k * 8 + T * 4 + x,
     }
 

@@ -379,9 +379,8 @@ moe_status enqueue_route(moe_ctx *ctx, const LayerSlot &ls, const void *x, int T
     ProfScope ps(ctx, K_TOPK, s);
     st = launched(ctx,
                   launch_topk(part, gp.k_split, gp.out_split_stride,
-                              gp.k_split > 1 ? logits : nullptr, x, ls.w.sh_gate_w, T,
-                              c.n_experts, c.top_k, c.hidden, idx, w, mask,
-                              ctx->at<float>(L.gate), ctx->prefill_pdl, s),
+                              gp.k_split > 1 ? logits : nullptr, T, c.n_experts, c.top_k, idx,
+                              w, mask, ctx->prefill_pdl, s),
                   "topk launch");
   }
   if (st) return st;
@@ -391,8 +390,8 @@ moe_status enqueue_route(moe_ctx *ctx, const LayerSlot &ls, const void *x, int T
                   launch_place(idx, mask, T, c.n_experts, c.top_k, counts, offsets,
                                ctx->at<int4>(L.blocks), ctx->at<int32_t>(L.nblocks),
                                ctx->block_rows, sorted_rows, pos, x,
-                               with_xg ? ctx->at<void>(L.xg) : nullptr, c.hidden,
-                               ctx->prefill_pdl, s),
+                               with_xg ? ctx->at<void>(L.xg) : nullptr, ls.w.sh_gate_w,
+                               ctx->at<float>(L.gate), c.hidden, ctx->prefill_pdl, s),
                   "placement launch");
   }
   return st;

@@ -91,23 +91,25 @@ cudaError_t launch_tc_gemm(const CUtensorMap &a_routed, const CUtensorMap &a_sha
                            const CUtensorMap (&b)[4], const CUtensorMap (&b2)[4],
                            const GemmParams &p, int conv, int grid, bool pdl, cudaStream_t stream);
 
-// Routing: top-k + masks, block scan + block map, stable scatter.
+// Routing: top-k + masks, then the placement (counts, offsets, block map,
+// stable scatter, shared gate, grouped copy of x).
 // Top-k over logits = sum of nsplit parts (part s at partial + s * split_stride,
 // summed in order s = 0, 1, ...); writes the sums to logits_out if non-null.
 cudaError_t launch_topk(const float *partial, int nsplit, size_t split_stride, float *logits_out,
-                        const void *x, const void *wsg, int T, int E, int k, int H, int32_t *idx,
-                        float *w, uint32_t *blk_mask, float *gate, bool pdl, cudaStream_t stream);
+                        int T, int E, int k, int32_t *idx, float *w, uint32_t *blk_mask, bool pdl,
+                        cudaStream_t stream);
 // After the top-k kernel: the per-expert counts and segment offsets
 // (offsets[E] = T * k), each assignment's grouped row (pos_of_assign) and
 // its inverse (sorted_rows), and the block map of the grouped GEMMs
 // (block_rows in kBlockRowsMin..kBlockRowsMax rows per block).  With xg
 // non-null, also writes xg[pos(t, j)] = x[t] (x [T, H] bf16, xg [T * k, H]
 // bf16: the token rows in grouped order, the routed gate/up GEMM's B
-// operand).
+// operand); with gate non-null, gate[t] = sigmoid(x[t] . wsg) (wsg [H] bf16).
 cudaError_t launch_place(const int32_t *idx, const uint32_t *blk_mask, int T, int E, int k,
                          int32_t *counts, int32_t *offsets, int4 *blocks, int32_t *n_blocks,
                          int block_rows, int32_t *sorted_rows, int32_t *pos_of_assign,
-                         const void *x, void *xg, int H, bool pdl, cudaStream_t stream);
+                         const void *x, void *xg, const void *wsg, float *gate, int H, bool pdl,
+                         cudaStream_t stream);
 
 // y[t] = sum_j w[t,j] o[pos(t,j)] + g[t] o[T*k + t]
 cudaError_t launch_combine(const float *gate, const void *o, const int32_t *pos, const float *w,

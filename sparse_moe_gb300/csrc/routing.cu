@@ -20,16 +20,14 @@ namespace moe {
 // ----------------------------------------------------------------- top-k --
 // One routing block of 32 tokens per CTA, one token per warp: the token's
 // logits (the sum of the router GEMM's split-K parts, in part order), its
-// top-k and weights, its bit in the block's per-expert masks, and the
-// shared-expert gate g[t] = sigmoid(x[t] . w_sg) for the combine.
+// top-k and weights, and its bit in the block's per-expert masks.
 constexpr int kTopkThreads = 32 * kRouteBlockTokens;
 
 template <int R, int SP>
 __global__ void __launch_bounds__(kTopkThreads) topk_kernel(
     const float *__restrict__ partial, int nsplit, size_t split_stride, float *__restrict__ logits_out,
-    const __nv_bfloat16 *__restrict__ x,
-    const __nv_bfloat16 *__restrict__ wsg, int T, int E, int k, int H, int32_t *__restrict__ idx,
-    float *__restrict__ w, uint32_t *__restrict__ blk_mask, float *__restrict__ gate) {
+    int T, int E, int k, int32_t *__restrict__ idx, float *__restrict__ w,
+    uint32_t *__restrict__ blk_mask) {
   __shared__ uint32_t mask_s[1024];
   pdl_trigger();
   for (int e = threadIdx.x; e < E; e += blockDim.x) mask_s[e] = 0;
@@ -78,20 +76,6 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(
         if (e < E) logits_out[static_cast<size_t>(t) * E + e] = v[r];
       }
     }
-    // the shared gate's dot product, loads in flight with the logits
-    const uint4 *x4 = reinterpret_cast<const uint4 *>(x + static_cast<size_t>(t) * H);
-    const uint4 *g4 = reinterpret_cast<const uint4 *>(wsg);
-    float d = 0.0f;
-#pragma unroll 4
-    for (int c = lane; c < H / 8; c += 32) {
-      const uint4 xv = x4[c], gv = __ldg(g4 + c);
-      const uint32_t xa[4] = {xv.x, xv.y, xv.z, xv.w}, ga[4] = {gv.x, gv.y, gv.z, gv.w};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        d = fmaf(bf16_lo(xa[i]), bf16_lo(ga[i]), d);
-        d = fmaf(bf16_hi(xa[i]), bf16_hi(ga[i]), d);
-      }
-    }
     int se;
     float sw;
     warp_topk_redux<R>(v, E, k, se, sw);
@@ -100,9 +84,6 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(
       w[static_cast<size_t>(t) * k + lane] = sw;
       atomicOr(&mask_s[se], 1u << tl);
     }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
-    if (lane == 0) gate[t] = sigmoid_f(d);
   }
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += blockDim.x)
@@ -110,17 +91,15 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(
 }
 
 cudaError_t launch_topk(const float *partial, int nsplit, size_t split_stride, float *logits_out,
-                        const void *x, const void *wsg, int T, int E, int k, int H, int32_t *idx,
-                        float *w, uint32_t *blk_mask, float *gate, bool pdl, cudaStream_t stream) {
+                        int T, int E, int k, int32_t *idx, float *w, uint32_t *blk_mask, bool pdl,
+                        cudaStream_t stream) {
   const int nblk = (T + kRouteBlockTokens - 1) / kRouteBlockTokens;
   const int R = (E + 31) / 32;
-  const __nv_bfloat16 *xb = static_cast<const __nv_bfloat16 *>(x);
-  const __nv_bfloat16 *gb = static_cast<const __nv_bfloat16 *>(wsg);
   // SP: parts loaded together (up to 4 parts for E <= 256), 0: part by part
   cudaError_t e = cudaSuccess;
 #define MOE_TOPK(RR, SS)                                                                        \
   e = launch_kernel(topk_kernel<RR, SS>, dim3(nblk), dim3(kTopkThreads), 0, stream, pdl, partial, \
-                    nsplit, split_stride, logits_out, xb, gb, T, E, k, H, idx, w, blk_mask, gate)
+                    nsplit, split_stride, logits_out, T, E, k, idx, w, blk_mask)
 #define MOE_TOPK_R(RR)                        \
   if (nsplit == 1) MOE_TOPK(RR, 1);           \
   else if (nsplit <= 4) MOE_TOPK(RR, 4);      \
@@ -153,10 +132,11 @@ cudaError_t launch_topk(const float *partial, int nsplit, size_t split_stride, f
 //     grouped row T * k; each CTA writes the blocks of the experts e with
 //     e % gridDim.x == blockIdx.x, CTA 0 the counts, offsets, shared blocks and
 //     block count;
-//  5. with xg, each token's x row is copied to its k positions of xg (one
-//     warp per token: the row is read once, into registers, and written k
-//     times), so that the grouped gate/up GEMM reads its token rows as
-//     consecutive rows.
+//  5. one warp per token reads the token's x row once, into registers: with
+//     gate, the shared-expert gate g[t] = sigmoid(x[t] . w_sg) for the
+//     combine; with xg, the row is written to the token's k positions of xg,
+//     so that the grouped gate/up GEMM reads its token rows as consecutive
+//     rows.
 // Every result is an integer function of the masks and indices: independent
 // of thread timing and of which CTA computes it.
 constexpr int kPlaceThreads = 1024;
@@ -196,7 +176,7 @@ __global__ void __launch_bounds__(kPlaceThreads) place_kernel(
     int k, int32_t *__restrict__ counts, int32_t *__restrict__ offsets, int4 *__restrict__ blocks,
     int32_t *__restrict__ n_blocks, int block_rows, int32_t *__restrict__ sorted_rows,
     int32_t *__restrict__ pos_of_assign, const uint4 *__restrict__ x, uint4 *__restrict__ xg,
-    int H) {
+    const uint4 *__restrict__ wsg, float *__restrict__ gate, int H) {
   __shared__ int tot_s[kPlaceThreads];    // per (part, expert), then per expert
   __shared__ int bef_s[kPlaceThreads];
   __shared__ int off_s[kPlaceThreads];
@@ -293,9 +273,9 @@ __global__ void __launch_bounds__(kPlaceThreads) place_kernel(
     }
     if (tid == 0) *n_blocks = nb_total + nb_sh;
   }
-  if (xg == nullptr) return;
+  if (xg == nullptr && gate == nullptr) return;
   __syncthreads();
-  // 5. the token rows in grouped order
+  // 5. the shared gate and the token rows in grouped order
   const int warp = tid >> 5, lane = tid & 31;
   const int nwarps = blockDim.x >> 5;
   const int nch = H / 8;   // 16-byte chunks per row
@@ -303,6 +283,7 @@ __global__ void __launch_bounds__(kPlaceThreads) place_kernel(
     const int tt = b * kRouteBlockTokens + u;
     if (tt >= T) break;
     const uint4 *src = x + static_cast<size_t>(tt) * nch;
+    float d = 0.0f;   // this lane's part of x[tt] . w_sg (chunks lane + 32 i, in order)
     for (int c0 = 0; c0 < nch; c0 += 32 * kScatterChunks) {
       uint4 v[kScatterChunks];
 #pragma unroll
@@ -310,6 +291,23 @@ __global__ void __launch_bounds__(kPlaceThreads) place_kernel(
         const int c = c0 + lane + 32 * i;
         if (c < nch) v[i] = __ldg(src + c);
       }
+      if (gate != nullptr) {
+#pragma unroll
+        for (int i = 0; i < kScatterChunks; ++i) {
+          const int c = c0 + lane + 32 * i;
+          if (c < nch) {
+            const uint4 gv = __ldg(wsg + c);
+            const uint32_t xa[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+            const uint32_t ga[4] = {gv.x, gv.y, gv.z, gv.w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              d = fmaf(bf16_lo(xa[q]), bf16_lo(ga[q]), d);
+              d = fmaf(bf16_hi(xa[q]), bf16_hi(ga[q]), d);
+            }
+          }
+        }
+      }
+      if (xg == nullptr) continue;
       for (int jj = 0; jj < k; ++jj) {
         uint4 *dst = xg + static_cast<size_t>(pos_s[u * k + jj]) * nch;
 #pragma unroll
@@ -319,18 +317,24 @@ __global__ void __launch_bounds__(kPlaceThreads) place_kernel(
         }
       }
     }
+    if (gate != nullptr) {
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
+      if (lane == 0) gate[tt] = sigmoid_f(d);
+    }
   }
 }
 
 cudaError_t launch_place(const int32_t *idx, const uint32_t *blk_mask, int T, int E, int k,
                          int32_t *counts, int32_t *offsets, int4 *blocks, int32_t *n_blocks,
                          int block_rows, int32_t *sorted_rows, int32_t *pos_of_assign,
-                         const void *x, void *xg, int H, bool pdl, cudaStream_t stream) {
+                         const void *x, void *xg, const void *wsg, float *gate, int H, bool pdl,
+                         cudaStream_t stream) {
   const int nblk = (T + kRouteBlockTokens - 1) / kRouteBlockTokens;
   return launch_kernel(place_kernel, dim3(nblk), dim3(kPlaceThreads), 0, stream, pdl, idx,
                        blk_mask, nblk, T, E, k, counts, offsets, blocks, n_blocks, block_rows,
                        sorted_rows, pos_of_assign, static_cast<const uint4 *>(x),
-                       static_cast<uint4 *>(xg), H);
+                       static_cast<uint4 *>(xg), static_cast<const uint4 *>(wsg), gate, H);
 }
 
 // --------------------------------------------------------------- combine --
