@@ -163,7 +163,17 @@ struct Tile {
   int out_limit;       // number of valid output rows of the operator (I/Is, H, E)
 };
 
-__device__ __forceinline__ Tile decode_tile(const GemmParams &p, int tile, int rank) {
+// The block-list entry of a grouped tile (zeros for the router, whose tiles
+// need none, and past the last tile).  Each role loads the entry of its next
+// tile while it works on the current one, so that decoding a tile never waits
+// for a global load (about 800 cycles at the top of every tile in the
+// MMA-issuing thread otherwise).
+__device__ __forceinline__ int4 load_tile_block(const GemmParams &p, int tile, int ntiles) {
+  if (p.mode == MODE_ROUTER || tile >= ntiles) return make_int4(0, 0, 0, 0);
+  return p.blocks[tile / p.m_tiles];
+}
+
+__device__ __forceinline__ Tile decode_tile(const GemmParams &p, int tile, int rank, int4 blk) {
   Tile t;
   t.k0 = 0;
   t.split = 0;
@@ -179,7 +189,6 @@ __device__ __forceinline__ Tile decode_tile(const GemmParams &p, int tile, int r
     t.nrows = min(p.block_rows, p.T - t.row0);
     t.shared = 0;
   } else {
-    const int4 blk = p.blocks[b];
     e = blk.x;
     t.row0 = blk.y;
     t.nrows = blk.z;
@@ -605,8 +614,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(num_threads<CONV>(),
     bool ok = true;
     if (lane == 0) {
       int st = 0;
+      int4 blk = load_tile_block(p, pair_id, ntiles);
       for (int tile = pair_id; tile < ntiles && ok; tile += num_pairs) {
-        const Tile t = decode_tile(p, tile, rank);
+        const Tile t = decode_tile(p, tile, rank, blk);
+        blk = load_tile_block(p, tile + num_pairs, ntiles);
         if (!t.valid) continue;
         const CUtensorMap *amap = t.shared ? &maps.a_shared : &maps.a_routed;
         const bool b_from_x = p.mode == MODE_GATEUP && t.shared;   // shared expert: x rows
@@ -694,8 +705,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(num_threads<CONV>(),
 #pragma unroll
       for (int s2 = 0; s2 < kCodeSlots; ++s2) issued_parity[s2] = -1;
       bool ok = true;
+      int4 blk = load_tile_block(p, pair_id, ntiles);
       for (int tile = pair_id; tile < ntiles && ok; tile += num_pairs) {
-        const Tile t = decode_tile(p, tile, rank);
+        const Tile t = decode_tile(p, tile, rank, blk);
+        blk = load_tile_block(p, tile + num_pairs, ntiles);
         if (!t.valid) continue;
         const CUtensorMap *amap = t.shared ? &maps.a_shared : &maps.a_routed;
         for (int ks = 0; ks < t.ns * HALVES; ++ks) {
@@ -752,11 +765,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(num_threads<CONV>(),
         // 256 KB)
         const uint64_t a_desc0 = smem_desc_sw128(smem_base);
         const uint64_t b_desc0 = smem_desc_sw128(smem_base + A_BYTES);
-        // the next tile's block-list entry is read one tile ahead
-        Tile tn = decode_tile(p, pair_id < ntiles ? pair_id : 0, 0);
+        int4 blk = load_tile_block(p, pair_id, ntiles);
         for (int tile = pair_id; tile < ntiles && ok; tile += num_pairs) {
-          const Tile t = tn;
-          if (tile + num_pairs < ntiles) tn = decode_tile(p, tile + num_pairs, 0);
+          const Tile t = decode_tile(p, tile, 0, blk);
+          blk = load_tile_block(p, tile + num_pairs, ntiles);
           if (!t.valid) continue;
           if (!mbar_wait_bounded_cluster(smem_u32(&tail->tmem_empty[acc]), aphase ^ 1, abort_flag,
                                          p.status, DEV_TIMEOUT_MMA)) {
@@ -839,8 +851,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(num_threads<CONV>(),
     // would otherwise sit inside every expansion).
     float sv_next[kInt4Batches] = {}, bv_next[kInt4Batches] = {};
     bool have_next = false;
+    int4 blk = load_tile_block(p, pair_id, ntiles);
     for (int tile = pair_id; tile < ntiles && ok; tile += num_pairs) {
-      const Tile t = decode_tile(p, tile, rank);
+      const Tile t = decode_tile(p, tile, rank, blk);
+      blk = load_tile_block(p, tile + num_pairs, ntiles);
       if (!t.valid) continue;
       for (int jj = 0; jj < t.ns; ++jj, ++st) {
         const int ks = jj * HALVES + h;
@@ -881,8 +895,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(num_threads<CONV>(),
     int acc = 0;
     uint32_t aphase = 0;
     bool range_bad = false;   // a stored h or o value outside the fp16 range
+    int4 blk = load_tile_block(p, pair_id, ntiles);
     for (int tile = pair_id; tile < ntiles; tile += num_pairs) {
-      const Tile t = decode_tile(p, tile, rank);
+      const Tile t = decode_tile(p, tile, rank, blk);
+      blk = load_tile_block(p, tile + num_pairs, ntiles);
       if (!t.valid) continue;
       int got = 1;
       if (lane == 0) {
