@@ -332,10 +332,11 @@ int router_block_rows(const moe_ctx *ctx, int T) {
   return static_cast<int>(std::min<long long>(kBlockRowsMax, std::max<long long>(32, br)));
 }
 
-// Router GEMM, top-k, histogram/scan/block map, scatter for T <= Tc tokens;
-// the summed logits go to `logits` when it is non-null.  map_x: the token-row
-// maps of x (T rows); with_xg: the scatter also writes x in grouped order
-// into the workspace (the routed gate/up GEMM's token rows).
+// Router GEMM, top-k, then the placement kernel (histogram, scan, block map,
+// scatter, shared gate) for T <= Tc tokens; the summed logits go to `logits`
+// when it is non-null.  map_x: the token-row maps of x (T rows); with_xg: the
+// placement also writes x in grouped order into the workspace (the routed
+// gate/up GEMM's token rows).
 moe_status enqueue_route(moe_ctx *ctx, const LayerSlot &ls, const void *x, int T, float *logits,
                          int32_t *idx, float *w, int32_t *counts, int32_t *offsets,
                          int32_t *sorted_rows, int32_t *pos, const CUtensorMap (&map_x)[4],
