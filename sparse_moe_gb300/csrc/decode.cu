@@ -290,6 +290,72 @@ __device__ __forceinline__ void warp_dots_x(const void *const (&rows)[NR],
   for (int r = 0; r < NR; ++r) out[r] = warp_sum(acc[r]);
 }
 
+// int4 rows: the activation pairs (and, affine, the sums) of this lane's
+// chunks of x, formed once per warp for every row it dots in a phase;
+// warp_dots_x forms them again for each call.  The same values in the same
+// order, so the dot products are bit-identical.  Only for a single segment
+// (K <= 32 * U * EPC elements: K <= 2048).
+template <int WF> struct XPairs {
+  uint32_t h[Fmt<WF>::U][4][4];
+  float s[Fmt<WF>::U];
+};
+template <int WF>
+__device__ __forceinline__ bool xpairs_fit(int K) {
+  return K / Fmt<WF>::EPC <= 32 * Fmt<WF>::U;
+}
+template <int WF>
+__device__ __forceinline__ void make_xpairs(const uint4 *xs, int K, uint32_t mb_x, uint32_t par,
+                                            int *status, XPairs<WF> &xp) {
+  using F = Fmt<WF>;
+  const int lane = threadIdx.x & 31;
+  const int nchunk = K / F::EPC;
+  {
+    volatile int no_abort = 0;
+    mbar_wait_bounded(mb_x, par, &no_abort, status, DEV_TIMEOUT_STAGE);
+  }
+  uint4 xv[F::U][F::XPC];
+  seg_load_x<WF>(xs, nchunk, 0, lane, xv);
+#pragma unroll
+  for (int u = 0; u < F::U; ++u) {
+    xp.s[u] = 0.0f;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      xpairs_bf16(xv[u][q], xp.h[u][q]);
+      if constexpr (WF == 2)
+        xp.s[u] += (bf16_lo(xv[u][q].x) + bf16_hi(xv[u][q].x)) +
+                   (bf16_lo(xv[u][q].y) + bf16_hi(xv[u][q].y)) +
+                   (bf16_lo(xv[u][q].z) + bf16_hi(xv[u][q].z)) +
+                   (bf16_lo(xv[u][q].w) + bf16_hi(xv[u][q].w));
+    }
+  }
+}
+// warp_dots_x for int4 rows with the activation pairs already formed.
+template <int WF, int NR>
+__device__ __forceinline__ void warp_dots_xp(const void *const (&rows)[NR],
+                                             const __nv_bfloat16 *const (&srows)[NR],
+                                             const __nv_bfloat16 *const (&brows)[NR], int K,
+                                             const XPairs<WF> &xp, float (&out)[NR]) {
+  using F = Fmt<WF>;
+  const int lane = threadIdx.x & 31;
+  const int nchunk = K / F::EPC;
+  uint4 wv[NR][F::U];
+  float sv[NR][F::U], bv[NR][F::U];
+  seg_load_w<WF, NR, false>(rows, srows, brows, nchunk, 0, lane, wv, sv, bv);
+  float acc[NR];
+#pragma unroll
+  for (int r = 0; r < NR; ++r) {
+    acc[r] = 0.0f;
+#pragma unroll
+    for (int u = 0; u < F::U; ++u) {
+      const float qx = dot32_int4<WF == 1>(wv[r][u], xp.h[u]);
+      if constexpr (WF == 1) acc[r] = fmaf(sv[r][u], qx, acc[r]);
+      else acc[r] = fmaf(sv[r][u], qx, fmaf(bv[r][u], xp.s[u], acc[r]));
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < NR; ++r) out[r] = warp_sum(acc[r]);
+}
+
 // The same for several activation rows: row t (bit t of `users`) is at
 // xs + t * xq, and out(t, d) receives its NR sums (in every lane).  One
 // warp_dots_x per user, the weights through L1, so that a row comes from HBM
@@ -648,6 +714,10 @@ __device__ __forceinline__ void decode_layer(const DecodeParams &p, const DecCta
   float *hg = p.h;   // [k+1][h_ld]: h of the k experts, then of the shared expert
   const size_t rbI = row_bytes<WF>(p.I);
   const int nA = p.E + 1 + p.Is;   // phase-A items: router rows, the gate row, shared pairs
+  // int4: this warp's activation pairs, formed once for phases A and B
+  const bool use_xp = WF != 0 && xpairs_fit<WF>(p.H);
+  XPairs<WF == 0 ? 1 : WF> xp;
+  bool have_xp = false;
   (void)n1;
   (void)lane;
   (void)x;
@@ -680,7 +750,19 @@ __device__ __forceinline__ void decode_layer(const DecodeParams &p, const DecCta
       const __nv_bfloat16 *br[2] = {scale_row(p.sh_gate_up_bias, i, p.H),
                                     scale_row(p.sh_gate_up_bias, p.Is + i, p.H)};
       float d[2];
-      warp_dots_x<WF, 2>(rows, sr, br, p.H, c.x_s, c.mb_x, par, p.status, d);
+      if constexpr (WF != 0) {
+        if (use_xp) {
+          if (!have_xp) {
+            make_xpairs<WF>(c.x_s, p.H, c.mb_x, par, p.status, xp);
+            have_xp = true;
+          }
+          warp_dots_xp<WF, 2>(rows, sr, br, p.H, xp, d);
+        } else {
+          warp_dots_x<WF, 2>(rows, sr, br, p.H, c.x_s, c.mb_x, par, p.status, d);
+        }
+      } else {
+        warp_dots_x<WF, 2>(rows, sr, br, p.H, c.x_s, c.mb_x, par, p.status, d);
+      }
       if (lane == 0) hg[static_cast<size_t>(p.k) * p.h_ld + i] = silu_f(d[0]) * d[1];
     }
   }
@@ -758,7 +840,19 @@ __device__ __forceinline__ void decode_layer(const DecodeParams &p, const DecCta
     const __nv_bfloat16 *br[2] = {scale_row(p.gate_up_bias, rg, p.H),
                                   scale_row(p.gate_up_bias, rg + p.I, p.H)};
     float d[2];
-    warp_dots_x<WF, 2>(rows, sr, br, p.H, c.x_s, c.mb_x, par, p.status, d);
+    if constexpr (WF != 0) {
+      if (use_xp) {
+        if (!have_xp) {
+          make_xpairs<WF>(c.x_s, p.H, c.mb_x, par, p.status, xp);
+          have_xp = true;
+        }
+        warp_dots_xp<WF, 2>(rows, sr, br, p.H, xp, d);
+      } else {
+        warp_dots_x<WF, 2>(rows, sr, br, p.H, c.x_s, c.mb_x, par, p.status, d);
+      }
+    } else {
+      warp_dots_x<WF, 2>(rows, sr, br, p.H, c.x_s, c.mb_x, par, p.status, d);
+    }
     if (lane == 0) hg[static_cast<size_t>(j) * p.h_ld + i] = silu_f(d[0]) * d[1];
   }
   // The shared expert's slot needs only h_s (complete since the first
