@@ -7,7 +7,7 @@
 //   down:    o[p, n]  = sum_i h[p,i] Wd[e,n,i]                      -> fp16
 //
 // where p runs over the rows routed to expert e in grouped order and xg is x
-// in that order (written by the routing's scatter step).
+// in that order (written by the routing's placement kernel).
 // (Sections "Dequantize weights during matrix multiplication", "Keep expert
 // routing on the GPU" and "Match tile size to expert load" of "Optimizing
 // On-Device Inference for Apple Silicon": grouped GEMM over the rows routed
@@ -34,7 +34,9 @@
 //    threads issuing 32 KB stages move about 78.  The tiles need about 64 at
 //    the tensor cores' full rate.  cp.async gathers of scattered rows reach
 //    about 28 and TMA gather4 about 3, which is why the gate/up token rows
-//    are read from a grouped copy of x rather than gathered.)
+//    are read from a grouped copy of x rather than gathered.  A version
+//    whose own gather warps copied the rows from x with cp.async measured
+//    slower: gate/up 217 against 167 us at T=4096.)
 //  * the pair's CTAs walk the device-built tile list persistently; one thread
 //    of the leader issues the MMAs once both CTAs' stage is ready.  Without a
 //    conversion (router, bf16 gate/up, down on fp16 weights) both CTAs' boxes
@@ -42,9 +44,10 @@
 //    needs no relay; when the weight tile must be converted first (int4
 //    codes, or bf16 down weights without fp16 copies), a team of four
 //    converter warps per k-step arrives on the leader's ready barrier;
-//    four epilogue warps per CTA drain their half of the double-buffered
-//    TMEM accumulator while the next tile computes, and transpose each 32x16
-//    piece through shared memory so global stores are 16-byte vectors;
+//    epilogue warps (two groups of four without a conversion) drain the
+//    double-buffered TMEM accumulator while the next tile computes, and
+//    transpose each 32x16 piece through shared memory so global stores are
+//    16-byte vectors;
 //  * the down projection runs with fp16 operands: the gate/up epilogue stores
 //    h in fp16 (11 significant bits instead of bf16's 8), and bf16 weight
 //    tiles are turned into fp16 in place in shared memory before the MMA
