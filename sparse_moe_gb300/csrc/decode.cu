@@ -7,10 +7,14 @@
 //
 //   A. router logits (+bias), the shared-expert gate sigmoid(x . w_sg) and
 //      the shared expert's gate and up dot products (all need only x);
-//   B. top-k selection (redone by every warp from the logits in L2), then the
-//      k routed experts' gate and up dot products;
+//   B. top-k selection (redone by one warp of every CTA from the logits in
+//      L2), then the k routed experts' gate and up dot products;
 //   C. y[n] = sum_j w_j (Wd_j h_j)[n] + g (Sd h_s)[n] in fixed j order, with
 //      h = silu(gate) * up formed from the phase-A/B dot products.
+//
+// The first barrier waits for the router rows alone: the shared expert's
+// rows, whose h only C needs, run beside it on the other warps and are
+// announced on a second counter.
 //
 // Phase C's weights are known early: the shared expert's output rows at the
 // start, the routed experts' right after top-k.  Each CTA owns a contiguous
@@ -400,23 +404,30 @@ __device__ __forceinline__ void red_release_add_u64(unsigned long long *p, unsig
   asm volatile("red.release.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 
+// Wait (one thread) until the counter holds `target` arrivals; the writes
+// those arrivals released are visible afterwards.  A thread that waits longer
+// than kWaitLimitCycles records DEV_TIMEOUT_GRID and carries on.
+__device__ __forceinline__ void grid_wait(const unsigned long long *bar, unsigned long long target,
+                                          int *status) {
+  if (ld_acquire_u64(bar) < target) {
+    const long long t0 = clock64();
+    while (ld_acquire_u64(bar) < target) {
+      if (clock64() - t0 > kWaitLimitCycles) {
+        atomicExch(status, DEV_TIMEOUT_GRID);
+        break;
+      }
+    }
+  }
+}
+
 // Arrive and wait until `target` arrivals; the CTA's earlier writes are
-// released with the arrival.  A CTA that waits longer than kWaitLimitCycles
-// records DEV_TIMEOUT_GRID and carries on.
+// released with the arrival.
 __device__ __forceinline__ void grid_sync(unsigned long long *bar, unsigned long long target,
                                           int *status) {
   __syncthreads();
   if (threadIdx.x == 0) {
     red_release_add_u64(bar, 1ull);
-    if (ld_acquire_u64(bar) < target) {
-      const long long t0 = clock64();
-      while (ld_acquire_u64(bar) < target) {
-        if (clock64() - t0 > kWaitLimitCycles) {
-          atomicExch(status, DEV_TIMEOUT_GRID);
-          break;
-        }
-      }
-    }
+    grid_wait(bar, target, status);
   }
   __syncthreads();
 }
@@ -691,13 +702,16 @@ __device__ __forceinline__ void layer_prefetch(const DecodeParams &p, const DecC
 
 // One decode layer, phases A to C (see the top of this file), after
 // layer_prefetch(p) has been issued and the layer's input is ready.  `par`
-// is the parity of this layer's mbarrier phases, bar_base the barrier
-// counter its two grid barriers count from (thread 0 only); `next`, if not
-// null, is the following layer, whose layer_prefetch is issued after this
-// layer's second grid barrier.
+// is the parity of this layer's mbarrier phases, bar_base the value of the
+// barrier counter p.bar[0] its two grid barriers count from (thread 0 only),
+// sh_base that of p.bar[1], on which every CTA announces its share of the
+// shared expert's h (all threads); `next`, if not null, is the following
+// layer, whose layer_prefetch is issued after this layer's second grid
+// barrier.
 template <int WF, int R>
 __device__ __forceinline__ void decode_layer(const DecodeParams &p, const DecCta &c, uint32_t par,
-                                             unsigned long long bar_base, const DecodeParams *next,
+                                             unsigned long long bar_base,
+                                             unsigned long long sh_base, const DecodeParams *next,
                                              int *idx_s, float *w_s) {
   float *part = c.part;
   unsigned char *w3 = c.w3;
@@ -713,7 +727,6 @@ __device__ __forceinline__ void decode_layer(const DecodeParams &p, const DecCta
   const int nw = G * kDecWarps;
   float *hg = p.h;   // [k+1][h_ld]: h of the k experts, then of the shared expert
   const size_t rbI = row_bytes<WF>(p.I);
-  const int nA = p.E + 1 + p.Is;   // phase-A items: router rows, the gate row, shared pairs
   // int4: this warp's activation pairs, formed once for phases A and B
   const bool use_xp = WF != 0 && xpairs_fit<WF>(p.H);
   XPairs<WF == 0 ? 1 : WF> xp;
@@ -730,9 +743,15 @@ __device__ __forceinline__ void decode_layer(const DecodeParams &p, const DecCta
     mbar_arrive_expect_tx(mb_x, xbytes);
     bulk_copy_g2s(smem_u32(c.x_s), p.x, xbytes, mb_x);
   }
-  // ---- phase A: router rows, the shared gate row, shared-expert row pairs
-  for (int it = gw; it < nA; it += nw) {
-    if (it <= p.E) {
+  // ---- phase A: router rows and the shared gate row on the first RW warps
+  // of every CTA, which arrive on the grid barrier as soon as they are done;
+  // the shared expert's row pairs on the other warps meanwhile (their h is
+  // needed only by the output projection: every CTA announces its share on
+  // the second counter, p.bar[1]).  Top-k then waits for the router alone.
+  const int nR = p.E + 1;
+  const int RW = min(kDecWarps - 1, (nR + G - 1) / G);
+  if (warp < RW) {
+    for (int it = warp * G + blockIdx.x; it < nR; it += RW * G) {
       const void *rows[1] = {it < p.E ? row_ptr<0>(p.router_w, it, p.H) : p.sh_gate_w};
       const __nv_bfloat16 *sr[1] = {nullptr};
       float d[1];
@@ -741,8 +760,14 @@ __device__ __forceinline__ void decode_layer(const DecodeParams &p, const DecCta
         if (it < p.E) p.logits[it] = d[0] + (p.router_b ? p.router_b[it] : 0.0f);
         else *p.g = sigmoid_f(d[0]);
       }
-    } else {
-      const int i = it - p.E - 1;
+    }
+    named_bar_sync(1, RW * 32);
+    if (threadIdx.x == 0) {
+      red_release_add_u64(p.bar, 1ull);
+      grid_wait(p.bar, bar_base + G, p.status);
+    }
+  } else {
+    for (int i = (warp - RW) * G + blockIdx.x; i < p.Is; i += (kDecWarps - RW) * G) {
       const void *rows[2] = {row_ptr<WF>(p.sh_gate_up, i, p.H),
                              row_ptr<WF>(p.sh_gate_up, p.Is + i, p.H)};
       const __nv_bfloat16 *sr[2] = {scale_row(p.sh_gate_up_scale, i, p.H),
@@ -765,11 +790,14 @@ __device__ __forceinline__ void decode_layer(const DecodeParams &p, const DecCta
       }
       if (lane == 0) hg[static_cast<size_t>(p.k) * p.h_ld + i] = silu_f(d[0]) * d[1];
     }
+    named_bar_sync(2, (kDecWarps - RW) * 32);
+    if (threadIdx.x == RW * 32) red_release_add_u64(p.bar + 1, 1ull);
   }
-  grid_sync(p.bar, bar_base + G, p.status);
 
-  // ---- top-k (one warp per CTA; the logits are in L2)
+  // ---- top-k (one warp per CTA, after the first grid barrier; the logits
+  // are in L2)
   if (warp == 0) {
+    __syncwarp();
     float v[R];
 #pragma unroll
     for (int r = 0; r < R; ++r) {
@@ -855,8 +883,12 @@ __device__ __forceinline__ void decode_layer(const DecodeParams &p, const DecCta
     }
     if (lane == 0) hg[static_cast<size_t>(j) * p.h_ld + i] = silu_f(d[0]) * d[1];
   }
-  // The shared expert's slot needs only h_s (complete since the first
-  // barrier): the last warps, which have the fewest phase-B rows, do it now.
+  // The shared expert's slot needs only h_s (announced on p.bar[1] long
+  // before): the last warps, which have the fewest phase-B rows, do it now.
+  if (kDecWarps - 1 - warp < ngroups) {
+    if (lane == 0) grid_wait(p.bar + 1, sh_base + G, p.status);
+    __syncwarp();
+  }
   for (int s = kDecWarps - 1 - warp; s < ngroups; s += kDecWarps) {
     if (p.p3_stage) {
       volatile int no_abort = 0;
@@ -918,13 +950,16 @@ __global__ void __launch_bounds__(kDecLayerThreads, 1) decode_layer_kernel(const
   const int G = gridDim.x;
   const int gw = (threadIdx.x >> 5) * G + blockIdx.x;
 
+  __shared__ unsigned long long sh_base_s;
   unsigned long long base = 0;   // barrier counter at launch (used by thread 0)
   if (threadIdx.x == 0) {
     // With a programmatic launch this CTA can start while the previous
     // layer's CTAs finish, but only after the one on this SM exited, i.e.
-    // after that layer's last barrier completed: the counter is final.
+    // after that layer's last barrier completed: both counters are final.
     const unsigned long long v = ld_acquire_u64(p.bar);
     base = v - v % static_cast<unsigned long long>(G);
+    const unsigned long long v1 = ld_acquire_u64(p.bar + 1);
+    sh_base_s = v1 - v1 % static_cast<unsigned long long>(G);
     if (p.p3_stage) {
       mbar_init(c.mb_sh, 1);
       mbar_init(c.mb_rt, 1);
@@ -938,7 +973,7 @@ __global__ void __launch_bounds__(kDecLayerThreads, 1) decode_layer_kernel(const
   layer_prefetch<WF>(p, c, gw);
   pdl_trigger();
   pdl_wait();
-  decode_layer<WF, R>(p, c, 0u, base, nullptr, idx_s, w_s);
+  decode_layer<WF, R>(p, c, 0u, base, sh_base_s, nullptr, idx_s, w_s);
 }
 
 // The same for n consecutive layers in one launch (P.layer[0..n-1], same
@@ -957,10 +992,13 @@ __global__ void __launch_bounds__(kDecLayerThreads, 1)
   const DecCta c = make_dec_cta<WF>(p0, dsm, mbar);
   const int G = gridDim.x;
   const int gw = (threadIdx.x >> 5) * G + blockIdx.x;
+  __shared__ unsigned long long sh_base_s;
   unsigned long long base = 0;
   if (threadIdx.x == 0) {
     const unsigned long long v = ld_acquire_u64(p0.bar);
     base = v - v % static_cast<unsigned long long>(G);
+    const unsigned long long v1 = ld_acquire_u64(p0.bar + 1);
+    sh_base_s = v1 - v1 % static_cast<unsigned long long>(G);
     if (p0.p3_stage) {
       mbar_init(c.mb_sh, 1);
       mbar_init(c.mb_rt, 1);
@@ -976,6 +1014,7 @@ __global__ void __launch_bounds__(kDecLayerThreads, 1)
     const DecodeParams &p = P.layer[l];
     const unsigned long long lb = base + 3ull * static_cast<unsigned long long>(l) * G;
     decode_layer<WF, R>(p, c, static_cast<uint32_t>(l & 1), lb,
+                        sh_base_s + static_cast<unsigned long long>(l) * G,
                         l + 1 < P.n ? &P.layer[l + 1] : nullptr, idx_s, w_s);
     // layer l's outputs are complete before layer l + 1 reads its input
     if (l + 1 < P.n) grid_sync(p.bar, lb + 3ull * G, p.status);
