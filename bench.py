@@ -124,10 +124,10 @@ class ClockSampler:
 # DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) of
 # the kernels the roofline lines name, from one ncu capture of the current
 # kernels (the summaries under profiles/): gate/up 705.0 + 33.8 MB at the
-# T=4096 prefill workload, decode layer 57.76 + 0.42 MB (bf16),
-# 16.21 + 0.00 MB (symmetric int4) and 17.10 + 0.00 MB (affine int4).
-TRAFFIC_BYTES = {"gateup_swiglu_gemm": 738.9e6, "decode_layer": 58.18e6,
-                 "decode_layer_int4_sym": 16.21e6, "decode_layer_int4_affine": 17.10e6}
+# T=4096 prefill workload, decode layer 57.77 + 0.51 MB (bf16),
+# 16.21 + 0.00 MB (symmetric int4) and 17.11 + 0.00 MB (affine int4).
+TRAFFIC_BYTES = {"gateup_swiglu_gemm": 738.9e6, "decode_layer": 58.29e6,
+                 "decode_layer_int4_sym": 16.21e6, "decode_layer_int4_affine": 17.11e6}
 
 
 # ------------------------------------------------------------- workload --
