@@ -231,9 +231,13 @@ moe_status moe_decode_routing(moe_ctx *ctx, float *logits, int32_t *idx, float *
  * with the union of the rows' experts.  Here every weight row in that union
  * (and of the router and the shared expert) is read from HBM once for all
  * the rows that need it; the prefill path would instead run its routing and
- * grouped GEMMs for a handful of rows.  Same arithmetic and tolerances as
- * moe_forward_decode (rows are independent: row t's result does not depend
- * on the other rows).  Uses the workspace's prefill regions: do not overlap
+ * grouped GEMMs for a handful of rows.  int4 weights, and bf16 weights
+ * with T < 5: the arithmetic of moe_forward_decode, operation for
+ * operation.  bf16 weights with T >= 5: the gate/up dot products run on the
+ * tensor cores (fp32 accumulation, every weight byte loaded once for all
+ * rows), the rest as in moe_forward_decode; the tolerances are the
+ * decode's.  Row t's result does not depend on the values of the other
+ * rows.  Uses the workspace's prefill regions: do not overlap
  * with a prefill call on the same context.  Errors: MOE_ERR_INVALID_ARG for
  * T out of range or misaligned buffers. */
 moe_status moe_forward_rows(moe_ctx *ctx, int layer, const void *x, int T, void *y,

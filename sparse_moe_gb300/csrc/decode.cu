@@ -379,6 +379,196 @@ __device__ __forceinline__ void warp_dots_users(const void *const (&rows)[NR],
   }
 }
 
+// D += A . B on the tensor cores (mma.sync m16n8k16, bf16 operands, fp32
+// accumulators).  Lane l = 4 g + t holds A (16 x 16, row-major) rows g and
+// g + 8 at columns 2t, 2t+1 (a0, a1) and 2t+8, 2t+9 (a2, a3); B (16 x 8,
+// column-major) rows 2t, 2t+1 (b0) and 2t+8, 2t+9 (b1) of column g; D rows
+// g (d0, d1) and g + 8 (d2, d3) at columns 2t, 2t + 1.
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1,
+                                               uint32_t a2, uint32_t a3, uint32_t b0,
+                                               uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+// The same for tf32 operands (mma.sync m16n8k8, fp32 accumulators): lane
+// l = 4 g + t holds A (16 x 8) rows g, g + 8 at columns t (a0, a1) and t + 4
+// (a2, a3), B (8 x 8) rows t (b0) and t + 4 (b1) of column g; D as above.
+__device__ __forceinline__ void mma_tf32_1688(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                              uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t tf32_rn(float v) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(v));
+  return r;
+}
+__device__ __forceinline__ float f4_at(const float4 &lo, const float4 &hi, int e) {
+  const float4 &v = e < 4 ? lo : hi;
+  const int w = e & 3;
+  return w == 0 ? v.x : w == 1 ? v.y : w == 2 ? v.z : v.w;
+}
+
+// Sixteen bf16 output-projection rows of K elements (K a multiple of 32;
+// this lane's rows g and g + 8 at rg, rg8) dotted with up to 8 NH users' h
+// (fp32 in global memory: hp[h] for user 8 h + g, null for none) on the
+// tensor cores in tf32 (the weights exactly, h rounded to 10 fraction bits).
+// In 32-wide chunk c, lane t's k slots t and t + 4 of step s are elements
+// 32 c + 8 t + 2 s and 32 c + 8 t + 2 s + 1.  Two chunks of loads in flight.
+// d[h] as for warp_mma_rows_users.
+template <int NH>
+__device__ __forceinline__ void warp_mma_tf32_rows_users(const __nv_bfloat16 *rg,
+                                                         const __nv_bfloat16 *rg8, int K,
+                                                         const float *const (&hp)[NH],
+                                                         float (&d)[NH][4]) {
+  const int lane = threadIdx.x & 31, t = lane & 3;
+#pragma unroll
+  for (int h = 0; h < NH; ++h) d[h][0] = d[h][1] = d[h][2] = d[h][3] = 0.0f;
+  const int nch = K / 32;
+  const uint4 *pa = reinterpret_cast<const uint4 *>(rg) + t;   // chunk c: pa[4 c]
+  const uint4 *pb = reinterpret_cast<const uint4 *>(rg8) + t;
+  uint4 w[2][2];
+  float4 hv[2][NH][2];
+  auto load = [&](int b, int c) {
+    w[b][0] = __ldcg(pa + 4 * c);
+    w[b][1] = __ldcg(pb + 4 * c);
+#pragma unroll
+    for (int h = 0; h < NH; ++h) {
+      if (hp[h] != nullptr) {
+        const float4 *q = reinterpret_cast<const float4 *>(hp[h] + 32 * c + 8 * t);
+        hv[b][h][0] = __ldcg(q);
+        hv[b][h][1] = __ldcg(q + 1);
+      } else {
+        hv[b][h][0] = hv[b][h][1] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      }
+    }
+  };
+#pragma unroll
+  for (int b = 0; b < 2; ++b)
+    if (b < nch) load(b, b);
+  for (int c = 0; c < nch; c += 2) {
+#pragma unroll
+    for (int b = 0; b < 2; ++b) {
+      const int cc = c + b;
+      if (cc < nch) {
+#pragma unroll
+        for (int st = 0; st < 4; ++st) {
+          const uint32_t wg = st == 0 ? w[b][0].x : st == 1 ? w[b][0].y : st == 2 ? w[b][0].z : w[b][0].w;
+          const uint32_t wg8 = st == 0 ? w[b][1].x : st == 1 ? w[b][1].y : st == 2 ? w[b][1].z : w[b][1].w;
+          const uint32_t a0 = wg << 16, a2 = wg & 0xffff0000u;
+          const uint32_t a1 = wg8 << 16, a3 = wg8 & 0xffff0000u;
+#pragma unroll
+          for (int h = 0; h < NH; ++h)
+            mma_tf32_1688(d[h], a0, a1, a2, a3, tf32_rn(f4_at(hv[b][h][0], hv[b][h][1], 2 * st)),
+                          tf32_rn(f4_at(hv[b][h][0], hv[b][h][1], 2 * st + 1)));
+        }
+        if (cc + 2 < nch) load(b, cc + 2);
+      }
+    }
+  }
+}
+
+constexpr int kRowsMmaDepth = 2;
+constexpr int kRowsMmaPrefetch = 6;   // chunks further ahead prefetched into L2
+// Word m (0..7) of the 32 bytes lo, hi.
+__device__ __forceinline__ uint32_t word8(const uint4 &lo, const uint4 &hi, int m) {
+  const uint4 &v = m < 4 ? lo : hi;
+  const int w = m & 3;
+  return w == 0 ? v.x : w == 1 ? v.y : w == 2 ? v.z : v.w;
+}
+
+// Sixteen bf16 weight rows of K elements (K a multiple of 64; this lane's
+// rows g and g + 8 start at rg and rg8) dotted with the rows of up to 8 NH
+// users in shared memory (xs: [T][K] bf16), on the tensor cores: every
+// weight byte is loaded once for all users.  Inside each 16-wide MMA step
+// the k order is permuted so that each lane's operands are whole 16-byte
+// loads: in 64-wide chunk c, the k slots 2t, 2t+1, 2t+8, 2t+9 of step s are
+// elements 64 c + 16 t + 4 s + 0..3, for A and B alike (the products summed
+// are the same).  kRowsMmaDepth chunks of loads are kept in flight, and the
+// next kRowsMmaPrefetch chunks are prefetched into L2.  On return d[h]
+// holds rows g, g + 8 (d0, d1 and d2, d3) of users 8 h + 2 t, 8 h + 2 t + 1.
+template <int NH>
+__device__ __forceinline__ void warp_mma_rows_users(const __nv_bfloat16 *rg,
+                                                    const __nv_bfloat16 *rg8, int K,
+                                                    const __nv_bfloat16 *xs, int T,
+                                                    uint32_t mb_x, int *status,
+                                                    float (&d)[NH][4]) {
+  constexpr int DEPTH = kRowsMmaDepth;   // chunks of loads in flight
+  const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+#pragma unroll
+  for (int h = 0; h < NH; ++h) d[h][0] = d[h][1] = d[h][2] = d[h][3] = 0.0f;
+  const int nch = K / 64;
+  const uint4 *pa = reinterpret_cast<const uint4 *>(rg) + 2 * t;   // chunk c: pa[8 c], pa[8 c + 1]
+  const uint4 *pb = reinterpret_cast<const uint4 *>(rg8) + 2 * t;
+  uint4 w[DEPTH][4];
+#pragma unroll
+  for (int b = 0; b < DEPTH; ++b)
+    if (b < nch) {
+      w[b][0] = ld_stream(pa + 8 * b);
+      w[b][1] = ld_stream(pa + 8 * b + 1);
+      w[b][2] = ld_stream(pb + 8 * b);
+      w[b][3] = ld_stream(pb + 8 * b + 1);
+    }
+  if (t == 0)
+    for (int c = DEPTH; c < DEPTH + kRowsMmaPrefetch && c < nch; ++c) {
+      prefetch_l2_line(rg + 64 * c);
+      prefetch_l2_line(rg8 + 64 * c);
+    }
+  {
+    volatile int no_abort = 0;   // the users' rows have landed in shared memory
+    mbar_wait_bounded(mb_x, 0u, &no_abort, status, DEV_TIMEOUT_STAGE);
+  }
+  for (int c = 0; c < nch; c += DEPTH) {
+#pragma unroll
+    for (int b = 0; b < DEPTH; ++b) {
+      const int cc = c + b;
+      if (cc < nch) {
+        uint4 xv[NH][2];
+#pragma unroll
+        for (int h = 0; h < NH; ++h) {
+          const int user = 8 * h + g;
+          if (user < T) {
+            const uint4 *px = reinterpret_cast<const uint4 *>(xs + static_cast<size_t>(user) * K) +
+                              8 * cc + 2 * t;
+            xv[h][0] = px[0];
+            xv[h][1] = px[1];
+          } else {
+            xv[h][0] = xv[h][1] = make_uint4(0u, 0u, 0u, 0u);
+          }
+        }
+#pragma unroll
+        for (int st = 0; st < 4; ++st) {
+          const uint32_t a0 = word8(w[b][0], w[b][1], 2 * st);
+          const uint32_t a2 = word8(w[b][0], w[b][1], 2 * st + 1);
+          const uint32_t a1 = word8(w[b][2], w[b][3], 2 * st);
+          const uint32_t a3 = word8(w[b][2], w[b][3], 2 * st + 1);
+#pragma unroll
+          for (int h = 0; h < NH; ++h)
+            mma_bf16_16816(d[h], a0, a1, a2, a3, word8(xv[h][0], xv[h][1], 2 * st),
+                           word8(xv[h][0], xv[h][1], 2 * st + 1));
+        }
+        if (t == 0 && cc + DEPTH + kRowsMmaPrefetch < nch) {
+          // one 128-byte line per row and chunk
+          prefetch_l2_line(rg + 64 * (cc + DEPTH + kRowsMmaPrefetch));
+          prefetch_l2_line(rg8 + 64 * (cc + DEPTH + kRowsMmaPrefetch));
+        }
+        if (cc + DEPTH < nch) {
+          w[b][0] = ld_stream(pa + 8 * (cc + DEPTH));
+          w[b][1] = ld_stream(pa + 8 * (cc + DEPTH) + 1);
+          w[b][2] = ld_stream(pb + 8 * (cc + DEPTH));
+          w[b][3] = ld_stream(pb + 8 * (cc + DEPTH) + 1);
+        }
+      }
+    }
+  }
+}
+
 // Row r of a K-major matrix with K columns, bf16 or packed int4.
 template <int WF>
 __device__ __forceinline__ const void *row_ptr(const void *base, size_t r, int K) {
@@ -1030,7 +1220,9 @@ __global__ void __launch_bounds__(kDecLayerThreads, 1)
 //      each dotted with all T inputs (x [T, H] staged in shared memory);
 //   B. per-row top-k (warp t of every CTA for row t), the union of the
 //      selected experts in ascending expert order, then items (u, i): the
-//      gate/up row pair i of union expert u with every row that selected u;
+//      gate/up row pair i of union expert u with every row that selected u
+//      (bf16 weights: items of eight row pairs on the tensor cores, with all
+//      T rows as the MMA's N columns, one or two blocks of eight);
 //   C. each CTA's output rows n0..n1 of every union expert and of the shared
 //      expert (tasks of 8 rows) with the h of each user row, then
 //      y[t][n] = sum_j w[t][j] part[t][j][n] + g[t] part[t][k][n] in fixed j
@@ -1050,6 +1242,9 @@ __host__ __device__ __forceinline__ RowsSmem rows_smem(int T, int k, int H, int 
   return L;
 }
 constexpr int kRowsMaxUnion = kSmallMaxRows * 32;   // T k with k <= 32
+// From this many rows up, bf16 gate/up items run on the tensor cores: with
+// fewer rows the per-user passes keep more loads in flight per SM.
+constexpr int kRowsMmaMinRows = 5;
 
 template <int WF, int R>
 __global__ void __launch_bounds__(kDecLayerThreads, 1) rows_kernel(const DecodeParams p) {
@@ -1196,7 +1391,45 @@ __global__ void __launch_bounds__(kDecLayerThreads, 1) rows_kernel(const DecodeP
   }
 
   // ---- B: union gate/up row pairs with their user rows -> h
-  const int nB = U * p.I;
+  bool b_done = false;
+  if constexpr (WF == 0) {
+    if (T >= kRowsMmaMinRows && p.I % 8 == 0 && H % 64 == 0) {
+      // bf16 rows on the tensor cores: items of 8 row pairs (gate rows
+      // i0..i0+7 as A rows 0..7, the matching up rows as A rows 8..15) with
+      // all T rows at once; lane (g, t) ends with gate and up of row pair
+      // i0 + g for users 2t, 2t + 1 (and 8 + 2t, 9 + 2t)
+      const int I8 = p.I / 8;
+      const int nB8 = U * I8;
+      const int g = lane >> 2, t2 = 2 * (lane & 3);
+      const __nv_bfloat16 *xsb = reinterpret_cast<const __nv_bfloat16 *>(x_s);
+      const __nv_bfloat16 *gu = static_cast<const __nv_bfloat16 *>(p.gate_up);
+      for (int q = gw; q < nB8; q += nw) {
+        const int u = q / I8, i = (q - u * I8) * 8 + g;
+        const size_t rg = static_cast<size_t>(ue[u]) * 2 * p.I + i;
+        const unsigned int us = users[u];
+        auto put = [&](const float (&dd)[4], int tb) {
+          if ((us >> tb) & 1u)
+            p.h[tb * hrow + static_cast<size_t>(slot_of[u][tb]) * p.h_ld + i] = silu_f(dd[0]) * dd[2];
+          if ((us >> (tb + 1)) & 1u)
+            p.h[(tb + 1) * hrow + static_cast<size_t>(slot_of[u][tb + 1]) * p.h_ld + i] =
+                silu_f(dd[1]) * dd[3];
+        };
+        if (T > 8) {
+          float d[2][4];
+          warp_mma_rows_users<2>(gu + rg * H, gu + (rg + p.I) * H, H, xsb, T, mb_x, p.status, d);
+          put(d[0], t2);
+          put(d[1], 8 + t2);
+        } else {
+          float d[1][4];
+          warp_mma_rows_users<1>(gu + rg * H, gu + (rg + p.I) * H, H, xsb, T, mb_x, p.status, d);
+          put(d[0], t2);
+        }
+      }
+      b_done = true;
+    }
+  }
+  // int4 rows (and bf16 rows of other shapes): one CUDA-core pass per user
+  const int nB = b_done ? 0 : U * p.I;
   for (int q = gw; q < nB; q += nw) {
     const int u = q / p.I, i = q - u * p.I;
     const size_t rg = static_cast<size_t>(ue[u]) * 2 * p.I + i;
@@ -1217,7 +1450,55 @@ __global__ void __launch_bounds__(kDecLayerThreads, 1) rows_kernel(const DecodeP
   // ---- C: output rows n0..n1 of the union experts (u < U) and the shared
   // expert (u = U), 8 rows per task, for each user row
   const size_t pstride = static_cast<size_t>(k + 1) * p.p3_rows;   // part floats per row t
-  for (int task = warp; task < (U + 1) * ngroups; task += kDecWarps) {
+  bool c_done = false;
+  if constexpr (WF == 0) {
+    if (b_done && p.I % 32 == 0 && p.Is % 32 == 0) {
+      // bf16 rows on the tensor cores (tf32): tasks of 16 output rows with
+      // all T rows at once; lane (g, t) ends with rows r0 + g, r0 + 8 + g
+      // for users 2t, 2t + 1 (and 8 + 2t, 9 + 2t)
+      const int g = lane >> 2, t2 = 2 * (lane & 3);
+      const int ng16 = (nrows + 15) / 16;
+      for (int task = warp; task < (U + 1) * ng16; task += kDecWarps) {
+        const int u = task / ng16, r0 = (task - u * ng16) * 16;
+        const bool sh = (u == U);
+        const int K = sh ? p.Is : p.I;
+        const unsigned int us = sh ? all_rows : users[u];
+        const __nv_bfloat16 *base = static_cast<const __nv_bfloat16 *>(sh ? p.sh_down : p.down);
+        const size_t row0 = (sh ? 0 : static_cast<size_t>(ue[u]) * H) + n0;
+        const int ra = min(r0 + g, nrows - 1), rb8 = min(r0 + 8 + g, nrows - 1);
+        auto slot = [&](int tt) { return sh ? k : static_cast<int>(slot_of[u][tt]); };
+        auto hptr = [&](int tt) -> const float * {
+          return (tt < T && ((us >> tt) & 1u)) ? p.h + tt * hrow + static_cast<size_t>(slot(tt)) * p.h_ld
+                                               : nullptr;
+        };
+        auto put = [&](const float (&dd)[4], int tb) {
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int tt = tb + e;
+            if (tt < T && ((us >> tt) & 1u)) {
+              float *pt = part + tt * pstride + static_cast<size_t>(slot(tt)) * p.p3_rows;
+              if (r0 + g < nrows) pt[r0 + g] = dd[e];
+              if (r0 + 8 + g < nrows) pt[r0 + 8 + g] = dd[2 + e];
+            }
+          }
+        };
+        if (T > 8) {
+          const float *hp[2] = {hptr(g), hptr(8 + g)};
+          float d[2][4];
+          warp_mma_tf32_rows_users<2>(base + (row0 + ra) * K, base + (row0 + rb8) * K, K, hp, d);
+          put(d[0], t2);
+          put(d[1], 8 + t2);
+        } else {
+          const float *hp[1] = {hptr(g)};
+          float d[1][4];
+          warp_mma_tf32_rows_users<1>(base + (row0 + ra) * K, base + (row0 + rb8) * K, K, hp, d);
+          put(d[0], t2);
+        }
+      }
+      c_done = true;
+    }
+  }
+  for (int task = warp; task < (c_done ? 0 : (U + 1) * ngroups); task += kDecWarps) {
     const int u = task / ngroups, t0 = (task - u * ngroups) * 8;
     const bool sh = (u == U);
     slot_task_users<WF>(p, p.h, hrow, sh ? all_rows : users[u],
