@@ -91,7 +91,7 @@ typedef struct moe_ctx moe_ctx;
 typedef enum {
   MOE_OK = 0,
   MOE_ERR_INVALID_ARG = 1,     /* NULL, misaligned or out-of-range argument      */
-  MOE_ERR_UNSUPPORTED = 2,     /* shape or format this build does not implement  */
+  MOE_ERR_UNSUPPORTED = 2,     /* shape or format the library does not implement */
   MOE_ERR_WORKSPACE = 3,       /* workspace missing, too small or misaligned     */
   MOE_ERR_CUDA = 4,            /* a CUDA runtime/driver call failed              */
   MOE_ERR_NOT_LOADED = 5,      /* weights of the requested layer slot not loaded */
