@@ -77,3 +77,29 @@ def test_odd_shape_decode_and_rows(wfmt):
     torch.cuda.synchronize()
     assert torch.equal(y, torch.stack(yd))
     assert ctx.check_device() == 0
+
+
+def test_odd_shape_rows_on_tensor_cores():
+    # 9 bf16 rows take the tensor-core phases (two column blocks, the second
+    # with one row); routed and shared output projections of different widths
+    # (I = 128, Is = 192) and 10 slots per row
+    wl, ctx, w = _ctx(moe_synth.WFMT_BF16, 9, 16, 73)
+    x = moe_synth.make_x(wl, device="cuda")
+    y = ctx.forward_rows(0, x)
+    r = ctx.rows_routing(9)
+    torch.cuda.synchronize()
+    lg = r["logits"].cpu().numpy()
+    x_np = x.float().cpu().numpy()
+    wr = w["router_w"].float().cpu().numpy()
+    b = None if w.get("router_b") is None else w["router_b"].cpu().numpy()
+    ref_l = orc.router_logits(x_np, wr, b)
+    assert np.all(np.abs(lg - ref_l) <= logits_bound(x_np, wr, ref_l, b))
+    o = orc.route(lg, ctx.top_k)
+    np.testing.assert_array_equal(r["topk_idx"].cpu().numpy(), o["topk_idx"])
+    ref = orc.moe_layer(x_np, host_layer(w), ctx.top_k, logits=lg)
+    assert_layer_close(y.float().cpu().numpy(), ref, what="odd shape rows (tensor cores)")
+    # the same rows among others: unchanged
+    y5 = ctx.forward_rows(0, x[4:9].contiguous())
+    torch.cuda.synchronize()
+    assert torch.equal(y5, y[4:9])
+    assert ctx.check_device() == 0
