@@ -510,6 +510,13 @@ def bench_decode(args, dev, stream, hbm, int4=None, wl=None):
         for l in range(L):
             ctx.forward_decode(l, xs[l:l + 1], ys[l:l + 1], stream=stream)
     torch.cuda.synchronize()
+    # the expert-weight stream on its own: phase B of single launches, whose
+    # CTAs stamp the global timer at its start and end while profiling is on
+    phases = []
+    for l in range(min(L, 10)):
+        ctx.forward_decode(l, xs[l:l + 1], ys[l:l + 1], stream=stream)
+        torch.cuda.synchronize()
+        phases.append(ctx.decode_phase_read())
     prof = ctx.profile_read()
     ctx.profile(False)
     g = torch.cuda.CUDAGraph()
@@ -554,6 +561,16 @@ def bench_decode(args, dev, stream, hbm, int4=None, wl=None):
         stream.synchronize()
     e2e_us = (time.perf_counter() - t0) * 1e6 / n_e2e
     nb = decode_bytes(s, int4, affine=wl.wfmt == moe_synth.WFMT_INT4_AFFINE)
+    b_bytes = nb["routed_gateup"] + nb["routed_down"]
+    win = float(np.median([ph["window_us"] for ph in phases]))
+    phase_b = {"bytes": b_bytes, "window_us": win,
+               "median_cta_us": float(np.median([ph["median_us"] for ph in phases])),
+               "GBps": b_bytes / (win * 1e-6) / 1e9,
+               "frac_of_hbm": b_bytes / (win * 1e-6) / 1e9 / hbm,
+               "how": "phase B of single eager launches (the k routed experts' gate/up rows, "
+                      "their output-projection rows bulk-copied alongside), global-timer "
+                      "stamps in every CTA, first start to last end; median of "
+                      f"{len(phases)} launches"}
     lay = prof.get("decode_layer", (1, float("nan")))
     lay_us = lay[1] * 1e3 / max(1, lay[0])
     # one launch per layer: its average duration in the timed graph replays
@@ -563,6 +580,7 @@ def bench_decode(args, dev, stream, hbm, int4=None, wl=None):
         "tokens_per_s": 1e6 / (us_layer * L), "layers": L, "graph_replays": reps,
         "expert_stream_GBps": nb["expert_stream"] / (us_layer * 1e-6) / 1e9,
         "expert_stream_frac_of_hbm": nb["expert_stream"] / (us_layer * 1e-6) / 1e9 / hbm,
+        "expert_stream_phase_b": phase_b,
         "bytes_per_layer": nb["total"],
         "roofline": {"kernel": "decode_layer", "bound": "hbm", "achieved": achieved,
                      "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,

@@ -347,6 +347,16 @@ moe_status moe_profile_enable(moe_ctx *ctx, int on);
 /* Synchronises the recorded events and returns up to `max` entries. */
 moe_status moe_profile_read(moe_ctx *ctx, moe_kernel_stat *stats, int max, int *n);
 
+/* Phase B of the most recent moe_forward_decode launched while profiling was
+ * enabled (the k routed experts' gate/up rows streamed by every CTA, the
+ * output-projection rows bulk-copied alongside): each CTA stamps the global
+ * timer when its phase B starts (after the top-k) and ends.  Synchronises
+ * the device; *window_us = latest end - earliest start over the CTAs,
+ * *median_us = the median CTA's duration.  MOE_ERR_INVALID_ARG if no
+ * profiled decode launch has stamped every CTA since profiling was enabled
+ * on this context. */
+moe_status moe_decode_phase_read(moe_ctx *ctx, double *window_us, double *median_us);
+
 /* Number of kernels this context has launched since creation. */
 int64_t moe_launch_count(const moe_ctx *ctx);
 

@@ -270,6 +270,16 @@ class MoEContext:
         return {arr[i].name.decode(): (arr[i].launches, arr[i].total_ms)
                 for i in range(min(n.value, 32))}
 
+    def decode_phase_read(self) -> dict:
+        """Phase B of the last decode launched while profiling was on: the
+        span from the first CTA's start to the last CTA's end, and the median
+        CTA's duration (µs)."""
+        win = ctypes.c_double(0.0)
+        med = ctypes.c_double(0.0)
+        self._check(self.lib.moe_decode_phase_read(self.handle, ctypes.byref(win), ctypes.byref(med)),
+                    "moe_decode_phase_read")
+        return {"window_us": win.value, "median_us": med.value}
+
     @property
     def launch_count(self) -> int:
         return int(self.lib.moe_launch_count(self.handle))

@@ -67,6 +67,7 @@ SIGNATURES = {
     "moe_check_device": (i32, [vp, ctypes.POINTER(ctypes.c_int32)]),
     "moe_profile_enable": (i32, [vp, i32]),
     "moe_profile_read": (i32, [vp, ctypes.POINTER(MoeKernelStat), i32, ctypes.POINTER(i32)]),
+    "moe_decode_phase_read": (i32, [vp, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double)]),
     "moe_launch_count": (i64, [vp]),
     "moe_last_error": (ctypes.c_char_p, [vp]),
     "moe_status_string": (ctypes.c_char_p, [i32]),

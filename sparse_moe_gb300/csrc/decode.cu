@@ -585,6 +585,11 @@ __device__ __forceinline__ const __nv_bfloat16 *scale_row(const void *base, size
 // exactly two grid-widths).  A CTA reads base before its first arrival; no
 // barrier of this launch can complete before that arrival, so the value it
 // reads lies in [base, base + gridDim.x).
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
 __device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long *p) {
   unsigned long long v;
   asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
@@ -1010,6 +1015,7 @@ __device__ __forceinline__ void decode_layer(const DecodeParams &p, const DecCta
     if (lane == 0) w_s[32] = g;
   }
   __syncthreads();
+  if (p.phase_ts != nullptr && threadIdx.x == 0) p.phase_ts[2 * blockIdx.x] = global_ns();
   // The last warps have the fewest phase-B rows: they issue the copies.
   if (warp == kDecWarps - 1 && p.p3_stage) {
     // the k routed experts' output rows n0..n1, one bulk copy per expert
@@ -1085,6 +1091,10 @@ __device__ __forceinline__ void decode_layer(const DecodeParams &p, const DecCta
       mbar_wait_bounded(mb_sh, par, &no_abort, p.status, DEV_TIMEOUT_STAGE);
     }
     run_slot_task<WF>(p, p.k, 8 * s, n0, nrows, 0, part, w3, w3_sh, &c);
+  }
+  if (p.phase_ts != nullptr) {   // profiling: the end of this CTA's phase B
+    __syncthreads();
+    if (threadIdx.x == 0) p.phase_ts[2 * blockIdx.x + 1] = global_ns();
   }
   grid_sync(p.bar, bar_base + 2 * static_cast<unsigned long long>(G), p.status);
   // The next layer's routing-independent weight traffic can start now: this

@@ -25,8 +25,8 @@ struct WsLayout {
   int Tc, nblk, R, Imax, max_blocks;
   size_t status, logits, idx, w, gate, mask, counts, offsets, sorted, pos, blocks, nblocks, xg, h,
       o;
-  size_t dec_logits, dec_idx, dec_w, dec_g, dec_h, dec_counter, x_stage, y_stage, dec_x_stage,
-      dec_y_stage, total;
+  size_t dec_logits, dec_idx, dec_w, dec_g, dec_h, dec_counter, dec_phase, x_stage, y_stage,
+      dec_x_stage, dec_y_stage, total;
 };
 
 WsLayout make_layout(const moe_config &c) {
@@ -65,6 +65,7 @@ WsLayout make_layout(const moe_config &c) {
   L.dec_g = take(4);
   L.dec_h = take(decode_h_floats(c.top_k, L.Imax) * 4);
   L.dec_counter = take(16);
+  L.dec_phase = take(static_cast<size_t>(kMaxPhaseCtas) * 2 * 8);
   L.x_stage = take(2 * Tc * H * 2);   // two slots: see moe_forward_prefill_host
   L.y_stage = take(2 * Tc * H * 2);
   L.dec_x_stage = take(H * 2);   // moe_forward_decode_host (apart from the prefill slots,
@@ -538,6 +539,9 @@ DecodeParams decode_params(const moe_ctx *ctx, const LayerSlot &ls, const void *
   p.h = ctx->at<float>(L.dec_h);
   p.h_ld = L.Imax;
   p.bar = ctx->at<unsigned long long>(L.dec_counter);
+  p.phase_ts = ctx->profiling && ctx->decode_grid <= kMaxPhaseCtas
+                   ? ctx->at<unsigned long long>(L.dec_phase)
+                   : nullptr;
   p.status = ctx->status();
   return p;
 }
@@ -1029,10 +1033,16 @@ moe_status moe_check_device(moe_ctx *ctx, int32_t *code) {
 moe_status moe_profile_enable(moe_ctx *ctx, int on) {
   if (!ctx) return MOE_ERR_INVALID_ARG;
   if (on && !ctx->profiling) {
+    const moe_status st = ensure_device(ctx);
+    if (st) return st;
     for (int i = 0; i < K_COUNT; ++i) {
       ctx->prof_ms[i] = 0.0;
       ctx->prof_launches[i] = 0;
     }
+    // no decode phase stamps from before this point
+    const cudaError_t e = cudaMemset(ctx->ws + ctx->L.dec_phase, 0,
+                                     static_cast<size_t>(kMaxPhaseCtas) * 2 * 8);
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "phase stamp reset");
   }
   ctx->profiling = on != 0;
   return MOE_OK;
@@ -1064,6 +1074,33 @@ moe_status moe_profile_read(moe_ctx *ctx, moe_kernel_stat *stats, int max, int *
     ++cnt;
   }
   *n = cnt;
+  return MOE_OK;
+}
+
+moe_status moe_decode_phase_read(moe_ctx *ctx, double *window_us, double *median_us) {
+  if (!ctx || !window_us || !median_us) return MOE_ERR_INVALID_ARG;
+  moe_status st = ensure_device(ctx);
+  if (st) return st;
+  const int G = ctx->decode_grid;
+  if (G <= 0 || G > kMaxPhaseCtas) return fail(ctx, MOE_ERR_UNSUPPORTED, "no phase stamps for this grid");
+  std::vector<unsigned long long> ts(static_cast<size_t>(G) * 2);
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e == cudaSuccess)
+    e = cudaMemcpy(ts.data(), ctx->ws + ctx->L.dec_phase, ts.size() * 8, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "phase stamp read");
+  unsigned long long lo = ~0ull, hi = 0;
+  std::vector<double> d(static_cast<size_t>(G));
+  for (int b = 0; b < G; ++b) {
+    const unsigned long long s0 = ts[2 * b], s1 = ts[2 * b + 1];
+    if (s0 == 0 || s1 < s0)
+      return fail(ctx, MOE_ERR_INVALID_ARG, "no profiled decode launch since profiling was enabled");
+    lo = std::min(lo, s0);
+    hi = std::max(hi, s1);
+    d[b] = static_cast<double>(s1 - s0) * 1e-3;
+  }
+  std::sort(d.begin(), d.end());
+  *window_us = static_cast<double>(hi - lo) * 1e-3;
+  *median_us = d[static_cast<size_t>(G) / 2];
   return MOE_OK;
 }
 

@@ -142,6 +142,8 @@ struct DecodeParams {
   float *h;                  // [(k+1) h_ld] fp32: h of the k experts, then of the shared expert
   int h_ld;                  // max(I, Is)
   unsigned long long *bar;   // grid-barrier arrival counter (16-byte slot, zeroed once)
+  unsigned long long *phase_ts;   // null, or [gridDim.x][2]: global-timer ns at the start and
+                                  // the end of phase B in each CTA (profiling only)
   int *status;               // device status word
   int p3_rows, p3_stage;     // set by launch_decode_layer
   int p3_scales;             // set by launch_decode_layer: int4 scales (biases) staged too
@@ -154,6 +156,8 @@ struct DecodeLayersParams {
   DecodeParams layer[kMaxDecodeLayers];
   int n;
 };
+// CTAs whose phase-B stamps the workspace holds (profiling).
+constexpr int kMaxPhaseCtas = 1024;
 // Floats of the h region a decode needs.
 inline size_t decode_h_floats(int k, int h_ld) { return (static_cast<size_t>(k) + 1) * h_ld; }
 // Raises the decode kernel's dynamic shared-memory limit on the current
