@@ -208,3 +208,21 @@ def test_decode_layers_rejects_bad_arguments(decode_bf16):
                                        ctypes.c_void_p(y.data_ptr()), H, None)
     assert st == _abi.MOE_ERR_INVALID_ARG             # stride not a multiple of 8
     assert lib.moe_forward_decode_layers(ctx.handle, 0, 0, None, 0, None, 0, None) == _abi.MOE_OK
+
+
+def test_decode_phase_stamps(decode_bf16):
+    # profiling on: every CTA stamps phase B; the output is unchanged by it
+    wl, ctx, layers = decode_bf16
+    x = moe_synth.make_x(wl, layer=0, device="cuda")
+    y0 = ctx.forward_decode(0, x)
+    ctx.profile(True)
+    with pytest.raises(MoEError):   # nothing stamped since profiling was enabled
+        ctx.decode_phase_read()
+    y1 = ctx.forward_decode(0, x)
+    ph = ctx.decode_phase_read()
+    ctx.profile_read()
+    ctx.profile(False)
+    torch.cuda.synchronize()
+    assert torch.equal(y0, y1)
+    assert 0.0 < ph["median_us"] <= ph["window_us"] < 1e4
+    assert ctx.check_device() == 0
