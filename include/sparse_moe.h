@@ -343,6 +343,9 @@ typedef struct {
   double total_ms;     /* sum of event-measured durations                     */
 } moe_kernel_stat;
 
+/* While profiling is on, every launch also records CUDA events around it,
+ * and decode launches stamp their phase B (moe_decode_phase_read).
+ * Enabling clears the counts and the stamps. */
 moe_status moe_profile_enable(moe_ctx *ctx, int on);
 /* Synchronises the recorded events and returns up to `max` entries. */
 moe_status moe_profile_read(moe_ctx *ctx, moe_kernel_stat *stats, int max, int *n);
