@@ -84,6 +84,10 @@ def test_null_arguments_rejected(lib):
     assert lib.moe_route(None, 0, None, 1, None, None, None, None, None, None, None, None) == \
         _abi.MOE_ERR_INVALID_ARG
     assert lib.moe_load_weights(None, 0, None) == _abi.MOE_ERR_INVALID_ARG
+    w, m = ctypes.c_double(0.0), ctypes.c_double(0.0)
+    assert lib.moe_decode_phase_read(None, ctypes.byref(w), ctypes.byref(m)) == \
+        _abi.MOE_ERR_INVALID_ARG
+    assert lib.moe_profile_enable(None, 1) == _abi.MOE_ERR_INVALID_ARG
     assert lib.moe_launch_count(None) == 0
     assert lib.moe_last_error(None) == b""
     assert lib.moe_status_string(_abi.MOE_ERR_DEVICE_TIMEOUT) == b"device-side wait timed out"
